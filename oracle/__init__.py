@@ -1,0 +1,135 @@
+"""CPU oracle for grouped convolution forward -- TEST INFRASTRUCTURE ONLY.
+
+The oracle (``oracle.c``) is a plain fp64 direct-loop grouped convolution
+written from the definition (see the header of ``oracle.c`` for the formula,
+the passages it follows and the readings it takes).  Only ``tests/``, the
+package smoke check and the benchmark's CPU-baseline leg may import this
+module.  It shares no code with the CUDA library and must never be used as a
+fallback for it.
+
+``build()`` compiles ``oracle.c`` with gcc (OpenMP when available) into
+``oracle/liboracle.so``; ``load(path)`` can load an alternative build, which
+the mutation tests use to show that the pins catch planted mistakes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(HERE, "oracle.c")
+LIB = os.path.join(HERE, "liboracle.so")
+
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_dp = ctypes.POINTER(ctypes.c_double)
+
+
+def compile_source(src: str, out: str, openmp: bool = True) -> str:
+    """Compile one C source file into a shared library with gcc."""
+    cmd = ["gcc", "-O2", "-std=c99", "-shared", "-fPIC", src, "-o", out]
+    if openmp:
+        cmd.insert(1, "-fopenmp")
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Build ``liboracle.so`` next to the source if it is missing or stale."""
+    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SOURCE):
+        tmp = LIB + f".tmp{os.getpid()}"
+        try:
+            compile_source(SOURCE, tmp, openmp=True)
+        except subprocess.CalledProcessError:
+            compile_source(SOURCE, tmp, openmp=False)
+        os.replace(tmp, LIB)
+    return LIB
+
+
+class Oracle:
+    """ctypes view of one oracle build."""
+
+    def __init__(self, path: str):
+        self.path = path
+        lib = ctypes.CDLL(path)
+        lib.oracle_out_extent.restype = ctypes.c_long
+        lib.oracle_out_extent.argtypes = [ctypes.c_long] * 5
+        lib.oracle_grouped_conv_fwd.restype = ctypes.c_int
+        lib.oracle_grouped_conv_fwd.argtypes = [_dp, _dp, _dp, _dp] + [ctypes.c_long] * 4 + [_i32p] * 5
+        lib.oracle_grouped_conv_fwd_points.restype = ctypes.c_int
+        lib.oracle_grouped_conv_fwd_points.argtypes = (
+            [_dp, _dp, _dp] + [ctypes.c_long] * 4 + [_i32p] * 5
+            + [ctypes.POINTER(ctypes.c_int64), ctypes.c_long, _dp])
+        self.lib = lib
+
+    # -- helpers ---------------------------------------------------------
+    @staticmethod
+    def _f64(a):
+        if a is None:
+            return None
+        if hasattr(a, "detach"):  # torch tensor: exact widening to float64
+            a = a.detach().to("cpu").double().contiguous().numpy()
+        return np.ascontiguousarray(a, dtype=np.float64)
+
+    @staticmethod
+    def _v3(v):
+        return (ctypes.c_int32 * 3)(*[int(t) for t in v])
+
+    def out_extent(self, i: int, k: int, s: int, p: int, d: int) -> int:
+        return int(self.lib.oracle_out_extent(i, k, s, p, d))
+
+    def out_shape(self, prob) -> tuple:
+        return tuple(self.out_extent(prob.inp[i], prob.ker[i], prob.stride[i], prob.pad[i],
+                                     prob.dil[i]) for i in range(3))
+
+    def _args(self, prob):
+        return (prob.N, prob.G, prob.Cg, prob.Kg, self._v3(prob.inp), self._v3(prob.ker),
+                self._v3(prob.stride), self._v3(prob.pad), self._v3(prob.dil))
+
+    def forward(self, prob, x, w, bias=None) -> np.ndarray:
+        """Full output as float64 [N, (Do), Ho, Wo, G, Kg] (Do omitted for 2D)."""
+        xd, wd, bd = self._f64(x), self._f64(w), self._f64(bias)
+        Do, Ho, Wo = self.out_shape(prob)
+        shape = (prob.N, Do, Ho, Wo, prob.G, prob.Kg)
+        y = np.empty(shape, dtype=np.float64)
+        rc = self.lib.oracle_grouped_conv_fwd(
+            xd.ctypes.data_as(_dp), wd.ctypes.data_as(_dp),
+            bd.ctypes.data_as(_dp) if bd is not None else None,
+            y.ctypes.data_as(_dp), *self._args(prob))
+        if rc != 0:
+            raise ValueError("oracle rejected the problem")
+        if prob.ndim == 2:
+            y = y.reshape(prob.N, Ho, Wo, prob.G, prob.Kg)
+        return y
+
+    def points(self, prob, x, w, bias, idx) -> np.ndarray:
+        """Outputs at flat indices ``idx`` into the [N,Do,Ho,Wo,G,Kg] layout."""
+        xd, wd, bd = self._f64(x), self._f64(w), self._f64(bias)
+        ii = np.ascontiguousarray(idx, dtype=np.int64)
+        out = np.empty(ii.shape[0], dtype=np.float64)
+        rc = self.lib.oracle_grouped_conv_fwd_points(
+            xd.ctypes.data_as(_dp), wd.ctypes.data_as(_dp),
+            bd.ctypes.data_as(_dp) if bd is not None else None, *self._args(prob),
+            ii.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), ii.shape[0],
+            out.ctypes.data_as(_dp))
+        if rc != 0:
+            raise ValueError("oracle rejected the problem or an index")
+        return out
+
+
+_default: Optional[Oracle] = None
+
+
+def get() -> Oracle:
+    """The oracle built from ``oracle.c`` (built on first use)."""
+    global _default
+    if _default is None:
+        _default = Oracle(build())
+    return _default
+
+
+def load(path: str) -> Oracle:
+    return Oracle(path)
