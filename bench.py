@@ -1,0 +1,579 @@
+#!/usr/bin/env python3
+"""Benchmark: grouped-convolution forward on GB300, device-timed.
+
+One "step" is one pass of the forward path over one batch of the workload
+(default: the MobileNetV2-style depthwise fp16 pair, N=32, C=G=144, 56x56,
+3x3, stride 1 and its stride-2 variant, with bias -- two launches).
+
+Timing (per rank): inputs and outputs are rotated over R buffer sets whose
+total exceeds twice the L2, so no step reads the previous step's data from
+L2.  The K timed steps are captured into CUDA graphs of the library's own
+C-ABI calls with external event-record nodes between launches, then replayed
+between a barrier + synchronize on both sides.  The per-launch events give
+each kernel's device time inside the timed region (used for the roofline
+entry); the events around the whole region give ms_per_step.  Clocks are
+sampled with nvidia-smi during the timed region.
+
+``--impl reference`` times the CPU oracle (the plain fp64 direct loop) on
+the host cores instead, each step a bounded sample of the same workload.
+
+Output: one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("grouped-conv fwd TFLOP/s & HBM GB/s, % of GB300 roofline (device-timed median)")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129 * 1024 * 1024
+
+BENCH_SETS = {
+    "mbv2_dw": ["mbv2_dw_s1_f16", "mbv2_dw_s2_f16"],
+    "resnext": ["resnext_a_bf16", "resnext_b_bf16"],
+    "resnext3d_n8": ["resnext3d_n8_f16"],
+    "resnext3d_n1": ["resnext3d_n1_f16"],
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mbv2_dw",
+                    help="a bench set (%s) or comma-separated workload names" % ", ".join(BENCH_SETS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tile", default="", help="tuning override TH,TW,WB,stages")
+    ap.add_argument("--force-kernel", type=int, default=0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# Driver-API events (external event-record nodes inside captured graphs)
+# ---------------------------------------------------------------------------
+class DriverEvents:
+    def __init__(self):
+        self.cu = ctypes.CDLL("libcuda.so.1")
+        self._create = self.cu.cuEventCreate
+        self._create.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_uint]
+        self._record = self.cu.cuEventRecordWithFlags
+        self._record.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        try:
+            self._elapsed = self.cu.cuEventElapsedTime_v2
+        except AttributeError:
+            self._elapsed = self.cu.cuEventElapsedTime
+        self._elapsed.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p]
+        try:
+            self._destroy = self.cu.cuEventDestroy_v2
+        except AttributeError:
+            self._destroy = self.cu.cuEventDestroy
+        self._destroy.argtypes = [ctypes.c_void_p]
+
+    def create(self, n):
+        out = []
+        for _ in range(n):
+            e = ctypes.c_void_p()
+            r = self._create(ctypes.byref(e), 0)
+            if r != 0:
+                raise RuntimeError(f"cuEventCreate failed: {r}")
+            out.append(e.value)
+        return out
+
+    def record_external(self, ev, stream_handle):
+        r = self._record(ctypes.c_void_p(ev), ctypes.c_void_p(stream_handle), 1)
+        if r != 0:
+            raise RuntimeError(f"cuEventRecordWithFlags failed: {r}")
+
+    def elapsed_ms(self, a, b):
+        ms = ctypes.c_float()
+        r = self._elapsed(ctypes.byref(ms), ctypes.c_void_p(a), ctypes.c_void_p(b))
+        if r != 0:
+            raise RuntimeError(f"cuEventElapsedTime failed: {r}")
+        return ms.value
+
+    def destroy(self, evs):
+        for e in evs:
+            self._destroy(ctypes.c_void_p(e))
+
+
+# ---------------------------------------------------------------------------
+# Clock sampler (nvidia-smi during the timed region)
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [t.strip() for t in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "sm_mhz_min": min(sm)}
+
+
+# ---------------------------------------------------------------------------
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "depthwise_convolution_forward_gb300", "csrc", "*"))):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def load_traffic(kernel_name: str, workload: str):
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    ent = d.get(f"{kernel_name}:{workload}")
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def resolve(names_arg):
+    from depthwise_convolution_forward_gb300 import inputs
+
+    names = BENCH_SETS.get(names_arg, None) or names_arg.split(",")
+    return names_arg, [inputs.by_name(n) for n in names]
+
+
+def describe(wls) -> str:
+    parts = []
+    for wl in wls:
+        sp = "x".join(map(str, wl.inp[3 - wl.ndim + 1:] if wl.ndim == 2 else wl.inp))
+        parts.append(f"{wl.name}: N={wl.N} G={wl.G} Cg={wl.Cg} Kg={wl.Kg} in={sp} "
+                     f"k={'x'.join(map(str, wl.ker[1:] if wl.ndim == 2 else wl.ker))} "
+                     f"s={wl.stride[1]} p={wl.pad[1]} d={wl.dil[1]} {wl.dtype}{' +bias' if wl.bias else ''}")
+    return "; ".join(parts)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_threads() -> int:
+    env = os.environ.get("OMP_NUM_THREADS")
+    return int(env) if env else (os.cpu_count() or 1)
+
+
+def cpu_oracle_prepare(wls):
+    import numpy as np
+
+    import oracle
+    from depthwise_convolution_forward_gb300 import inputs, roofline
+
+    orc = oracle.get()
+    prep = []
+    for wl in wls:
+        x, w, b = inputs.make_inputs(wl)
+        out = orc.out_shape(wl)
+        prep.append(dict(wl=wl, x=orc._f64(x), w=orc._f64(w), b=orc._f64(b), out=out,
+                         total=roofline.outputs(wl, out), bytes=roofline.algorithmic_bytes(wl, out),
+                         flops=roofline.flops(wl, out)))
+    return orc, prep, np
+
+
+def cpu_baseline(wls, min_seconds=10.0, max_seconds=30.0):
+    """Whole-workload oracle passes, repeated for about min_seconds."""
+    orc, prep, np = cpu_oracle_prepare(wls)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        for p in prep:
+            orc.forward(p["wl"], p["x"], p["w"], p["b"])
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or el * (reps + 1) / reps > max_seconds:
+            break
+    per = el / reps
+    tot_bytes = sum(p["bytes"] for p in prep)
+    tot_flops = sum(p["flops"] for p in prep)
+    return {"value": tot_bytes / per / 1e9, "unit": "GB/s", "tflops": tot_flops / per / 1e12,
+            "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"{reps} full pass(es) of the whole workload ({len(prep)} convolutions), "
+                      f"{el:.1f} s of fp64 direct-loop OpenMP work", "ms_per_step": per * 1e3}
+
+
+def run_reference(args, wls, rank, world):
+    """--impl reference: the oracle on the host cores, bounded sample per step."""
+    if rank != 0:
+        return
+    orc, prep, np = cpu_oracle_prepare(wls)
+    total_steps = args.steps + args.warmup
+    budget_s = 120.0
+    # outputs per step for each conv: a contiguous run of flat outputs sized
+    # from a quick rate probe so the whole run stays within the budget
+    probe_n = 20000
+    for p in prep:
+        idx = np.arange(min(probe_n, p["total"]), dtype=np.int64)
+        t0 = time.perf_counter()
+        orc.points(p["wl"], p["x"], p["w"], p["b"], idx)
+        p["rate"] = len(idx) / max(time.perf_counter() - t0, 1e-6)
+    per_step_s = budget_s / total_steps / len(prep)
+    for p in prep:
+        p["n"] = int(max(64, min(p["total"], p["rate"] * per_step_s)))
+    rng = np.random.default_rng(0)
+
+    def step(i):
+        for p in prep:
+            start = int(rng.integers(0, max(1, p["total"] - p["n"])))
+            orc.points(p["wl"], p["x"], p["w"], p["b"], np.arange(start, start + p["n"], dtype=np.int64))
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    el = time.perf_counter() - t0
+    frac_bytes = sum(p["bytes"] * p["n"] / p["total"] for p in prep)
+    value = frac_bytes * args.steps / el / 1e9
+    sample = ("per step: " + ", ".join(f"{p['n']} of {p['total']} outputs of {p['wl'].name}" for p in prep)
+              + "; bytes credited in proportion to outputs computed")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": wls[0].dtype, "data": "synthetic",
+            "config": {"workload": describe(wls), "layout": "NHWGC / GKYXC / NHWGK"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args, wls, set_name, rank, world):
+    import torch
+
+    import depthwise_convolution_forward_gb300 as gc
+    from depthwise_convolution_forward_gb300 import _binding as B
+    from depthwise_convolution_forward_gb300 import build, inputs, roofline
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    lib = B.load_library()
+    stream = torch.cuda.Stream(dev)
+    sh = stream.cuda_stream
+
+    tile = [int(t) for t in args.tile.split(",")] if args.tile else []
+    convs = []
+    step_bytes = 0
+    step_flops = 0
+    for wl in wls:
+        x, w, b = inputs.make_inputs(wl)
+        p = gc.problem_of(wl)
+        out = gc.grouped_conv_out_shape(p)
+        ysh = (wl.N, out[1], out[2], wl.G, wl.Kg) if wl.ndim == 2 else (wl.N, *out, wl.G, wl.Kg)
+        nbytes = roofline.algorithmic_bytes(wl, out)
+        step_bytes += nbytes
+        step_flops += roofline.flops(wl, out)
+        convs.append(dict(wl=wl, x=x, w=w, b=b, p=p, ysh=ysh, bytes=nbytes, flops=roofline.flops(wl, out),
+                          dt=gc.DTYPE_CODES[wl.dtype],
+                          kernel=gc.grouped_conv_select(p, gc.DTYPE_CODES[wl.dtype]) if not args.force_kernel
+                          else args.force_kernel))
+    per_set = sum(c["bytes"] for c in convs)  # x + y + w + bias of one step
+    R = max(3, -(-2 * L2_BYTES // max(per_set, 1)) + 1)
+    sets = []
+    for r in range(R):
+        s = []
+        for c in convs:
+            xd = c["x"].to(dev)
+            wd = c["w"].to(dev)
+            bd = c["b"].to(dev) if c["b"] is not None else None
+            yd = torch.empty(c["ysh"], dtype=c["x"].dtype, device=dev)
+            s.append((xd, wd, bd, yd))
+        sets.append(s)
+    torch.cuda.synchronize(dev)
+
+    opt = B.gconv_options()
+    opt.force_kernel = args.force_kernel
+    for i, t in enumerate(tile[:4]):
+        opt.tile[i] = t
+    optp = ctypes.byref(opt)
+
+    def launch(r, ci):
+        c = convs[ci]
+        xd, wd, bd, yd = sets[r][ci]
+        st = lib.grouped_conv_fwd_ex(xd.data_ptr(), wd.data_ptr(), bd.data_ptr() if bd is not None else None,
+                                     yd.data_ptr(), ctypes.byref(c["p"]), c["dt"], sh, optp)
+        if st != 0:
+            raise RuntimeError(f"grouped_conv_fwd_ex failed: {gc.gconv_last_error()}")
+
+    # warm-up (eager): plans cached, device state initialised
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            for ci in range(len(convs)):
+                launch(i % R, ci)
+    stream.synchronize()
+
+    # capture the timed steps into graphs with external event nodes
+    dv = DriverEvents()
+    nl = len(convs)
+    K = args.steps
+    chunk = 1000
+    events = dv.create(K * nl + 1)
+    graphs = []
+    k0 = 0
+    while k0 < K:
+        k1 = min(K, k0 + chunk)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            if k0 == 0:
+                dv.record_external(events[0], sh)
+            for k in range(k0, k1):
+                for ci in range(nl):
+                    launch(k % R, ci)
+                    dv.record_external(events[k * nl + ci + 1], sh)
+        graphs.append(g)
+        k0 = k1
+    # one untimed replay of the first graph to settle
+    graphs[0].replay()
+    stream.synchronize()
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist  # noqa: F811
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local)
+    sampler = ClockSampler(os.environ.get("BENCH_SMI_ID", gpu_id))
+    sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for g in graphs:
+            g.replay()
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+
+    total_ms = dv.elapsed_ms(events[0], events[K * nl])
+    launch_ms = [[] for _ in range(nl)]
+    step_ms = []
+    for k in range(K):
+        for ci in range(nl):
+            launch_ms[ci].append(dv.elapsed_ms(events[k * nl + ci], events[k * nl + ci + 1]))
+        step_ms.append(dv.elapsed_ms(events[k * nl], events[(k + 1) * nl]))
+    dv.destroy(events)
+
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # per-kernel aggregation (kernel id -> bytes, ms, launches)
+    per_kernel = {}
+    for ci, c in enumerate(convs):
+        name = gc.KERNEL_NAMES.get(c["kernel"], str(c["kernel"]))
+        e = per_kernel.setdefault(name, {"bytes": 0, "flops": 0, "ms": 0.0, "launches": 0})
+        e["bytes"] += c["bytes"] * K
+        e["flops"] += c["flops"] * K
+        e["ms"] += sum(launch_ms[ci])
+        e["launches"] += K
+    dom = max(per_kernel, key=lambda n: per_kernel[n]["ms"])
+    d = per_kernel[dom]
+    hbm_peak, tc_peak, peak_kind = load_peaks()
+    bound = "tensor" if dom == "igemm_tc" and d["flops"] / d["bytes"] > (tc_peak * 1e12) / (hbm_peak * 1e9) \
+        else "hbm"
+    if bound == "hbm":
+        achieved = d["bytes"] / (d["ms"] / 1e3) / 1e9
+        peak, unit = hbm_peak, "GB/s"
+    else:
+        achieved = d["flops"] / (d["ms"] / 1e3) / 1e12
+        peak, unit = tc_peak, "TFLOP/s"
+    traffic = load_traffic(dom, set_name)
+    roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "traffic": traffic, "kernel": dom, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)"
+            if peak_kind == "measured" else "fallback",
+            "algorithmic_bytes_per_launch": d["bytes"] / d["launches"],
+            "avg_launch_us": d["ms"] / d["launches"] * 1e3}
+
+    ms_per_step = total_ms / K
+    value = step_bytes * K * world / (total_ms / 1e3) / 1e9
+    tflops = step_flops * K * world / (total_ms / 1e3) / 1e12
+    med = statistics.median(step_ms)
+    per_launch = {}
+    for ci, c in enumerate(convs):
+        m = statistics.median(launch_ms[ci])
+        per_launch[c["wl"].name] = {
+            "kernel": gc.KERNEL_NAMES.get(c["kernel"]), "median_us": m * 1e3,
+            "GB_s": c["bytes"] / (m / 1e3) / 1e9, "TFLOP_s": c["flops"] / (m / 1e3) / 1e12,
+            "frac_hbm": c["bytes"] / (m / 1e3) / 1e9 / hbm_peak,
+            "frac_roofline": max(c["bytes"] / (hbm_peak * 1e9), c["flops"] / (tc_peak * 1e12)) / (m / 1e3)}
+
+    # end-to-end: pinned host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, convs, lib, dev, stream, world, dist, step_bytes, gc)
+
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wls[0].dtype, "data": "synthetic",
+            "config": {"workload": describe(wls), "layout": "NHWGC / GKYXC / NHWGK",
+                       "l2": f"rotating {R} input/output sets ({R * per_set / 1e6:.0f} MB > 2x L2)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "tflops": tflops, "median_ms_per_step": med,
+            "value_from_median": step_bytes / (med / 1e3) / 1e9,
+            "per_launch": per_launch, "roofline": roof,
+            "gpu_launches": K * nl, "timed_region_wall_s": wall}
+    if clocks:
+        line["clocks"] = clocks
+    if e2e:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wls)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, convs, lib, dev, stream, world, dist, step_bytes, gc):
+    import torch
+
+    host = []
+    h2d = d2h = 0
+    for c in convs:
+        xh = c["x"].pin_memory()
+        wh = c["w"].pin_memory()
+        bh = c["b"].pin_memory() if c["b"] is not None else None
+        yh = torch.empty(c["ysh"], dtype=c["x"].dtype).pin_memory()
+        xd = torch.empty_like(xh, device=dev)
+        wd = torch.empty_like(wh, device=dev)
+        bd = torch.empty_like(bh, device=dev) if bh is not None else None
+        yd = torch.empty(c["ysh"], dtype=c["x"].dtype, device=dev)
+        host.append((xh, wh, bh, yh, xd, wd, bd, yd))
+        h2d += xh.numel() * xh.element_size() + wh.numel() * wh.element_size() + \
+            (bh.numel() * bh.element_size() if bh is not None else 0)
+        d2h += yh.numel() * yh.element_size()
+    sh = stream.cuda_stream
+
+    def step():
+        with torch.cuda.stream(stream):
+            for c, (xh, wh, bh, yh, xd, wd, bd, yd) in zip(convs, host):
+                xd.copy_(xh, non_blocking=True)
+                wd.copy_(wh, non_blocking=True)
+                if bh is not None:
+                    bd.copy_(bh, non_blocking=True)
+                st = lib.grouped_conv_fwd(xd.data_ptr(), wd.data_ptr(),
+                                          bd.data_ptr() if bd is not None else None, yd.data_ptr(),
+                                          ctypes.byref(c["p"]), c["dt"], sh)
+                if st != 0:
+                    raise RuntimeError(gc.gconv_last_error())
+                yh.copy_(yd, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    stream.synchronize()
+    n = max(3, min(args.steps, 50))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": step_bytes * n * world / (ms / 1e3) / 1e9, "unit": "GB/s", "steps": n,
+            "ms_per_step": ms / n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "grouped_conv_fwd (C ABI) with pinned host buffers copied in and out each step"}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    set_name, wls = resolve(args.workload)
+    if args.impl == "reference":
+        run_reference(args, wls, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    run_ours(args, wls, set_name, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

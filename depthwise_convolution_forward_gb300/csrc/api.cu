@@ -1,0 +1,283 @@
+// C ABI of the grouped-convolution forward library: argument validation,
+// output-shape rule, shape-based kernel selection, tensor-map encoding and
+// launch.  Everything here runs on the host; the arithmetic runs in the
+// kernels (dw*.cu, generic.cu, tc*.cu).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gconv.h"
+#include "kernels.h"
+
+namespace gconv {
+
+// Device status word: [code, where].  Kernels set it when a bounded wait
+// expires; gconv_device_status / debug mode read and clear it.
+__device__ int g_status_word[2];
+
+namespace {
+
+thread_local char t_last_error[512] = "";
+
+gconv_status fail(gconv_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+// ---------------------------------------------------------------------------
+// Output extent: floor((I + 2p - d*(k-1) - 1) / s) + 1 (0 when nothing fits).
+// ---------------------------------------------------------------------------
+int64_t out_extent(int64_t in, int64_t k, int64_t s, int64_t p, int64_t d) {
+  const int64_t span = d * (k - 1) + 1;
+  const int64_t room = in + 2 * p - span;
+  if (room < 0) return 0;
+  return room / s + 1;
+}
+
+gconv_status validate(const gconv_problem* p, Geometry* g) {
+  if (p == nullptr) return fail(GCONV_ERR_INVALID_ARG, "problem pointer is NULL");
+  if (p->ndim != 2 && p->ndim != 3) return fail(GCONV_ERR_INVALID_ARG, "ndim must be 2 or 3 (got %d)", p->ndim);
+  if (p->reserved != 0) return fail(GCONV_ERR_INVALID_ARG, "reserved field must be 0");
+  if (p->N < 1) return fail(GCONV_ERR_INVALID_ARG, "N must be >= 1");
+  if (p->G < 1 || p->C < 1 || p->K < 1) return fail(GCONV_ERR_INVALID_ARG, "G, C and K must be >= 1");
+  if (p->C % p->G != 0) return fail(GCONV_ERR_INVALID_ARG, "C (%d) is not divisible by G (%d)", p->C, p->G);
+  if (p->K % p->G != 0) return fail(GCONV_ERR_INVALID_ARG, "K (%d) is not divisible by G (%d)", p->K, p->G);
+  for (int i = 0; i < 3; ++i) {
+    if (p->in[i] < 1 || p->ker[i] < 1) return fail(GCONV_ERR_INVALID_ARG, "extents must be >= 1 (dim %d)", i);
+    if (p->stride[i] < 1 || p->dil[i] < 1) return fail(GCONV_ERR_INVALID_ARG, "stride and dilation must be >= 1 (dim %d)", i);
+    if (p->pad[i] < 0) return fail(GCONV_ERR_INVALID_ARG, "padding must be >= 0 (dim %d)", i);
+  }
+  if (p->ndim == 2 && (p->in[0] != 1 || p->ker[0] != 1 || p->stride[0] != 1 || p->dil[0] != 1 || p->pad[0] != 0))
+    return fail(GCONV_ERR_INVALID_ARG, "2D problem: depth fields must be in=ker=stride=dil=1, pad=0");
+  int64_t o[3];
+  for (int i = 0; i < 3; ++i) {
+    o[i] = out_extent(p->in[i], p->ker[i], p->stride[i], p->pad[i], p->dil[i]);
+    if (o[i] < 1) return fail(GCONV_ERR_INVALID_ARG, "output extent of dim %d is empty", i);
+  }
+  // Element counts must fit comfortably in 63 bits.
+  const double xe = (double)p->N * p->in[0] * p->in[1] * p->in[2] * p->C;
+  const double ye = (double)p->N * o[0] * o[1] * o[2] * p->K;
+  if (xe > 4e18 || ye > 4e18) return fail(GCONV_ERR_INVALID_ARG, "tensor too large");
+  if (p->N > (int64_t)1 << 31) return fail(GCONV_ERR_INVALID_ARG, "N too large");
+  g->N = p->N;
+  g->G = p->G;
+  g->Cg = p->C / p->G;
+  g->Kg = p->K / p->G;
+  g->D = p->in[0], g->H = p->in[1], g->W = p->in[2];
+  g->Do = (int)o[0], g->Ho = (int)o[1], g->Wo = (int)o[2];
+  g->Z = p->ker[0], g->Y = p->ker[1], g->X = p->ker[2];
+  g->sD = p->stride[0], g->sH = p->stride[1], g->sW = p->stride[2];
+  g->pD = p->pad[0], g->pH = p->pad[1], g->pW = p->pad[2];
+  g->dD = p->dil[0], g->dH = p->dil[1], g->dW = p->dil[2];
+  g->ndim = p->ndim;
+  return GCONV_OK;
+}
+
+bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+  if (a == nullptr || b == nullptr) return false;
+  const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  return a0 < b0 + (uintptr_t)bbytes && b0 < a0 + (uintptr_t)abytes;
+}
+
+int select_kernel(const Geometry& g, DType dt, const LaunchArgs* a) {
+  if (dw_supported(g, dt, a)) return GCONV_KERNEL_DIRECT_DW;
+  if (tc_supported(g, dt, a)) return GCONV_KERNEL_IGEMM_TC;
+  return GCONV_KERNEL_DIRECT_GENERIC;
+}
+
+// ---------------------------------------------------------------------------
+// Per-device cache: SM count, shared-memory limit, status-word address.
+// ---------------------------------------------------------------------------
+struct DevSlot {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  DeviceInfo info{};
+  int* status = nullptr;
+};
+constexpr int kMaxDevices = 64;
+DevSlot g_dev[kMaxDevices];
+
+cudaError_t device_slot(DevSlot** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  DevSlot& s = g_dev[dev];
+  std::call_once(s.once, [&s, dev]() {
+    s.info.device = dev;
+    cudaError_t r = cudaDeviceGetAttribute(&s.info.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (r == cudaSuccess)
+      r = cudaDeviceGetAttribute(&s.info.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (r == cudaSuccess) r = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.status), g_status_word);
+    if (r == cudaSuccess) r = cudaMemset(s.status, 0, 2 * sizeof(int));
+    if (r == cudaSuccess) r = cudaDeviceSynchronize();
+    s.err = r;
+  });
+  *out = &s;
+  return s.err;
+}
+
+// ---------------------------------------------------------------------------
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+gconv_status read_and_clear_status(DevSlot* slot, cudaStream_t stream, int32_t* code, int32_t* where) {
+  int host[2] = {0, 0};
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(host, slot->status, sizeof(host), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess && host[0] != 0) {
+    e = cudaMemsetAsync(slot->status, 0, sizeof(host), stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  }
+  if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "status read failed: %s", cudaGetErrorString(e));
+  if (code) *code = host[0];
+  if (where) *where = host[1];
+  return GCONV_OK;
+}
+
+}  // namespace
+
+CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, uint32_t rank, const void* base,
+                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                      const uint32_t* elem_strides) {
+  std::call_once(g_encode_once, []() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  if (g_encode == nullptr) return CUDA_ERROR_NOT_FOUND;
+  return g_encode(map, type, rank, const_cast<void*>(base), dims, strides_bytes, box, elem_strides,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace gconv
+
+using namespace gconv;
+
+extern "C" {
+
+const char* gconv_status_string(gconv_status s) {
+  switch (s) {
+    case GCONV_OK: return "ok";
+    case GCONV_ERR_INVALID_ARG: return "invalid argument";
+    case GCONV_ERR_UNSUPPORTED: return "unsupported";
+    case GCONV_ERR_CUDA: return "CUDA error";
+    case GCONV_ERR_TIMEOUT: return "in-kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* gconv_last_error(void) { return t_last_error; }
+
+gconv_status grouped_conv_out_shape(const gconv_problem* p, int32_t out[3]) {
+  Geometry g;
+  gconv_status s = validate(p, &g);
+  if (s != GCONV_OK) return s;
+  if (out == nullptr) return fail(GCONV_ERR_INVALID_ARG, "out pointer is NULL");
+  out[0] = g.Do, out[1] = g.Ho, out[2] = g.Wo;
+  return GCONV_OK;
+}
+
+gconv_status grouped_conv_select(const gconv_problem* p, gconv_dtype dt, int32_t* kernel) {
+  Geometry g;
+  gconv_status s = validate(p, &g);
+  if (s != GCONV_OK) return s;
+  if (dt != GCONV_F32 && dt != GCONV_F16 && dt != GCONV_BF16) return fail(GCONV_ERR_UNSUPPORTED, "unknown dtype %d", (int)dt);
+  if (kernel == nullptr) return fail(GCONV_ERR_INVALID_ARG, "kernel pointer is NULL");
+  *kernel = select_kernel(g, (DType)dt, nullptr);
+  return GCONV_OK;
+}
+
+gconv_status grouped_conv_fwd_ex(const void* x, const void* w, const void* bias, void* y, const gconv_problem* p,
+                                 gconv_dtype dt, struct CUstream_st* stream, gconv_options* opt) {
+  Geometry g;
+  gconv_status s = validate(p, &g);
+  if (s != GCONV_OK) return s;
+  if (dt != GCONV_F32 && dt != GCONV_F16 && dt != GCONV_BF16) return fail(GCONV_ERR_UNSUPPORTED, "unknown dtype %d", (int)dt);
+  if (x == nullptr || w == nullptr || y == nullptr) return fail(GCONV_ERR_INVALID_ARG, "x, w and y must not be NULL");
+  const int es = dtype_bytes((DType)dt);
+  const int64_t yb = g.y_elems() * es;
+  if (overlaps(y, yb, x, g.x_elems() * es) || overlaps(y, yb, w, g.w_elems() * es) ||
+      overlaps(y, yb, bias, (int64_t)g.K() * es))
+    return fail(GCONV_ERR_INVALID_ARG, "y overlaps an input buffer");
+
+  DevSlot* slot = nullptr;
+  cudaError_t e = device_slot(&slot);
+  if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
+
+  LaunchArgs a;
+  a.x = x, a.w = w, a.bias = bias, a.y = y;
+  a.dt = (DType)dt;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  a.status = slot->status;
+  a.wait_limit_ns = (opt && opt->wait_limit_ns > 0) ? (uint64_t)opt->wait_limit_ns : 2000000000ull;
+  a.test_flags = opt ? opt->test_flags : 0;
+  for (int i = 0; i < 4; ++i) a.tile[i] = opt ? opt->tile[i] : 0;
+
+  int kernel = (opt && opt->force_kernel) ? opt->force_kernel : select_kernel(g, a.dt, &a);
+  if (kernel == GCONV_KERNEL_DIRECT_DW && !dw_supported(g, a.dt, &a))
+    return fail(GCONV_ERR_UNSUPPORTED, "depthwise kernel cannot run this problem");
+  if (kernel == GCONV_KERNEL_IGEMM_TC && !tc_supported(g, a.dt, &a))
+    return fail(GCONV_ERR_UNSUPPORTED, "tensor-core kernel cannot run this problem");
+  if (kernel < GCONV_KERNEL_DIRECT_DW || kernel > GCONV_KERNEL_IGEMM_TC)
+    return fail(GCONV_ERR_UNSUPPORTED, "unknown kernel id %d", kernel);
+  if (opt) opt->selected = kernel;
+
+  switch (kernel) {
+    case GCONV_KERNEL_DIRECT_DW: e = dw_launch(g, a, slot->info); break;
+    case GCONV_KERNEL_IGEMM_TC: e = tc_launch(g, a, slot->info); break;
+    default: e = generic_launch(g, a, slot->info); break;
+  }
+  if (e == cudaErrorNotSupported) return fail(GCONV_ERR_UNSUPPORTED, "no launch plan for this problem");
+  if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+
+  if (opt && opt->debug) {
+    int32_t code = 0, where = 0;
+    gconv_status st = read_and_clear_status(slot, a.stream, &code, &where);
+    if (st != GCONV_OK) return st;
+    if (code != 0) return fail(GCONV_ERR_TIMEOUT, "in-kernel wait timed out (site %d)", where);
+  }
+  return GCONV_OK;
+}
+
+gconv_status grouped_conv_fwd(const void* x, const void* w, const void* bias, void* y, const gconv_problem* p,
+                              gconv_dtype dt, struct CUstream_st* stream) {
+  return grouped_conv_fwd_ex(x, w, bias, y, p, dt, stream, nullptr);
+}
+
+gconv_status gconv_epilogue_apply(const float* acc, const void* bias, void* y, int64_t rows, int32_t cols,
+                                  gconv_dtype dt, struct CUstream_st* stream) {
+  if (acc == nullptr || y == nullptr) return fail(GCONV_ERR_INVALID_ARG, "acc and y must not be NULL");
+  if (rows < 0 || cols < 1) return fail(GCONV_ERR_INVALID_ARG, "rows must be >= 0 and cols >= 1");
+  if (dt != GCONV_F32 && dt != GCONV_F16 && dt != GCONV_BF16) return fail(GCONV_ERR_UNSUPPORTED, "unknown dtype %d", (int)dt);
+  cudaError_t e = epilogue_launch(acc, bias, y, rows, cols, (DType)dt, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+  return GCONV_OK;
+}
+
+gconv_status gconv_device_status(struct CUstream_st* stream, int32_t* code, int32_t* where) {
+  DevSlot* slot = nullptr;
+  cudaError_t e = device_slot(&slot);
+  if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
+  return read_and_clear_status(slot, reinterpret_cast<cudaStream_t>(stream), code, where);
+}
+
+}  // extern "C"

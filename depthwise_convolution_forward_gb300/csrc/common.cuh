@@ -1,0 +1,170 @@
+// Shared device helpers for the grouped-convolution kernels: element traits,
+// the fused bias + cast epilogue, mbarrier / TMA wrappers and the bounded
+// waits that report a timeout through a status word instead of hanging.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+
+namespace gconv {
+
+// ---------------------------------------------------------------------------
+// Element traits: storage type <-> fp32, 16-byte vectors.
+// ---------------------------------------------------------------------------
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static constexpr int kVec = 4;  // elements per 16-byte vector
+  __device__ __forceinline__ static float to_f32(float v) { return v; }
+  __device__ __forceinline__ static float from_f32(float v) { return v; }
+};
+template <> struct Elem<__half> {
+  static constexpr int kVec = 8;
+  __device__ __forceinline__ static float to_f32(__half v) { return __half2float(v); }
+  __device__ __forceinline__ static __half from_f32(float v) { return __float2half_rn(v); }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static constexpr int kVec = 8;
+  __device__ __forceinline__ static float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+  __device__ __forceinline__ static __nv_bfloat16 from_f32(float v) { return __float2bfloat16_rn(v); }
+};
+
+// Unpack one 16-byte vector into fp32 values.
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& v, float* out) {
+  const T* e = reinterpret_cast<const T*>(&v);
+#pragma unroll
+  for (int i = 0; i < Elem<T>::kVec; ++i) out[i] = Elem<T>::to_f32(e[i]);
+}
+
+// ---------------------------------------------------------------------------
+// Kc: fused epilogue.  acc (fp32) + bias (already widened to fp32), then one
+// round-to-nearest-even cast to the output type.  The single rounding step is
+// the only place output precision is lost.
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ T epilogue_one(float acc, float bias) {
+  return Elem<T>::from_f32(acc + bias);
+}
+
+// VEC consecutive outputs -> one aligned vector store (VEC * sizeof(T) bytes).
+template <typename T, int VEC>
+__device__ __forceinline__ void epilogue_store(T* dst, const float* acc, const float* bias) {
+  static_assert((VEC * sizeof(T)) % 4 == 0, "vector store must be whole words");
+  constexpr int kWords = VEC * sizeof(T) / 4;
+  uint32_t words[kWords];
+  T* e = reinterpret_cast<T*>(words);
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) e[i] = epilogue_one<T>(acc[i], bias[i]);
+  if constexpr (kWords == 4) {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+  } else if constexpr (kWords == 2) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(words[0], words[1]);
+  } else if constexpr (kWords == 8) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    d4[0] = make_uint4(words[0], words[1], words[2], words[3]);
+    d4[1] = make_uint4(words[4], words[5], words[6], words[7]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < kWords; ++i) reinterpret_cast<uint32_t*>(dst)[i] = words[i];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Status word (two ints: code, where).  First writer wins.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void report(int* status, int code, int where) {
+  if (status != nullptr && atomicCAS(status, 0, code) == 0) atomicExch(status + 1, where);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on phase `parity`.  Returns false once `limit_ns` of wall time
+// (the GPU global timer) has passed without the phase completing.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA (tiled tensor copies global -> shared, completion on an mbarrier)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
+                                            int c1, int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(c4)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
+                                            int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+// Plain bulk copy (no tensor map): both addresses 16-byte aligned, size % 16 == 0.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+}  // namespace gconv

@@ -1,0 +1,38 @@
+// Ka dispatch: support check and per-dtype launch.
+#include "kernels.h"
+
+namespace gconv {
+
+cudaError_t dw_launch_f32(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
+cudaError_t dw_launch_f16(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
+cudaError_t dw_launch_bf16(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
+
+// Depthwise (Cg == Kg == 1), 3x3 spatial filter, equal H/W stride and
+// dilation in {1, 2}; channels a multiple of one 16-byte vector; x and y
+// 16-byte aligned (TMA and vector-store requirements).  Any depth filter.
+bool dw_supported(const Geometry& g, DType dt, const LaunchArgs* a) {
+  const int es = dtype_bytes(dt);
+  const int vec = 16 / es;
+  if (g.Cg != 1 || g.Kg != 1) return false;
+  if (g.Y != 3 || g.X != 3) return false;
+  if (g.sH != g.sW || g.dH != g.dW) return false;
+  if (g.sH < 1 || g.sH > 2 || g.dH < 1 || g.dH > 2) return false;
+  if (g.C() % vec != 0) return false;
+  if (g.Z > 7 || (g.Z - 1) * g.dD + 1 > 16) return false;
+  if (g.W > (1 << 30) || g.H > (1 << 30)) return false;
+  if (a) {
+    if ((reinterpret_cast<uintptr_t>(a->x) & 15) || (reinterpret_cast<uintptr_t>(a->y) & 15)) return false;
+  }
+  return true;
+}
+
+cudaError_t dw_launch(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev) {
+  switch (a.dt) {
+    case kF32: return dw_launch_f32(g, a, dev);
+    case kF16: return dw_launch_f16(g, a, dev);
+    case kBF16: return dw_launch_bf16(g, a, dev);
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace gconv

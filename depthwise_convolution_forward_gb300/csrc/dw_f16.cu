@@ -1,0 +1,8 @@
+// Depthwise direct kernel (Ka) instantiations for __half storage.
+#include "dw_launch.cuh"
+
+namespace gconv {
+cudaError_t dw_launch_f16(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev) {
+  return dw::dw_launch_typed<__half>(g, a, dev);
+}
+}  // namespace gconv

@@ -1,0 +1,8 @@
+// Depthwise direct kernel (Ka) instantiations for float storage.
+#include "dw_launch.cuh"
+
+namespace gconv {
+cudaError_t dw_launch_f32(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev) {
+  return dw::dw_launch_typed<float>(g, a, dev);
+}
+}  // namespace gconv

@@ -1,0 +1,183 @@
+// Host-side planning and launch of the depthwise direct kernel (Ka) for one
+// element type.  Included once per dtype translation unit so the template
+// instantiations compile in parallel.
+#pragma once
+
+#include <algorithm>
+
+#include "dw_impl.cuh"
+#include "plan_cache.h"
+
+namespace gconv {
+namespace dw {
+
+struct Plan {
+  int TH, TW, TC, WB, stages;
+  int Dh, Hh, Wh;
+  int tiles_c, tiles_w, tiles_h;
+  int64_t num_tiles;
+  uint32_t stage_bytes, stage_stride, stage_off, smem_bytes;
+  int threads;
+};
+
+constexpr int kDwK = 3;  // compiled filter extent (Y == X == 3)
+constexpr uint32_t kStageBudget = 48 * 1024;
+
+inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+// Choose TC (channels per tile): the whole pixel when it fits a TMA box,
+// otherwise the largest divisor of C that is a multiple of VEC and <= 256.
+inline int pick_tc(int C, int vec) {
+  if (C <= 256) return C;
+  for (int tc = 256 / vec * vec; tc >= vec; tc -= vec)
+    if (C % tc == 0) return tc;
+  return 256 / vec * vec;
+}
+
+inline bool make_plan(const Geometry& g, int es, const int* tile_override, int num_sms, Plan* out) {
+  const int vec = 16 / es;
+  const int S = g.sH, DL = g.dH;
+  Plan best{};
+  double best_cost = 1e30;
+  const int TC = pick_tc(g.C(), vec);
+  const int NV = TC / vec;
+  const int Dh = (g.Z - 1) * g.dD + 1;
+  for (int WB : {4, 8}) {
+    if (tile_override && tile_override[2] && tile_override[2] != WB) continue;
+    const int tw_max = std::min(ceil_div(g.Wo, WB) * WB, 64);
+    for (int TW = WB; TW <= tw_max; TW += WB) {
+      if (tile_override && tile_override[1] && tile_override[1] != TW) continue;
+      const int Wh = (TW - 1) * S + (kDwK - 1) * DL + 1;
+      if (Wh > 256) break;
+      for (int TH = 1; TH <= std::min(g.Ho, 64); ++TH) {
+        if (tile_override && tile_override[0] && tile_override[0] != TH) continue;
+        const int Hh = (TH - 1) * S + (kDwK - 1) * DL + 1;
+        if (Hh > 256) break;
+        const uint32_t bytes = (uint32_t)Dh * Hh * Wh * TC * es;
+        const int items = NV * (TW / WB) * TH;
+        if (items > (WB == 8 ? 256 : 512)) break;
+        if (bytes > kStageBudget && !(tile_override && tile_override[0])) break;
+        const int tiles_w = ceil_div(g.Wo, TW), tiles_h = ceil_div(g.Ho, TH);
+        const int tiles_c = ceil_div(g.C(), TC);
+        const int64_t tiles = (int64_t)tiles_c * tiles_w * tiles_h * g.Do * g.N;
+        // cost: shared-memory fill bytes per useful output byte, plus idle
+        // compute slots, plus a penalty for too few threads per CTA and for
+        // grids that leave SMs without work.
+        const double fill = (double)tiles * bytes;
+        const double useful = (double)g.N * g.Do * g.Ho * g.Wo * g.C() * es;
+        const double slots = (double)tiles * TH * TW * TC;
+        const double outs = (double)g.N * g.Do * g.Ho * g.Wo * g.C();
+        double cost = fill / useful + 0.5 * (slots / outs);
+        if (items < 128) cost += 0.5;
+        if (tiles < num_sms) cost += 1.0;
+        if (cost < best_cost) {
+          best_cost = cost;
+          best.TH = TH, best.TW = TW, best.TC = TC, best.WB = WB;
+          best.Dh = Dh, best.Hh = Hh, best.Wh = Wh;
+          best.tiles_c = tiles_c, best.tiles_w = tiles_w, best.tiles_h = tiles_h;
+          best.num_tiles = tiles;
+          best.stage_bytes = bytes;
+          best.threads = std::min(512, (items + 31) / 32 * 32);
+        }
+      }
+    }
+  }
+  if (best_cost >= 1e30) return false;
+  best.stage_stride = align_up(best.stage_bytes, 1024);
+  best.stage_off = align_up(fixed_smem_bytes<kDwK>(g.Z, best.TC), 1024);
+  int stages = (tile_override && tile_override[3]) ? tile_override[3] : 4;
+  while (stages > 2 && best.stage_off + stages * best.stage_stride > 200 * 1024) --stages;
+  best.stages = stages;
+  best.smem_bytes = best.stage_off + stages * best.stage_stride;
+  *out = best;
+  return true;
+}
+
+template <typename T>
+inline CUtensorMapDataType tma_type() {
+  if (std::is_same<T, float>::value) return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  if (std::is_same<T, __half>::value) return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
+
+template <typename T, int S, int DL, int WB>
+cudaError_t launch_variant(const CUtensorMap& map, const DwArgs& a, const Plan& p, int grid,
+                           cudaStream_t stream, int device) {
+  static SmemAttr attr;
+  auto kern = dw_kernel<T, kDwK, S, DL, WB>;
+  cudaError_t e = attr.ensure(kern, device, (int)p.smem_bytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, p.threads, p.smem_bytes, stream>>>(map, a);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const DeviceInfo& dev) {
+  const int es = sizeof(T);
+  struct Key {
+    Geometry g;
+    int tile[4];
+    int num_sms;
+  } key;
+  std::memset(&key, 0, sizeof(key));
+  key.g = g;
+  std::memcpy(key.tile, la.tile, sizeof(key.tile));
+  key.num_sms = dev.num_sms;
+  static PlanCache<Plan> cache;
+  Plan p;
+  if (!cache.get(key, &p)) {
+    if (!make_plan(g, es, la.tile, dev.num_sms, &p)) return cudaErrorNotSupported;
+    cache.put(key, p);
+  }
+  if (p.smem_bytes > (uint32_t)dev.max_smem_optin) return cudaErrorNotSupported;
+
+  // x viewed as a 5-D tensor (C, W, H, D, N), innermost first.
+  CUtensorMap map;
+  const uint64_t C = g.C();
+  uint64_t dims[5] = {C, (uint64_t)g.W, (uint64_t)g.H, (uint64_t)g.D, (uint64_t)g.N};
+  uint64_t strides[4] = {C * es, C * es * g.W, C * es * g.W * g.H, C * es * g.W * g.H * g.D};
+  uint32_t box[5] = {(uint32_t)p.TC, (uint32_t)p.Wh, (uint32_t)p.Hh, (uint32_t)p.Dh, 1u};
+  uint32_t estr[5] = {1, 1, 1, 1, 1};
+  if (encode_tiled(&map, tma_type<T>(), 5, la.x, dims, strides, box, estr) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+
+  DwArgs a;
+  a.w = la.w;
+  a.bias = la.bias;
+  a.y = la.y;
+  a.C = g.C();
+  a.Do = g.Do, a.Ho = g.Ho, a.Wo = g.Wo;
+  a.Z = g.Z, a.dD = g.dD, a.sD = g.sD, a.pD = g.pD, a.pH = g.pH, a.pW = g.pW;
+  a.TH = p.TH, a.TW = p.TW, a.TC = p.TC;
+  a.Dh = p.Dh, a.Hh = p.Hh, a.Wh = p.Wh;
+  a.tiles_c = p.tiles_c, a.tiles_w = p.tiles_w, a.tiles_h = p.tiles_h;
+  a.num_tiles = p.num_tiles;
+  a.stages = p.stages;
+  a.stage_bytes = p.stage_bytes;
+  a.stage_stride = p.stage_stride;
+  a.stage_off = p.stage_off;
+  a.status = la.status;
+  a.wait_limit_ns = la.wait_limit_ns;
+  a.test_flags = la.test_flags;
+
+  const int64_t grid64 = std::min<int64_t>(p.num_tiles, (int64_t)dev.num_sms);
+  const int grid = (int)std::max<int64_t>(1, grid64);
+  const int S = g.sH, DL = g.dH;
+#define GCONV_DW_CASE(s_, d_, wb_)                            \
+  if (S == s_ && DL == d_ && p.WB == wb_)                     \
+    return launch_variant<T, s_, d_, wb_>(map, a, p, grid, la.stream, dev.device);
+  GCONV_DW_CASE(1, 1, 4)
+  GCONV_DW_CASE(1, 1, 8)
+  GCONV_DW_CASE(2, 1, 4)
+  GCONV_DW_CASE(2, 1, 8)
+  GCONV_DW_CASE(1, 2, 4)
+  GCONV_DW_CASE(1, 2, 8)
+  GCONV_DW_CASE(2, 2, 4)
+  GCONV_DW_CASE(2, 2, 8)
+#undef GCONV_DW_CASE
+  return cudaErrorNotSupported;
+}
+
+}  // namespace dw
+}  // namespace gconv

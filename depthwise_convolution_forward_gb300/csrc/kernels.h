@@ -1,0 +1,78 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not installed, not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gconv {
+
+enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+inline int dtype_bytes(DType t) { return t == kF32 ? 4 : 2; }
+
+// Validated, normalised problem.  2D problems have D = Do = Z = 1.
+struct Geometry {
+  int64_t N;
+  int G, Cg, Kg;
+  int D, H, W;
+  int Do, Ho, Wo;
+  int Z, Y, X;
+  int sD, sH, sW;
+  int pD, pH, pW;
+  int dD, dH, dW;
+  int ndim;
+  int C() const { return G * Cg; }
+  int K() const { return G * Kg; }
+  int taps() const { return Z * Y * X; }
+  int64_t x_elems() const { return N * D * H * W * (int64_t)C(); }
+  int64_t y_elems() const { return N * Do * Ho * Wo * (int64_t)K(); }
+  int64_t w_elems() const { return (int64_t)K() * taps() * Cg; }
+};
+
+struct LaunchArgs {
+  const void* x;
+  const void* w;
+  const void* bias;  // may be null
+  void* y;
+  DType dt;
+  cudaStream_t stream;
+  int* status;  // device status word [code, where]
+  uint64_t wait_limit_ns;
+  int test_flags;
+  int tile[4];  // tuning overrides, 0 = automatic
+};
+
+// Device properties needed by the launchers (cached per device by api.cu).
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  int max_smem_optin;  // bytes per block
+};
+
+// Tensor-map encoder (driver entry point resolved once by api.cu).
+CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, uint32_t rank, const void* base,
+                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                      const uint32_t* elem_strides);
+
+// ---- Ka: TMA-staged depthwise direct kernel (Cg == Kg == 1) -------------
+// Returns true when the kernel supports this problem (shape, dtype, alignment).
+bool dw_supported(const Geometry& g, DType dt, const LaunchArgs* a);
+cudaError_t dw_launch(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
+
+// ---- generic direct kernel (any shape, dtype, alignment) ----------------
+cudaError_t generic_launch(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
+
+// ---- Kb: tcgen05 / TMEM grouped implicit GEMM ----------------------------
+bool tc_supported(const Geometry& g, DType dt, const LaunchArgs* a);
+cudaError_t tc_launch(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
+
+// ---- Kc alone (epilogue test entry) --------------------------------------
+cudaError_t epilogue_launch(const float* acc, const void* bias, void* y, int64_t rows, int cols,
+                            DType dt, cudaStream_t stream);
+
+// Status codes written into the device status word.
+enum DevStatus : int { kDevOk = 0, kDevTimeout = 1 };
+
+}  // namespace gconv

@@ -1,0 +1,177 @@
+/*
+ * gconv.h -- C ABI of the GB300 grouped-convolution forward library.
+ *
+ * The operation is the grouped convolution forward pass (groups > 1,
+ * including depthwise groups == C), 2D and 3D, with optional bias, stride,
+ * padding and dilation:
+ *
+ *   y[n, od, oh, ow, g, k] = sum_{z,yy,xx} sum_{cg < Cg}
+ *        x[n, od*sD - pD + z*dD, oh*sH - pH + yy*dH, ow*sW - pW + xx*dW, g, cg]
+ *      * w[g, k, z, yy, xx, cg]  (+ bias[g*Kg + k])
+ *
+ * with Cg = C/G, Kg = K/G and zero padding outside the input.  Passages that
+ * define it:
+ *   - rocm-libraries PR #10064 (Rocke grouped implicit-GEMM conv), Technical
+ *     Details: input channel c = g*Cg + c_in_group, weight channel extent Cg,
+ *     output channel k_out = g*Kg + n, C and K divisible by G.
+ *   - CK "Grouped Convolution -- Python Examples", Runner argument contract:
+ *     forward input X in NHWGC, weight W in GKYXC.
+ *   - CK "Grouped Convolution Tile Engine", Problem Registry: the problem
+ *     record N, C, K, G, Hi, Wi[, Di], Y, X[, Z], stride_*, pad_*, dilation_*.
+ *   - TileOps PR #1568 review, Code Review: bias and no-bias forward ops.
+ * Readings where the pages are silent: cross-correlation (no kernel flip);
+ * output extent O = floor((I + 2p - d*(k-1) - 1)/s) + 1 with symmetric zero
+ * padding; output layout channels-last [N, (Do), Ho, Wo, G, Kg]; bias in the
+ * tensors' dtype, added in fp32 before one round-to-nearest-even cast.
+ *
+ * Every function is thread-safe.  Device functions are asynchronous on the
+ * caller's stream unless stated otherwise.
+ */
+#ifndef GCONV_H_
+#define GCONV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's cudaStream_t is `struct CUstream_st *`; NULL is the
+ * legacy default stream. */
+struct CUstream_st;
+
+typedef enum gconv_status {
+  GCONV_OK = 0,
+  GCONV_ERR_INVALID_ARG = 1, /* malformed problem or pointer; nothing launched      */
+  GCONV_ERR_UNSUPPORTED = 2, /* well-formed but not handled (dtype, forced kernel)   */
+  GCONV_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed                    */
+  GCONV_ERR_TIMEOUT = 4      /* a bounded in-kernel wait expired (debug mode only)   */
+} gconv_status;
+
+typedef enum gconv_dtype {
+  GCONV_F32 = 0,  /* float32 storage, fp32 accumulation, FFMA only (no TF32) */
+  GCONV_F16 = 1,  /* IEEE binary16 storage, fp32 accumulation                */
+  GCONV_BF16 = 2  /* bfloat16 storage, fp32 accumulation                     */
+} gconv_dtype;
+
+/*
+ * Problem record.  All extents are element counts.  Spatial arrays are
+ * ordered outer to inner: [0] = depth (D / Z), [1] = height (H / Y),
+ * [2] = width (W / X).  A 2D problem sets ndim = 2 and in[0] = ker[0] =
+ * stride[0] = dil[0] = 1, pad[0] = 0.  Padding is symmetric per dimension.
+ * Layout: 88 bytes, naturally aligned, no implicit padding.
+ */
+typedef struct gconv_problem {
+  int32_t ndim;      /* 2 or 3                                               */
+  int32_t reserved;  /* must be 0                                            */
+  int64_t N;         /* batch, >= 1                                          */
+  int32_t G;         /* groups, >= 1                                         */
+  int32_t C;         /* input channels, C % G == 0                           */
+  int32_t K;         /* output channels, K % G == 0                          */
+  int32_t in[3];     /* input extents D, H, W  (>= 1)                        */
+  int32_t ker[3];    /* filter extents Z, Y, X (>= 1)                        */
+  int32_t stride[3]; /* >= 1                                                 */
+  int32_t pad[3];    /* >= 0, applied on both sides                          */
+  int32_t dil[3];    /* >= 1                                                 */
+} gconv_problem;
+
+/* Kernels the selector can pick (for options.force_kernel / options.selected). */
+typedef enum gconv_kernel {
+  GCONV_KERNEL_AUTO = 0,
+  GCONV_KERNEL_DIRECT_DW = 1,      /* Ka: TMA-staged depthwise direct kernel        */
+  GCONV_KERNEL_DIRECT_GENERIC = 2, /* direct kernel for any shape/dtype/alignment   */
+  GCONV_KERNEL_IGEMM_TC = 3        /* Kb: tcgen05/TMEM grouped implicit GEMM        */
+} gconv_kernel;
+
+/* Options of grouped_conv_fwd_ex.  Zero-initialise, then set what you need. */
+typedef struct gconv_options {
+  int32_t force_kernel;  /* gconv_kernel; AUTO (0) lets the selector choose        */
+  int32_t debug;         /* 1: synchronise the stream after the launch and turn a
+                            device-side status (timeout) into the return value   */
+  int64_t wait_limit_ns; /* bound on each in-kernel wait; 0 = 2 s                  */
+  int32_t test_flags;    /* bit 0: withhold the first input copy of CTA 0 so its
+                            first wait cannot complete (timeout-path test)       */
+  int32_t selected;      /* out: the gconv_kernel that was launched               */
+  int32_t tile[4];       /* tile overrides for tuning, 0 = automatic              */
+} gconv_options;
+
+/*
+ * grouped_conv_fwd -- y = grouped_conv(x, w) (+ bias).
+ *   x    device, [N, (D), H, W, G, Cg] packed, dtype dt          (read only)
+ *   w    device, [G, Kg, (Z), Y, X, Cg] packed, dtype dt         (read only)
+ *   bias device, [G*Kg] in dtype dt, or NULL for no bias           (read only)
+ *   y    device, [N, (Do), Ho, Wo, G, Kg] packed, dtype dt (written; must not
+ *        overlap x, w or bias)
+ *   p    host pointer to the problem record (read during the call only)
+ *   stream  the CUDA stream the kernel is enqueued on
+ * Ownership: the caller owns every buffer and the stream.  The library
+ * allocates no device memory, keeps no per-call state and copies nothing
+ * between host and device.  The launch is asynchronous; buffers must stay
+ * valid until the stream reaches it.
+ * Errors: GCONV_ERR_INVALID_ARG for a malformed problem (C or K not divisible
+ * by G, non-positive extents, empty output, 2D fields not neutral), NULL
+ * x/w/y/p, or y overlapping an input; GCONV_ERR_UNSUPPORTED for an unknown
+ * dtype; GCONV_ERR_CUDA if the launch fails.  Nothing is launched on error;
+ * gconv_last_error() then describes the reason.
+ */
+gconv_status grouped_conv_fwd(const void *x, const void *w, const void *bias, void *y,
+                              const gconv_problem *p, gconv_dtype dt, struct CUstream_st *stream);
+
+/*
+ * grouped_conv_fwd_ex -- grouped_conv_fwd with options (kernel override,
+ * debug synchronisation, wait bound, timeout-path test).  `opt` may be NULL.
+ * Same arguments, ownership and errors as grouped_conv_fwd, plus:
+ * GCONV_ERR_UNSUPPORTED when a forced kernel cannot run this problem, and,
+ * with opt->debug set, GCONV_ERR_TIMEOUT when a bounded in-kernel wait expired
+ * (the kernel then returned early and y is incomplete).  With debug set the
+ * call blocks until the stream has drained.
+ */
+gconv_status grouped_conv_fwd_ex(const void *x, const void *w, const void *bias, void *y,
+                                 const gconv_problem *p, gconv_dtype dt, struct CUstream_st *stream,
+                                 gconv_options *opt);
+
+/*
+ * grouped_conv_out_shape -- output extents {Do, Ho, Wo} of problem p
+ * (Do = 1 for 2D), by O = floor((I + 2p - d*(k-1) - 1)/s) + 1.  Host only,
+ * no GPU needed.  GCONV_ERR_INVALID_ARG for a malformed or empty problem.
+ */
+gconv_status grouped_conv_out_shape(const gconv_problem *p, int32_t out[3]);
+
+/*
+ * grouped_conv_select -- which gconv_kernel grouped_conv_fwd would launch for
+ * (p, dt) with 16-byte aligned buffers.  Host only, no GPU needed.
+ */
+gconv_status grouped_conv_select(const gconv_problem *p, gconv_dtype dt, int32_t *kernel);
+
+/*
+ * gconv_epilogue_apply -- runs the fused epilogue (Kc) alone:
+ *   y[r, c] = round_to_nearest_even_dt(acc[r, c] + (bias ? float(bias[c]) : 0))
+ *   acc  device fp32 [rows, cols];  bias device [cols] in dt or NULL;
+ *   y    device [rows, cols] in dt.  Asynchronous on `stream`.
+ * The same device code finishes every convolution kernel; this entry point
+ * exists so the epilogue can be tested bit-for-bit on its own.
+ * Errors: GCONV_ERR_INVALID_ARG (NULL acc/y, rows < 0, cols < 1),
+ * GCONV_ERR_UNSUPPORTED (dtype), GCONV_ERR_CUDA.
+ */
+gconv_status gconv_epilogue_apply(const float *acc, const void *bias, void *y, int64_t rows,
+                                  int32_t cols, gconv_dtype dt, struct CUstream_st *stream);
+
+/*
+ * gconv_device_status -- synchronises `stream`, then reads and clears the
+ * current device's status word that kernels set when a bounded wait expires.
+ * *code = 0 (none) or 1 (timeout); *where = the kernel-specific wait site.
+ * Returns GCONV_ERR_CUDA if synchronisation or the read fails.
+ */
+gconv_status gconv_device_status(struct CUstream_st *stream, int32_t *code, int32_t *where);
+
+/* Static description of a status code. */
+const char *gconv_status_string(gconv_status s);
+
+/* Human-readable reason for the calling thread's last non-OK status. */
+const char *gconv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GCONV_H_ */

@@ -1,0 +1,126 @@
+"""Host-side C-ABI checks: library loads, exports what the header declares,
+validates arguments and computes output shapes.  No GPU needed."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import depthwise_convolution_forward_gb300 as gc
+from depthwise_convolution_forward_gb300 import _binding as B
+from depthwise_convolution_forward_gb300 import build, inputs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    build.build()
+    return B.load_library()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "gconv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)))
+
+
+def test_header_symbols_exported(lib):
+    names = header_functions()
+    assert "grouped_conv_fwd" in names and len(names) >= 8, names
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    for n in names:
+        assert n in exported, f"{n} declared in gconv.h but not exported"
+        assert hasattr(lib, n)
+
+
+def test_struct_layout():
+    assert ctypes.sizeof(B.gconv_problem) == 88
+    assert B.gconv_problem.N.offset == 8
+    assert B.gconv_problem.dil.offset == 76
+    assert ctypes.sizeof(B.gconv_options) == 40
+
+
+def good(**kw):
+    base = dict(ndim=2, N=2, G=4, C=8, K=12, inp=(1, 9, 7), ker=(1, 3, 3), stride=(1, 1, 1),
+                pad=(0, 1, 1), dil=(1, 1, 1))
+    base.update(kw)
+    return B.make_problem(**base)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(C=9), dict(K=10), dict(G=0), dict(N=0), dict(ndim=4), dict(inp=(1, 0, 7)),
+    dict(ker=(1, 0, 3)), dict(stride=(1, 0, 1)), dict(dil=(1, 1, 0)), dict(pad=(0, -1, 1)),
+    dict(inp=(2, 9, 7)), dict(ker=(3, 3, 3)), dict(pad=(1, 1, 1)), dict(stride=(2, 1, 1)),
+    dict(inp=(1, 2, 2), pad=(0, 0, 0)),  # 3x3 window does not fit: empty output
+])
+def test_invalid_problem_rejected(bad):
+    p = good(**bad)
+    with pytest.raises(gc.GconvError) as e:
+        gc.grouped_conv_out_shape(p)
+    assert e.value.status == B.GCONV_ERR_INVALID_ARG
+    assert gc.gconv_last_error()
+
+
+def test_reserved_must_be_zero():
+    p = good()
+    p.reserved = 1
+    with pytest.raises(gc.GconvError):
+        gc.grouped_conv_out_shape(p)
+
+
+def test_null_pointers_rejected_before_launch():
+    p = good()
+    with pytest.raises(gc.GconvError) as e:
+        gc.grouped_conv_fwd(None, 16, None, 32, p, B.GCONV_F32, None)
+    assert e.value.status == B.GCONV_ERR_INVALID_ARG
+    with pytest.raises(gc.GconvError) as e:
+        gc.grouped_conv_fwd(16, 16, None, 32, p, 7, None)
+    assert e.value.status == B.GCONV_ERR_UNSUPPORTED
+
+
+def test_overlapping_output_rejected():
+    p = good()
+    base = 1 << 20
+    with pytest.raises(gc.GconvError) as e:
+        gc.grouped_conv_fwd(base, base + (1 << 16), None, base + 64, p, B.GCONV_F32, None)
+    assert e.value.status == B.GCONV_ERR_INVALID_ARG
+    assert "overlap" in gc.gconv_last_error()
+
+
+def test_out_shape_matches_oracle(orc):
+    rng = np.random.default_rng(5)
+    for _ in range(300):
+        wl = inputs.random_problem(rng)
+        got = gc.grouped_conv_out_shape(gc.problem_of(wl))
+        assert got == orc.out_shape(wl), wl
+
+
+def test_status_strings():
+    for s in range(5):
+        assert gc.gconv_status_string(s)
+    assert "unknown" in gc.gconv_status_string(42)
+
+
+def test_selector_is_shape_based():
+    sel = {wl.name: gc.grouped_conv_select(gc.problem_of(wl), gc.DTYPE_CODES[wl.dtype])
+           for wl in inputs.all_workloads()}
+    assert sel["mbv2_dw_s1_f16"] == B.KERNEL_DIRECT_DW
+    assert sel["mbv2_dw_s2_f16"] == B.KERNEL_DIRECT_DW
+    assert sel["sweep_g512_d2_s2_bf16"] == B.KERNEL_DIRECT_DW
+    assert sel["grouped2d_f32_smoke"] == B.KERNEL_DIRECT_GENERIC  # fp32 never on tensor cores
+    # depthwise with 3 channels breaks 16-byte vectors: generic path
+    wl = inputs.by_name("mbv2_dw_s1_f16").with_(G=3)
+    assert gc.grouped_conv_select(gc.problem_of(wl), B.GCONV_F16) == B.KERNEL_DIRECT_GENERIC
+
+
+def test_epilogue_entry_validates():
+    with pytest.raises(gc.GconvError) as e:
+        gc.gconv_epilogue_apply(None, None, 16, 4, 4, B.GCONV_F16, None)
+    assert e.value.status == B.GCONV_ERR_INVALID_ARG
+    with pytest.raises(gc.GconvError):
+        gc.gconv_epilogue_apply(16, None, 32, 4, 0, B.GCONV_F16, None)

@@ -1,0 +1,162 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+* every workload family at reduced batch, compared on every output;
+* every workload at its full benchmark size in the launch configuration the
+  benchmark uses, compared on sampled outputs (random + padding borders);
+* random small 2D/3D problems over all dtypes, auto-selected and forced onto
+  each kernel that accepts them;
+* edge cases: ragged tiles, odd sizes, 1x1 filters, channel counts that break
+  16-byte vectors, misaligned input, integer inputs that must be bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import depthwise_convolution_forward_gb300 as gc
+from depthwise_convolution_forward_gb300 import _binding as B
+from depthwise_convolution_forward_gb300 import inputs
+from gpu_util import assert_close, out_shape_of, require_gpu, run_gpu, sample_indices
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _reduced(wl):
+    """Same family, small enough for a full oracle comparison in seconds."""
+    if wl.cfg == 5:
+        return wl.with_(N=2)
+    if wl.cfg in (2, 3):
+        return wl.with_(N=2)
+    return wl.with_(N=min(wl.N, 2))
+
+
+ALL = list(inputs.all_workloads())
+
+
+@pytest.mark.parametrize("wl", ALL, ids=lambda w: w.name)
+def test_reduced_batch_full_compare(orc, wl):
+    r = _reduced(wl)
+    x, w, b = inputs.make_inputs(r)
+    y, sel = run_gpu(r, x, w, b)
+    ref = orc.forward(r, x, w, b)
+    assert_close(y.double().numpy(), ref, r.dtype, f"{r.name} (kernel {sel})")
+
+
+@pytest.mark.parametrize("wl", ALL, ids=lambda w: w.name)
+def test_full_size_sampled(orc, wl):
+    x, w, b = inputs.make_inputs(wl)
+    y, sel = run_gpu(wl, x, w, b)
+    shape = out_shape_of(wl)
+    idx = sample_indices(shape, 4000, seed=wl.variant + 17 * wl.cfg)
+    ref = orc.points(wl, x, w, b, idx)
+    got = y.reshape(-1)[torch.from_numpy(idx)].double().numpy()
+    assert_close(got, ref, wl.dtype, f"{wl.name} (kernel {sel})")
+
+
+def _forced_kernels(wl):
+    ks = [B.KERNEL_DIRECT_GENERIC]
+    if gc.grouped_conv_select(gc.problem_of(wl), gc.DTYPE_CODES[wl.dtype]) != B.KERNEL_DIRECT_GENERIC:
+        ks.append(0)
+    return ks
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_small_problems(orc, seed):
+    rng = np.random.default_rng(1000 + seed)
+    wl = inputs.random_problem(rng)
+    x, w, b = inputs.make_inputs(wl)
+    ref = orc.forward(wl, x, w, b)
+    for k in _forced_kernels(wl):
+        y, sel = run_gpu(wl, x, w, b, force=k)
+        assert_close(y.double().numpy(), ref, wl.dtype, f"seed {seed} kernel {sel} {wl}")
+
+
+DW_EDGE = [
+    # (N, C, H, W, stride, pad, dil, dtype)
+    (1, 8, 7, 7, 1, 1, 1, "f16"),
+    (2, 16, 13, 11, 2, 1, 1, "bf16"),
+    (1, 24, 9, 17, 2, 0, 1, "f16"),
+    (1, 8, 12, 12, 1, 2, 2, "bf16"),
+    (1, 8, 12, 12, 1, 0, 2, "f16"),
+    (2, 16, 15, 15, 2, 2, 2, "bf16"),
+    (1, 4, 10, 9, 1, 1, 1, "f32"),
+    (1, 8, 10, 9, 2, 1, 1, "f32"),
+    (1, 264, 9, 9, 1, 1, 1, "f16"),   # channels above one TMA box: channel tiles
+    (1, 520, 6, 7, 2, 1, 1, "bf16"),  # channel tiles that do not divide C evenly
+    (1, 16, 3, 300, 1, 1, 1, "f16"),  # wide rows: several column tiles
+    (3, 32, 1, 1, 1, 1, 1, "bf16"),   # 1x1 input, padding only
+    (1, 16, 3, 3, 2, 1, 2, "f16"),    # output 1x1, dilated
+]
+
+
+@pytest.mark.parametrize("case", DW_EDGE, ids=lambda c: "-".join(map(str, c)))
+def test_depthwise_edges(orc, case):
+    N, C, H, W, s, p, d, dt = case
+    wl = inputs.Workload("dw_edge", 7, DW_EDGE.index(case), 2, N, C, 1, 1, (1, H, W), (1, 3, 3),
+                         (1, s, s), (0, p, p), (1, d, d), dt, True)
+    x, w, b = inputs.make_inputs(wl)
+    y, sel = run_gpu(wl, x, w, b, force=B.KERNEL_DIRECT_DW)
+    assert sel == B.KERNEL_DIRECT_DW
+    assert_close(y.double().numpy(), orc.forward(wl, x, w, b), dt, str(case))
+
+
+def test_depthwise_3d(orc):
+    wl = inputs.Workload("dw3d", 7, 1, 3, 2, 16, 1, 1, (5, 9, 10), (3, 3, 3), (2, 1, 1), (1, 1, 1),
+                         (1, 1, 1), "f16", True)
+    x, w, b = inputs.make_inputs(wl)
+    y, sel = run_gpu(wl, x, w, b, force=B.KERNEL_DIRECT_DW)
+    assert_close(y.double().numpy(), orc.forward(wl, x, w, b), "f16", "dw3d")
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+def test_integer_inputs_bit_exact(orc, dt):
+    """Small integers: every product and partial sum is exact in fp32 and the
+    result is representable, so GPU and oracle must agree exactly."""
+    for wl in (inputs.Workload("int_dw", 8, 0, 2, 2, 32, 1, 1, (1, 11, 10), (1, 3, 3), (1, 1, 1),
+                               (0, 1, 1), (1, 1, 1), dt, True),
+               inputs.Workload("int_grp", 8, 1, 2, 1, 4, 3, 5, (1, 7, 6), (1, 3, 3), (1, 2, 1),
+                               (0, 1, 1), (1, 1, 2), dt, True)):
+        g = torch.Generator().manual_seed(3)
+        tdt = inputs.DTYPES[dt]
+        x = torch.randint(-3, 4, wl.x_shape(), generator=g).to(tdt)
+        w = torch.randint(-2, 3, wl.w_shape(), generator=g).to(tdt)
+        b = torch.randint(-4, 5, (wl.K,), generator=g).to(tdt)
+        ref = orc.forward(wl, x, w, b)
+        for k in _forced_kernels(wl):
+            y, _ = run_gpu(wl, x, w, b, force=k)
+            assert np.array_equal(y.double().numpy(), ref), (wl.name, k)
+
+
+def test_misaligned_input_falls_back(orc):
+    wl = inputs.Workload("dw_mis", 7, 9, 2, 1, 16, 1, 1, (1, 8, 8), (1, 3, 3), (1, 1, 1), (0, 1, 1),
+                         (1, 1, 1), "f16", True)
+    x, w, b = inputs.make_inputs(wl)
+    y, sel = run_gpu(wl, x, w, b, x_offset=1)
+    assert sel == B.KERNEL_DIRECT_GENERIC
+    assert_close(y.double().numpy(), orc.forward(wl, x, w, b), "f16", "misaligned")
+    with pytest.raises(gc.GconvError) as e:
+        run_gpu(wl, x, w, b, x_offset=1, force=B.KERNEL_DIRECT_DW)
+    assert e.value.status == B.GCONV_ERR_UNSUPPORTED
+
+
+def test_no_bias_and_groups_one(orc):
+    for wl in (inputs.by_name("mbv2_dw_s1_f16").with_(N=1, bias=False),
+               inputs.Workload("g1", 8, 2, 2, 1, 1, 12, 10, (1, 9, 9), (1, 3, 3), (1, 1, 1), (0, 1, 1),
+                               (1, 1, 1), "bf16", False)):
+        x, w, b = inputs.make_inputs(wl)
+        y, _ = run_gpu(wl, x, w, None)
+        assert_close(y.double().numpy(), orc.forward(wl, x, w, None), wl.dtype, wl.name)
+
+
+def test_repeat_calls_and_streams(orc):
+    wl = inputs.by_name("mbv2_dw_s2_f16").with_(N=2)
+    x, w, b = inputs.make_inputs(wl)
+    ref = orc.forward(wl, x, w, b)
+    s = torch.cuda.Stream()
+    for i in range(3):
+        y, _ = run_gpu(wl, x, w, b, stream=s if i % 2 else None, debug=False)
+        assert_close(y.double().numpy(), ref, wl.dtype, f"call {i}")

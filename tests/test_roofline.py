@@ -1,0 +1,32 @@
+"""The benchmark's work and traffic formulas against the numbers the TileOps
+review prints for its 3D grouped case (tests/golden/resnext3d_n1_counts.json)."""
+import json
+import os
+
+import depthwise_convolution_forward_gb300 as gc
+from depthwise_convolution_forward_gb300 import build, inputs, roofline
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "resnext3d_n1_counts.json")
+
+
+def test_printed_3d_counts():
+    build.build()
+    g = json.load(open(GOLDEN))["printed"]
+    wl = inputs.by_name("resnext3d_n1_f16")
+    out = gc.grouped_conv_out_shape(gc.problem_of(wl))
+    assert roofline.outputs(wl, out) == g["output_elements"]
+    assert wl.Cg * wl.taps == g["macs_per_output"]
+    assert round(roofline.flops(wl, out) / 1e6, 1) == g["mflop_approx"]
+    tb = roofline.tensor_bytes(wl, out)
+    assert round(tb["x"] / 1e6, 1) == g["input_mb_approx"]
+    assert round(tb["y"] / 1e6, 1) == g["output_mb_approx"]
+    assert round(tb["w"] / 1e3) == g["weight_kb_approx"]
+    assert round((tb["x"] + tb["y"] + tb["w"]) / 1e6, 1) == g["io_mb_approx"]
+
+
+def test_flops_scale_with_per_group_channels():
+    wl = inputs.by_name("sweep_g8_d1_s1_bf16")
+    out = gc.grouped_conv_out_shape(gc.problem_of(wl))
+    f8 = roofline.flops(wl, out)
+    f512 = roofline.flops(inputs.by_name("sweep_g512_d1_s1_bf16"), out)
+    assert f8 == 64 * f512
