@@ -59,7 +59,7 @@ def parse():
                     help="a bench set (%s) or comma-separated workload names" % ", ".join(BENCH_SETS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--tile", default="", help="tuning override TH,TW,WB,stages")
+    ap.add_argument("--tile", default="", help="tuning override TH,TW,WB,stages,ctas_per_sm,fma_form")
     ap.add_argument("--force-kernel", type=int, default=0)
     return ap.parse_args()
 
@@ -355,7 +355,7 @@ def run_ours(args, wls, set_name, rank, world):
 
     opt = B.gconv_options()
     opt.force_kernel = args.force_kernel
-    for i, t in enumerate(tile[:4]):
+    for i, t in enumerate(tile[:8]):
         opt.tile[i] = t
     optp = ctypes.byref(opt)
 

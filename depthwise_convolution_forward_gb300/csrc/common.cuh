@@ -33,12 +33,65 @@ template <> struct Elem<__nv_bfloat16> {
   __device__ __forceinline__ static __nv_bfloat16 from_f32(float v) { return __float2bfloat16_rn(v); }
 };
 
-// Unpack one 16-byte vector into fp32 values.
+// Widen the two 16-bit (or one 32-bit) values packed in a 32-bit word.
+// Bit operations on whole words keep the compiler from splitting the
+// 128-bit load that produced them into narrow loads.
+template <typename T>
+__device__ __forceinline__ void widen_word(uint32_t w, float* out);
+template <>
+__device__ __forceinline__ void widen_word<float>(uint32_t w, float* out) {
+  out[0] = __uint_as_float(w);
+}
+template <>
+__device__ __forceinline__ void widen_word<__half>(uint32_t w, float* out) {
+  out[0] = __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+  out[1] = __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+}
+template <>
+__device__ __forceinline__ void widen_word<__nv_bfloat16>(uint32_t w, float* out) {
+  out[0] = __uint_as_float(w << 16);
+  out[1] = __uint_as_float(w & 0xffff0000u);
+}
+
+// Unpack one 16-byte vector (as four words) into fp32 values.
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint32_t (&v)[4], float* out) {
+  constexpr int per = 4 / sizeof(T) > 0 ? (int)(4 / sizeof(T)) : 1;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) widen_word<T>(v[i], out + i * per);
+}
 template <typename T>
 __device__ __forceinline__ void unpack16(const uint4& v, float* out) {
-  const T* e = reinterpret_cast<const T*>(&v);
-#pragma unroll
-  for (int i = 0; i < Elem<T>::kVec; ++i) out[i] = Elem<T>::to_f32(e[i]);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  unpack16<T>(w, out);
+}
+
+// 128-bit shared-memory load (always one LDS.128).
+__device__ __forceinline__ void lds128(const void* p, uint32_t (&v)[4]) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+}
+
+// acc += lo/hi half of x * lo/hi half of w, product and sum in fp32 with a
+// single rounding (PTX mixed-precision fma, sm_100+).
+template <typename T>
+__device__ __forceinline__ void fma_mixed_pair(uint32_t x, uint32_t w, float& acc_lo, float& acc_hi);
+template <>
+__device__ __forceinline__ void fma_mixed_pair<__half>(uint32_t x, uint32_t w, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\tmov.b32 {wl, wh}, %3;\n\t"
+      "fma.rn.f32.f16 %0, xl, wl, %0;\n\tfma.rn.f32.f16 %1, xh, wh, %1;\n\t}"
+      : "+f"(lo), "+f"(hi)
+      : "r"(x), "r"(w));
+}
+template <>
+__device__ __forceinline__ void fma_mixed_pair<__nv_bfloat16>(uint32_t x, uint32_t w, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\tmov.b32 {wl, wh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, xl, wl, %0;\n\tfma.rn.f32.bf16 %1, xh, wh, %1;\n\t}"
+      : "+f"(lo), "+f"(hi)
+      : "r"(x), "r"(w));
 }
 
 // ---------------------------------------------------------------------------

@@ -12,7 +12,8 @@ namespace gconv {
 namespace dw {
 
 struct Plan {
-  int TH, TW, TC, WB, stages;
+  int TH, TW, TC, WB, stages, ctas_per_sm, mode;
+  int direct;  // 1: direct-load variant (dw_ldg_kernel), 0: TMA-staged pipeline
   int Dh, Hh, Wh;
   int tiles_c, tiles_w, tiles_h;
   int64_t num_tiles;
@@ -22,6 +23,8 @@ struct Plan {
 
 constexpr int kDwK = 3;  // compiled filter extent (Y == X == 3)
 constexpr uint32_t kStageBudget = 48 * 1024;
+constexpr int kDwModeDefault16 = kMixedFma;    // 16-bit storage
+constexpr int kDwModeDefault32 = kWidenFfma2;  // fp32 storage
 
 inline int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -37,6 +40,7 @@ inline int pick_tc(int C, int vec) {
 
 inline bool make_plan(const Geometry& g, int es, const int* tile_override, int num_sms, Plan* out) {
   const int vec = 16 / es;
+  const int direct = (tile_override && tile_override[6] == 2) ? 1 : 0;
   const int S = g.sH, DL = g.dH;
   Plan best{};
   double best_cost = 1e30;
@@ -56,8 +60,8 @@ inline bool make_plan(const Geometry& g, int es, const int* tile_override, int n
         if (Hh > 256) break;
         const uint32_t bytes = (uint32_t)Dh * Hh * Wh * TC * es;
         const int items = NV * (TW / WB) * TH;
-        if (items > (WB == 8 ? 256 : 512)) break;
-        if (bytes > kStageBudget && !(tile_override && tile_override[0])) break;
+        if (items > (direct ? 256 : (WB >= 8 ? 256 : 480))) break;
+        if (!direct && bytes > kStageBudget && !(tile_override && tile_override[0])) break;
         const int tiles_w = ceil_div(g.Wo, TW), tiles_h = ceil_div(g.Ho, TH);
         const int tiles_c = ceil_div(g.C(), TC);
         const int64_t tiles = (int64_t)tiles_c * tiles_w * tiles_h * g.Do * g.N;
@@ -78,18 +82,37 @@ inline bool make_plan(const Geometry& g, int es, const int* tile_override, int n
           best.tiles_c = tiles_c, best.tiles_w = tiles_w, best.tiles_h = tiles_h;
           best.num_tiles = tiles;
           best.stage_bytes = bytes;
-          best.threads = std::min(512, (items + 31) / 32 * 32);
+          best.threads = (direct ? 0 : 32) + (items + 31) / 32 * 32;  // (producer warp) + consumers
         }
       }
     }
   }
   if (best_cost >= 1e30) return false;
+  best.direct = direct;
   best.stage_stride = align_up(best.stage_bytes, 1024);
-  best.stage_off = align_up(fixed_smem_bytes<kDwK>(g.Z, best.TC), 1024);
-  int stages = (tile_override && tile_override[3]) ? tile_override[3] : 4;
-  while (stages > 2 && best.stage_off + stages * best.stage_stride > 200 * 1024) --stages;
+  // FMA form: override 1 = widen + fp32 FMA, 2 = mixed f16/bf16, 3 = widen + fp32x2
+  const int ov_mode = tile_override ? tile_override[5] : 0;
+  int mode = es == 2 ? kDwModeDefault16 : kDwModeDefault32;
+  if (ov_mode >= 1 && ov_mode <= 3) mode = ov_mode - 1;
+  if (mode == kMixedFma && es != 2) mode = kWidenFfma;
+  best.mode = mode;
+  best.stage_off = align_up(fixed_smem_bytes<kDwK>(g.Z, g.C(), es, mode), 1024);
+  // Prefer two CTAs per SM (two independent copy/compute streams) with two
+  // stages each; fall back to one CTA with up to four stages.
+  const int ov_stages = tile_override ? tile_override[3] : 0;
+  const int ov_ctas = tile_override ? tile_override[4] : 0;
+  const uint32_t half_sm = 113 * 1024, full_sm = 220 * 1024;
+  int ctas = ov_ctas ? ov_ctas : (best.stage_off + 2 * best.stage_stride <= half_sm ? 2 : 1);
+  int stages = ov_stages ? std::min(ov_stages, kDwMaxStages) : (ctas == 2 ? 2 : kDwMaxStages);
+  const uint32_t cap = ctas == 2 ? half_sm : full_sm;
+  while (!ov_stages && stages > 2 && best.stage_off + stages * best.stage_stride > cap) --stages;
   best.stages = stages;
+  best.ctas_per_sm = ctas;
   best.smem_bytes = best.stage_off + stages * best.stage_stride;
+  if (direct) {
+    best.stages = 0;
+    best.smem_bytes = weight_smem_bytes(g.Z * kDwK * kDwK, best.TC, es, mode) + 4u * (uint32_t)best.TC;
+  }
   *out = best;
   return true;
 }
@@ -101,15 +124,55 @@ inline CUtensorMapDataType tma_type() {
   return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 }
 
-template <typename T, int S, int DL, int WB>
-cudaError_t launch_variant(const CUtensorMap& map, const DwArgs& a, const Plan& p, int grid,
-                           cudaStream_t stream, int device) {
-  static SmemAttr attr;
-  auto kern = dw_kernel<T, kDwK, S, DL, WB>;
-  cudaError_t e = attr.ensure(kern, device, (int)p.smem_bytes);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, p.threads, p.smem_bytes, stream>>>(map, a);
-  return cudaGetLastError();
+template <typename T>
+using DwKernel = void (*)(const CUtensorMap, const DwArgs);
+
+// The compiled variant for (stride, dilation, register block, FMA form).
+template <typename T>
+DwKernel<T> pick_kernel(int S, int DL, int WB, int mode) {
+#define GCONV_DW_CASE(s_, d_, wb_)                                               \
+  if (S == s_ && DL == d_ && WB == wb_) {                                        \
+    if constexpr (sizeof(T) == 2) {                                              \
+      if (mode == kMixedFma) return dw_kernel<T, kDwK, s_, d_, wb_, kMixedFma>;  \
+    }                                                                            \
+    if (mode == kWidenFfma2) return dw_kernel<T, kDwK, s_, d_, wb_, kWidenFfma2>; \
+    return dw_kernel<T, kDwK, s_, d_, wb_, kWidenFfma>;                          \
+  }
+  GCONV_DW_CASE(1, 1, 4)
+  GCONV_DW_CASE(1, 1, 8)
+  GCONV_DW_CASE(2, 1, 4)
+  GCONV_DW_CASE(2, 1, 8)
+  GCONV_DW_CASE(1, 2, 4)
+  GCONV_DW_CASE(1, 2, 8)
+  GCONV_DW_CASE(2, 2, 4)
+  GCONV_DW_CASE(2, 2, 8)
+#undef GCONV_DW_CASE
+  return nullptr;
+}
+
+template <typename T>
+using DwLdgKernel = void (*)(const DwArgs);
+
+template <typename T>
+DwLdgKernel<T> pick_ldg_kernel(int S, int DL, int WB, int mode) {
+#define GCONV_DW_CASE(s_, d_, wb_)                                                   \
+  if (S == s_ && DL == d_ && WB == wb_) {                                            \
+    if constexpr (sizeof(T) == 2) {                                                  \
+      if (mode == kMixedFma) return dw_ldg_kernel<T, kDwK, s_, d_, wb_, kMixedFma>;  \
+    }                                                                                \
+    if (mode == kWidenFfma2) return dw_ldg_kernel<T, kDwK, s_, d_, wb_, kWidenFfma2>; \
+    return dw_ldg_kernel<T, kDwK, s_, d_, wb_, kWidenFfma>;                          \
+  }
+  GCONV_DW_CASE(1, 1, 4)
+  GCONV_DW_CASE(1, 1, 8)
+  GCONV_DW_CASE(2, 1, 4)
+  GCONV_DW_CASE(2, 1, 8)
+  GCONV_DW_CASE(1, 2, 4)
+  GCONV_DW_CASE(1, 2, 8)
+  GCONV_DW_CASE(2, 2, 4)
+  GCONV_DW_CASE(2, 2, 8)
+#undef GCONV_DW_CASE
+  return nullptr;
 }
 
 template <typename T>
@@ -117,20 +180,54 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   const int es = sizeof(T);
   struct Key {
     Geometry g;
-    int tile[4];
+    int tile[8];
     int num_sms;
+    int device;
   } key;
   std::memset(&key, 0, sizeof(key));
   key.g = g;
   std::memcpy(key.tile, la.tile, sizeof(key.tile));
   key.num_sms = dev.num_sms;
+  key.device = dev.device;
   static PlanCache<Plan> cache;
   Plan p;
+  static SmemAttr attr[2][2][2][3];  // [S-1][DL-1][WB==8][mode]
   if (!cache.get(key, &p)) {
     if (!make_plan(g, es, la.tile, dev.num_sms, &p)) return cudaErrorNotSupported;
+    if (p.direct) {
+      if (pick_ldg_kernel<T>(g.sH, g.dH, p.WB, p.mode) == nullptr) return cudaErrorNotSupported;
+    } else {
+      DwKernel<T> k = pick_kernel<T>(g.sH, g.dH, p.WB, p.mode);
+      if (k == nullptr || p.smem_bytes > (uint32_t)dev.max_smem_optin) return cudaErrorNotSupported;
+      cudaError_t e = attr[g.sH - 1][g.dH - 1][p.WB == 8][p.mode].ensure(k, dev.device, (int)p.smem_bytes);
+      if (e != cudaSuccess) return e;
+      int occ = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, p.threads, p.smem_bytes);
+      if (e != cudaSuccess) return e;
+      if (occ < 1) return cudaErrorNotSupported;
+      p.ctas_per_sm = std::min(occ, p.ctas_per_sm);
+    }
     cache.put(key, p);
   }
-  if (p.smem_bytes > (uint32_t)dev.max_smem_optin) return cudaErrorNotSupported;
+  if (p.direct) {
+    DwArgs a{};
+    a.x = la.x;
+    a.D = g.D, a.H = g.H, a.W = g.W;
+    a.w = la.w;
+    a.bias = la.bias;
+    a.y = la.y;
+    a.C = g.C();
+    a.Do = g.Do, a.Ho = g.Ho, a.Wo = g.Wo;
+    a.Z = g.Z, a.dD = g.dD, a.sD = g.sD, a.pD = g.pD, a.pH = g.pH, a.pW = g.pW;
+    a.TH = p.TH, a.TW = p.TW, a.TC = p.TC;
+    a.tiles_c = p.tiles_c, a.tiles_w = p.tiles_w, a.tiles_h = p.tiles_h;
+    a.num_tiles = p.num_tiles;
+    a.status = la.status;
+    a.wait_limit_ns = la.wait_limit_ns;
+    DwLdgKernel<T> k = pick_ldg_kernel<T>(g.sH, g.dH, p.WB, p.mode);
+    k<<<(unsigned)p.num_tiles, p.threads, p.smem_bytes, la.stream>>>(a);
+    return cudaGetLastError();
+  }
 
   // x viewed as a 5-D tensor (C, W, H, D, N), innermost first.
   CUtensorMap map;
@@ -142,7 +239,9 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   if (encode_tiled(&map, tma_type<T>(), 5, la.x, dims, strides, box, estr) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
-  DwArgs a;
+  DwArgs a{};
+  a.x = la.x;
+  a.D = g.D, a.H = g.H, a.W = g.W;
   a.w = la.w;
   a.bias = la.bias;
   a.y = la.y;
@@ -161,22 +260,11 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   a.wait_limit_ns = la.wait_limit_ns;
   a.test_flags = la.test_flags;
 
-  const int64_t grid64 = std::min<int64_t>(p.num_tiles, (int64_t)dev.num_sms);
+  const int64_t grid64 = std::min<int64_t>(p.num_tiles, (int64_t)dev.num_sms * p.ctas_per_sm);
   const int grid = (int)std::max<int64_t>(1, grid64);
-  const int S = g.sH, DL = g.dH;
-#define GCONV_DW_CASE(s_, d_, wb_)                            \
-  if (S == s_ && DL == d_ && p.WB == wb_)                     \
-    return launch_variant<T, s_, d_, wb_>(map, a, p, grid, la.stream, dev.device);
-  GCONV_DW_CASE(1, 1, 4)
-  GCONV_DW_CASE(1, 1, 8)
-  GCONV_DW_CASE(2, 1, 4)
-  GCONV_DW_CASE(2, 1, 8)
-  GCONV_DW_CASE(1, 2, 4)
-  GCONV_DW_CASE(1, 2, 8)
-  GCONV_DW_CASE(2, 2, 4)
-  GCONV_DW_CASE(2, 2, 8)
-#undef GCONV_DW_CASE
-  return cudaErrorNotSupported;
+  DwKernel<T> kern = pick_kernel<T>(g.sH, g.dH, p.WB, p.mode);
+  kern<<<grid, p.threads, p.smem_bytes, la.stream>>>(map, a);
+  return cudaGetLastError();
 }
 
 }  // namespace dw

@@ -41,7 +41,7 @@ struct LaunchArgs {
   int* status;  // device status word [code, where]
   uint64_t wait_limit_ns;
   int test_flags;
-  int tile[4];  // tuning overrides, 0 = automatic
+  int tile[8];  // tuning overrides, 0 = automatic
 };
 
 // Device properties needed by the launchers (cached per device by api.cu).

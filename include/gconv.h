@@ -92,7 +92,10 @@ typedef struct gconv_options {
   int32_t test_flags;    /* bit 0: withhold the first input copy of CTA 0 so its
                             first wait cannot complete (timeout-path test)       */
   int32_t selected;      /* out: the gconv_kernel that was launched               */
-  int32_t tile[4];       /* tile overrides for tuning, 0 = automatic              */
+  int32_t tile[8];       /* tuning overrides, 0 = automatic; for the depthwise
+                            kernel: TH, TW, WB, stages, CTAs per SM, FMA form
+                            (1 = widen + fp32 FMA, 2 = mixed f16/bf16 FMA,
+                            3 = widen + packed fp32x2 FMA) */
 } gconv_options;
 
 /*

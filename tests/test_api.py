@@ -42,7 +42,7 @@ def test_struct_layout():
     assert ctypes.sizeof(B.gconv_problem) == 88
     assert B.gconv_problem.N.offset == 8
     assert B.gconv_problem.dil.offset == 76
-    assert ctypes.sizeof(B.gconv_options) == 40
+    assert ctypes.sizeof(B.gconv_options) == 56
 
 
 def good(**kw):
