@@ -1,10 +1,254 @@
-// Kb: tcgen05 / TMEM grouped implicit GEMM (placeholder until implemented).
+// Kb host side: support check, tile planning, tensor-map encoding, launch.
+#include <algorithm>
+#include <cstring>
+
 #include "kernels.h"
+#include "plan_cache.h"
+#include "tc_impl.cuh"
 
 namespace gconv {
+namespace {
 
-bool tc_supported(const Geometry&, DType, const LaunchArgs*) { return false; }
+using tc::TcArgs;
 
-cudaError_t tc_launch(const Geometry&, const LaunchArgs&, const DeviceInfo&) { return cudaErrorNotSupported; }
+inline int mod_pos(int v, int m) { return ((v % m) + m) % m; }
+inline uint32_t round_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+// Smallest merge factor m (groups per MMA) with K = m*Cg and N = m*Kg both
+// multiples of 16 (tcgen05 kind::f16 with M = 128 wants N % 16 == 0 and each
+// MMA consumes K = 16), or 0 if none within 16 groups.
+int merge_factor(const Geometry& g) {
+  for (int m = 1; m <= 16; ++m) {
+    if (g.G % m) continue;
+    if ((m * g.Cg) % 16 == 0 && (m * g.Kg) % 16 == 0 && m * g.Kg <= 256 && m * g.Cg <= 256) return m;
+  }
+  return 0;
+}
+
+struct TcPlan {
+  TcArgs a;  // everything except pointers / status
+  uint32_t smem_bytes;
+  int grid;
+  bool ok;
+};
+
+bool make_tc_plan(const Geometry& g, bool bf16, int num_sms, int max_smem, const int* ov, TcPlan* out) {
+  TcArgs a;
+  std::memset(&a, 0, sizeof(a));
+  const int m = merge_factor(g);
+  if (m == 0) return false;
+  if (g.sH != g.sW || g.sH < 1 || g.sH > 2) return false;
+  const int taps = g.taps();
+  if (taps > tc::kMaxTaps) return false;
+  a.G = g.G, a.Cg = g.Cg, a.Kg = g.Kg, a.m = m;
+  a.Do = g.Do, a.Ho = g.Ho, a.Wo = g.Wo, a.Ktot = g.K();
+  a.sD = g.sD, a.pD = g.pD, a.taps_total = taps;
+  a.s = g.sH;
+  a.Kt = m * g.Cg, a.Nn = m * g.Kg, a.KS = a.Kt / 16, a.nchunks = a.Kt / 8;
+  a.n_gc = g.G / m;
+  a.ntaps = taps;
+  a.Dh = (g.Z - 1) * g.dD + 1;
+  // Phase decomposition: input row of tap ky for output row oh is
+  // s*(oh + qy) + py with py in [0, s).
+  int qy[16], py[16], qx[16], px[16];
+  if (g.Y > 16 || g.X > 16) return false;
+  int qy_min = 1 << 30, qy_max = -(1 << 30), qx_min = 1 << 30, qx_max = -(1 << 30);
+  for (int ky = 0; ky < g.Y; ++ky) {
+    const int v = ky * g.dH - g.pH;
+    py[ky] = mod_pos(v, a.s);
+    qy[ky] = (v - py[ky]) / a.s;
+    qy_min = std::min(qy_min, qy[ky]);
+    qy_max = std::max(qy_max, qy[ky]);
+  }
+  for (int kx = 0; kx < g.X; ++kx) {
+    const int v = kx * g.dW - g.pW;
+    px[kx] = mod_pos(v, a.s);
+    qx[kx] = (v - px[kx]) / a.s;
+    qx_min = std::min(qx_min, qx[kx]);
+    qx_max = std::max(qx_max, qx[kx]);
+  }
+  a.qy_min = qy_min, a.qx_min = qx_min;
+  // used phases
+  int phase_of[4];
+  a.nphase = 0;
+  for (int p = 0; p < 4; ++p) phase_of[p] = -1;
+  for (int ky = 0; ky < g.Y; ++ky)
+    for (int kx = 0; kx < g.X; ++kx) {
+      const int p = py[ky] * 2 + px[kx];
+      if (phase_of[p] < 0) {
+        phase_of[p] = a.nphase;
+        a.phase_py[a.nphase] = py[ky];
+        a.phase_px[a.nphase] = px[kx];
+        ++a.nphase;
+      }
+    }
+  const int range_x = qx_max - qx_min, range_y = qy_max - qy_min;
+  const uint32_t budget = (uint32_t)std::min(max_smem, 227 * 1024);
+  // Tile shape: full output rows when they fit, TH rows so the flattened
+  // M = TH * pitch fills nmt MMAs of 128 rows.  Every candidate nmt is
+  // planned completely; the cheapest one that fits shared and tensor memory
+  // wins (cost = MMA rows issued + a per-tile overhead).
+  const int tw_cap = std::min(256 / a.s, 128 * 4) - range_x;
+  if (tw_cap < 1) return false;
+  double best = 1e30;
+  TcPlan bestp;
+  std::memset(&bestp, 0, sizeof(bestp));
+  for (int nmt = 1; nmt <= 4; ++nmt) {
+    if (ov && ov[2] && ov[2] != nmt) continue;
+    TcArgs c = a;
+    const int TWo = std::min(g.Wo, std::min(tw_cap, 128 * nmt - range_x));
+    if (TWo < 1) continue;
+    const int P = TWo + range_x;
+    int TH = std::min(g.Ho, (128 * nmt) / P);
+    if (ov && ov[0]) TH = std::min(ov[0], (128 * nmt) / P);
+    if (TH < 1) continue;
+    if (a.s * (TH + range_y) > 256) continue;
+    c.TH = TH, c.TWo = TWo, c.nmt = nmt, c.P = P, c.Hh = TH + range_y;
+    c.tiles_w = (g.Wo + TWo - 1) / TWo;
+    c.tiles_h = (g.Ho + TH - 1) / TH;
+    const double sp = (double)g.N * g.Do * c.tiles_h * c.tiles_w;
+    if (sp >= 2e9) continue;
+    c.spatial_tiles = (int)sp;
+    int max_off = 0;
+    for (int z = 0; z < g.Z; ++z)
+      for (int ky = 0; ky < g.Y; ++ky)
+        for (int kx = 0; kx < g.X; ++kx) {
+          const int t = (z * g.Y + ky) * g.X + kx;
+          c.tap_phase[t] = phase_of[py[ky] * 2 + px[kx]];
+          c.tap_off[t] = z * g.dD * c.Hh * c.P + (qy[ky] - qy_min) * c.P + (qx[kx] - qx_min);
+          max_off = std::max(max_off, c.tap_off[t]);
+        }
+    const uint32_t plane_px = round_up((uint32_t)std::max(c.Dh * c.Hh * c.P, c.nmt * 128 + max_off), 8);
+    c.plane_stride = plane_px * 16u;
+    c.a_stage_bytes = round_up((uint32_t)(c.nphase * c.nchunks) * c.plane_stride, 1024);
+    c.tx_bytes = (uint32_t)(c.nphase * c.nchunks) * (uint32_t)(c.Dh * c.Hh * c.P) * 16u;
+    const uint32_t b_bytes = round_up((uint32_t)(taps * c.Kt * c.Nn * 2), 1024);
+    c.bias_off = 1024;
+    c.b_off = c.bias_off + round_up((uint32_t)c.Nn * 4u, 1024);
+    c.a_off = c.b_off + b_bytes;
+    int stages = (ov && ov[3]) ? ov[3] : tc::kMaxStages;
+    stages = std::min(stages, tc::kMaxStages);
+    while (stages > 2 && c.a_off + stages * c.a_stage_bytes > budget) --stages;
+    if (c.a_off + stages * c.a_stage_bytes > budget) continue;
+    c.stages = stages;
+    uint32_t cols = 32;
+    while (cols < (uint32_t)(2 * c.nmt * c.Nn)) cols <<= 1;
+    if (cols > 512) continue;
+    c.tmem_cols = cols;
+    c.idesc = tc::idesc_f16(bf16, 128, c.Nn);
+    // A CTA keeps one group chunk (its weights stay resident); the chunk's
+    // spatial tiles are dealt round-robin to cpg CTAs.
+    c.cpg = std::max(1, num_sms / c.n_gc);
+    TcPlan p;
+    p.a = c;
+    p.smem_bytes = c.a_off + stages * c.a_stage_bytes;
+    // Keep a second CTA off the SM when both could not hold their tensor
+    // memory at once (its allocation would wait for the first CTA to exit).
+    if (cols > 256) p.smem_bytes = std::max<uint32_t>(p.smem_bytes, 117 * 1024);
+    if (ov && ov[7] > 0) p.smem_bytes += (uint32_t)ov[7] * 1024u;  // allocation padding (layout checks)
+    if (p.smem_bytes > budget) continue;
+    p.grid = c.n_gc * c.cpg;
+    p.ok = true;
+    const double cost = (double)c.tiles_h * c.tiles_w * (nmt * 128 + 96);
+    if (cost < best) best = cost, bestp = p;
+  }
+  if (best >= 1e30) return false;
+  *out = bestp;
+  return true;
+}
+
+template <typename T>
+cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const DeviceInfo& dev) {
+  struct Key {
+    Geometry g;
+    int tile[8];
+    int num_sms, device, bf16;
+  } key;
+  std::memset(&key, 0, sizeof(key));
+  key.g = g;
+  std::memcpy(key.tile, la.tile, sizeof(key.tile));
+  key.num_sms = dev.num_sms;
+  key.device = dev.device;
+  key.bf16 = std::is_same<T, __nv_bfloat16>::value;
+  static PlanCache<TcPlan> cache;
+  static SmemAttr attr;
+  TcPlan p;
+  if (!cache.get(key, &p)) {
+    if (!make_tc_plan(g, key.bf16, dev.num_sms, dev.max_smem_optin, la.tile, &p)) return cudaErrorNotSupported;
+    cudaError_t e = attr.ensure(tc::tc_kernel<T>, dev.device, (int)p.smem_bytes);
+    if (e != cudaSuccess) return e;
+    // Co-resident CTAs must never need more than the SM's 512 TMEM columns,
+    // or an allocation would wait for another CTA to exit.  Raise the
+    // shared-memory request until occupancy x columns fits.
+    for (int guard = 0; guard < 64; ++guard) {
+      int occ = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, tc::tc_kernel<T>, tc::kThreads, p.smem_bytes);
+      if (e != cudaSuccess) return e;
+      if (occ < 1) return cudaErrorNotSupported;
+      if ((uint32_t)occ * p.a.tmem_cols <= 512u) break;
+      p.smem_bytes += 8 * 1024;
+      if (p.smem_bytes > (uint32_t)dev.max_smem_optin) return cudaErrorNotSupported;
+      e = attr.ensure(tc::tc_kernel<T>, dev.device, (int)p.smem_bytes);
+      if (e != cudaSuccess) return e;
+    }
+    cache.put(key, p);
+  }
+  const int es = (int)sizeof(T);
+  const uint64_t C = g.C();
+  CUtensorMap map;
+  uint64_t dims[5] = {C, (uint64_t)g.W, (uint64_t)g.H, (uint64_t)g.D, (uint64_t)g.N};
+  uint64_t strides[4] = {C * es, C * es * g.W, C * es * g.W * g.H, C * es * g.W * g.H * g.D};
+  const int s = p.a.s;
+  uint32_t box[5] = {8u, (uint32_t)(s * p.a.P), (uint32_t)(s * p.a.Hh), (uint32_t)p.a.Dh, 1u};
+  uint32_t estr[5] = {1u, (uint32_t)s, (uint32_t)s, 1u, 1u};
+  CUtensorMapDataType tt = std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                          : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (encode_tiled(&map, tt, 5, la.x, dims, strides, box, estr) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  TcArgs a = p.a;
+  a.w = la.w;
+  a.bias = la.bias;
+  a.y = la.y;
+  a.status = la.status;
+  a.wait_limit_ns = la.wait_limit_ns;
+  a.test_flags = la.test_flags;
+  tc::tc_kernel<T><<<p.grid, tc::kThreads, p.smem_bytes, la.stream>>>(map, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(const Geometry& g, DType dt, const LaunchArgs* a) {
+  if (dt == kF32) return false;  // fp32 stays on FFMA (no TF32 rounding)
+  if (merge_factor(g) == 0) return false;
+  if (g.sH != g.sW || g.sH < 1 || g.sH > 2) return false;
+  if (g.taps() > tc::kMaxTaps || g.Y > 16 || g.X > 16) return false;
+  if (g.C() % 8 || g.K() % 8) return false;
+  if ((g.Z - 1) * g.dD + 1 > 256) return false;
+  if (a) {
+    if ((reinterpret_cast<uintptr_t>(a->x) & 15) || (reinterpret_cast<uintptr_t>(a->y) & 15)) return false;
+  }
+  struct Key {
+    Geometry g;
+    int tile[8];
+    int bf16;
+  } key;
+  std::memset(&key, 0, sizeof(key));
+  key.g = g;
+  if (a) std::memcpy(key.tile, a->tile, sizeof(key.tile));
+  key.bf16 = dt == kBF16;
+  static PlanCache<int> cache;
+  int ok = 0;
+  if (cache.get(key, &ok)) return ok != 0;
+  TcPlan p;
+  ok = make_tc_plan(g, dt == kBF16, 148, 227 * 1024, a ? a->tile : nullptr, &p) ? 1 : 0;
+  cache.put(key, ok);
+  return ok != 0;
+}
+
+cudaError_t tc_launch(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev) {
+  if (a.dt == kF16) return tc_launch_typed<__half>(g, a, dev);
+  if (a.dt == kBF16) return tc_launch_typed<__nv_bfloat16>(g, a, dev);
+  return cudaErrorNotSupported;
+}
 
 }  // namespace gconv
