@@ -153,7 +153,7 @@ gconv_status read_and_clear_status(DevSlot* slot, cudaStream_t stream, int32_t* 
 
 CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, uint32_t rank, const void* base,
                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
-                      const uint32_t* elem_strides) {
+                      const uint32_t* elem_strides, CUtensorMapSwizzle swizzle) {
   std::call_once(g_encode_once, []() {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -164,7 +164,7 @@ CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, uint32_t rank,
   });
   if (g_encode == nullptr) return CUDA_ERROR_NOT_FOUND;
   return g_encode(map, type, rank, const_cast<void*>(base), dims, strides_bytes, box, elem_strides,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 

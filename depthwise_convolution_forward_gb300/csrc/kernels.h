@@ -54,7 +54,7 @@ struct DeviceInfo {
 // Tensor-map encoder (driver entry point resolved once by api.cu).
 CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, uint32_t rank, const void* base,
                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
-                      const uint32_t* elem_strides);
+                      const uint32_t* elem_strides, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE);
 
 // ---- Ka: TMA-staged depthwise direct kernel (Cg == Kg == 1) -------------
 // Returns true when the kernel supports this problem (shape, dtype, alignment).

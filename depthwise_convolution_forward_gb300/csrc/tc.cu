@@ -27,12 +27,14 @@ int merge_factor(const Geometry& g) {
 
 struct TcPlan {
   TcArgs a;  // everything except pointers / status
+  bool sw;   // 128-byte swizzled rows of 64 channels (else 16-byte chunk planes)
   uint32_t smem_bytes;
   int grid;
   bool ok;
 };
 
-bool make_tc_plan(const Geometry& g, bool bf16, int num_sms, int max_smem, const int* ov, TcPlan* out) {
+bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, const int* ov, bool allow_sw,
+                       TcPlan* out) {
   TcArgs a;
   std::memset(&a, 0, sizeof(a));
   const int m = merge_factor(g);
@@ -46,6 +48,11 @@ bool make_tc_plan(const Geometry& g, bool bf16, int num_sms, int max_smem, const
   a.s = g.sH;
   a.Kt = m * g.Cg, a.Nn = m * g.Kg, a.KS = a.Kt / 16, a.nchunks = a.Kt / 8;
   a.n_gc = g.G / m;
+  // 128-byte rows: 64 input channels per pixel cover sc = 64 / Kt group
+  // chunks, read by one TMA box per phase (override 6: 1 = chunk planes).
+  const bool sw = allow_sw && g.C() % 64 == 0 && 64 % a.Kt == 0 && a.n_gc % (64 / a.Kt) == 0 && !(ov && ov[6] == 1);
+  a.sc = sw ? 64 / a.Kt : 1;
+  if (sw) a.nchunks = 1;
   a.ntaps = taps;
   a.Dh = (g.Z - 1) * g.dD + 1;
   // Phase decomposition: input row of tap ky for output row oh is
@@ -119,12 +126,15 @@ bool make_tc_plan(const Geometry& g, bool bf16, int num_sms, int max_smem, const
           max_off = std::max(max_off, c.tap_off[t]);
         }
     const uint32_t plane_px = round_up((uint32_t)std::max(c.Dh * c.Hh * c.P, c.nmt * 128 + max_off), 8);
-    c.plane_stride = plane_px * 16u;
+    const uint32_t row_bytes = sw ? 128u : 16u;
+    c.plane_stride = plane_px * row_bytes;
     c.a_stage_bytes = round_up((uint32_t)(c.nphase * c.nchunks) * c.plane_stride, 1024);
-    c.tx_bytes = (uint32_t)(c.nphase * c.nchunks) * (uint32_t)(c.Dh * c.Hh * c.P) * 16u;
-    const uint32_t b_bytes = round_up((uint32_t)(taps * c.Kt * c.Nn * 2), 1024);
+    c.tx_bytes = (uint32_t)(c.nphase * c.nchunks) * (uint32_t)(c.Dh * c.Hh * c.P) * row_bytes;
+    const uint32_t b_bytes = round_up((uint32_t)(c.sc * taps * c.Kt * c.Nn * 2), 1024);
     c.bias_off = 1024;
-    c.b_off = c.bias_off + round_up((uint32_t)c.Nn * 4u, 1024);
+    c.tab_off = c.bias_off + round_up((uint32_t)(c.sc * c.Nn) * 4u, 16);
+    const uint32_t tab_bytes = (uint32_t)(c.sc * c.nmt * taps * c.KS) * 16u;
+    c.b_off = round_up(c.tab_off + tab_bytes, 1024);
     c.a_off = c.b_off + b_bytes;
     int stages = (ov && ov[3]) ? ov[3] : tc::kMaxStages;
     stages = std::min(stages, tc::kMaxStages);
@@ -132,30 +142,40 @@ bool make_tc_plan(const Geometry& g, bool bf16, int num_sms, int max_smem, const
     if (c.a_off + stages * c.a_stage_bytes > budget) continue;
     c.stages = stages;
     uint32_t cols = 32;
-    while (cols < (uint32_t)(2 * c.nmt * c.Nn)) cols <<= 1;
+    while (cols < (uint32_t)(2 * c.nmt * c.sc * c.Nn)) cols <<= 1;
     if (cols > 512) continue;
     c.tmem_cols = cols;
     c.idesc = tc::idesc_f16(bf16, 128, c.Nn);
     // A CTA keeps one group chunk (its weights stay resident); the chunk's
     // spatial tiles are dealt round-robin to cpg CTAs.
-    c.cpg = std::max(1, num_sms / c.n_gc);
+    const int n_sc = c.n_gc / c.sc;
+    c.cpg = std::max(1, num_sms / n_sc);
     TcPlan p;
     p.a = c;
+    p.sw = sw;
     p.smem_bytes = c.a_off + stages * c.a_stage_bytes;
     // Keep a second CTA off the SM when both could not hold their tensor
     // memory at once (its allocation would wait for the first CTA to exit).
     if (cols > 256) p.smem_bytes = std::max<uint32_t>(p.smem_bytes, 117 * 1024);
     if (ov && ov[7] > 0) p.smem_bytes += (uint32_t)ov[7] * 1024u;  // allocation padding (layout checks)
     if (p.smem_bytes > budget) continue;
-    p.grid = c.n_gc * c.cpg;
+    p.grid = n_sc * c.cpg;
     p.ok = true;
-    const double cost = (double)c.tiles_h * c.tiles_w * (nmt * 128 + 96);
+    const double cost = (double)c.tiles_h * c.tiles_w * (nmt * 128 + 96) / c.cpg;
     if (cost < best) best = cost, bestp = p;
   }
   if (best >= 1e30) return false;
   *out = bestp;
   return true;
 }
+
+bool make_tc_plan(const Geometry& g, bool bf16, int num_sms, int max_smem, const int* ov, TcPlan* out) {
+  return make_tc_plan_mode(g, bf16, num_sms, max_smem, ov, true, out) ||
+         make_tc_plan_mode(g, bf16, num_sms, max_smem, ov, false, out);
+}
+
+template <typename T>
+using TcKernel = void (*)(const CUtensorMap, const TcArgs);
 
 template <typename T>
 cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const DeviceInfo& dev) {
@@ -171,24 +191,25 @@ cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   key.device = dev.device;
   key.bf16 = std::is_same<T, __nv_bfloat16>::value;
   static PlanCache<TcPlan> cache;
-  static SmemAttr attr;
+  static SmemAttr attr[2];
   TcPlan p;
   if (!cache.get(key, &p)) {
     if (!make_tc_plan(g, key.bf16, dev.num_sms, dev.max_smem_optin, la.tile, &p)) return cudaErrorNotSupported;
-    cudaError_t e = attr.ensure(tc::tc_kernel<T>, dev.device, (int)p.smem_bytes);
+    const TcKernel<T> kern = p.sw ? tc::tc_kernel<T, true> : tc::tc_kernel<T, false>;
+    cudaError_t e = attr[p.sw].ensure(kern, dev.device, (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
     // Co-resident CTAs must never need more than the SM's 512 TMEM columns,
     // or an allocation would wait for another CTA to exit.  Raise the
     // shared-memory request until occupancy x columns fits.
     for (int guard = 0; guard < 64; ++guard) {
       int occ = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, tc::tc_kernel<T>, tc::kThreads, p.smem_bytes);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, tc::kThreads, p.smem_bytes);
       if (e != cudaSuccess) return e;
       if (occ < 1) return cudaErrorNotSupported;
       if ((uint32_t)occ * p.a.tmem_cols <= 512u) break;
       p.smem_bytes += 8 * 1024;
       if (p.smem_bytes > (uint32_t)dev.max_smem_optin) return cudaErrorNotSupported;
-      e = attr.ensure(tc::tc_kernel<T>, dev.device, (int)p.smem_bytes);
+      e = attr[p.sw].ensure(kern, dev.device, (int)p.smem_bytes);
       if (e != cudaSuccess) return e;
     }
     cache.put(key, p);
@@ -199,11 +220,13 @@ cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   uint64_t dims[5] = {C, (uint64_t)g.W, (uint64_t)g.H, (uint64_t)g.D, (uint64_t)g.N};
   uint64_t strides[4] = {C * es, C * es * g.W, C * es * g.W * g.H, C * es * g.W * g.H * g.D};
   const int s = p.a.s;
-  uint32_t box[5] = {8u, (uint32_t)(s * p.a.P), (uint32_t)(s * p.a.Hh), (uint32_t)p.a.Dh, 1u};
+  uint32_t box[5] = {p.sw ? 64u : 8u, (uint32_t)(s * p.a.P), (uint32_t)(s * p.a.Hh), (uint32_t)p.a.Dh, 1u};
   uint32_t estr[5] = {1u, (uint32_t)s, (uint32_t)s, 1u, 1u};
   CUtensorMapDataType tt = std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (encode_tiled(&map, tt, 5, la.x, dims, strides, box, estr) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  if (encode_tiled(&map, tt, 5, la.x, dims, strides, box, estr,
+                   p.sw ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   TcArgs a = p.a;
   a.w = la.w;
   a.bias = la.bias;
@@ -211,7 +234,8 @@ cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   a.status = la.status;
   a.wait_limit_ns = la.wait_limit_ns;
   a.test_flags = la.test_flags;
-  tc::tc_kernel<T><<<p.grid, tc::kThreads, p.smem_bytes, la.stream>>>(map, a);
+  const TcKernel<T> kern = p.sw ? tc::tc_kernel<T, true> : tc::tc_kernel<T, false>;
+  kern<<<p.grid, tc::kThreads, p.smem_bytes, la.stream>>>(map, a);
   return cudaGetLastError();
 }
 

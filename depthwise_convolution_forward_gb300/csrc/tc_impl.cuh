@@ -56,8 +56,9 @@ struct TcArgs {
   int ntaps;
   int tap_phase[kMaxTaps], tap_off[kMaxTaps];
   int nchunks, Kt, Nn, KS, nmt;
+  int sc;                  // group chunks per 128-byte row (swizzled layout), else 1
   uint32_t plane_stride, a_stage_bytes, tx_bytes;
-  uint32_t a_off, b_off, bias_off;
+  uint32_t a_off, b_off, bias_off, tab_off;  // smem offsets (tab: MMA descriptor table)
   int stages;
   uint32_t tmem_cols, idesc;
   int n_gc, cpg, tiles_w, tiles_h;
@@ -94,7 +95,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
   return __all_sync(0xffffffffu, ok);
 }
 
-template <typename T>
+// SW = false: A planes hold one 8-channel chunk per pixel (16-byte rows,
+// no swizzle), one TMA box per (phase, chunk).  SW = true: A planes hold 64
+// channels per pixel (128-byte rows, 128-byte swizzle) covering `sc` group
+// chunks, one TMA box per phase; each chunk is a K-offset inside the row.
+template <typename T, bool SW>
 __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* a_full = reinterpret_cast<uint64_t*>(smem);
@@ -108,9 +113,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
   uint8_t* As = smem + a.a_off;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gc = blockIdx.x % a.n_gc;
-  const int cta_in_gc = blockIdx.x / a.n_gc;
-  const int g0 = gc * a.m;
+  const int n_sc = a.n_gc / a.sc;
+  const int gsc = blockIdx.x % n_sc;  // this CTA's row of sc group chunks
+  const int cta_in_gc = blockIdx.x / n_sc;
+  const int g0 = gsc * a.sc * a.m;
   const T* __restrict__ wg = static_cast<const T*>(a.w);
   const T* __restrict__ bg = static_cast<const T*>(a.bias);
   T* __restrict__ yg = static_cast<T*>(a.y);
@@ -136,12 +142,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
   // matrices: byte offset ((((t*KS + ks)*2 + kc2)*Nn + n)*8 + e)*2 holds
   // k = ks*16 + kc2*8 + e.
   {
+    // sc sub-blocks (one per group chunk j), each [t][ks][kc2][n][8]
     const int per_tap = a.Kt * a.Nn;
-    const int total = a.ntaps * per_tap;
+    const int per_chunk = a.ntaps * per_tap;
+    const int total = a.sc * per_chunk;
     T* B = reinterpret_cast<T*>(Bs);
     for (int i = tid; i < total; i += blockDim.x) {
-      const int t = i / per_tap;
-      int r = i - t * per_tap;
+      const int j = i / per_chunk;
+      int r = i - j * per_chunk;
+      const int t = r / per_tap;
+      r -= t * per_tap;
       const int e = r & 7;
       r >>= 3;
       const int n = r % a.Nn;
@@ -151,13 +161,41 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
       const int k = ks * 16 + kc2 * 8 + e;
       const int gj = k / a.Cg, cc = k - gj * a.Cg;
       const int gi = n / a.Kg, kk = n - gi * a.Kg;
+      const int gbase = g0 + j * a.m;
       T v = Elem<T>::from_f32(0.f);
       if (gi == gj)
-        v = wg[((int64_t)(g0 + gi) * a.Kg + kk) * a.taps_total * a.Cg + (int64_t)t * a.Cg + cc];
+        v = wg[((int64_t)(gbase + gi) * a.Kg + kk) * a.taps_total * a.Cg + (int64_t)t * a.Cg + cc];
       B[i] = v;
     }
-    for (int i = tid; i < a.Nn; i += blockDim.x)
+    for (int i = tid; i < a.sc * a.Nn; i += blockDim.x)
       bias_s[i] = bg != nullptr ? Elem<T>::to_f32(bg[(int64_t)g0 * a.Kg + i]) : 0.f;
+  }
+  // Descriptor table: for every MMA of a tile, in issue order (chunk j, M-tile
+  // mt, tap t, K-step ks), the A descriptor for stage 0 and the B descriptor.
+  // The issuing thread then only adds the stage offset, so one MMA costs a
+  // table read instead of a chain of address arithmetic.
+  {
+    uint64_t* tab = reinterpret_cast<uint64_t*>(smem + a.tab_off);
+    const int per_grp = a.ntaps * a.KS;
+    const int n = a.sc * a.nmt * per_grp;
+    const uint32_t a_base = smem_u32(As), b_base = smem_u32(Bs);
+    const uint32_t lbo_b = (uint32_t)a.Nn * 16u;
+    for (int i = tid; i < n; i += blockDim.x) {
+      const int grp = i / per_grp, e = i - grp * per_grp;
+      const int j = grp / a.nmt, mt = grp - j * a.nmt;
+      const int t = e / a.KS, ks = e - t * a.KS;
+      uint64_t adesc;
+      if constexpr (SW) {
+        const uint32_t row = a_base + (uint32_t)a.tap_phase[t] * a.plane_stride + (uint32_t)(mt * 128 + a.tap_off[t]) * 128u;
+        adesc = smem_desc_sw128(row + (uint32_t)(j * a.Kt * 2 + ks * 32));
+      } else {
+        const uint32_t plane0 = a_base + (uint32_t)(a.tap_phase[t] * a.nchunks) * a.plane_stride;
+        const uint32_t row0 = (uint32_t)(mt * 128 + a.tap_off[t]) * 16u;
+        adesc = smem_desc(plane0 + (uint32_t)(2 * ks) * a.plane_stride + row0, a.plane_stride, 128u);
+      }
+      tab[2 * i] = adesc;
+      tab[2 * i + 1] = smem_desc(b_base + (uint32_t)(((j * a.ntaps + t) * a.KS + ks) * 2) * lbo_b, lbo_b, 128u);
+    }
   }
   fence_proxy_async_smem();  // generic-proxy writes of B -> visible to the tensor core
   fence_before_sync();
@@ -185,9 +223,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         for (int ph = 0; ph < a.nphase; ++ph) {
           const int ih0 = a.s * (st.oh0 + a.qy_min) + a.phase_py[ph];
           const int iw0 = a.s * (st.ow0 + a.qx_min) + a.phase_px[ph];
-          for (int c = 0; c < a.nchunks; ++c)
-            tma_load_5d(stage + (size_t)(ph * a.nchunks + c) * a.plane_stride, &xmap, &a_full[s],
-                        g0 * a.Cg + c * 8, iw0, ih0, id0, st.n);
+          if constexpr (SW) {
+            tma_load_5d(stage + (size_t)ph * a.plane_stride, &xmap, &a_full[s], g0 * a.Cg, iw0, ih0, id0, st.n);
+          } else {
+            for (int c = 0; c < a.nchunks; ++c)
+              tma_load_5d(stage + (size_t)(ph * a.nchunks + c) * a.plane_stride, &xmap, &a_full[s],
+                          g0 * a.Cg + c * 8, iw0, ih0, id0, st.n);
+          }
         }
       }
       if (failed) report(a.status, kDevTimeout, 3);
@@ -201,8 +243,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     if (lane == 0) {
       int k = 0;
       bool failed = false;
-      const uint32_t b_base = smem_u32(Bs);
-      const uint32_t lbo_b = (uint32_t)a.Nn * 16u;
       for (int sp = cta_in_gc; sp < a.spatial_tiles; sp += a.cpg, ++k) {
         const int s = k % a.stages;
         const int ab = k & 1;
@@ -215,17 +255,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
           break;
         }
         fence_after_sync();
-        const uint32_t a_base = smem_u32(As + (size_t)s * a.a_stage_bytes);
-        for (int mt = 0; mt < a.nmt; ++mt) {
-          const uint32_t d = tmem_base + (uint32_t)((ab * a.nmt + mt) * a.Nn);
-          for (int t = 0; t < a.ntaps; ++t) {
-            const uint32_t plane0 = a_base + (uint32_t)(a.tap_phase[t] * a.nchunks) * a.plane_stride;
-            const uint32_t row0 = (uint32_t)(mt * 128 + a.tap_off[t]) * 16u;
-            for (int ks = 0; ks < a.KS; ++ks) {
-              const uint64_t adesc = smem_desc(plane0 + (uint32_t)(2 * ks) * a.plane_stride + row0, a.plane_stride, 128u);
-              const uint64_t bdesc = smem_desc(b_base + (uint32_t)((t * a.KS + ks) * 2) * lbo_b, lbo_b, 128u);
-              mma_f16(d, adesc, bdesc, a.idesc, (t | ks) != 0 ? 1u : 0u);
-            }
+        // descriptor start addresses are in 16-byte units in the low bits
+        const uint64_t stage_delta = (uint64_t)(((uint32_t)s * a.a_stage_bytes) >> 4);
+        const uint64_t* tab = reinterpret_cast<const uint64_t*>(smem + a.tab_off);
+        const int per_grp = a.ntaps * a.KS;
+        for (int grp = 0; grp < a.sc * a.nmt; ++grp) {
+          const int j = grp / a.nmt, mt = grp - j * a.nmt;
+          const uint32_t d = tmem_base + (uint32_t)(((ab * a.nmt + mt) * a.sc + j) * a.Nn);
+          const uint64_t* te = tab + 2 * grp * per_grp;
+          for (int e = 0; e < per_grp; ++e) {
+            const uint2 ad = *reinterpret_cast<const uint2*>(te + 2 * e);  // low/high words of A
+            const uint64_t adesc = (((uint64_t)ad.y << 32) | ad.x) + stage_delta;
+            mma_f16(d, adesc, te[2 * e + 1], a.idesc, e != 0 ? 1u : 0u);
           }
         }
         commit(&a_empty[s]);   // stage reusable once these MMAs have read it
@@ -255,17 +296,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         const bool valid = i < a.TH && j < a.TWo && oh < a.Ho && ow < a.Wo;
         T* dst = yg + ((((int64_t)st.n * a.Do + st.od) * a.Ho + oh) * (int64_t)a.Wo + ow) * a.Ktot +
                  (int64_t)g0 * a.Kg;
-        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)((ab * a.nmt + mt) * a.Nn);
-        for (int c0 = 0; c0 < a.Nn; c0 += 16) {
-          uint32_t r[16];
-          tmem_ld16(taddr + (uint32_t)c0, r);
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)((ab * a.nmt + mt) * a.sc * a.Nn);
+        // columns of chunk j follow those of chunk j-1; four 16-column loads
+        // are issued before one wait
+        for (int c0 = 0; c0 < a.sc * a.Nn; c0 += 64) {
+          uint32_t r[4][16];
+          const int nq = min(4, (a.sc * a.Nn - c0) / 16);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (u < nq) tmem_ld16(taddr + (uint32_t)(c0 + 16 * u), r[u]);
           tmem_ld_wait();
           if (valid) {
-            float v[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
-            epilogue_store<T, 8>(dst + c0, v, bias_s + c0);
-            epilogue_store<T, 8>(dst + c0 + 8, v + 8, bias_s + c0 + 8);
+            for (int u = 0; u < 4; ++u) {
+              if (u < nq) {
+                float v[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[u][e]);
+                epilogue_store<T, 8>(dst + c0 + 16 * u, v, bias_s + c0 + 16 * u);
+                epilogue_store<T, 8>(dst + c0 + 16 * u + 8, v + 8, bias_s + c0 + 16 * u + 8);
+              }
+            }
           }
         }
       }

@@ -72,6 +72,24 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;                 // base offset 0, relative LBO, swizzle none
 }
 
+// Shared-memory matrix descriptor, 128-byte swizzle, K-major: rows of 128
+// bytes (64 16-bit elements of K), 8-row atoms of 1024 bytes (SBO), the
+// 16-byte chunk c of a row stored at c ^ (address bits 7..9).  The swizzle
+// phase comes from the absolute shared-memory address of each row -- the same
+// rule TMA applies when it writes 1024-byte-aligned atoms -- so a start
+// address shifted by any whole number of rows reads those rows correctly with
+// the base-offset field left at 0 (verified against the oracle for shifts
+// that are and are not multiples of 8 rows).  K-steps inside a row advance
+// the start by 32 bytes.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;  // SBO: 8 rows x 128 B
+  d |= (uint64_t)1u << 46;                        // fixed descriptor version bits
+  d |= (uint64_t)2u << 61;                        // layout: 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor of kind::f16 with fp32 accumulation, both operands
 // K-major, dense.  bf16 = true selects bf16 inputs, else f16.
 __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N) {
