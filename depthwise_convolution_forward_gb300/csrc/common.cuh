@@ -173,13 +173,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 // Bounded wait on phase `parity`.  Returns false once `limit_ns` of wall time
 // (the GPU global timer) has passed without the phase completing.
+// Polls back off exponentially (up to 256 ns between polls) so that waiting
+// threads do not flood the shared-memory / MIO path that the producers,
+// TMA engine and tensor-core issue also use.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  uint32_t sleep_ns = 8;
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 4; ++i) {
       if (mbar_try_wait(bar, parity)) return true;
+      __nanosleep(sleep_ns);
+      if (sleep_ns < 256) sleep_ns <<= 1;
+    }
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }

@@ -131,9 +131,25 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     c.a_stage_bytes = round_up((uint32_t)(c.nphase * c.nchunks) * c.plane_stride, 1024);
     c.tx_bytes = (uint32_t)(c.nphase * c.nchunks) * (uint32_t)(c.Dh * c.Hh * c.P) * row_bytes;
     const uint32_t b_bytes = round_up((uint32_t)(c.sc * taps * c.Kt * c.Nn * 2), 1024);
+    // Partial accumulators so that the tile has at least kIssuers
+    // independent units of MMA work: np in {4, 2, 1} within 512 TMEM columns.
+    const int G2 = c.sc * c.nmt;
+    int np = 1;
+    while (np * 2 <= tc::kIssuers && G2 * np < tc::kIssuers && np * 2 <= taps &&
+           2 * (np * 2) * G2 * c.Nn <= 512)
+      np *= 2;
+    if (ov && ov[4]) np = ov[4];
+    c.np = np;
+    // per-issuer MMA lists: 32 bytes per entry
+    uint32_t entries = 0;
+    {
+      const int units = G2 * np, steps = ((taps + np - 1) / np) * c.KS;
+      for (int w = 0; w < tc::kIssuers; ++w)
+        entries += (uint32_t)(steps * (units > w ? (units - w + tc::kIssuers - 1) / tc::kIssuers : 0));
+    }
     c.bias_off = 1024;
-    c.tab_off = c.bias_off + round_up((uint32_t)(c.sc * c.Nn) * 4u, 16);
-    const uint32_t tab_bytes = (uint32_t)(c.sc * c.nmt * taps * c.KS) * 16u;
+    c.tab_off = round_up(c.bias_off + (uint32_t)(c.sc * c.Nn) * 4u, 16);
+    const uint32_t tab_bytes = entries * 32u;
     c.b_off = round_up(c.tab_off + tab_bytes, 1024);
     c.a_off = c.b_off + b_bytes;
     int stages = (ov && ov[3]) ? ov[3] : tc::kMaxStages;
@@ -142,7 +158,7 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     if (c.a_off + stages * c.a_stage_bytes > budget) continue;
     c.stages = stages;
     uint32_t cols = 32;
-    while (cols < (uint32_t)(2 * c.nmt * c.sc * c.Nn)) cols <<= 1;
+    while (cols < (uint32_t)(2 * np * G2 * c.Nn)) cols <<= 1;
     if (cols > 512) continue;
     c.tmem_cols = cols;
     c.idesc = tc::idesc_f16(bf16, 128, c.Nn);

@@ -40,7 +40,8 @@ namespace tc {
 constexpr int kMaxTaps = 32;
 constexpr int kMaxPhases = 4;
 constexpr int kMaxStages = 4;
-constexpr int kThreads = 192;
+constexpr int kIssuers = 4;                       // MMA-issuing warps
+constexpr int kThreads = 32 * (1 + kIssuers + 4);  // producer, issuers, epilogue
 
 struct TcArgs {
   const void* w;
@@ -57,6 +58,7 @@ struct TcArgs {
   int tap_phase[kMaxTaps], tap_off[kMaxTaps];
   int nchunks, Kt, Nn, KS, nmt;
   int sc;                  // group chunks per 128-byte row (swizzled layout), else 1
+  int np;                  // partial accumulators per accumulator (taps split np ways)
   uint32_t plane_stride, a_stage_bytes, tx_bytes;
   uint32_t a_off, b_off, bias_off, tab_off;  // smem offsets (tab: MMA descriptor table)
   int stages;
@@ -95,6 +97,48 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
   return __all_sync(0xffffffffu, ok);
 }
 
+// Epilogue for one output row of a tile: per batch, load 4 / NP chunks of 16
+// channels from each of the NP partial accumulators (at most 4 loads in
+// flight, one wait), sum the partials, add bias, round, store.
+template <typename T, int NP>
+__device__ __forceinline__ void epilogue_row(uint32_t lane_base, int mt, int G2, int sc, int Nn, bool valid, T* dst,
+                                             const float* bias_s) {
+  constexpr int kPer = 4 / NP;
+  const int nchunk16 = sc * Nn / 16;
+  for (int c = 0; c < nchunk16; c += kPer) {
+    uint32_t r[kPer][NP][16];
+#pragma unroll
+    for (int b = 0; b < kPer; ++b) {
+      const int cc = c + b;
+      if (cc < nchunk16) {
+        const int col = cc * 16;  // channel offset within the row of sc chunks
+        const int j = col / Nn, cn = col - j * Nn;
+#pragma unroll
+        for (int p = 0; p < NP; ++p) tmem_ld16(lane_base + (uint32_t)((p * G2 + mt * sc + j) * Nn + cn), r[b][p]);
+      }
+    }
+    tmem_ld_wait();
+    if (valid) {
+#pragma unroll
+      for (int b = 0; b < kPer; ++b) {
+        const int cc = c + b;
+        if (cc < nchunk16) {
+          float v[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float sum = __uint_as_float(r[b][0][e]);
+#pragma unroll
+            for (int p = 1; p < NP; ++p) sum += __uint_as_float(r[b][p][e]);
+            v[e] = sum;
+          }
+          epilogue_store<T, 8>(dst + cc * 16, v, bias_s + cc * 16);
+          epilogue_store<T, 8>(dst + cc * 16 + 8, v + 8, bias_s + cc * 16 + 8);
+        }
+      }
+    }
+  }
+}
+
 // SW = false: A planes hold one 8-channel chunk per pixel (16-byte rows,
 // no swizzle), one TMA box per (phase, chunk).  SW = true: A planes hold 64
 // channels per pixel (128-byte rows, 128-byte swizzle) covering `sc` group
@@ -124,13 +168,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
   if (tid == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(&a_full[s], 1);
-      mbar_init(&a_empty[s], 1);
+      mbar_init(&a_empty[s], kIssuers);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_full[b], kIssuers);
       mbar_init(&acc_empty[b], 4);
     }
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, kIssuers);
     fence_mbar_init();
     tma_prefetch_desc(&xmap);
   }
@@ -170,31 +214,51 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     for (int i = tid; i < a.sc * a.Nn; i += blockDim.x)
       bias_s[i] = bg != nullptr ? Elem<T>::to_f32(bg[(int64_t)g0 * a.Kg + i]) : 0.f;
   }
-  // Descriptor table: for every MMA of a tile, in issue order (chunk j, M-tile
-  // mt, tap t, K-step ks), the A descriptor for stage 0 and the B descriptor.
-  // The issuing thread then only adds the stage offset, so one MMA costs a
-  // table read instead of a chain of address arithmetic.
+  // Per-issuer MMA lists.  The tile's work is split into units u = grp * np
+  // + p (accumulator grp = mt * sc + j, partial p summing the taps t with
+  // t % np == p); issuer w owns units w, w + kIssuers, ...  Its list holds,
+  // in issue order (unit-local step s outer, its units inner, so consecutive
+  // MMAs write different accumulators), one 32-byte entry per MMA: A
+  // descriptor for stage 0, B descriptor, accumulator column, flags (bit 0:
+  // accumulate, bit 1: skip).  The issuing thread then only adds the stage
+  // offset, and can fetch entry i + 1 while MMA i issues.
   {
-    uint64_t* tab = reinterpret_cast<uint64_t*>(smem + a.tab_off);
-    const int per_grp = a.ntaps * a.KS;
-    const int n = a.sc * a.nmt * per_grp;
+    uint4* tab = reinterpret_cast<uint4*>(smem + a.tab_off);
+    const int G2 = a.sc * a.nmt, NP = a.np;
+    const int units = G2 * NP;
+    const int steps = ((a.ntaps + NP - 1) / NP) * a.KS;
     const uint32_t a_base = smem_u32(As), b_base = smem_u32(Bs);
     const uint32_t lbo_b = (uint32_t)a.Nn * 16u;
-    for (int i = tid; i < n; i += blockDim.x) {
-      const int grp = i / per_grp, e = i - grp * per_grp;
-      const int j = grp / a.nmt, mt = grp - j * a.nmt;
-      const int t = e / a.KS, ks = e - t * a.KS;
-      uint64_t adesc;
-      if constexpr (SW) {
-        const uint32_t row = a_base + (uint32_t)a.tap_phase[t] * a.plane_stride + (uint32_t)(mt * 128 + a.tap_off[t]) * 128u;
-        adesc = smem_desc_sw128(row + (uint32_t)(j * a.Kt * 2 + ks * 32));
-      } else {
-        const uint32_t plane0 = a_base + (uint32_t)(a.tap_phase[t] * a.nchunks) * a.plane_stride;
-        const uint32_t row0 = (uint32_t)(mt * 128 + a.tap_off[t]) * 16u;
-        adesc = smem_desc(plane0 + (uint32_t)(2 * ks) * a.plane_stride + row0, a.plane_stride, 128u);
+    int base = 0;
+    for (int w = 0; w < kIssuers; ++w) {
+      const int nu = units > w ? (units - w + kIssuers - 1) / kIssuers : 0;
+      const int len = steps * nu;
+      for (int i = tid; i < len; i += blockDim.x) {
+        const int st = i / nu, ui = i - st * nu;
+        const int u = w + kIssuers * ui;
+        const int grp = u / NP, p = u - grp * NP;
+        const int t = p + NP * (st / a.KS), ks = st % a.KS;
+        const int mt = grp / a.sc, j = grp - mt * a.sc;
+        uint4 e0 = make_uint4(0u, 0u, 0u, 0u), e1 = make_uint4(0u, 0u, 0u, 2u);  // default: skip
+        if (t < a.ntaps) {
+          uint64_t adesc;
+          if constexpr (SW) {
+            const uint32_t row = a_base + (uint32_t)a.tap_phase[t] * a.plane_stride +
+                                 (uint32_t)(mt * 128 + a.tap_off[t]) * 128u;
+            adesc = smem_desc_sw128(row + (uint32_t)(j * a.Kt * 2 + ks * 32));
+          } else {
+            const uint32_t plane0 = a_base + (uint32_t)(a.tap_phase[t] * a.nchunks) * a.plane_stride;
+            const uint32_t row0 = (uint32_t)(mt * 128 + a.tap_off[t]) * 16u;
+            adesc = smem_desc(plane0 + (uint32_t)(2 * ks) * a.plane_stride + row0, a.plane_stride, 128u);
+          }
+          const uint64_t bdesc = smem_desc(b_base + (uint32_t)(((j * a.ntaps + t) * a.KS + ks) * 2) * lbo_b, lbo_b, 128u);
+          e0 = make_uint4((uint32_t)adesc, (uint32_t)(adesc >> 32), (uint32_t)bdesc, (uint32_t)(bdesc >> 32));
+          e1 = make_uint4((uint32_t)((p * G2 + grp) * a.Nn), 0u, 0u, st == 0 ? 0u : 1u);
+        }
+        tab[2 * (base + i)] = e0;
+        tab[2 * (base + i) + 1] = e1;
       }
-      tab[2 * i] = adesc;
-      tab[2 * i + 1] = smem_desc(b_base + (uint32_t)(((j * a.ntaps + t) * a.KS + ks) * 2) * lbo_b, lbo_b, 128u);
+      base += len;
     }
   }
   fence_proxy_async_smem();  // generic-proxy writes of B -> visible to the tensor core
@@ -238,11 +302,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         mbar_wait(&a_full[j % a.stages], (uint32_t)((j / a.stages) & 1), a.wait_limit_ns);
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp <= kIssuers) {
+    // ---------------- MMA issuers (warps 1..kIssuers) ----------------
+    // A single thread can only have one tcgen05.mma in its issue pipeline
+    // at a time (about 160 cycles per instruction, whatever M and N), so
+    // several warps issue in parallel.  The tile's work is split into units
+    // (accumulator grp, partial p): partial p of an accumulator sums the taps
+    // t with t % np == p, and the epilogue adds the np partials.  Issuer w
+    // takes the units u = grp * np + p with u % kIssuers == w; within an
+    // issuer, consecutive MMAs cycle over its units (no back-to-back
+    // accumulation into one accumulator).
     if (lane == 0) {
+      const int w = warp - 1;
       int k = 0;
       bool failed = false;
+      const int G2 = a.sc * a.nmt;
+      const int NP = a.np;
+      const int units = G2 * NP;
+      const int steps = ((a.ntaps + NP - 1) / NP) * a.KS;
+      int my_base = 0, my_len = 0;
+      for (int v = 0; v <= w; ++v) {
+        const int nu = units > v ? (units - v + kIssuers - 1) / kIssuers : 0;
+        if (v < w) my_base += steps * nu; else my_len = steps * nu;
+      }
+      const uint4* my_list = reinterpret_cast<const uint4*>(smem + a.tab_off) + 2 * my_base;
       for (int sp = cta_in_gc; sp < a.spatial_tiles; sp += a.cpg, ++k) {
         const int s = k % a.stages;
         const int ab = k & 1;
@@ -257,29 +340,35 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         fence_after_sync();
         // descriptor start addresses are in 16-byte units in the low bits
         const uint64_t stage_delta = (uint64_t)(((uint32_t)s * a.a_stage_bytes) >> 4);
-        const uint64_t* tab = reinterpret_cast<const uint64_t*>(smem + a.tab_off);
-        const int per_grp = a.ntaps * a.KS;
-        for (int grp = 0; grp < a.sc * a.nmt; ++grp) {
-          const int j = grp / a.nmt, mt = grp - j * a.nmt;
-          const uint32_t d = tmem_base + (uint32_t)(((ab * a.nmt + mt) * a.sc + j) * a.Nn);
-          const uint64_t* te = tab + 2 * grp * per_grp;
-          for (int e = 0; e < per_grp; ++e) {
-            const uint2 ad = *reinterpret_cast<const uint2*>(te + 2 * e);  // low/high words of A
-            const uint64_t adesc = (((uint64_t)ad.y << 32) | ad.x) + stage_delta;
-            mma_f16(d, adesc, te[2 * e + 1], a.idesc, e != 0 ? 1u : 0u);
+        // unit (grp, p) of buffer ab sits at columns ((ab * np + p) * G2 + grp) * Nn
+        const uint32_t dbuf = tmem_base + (uint32_t)(ab * NP * G2 * a.Nn);
+        if (my_len > 0) {
+          uint4 c0 = my_list[0], c1 = my_list[1];
+          for (int i = 0; i < my_len; ++i) {
+            const int nx = i + 1 < my_len ? i + 1 : i;
+            const uint4 n0 = my_list[2 * nx], n1 = my_list[2 * nx + 1];
+            if (!(c1.w & 2u)) {
+              const uint64_t adesc = (((uint64_t)c0.y << 32) | c0.x) + stage_delta;
+              const uint64_t bdesc = ((uint64_t)c0.w << 32) | c0.z;
+              mma_f16(dbuf + c1.x, adesc, bdesc, a.idesc, c1.w & 1u);
+            }
+            c0 = n0;
+            c1 = n1;
           }
         }
-        commit(&a_empty[s]);   // stage reusable once these MMAs have read it
-        commit(&acc_full[ab]);  // accumulators of this tile complete
+        commit(&a_empty[s]);    // this issuer's reads of the stage are done
+        commit(&acc_full[ab]);  // this issuer's accumulations are done
       }
       if (failed) report(a.status, kDevTimeout, 4);
-      commit(mma_done);  // every MMA issued so far has completed
+      commit(mma_done);  // every MMA this issuer issued has completed
       mbar_wait(mma_done, 0, a.wait_limit_ns);
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (warps kIssuers+1 .. kIssuers+4) ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
+    const int G2 = a.sc * a.nmt;
+    const int NP = a.np;
     int k = 0;
     for (int sp = cta_in_gc; sp < a.spatial_tiles; sp += a.cpg, ++k) {
       const int ab = k & 1;
@@ -289,36 +378,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
       }
       fence_after_sync();
       const SpatialTile st = decode_spatial(a, sp);
+      const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * NP * G2 * a.Nn);
       for (int mt = 0; mt < a.nmt; ++mt) {
         const int f = mt * 128 + row;
-        const int i = f / a.P, j = f - i * a.P;
-        const int oh = st.oh0 + i, ow = st.ow0 + j;
-        const bool valid = i < a.TH && j < a.TWo && oh < a.Ho && ow < a.Wo;
+        const int i = f / a.P, jj = f - i * a.P;
+        const int oh = st.oh0 + i, ow = st.ow0 + jj;
+        const bool valid = i < a.TH && jj < a.TWo && oh < a.Ho && ow < a.Wo;
         T* dst = yg + ((((int64_t)st.n * a.Do + st.od) * a.Ho + oh) * (int64_t)a.Wo + ow) * a.Ktot +
                  (int64_t)g0 * a.Kg;
-        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)((ab * a.nmt + mt) * a.sc * a.Nn);
-        // columns of chunk j follow those of chunk j-1; four 16-column loads
-        // are issued before one wait
-        for (int c0 = 0; c0 < a.sc * a.Nn; c0 += 64) {
-          uint32_t r[4][16];
-          const int nq = min(4, (a.sc * a.Nn - c0) / 16);
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (u < nq) tmem_ld16(taddr + (uint32_t)(c0 + 16 * u), r[u]);
-          tmem_ld_wait();
-          if (valid) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              if (u < nq) {
-                float v[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[u][e]);
-                epilogue_store<T, 8>(dst + c0 + 16 * u, v, bias_s + c0 + 16 * u);
-                epilogue_store<T, 8>(dst + c0 + 16 * u + 8, v + 8, bias_s + c0 + 16 * u + 8);
-              }
-            }
-          }
-        }
+        if (NP == 1) epilogue_row<T, 1>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s);
+        else if (NP == 2) epilogue_row<T, 2>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s);
+        else epilogue_row<T, 4>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s);
       }
       fence_before_sync();
       __syncwarp();

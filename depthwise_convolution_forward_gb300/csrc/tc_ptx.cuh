@@ -29,14 +29,17 @@ __device__ __forceinline__ void fence_after_sync() {
 }
 
 // --- MMA: D(tmem, fp32) (+)= A(smem) x B(smem)^T, kind::f16 (f16 or bf16) --
+// No "memory" clobber: the operands are ordered by the mbarrier waits and
+// fences around the issue loop (all volatile asm with clobbers, which this
+// statement is never reordered across), and leaving ordinary loads free lets
+// the compiler fetch the next MMA's descriptors while this one issues.
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                         uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
