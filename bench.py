@@ -171,6 +171,26 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# Multi-rank helpers (replicas: every rank runs the whole workload on its GPU)
+# ---------------------------------------------------------------------------
+def reduce_max(value: float, dist=None, device=None) -> float:
+    """Max of `value` over all ranks (identity without a process group)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Units per second of the whole job: every rank processed `steps` steps
+    of `units_per_step` units, and the job took the slowest rank's time."""
+    return units_per_step * steps * world / (max_ms / 1e3)
+
+
+# ---------------------------------------------------------------------------
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for p in sorted(glob.glob(os.path.join(ROOT, "depthwise_convolution_forward_gb300", "csrc", "*"))):
@@ -427,10 +447,7 @@ def run_ours(args, wls, set_name, rank, world):
         step_ms.append(dv.elapsed_ms(events[k * nl], events[(k + 1) * nl]))
     dv.destroy(events)
 
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(total_ms, dist, dev)
 
     # per-kernel aggregation (kernel id -> bytes, ms, launches)
     per_kernel = {}
@@ -460,8 +477,8 @@ def run_ours(args, wls, set_name, rank, world):
             "avg_launch_us": d["ms"] / d["launches"] * 1e3}
 
     ms_per_step = total_ms / K
-    value = step_bytes * K * world / (total_ms / 1e3) / 1e9
-    tflops = step_flops * K * world / (total_ms / 1e3) / 1e12
+    value = whole_job_rate(step_bytes, K, world, total_ms) / 1e9
+    tflops = whole_job_rate(step_flops, K, world, total_ms) / 1e12
     med = statistics.median(step_ms)
     per_launch = {}
     for ci, c in enumerate(convs):
@@ -545,12 +562,8 @@ def run_e2e(args, convs, lib, dev, stream, world, dist, step_bytes, gc):
         step()
     e1.record(stream)
     stream.synchronize()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": step_bytes * n * world / (ms / 1e3) / 1e9, "unit": "GB/s", "steps": n,
+    ms = reduce_max(e0.elapsed_time(e1), dist, dev)
+    return {"value": whole_job_rate(step_bytes, n, world, ms) / 1e9, "unit": "GB/s", "steps": n,
             "ms_per_step": ms / n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "api": "grouped_conv_fwd (C ABI) with pinned host buffers copied in and out each step"}
 
