@@ -218,10 +218,17 @@ def load_traffic(kernel_name: str, workload: str):
 
 
 def resolve(names_arg):
+    """Bench set or comma-separated workload names; ``name:dtype`` runs a
+    workload's shape in another storage type (f32, f16, bf16)."""
     from depthwise_convolution_forward_gb300 import inputs
 
     names = BENCH_SETS.get(names_arg, None) or names_arg.split(",")
-    return names_arg, [inputs.by_name(n) for n in names]
+    wls = []
+    for n in names:
+        base, _, dt = n.partition(":")
+        wl = inputs.by_name(base)
+        wls.append(wl.with_(dtype=dt, name=n) if dt else wl)
+    return names_arg, wls
 
 
 def describe(wls) -> str:
@@ -485,6 +492,7 @@ def run_ours(args, wls, set_name, rank, world):
         m = statistics.median(launch_ms[ci])
         per_launch[c["wl"].name] = {
             "kernel": gc.KERNEL_NAMES.get(c["kernel"]), "median_us": m * 1e3,
+            "mean_us": statistics.fmean(launch_ms[ci]) * 1e3,
             "GB_s": c["bytes"] / (m / 1e3) / 1e9, "TFLOP_s": c["flops"] / (m / 1e3) / 1e12,
             "frac_hbm": c["bytes"] / (m / 1e3) / 1e9 / hbm_peak,
             "frac_roofline": max(c["bytes"] / (hbm_peak * 1e9), c["flops"] / (tc_peak * 1e12)) / (m / 1e3)}

@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(256, 2) dw_ldg_kernel(const DwArgs a) {
   constexpr int VEC = Elem<T>::kVec;
   constexpr int NCOL = (WB - 1) * S + (K - 1) * DL + 1;
   static_assert(MODE != kMixedFma || sizeof(T) == 2, "mixed-precision FMA needs 16-bit storage");
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];
   const int taps = a.Z * K * K;
   uint8_t* w_raw = smem;
   float* b_s = reinterpret_cast<float*>(smem + weight_smem_bytes(taps, a.TC, (int)sizeof(T), MODE));

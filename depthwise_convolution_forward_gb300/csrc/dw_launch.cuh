@@ -6,6 +6,7 @@
 #include <algorithm>
 
 #include "dw_impl.cuh"
+#include "dwc_impl.cuh"
 #include "plan_cache.h"
 
 namespace gconv {
@@ -14,6 +15,7 @@ namespace dw {
 struct Plan {
   int TH, TW, TC, WB, stages, ctas_per_sm, mode;
   int direct;  // 1: direct-load variant (dw_ldg_kernel), 0: TMA-staged pipeline
+  int col;     // 1: column form (dw_col_kernel)
   int Dh, Hh, Wh;
   int tiles_c, tiles_w, tiles_h;
   int64_t num_tiles;
@@ -117,6 +119,95 @@ inline bool make_plan(const Geometry& g, int es, const int* tile_override, int n
   return true;
 }
 
+// Operand form of the column kernel (override slot 5): 1 split 16-bit /
+// scalar fp32, 2 packed 16-bit x4, 3 widened fp32x2, 4 packed 16-bit x8;
+// automatic: packed x8 for 16-bit storage, scalar for fp32.
+inline int col_form(int es, const int* ov) {
+  const int ov_form = ov ? ov[5] : 0;
+  int form = es == 2 ? kColPacked8 : kColSplit;
+  if (ov_form == 1) form = kColSplit;
+  if (ov_form == 2 && es == 2) form = kColPacked;
+  if (ov_form == 3) form = kColWide;
+  if (ov_form == 4 && es == 2) form = kColPacked8;
+  return form;
+}
+
+// Column form (dw_col_kernel): depth filter 1 only.  Each consumer thread
+// owns one output column of the tile and CPT channels, so a tile is TW
+// columns x TC channels of threads and TH rows deep.  The plan minimises
+//   rounds x (per-tile row work) x max(1, resident warps / 16)
+// where rounds = ceil(tiles / resident CTAs).  A thread's rows run in
+// sequence, so a tile takes as long as one thread's rows (its output rows, a
+// share for loading halo rows and a fixed start-up); once more than about 16
+// consumer warps share an SM it is issue-bound and tiles slow down in
+// proportion.  Resident CTAs per SM are bounded by shared memory, threads and
+// the kernel's registers per thread (`regs`).
+inline bool make_col_plan(const Geometry& g, int es, const int* ov, int num_sms, int form, int regs, Plan* out) {
+  if (g.Z != 1) return false;
+  const int S = g.sH, DL = g.dH;
+  const int vec = 16 / es;
+  const int cpt = col_cpt(es, form);
+  const int TC = pick_tc(g.C(), vec);
+  const int NQ = TC / cpt;
+  const uint32_t fixed = align_up(col_fixed_smem_bytes(g.C()), 1024);
+  const uint32_t half_sm = 113 * 1024, third_sm = 75 * 1024, full_sm = 220 * 1024;
+  const int ov_th = ov ? ov[0] : 0, ov_tw = ov ? ov[1] : 0, ov_stages = ov ? ov[3] : 0, ov_ctas = ov ? ov[4] : 0;
+  const int tiles_c = ceil_div(g.C(), TC);
+  const int regs_warp = (regs + 7) / 8 * 8 * 32;
+  Plan best{};
+  double best_cost = 1e30;
+  const int tw_max = std::min(g.Wo, (col_max_threads(form) - 32) / NQ);
+  for (int TW = 1; TW <= tw_max; ++TW) {
+    if (ov_tw && ov_tw != TW) continue;
+    const int Wh = (TW - 1) * S + 2 * DL + 1;
+    if (Wh > 256) break;
+    const int ncons = (TW * NQ + 31) / 32 * 32;
+    const int warps = ncons / 32;
+    const int tiles_w = ceil_div(g.Wo, TW);
+    for (int TH = 1; TH <= std::min(g.Ho, 64); ++TH) {
+      if (ov_th && ov_th != TH) continue;
+      const int Hh = (TH - 1) * S + 2 * DL + 1;
+      if (Hh > 256) break;
+      const uint32_t bytes = (uint32_t)Hh * Wh * TC * es;
+      const uint32_t stride = align_up(bytes, 1024);
+      for (int ctas = 1; ctas <= 3; ++ctas) {
+        if (ov_ctas && ov_ctas != ctas) continue;
+        const uint32_t cap = ctas == 1 ? full_sm : (ctas == 2 ? half_sm : third_sm);
+        const int stages = ov_stages ? std::min(ov_stages, kDwMaxStages) : 2;
+        if (fixed + (uint32_t)stages * stride > cap) continue;
+        if (ctas * (ncons + 32) > 2048) continue;
+        if (ctas * (warps + 1) * regs_warp > 65536) continue;
+        const int tiles_h = ceil_div(g.Ho, TH);
+        const int64_t tiles = (int64_t)tiles_c * tiles_w * tiles_h * g.Do * g.N;
+        const int64_t slots = (int64_t)num_sms * ctas;
+        const double rounds = (double)((tiles + slots - 1) / slots);
+        const int resident = ctas * warps;
+        const double cost = rounds * (TH + 0.35 * Hh + 4.0) * std::max(1.0, resident / 16.0);
+        if (cost < best_cost) {
+          best_cost = cost;
+          best = Plan{};
+          best.TH = TH, best.TW = TW, best.TC = TC;
+          best.Dh = 1, best.Hh = Hh, best.Wh = Wh;
+          best.tiles_c = tiles_c, best.tiles_w = tiles_w, best.tiles_h = tiles_h;
+          best.num_tiles = tiles;
+          best.stage_bytes = bytes;
+          best.stage_stride = stride;
+          best.stage_off = fixed;
+          best.stages = stages;
+          best.ctas_per_sm = ctas;
+          best.threads = 32 + ncons;
+        }
+      }
+    }
+  }
+  if (best_cost >= 1e30) return false;
+  best.col = 1;
+  best.mode = form;
+  best.smem_bytes = best.stage_off + best.stages * best.stage_stride;
+  *out = best;
+  return true;
+}
+
 template <typename T>
 inline CUtensorMapDataType tma_type() {
   if (std::is_same<T, float>::value) return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -147,6 +238,25 @@ DwKernel<T> pick_kernel(int S, int DL, int WB, int mode) {
   GCONV_DW_CASE(2, 2, 4)
   GCONV_DW_CASE(2, 2, 8)
 #undef GCONV_DW_CASE
+  return nullptr;
+}
+
+template <typename T>
+DwKernel<T> pick_col_kernel(int S, int DL, int form) {
+#define GCONV_COL_CASE(s_, d_)                                                      \
+  if (S == s_ && DL == d_) {                                                        \
+    if constexpr (sizeof(T) == 2) {                                                 \
+      if (form == kColPacked) return dw_col_kernel<T, s_, d_, kColPacked>;          \
+      if (form == kColPacked8) return dw_col_kernel<T, s_, d_, kColPacked8>;        \
+    }                                                                               \
+    if (form == kColWide) return dw_col_kernel<T, s_, d_, kColWide>;                \
+    return dw_col_kernel<T, s_, d_, kColSplit>;                                     \
+  }
+  GCONV_COL_CASE(1, 1)
+  GCONV_COL_CASE(2, 1)
+  GCONV_COL_CASE(1, 2)
+  GCONV_COL_CASE(2, 2)
+#undef GCONV_COL_CASE
   return nullptr;
 }
 
@@ -192,14 +302,30 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   static PlanCache<Plan> cache;
   Plan p;
   static SmemAttr attr[2][2][2][3];  // [S-1][DL-1][WB==8][mode]
+  static SmemAttr attr_col[2][2][4];  // [S-1][DL-1][form]
   if (!cache.get(key, &p)) {
-    if (!make_plan(g, es, la.tile, dev.num_sms, &p)) return cudaErrorNotSupported;
+    // tile[6]: 0 automatic (column form when the depth filter is 1),
+    // 1 row-blocked form, 2 direct-load variant, 3 column form only.
+    const int kind = la.tile[6];
+    bool planned = false;
+    if ((kind == 0 || kind == 3) && g.Z == 1) {
+      const int form = col_form(es, la.tile);
+      DwKernel<T> k = pick_col_kernel<T>(g.sH, g.dH, form);
+      cudaFuncAttributes fa{};
+      if (k == nullptr) return cudaErrorNotSupported;
+      cudaError_t e = cudaFuncGetAttributes(&fa, k);
+      if (e != cudaSuccess) return e;
+      planned = make_col_plan(g, es, la.tile, dev.num_sms, form, fa.numRegs, &p);
+    }
+    if (!planned && kind != 3) planned = make_plan(g, es, la.tile, dev.num_sms, &p);
+    if (!planned) return cudaErrorNotSupported;
     if (p.direct) {
       if (pick_ldg_kernel<T>(g.sH, g.dH, p.WB, p.mode) == nullptr) return cudaErrorNotSupported;
     } else {
-      DwKernel<T> k = pick_kernel<T>(g.sH, g.dH, p.WB, p.mode);
+      DwKernel<T> k = p.col ? pick_col_kernel<T>(g.sH, g.dH, p.mode) : pick_kernel<T>(g.sH, g.dH, p.WB, p.mode);
       if (k == nullptr || p.smem_bytes > (uint32_t)dev.max_smem_optin) return cudaErrorNotSupported;
-      cudaError_t e = attr[g.sH - 1][g.dH - 1][p.WB == 8][p.mode].ensure(k, dev.device, (int)p.smem_bytes);
+      SmemAttr& at = p.col ? attr_col[g.sH - 1][g.dH - 1][p.mode] : attr[g.sH - 1][g.dH - 1][p.WB == 8][p.mode];
+      cudaError_t e = at.ensure(k, dev.device, (int)p.smem_bytes);
       if (e != cudaSuccess) return e;
       int occ = 0;
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, p.threads, p.smem_bytes);
@@ -262,7 +388,7 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
 
   const int64_t grid64 = std::min<int64_t>(p.num_tiles, (int64_t)dev.num_sms * p.ctas_per_sm);
   const int grid = (int)std::max<int64_t>(1, grid64);
-  DwKernel<T> kern = pick_kernel<T>(g.sH, g.dH, p.WB, p.mode);
+  DwKernel<T> kern = p.col ? pick_col_kernel<T>(g.sH, g.dH, p.mode) : pick_kernel<T>(g.sH, g.dH, p.WB, p.mode);
   kern<<<grid, p.threads, p.smem_bytes, la.stream>>>(map, a);
   return cudaGetLastError();
 }

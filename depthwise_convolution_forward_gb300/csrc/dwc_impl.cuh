@@ -1,0 +1,447 @@
+// Ka, column form: depthwise direct kernel (Cg == Kg == 1, 3x3 spatial
+// filter, depth filter 1) that walks each output column down the tile with a
+// rolling window of accumulator rows.
+//
+// Design (sm_103a):
+//  * Persistent CTAs walk a static list of output tiles
+//    (n, od, TH x TW output pixels, TC channels), as in the row-blocked
+//    form: warp 0 is the producer and issues one 5-D TMA copy of each tile's
+//    haloed input box into a ring of shared-memory stages (zero fill at the
+//    borders is the convolution's zero padding).
+//  * Consumer thread f of the tile owns output column f / NQ and the CPT
+//    channels CPT (f % NQ) .. +CPT-1 (NQ = TC / CPT; CPT = 8 for 16-bit
+//    storage, 4 otherwise).  Consecutive lanes therefore read consecutive
+//    pieces of one shared-memory row (conflict-free), and every output row a
+//    warp stores is one contiguous run of global memory.
+//  * The thread walks the input rows of its column from top to bottom.  Each
+//    input row is loaded once (three shared loads: the three horizontal taps)
+//    and is added into every output row that uses it, with the filter row
+//    that the row sits under; an output row is stored as soon as its last
+//    filter row has been added.  For stride S and dilation DL that keeps
+//    2*DL/S + 1 output rows live.
+//  * The thread's 3x3xCPT weights and CPT bias values stay in registers for
+//    the whole tile; the bias is the addend of each output's first fused
+//    multiply-add.  16-bit inputs are multiplied with the mixed-precision
+//    fma.rn.f32.{f16,bf16} (fp32 product and sum, one rounding), fp32 inputs
+//    with fmaf.
+//  * Fused epilogue (Kc): one round-to-nearest-even pack of the fp32 sums and
+//    one vector store per output.
+//  * Every mbarrier wait is bounded; a timed-out warp records the timeout in
+//    the status word and exits, and the producer drains its copies first.
+#pragma once
+
+#include <type_traits>
+
+#include "dw_impl.cuh"
+
+namespace gconv {
+namespace dw {
+
+
+// Operand forms of the multiply (tuning override slot 5):
+//  kColPacked8  16-bit storage, 8 channels per thread, pairs kept packed in
+//               registers (the default for 16-bit storage);
+//  kColPacked   the same with 4 channels per thread;
+//  kColSplit    16-bit storage, 4 channels, every 16-bit value in the low half
+//               of its own register (weights staged split, the high half of
+//               an input word shifted down once per load); fp32 storage:
+//               scalar fmaf (the default for fp32);
+//  kColWide     4 channels widened to fp32 once per load, multiplied in
+//               channel pairs with the packed fp32x2 FMA.
+enum ColForm : int { kColSplit = 0, kColPacked = 1, kColWide = 2, kColPacked8 = 3 };
+
+// Threads per CTA: a producer warp and up to 16 consumer warps (12 for the
+// 8-channel form, whose threads hold twice the weights and accumulators).
+__host__ __device__ constexpr int col_max_threads(int form) { return form == kColPacked8 ? 416 : 544; }
+
+__device__ __forceinline__ void lds64(uint32_t addr, uint32_t (&v)[2]) {
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(addr));
+}
+__device__ __forceinline__ void lds128a(uint32_t addr, uint32_t (&v)[4]) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(addr));
+}
+
+template <typename T>
+__device__ __forceinline__ float mixed_fma(unsigned short x, unsigned short w, float c);
+template <>
+__device__ __forceinline__ float mixed_fma<__half>(unsigned short x, unsigned short w, float c) {
+  float d;
+  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(x), "h"(w), "f"(c));
+  return d;
+}
+template <>
+__device__ __forceinline__ float mixed_fma<__nv_bfloat16>(unsigned short x, unsigned short w, float c) {
+  float d;
+  asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(x), "h"(w), "f"(c));
+  return d;
+}
+
+// Per (storage type, operand form): channels per thread, register operand
+// type, how one thread's input piece and weight piece are read from shared
+// memory, the multiply, and the bytes one staged weight takes.
+
+struct ColOpsF32 {
+  static constexpr int kCpt = 4;
+  static constexpr int kOps = 4;  // registers per 4-channel piece
+  using Op = float;
+  static constexpr int kWeightBytes = 4;
+  __device__ __forceinline__ static void load_x(uint32_t addr, Op (&v)[kOps]) {
+    uint32_t w[4];
+    lds128a(addr, w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = __uint_as_float(w[e]);
+  }
+  __device__ __forceinline__ static void load_w(uint32_t addr, Op (&v)[kOps]) { load_x(addr, v); }
+  __device__ __forceinline__ static void stage_w(uint8_t* dst, float v) { *reinterpret_cast<float*>(dst) = v; }
+  __device__ __forceinline__ static void mac(float (&d)[kCpt], const Op (&x)[kOps], const Op (&w)[kOps],
+                                             const float (&c)[kCpt]) {
+#pragma unroll
+    for (int e = 0; e < kCpt; ++e) d[e] = fmaf(x[e], w[e], c[e]);
+  }
+};
+
+template <typename T>
+struct ColOpsWide {
+  static constexpr int kCpt = 4;
+  static constexpr int kOps = 4;
+  using Op = float;
+  static constexpr int kWeightBytes = 4;
+  __device__ __forceinline__ static void load_x(uint32_t addr, Op (&v)[kOps]) {
+    if constexpr (sizeof(T) == 4) {
+      uint32_t w[4];
+      lds128a(addr, w);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = __uint_as_float(w[e]);
+    } else {
+      uint32_t w[2];
+      lds64(addr, w);
+      widen_word<T>(w[0], v);
+      widen_word<T>(w[1], v + 2);
+    }
+  }
+  __device__ __forceinline__ static void load_w(uint32_t addr, Op (&v)[kOps]) {
+    uint32_t w[4];
+    lds128a(addr, w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = __uint_as_float(w[e]);
+  }
+  __device__ __forceinline__ static void stage_w(uint8_t* dst, T v) {
+    *reinterpret_cast<float*>(dst) = Elem<T>::to_f32(v);
+  }
+  __device__ __forceinline__ static void mac(float (&d)[kCpt], const Op (&x)[kOps], const Op (&w)[kOps],
+                                             const float (&c)[kCpt]) {
+#pragma unroll
+    for (int e = 0; e < kCpt; e += 2) {
+      const float2 r = __ffma2_rn(make_float2(x[e], x[e + 1]), make_float2(w[e], w[e + 1]), make_float2(c[e], c[e + 1]));
+      d[e] = r.x;
+      d[e + 1] = r.y;
+    }
+  }
+};
+
+template <typename T>
+struct ColOps16Split {
+  static constexpr int kCpt = 4;
+  static constexpr int kOps = 4;
+  using Op = uint32_t;  // value in the low 16 bits
+  static constexpr int kWeightBytes = 4;
+  __device__ __forceinline__ static void load_x(uint32_t addr, Op (&v)[kOps]) {
+    uint32_t w[2];
+    lds64(addr, w);
+    v[0] = w[0], v[1] = w[0] >> 16, v[2] = w[1], v[3] = w[1] >> 16;
+  }
+  __device__ __forceinline__ static void load_w(uint32_t addr, Op (&v)[kOps]) {
+    uint32_t w[4];
+    lds128a(addr, w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = w[e];
+  }
+  __device__ __forceinline__ static void stage_w(uint8_t* dst, T v) {
+    *reinterpret_cast<uint32_t*>(dst) = (uint32_t)(*reinterpret_cast<const unsigned short*>(&v));
+  }
+  __device__ __forceinline__ static void mac(float (&d)[kCpt], const Op (&x)[kOps], const Op (&w)[kOps],
+                                             const float (&c)[kCpt]) {
+#pragma unroll
+    for (int e = 0; e < kCpt; ++e) d[e] = mixed_fma<T>((unsigned short)x[e], (unsigned short)w[e], c[e]);
+  }
+};
+
+// Two mixed-precision FMAs on the halves of packed 16-bit pairs:
+// d_lo = x.lo * w.lo + c_lo, d_hi = x.hi * w.hi + c_hi.  The halves are taken
+// apart inside the asm so the pairs stay packed in registers.
+template <typename T>
+__device__ __forceinline__ void mixed_fma_pair(uint32_t x, uint32_t w, float c_lo, float c_hi, float& d_lo,
+                                               float& d_hi);
+template <>
+__device__ __forceinline__ void mixed_fma_pair<__half>(uint32_t x, uint32_t w, float c_lo, float c_hi, float& d_lo,
+                                                       float& d_hi) {
+  asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\tmov.b32 {wl, wh}, %3;\n\t"
+      "fma.rn.f32.f16 %0, xl, wl, %4;\n\tfma.rn.f32.f16 %1, xh, wh, %5;\n\t}"
+      : "=f"(d_lo), "=f"(d_hi)
+      : "r"(x), "r"(w), "f"(c_lo), "f"(c_hi));
+}
+template <>
+__device__ __forceinline__ void mixed_fma_pair<__nv_bfloat16>(uint32_t x, uint32_t w, float c_lo, float c_hi,
+                                                              float& d_lo, float& d_hi) {
+  asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\tmov.b32 {wl, wh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, xl, wl, %4;\n\tfma.rn.f32.bf16 %1, xh, wh, %5;\n\t}"
+      : "=f"(d_lo), "=f"(d_hi)
+      : "r"(x), "r"(w), "f"(c_lo), "f"(c_hi));
+}
+
+template <typename T, int CPT>
+struct ColOps16Packed {
+  static constexpr int kCpt = CPT;      // 4 or 8 channels
+  static constexpr int kOps = CPT / 2;  // packed pairs
+  using Op = uint32_t;
+  static constexpr int kWeightBytes = 2;
+  __device__ __forceinline__ static void load_x(uint32_t addr, Op (&v)[kOps]) {
+    if constexpr (CPT == 8) {
+      lds128a(addr, v);
+    } else {
+      lds64(addr, v);
+    }
+  }
+  __device__ __forceinline__ static void load_w(uint32_t addr, Op (&v)[kOps]) { load_x(addr, v); }
+  __device__ __forceinline__ static void stage_w(uint8_t* dst, T v) { *reinterpret_cast<T*>(dst) = v; }
+  __device__ __forceinline__ static void mac(float (&d)[kCpt], const Op (&x)[kOps], const Op (&w)[kOps],
+                                             const float (&c)[kCpt]) {
+#pragma unroll
+    for (int i = 0; i < kOps; ++i) mixed_fma_pair<T>(x[i], w[i], c[2 * i], c[2 * i + 1], d[2 * i], d[2 * i + 1]);
+  }
+};
+
+template <typename T, int FORM>
+using ColOps = typename std::conditional<
+    FORM == kColWide, ColOpsWide<T>,
+    typename std::conditional<
+        std::is_same<T, float>::value, ColOpsF32,
+        typename std::conditional<
+            FORM == kColPacked8, ColOps16Packed<T, 8>,
+            typename std::conditional<FORM == kColPacked, ColOps16Packed<T, 4>,
+                                      ColOps16Split<T>>::type>::type>::type>::type;
+
+// Channels per thread of a (storage type, form) pair, for the host planner.
+inline int col_cpt(int es, int form) { return (es == 2 && form == kColPacked8) ? 8 : 4; }
+
+// Kc for one thread's CPT outputs: round to T, one vector store.
+template <typename T, int CPT>
+__device__ __forceinline__ void col_store(T* dst, const float (&acc)[CPT]) {
+  if constexpr (std::is_same<T, float>::value) {
+    static_assert(CPT == 4, "fp32 stores 4 channels");
+    *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  } else {
+    uint32_t wd[CPT / 2];
+#pragma unroll
+    for (int i = 0; i < CPT / 2; ++i) {
+      if constexpr (std::is_same<T, __half>::value) {
+        const __half2 h = __floats2half2_rn(acc[2 * i], acc[2 * i + 1]);
+        wd[i] = *reinterpret_cast<const uint32_t*>(&h);
+      } else {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        wd[i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+    }
+    if constexpr (CPT == 8) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    } else {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(wd[0], wd[1]);
+    }
+  }
+}
+
+// Shared-memory layout: [full mbarriers x4][empty mbarriers x4][weights
+// [9][C], at most 4 bytes per value][bias fp32 [C]] ... [stages, 1024-aligned].
+__host__ __device__ inline uint32_t col_fixed_smem_bytes(int C) { return 64u + 36u * (uint32_t)C + 4u * (uint32_t)C; }
+
+// One block of U input rows of the column: each row is read with three
+// shared loads (horizontal taps) and added into every live output row it sits
+// under.  Blocks of U rows keep the accumulator slot of each (row, filter
+// row) pair a compile-time constant: output row oh uses slot oh % NA, and
+// every block starts at an output row that is a multiple of NA.  Rows above
+// the tile (oh < 0) and below it (oh >= rows) are accumulated as well, into
+// slots no valid row holds at that moment, and are never stored, so the row
+// loop needs no bounds tests.
+template <typename T, int FORM, int S, int DL, int NA, int U, bool CHECK>
+__device__ __forceinline__ void col_block(uint32_t st, uint32_t row_pitch, uint32_t col_step, int r0, int Hh,
+                                          int nrows, bool store_ok, T* yb, int64_t y_row_step,
+                                          const typename ColOps<T, FORM>::Op (&wr)[3][3][ColOps<T, FORM>::kOps],
+                                          const float (&br)[ColOps<T, FORM>::kCpt],
+                                          float (&acc)[NA][ColOps<T, FORM>::kCpt]) {
+  using Ops = ColOps<T, FORM>;
+  using Op = typename Ops::Op;
+  constexpr int CPT = Ops::kCpt;
+  const int oh_base = r0 / S;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    bool used = false;
+#pragma unroll
+    for (int ky = 0; ky < 3; ++ky) used |= ((u - ky * DL) % S) == 0;
+    if (!used) continue;
+    if (CHECK && r0 + u >= Hh) break;
+    Op xv[3][Ops::kOps];
+    const uint32_t rb = st + (uint32_t)(r0 + u) * row_pitch;
+#pragma unroll
+    for (int kx = 0; kx < 3; ++kx) Ops::load_x(rb + (uint32_t)kx * col_step, xv[kx]);
+#pragma unroll
+    for (int ky = 0; ky < 3; ++ky) {
+      if (((u - ky * DL) % S) != 0) continue;
+      const int rel = (u - ky * DL) / S;  // output row - oh_base (exact)
+      const int slot = ((rel % NA) + NA) % NA;
+#pragma unroll
+      for (int kx = 0; kx < 3; ++kx) {
+        if (ky == 0 && kx == 0) {
+          Ops::mac(acc[slot], xv[kx], wr[ky][kx], br);  // the bias is the first addend
+        } else {
+          Ops::mac(acc[slot], xv[kx], wr[ky][kx], acc[slot]);
+        }
+      }
+      if (ky == 2) {
+        const int oh_l = oh_base + rel;
+        if (store_ok && (unsigned)oh_l < (unsigned)nrows) col_store<T, CPT>(yb + rel * y_row_step, acc[slot]);
+      }
+    }
+  }
+}
+
+template <typename T, int S, int DL, int FORM>
+__global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                  const DwArgs a) {
+  using Ops = ColOps<T, FORM>;
+  using Op = typename Ops::Op;
+  constexpr int CPT = Ops::kCpt;
+  constexpr int es = sizeof(T);
+  constexpr int NA = (2 * DL) / S + 1;  // live output rows
+  constexpr int U = NA * S;             // input rows per block
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kDwMaxStages;
+  uint8_t* w_s = smem + 64;
+  float* b_s = reinterpret_cast<float*>(smem + 64 + 36u * (uint32_t)a.C);
+  uint8_t* stage0 = smem + a.stage_off;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int ncons = (int)blockDim.x - 32;
+  const T* __restrict__ wg = static_cast<const T*>(a.w);
+  const T* __restrict__ bg = static_cast<const T*>(a.bias);
+  T* __restrict__ yg = static_cast<T*>(a.y);
+
+  if (tid == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], (uint32_t)(ncons / 32));
+    }
+    fence_mbar_init();
+    tma_prefetch_desc(&xmap);
+  }
+  // weights [c][tap] in global -> [tap][c] in shared; bias -> fp32
+  for (int i = tid; i < 9 * a.C; i += blockDim.x) {
+    const int t = i / a.C, ch = i - t * a.C;
+    Ops::stage_w(w_s + (size_t)i * Ops::kWeightBytes, wg[(int64_t)ch * 9 + t]);
+  }
+  for (int i = tid; i < a.C; i += blockDim.x) b_s[i] = bg != nullptr ? Elem<T>::to_f32(bg[i]) : 0.f;
+  __syncthreads();
+
+  const bool withhold = (a.test_flags & 1) && blockIdx.x == 0;
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      int k = 0;
+      bool failed = false;
+      for (;; ++k) {
+        const int64_t tile = blockIdx.x + (int64_t)k * gridDim.x;
+        if (tile >= a.num_tiles) break;
+        const int s = k % a.stages;
+        if (k >= a.stages &&
+            !mbar_wait(&empty[s], (uint32_t)(((k / a.stages) - 1) & 1), a.wait_limit_ns)) {
+          failed = true;
+          break;
+        }
+        if (withhold && k == 0) continue;
+        const TileCoord c = decode_tile(a, tile);
+        mbar_arrive_expect_tx(&full[s], a.stage_bytes);
+        tma_load_5d(stage0 + (size_t)s * a.stage_stride, &xmap, &full[s], c.ct * a.TC,
+                    c.tw * a.TW * S - a.pW, c.th * a.TH * S - a.pH, c.od * a.sD - a.pD, (int)c.n);
+      }
+      if (failed) report(a.status, kDevTimeout, 2);
+      for (int j = k > a.stages ? k - a.stages : 0; j < k; ++j) {
+        if (withhold && j == 0) continue;
+        mbar_wait(&full[j % a.stages], (uint32_t)((j / a.stages) & 1), a.wait_limit_ns);
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const int ctid = tid - 32;
+  const int NQ = a.TC / CPT;
+  const int q = ctid % NQ;
+  const int wl = ctid / NQ;
+  const bool active = wl < a.TW;
+  const uint32_t row_pitch = (uint32_t)(a.Wh * a.TC * es);
+  const uint32_t col_step = (uint32_t)(DL * a.TC * es);
+  const uint32_t lane_off = (uint32_t)(((wl * S) * a.TC + q * CPT) * es);
+  const int64_t y_row_step = (int64_t)a.Wo * a.C;
+  const int Hh = a.Hh;
+
+  for (int k = 0;; ++k) {
+    const int64_t tile = blockIdx.x + (int64_t)k * gridDim.x;
+    if (tile >= a.num_tiles) break;
+    const int s = k % a.stages;
+    const uint32_t parity = (uint32_t)((k / a.stages) & 1);
+    const TileCoord c = decode_tile(a, tile);
+
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait(&full[s], parity, a.wait_limit_ns);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (ok && lane != 0) ok = mbar_wait(&full[s], parity, a.wait_limit_ns);
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) report(a.status, kDevTimeout, 1);
+      return;
+    }
+
+    const int ch = c.ct * a.TC + q * CPT;
+    const int ow = c.tw * a.TW + wl;
+    if (active && ch < a.C) {
+      // this tile's weights and bias (a few shared loads per tile)
+      Op wr[3][3][Ops::kOps];
+      float br[CPT];
+#pragma unroll
+      for (int t = 0; t < 9; ++t)
+        Ops::load_w(smem_u32(w_s + ((size_t)t * a.C + ch) * Ops::kWeightBytes), wr[t / 3][t % 3]);
+#pragma unroll
+      for (int i = 0; i < CPT; i += 4) {
+        const float4 b4 = *reinterpret_cast<const float4*>(b_s + ch + i);
+        br[i] = b4.x, br[i + 1] = b4.y, br[i + 2] = b4.z, br[i + 3] = b4.w;
+      }
+      const int oh0 = c.th * a.TH;
+      const int nrows = min(a.TH, a.Ho - oh0);
+      const bool store_ok = ow < a.Wo;
+      T* yb = yg + ((((int64_t)c.n * a.Do + c.od) * a.Ho + oh0) * (int64_t)a.Wo + ow) * a.C + ch;
+      const uint32_t st = smem_u32(stage0 + (size_t)s * a.stage_stride) + lane_off;
+      float acc[NA][CPT];
+#pragma unroll
+      for (int i = 0; i < NA; ++i)
+#pragma unroll
+        for (int e = 0; e < CPT; ++e) acc[i][e] = 0.f;
+      int r0 = 0;
+      for (; r0 + U <= Hh; r0 += U, yb += NA * y_row_step)
+        col_block<T, FORM, S, DL, NA, U, false>(st, row_pitch, col_step, r0, Hh, nrows, store_ok, yb, y_row_step,
+                                                wr, br, acc);
+      if (r0 < Hh)
+        col_block<T, FORM, S, DL, NA, U, true>(st, row_pitch, col_step, r0, Hh, nrows, store_ok, yb, y_row_step,
+                                               wr, br, acc);
+    }
+
+    __syncwarp();  // this warp is done with stage s
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+}
+
+}  // namespace dw
+}  // namespace gconv

@@ -184,32 +184,41 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
   }
   // Weights of this group chunk as block-diagonal B_t[n][k], K-major core
   // matrices: byte offset ((((t*KS + ks)*2 + kc2)*Nn + n)*8 + e)*2 holds
-  // k = ks*16 + kc2*8 + e.
+  // k = ks*16 + kc2*8 + e, in sc sub-blocks (one per group chunk j), each
+  // [t][ks][kc2][n][8].  Zero-fill, then copy each group's weights into its
+  // diagonal block: 8 consecutive input channels of one (group, output
+  // channel, tap) are one 16-byte global load and one 16-byte shared store.
   {
-    // sc sub-blocks (one per group chunk j), each [t][ks][kc2][n][8]
-    const int per_tap = a.Kt * a.Nn;
-    const int per_chunk = a.ntaps * per_tap;
-    const int total = a.sc * per_chunk;
+    const int total = a.sc * a.ntaps * a.Kt * a.Nn;  // elements, a multiple of 8
+    uint4* B16 = reinterpret_cast<uint4*>(Bs);
+    for (int i = tid; i < total / 8; i += blockDim.x) B16[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
     T* B = reinterpret_cast<T*>(Bs);
-    for (int i = tid; i < total; i += blockDim.x) {
-      const int j = i / per_chunk;
-      int r = i - j * per_chunk;
-      const int t = r / per_tap;
-      r -= t * per_tap;
-      const int e = r & 7;
-      r >>= 3;
-      const int n = r % a.Nn;
-      r /= a.Nn;
-      const int kc2 = r & 1;
-      const int ks = r >> 1;
-      const int k = ks * 16 + kc2 * 8 + e;
-      const int gj = k / a.Cg, cc = k - gj * a.Cg;
-      const int gi = n / a.Kg, kk = n - gi * a.Kg;
-      const int gbase = g0 + j * a.m;
-      T v = Elem<T>::from_f32(0.f);
-      if (gi == gj)
-        v = wg[((int64_t)(gbase + gi) * a.Kg + kk) * a.taps_total * a.Cg + (int64_t)t * a.Cg + cc];
-      B[i] = v;
+    const bool vec = (a.Cg % 8) == 0 && (reinterpret_cast<uintptr_t>(wg) & 15) == 0;
+    const int per = vec ? a.Cg / 8 : a.Cg;  // pieces per (group, output channel, tap) row
+    const int rows = a.sc * a.m * a.Kg * a.ntaps;
+    for (int idx = tid; idx < rows * per; idx += blockDim.x) {
+      const int piece = idx % per;
+      int r = idx / per;
+      const int t = r % a.ntaps;
+      r /= a.ntaps;
+      const int kk = r % a.Kg;
+      r /= a.Kg;
+      const int gi = r % a.m;
+      const int j = r / a.m;
+      const int g = g0 + j * a.m + gi;
+      const int n = gi * a.Kg + kk;
+      const int64_t src = ((int64_t)g * a.Kg + kk) * a.taps_total * a.Cg + (int64_t)t * a.Cg;
+      const int tap_base = (j * a.ntaps + t) * a.KS;
+      if (vec) {
+        const int k = gi * a.Cg + piece * 8;
+        const int dst = (((tap_base + (k >> 4)) * 2 + ((k >> 3) & 1)) * a.Nn + n) * 8;
+        *reinterpret_cast<uint4*>(B + dst) = *reinterpret_cast<const uint4*>(wg + src + piece * 8);
+      } else {
+        const int k = gi * a.Cg + piece;
+        const int dst = (((tap_base + (k >> 4)) * 2 + ((k >> 3) & 1)) * a.Nn + n) * 8 + (k & 7);
+        B[dst] = wg[src + piece];
+      }
     }
     for (int i = tid; i < a.sc * a.Nn; i += blockDim.x)
       bias_s[i] = bg != nullptr ? Elem<T>::to_f32(bg[(int64_t)g0 * a.Kg + i]) : 0.f;

@@ -92,10 +92,22 @@ typedef struct gconv_options {
   int32_t test_flags;    /* bit 0: withhold the first input copy of CTA 0 so its
                             first wait cannot complete (timeout-path test)       */
   int32_t selected;      /* out: the gconv_kernel that was launched               */
-  int32_t tile[8];       /* tuning overrides, 0 = automatic; for the depthwise
-                            kernel: TH, TW, WB, stages, CTAs per SM, FMA form
-                            (1 = widen + fp32 FMA, 2 = mixed f16/bf16 FMA,
-                            3 = widen + packed fp32x2 FMA) */
+  int32_t tile[8];       /* tuning overrides, 0 = automatic.
+                            Depthwise kernel: [0] TH, [1] TW, [2] WB, [3] stages,
+                            [4] CTAs per SM, [5] FMA form (row-blocked form:
+                            1 = widen + fp32 FMA, 2 = mixed f16/bf16 FMA,
+                            3 = widen + packed fp32x2 FMA; column form: 1 =
+                            split 16-bit operands / scalar fp32, 2 = packed
+                            16-bit pairs with 4 channels per thread, 3 = widen
+                            + packed fp32x2 FMA, 4 = packed 16-bit pairs with 8
+                            channels per thread, 0 = 4 for 16-bit storage and
+                            1 for fp32), [6] form (1 =
+                            row-blocked, 2 = direct loads, 3 = column form; the
+                            automatic choice is the column form when the depth
+                            filter is 1, else the row-blocked form).
+                            Tensor-core kernel: [0] TH, [2] M tiles per CTA,
+                            [3] stages, [4] partial accumulators, [6] 1 = force
+                            16-byte chunk planes, [7] extra shared memory (KB). */
 } gconv_options;
 
 /*

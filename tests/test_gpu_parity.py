@@ -93,15 +93,46 @@ DW_EDGE = [
 ]
 
 
+# depthwise kernel forms (tuning override slot 6): 1 row-blocked, 2 direct
+# loads, 3 column form (the automatic choice for a depth filter of 1); slot 5
+# selects the column form's operands: 1 split, 2 packed x4, 3 widened fp32x2,
+# 4 packed x8 (the automatic choice for 16-bit storage)
+DW_FORMS = [(1, 0), (2, 0), (3, 0), (3, 1), (3, 2), (3, 3)]
+
+
+@pytest.mark.parametrize("form", DW_FORMS, ids=lambda f: f"form{f[0]}-{f[1]}")
 @pytest.mark.parametrize("case", DW_EDGE, ids=lambda c: "-".join(map(str, c)))
-def test_depthwise_edges(orc, case):
+def test_depthwise_edges(orc, case, form):
     N, C, H, W, s, p, d, dt = case
     wl = inputs.Workload("dw_edge", 7, DW_EDGE.index(case), 2, N, C, 1, 1, (1, H, W), (1, 3, 3),
                          (1, s, s), (0, p, p), (1, d, d), dt, True)
     x, w, b = inputs.make_inputs(wl)
-    y, sel = run_gpu(wl, x, w, b, force=B.KERNEL_DIRECT_DW)
+    y, sel = run_gpu(wl, x, w, b, force=B.KERNEL_DIRECT_DW, tile=[0, 0, 0, 0, 0, form[1], form[0]])
     assert sel == B.KERNEL_DIRECT_DW
     assert_close(y.double().numpy(), orc.forward(wl, x, w, b), dt, str(case))
+
+
+# column form with explicit tiles (TH, TW, stages, CTAs per SM): ragged row
+# and column tiles, one to three CTAs per SM, two to four stages.  Every tile
+# set fits the shared memory of its workload.
+COL_TILES = {
+    "mbv2_dw_s1_f16": [(5, 3, 2, 1), (1, 1, 2, 2), (7, 13, 3, 1), (14, 8, 2, 2), (3, 5, 4, 3), (56, 2, 2, 1)],
+    "mbv2_dw_s2_f16": [(5, 3, 2, 1), (1, 1, 2, 2), (7, 7, 2, 1), (3, 5, 2, 3), (28, 1, 2, 1)],
+    "sweep_g512_d2_s1_bf16": [(5, 3, 2, 1), (1, 1, 2, 2), (7, 8, 2, 1), (3, 2, 2, 3)],
+    "sweep_g512_d2_s2_bf16": [(5, 3, 2, 1), (1, 1, 2, 2), (3, 4, 2, 1), (2, 2, 2, 3), (14, 1, 2, 1)],
+}
+COL_CASES = [(n, t) for n, ts in COL_TILES.items() for t in ts]
+
+
+@pytest.mark.parametrize("name,tiles", COL_CASES, ids=lambda v: v if isinstance(v, str) else "-".join(map(str, v)))
+def test_depthwise_column_tiles(orc, name, tiles):
+    TH, TW, stages, ctas = tiles
+    wl = inputs.by_name(name).with_(N=2)
+    x, w, b = inputs.make_inputs(wl)
+    ref = orc.forward(wl, x, w, b)
+    y, sel = run_gpu(wl, x, w, b, force=B.KERNEL_DIRECT_DW, tile=[TH, TW, 0, stages, ctas, 0, 3])
+    assert sel == B.KERNEL_DIRECT_DW
+    assert_close(y.double().numpy(), ref, wl.dtype, f"{name} tiles {tiles}")
 
 
 def test_depthwise_3d(orc):
