@@ -104,6 +104,22 @@ __device__ __forceinline__ T epilogue_one(float acc, float bias) {
   return Elem<T>::from_f32(acc + bias);
 }
 
+// Two consecutive outputs packed into one word (low half = first channel):
+// the same round-to-nearest-even of (acc + bias) as epilogue_one, done by
+// one paired conversion.
+template <typename T>
+__device__ __forceinline__ uint32_t epilogue_pair(float a0, float a1, float b0, float b1);
+template <>
+__device__ __forceinline__ uint32_t epilogue_pair<__half>(float a0, float a1, float b0, float b1) {
+  const __half2 h = __floats2half2_rn(a0 + b0, a1 + b1);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t epilogue_pair<__nv_bfloat16>(float a0, float a1, float b0, float b1) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a0 + b0, a1 + b1);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // VEC consecutive outputs -> one aligned vector store (VEC * sizeof(T) bytes).
 template <typename T, int VEC>
 __device__ __forceinline__ void epilogue_store(T* dst, const float* acc, const float* bias) {

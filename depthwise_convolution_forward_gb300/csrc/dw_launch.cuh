@@ -121,10 +121,11 @@ inline bool make_plan(const Geometry& g, int es, const int* tile_override, int n
 
 // Operand form of the column kernel (override slot 5): 1 split 16-bit /
 // scalar fp32, 2 packed 16-bit x4, 3 widened fp32x2, 4 packed 16-bit x8;
-// automatic: packed x8 for 16-bit storage, scalar for fp32.
+// automatic: packed x4 for 16-bit storage (as fast as the others and the
+// fewest registers), scalar for fp32.
 inline int col_form(int es, const int* ov) {
   const int ov_form = ov ? ov[5] : 0;
-  int form = es == 2 ? kColPacked8 : kColSplit;
+  int form = es == 2 ? kColPacked : kColSplit;
   if (ov_form == 1) form = kColSplit;
   if (ov_form == 2 && es == 2) form = kColPacked;
   if (ov_form == 3) form = kColWide;

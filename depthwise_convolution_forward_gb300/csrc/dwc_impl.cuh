@@ -9,8 +9,8 @@
 //    haloed input box into a ring of shared-memory stages (zero fill at the
 //    borders is the convolution's zero padding).
 //  * Consumer thread f of the tile owns output column f / NQ and the CPT
-//    channels CPT (f % NQ) .. +CPT-1 (NQ = TC / CPT; CPT = 8 for 16-bit
-//    storage, 4 otherwise).  Consecutive lanes therefore read consecutive
+//    channels CPT (f % NQ) .. +CPT-1 (NQ = TC / CPT; CPT = 4, or 8 in the
+//    kColPacked8 form).  Consecutive lanes therefore read consecutive
 //    pieces of one shared-memory row (conflict-free), and every output row a
 //    warp stores is one contiguous run of global memory.
 //  * The thread walks the input rows of its column from top to bottom.  Each
@@ -31,6 +31,7 @@
 #pragma once
 
 #include <type_traits>
+#include <utility>
 
 #include "dw_impl.cuh"
 
@@ -39,9 +40,9 @@ namespace dw {
 
 
 // Operand forms of the multiply (tuning override slot 5):
-//  kColPacked8  16-bit storage, 8 channels per thread, pairs kept packed in
+//  kColPacked   16-bit storage, 4 channels per thread, pairs kept packed in
 //               registers (the default for 16-bit storage);
-//  kColPacked   the same with 4 channels per thread;
+//  kColPacked8  the same with 8 channels per thread;
 //  kColSplit    16-bit storage, 4 channels, every 16-bit value in the low half
 //               of its own register (weights staged split, the high half of
 //               an input word shifted down once per load); fp32 storage:
@@ -254,58 +255,107 @@ __device__ __forceinline__ void col_store(T* dst, const float (&acc)[CPT]) {
   }
 }
 
-// Shared-memory layout: [full mbarriers x4][empty mbarriers x4][weights
-// [9][C], at most 4 bytes per value][bias fp32 [C]] ... [stages, 1024-aligned].
-__host__ __device__ inline uint32_t col_fixed_smem_bytes(int C) { return 64u + 36u * (uint32_t)C + 4u * (uint32_t)C; }
+// Per-stage tile header, written by the producer before it arms the stage's
+// barrier: the output element index of the tile origin (n, od, oh0, ow0, c0)
+// and the tile's first output row, rows, first column and first channel.
+struct ColTile {
+  int64_t y_base;
+  int oh0, nrows, ow0, c0;
+  int pad[2];
+};
+static_assert(sizeof(ColTile) == 32, "tile header is 32 bytes");
 
-// One block of U input rows of the column: each row is read with three
-// shared loads (horizontal taps) and added into every live output row it sits
-// under.  Blocks of U rows keep the accumulator slot of each (row, filter
-// row) pair a compile-time constant: output row oh uses slot oh % NA, and
-// every block starts at an output row that is a multiple of NA.  Rows above
-// the tile (oh < 0) and below it (oh >= rows) are accumulated as well, into
-// slots no valid row holds at that moment, and are never stored, so the row
-// loop needs no bounds tests.
-template <typename T, int FORM, int S, int DL, int NA, int U, bool CHECK>
-__device__ __forceinline__ void col_block(uint32_t st, uint32_t row_pitch, uint32_t col_step, int r0, int Hh,
-                                          int nrows, bool store_ok, T* yb, int64_t y_row_step,
-                                          const typename ColOps<T, FORM>::Op (&wr)[3][3][ColOps<T, FORM>::kOps],
-                                          const float (&br)[ColOps<T, FORM>::kCpt],
-                                          float (&acc)[NA][ColOps<T, FORM>::kCpt]) {
+// Shared-memory layout: [full mbarriers x4][empty mbarriers x4][tile headers
+// x4][weights [9][C], at most 4 bytes per value][bias fp32 [C]] ... [stages,
+// 1024-aligned].
+constexpr uint32_t kColHeaderOff = 64;
+constexpr uint32_t kColWeightOff = kColHeaderOff + 32u * kDwMaxStages;
+__host__ __device__ inline uint32_t col_fixed_smem_bytes(int C) {
+  return kColWeightOff + 36u * (uint32_t)C + 4u * (uint32_t)C;
+}
+
+// Column state shared by the per-row steps: shared-memory address of the
+// thread's piece in row 0 of the stage, strides, the store window and the
+// register-resident weights, bias and live accumulators.
+template <typename T, int FORM, int NA>
+struct ColState {
   using Ops = ColOps<T, FORM>;
-  using Op = typename Ops::Op;
-  constexpr int CPT = Ops::kCpt;
-  const int oh_base = r0 / S;
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    bool used = false;
-#pragma unroll
-    for (int ky = 0; ky < 3; ++ky) used |= ((u - ky * DL) % S) == 0;
-    if (!used) continue;
-    if (CHECK && r0 + u >= Hh) break;
-    Op xv[3][Ops::kOps];
-    const uint32_t rb = st + (uint32_t)(r0 + u) * row_pitch;
-#pragma unroll
-    for (int kx = 0; kx < 3; ++kx) Ops::load_x(rb + (uint32_t)kx * col_step, xv[kx]);
-#pragma unroll
-    for (int ky = 0; ky < 3; ++ky) {
-      if (((u - ky * DL) % S) != 0) continue;
-      const int rel = (u - ky * DL) / S;  // output row - oh_base (exact)
-      const int slot = ((rel % NA) + NA) % NA;
-#pragma unroll
-      for (int kx = 0; kx < 3; ++kx) {
-        if (ky == 0 && kx == 0) {
-          Ops::mac(acc[slot], xv[kx], wr[ky][kx], br);  // the bias is the first addend
-        } else {
-          Ops::mac(acc[slot], xv[kx], wr[ky][kx], acc[slot]);
-        }
-      }
-      if (ky == 2) {
-        const int oh_l = oh_base + rel;
-        if (store_ok && (unsigned)oh_l < (unsigned)nrows) col_store<T, CPT>(yb + rel * y_row_step, acc[slot]);
-      }
+  uint32_t st, row_pitch, col_step;
+  int nrows;
+  bool store_ok;
+  int64_t y_row_step;
+  const typename Ops::Op (&wr)[3][3][Ops::kOps];
+  const float (&br)[Ops::kCpt];
+  float (&acc)[NA][Ops::kCpt];
+};
+
+// Filter row ky of input row u (u = row index within its block) lands on
+// output row (u - ky*DL) / S of the block when the division is exact.
+template <int S, int DL>
+__host__ __device__ constexpr bool col_hits(int u, int ky) { return ((u - ky * DL) % S) == 0; }
+template <int S, int DL>
+__host__ __device__ constexpr bool col_row_used(int u) {
+  return col_hits<S, DL>(u, 0) || col_hits<S, DL>(u, 1) || col_hits<S, DL>(u, 2);
+}
+
+// Add input row xv into the output row it sits under with filter row KY;
+// the slot (output row mod NA) is a compile-time constant.  Output rows
+// above the tile (oh < 0) or below it (oh >= rows) are accumulated like any
+// other, into slots no valid row holds at that moment, and never stored, so
+// the row walk needs no bounds tests.
+template <typename T, int FORM, int S, int DL, int NA, int U_, int KY>
+__device__ __forceinline__ void col_tap_row(ColState<T, FORM, NA>& c, const typename ColOps<T, FORM>::Op (&xv)[3][ColOps<T, FORM>::kOps],
+                                            int oh_base, T* yb) {
+  using Ops = ColOps<T, FORM>;
+  if constexpr (col_hits<S, DL>(U_, KY)) {
+    constexpr int rel = (U_ - KY * DL) / S;  // output row - oh_base (exact)
+    constexpr int slot = ((rel % NA) + NA) % NA;
+    if constexpr (KY == 0) {
+      Ops::mac(c.acc[slot], xv[0], c.wr[KY][0], c.br);  // the bias is the first addend
+    } else {
+      Ops::mac(c.acc[slot], xv[0], c.wr[KY][0], c.acc[slot]);
+    }
+    Ops::mac(c.acc[slot], xv[1], c.wr[KY][1], c.acc[slot]);
+    Ops::mac(c.acc[slot], xv[2], c.wr[KY][2], c.acc[slot]);
+    if constexpr (KY == 2) {
+      const int oh_l = oh_base + rel;
+      if (c.store_ok && (unsigned)oh_l < (unsigned)c.nrows)
+        col_store<T, Ops::kCpt>(yb + rel * c.y_row_step, c.acc[slot]);
     }
   }
+}
+
+// Input row r0 + U_ of the column: three shared loads (horizontal taps), then
+// the filter rows it sits under.  Returns false (and does nothing) past the
+// last halo row when CHECK is set.
+template <typename T, int FORM, int S, int DL, int NA, bool CHECK, int U_>
+__device__ __forceinline__ bool col_row(ColState<T, FORM, NA>& c, int r0, int Hh, int oh_base, T* yb) {
+  using Ops = ColOps<T, FORM>;
+  if constexpr (!col_row_used<S, DL>(U_)) {
+    return true;
+  } else {
+    if (CHECK && r0 + U_ >= Hh) return false;
+    typename Ops::Op xv[3][Ops::kOps];
+    const uint32_t rb = c.st + (uint32_t)(r0 + U_) * c.row_pitch;
+    Ops::load_x(rb, xv[0]);
+    Ops::load_x(rb + c.col_step, xv[1]);
+    Ops::load_x(rb + 2 * c.col_step, xv[2]);
+    col_tap_row<T, FORM, S, DL, NA, U_, 0>(c, xv, oh_base, yb);
+    col_tap_row<T, FORM, S, DL, NA, U_, 1>(c, xv, oh_base, yb);
+    col_tap_row<T, FORM, S, DL, NA, U_, 2>(c, xv, oh_base, yb);
+    return true;
+  }
+}
+
+// One block of U input rows starting at r0 (a multiple of U, so every block
+// starts at an output row that is a multiple of NA and the accumulator slot
+// of each (row, filter row) pair is the same in every block).  Expanded at
+// compile time over the U rows.
+template <typename T, int FORM, int S, int DL, int NA, bool CHECK, int... Us>
+__device__ __forceinline__ void col_block(ColState<T, FORM, NA>& c, int r0, int Hh, T* yb,
+                                          std::integer_sequence<int, Us...>) {
+  const int oh_base = r0 / S;
+  (void)(col_row<T, FORM, S, DL, NA, CHECK, Us>(c, r0, Hh, oh_base, yb) && ...);
 }
 
 template <typename T, int S, int DL, int FORM>
@@ -320,8 +370,9 @@ __global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __g
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kDwMaxStages;
-  uint8_t* w_s = smem + 64;
-  float* b_s = reinterpret_cast<float*>(smem + 64 + 36u * (uint32_t)a.C);
+  ColTile* hdr = reinterpret_cast<ColTile*>(smem + kColHeaderOff);
+  uint8_t* w_s = smem + kColWeightOff;
+  float* b_s = reinterpret_cast<float*>(smem + kColWeightOff + 36u * (uint32_t)a.C);
   uint8_t* stage0 = smem + a.stage_off;
 
   const int tid = threadIdx.x;
@@ -339,34 +390,37 @@ __global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __g
     fence_mbar_init();
     tma_prefetch_desc(&xmap);
   }
-  // weights [c][tap] in global -> [tap][c] in shared; bias -> fp32
-  for (int i = tid; i < 9 * a.C; i += blockDim.x) {
-    const int t = i / a.C, ch = i - t * a.C;
-    Ops::stage_w(w_s + (size_t)i * Ops::kWeightBytes, wg[(int64_t)ch * 9 + t]);
-  }
-  for (int i = tid; i < a.C; i += blockDim.x) b_s[i] = bg != nullptr ? Elem<T>::to_f32(bg[i]) : 0.f;
   __syncthreads();
 
   const bool withhold = (a.test_flags & 1) && blockIdx.x == 0;
   if (warp == 0) {
     // ---------------- producer ----------------
+    // Starts copying at once; the consumers stage the weights meanwhile.
     if (lane == 0) {
-      int k = 0;
+      int k = 0, s = 0;
       bool failed = false;
       for (;; ++k) {
         const int64_t tile = blockIdx.x + (int64_t)k * gridDim.x;
         if (tile >= a.num_tiles) break;
-        const int s = k % a.stages;
         if (k >= a.stages &&
             !mbar_wait(&empty[s], (uint32_t)(((k / a.stages) - 1) & 1), a.wait_limit_ns)) {
           failed = true;
           break;
         }
-        if (withhold && k == 0) continue;
-        const TileCoord c = decode_tile(a, tile);
-        mbar_arrive_expect_tx(&full[s], a.stage_bytes);
-        tma_load_5d(stage0 + (size_t)s * a.stage_stride, &xmap, &full[s], c.ct * a.TC,
-                    c.tw * a.TW * S - a.pW, c.th * a.TH * S - a.pH, c.od * a.sD - a.pD, (int)c.n);
+        if (!(withhold && k == 0)) {
+          const TileCoord c = decode_tile(a, tile);
+          ColTile h;
+          h.oh0 = c.th * a.TH;
+          h.nrows = min(a.TH, a.Ho - h.oh0);
+          h.ow0 = c.tw * a.TW;
+          h.c0 = c.ct * a.TC;
+          h.y_base = ((((int64_t)c.n * a.Do + c.od) * a.Ho + h.oh0) * (int64_t)a.Wo + h.ow0) * a.C + h.c0;
+          hdr[s] = h;  // published to the consumers by the barrier arrive below
+          mbar_arrive_expect_tx(&full[s], a.stage_bytes);
+          tma_load_5d(stage0 + (size_t)s * a.stage_stride, &xmap, &full[s], h.c0, h.ow0 * S - a.pW,
+                      h.oh0 * S - a.pH, c.od * a.sD - a.pD, (int)c.n);
+        }
+        if (++s == a.stages) s = 0;
       }
       if (failed) report(a.status, kDevTimeout, 2);
       for (int j = k > a.stages ? k - a.stages : 0; j < k; ++j) {
@@ -379,6 +433,15 @@ __global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __g
 
   // ---------------- consumers ----------------
   const int ctid = tid - 32;
+  // weights [c][tap] in global -> [tap][c] in shared; bias -> fp32 (consumer
+  // warps only, while the first copies are in flight)
+  for (int i = ctid; i < 9 * a.C; i += ncons) {
+    const int t = i / a.C, ch = i - t * a.C;
+    Ops::stage_w(w_s + (size_t)i * Ops::kWeightBytes, wg[(int64_t)ch * 9 + t]);
+  }
+  for (int i = ctid; i < a.C; i += ncons) b_s[i] = bg != nullptr ? Elem<T>::to_f32(bg[i]) : 0.f;
+  asm volatile("bar.sync 1, %0;" ::"r"(ncons) : "memory");
+
   const int NQ = a.TC / CPT;
   const int q = ctid % NQ;
   const int wl = ctid / NQ;
@@ -387,14 +450,17 @@ __global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __g
   const uint32_t col_step = (uint32_t)(DL * a.TC * es);
   const uint32_t lane_off = (uint32_t)(((wl * S) * a.TC + q * CPT) * es);
   const int64_t y_row_step = (int64_t)a.Wo * a.C;
+  const int64_t thread_off = (int64_t)wl * a.C + q * CPT;
   const int Hh = a.Hh;
 
+  Op wr[3][3][Ops::kOps];
+  float br[CPT];
+  int cur_c0 = -1;
+  int s = 0;
+  uint32_t parity = 0;
   for (int k = 0;; ++k) {
     const int64_t tile = blockIdx.x + (int64_t)k * gridDim.x;
     if (tile >= a.num_tiles) break;
-    const int s = k % a.stages;
-    const uint32_t parity = (uint32_t)((k / a.stages) & 1);
-    const TileCoord c = decode_tile(a, tile);
 
     bool ok = true;
     if (lane == 0) ok = mbar_wait(&full[s], parity, a.wait_limit_ns);
@@ -405,41 +471,41 @@ __global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __g
       return;
     }
 
-    const int ch = c.ct * a.TC + q * CPT;
-    const int ow = c.tw * a.TW + wl;
+    const ColTile h = hdr[s];
+    const int ch = h.c0 + q * CPT;
     if (active && ch < a.C) {
-      // this tile's weights and bias (a few shared loads per tile)
-      Op wr[3][3][Ops::kOps];
-      float br[CPT];
+      if (h.c0 != cur_c0) {  // weights and bias of this channel tile
+        cur_c0 = h.c0;
 #pragma unroll
-      for (int t = 0; t < 9; ++t)
-        Ops::load_w(smem_u32(w_s + ((size_t)t * a.C + ch) * Ops::kWeightBytes), wr[t / 3][t % 3]);
+        for (int t = 0; t < 9; ++t)
+          Ops::load_w(smem_u32(w_s + ((size_t)t * a.C + ch) * Ops::kWeightBytes), wr[t / 3][t % 3]);
 #pragma unroll
-      for (int i = 0; i < CPT; i += 4) {
-        const float4 b4 = *reinterpret_cast<const float4*>(b_s + ch + i);
-        br[i] = b4.x, br[i + 1] = b4.y, br[i + 2] = b4.z, br[i + 3] = b4.w;
+        for (int i = 0; i < CPT; i += 4) {
+          const float4 b4 = *reinterpret_cast<const float4*>(b_s + ch + i);
+          br[i] = b4.x, br[i + 1] = b4.y, br[i + 2] = b4.z, br[i + 3] = b4.w;
+        }
       }
-      const int oh0 = c.th * a.TH;
-      const int nrows = min(a.TH, a.Ho - oh0);
-      const bool store_ok = ow < a.Wo;
-      T* yb = yg + ((((int64_t)c.n * a.Do + c.od) * a.Ho + oh0) * (int64_t)a.Wo + ow) * a.C + ch;
+      const bool store_ok = h.ow0 + wl < a.Wo;
+      T* yb = yg + h.y_base + thread_off;
       const uint32_t st = smem_u32(stage0 + (size_t)s * a.stage_stride) + lane_off;
       float acc[NA][CPT];
 #pragma unroll
       for (int i = 0; i < NA; ++i)
 #pragma unroll
         for (int e = 0; e < CPT; ++e) acc[i][e] = 0.f;
+      ColState<T, FORM, NA> cs{st, row_pitch, col_step, h.nrows, store_ok, y_row_step, wr, br, acc};
       int r0 = 0;
       for (; r0 + U <= Hh; r0 += U, yb += NA * y_row_step)
-        col_block<T, FORM, S, DL, NA, U, false>(st, row_pitch, col_step, r0, Hh, nrows, store_ok, yb, y_row_step,
-                                                wr, br, acc);
-      if (r0 < Hh)
-        col_block<T, FORM, S, DL, NA, U, true>(st, row_pitch, col_step, r0, Hh, nrows, store_ok, yb, y_row_step,
-                                               wr, br, acc);
+        col_block<T, FORM, S, DL, NA, false>(cs, r0, Hh, yb, std::make_integer_sequence<int, U>{});
+      if (r0 < Hh) col_block<T, FORM, S, DL, NA, true>(cs, r0, Hh, yb, std::make_integer_sequence<int, U>{});
     }
 
     __syncwarp();  // this warp is done with stage s
     if (lane == 0) mbar_arrive(&empty[s]);
+    if (++s == a.stages) {
+      s = 0;
+      parity ^= 1u;
+    }
   }
 }
 

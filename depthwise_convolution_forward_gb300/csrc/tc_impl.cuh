@@ -97,12 +97,24 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
   return __all_sync(0xffffffffu, ok);
 }
 
+// Kc for 16 consecutive channels: bias add, round to T, one 32-byte store
+// (a whole sector per lane).  dst must be 32-byte aligned.
+template <typename T>
+__device__ __forceinline__ void epilogue_store32(T* dst, const float* v, const float* bias) {
+  uint32_t wd[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) wd[i] = epilogue_pair<T>(v[2 * i], v[2 * i + 1], bias[2 * i], bias[2 * i + 1]);
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(wd[0]), "r"(wd[1]),
+               "r"(wd[2]), "r"(wd[3]), "r"(wd[4]), "r"(wd[5]), "r"(wd[6]), "r"(wd[7])
+               : "memory");
+}
+
 // Epilogue for one output row of a tile: per batch, load 4 / NP chunks of 16
 // channels from each of the NP partial accumulators (at most 4 loads in
 // flight, one wait), sum the partials, add bias, round, store.
 template <typename T, int NP>
 __device__ __forceinline__ void epilogue_row(uint32_t lane_base, int mt, int G2, int sc, int Nn, bool valid, T* dst,
-                                             const float* bias_s) {
+                                             const float* bias_s, bool v8) {
   constexpr int kPer = 4 / NP;
   const int nchunk16 = sc * Nn / 16;
   for (int c = 0; c < nchunk16; c += kPer) {
@@ -131,8 +143,12 @@ __device__ __forceinline__ void epilogue_row(uint32_t lane_base, int mt, int G2,
             for (int p = 1; p < NP; ++p) sum += __uint_as_float(r[b][p][e]);
             v[e] = sum;
           }
-          epilogue_store<T, 8>(dst + cc * 16, v, bias_s + cc * 16);
-          epilogue_store<T, 8>(dst + cc * 16 + 8, v + 8, bias_s + cc * 16 + 8);
+          if (v8) {
+            epilogue_store32<T>(dst + cc * 16, v, bias_s + cc * 16);
+          } else {
+            epilogue_store<T, 8>(dst + cc * 16, v, bias_s + cc * 16);
+            epilogue_store<T, 8>(dst + cc * 16 + 8, v + 8, bias_s + cc * 16 + 8);
+          }
         }
       }
     }
@@ -144,7 +160,8 @@ __device__ __forceinline__ void epilogue_row(uint32_t lane_base, int mt, int G2,
 // channels per pixel (128-byte rows, 128-byte swizzle) covering `sc` group
 // chunks, one TMA box per phase; each chunk is a K-offset inside the row.
 template <typename T, bool SW>
-__global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                        const __grid_constant__ TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* a_full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* a_empty = a_full + kMaxStages;
@@ -182,100 +199,119 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     tmem_alloc(tmem_slot, a.tmem_cols);
     tmem_relinquish();
   }
-  // Weights of this group chunk as block-diagonal B_t[n][k], K-major core
-  // matrices: byte offset ((((t*KS + ks)*2 + kc2)*Nn + n)*8 + e)*2 holds
-  // k = ks*16 + kc2*8 + e, in sc sub-blocks (one per group chunk j), each
-  // [t][ks][kc2][n][8].  Zero-fill, then copy each group's weights into its
-  // diagonal block: 8 consecutive input channels of one (group, output
-  // channel, tap) are one 16-byte global load and one 16-byte shared store.
-  {
-    const int total = a.sc * a.ntaps * a.Kt * a.Nn;  // elements, a multiple of 8
-    uint4* B16 = reinterpret_cast<uint4*>(Bs);
-    for (int i = tid; i < total / 8; i += blockDim.x) B16[i] = make_uint4(0u, 0u, 0u, 0u);
-    __syncthreads();
-    T* B = reinterpret_cast<T*>(Bs);
-    const bool vec = (a.Cg % 8) == 0 && (reinterpret_cast<uintptr_t>(wg) & 15) == 0;
-    const int per = vec ? a.Cg / 8 : a.Cg;  // pieces per (group, output channel, tap) row
-    const int rows = a.sc * a.m * a.Kg * a.ntaps;
-    for (int idx = tid; idx < rows * per; idx += blockDim.x) {
-      const int piece = idx % per;
-      int r = idx / per;
-      const int t = r % a.ntaps;
-      r /= a.ntaps;
-      const int kk = r % a.Kg;
-      r /= a.Kg;
-      const int gi = r % a.m;
-      const int j = r / a.m;
-      const int g = g0 + j * a.m + gi;
-      const int n = gi * a.Kg + kk;
-      const int64_t src = ((int64_t)g * a.Kg + kk) * a.taps_total * a.Cg + (int64_t)t * a.Cg;
-      const int tap_base = (j * a.ntaps + t) * a.KS;
-      if (vec) {
-        const int k = gi * a.Cg + piece * 8;
-        const int dst = (((tap_base + (k >> 4)) * 2 + ((k >> 3) & 1)) * a.Nn + n) * 8;
-        *reinterpret_cast<uint4*>(B + dst) = *reinterpret_cast<const uint4*>(wg + src + piece * 8);
-      } else {
-        const int k = gi * a.Cg + piece;
-        const int dst = (((tap_base + (k >> 4)) * 2 + ((k >> 3) & 1)) * a.Nn + n) * 8 + (k & 7);
-        B[dst] = wg[src + piece];
-      }
-    }
-    for (int i = tid; i < a.sc * a.Nn; i += blockDim.x)
-      bias_s[i] = bg != nullptr ? Elem<T>::to_f32(bg[(int64_t)g0 * a.Kg + i]) : 0.f;
-  }
-  // Per-issuer MMA lists.  The tile's work is split into units u = grp * np
-  // + p (accumulator grp = mt * sc + j, partial p summing the taps t with
-  // t % np == p); issuer w owns units w, w + kIssuers, ...  Its list holds,
-  // in issue order (unit-local step s outer, its units inner, so consecutive
-  // MMAs write different accumulators), one 32-byte entry per MMA: A
-  // descriptor for stage 0, B descriptor, accumulator column, flags (bit 0:
-  // accumulate, bit 1: skip).  The issuing thread then only adds the stage
-  // offset, and can fetch entry i + 1 while MMA i issues.
-  {
-    uint4* tab = reinterpret_cast<uint4*>(smem + a.tab_off);
-    const int G2 = a.sc * a.nmt, NP = a.np;
-    const int units = G2 * NP;
-    const int steps = ((a.ntaps + NP - 1) / NP) * a.KS;
-    const uint32_t a_base = smem_u32(As), b_base = smem_u32(Bs);
-    const uint32_t lbo_b = (uint32_t)a.Nn * 16u;
-    int base = 0;
-    for (int w = 0; w < kIssuers; ++w) {
-      const int nu = units > w ? (units - w + kIssuers - 1) / kIssuers : 0;
-      const int len = steps * nu;
-      for (int i = tid; i < len; i += blockDim.x) {
-        const int st = i / nu, ui = i - st * nu;
-        const int u = w + kIssuers * ui;
-        const int grp = u / NP, p = u - grp * NP;
-        const int t = p + NP * (st / a.KS), ks = st % a.KS;
-        const int mt = grp / a.sc, j = grp - mt * a.sc;
-        uint4 e0 = make_uint4(0u, 0u, 0u, 0u), e1 = make_uint4(0u, 0u, 0u, 2u);  // default: skip
-        if (t < a.ntaps) {
-          uint64_t adesc;
-          if constexpr (SW) {
-            const uint32_t row = a_base + (uint32_t)a.tap_phase[t] * a.plane_stride +
-                                 (uint32_t)(mt * 128 + a.tap_off[t]) * 128u;
-            adesc = smem_desc_sw128(row + (uint32_t)(j * a.Kt * 2 + ks * 32));
-          } else {
-            const uint32_t plane0 = a_base + (uint32_t)(a.tap_phase[t] * a.nchunks) * a.plane_stride;
-            const uint32_t row0 = (uint32_t)(mt * 128 + a.tap_off[t]) * 16u;
-            adesc = smem_desc(plane0 + (uint32_t)(2 * ks) * a.plane_stride + row0, a.plane_stride, 128u);
-          }
-          const uint64_t bdesc = smem_desc(b_base + (uint32_t)(((j * a.ntaps + t) * a.KS + ks) * 2) * lbo_b, lbo_b, 128u);
-          e0 = make_uint4((uint32_t)adesc, (uint32_t)(adesc >> 32), (uint32_t)bdesc, (uint32_t)(bdesc >> 32));
-          e1 = make_uint4((uint32_t)((p * G2 + grp) * a.Nn), 0u, 0u, st == 0 ? 0u : 1u);
-        }
-        tab[2 * (base + i)] = e0;
-        tab[2 * (base + i) + 1] = e1;
-      }
-      base += len;
-    }
-  }
-  fence_proxy_async_smem();  // generic-proxy writes of B -> visible to the tensor core
   fence_before_sync();
-  __syncthreads();
+  __syncthreads();  // barriers initialised, tensor memory allocated
   fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   const bool withhold = (a.test_flags & 1) && blockIdx.x == 0;
+
+  if (warp != 0) {
+    // Warps 1.. stage the weights, bias and MMA lists while the producer
+    // (warp 0) already copies the first input tiles: the A stages do not
+    // depend on them.
+    const int btid = tid - 32, bthreads = (int)blockDim.x - 32;
+    // Weights of this group chunk as block-diagonal B_t[n][k], K-major core
+    // matrices: byte offset ((((t*KS + ks)*2 + kc2)*Nn + n)*8 + e)*2 holds
+    // k = ks*16 + kc2*8 + e, in sc sub-blocks (one per group chunk j), each
+    // [t][ks][kc2][n][8].  Walked in destination order (consecutive threads
+    // fill consecutive 16-byte chunks: no bank conflicts); each chunk's
+    // nonzero run (the input channels of output n's group) is one cp.async
+    // when it is 16, 8 or 4 bytes and aligned, and every thread issues all its
+    // copies before waiting once.  Chunks are zero-filled first when some
+    // run is shorter than a chunk (merged groups).
+    const int nchunk = a.sc * a.ntaps * a.KS * 2 * a.Nn;
+    const uintptr_t wa = reinterpret_cast<uintptr_t>(wg);
+    const bool full_runs = a.m == 1 && a.Cg % 8 == 0;
+    if (!full_runs) {
+      uint4* B16 = reinterpret_cast<uint4*>(Bs);
+      for (int i = btid; i < nchunk; i += bthreads) B16[i] = make_uint4(0u, 0u, 0u, 0u);
+      asm volatile("bar.sync 1, %0;" ::"r"(bthreads) : "memory");
+    }
+    T* B = reinterpret_cast<T*>(Bs);
+    for (int ci = btid; ci < nchunk; ci += bthreads) {
+      const int n = ci % a.Nn;
+      int r = ci / a.Nn;
+      const int kc2 = r & 1;
+      r >>= 1;
+      const int ks = r % a.KS;
+      r /= a.KS;
+      const int t = r % a.ntaps;
+      const int j = r / a.ntaps;
+      const int gi = n / a.Kg, kk = n - gi * a.Kg;
+      const int k0 = ks * 16 + kc2 * 8;
+      const int ka = max(k0, gi * a.Cg), kb = min(k0 + 8, (gi + 1) * a.Cg);
+      if (ka >= kb) continue;  // off the diagonal: zero
+      const T* src = wg + ((int64_t)(g0 + j * a.m + gi) * a.Kg + kk) * a.taps_total * a.Cg + (int64_t)t * a.Cg +
+                     (ka - gi * a.Cg);
+      T* dst = B + (size_t)ci * 8 + (ka - k0);
+      const int bytes = (kb - ka) * (int)sizeof(T);
+      const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
+      const uint32_t da = smem_u32(dst);
+      if (bytes == 16 && ((sa | da) & 15) == 0) {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(da), "l"(src) : "memory");
+      } else if (bytes == 8 && ((sa | da) & 7) == 0) {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(da), "l"(src) : "memory");
+      } else if (bytes == 4 && ((sa | da) & 3) == 0) {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(da), "l"(src) : "memory");
+      } else {
+        for (int e = 0; e < kb - ka; ++e) dst[e] = src[e];
+      }
+    }
+    (void)wa;
+    for (int i = btid; i < a.sc * a.Nn; i += bthreads)
+      bias_s[i] = bg != nullptr ? Elem<T>::to_f32(bg[(int64_t)g0 * a.Kg + i]) : 0.f;
+    // Per-issuer MMA lists.  The tile's work is split into units u = grp * np
+    // + p (accumulator grp = mt * sc + j, partial p summing the taps t with
+    // t % np == p); issuer w owns units w, w + kIssuers, ...  Its list holds,
+    // in issue order (unit-local step s outer, its units inner, so consecutive
+    // MMAs write different accumulators), one 32-byte entry per MMA: A
+    // descriptor for stage 0, B descriptor, accumulator column, flags (bit 0:
+    // accumulate, bit 1: skip).  The issuing thread then only adds the stage
+    // offset, and can fetch entry i + 1 while MMA i issues.
+    {
+      uint4* tab = reinterpret_cast<uint4*>(smem + a.tab_off);
+      const int G2 = a.sc * a.nmt, NP = a.np;
+      const int units = G2 * NP;
+      const int steps = ((a.ntaps + NP - 1) / NP) * a.KS;
+      const uint32_t a_base = smem_u32(As), b_base = smem_u32(Bs);
+      const uint32_t lbo_b = (uint32_t)a.Nn * 16u;
+      int base = 0;
+      for (int w = 0; w < kIssuers; ++w) {
+        const int nu = units > w ? (units - w + kIssuers - 1) / kIssuers : 0;
+        const int len = steps * nu;
+        for (int i = btid; i < len; i += bthreads) {
+          const int st = i / nu, ui = i - st * nu;
+          const int u = w + kIssuers * ui;
+          const int grp = u / NP, p = u - grp * NP;
+          const int t = p + NP * (st / a.KS), ks = st % a.KS;
+          const int mt = grp / a.sc, j = grp - mt * a.sc;
+          uint4 e0 = make_uint4(0u, 0u, 0u, 0u), e1 = make_uint4(0u, 0u, 0u, 2u);  // default: skip
+          if (t < a.ntaps) {
+            uint64_t adesc;
+            if constexpr (SW) {
+              const uint32_t row = a_base + (uint32_t)a.tap_phase[t] * a.plane_stride +
+                                   (uint32_t)(mt * 128 + a.tap_off[t]) * 128u;
+              adesc = smem_desc_sw128(row + (uint32_t)(j * a.Kt * 2 + ks * 32));
+            } else {
+              const uint32_t plane0 = a_base + (uint32_t)(a.tap_phase[t] * a.nchunks) * a.plane_stride;
+              const uint32_t row0 = (uint32_t)(mt * 128 + a.tap_off[t]) * 16u;
+              adesc = smem_desc(plane0 + (uint32_t)(2 * ks) * a.plane_stride + row0, a.plane_stride, 128u);
+            }
+            const uint64_t bdesc =
+                smem_desc(b_base + (uint32_t)(((j * a.ntaps + t) * a.KS + ks) * 2) * lbo_b, lbo_b, 128u);
+            e0 = make_uint4((uint32_t)adesc, (uint32_t)(adesc >> 32), (uint32_t)bdesc, (uint32_t)(bdesc >> 32));
+            e1 = make_uint4((uint32_t)((p * G2 + grp) * a.Nn), 0u, 0u, st == 0 ? 0u : 1u);
+          }
+          tab[2 * (base + i)] = e0;
+          tab[2 * (base + i) + 1] = e1;
+        }
+        base += len;
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    fence_proxy_async_smem();  // generic-proxy writes of B -> visible to the tensor core
+    asm volatile("bar.sync 1, %0;" ::"r"(bthreads) : "memory");
+  }
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -378,6 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     const int row = q * 32 + lane;
     const int G2 = a.sc * a.nmt;
     const int NP = a.np;
+    // 32-byte stores when every 16-channel piece starts on a 32-byte boundary
+    // (each chunk row's channel offset is a multiple of 16)
+    const bool v8 = (reinterpret_cast<uintptr_t>(yg) & 31) == 0 && (a.Ktot & 15) == 0;
     int k = 0;
     for (int sp = cta_in_gc; sp < a.spatial_tiles; sp += a.cpg, ++k) {
       const int ab = k & 1;
@@ -395,9 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         const bool valid = i < a.TH && jj < a.TWo && oh < a.Ho && ow < a.Wo;
         T* dst = yg + ((((int64_t)st.n * a.Do + st.od) * a.Ho + oh) * (int64_t)a.Wo + ow) * a.Ktot +
                  (int64_t)g0 * a.Kg;
-        if (NP == 1) epilogue_row<T, 1>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s);
-        else if (NP == 2) epilogue_row<T, 2>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s);
-        else epilogue_row<T, 4>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s);
+        if (NP == 1) epilogue_row<T, 1>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8);
+        else if (NP == 2) epilogue_row<T, 2>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8);
+        else epilogue_row<T, 4>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8);
       }
       fence_before_sync();
       __syncwarp();

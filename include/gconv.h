@@ -100,7 +100,7 @@ typedef struct gconv_options {
                             split 16-bit operands / scalar fp32, 2 = packed
                             16-bit pairs with 4 channels per thread, 3 = widen
                             + packed fp32x2 FMA, 4 = packed 16-bit pairs with 8
-                            channels per thread, 0 = 4 for 16-bit storage and
+                            channels per thread, 0 = 2 for 16-bit storage and
                             1 for fp32), [6] form (1 =
                             row-blocked, 2 = direct loads, 3 = column form; the
                             automatic choice is the column form when the depth
