@@ -152,6 +152,40 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     const uint32_t tab_bytes = entries * 32u;
     c.b_off = round_up(c.tab_off + tab_bytes, 1024);
     c.a_off = c.b_off + b_bytes;
+    c.ntab = 0;
+    if (entries <= (uint32_t)tc::kMaxTab) {
+      // The same lists the kernel would build, with shared-memory offsets
+      // instead of descriptors (the kernel adds its shared-memory base).
+      const int units = G2 * np, steps = ((taps + np - 1) / np) * c.KS;
+      const uint32_t lbo_b = (uint32_t)c.Nn * 16u;
+      int base = 0;
+      for (int w = 0; w < tc::kIssuers; ++w) {
+        const int nu = units > w ? (units - w + tc::kIssuers - 1) / tc::kIssuers : 0;
+        for (int i = 0; i < steps * nu; ++i) {
+          const int st = i / nu, ui = i - st * nu;
+          const int u = w + tc::kIssuers * ui;
+          const int grp = u / np, pp = u - grp * np;
+          const int t = pp + np * (st / c.KS), ks = st % c.KS;
+          const int mt = grp / c.sc, j = grp - mt * c.sc;
+          uint2 e = make_uint2(0u, 2u << 16);  // skip
+          if (t < taps) {
+            uint32_t aoff;
+            if (sw)
+              aoff = c.a_off + (uint32_t)c.tap_phase[t] * c.plane_stride + (uint32_t)(mt * 128 + c.tap_off[t]) * 128u +
+                     (uint32_t)(j * c.Kt * 2 + ks * 32);
+            else
+              aoff = c.a_off + (uint32_t)(c.tap_phase[t] * c.nchunks + 2 * ks) * c.plane_stride +
+                     (uint32_t)(mt * 128 + c.tap_off[t]) * 16u;
+            const uint32_t boff = c.b_off + (uint32_t)(((j * taps + t) * c.KS + ks) * 2) * lbo_b;
+            e = make_uint2((aoff >> 4) | ((boff >> 4) << 16),
+                           (uint32_t)((pp * G2 + grp) * c.Nn) | ((st == 0 ? 0u : 1u) << 16));
+          }
+          c.tab[base + i] = e;
+        }
+        base += steps * nu;
+      }
+      c.ntab = (int)entries;
+    }
     int stages = (ov && ov[3]) ? ov[3] : tc::kMaxStages;
     stages = std::min(stages, tc::kMaxStages);
     while (stages > 2 && c.a_off + stages * c.a_stage_bytes > budget) --stages;

@@ -40,6 +40,7 @@ namespace tc {
 constexpr int kMaxTaps = 32;
 constexpr int kMaxPhases = 4;
 constexpr int kMaxStages = 4;
+constexpr int kMaxTab = 2048;                     // host-built MMA list entries
 constexpr int kIssuers = 4;                       // MMA-issuing warps
 constexpr int kThreads = 32 * (1 + kIssuers + 4);  // producer, issuers, epilogue
 
@@ -68,6 +69,13 @@ struct TcArgs {
   int* status;
   uint64_t wait_limit_ns;
   int test_flags;
+  // MMA lists computed on the host (ntab entries, issuer lists back to back),
+  // or ntab = 0 to build them in the kernel.  Entry: x = A start offset >> 4
+  // | B start offset >> 4 << 16 (bytes from the dynamic shared-memory base,
+  // stage 0), y = accumulator column | flags << 16 (bit 0 accumulate, bit 1
+  // skip).
+  int ntab;
+  uint2 tab[kMaxTab];
 };
 
 struct SpatialTile {
@@ -228,16 +236,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
       asm volatile("bar.sync 1, %0;" ::"r"(bthreads) : "memory");
     }
     T* B = reinterpret_cast<T*>(Bs);
+    // chunk index ci = (((j*ntaps + t)*KS + ks)*2 + kc2)*Nn + n, n = gi*Kg + kk,
+    // as mixed-radix digits advanced by bthreads with carries (no division
+    // per chunk)
+    const int rad[6] = {a.Kg, a.m, 2, a.KS, a.ntaps, a.sc};
+    int dig[6], inc[6];
+    {
+      int v = btid, w = bthreads;
+      for (int i = 0; i < 6; ++i) {
+        dig[i] = v % rad[i], v /= rad[i];
+        inc[i] = w % rad[i], w /= rad[i];
+      }
+    }
     for (int ci = btid; ci < nchunk; ci += bthreads) {
-      const int n = ci % a.Nn;
-      int r = ci / a.Nn;
-      const int kc2 = r & 1;
-      r >>= 1;
-      const int ks = r % a.KS;
-      r /= a.KS;
-      const int t = r % a.ntaps;
-      const int j = r / a.ntaps;
-      const int gi = n / a.Kg, kk = n - gi * a.Kg;
+      const int kk = dig[0], gi = dig[1], kc2 = dig[2], ks = dig[3], t = dig[4], j = dig[5];
+      {
+        int carry = 0;
+#pragma unroll
+        for (int i = 0; i < 6; ++i) {
+          dig[i] += inc[i] + carry;
+          carry = dig[i] >= rad[i];
+          if (carry) dig[i] -= rad[i];
+        }
+      }
       const int k0 = ks * 16 + kc2 * 8;
       const int ka = max(k0, gi * a.Cg), kb = min(k0 + 8, (gi + 1) * a.Cg);
       if (ka >= kb) continue;  // off the diagonal: zero
@@ -268,7 +289,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     // descriptor for stage 0, B descriptor, accumulator column, flags (bit 0:
     // accumulate, bit 1: skip).  The issuing thread then only adds the stage
     // offset, and can fetch entry i + 1 while MMA i issues.
-    {
+    if (a.ntab > 0) {
+      uint4* tab = reinterpret_cast<uint4*>(smem + a.tab_off);
+      const uint32_t base = smem_u32(smem);
+      const uint32_t lbo_b = (uint32_t)a.Nn * 16u;
+      for (int i = btid; i < a.ntab; i += bthreads) {
+        const uint2 e = a.tab[i];
+        uint4 e0 = make_uint4(0u, 0u, 0u, 0u);
+        if (!((e.y >> 16) & 2u)) {
+          const uint32_t aaddr = base + ((e.x & 0xffffu) << 4), baddr = base + ((e.x >> 16) << 4);
+          uint64_t adesc;
+          if constexpr (SW) {
+            adesc = smem_desc_sw128(aaddr);
+          } else {
+            adesc = smem_desc(aaddr, a.plane_stride, 128u);
+          }
+          const uint64_t bdesc = smem_desc(baddr, lbo_b, 128u);
+          e0 = make_uint4((uint32_t)adesc, (uint32_t)(adesc >> 32), (uint32_t)bdesc, (uint32_t)(bdesc >> 32));
+        }
+        tab[2 * i] = e0;
+        tab[2 * i + 1] = make_uint4(e.y & 0xffffu, 0u, 0u, e.y >> 16);
+      }
+    } else {
       uint4* tab = reinterpret_cast<uint4*>(smem + a.tab_off);
       const int G2 = a.sc * a.nmt, NP = a.np;
       const int units = G2 * NP;
