@@ -43,6 +43,8 @@ struct DwArgs {
   uint32_t stage_bytes;   // bytes one TMA box writes
   uint32_t stage_stride;  // bytes between stages (>= stage_bytes, 1024-aligned)
   uint32_t stage_off;     // offset of stage 0 in dynamic shared memory
+  int h0;                 // column form: halo rows in the first of two copies per tile (Hh: one copy)
+  uint32_t bytes0;        // bytes of the first copy (bytes of the second: stage_bytes - bytes0)
   int* status;
   uint64_t wait_limit_ns;
   int test_flags;
@@ -104,7 +106,8 @@ __host__ __device__ inline uint32_t fixed_smem_bytes(int Z, int C, int es, int m
 // stall the issuing thread for about a microsecond; on its own warp that stall
 // overlaps with the consumers' arithmetic.
 template <typename T, int K, int S, int DL, int WB, int MODE>
-__global__ void __launch_bounds__(WB >= 8 ? 288 : 512) dw_kernel(const __grid_constant__ CUtensorMap xmap,
+__global__ void __launch_bounds__(WB >= 8 ? 288 : 512) dw_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap,
+                                                                 const __grid_constant__ CUtensorMap,
                                                                  const DwArgs a) {
   constexpr int VEC = Elem<T>::kVec;
   constexpr int NCOL = (WB - 1) * S + (K - 1) * DL + 1;  // input columns per WB outputs

@@ -16,6 +16,7 @@ struct Plan {
   int TH, TW, TC, WB, stages, ctas_per_sm, mode;
   int direct;  // 1: direct-load variant (dw_ldg_kernel), 0: TMA-staged pipeline
   int col;     // 1: column form (dw_col_kernel)
+  int h0;      // column form: halo rows of a tile's first copy (Hh: one copy)
   int Dh, Hh, Wh;
   int tiles_c, tiles_w, tiles_h;
   int64_t num_tiles;
@@ -136,13 +137,18 @@ inline int col_form(int es, const int* ov) {
 // Column form (dw_col_kernel): depth filter 1 only.  Each consumer thread
 // owns one output column of the tile and CPT channels, so a tile is TW
 // columns x TC channels of threads and TH rows deep.  The plan minimises
-//   rounds x (per-tile row work) x max(1, resident warps / 16)
-// where rounds = ceil(tiles / resident CTAs).  A thread's rows run in
-// sequence, so a tile takes as long as one thread's rows (its output rows, a
-// share for loading halo rows and a fixed start-up); once more than about 16
-// consumer warps share an SM it is issue-bound and tiles slow down in
-// proportion.  Resident CTAs per SM are bounded by shared memory, threads and
-// the kernel's registers per thread (`regs`).
+//   rounds x (Hh + 4) x max(1, busiest scheduler's warps / 4)
+// with rounds = tiles / resident CTAs.  A thread walks the Hh input rows of
+// its column in sequence (each costs three loads and the taps it feeds), so
+// a tile takes about as long as Hh rows plus a fixed start-up.  Warps of a
+// CTA are dealt to the
+// SM's 4 schedulers in turn, so the busiest one holds ceil(consumer warps / 4)
+// per CTA; beyond about 4 warps a scheduler is issue-bound and its tiles slow
+// down in proportion (9 consumer warps per CTA measured slower than 8).  A
+// single CTA per SM has only its own stages to hide copy latency behind and
+// measured slower than two, so it costs 10% more.  Resident CTAs per SM are
+// bounded by shared memory, threads and the kernel's registers per thread
+// (`regs`).
 inline bool make_col_plan(const Geometry& g, int es, const int* ov, int num_sms, int form, int regs, Plan* out) {
   if (g.Z != 1) return false;
   const int S = g.sH, DL = g.dH;
@@ -181,9 +187,9 @@ inline bool make_col_plan(const Geometry& g, int es, const int* ov, int num_sms,
         const int tiles_h = ceil_div(g.Ho, TH);
         const int64_t tiles = (int64_t)tiles_c * tiles_w * tiles_h * g.Do * g.N;
         const int64_t slots = (int64_t)num_sms * ctas;
-        const double rounds = (double)((tiles + slots - 1) / slots);
-        const int resident = ctas * warps;
-        const double cost = rounds * (TH + 0.35 * Hh + 4.0) * std::max(1.0, resident / 16.0);
+        const double rounds = (double)tiles / (double)slots;
+        const int busiest = ctas * ((warps + 3) / 4);
+        const double cost = rounds * (Hh + 4.0) * std::max(1.0, busiest / 4.0) * (ctas == 1 ? 1.1 : 1.0);
         if (cost < best_cost) {
           best_cost = cost;
           best = Plan{};
@@ -204,6 +210,22 @@ inline bool make_col_plan(const Geometry& g, int es, const int* ov, int num_sms,
   if (best_cost >= 1e30) return false;
   best.col = 1;
   best.mode = form;
+  // Two copies per tile: the first ends at a multiple of the row block
+  // (U = NA*S rows) near the middle, with the second copy's shared-memory
+  // destination on a 128-byte boundary; otherwise one copy.
+  {
+    const int U = ((2 * DL) / S + 1) * S;
+    const uint32_t row_bytes = (uint32_t)best.Wh * best.TC * es;
+    best.h0 = best.Hh;
+    for (int h0 = best.Hh / 2 / U * U; h0 >= U; h0 -= U)
+      if (((uint32_t)h0 * row_bytes) % 128u == 0) {
+        best.h0 = h0;
+        break;
+      }
+    // The split measured slower than one copy (all CTAs' first copies compete
+    // for DRAM either way), so it is used only on request: override slot 2 = 2.
+    if (!(ov && ov[2] == 2)) best.h0 = best.Hh;
+  }
   best.smem_bytes = best.stage_off + best.stages * best.stage_stride;
   *out = best;
   return true;
@@ -217,7 +239,7 @@ inline CUtensorMapDataType tma_type() {
 }
 
 template <typename T>
-using DwKernel = void (*)(const CUtensorMap, const DwArgs);
+using DwKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const DwArgs);
 
 // The compiled variant for (stride, dilation, register block, FMA form).
 template <typename T>
@@ -361,10 +383,21 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   const uint64_t C = g.C();
   uint64_t dims[5] = {C, (uint64_t)g.W, (uint64_t)g.H, (uint64_t)g.D, (uint64_t)g.N};
   uint64_t strides[4] = {C * es, C * es * g.W, C * es * g.W * g.H, C * es * g.W * g.H * g.D};
+  const int h0 = p.col ? p.h0 : p.Hh;
   uint32_t box[5] = {(uint32_t)p.TC, (uint32_t)p.Wh, (uint32_t)p.Hh, (uint32_t)p.Dh, 1u};
   uint32_t estr[5] = {1, 1, 1, 1, 1};
   if (encode_tiled(&map, tma_type<T>(), 5, la.x, dims, strides, box, estr) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  // column form, a CTA's first tile in two copies: rows 0 .. h0-1, h0 .. Hh-1
+  CUtensorMap map0 = map, map1 = map;
+  if (h0 < p.Hh) {
+    box[2] = (uint32_t)h0;
+    if (encode_tiled(&map0, tma_type<T>(), 5, la.x, dims, strides, box, estr) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    box[2] = (uint32_t)(p.Hh - h0);
+    if (encode_tiled(&map1, tma_type<T>(), 5, la.x, dims, strides, box, estr) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
 
   DwArgs a{};
   a.x = la.x;
@@ -390,7 +423,9 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   const int64_t grid64 = std::min<int64_t>(p.num_tiles, (int64_t)dev.num_sms * p.ctas_per_sm);
   const int grid = (int)std::max<int64_t>(1, grid64);
   DwKernel<T> kern = p.col ? pick_col_kernel<T>(g.sH, g.dH, p.mode) : pick_kernel<T>(g.sH, g.dH, p.WB, p.mode);
-  kern<<<grid, p.threads, p.smem_bytes, la.stream>>>(map, a);
+  a.h0 = h0;
+  a.bytes0 = (uint32_t)h0 * p.Wh * p.TC * p.Dh * es;
+  kern<<<grid, p.threads, p.smem_bytes, la.stream>>>(map, map0, map1, a);
   return cudaGetLastError();
 }
 

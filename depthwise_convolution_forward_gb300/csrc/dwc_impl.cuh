@@ -5,9 +5,11 @@
 // Design (sm_103a):
 //  * Persistent CTAs walk a static list of output tiles
 //    (n, od, TH x TW output pixels, TC channels), as in the row-blocked
-//    form: warp 0 is the producer and issues one 5-D TMA copy of each tile's
-//    haloed input box into a ring of shared-memory stages (zero fill at the
-//    borders is the convolution's zero padding).
+//    form: warp 0 is the producer and copies each tile's haloed input box
+//    with 5-D TMA into a ring of shared-memory stages (zero fill at the
+//    borders is the convolution's zero padding).  On request a CTA's first
+//    box goes as two copies (top rows, then the rest) on two barriers, so the
+//    consumers can start on the top rows while the bottom rows arrive.
 //  * Consumer thread f of the tile owns output column f / NQ and the CPT
 //    channels CPT (f % NQ) .. +CPT-1 (NQ = TC / CPT; CPT = 4, or 8 in the
 //    kColPacked8 form).  Consecutive lanes therefore read consecutive
@@ -265,10 +267,10 @@ struct ColTile {
 };
 static_assert(sizeof(ColTile) == 32, "tile header is 32 bytes");
 
-// Shared-memory layout: [full mbarriers x4][empty mbarriers x4][tile headers
-// x4][weights [9][C], at most 4 bytes per value][bias fp32 [C]] ... [stages,
-// 1024-aligned].
-constexpr uint32_t kColHeaderOff = 64;
+// Shared-memory layout: [full mbarriers x4][empty mbarriers x4][second-copy
+// mbarriers x4][tile headers x4][weights [9][C], at most 4 bytes per
+// value][bias fp32 [C]] ... [stages, 1024-aligned].
+constexpr uint32_t kColHeaderOff = 128;  // after 3 x kDwMaxStages mbarriers (full, full1, empty)
 constexpr uint32_t kColWeightOff = kColHeaderOff + 32u * kDwMaxStages;
 __host__ __device__ inline uint32_t col_fixed_smem_bytes(int C) {
   return kColWeightOff + 36u * (uint32_t)C + 4u * (uint32_t)C;
@@ -360,6 +362,8 @@ __device__ __forceinline__ void col_block(ColState<T, FORM, NA>& c, int r0, int 
 
 template <typename T, int S, int DL, int FORM>
 __global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                  const __grid_constant__ CUtensorMap xmap0,
+                                                                  const __grid_constant__ CUtensorMap xmap1,
                                                                   const DwArgs a) {
   using Ops = ColOps<T, FORM>;
   using Op = typename Ops::Op;
@@ -370,6 +374,8 @@ __global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __g
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kDwMaxStages;
+  uint64_t* full1 = empty + kDwMaxStages;  // second copy of each tile
+  const bool split = a.h0 < a.Hh;
   ColTile* hdr = reinterpret_cast<ColTile*>(smem + kColHeaderOff);
   uint8_t* w_s = smem + kColWeightOff;
   float* b_s = reinterpret_cast<float*>(smem + kColWeightOff + 36u * (uint32_t)a.C);
@@ -385,10 +391,15 @@ __global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __g
   if (tid == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(&full[s], 1);
+      mbar_init(&full1[s], 1);
       mbar_init(&empty[s], (uint32_t)(ncons / 32));
     }
     fence_mbar_init();
     tma_prefetch_desc(&xmap);
+    if (split) {
+      tma_prefetch_desc(&xmap0);
+      tma_prefetch_desc(&xmap1);
+    }
   }
   __syncthreads();
 
@@ -407,6 +418,13 @@ __global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __g
           failed = true;
           break;
         }
+        // At launch every CTA requests its first tiles at once.  Holding the
+        // second copy until the first has landed lets the first tile arrive
+        // (and its computation start) sooner; later copies overlap compute.
+        if (k == 1 && !withhold && !mbar_wait(&full[0], 0u, a.wait_limit_ns)) {
+          failed = true;
+          break;
+        }
         if (!(withhold && k == 0)) {
           const TileCoord c = decode_tile(a, tile);
           ColTile h;
@@ -416,9 +434,17 @@ __global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __g
           h.c0 = c.ct * a.TC;
           h.y_base = ((((int64_t)c.n * a.Do + c.od) * a.Ho + h.oh0) * (int64_t)a.Wo + h.ow0) * a.C + h.c0;
           hdr[s] = h;  // published to the consumers by the barrier arrive below
-          mbar_arrive_expect_tx(&full[s], a.stage_bytes);
-          tma_load_5d(stage0 + (size_t)s * a.stage_stride, &xmap, &full[s], h.c0, h.ow0 * S - a.pW,
-                      h.oh0 * S - a.pH, c.od * a.sD - a.pD, (int)c.n);
+          uint8_t* dst = stage0 + (size_t)s * a.stage_stride;
+          const int iw = h.ow0 * S - a.pW, ih = h.oh0 * S - a.pH, id = c.od * a.sD - a.pD;
+          if (!(split && k == 0)) {
+            mbar_arrive_expect_tx(&full[s], a.stage_bytes);
+            tma_load_5d(dst, &xmap, &full[s], h.c0, iw, ih, id, (int)c.n);
+          } else {
+            mbar_arrive_expect_tx(&full[s], a.bytes0);
+            tma_load_5d(dst, &xmap0, &full[s], h.c0, iw, ih, id, (int)c.n);
+            mbar_arrive_expect_tx(&full1[s], a.stage_bytes - a.bytes0);
+            tma_load_5d(dst + a.bytes0, &xmap1, &full1[s], h.c0, iw, ih + a.h0, id, (int)c.n);
+          }
         }
         if (++s == a.stages) s = 0;
       }
@@ -426,6 +452,7 @@ __global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __g
       for (int j = k > a.stages ? k - a.stages : 0; j < k; ++j) {
         if (withhold && j == 0) continue;
         mbar_wait(&full[j % a.stages], (uint32_t)((j / a.stages) & 1), a.wait_limit_ns);
+        if (split && j == 0) mbar_wait(&full1[0], 0u, a.wait_limit_ns);
       }
     }
     return;
@@ -435,9 +462,22 @@ __global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __g
   const int ctid = tid - 32;
   // weights [c][tap] in global -> [tap][c] in shared; bias -> fp32 (consumer
   // warps only, while the first copies are in flight)
-  for (int i = ctid; i < 9 * a.C; i += ncons) {
-    const int t = i / a.C, ch = i - t * a.C;
-    Ops::stage_w(w_s + (size_t)i * Ops::kWeightBytes, wg[(int64_t)ch * 9 + t]);
+  // (global reads in source order: coalesced; four loads in flight per thread)
+  for (int i0 = ctid; i0 < 9 * a.C; i0 += 4 * ncons) {
+    T v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * ncons;
+      if (i < 9 * a.C) v[u] = wg[i];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * ncons;
+      if (i < 9 * a.C) {
+        const int ch = i / 9, t = i - ch * 9;
+        Ops::stage_w(w_s + ((size_t)t * a.C + ch) * Ops::kWeightBytes, v[u]);
+      }
+    }
   }
   for (int i = ctid; i < a.C; i += ncons) b_s[i] = bg != nullptr ? Elem<T>::to_f32(bg[i]) : 0.f;
   asm volatile("bar.sync 1, %0;" ::"r"(ncons) : "memory");
@@ -462,42 +502,65 @@ __global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __g
     const int64_t tile = blockIdx.x + (int64_t)k * gridDim.x;
     if (tile >= a.num_tiles) break;
 
-    bool ok = true;
-    if (lane == 0) ok = mbar_wait(&full[s], parity, a.wait_limit_ns);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (ok && lane != 0) ok = mbar_wait(&full[s], parity, a.wait_limit_ns);
-    if (!__all_sync(0xffffffffu, ok)) {
+    // Lane 0 polls; after the warp agrees, every lane observes the completed
+    // phase itself (acquire) before reading the stage.
+    auto warp_wait = [&](uint64_t* bar) {
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(bar, parity, a.wait_limit_ns);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (ok && lane != 0) ok = mbar_wait(bar, parity, a.wait_limit_ns);
+      return __all_sync(0xffffffffu, ok);
+    };
+    if (!warp_wait(&full[s])) {
       if (lane == 0) report(a.status, kDevTimeout, 1);
       return;
     }
 
     const ColTile h = hdr[s];
+    // Every lane of the warp walks the rows (the waits are warp-wide); lanes
+    // without a column or channel of this tile read row 0 of their stage and
+    // store nothing.
     const int ch = h.c0 + q * CPT;
-    if (active && ch < a.C) {
-      if (h.c0 != cur_c0) {  // weights and bias of this channel tile
-        cur_c0 = h.c0;
+    const bool act = active && ch < a.C;
+    const int chl = act ? ch : 0;
+    if (h.c0 != cur_c0) {  // weights and bias of this channel tile
+      cur_c0 = h.c0;
 #pragma unroll
-        for (int t = 0; t < 9; ++t)
-          Ops::load_w(smem_u32(w_s + ((size_t)t * a.C + ch) * Ops::kWeightBytes), wr[t / 3][t % 3]);
+      for (int t = 0; t < 9; ++t)
+        Ops::load_w(smem_u32(w_s + ((size_t)t * a.C + chl) * Ops::kWeightBytes), wr[t / 3][t % 3]);
 #pragma unroll
-        for (int i = 0; i < CPT; i += 4) {
-          const float4 b4 = *reinterpret_cast<const float4*>(b_s + ch + i);
-          br[i] = b4.x, br[i + 1] = b4.y, br[i + 2] = b4.z, br[i + 3] = b4.w;
-        }
+      for (int i = 0; i < CPT; i += 4) {
+        const float4 b4 = *reinterpret_cast<const float4*>(b_s + chl + i);
+        br[i] = b4.x, br[i + 1] = b4.y, br[i + 2] = b4.z, br[i + 3] = b4.w;
       }
-      const bool store_ok = h.ow0 + wl < a.Wo;
-      T* yb = yg + h.y_base + thread_off;
-      const uint32_t st = smem_u32(stage0 + (size_t)s * a.stage_stride) + lane_off;
-      float acc[NA][CPT];
+    }
+    const bool store_ok = act && h.ow0 + wl < a.Wo;
+    T* yb = yg + h.y_base + thread_off;
+    const uint32_t st = smem_u32(stage0 + (size_t)s * a.stage_stride) + (act ? lane_off : 0u);
+    float acc[NA][CPT];
 #pragma unroll
-      for (int i = 0; i < NA; ++i)
+    for (int i = 0; i < NA; ++i)
 #pragma unroll
-        for (int e = 0; e < CPT; ++e) acc[i][e] = 0.f;
-      ColState<T, FORM, NA> cs{st, row_pitch, col_step, h.nrows, store_ok, y_row_step, wr, br, acc};
-      int r0 = 0;
-      for (; r0 + U <= Hh; r0 += U, yb += NA * y_row_step)
-        col_block<T, FORM, S, DL, NA, false>(cs, r0, Hh, yb, std::make_integer_sequence<int, U>{});
-      if (r0 < Hh) col_block<T, FORM, S, DL, NA, true>(cs, r0, Hh, yb, std::make_integer_sequence<int, U>{});
+      for (int e = 0; e < CPT; ++e) acc[i][e] = 0.f;
+    ColState<T, FORM, NA> cs{st, row_pitch, col_step, h.nrows, store_ok, y_row_step, wr, br, acc};
+    int r0 = 0;
+    bool have1 = !(split && k == 0);  // first tile: rows from h0 on are in the second copy
+    for (; r0 + U <= Hh; r0 += U, yb += NA * y_row_step) {
+      if (!have1 && r0 + U > a.h0) {
+        if (!warp_wait(&full1[s])) {
+          if (lane == 0) report(a.status, kDevTimeout, 1);
+          return;
+        }
+        have1 = true;
+      }
+      col_block<T, FORM, S, DL, NA, false>(cs, r0, Hh, yb, std::make_integer_sequence<int, U>{});
+    }
+    if (r0 < Hh) {
+      if (!have1 && !warp_wait(&full1[s])) {
+        if (lane == 0) report(a.status, kDevTimeout, 1);
+        return;
+      }
+      col_block<T, FORM, S, DL, NA, true>(cs, r0, Hh, yb, std::make_integer_sequence<int, U>{});
     }
 
     __syncwarp();  // this warp is done with stage s

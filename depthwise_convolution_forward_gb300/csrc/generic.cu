@@ -1,7 +1,11 @@
-// Generic direct grouped convolution: one thread per output element, any
-// shape, dtype or alignment.  It is the path for fp32 grouped problems (which
-// must not use TF32 tensor cores) and for shapes the specialised kernels do
-// not cover.  Also hosts the stand-alone epilogue (Kc) kernel.
+// Generic direct grouped convolution, any shape, dtype or alignment: one
+// thread per output element, or one warp per output (lanes split the
+// reduction) for small problems with long reductions.  It is the path for
+// fp32 grouped problems (which must not use TF32 tensor cores) and for shapes
+// the specialised kernels do not cover.  Also hosts the stand-alone epilogue
+// (Kc) kernel.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace gconv {
@@ -52,6 +56,8 @@ __global__ void __launch_bounds__(256) generic_direct_kernel(const GenericArgs a
           if (iw < 0 || iw >= a.W) continue;
           const T* xp = x + (((n * a.D + id) * a.H + ih) * (int64_t)a.W + iw) * C + (int64_t)g * a.Cg;
           const T* wp = wk + ((z * a.Y + yy) * a.X + xx) * a.Cg;
+          // unrolled so that several loads are in flight (same summation order)
+#pragma unroll 8
           for (int cg = 0; cg < a.Cg; ++cg)
             acc = fmaf(Elem<T>::to_f32(xp[cg]), Elem<T>::to_f32(wp[cg]), acc);
         }
@@ -59,6 +65,54 @@ __global__ void __launch_bounds__(256) generic_direct_kernel(const GenericArgs a
     }
     const float b = bias ? Elem<T>::to_f32(bias[(int64_t)g * a.Kg + k]) : 0.f;
     y[o] = epilogue_one<T>(acc, b);
+  }
+}
+
+// Warp per output: the warp's lanes split the (tap, input channel) reduction
+// of one output and combine it with a butterfly sum.  For problems with few
+// outputs and long reductions (one thread per output would leave most SMs
+// idle and walk a long chain of dependent loads).
+template <typename T>
+__global__ void __launch_bounds__(256) generic_warp_kernel(const GenericArgs a) {
+  const T* __restrict__ x = static_cast<const T*>(a.x);
+  const T* __restrict__ w = static_cast<const T*>(a.w);
+  const T* __restrict__ bias = static_cast<const T*>(a.bias);
+  T* __restrict__ y = static_cast<T*>(a.y);
+  const int lane = threadIdx.x & 31;
+  const int64_t C = (int64_t)a.G * a.Cg;
+  const int taps = a.Z * a.Y * a.X;
+  const int red = taps * a.Cg;  // reduction length
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t o = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); o < a.total; o += warps) {
+    int64_t f = o;
+    const int k = (int)(f % a.Kg);
+    f /= a.Kg;
+    const int g = (int)(f % a.G);
+    f /= a.G;
+    const int ow = (int)(f % a.Wo);
+    f /= a.Wo;
+    const int oh = (int)(f % a.Ho);
+    f /= a.Ho;
+    const int od = (int)(f % a.Do);
+    const int64_t n = f / a.Do;
+    const T* wk = w + ((int64_t)g * a.Kg + k) * red;
+    float acc = 0.f;
+    for (int i = lane; i < red; i += 32) {
+      const int t = i / a.Cg, cg = i - t * a.Cg;
+      const int xx = t % a.X, yy = (t / a.X) % a.Y, z = t / (a.X * a.Y);
+      const int id = od * a.sD - a.pD + z * a.dD;
+      const int ih = oh * a.sH - a.pH + yy * a.dH;
+      const int iw = ow * a.sW - a.pW + xx * a.dW;
+      if (id < 0 || id >= a.D || ih < 0 || ih >= a.H || iw < 0 || iw >= a.W) continue;
+      const T* xp = x + (((n * a.D + id) * a.H + ih) * (int64_t)a.W + iw) * C + (int64_t)g * a.Cg;
+      acc = fmaf(Elem<T>::to_f32(xp[cg]), Elem<T>::to_f32(wk[i]), acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+      const float b = bias ? Elem<T>::to_f32(bias[(int64_t)g * a.Kg + k]) : 0.f;
+      y[o] = epilogue_one<T>(acc, b);
+    }
   }
 }
 
@@ -95,6 +149,20 @@ cudaError_t generic_launch(const Geometry& g, const LaunchArgs& a, const DeviceI
   p.sD = g.sD, p.sH = g.sH, p.sW = g.sW, p.pD = g.pD, p.pH = g.pH, p.pW = g.pW;
   p.dD = g.dD, p.dH = g.dH, p.dW = g.dW;
   const int block = 256;
+  // Warp per output when one thread per output would not fill the GPU
+  // (fewer than 16 threads per SM lane group) and each output sums at least
+  // 64 products; otherwise thread per output.
+  const int64_t red = (int64_t)g.taps() * g.Cg;
+  if (p.total < (int64_t)dev.num_sms * 2048 && red >= 64) {
+    const int64_t wblocks = (p.total + (block / 32) - 1) / (block / 32);
+    const int grid = (int)std::min<int64_t>(wblocks, (int64_t)dev.num_sms * 16);
+    switch (a.dt) {
+      case kF32: generic_warp_kernel<float><<<grid, block, 0, a.stream>>>(p); break;
+      case kF16: generic_warp_kernel<__half><<<grid, block, 0, a.stream>>>(p); break;
+      case kBF16: generic_warp_kernel<__nv_bfloat16><<<grid, block, 0, a.stream>>>(p); break;
+    }
+    return cudaGetLastError();
+  }
   const int grid = grid_for(p.total, block, &dev);
   switch (a.dt) {
     case kF32: generic_direct_kernel<float><<<grid, block, 0, a.stream>>>(p); break;

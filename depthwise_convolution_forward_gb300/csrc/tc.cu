@@ -100,7 +100,9 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
   double best = 1e30;
   TcPlan bestp;
   std::memset(&bestp, 0, sizeof(bestp));
-  for (int nmt = 1; nmt <= 4; ++nmt) {
+  // Candidates: nmt M tiles per CTA tile x np partial accumulators.
+  for (int combo = 0; combo < 12; ++combo) {
+    const int nmt = combo / 3 + 1, np_cand = 1 << (combo % 3);
     if (ov && ov[2] && ov[2] != nmt) continue;
     TcArgs c = a;
     const int TWo = std::min(g.Wo, std::min(tw_cap, 128 * nmt - range_x));
@@ -133,12 +135,19 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     const uint32_t b_bytes = round_up((uint32_t)(c.sc * taps * c.Kt * c.Nn * 2), 1024);
     // Partial accumulators so that the tile has at least kIssuers
     // independent units of MMA work: np in {4, 2, 1} within 512 TMEM columns.
+    // Partial accumulators (taps split np ways, summed by the epilogue): at
+    // least enough that the tile has kIssuers independent units of MMA work.
     const int G2 = c.sc * c.nmt;
     int np = 1;
     while (np * 2 <= tc::kIssuers && G2 * np < tc::kIssuers && np * 2 <= taps &&
            2 * (np * 2) * G2 * c.Nn <= 512)
       np *= 2;
-    if (ov && ov[4]) np = ov[4];
+    if (np_cand < np || np_cand > taps) continue;
+    np = np_cand;
+    if (ov && ov[4]) {
+      if (np_cand != 1) continue;
+      np = ov[4];
+    }
     c.np = np;
     // per-issuer MMA lists: 32 bytes per entry
     uint32_t entries = 0;
@@ -191,6 +200,13 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     while (stages > 2 && c.a_off + stages * c.a_stage_bytes > budget) --stages;
     if (c.a_off + stages * c.a_stage_bytes > budget) continue;
     c.stages = stages;
+    // Epilogue through shared-memory staging (coalesced 128-byte stores), on
+    // request (override 7 < 0) when 16 KB are left.  Measured slower than
+    // storing from registers on GB300 (the staged path spills at the
+    // 168-register cap of 9 warps per CTA), so it is off by default.
+    c.epi_off = 0;
+    const uint32_t a_end = c.a_off + stages * c.a_stage_bytes;
+    if (a_end + 16384u <= budget && ov && ov[7] < 0) c.epi_off = a_end;
     uint32_t cols = 32;
     while (cols < (uint32_t)(2 * np * G2 * c.Nn)) cols <<= 1;
     if (cols > 512) continue;
@@ -203,7 +219,7 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     TcPlan p;
     p.a = c;
     p.sw = sw;
-    p.smem_bytes = c.a_off + stages * c.a_stage_bytes;
+    p.smem_bytes = c.a_off + stages * c.a_stage_bytes + (c.epi_off ? 16384u : 0u);
     // Keep a second CTA off the SM when both could not hold their tensor
     // memory at once (its allocation would wait for the first CTA to exit).
     if (cols > 256) p.smem_bytes = std::max<uint32_t>(p.smem_bytes, 117 * 1024);
@@ -211,7 +227,10 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     if (p.smem_bytes > budget) continue;
     p.grid = n_sc * c.cpg;
     p.ok = true;
-    const double cost = (double)c.tiles_h * c.tiles_w * (nmt * 128 + 96) / c.cpg;
+    // Cost: MMA rows per CTA plus a per-tile overhead.  Splitting the taps
+    // over 2 or more partial accumulators measured 5-7% faster on ResNeXt (a)
+    // and the G=32 / G=256 sweeps (shorter accumulation chains, finer tiles).
+    const double cost = (double)c.tiles_h * c.tiles_w * (nmt * 128 + 96) / c.cpg * (np >= 2 ? 0.8 : 1.0);
     if (cost < best) best = cost, bestp = p;
   }
   if (best >= 1e30) return false;
@@ -225,7 +244,13 @@ bool make_tc_plan(const Geometry& g, bool bf16, int num_sms, int max_smem, const
 }
 
 template <typename T>
-using TcKernel = void (*)(const CUtensorMap, const TcArgs);
+using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const TcArgs);
+
+template <typename T>
+TcKernel<T> pick_tc_kernel(const TcPlan& p) {
+  if (p.a.epi_off != 0) return p.sw ? tc::tc_kernel<T, true, true> : tc::tc_kernel<T, false, true>;
+  return p.sw ? tc::tc_kernel<T, true, false> : tc::tc_kernel<T, false, false>;
+}
 
 template <typename T>
 cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const DeviceInfo& dev) {
@@ -241,12 +266,12 @@ cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   key.device = dev.device;
   key.bf16 = std::is_same<T, __nv_bfloat16>::value;
   static PlanCache<TcPlan> cache;
-  static SmemAttr attr[2];
+  static SmemAttr attr[2][2];  // [swizzled rows][staged epilogue]
   TcPlan p;
   if (!cache.get(key, &p)) {
     if (!make_tc_plan(g, key.bf16, dev.num_sms, dev.max_smem_optin, la.tile, &p)) return cudaErrorNotSupported;
-    const TcKernel<T> kern = p.sw ? tc::tc_kernel<T, true> : tc::tc_kernel<T, false>;
-    cudaError_t e = attr[p.sw].ensure(kern, dev.device, (int)p.smem_bytes);
+    const TcKernel<T> kern = pick_tc_kernel<T>(p);
+    cudaError_t e = attr[p.sw][p.a.epi_off != 0].ensure(kern, dev.device, (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
     // Co-resident CTAs must never need more than the SM's 512 TMEM columns,
     // or an allocation would wait for another CTA to exit.  Raise the
@@ -259,7 +284,7 @@ cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
       if ((uint32_t)occ * p.a.tmem_cols <= 512u) break;
       p.smem_bytes += 8 * 1024;
       if (p.smem_bytes > (uint32_t)dev.max_smem_optin) return cudaErrorNotSupported;
-      e = attr[p.sw].ensure(kern, dev.device, (int)p.smem_bytes);
+      e = attr[p.sw][p.a.epi_off != 0].ensure(kern, dev.device, (int)p.smem_bytes);
       if (e != cudaSuccess) return e;
     }
     cache.put(key, p);
@@ -277,15 +302,28 @@ cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   if (encode_tiled(&map, tt, 5, la.x, dims, strides, box, estr,
                    p.sw ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  // Weights as [G*Kg][taps][Cg] for TMA staging of the block-diagonal B
+  // (8-channel boxes of Kg output channels); otherwise the threads copy them.
+  CUtensorMap wmap = map;
+  int w_tma = 0;
+  if (g.Cg % 8 == 0 && g.Kg % 8 == 0 && (reinterpret_cast<uintptr_t>(la.w) & 15) == 0) {
+    const uint64_t taps = (uint64_t)g.taps();
+    uint64_t wdims[3] = {(uint64_t)g.Cg, taps, (uint64_t)g.K()};
+    uint64_t wstrides[2] = {(uint64_t)g.Cg * es, taps * g.Cg * es};
+    uint32_t wbox[3] = {8u, 1u, (uint32_t)g.Kg};
+    uint32_t westr[3] = {1u, 1u, 1u};
+    if (encode_tiled(&wmap, tt, 3, la.w, wdims, wstrides, wbox, westr) == CUDA_SUCCESS) w_tma = 1;
+  }
   TcArgs a = p.a;
+  a.w_tma = w_tma;
   a.w = la.w;
   a.bias = la.bias;
   a.y = la.y;
   a.status = la.status;
   a.wait_limit_ns = la.wait_limit_ns;
   a.test_flags = la.test_flags;
-  const TcKernel<T> kern = p.sw ? tc::tc_kernel<T, true> : tc::tc_kernel<T, false>;
-  kern<<<p.grid, tc::kThreads, p.smem_bytes, la.stream>>>(map, a);
+  const TcKernel<T> kern = pick_tc_kernel<T>(p);
+  kern<<<p.grid, tc::kThreads, p.smem_bytes, la.stream>>>(map, wmap, a);
   return cudaGetLastError();
 }
 

@@ -62,6 +62,8 @@ struct TcArgs {
   int np;                  // partial accumulators per accumulator (taps split np ways)
   uint32_t plane_stride, a_stage_bytes, tx_bytes;
   uint32_t a_off, b_off, bias_off, tab_off;  // smem offsets (tab: MMA descriptor table)
+  uint32_t epi_off;  // epilogue staging (4 x 4 KB), or 0 to store straight from registers
+  int w_tma;         // 1: weights staged by TMA through the weight tensor map (Cg, Kg % 8 == 0)
   int stages;
   uint32_t tmem_cols, idesc;
   int n_gc, cpg, tiles_w, tiles_h;
@@ -163,12 +165,101 @@ __device__ __forceinline__ void epilogue_row(uint32_t lane_base, int mt, int G2,
   }
 }
 
+// Epilogue for one 128-row slab of a tile through a per-warp shared-memory
+// staging buffer (32 rows x 128 bytes, 16-byte units XOR-swizzled by row).
+// Each group of 4 chunks (64 channels) is written row by row (lane = pixel
+// row), then read back transposed: in each of 4 rounds, 4 lanes cover the
+// 4 chunks of one pixel and a warp store instruction writes 8 whole 128-byte
+// pixel segments instead of 32 scattered 32-byte pieces.
+template <typename T, int NP>
+__device__ __forceinline__ void epilogue_row_staged(uint32_t lane_base, int mt, int G2, int sc, int Nn, bool valid,
+                                                    T* dst, const float* bias_s, bool v8, uint32_t sbuf) {
+  constexpr int kPer = 4 / NP;
+  const int lane = threadIdx.x & 31;
+  const int nchunk16 = sc * Nn / 16;
+  const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+  const uint32_t row_addr = sbuf + (uint32_t)lane * 128u;
+  const uint64_t my_dst = reinterpret_cast<uint64_t>(dst);
+  for (int c0 = 0; c0 < nchunk16; c0 += 4) {
+    const int cend = min(c0 + 4, nchunk16);
+    for (int cb = c0; cb < cend; cb += kPer) {
+      uint32_t r[kPer][NP][16];
+#pragma unroll
+      for (int b = 0; b < kPer; ++b) {
+        const int cc = cb + b;
+        if (cc < cend) {
+          const int col = cc * 16;  // channel offset within the row of sc chunks
+          const int j = col / Nn, cn = col - j * Nn;
+#pragma unroll
+          for (int p = 0; p < NP; ++p) tmem_ld16(lane_base + (uint32_t)((p * G2 + mt * sc + j) * Nn + cn), r[b][p]);
+        }
+      }
+      tmem_ld_wait();
+#pragma unroll
+      for (int b = 0; b < kPer; ++b) {
+        const int cc = cb + b;
+        if (cc < cend) {
+          uint32_t wd[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float s0 = __uint_as_float(r[b][0][2 * i]), s1 = __uint_as_float(r[b][0][2 * i + 1]);
+#pragma unroll
+            for (int p = 1; p < NP; ++p) {
+              s0 += __uint_as_float(r[b][p][2 * i]);
+              s1 += __uint_as_float(r[b][p][2 * i + 1]);
+            }
+            wd[i] = epilogue_pair<T>(s0, s1, bias_s[cc * 16 + 2 * i], bias_s[cc * 16 + 2 * i + 1]);
+          }
+          const uint32_t u0 = (uint32_t)(cc - c0) * 2u;
+          const uint32_t sw = (uint32_t)(lane & 7);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row_addr + ((u0 ^ sw) << 4)), "r"(wd[0]),
+                       "r"(wd[1]), "r"(wd[2]), "r"(wd[3])
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row_addr + (((u0 + 1u) ^ sw) << 4)),
+                       "r"(wd[4]), "r"(wd[5]), "r"(wd[6]), "r"(wd[7])
+                       : "memory");
+        }
+      }
+    }
+    __syncwarp();
+    const int c = lane & 3;
+    const bool c_ok = c0 + c < cend;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int p = 8 * i + (lane >> 2);  // pixel row whose chunk c this lane stores
+      const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)my_dst, p);
+      const uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)(my_dst >> 32), p);
+      if (((vmask >> p) & 1u) && c_ok) {
+        T* pd = reinterpret_cast<T*>(((uint64_t)hi << 32) | lo) + (c0 + c) * 16;
+        const uint32_t prow = sbuf + (uint32_t)p * 128u, psw = (uint32_t)(p & 7);
+        uint32_t a[4], b[4];
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                     : "r"(prow + (((2u * c) ^ psw) << 4)));
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3])
+                     : "r"(prow + (((2u * c + 1u) ^ psw) << 4)));
+        if (v8) {
+          asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(pd), "r"(a[0]), "r"(a[1]),
+                       "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3])
+                       : "memory");
+        } else {
+          *reinterpret_cast<uint4*>(pd) = make_uint4(a[0], a[1], a[2], a[3]);
+          *reinterpret_cast<uint4*>(pd + 8) = make_uint4(b[0], b[1], b[2], b[3]);
+        }
+      }
+    }
+    __syncwarp();  // the staging rows are rewritten by the next group
+  }
+}
+
 // SW = false: A planes hold one 8-channel chunk per pixel (16-byte rows,
 // no swizzle), one TMA box per (phase, chunk).  SW = true: A planes hold 64
 // channels per pixel (128-byte rows, 128-byte swizzle) covering `sc` group
 // chunks, one TMA box per phase; each chunk is a K-offset inside the row.
-template <typename T, bool SW>
+template <typename T, bool SW, bool STAGED>
 __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                        const __grid_constant__ CUtensorMap wmap,
                                                         const __grid_constant__ TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* a_full = reinterpret_cast<uint64_t*>(smem);
@@ -176,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
   uint64_t* acc_full = a_full + 2 * kMaxStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* mma_done = acc_empty + 2;
+  uint64_t* w_full = mma_done + 1;  // weight copies (TMA staging)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 256);
   float* bias_s = reinterpret_cast<float*>(smem + a.bias_off);
   uint8_t* Bs = smem + a.b_off;
@@ -200,8 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
       mbar_init(&acc_empty[b], 4);
     }
     mbar_init(mma_done, kIssuers);
+    mbar_init(w_full, 1);
     fence_mbar_init();
     tma_prefetch_desc(&xmap);
+    if (a.w_tma) tma_prefetch_desc(&wmap);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, a.tmem_cols);
@@ -233,9 +327,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     if (!full_runs) {
       uint4* B16 = reinterpret_cast<uint4*>(Bs);
       for (int i = btid; i < nchunk; i += bthreads) B16[i] = make_uint4(0u, 0u, 0u, 0u);
+      fence_proxy_async_smem();  // zeros before the TMA copies into the same slabs
       asm volatile("bar.sync 1, %0;" ::"r"(bthreads) : "memory");
     }
     T* B = reinterpret_cast<T*>(Bs);
+    if (a.w_tma) {
+      // Cg and Kg multiples of 8: the 8 input channels of a (tap, ks, kc2)
+      // slab lie in one group gi, and for that group the slab's Kg rows n =
+      // gi*Kg + kk are one TMA box {8 channels, 1 tap, Kg output channels}
+      // of the weight tensor viewed as [G*Kg][taps][Cg].
+      // One copy per builder thread (a single thread issuing them all would
+      // serialise about 0.1 us per copy); thread 0 arms the barrier with the
+      // total bytes (copies may complete before that: the transaction count
+      // may go negative until then).
+      const int ncopy = a.sc * a.ntaps * a.KS * 2;
+      if (btid == 0) mbar_arrive_expect_tx(w_full, (uint32_t)ncopy * (uint32_t)a.Kg * 16u);
+      for (int i = btid; i < ncopy; i += bthreads) {
+        const int kc2 = i & 1, r = i >> 1;
+        const int ks = r % a.KS, t = (r / a.KS) % a.ntaps, j = r / (a.KS * a.ntaps);
+        const int k0 = ks * 16 + kc2 * 8;
+        const int gi = k0 / a.Cg, c0 = k0 - gi * a.Cg;
+        tma_load_3d(B + ((size_t)i * a.Nn + (size_t)gi * a.Kg) * 8, &wmap, w_full, c0, t, (g0 + j * a.m + gi) * a.Kg);
+      }
+    } else {
     // chunk index ci = (((j*ntaps + t)*KS + ks)*2 + kc2)*Nn + n, n = gi*Kg + kk,
     // as mixed-radix digits advanced by bthreads with carries (no division
     // per chunk)
@@ -243,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     int dig[6], inc[6];
     {
       int v = btid, w = bthreads;
+#pragma unroll
       for (int i = 0; i < 6; ++i) {
         dig[i] = v % rad[i], v /= rad[i];
         inc[i] = w % rad[i], w /= rad[i];
@@ -277,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
       } else {
         for (int e = 0; e < kb - ka; ++e) dst[e] = src[e];
       }
+    }
     }
     (void)wa;
     for (int i = btid; i < a.sc * a.Nn; i += bthreads)
@@ -351,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
+    if (a.w_tma && !mbar_wait(w_full, 0u, a.wait_limit_ns)) report(a.status, kDevTimeout, 6);
     fence_proxy_async_smem();  // generic-proxy writes of B -> visible to the tensor core
     asm volatile("bar.sync 1, %0;" ::"r"(bthreads) : "memory");
   }
@@ -476,9 +593,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         const bool valid = i < a.TH && jj < a.TWo && oh < a.Ho && ow < a.Wo;
         T* dst = yg + ((((int64_t)st.n * a.Do + st.od) * a.Ho + oh) * (int64_t)a.Wo + ow) * a.Ktot +
                  (int64_t)g0 * a.Kg;
-        if (NP == 1) epilogue_row<T, 1>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8);
-        else if (NP == 2) epilogue_row<T, 2>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8);
-        else epilogue_row<T, 4>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8);
+        if constexpr (STAGED) {
+          const uint32_t sbuf = smem_u32(smem + a.epi_off) + (uint32_t)q * 4096u;
+          if (NP == 1) epilogue_row_staged<T, 1>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8, sbuf);
+          else if (NP == 2) epilogue_row_staged<T, 2>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8, sbuf);
+          else epilogue_row_staged<T, 4>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8, sbuf);
+        } else {
+          if (NP == 1) epilogue_row<T, 1>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8);
+          else if (NP == 2) epilogue_row<T, 2>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8);
+          else epilogue_row<T, 4>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8);
+        }
       }
       fence_before_sync();
       __syncwarp();

@@ -93,7 +93,9 @@ typedef struct gconv_options {
                             first wait cannot complete (timeout-path test)       */
   int32_t selected;      /* out: the gconv_kernel that was launched               */
   int32_t tile[8];       /* tuning overrides, 0 = automatic.
-                            Depthwise kernel: [0] TH, [1] TW, [2] WB, [3] stages,
+                            Depthwise kernel: [0] TH, [1] TW, [2] WB (row-blocked
+                            form) / 2 = first tile's input in two copies (column
+                            form), [3] stages,
                             [4] CTAs per SM, [5] FMA form (row-blocked form:
                             1 = widen + fp32 FMA, 2 = mixed f16/bf16 FMA,
                             3 = widen + packed fp32x2 FMA; column form: 1 =
@@ -107,7 +109,9 @@ typedef struct gconv_options {
                             filter is 1, else the row-blocked form).
                             Tensor-core kernel: [0] TH, [2] M tiles per CTA,
                             [3] stages, [4] partial accumulators, [6] 1 = force
-                            16-byte chunk planes, [7] extra shared memory (KB). */
+                            16-byte chunk planes, [7] extra shared memory (KB),
+                            negative: stage the epilogue through shared memory
+                            for coalesced stores (default: store from registers). */
 } gconv_options;
 
 /*

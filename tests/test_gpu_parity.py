@@ -124,15 +124,32 @@ COL_TILES = {
 COL_CASES = [(n, t) for n, ts in COL_TILES.items() for t in ts]
 
 
+@pytest.mark.parametrize("one_copy", [2, 0], ids=["split-copy", "one-copy"])
 @pytest.mark.parametrize("name,tiles", COL_CASES, ids=lambda v: v if isinstance(v, str) else "-".join(map(str, v)))
-def test_depthwise_column_tiles(orc, name, tiles):
+def test_depthwise_column_tiles(orc, name, tiles, one_copy):
+    """Explicit tiles; each CTA's first tile either as two copies on two
+    barriers (slot 2 = 2, where the split point is aligned) or as one copy."""
     TH, TW, stages, ctas = tiles
     wl = inputs.by_name(name).with_(N=2)
     x, w, b = inputs.make_inputs(wl)
     ref = orc.forward(wl, x, w, b)
-    y, sel = run_gpu(wl, x, w, b, force=B.KERNEL_DIRECT_DW, tile=[TH, TW, 0, stages, ctas, 0, 3])
+    y, sel = run_gpu(wl, x, w, b, force=B.KERNEL_DIRECT_DW, tile=[TH, TW, one_copy, stages, ctas, 0, 3])
     assert sel == B.KERNEL_DIRECT_DW
     assert_close(y.double().numpy(), ref, wl.dtype, f"{name} tiles {tiles}")
+
+
+@pytest.mark.parametrize("name", ["resnext_b_bf16", "sweep_g8_d1_s1_bf16", "resnext3d_n1_f16", "sweep_g256_d2_s2_bf16"])
+@pytest.mark.parametrize("staged", [True, False], ids=["staged", "direct"])
+def test_tensor_core_epilogue_paths(orc, name, staged):
+    """Both epilogues of the tensor-core kernel: straight from registers (the
+    default) and through shared-memory staging (override slot 7 < 0)."""
+    wl = inputs.by_name(name).with_(N=min(inputs.by_name(name).N, 2))
+    x, w, b = inputs.make_inputs(wl)
+    ref = orc.forward(wl, x, w, b)
+    tile = [0, 0, 0, 0, 0, 0, 0, -1] if staged else None
+    y, sel = run_gpu(wl, x, w, b, force=B.KERNEL_IGEMM_TC, tile=tile)
+    assert sel == B.KERNEL_IGEMM_TC
+    assert_close(y.double().numpy(), ref, wl.dtype, f"{name} staged={staged}")
 
 
 def test_depthwise_3d(orc):
