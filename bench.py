@@ -61,6 +61,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tile", default="", help="tuning override TH,TW,WB,stages,ctas_per_sm,fma_form")
     ap.add_argument("--force-kernel", type=int, default=0)
+    ap.add_argument("--serial-launch", action="store_true",
+                    help="launch without programmatic dependent launch (each kernel starts after the previous ends)")
     return ap.parse_args()
 
 
@@ -382,6 +384,7 @@ def run_ours(args, wls, set_name, rank, world):
 
     opt = B.gconv_options()
     opt.force_kernel = args.force_kernel
+    opt.serial_launch = 1 if args.serial_launch else 0
     for i, t in enumerate(tile[:8]):
         opt.tile[i] = t
     optp = ctypes.byref(opt)
@@ -537,7 +540,8 @@ def run_ours(args, wls, set_name, rank, world):
             "scaling": "weak", "vs_baseline": None, "dtype": wls[0].dtype, "data": "synthetic",
             "config": {"workload": describe(wls), "layout": "NHWGC / GKYXC / NHWGK",
                        "l2": f"rotating {R} input/output sets ({R * per_set / 1e6:.0f} MB > 2x L2)",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "launch": "serial" if args.serial_launch else "programmatic dependent launch"},
             "tflops": tflops, "median_ms_per_step": med,
             "value_from_median": step_bytes / (med / 1e3) / 1e9,
             "per_launch": per_launch, "roofline": roof,

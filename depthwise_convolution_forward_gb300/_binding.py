@@ -41,7 +41,8 @@ class gconv_problem(ctypes.Structure):
 class gconv_options(ctypes.Structure):
     _fields_ = [("force_kernel", ctypes.c_int32), ("debug", ctypes.c_int32),
                 ("wait_limit_ns", ctypes.c_int64), ("test_flags", ctypes.c_int32),
-                ("selected", ctypes.c_int32), ("tile", ctypes.c_int32 * 8)]
+                ("selected", ctypes.c_int32), ("tile", ctypes.c_int32 * 8),
+                ("serial_launch", ctypes.c_int32)]
 
 
 class GconvError(RuntimeError):

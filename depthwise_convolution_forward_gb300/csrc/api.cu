@@ -231,6 +231,7 @@ gconv_status grouped_conv_fwd_ex(const void* x, const void* w, const void* bias,
   a.wait_limit_ns = (opt && opt->wait_limit_ns > 0) ? (uint64_t)opt->wait_limit_ns : 2000000000ull;
   a.test_flags = opt ? opt->test_flags : 0;
   for (int i = 0; i < 8; ++i) a.tile[i] = opt ? opt->tile[i] : 0;
+  a.pdl = !(opt && opt->serial_launch);
 
   int kernel = (opt && opt->force_kernel) ? opt->force_kernel : select_kernel(g, a.dt, &a);
   if (kernel == GCONV_KERNEL_DIRECT_DW && !dw_supported(g, a.dt, &a))

@@ -150,6 +150,20 @@ __device__ __forceinline__ void report(int* status, int code, int where) {
   if (status != nullptr && atomicCAS(status, 0, code) == 0) atomicExch(status + 1, where);
 }
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  allow_dependent_launch() lets the next
+// kernel in the stream begin launching its CTAs once every CTA of this grid
+// has called it (or exited); those CTAs then occupy only resources this grid
+// leaves free.  grid_dependency_wait() returns once the previous grid in the
+// stream has completed and its memory operations are visible; it returns at
+// once when the kernel was not launched as a dependent.  Neither is a spin
+// loop in the kernel.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(WB >= 8 ? 288 : 512) dw_kernel(const __grid_co
     fence_mbar_init();
     tma_prefetch_desc(&xmap);
   }
+  grid_dependency_wait();  // x, w, bias and y are touched only from here on
   // resident weights and bias for every channel
   for (int i = tid; i < taps * a.C; i += blockDim.x) {
     const int t = i / a.C, ch = i - t * a.C;
@@ -334,6 +335,7 @@ __global__ void __launch_bounds__(256, 2) dw_ldg_kernel(const DwArgs a) {
   T* __restrict__ yg = static_cast<T*>(a.y);
   const TileCoord c = decode_tile(a, blockIdx.x);
   const int c0 = c.ct * a.TC;
+  grid_dependency_wait();  // x, w, bias and y are touched only from here on
 
   // this tile's channel slice of the weights and bias
   for (int i = tid; i < taps * a.TC; i += blockDim.x) {

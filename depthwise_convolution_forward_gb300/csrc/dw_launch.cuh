@@ -374,8 +374,7 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
     a.status = la.status;
     a.wait_limit_ns = la.wait_limit_ns;
     DwLdgKernel<T> k = pick_ldg_kernel<T>(g.sH, g.dH, p.WB, p.mode);
-    k<<<(unsigned)p.num_tiles, p.threads, p.smem_bytes, la.stream>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(k, dim3((unsigned)p.num_tiles), dim3(p.threads), p.smem_bytes, la, a);
   }
 
   // x viewed as a 5-D tensor (C, W, H, D, N), innermost first.
@@ -425,8 +424,7 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   DwKernel<T> kern = p.col ? pick_col_kernel<T>(g.sH, g.dH, p.mode) : pick_kernel<T>(g.sH, g.dH, p.WB, p.mode);
   a.h0 = h0;
   a.bytes0 = (uint32_t)h0 * p.Wh * p.TC * p.Dh * es;
-  kern<<<grid, p.threads, p.smem_bytes, la.stream>>>(map, map0, map1, a);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(grid), dim3(p.threads), p.smem_bytes, la, map, map0, map1, a);
 }
 
 }  // namespace dw

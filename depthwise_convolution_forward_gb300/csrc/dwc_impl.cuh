@@ -388,6 +388,12 @@ __global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __g
   const T* __restrict__ bg = static_cast<const T*>(a.bias);
   T* __restrict__ yg = static_cast<T*>(a.y);
 
+  // Stride 2 computes a quarter of the outputs per input byte, so its CTAs
+  // are bandwidth-bound and let the next kernel's CTAs launch at once.  At
+  // stride 1 they are issue-bound: the next kernel's CTAs, resident beside
+  // them while they wait on this grid, measured about 1 us slower per
+  // launch, so the dependents launch only as this grid's CTAs exit.
+  if constexpr (S == 2) allow_dependent_launch();
   if (tid == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(&full[s], 1);
@@ -402,6 +408,7 @@ __global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __g
     }
   }
   __syncthreads();
+  grid_dependency_wait();  // x, w, bias and y are touched only from here on
 
   const bool withhold = (a.test_flags & 1) && blockIdx.x == 0;
   if (warp == 0) {

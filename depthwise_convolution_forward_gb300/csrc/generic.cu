@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(256) generic_direct_kernel(const GenericArgs a
   T* __restrict__ y = static_cast<T*>(a.y);
   const int64_t C = (int64_t)a.G * a.Cg;
   const int taps = a.Z * a.Y * a.X;
+  grid_dependency_wait();  // x, w, bias and y are touched only from here on
   for (int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; o < a.total;
        o += (int64_t)gridDim.x * blockDim.x) {
     int64_t f = o;
@@ -83,6 +84,7 @@ __global__ void __launch_bounds__(256) generic_warp_kernel(const GenericArgs a) 
   const int taps = a.Z * a.Y * a.X;
   const int red = taps * a.Cg;  // reduction length
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  grid_dependency_wait();  // x, w, bias and y are touched only from here on
   for (int64_t o = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); o < a.total; o += warps) {
     int64_t f = o;
     const int k = (int)(f % a.Kg);
@@ -149,6 +151,7 @@ cudaError_t generic_launch(const Geometry& g, const LaunchArgs& a, const DeviceI
   p.sD = g.sD, p.sH = g.sH, p.sW = g.sW, p.pD = g.pD, p.pH = g.pH, p.pW = g.pW;
   p.dD = g.dD, p.dH = g.dH, p.dW = g.dW;
   const int block = 256;
+  cudaError_t e = cudaSuccess;
   // Warp per output when one thread per output would not fill the GPU
   // (fewer than 16 threads per SM lane group) and each output sums at least
   // 64 products; otherwise thread per output.
@@ -157,19 +160,19 @@ cudaError_t generic_launch(const Geometry& g, const LaunchArgs& a, const DeviceI
     const int64_t wblocks = (p.total + (block / 32) - 1) / (block / 32);
     const int grid = (int)std::min<int64_t>(wblocks, (int64_t)dev.num_sms * 16);
     switch (a.dt) {
-      case kF32: generic_warp_kernel<float><<<grid, block, 0, a.stream>>>(p); break;
-      case kF16: generic_warp_kernel<__half><<<grid, block, 0, a.stream>>>(p); break;
-      case kBF16: generic_warp_kernel<__nv_bfloat16><<<grid, block, 0, a.stream>>>(p); break;
+      case kF32: e = launch_kernel(generic_warp_kernel<float>, dim3(grid), dim3(block), 0, a, p); break;
+      case kF16: e = launch_kernel(generic_warp_kernel<__half>, dim3(grid), dim3(block), 0, a, p); break;
+      case kBF16: e = launch_kernel(generic_warp_kernel<__nv_bfloat16>, dim3(grid), dim3(block), 0, a, p); break;
     }
-    return cudaGetLastError();
+    return e;
   }
   const int grid = grid_for(p.total, block, &dev);
   switch (a.dt) {
-    case kF32: generic_direct_kernel<float><<<grid, block, 0, a.stream>>>(p); break;
-    case kF16: generic_direct_kernel<__half><<<grid, block, 0, a.stream>>>(p); break;
-    case kBF16: generic_direct_kernel<__nv_bfloat16><<<grid, block, 0, a.stream>>>(p); break;
+    case kF32: e = launch_kernel(generic_direct_kernel<float>, dim3(grid), dim3(block), 0, a, p); break;
+    case kF16: e = launch_kernel(generic_direct_kernel<__half>, dim3(grid), dim3(block), 0, a, p); break;
+    case kBF16: e = launch_kernel(generic_direct_kernel<__nv_bfloat16>, dim3(grid), dim3(block), 0, a, p); break;
   }
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t epilogue_launch(const float* acc, const void* bias, void* y, int64_t rows, int cols,

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace gconv {
 
 enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
@@ -42,7 +44,29 @@ struct LaunchArgs {
   uint64_t wait_limit_ns;
   int test_flags;
   int tile[8];  // tuning overrides, 0 = automatic
+  bool pdl;     // programmatic dependent launch (the kernels wait on the grid dependency)
 };
+
+// Launches kernel k on a.stream.  With a.pdl the launch carries the
+// programmatic-stream-serialisation attribute: the kernel's CTAs may start
+// while the previous kernel in the stream is still running, so every kernel
+// launched this way calls grid_dependency_wait() before its first access to
+// global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, const LaunchArgs& a,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+}
 
 // Device properties needed by the launchers (cached per device by api.cu).
 struct DeviceInfo {

@@ -323,8 +323,7 @@ cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   a.wait_limit_ns = la.wait_limit_ns;
   a.test_flags = la.test_flags;
   const TcKernel<T> kern = pick_tc_kernel<T>(p);
-  kern<<<p.grid, tc::kThreads, p.smem_bytes, la.stream>>>(map, wmap, a);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(p.grid), dim3(tc::kThreads), p.smem_bytes, la, map, wmap, a);
 }
 
 }  // namespace

@@ -282,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
   const T* __restrict__ bg = static_cast<const T*>(a.bias);
   T* __restrict__ yg = static_cast<T*>(a.y);
 
+  allow_dependent_launch();
   if (tid == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(&a_full[s], 1);
@@ -297,20 +298,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     tma_prefetch_desc(&xmap);
     if (a.w_tma) tma_prefetch_desc(&wmap);
   }
+  // Named barrier 2 (all threads): warp 0 arrives once the barriers are
+  // initialised and goes straight on to copy input tiles; warps 1.. sync on
+  // it after their set-up that needs neither.  Warp 1 allocates tensor
+  // memory after the wait on the previous grid in the stream: a CTA that
+  // holds tensor memory never waits on another grid, so a later grid's CTA
+  // waiting in its own allocation always sees it freed.
   if (warp == 0) {
-    tmem_alloc(tmem_slot, a.tmem_cols);
-    tmem_relinquish();
+    __syncwarp();
+    asm volatile("bar.arrive 2, %0;" ::"r"(kThreads) : "memory");
+    grid_dependency_wait();  // x from here on
   }
-  fence_before_sync();
-  __syncthreads();  // barriers initialised, tensor memory allocated
-  fence_after_sync();
-  const uint32_t tmem_base = *tmem_slot;
+  uint32_t tmem_base = 0;
   const bool withhold = (a.test_flags & 1) && blockIdx.x == 0;
 
   if (warp != 0) {
-    // Warps 1.. stage the weights, bias and MMA lists while the producer
-    // (warp 0) already copies the first input tiles: the A stages do not
-    // depend on them.
+    // Warps 1.. build the MMA lists and stage the weights and bias while the
+    // producer (warp 0) already copies the first input tiles: the A stages do
+    // not depend on them.  The zero fill and the lists touch only shared
+    // memory and kernel parameters, so they run before the wait on the
+    // previous kernel in the stream.
     const int btid = tid - 32, bthreads = (int)blockDim.x - 32;
     // Weights of this group chunk as block-diagonal B_t[n][k], K-major core
     // matrices: byte offset ((((t*KS + ks)*2 + kc2)*Nn + n)*8 + e)*2 holds
@@ -327,76 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     if (!full_runs) {
       uint4* B16 = reinterpret_cast<uint4*>(Bs);
       for (int i = btid; i < nchunk; i += bthreads) B16[i] = make_uint4(0u, 0u, 0u, 0u);
-      fence_proxy_async_smem();  // zeros before the TMA copies into the same slabs
-      asm volatile("bar.sync 1, %0;" ::"r"(bthreads) : "memory");
+      fence_proxy_async_smem();  // zeros before the copies into the same slabs (barrier 2 below)
     }
-    T* B = reinterpret_cast<T*>(Bs);
-    if (a.w_tma) {
-      // Cg and Kg multiples of 8: the 8 input channels of a (tap, ks, kc2)
-      // slab lie in one group gi, and for that group the slab's Kg rows n =
-      // gi*Kg + kk are one TMA box {8 channels, 1 tap, Kg output channels}
-      // of the weight tensor viewed as [G*Kg][taps][Cg].
-      // One copy per builder thread (a single thread issuing them all would
-      // serialise about 0.1 us per copy); thread 0 arms the barrier with the
-      // total bytes (copies may complete before that: the transaction count
-      // may go negative until then).
-      const int ncopy = a.sc * a.ntaps * a.KS * 2;
-      if (btid == 0) mbar_arrive_expect_tx(w_full, (uint32_t)ncopy * (uint32_t)a.Kg * 16u);
-      for (int i = btid; i < ncopy; i += bthreads) {
-        const int kc2 = i & 1, r = i >> 1;
-        const int ks = r % a.KS, t = (r / a.KS) % a.ntaps, j = r / (a.KS * a.ntaps);
-        const int k0 = ks * 16 + kc2 * 8;
-        const int gi = k0 / a.Cg, c0 = k0 - gi * a.Cg;
-        tma_load_3d(B + ((size_t)i * a.Nn + (size_t)gi * a.Kg) * 8, &wmap, w_full, c0, t, (g0 + j * a.m + gi) * a.Kg);
-      }
-    } else {
-    // chunk index ci = (((j*ntaps + t)*KS + ks)*2 + kc2)*Nn + n, n = gi*Kg + kk,
-    // as mixed-radix digits advanced by bthreads with carries (no division
-    // per chunk)
-    const int rad[6] = {a.Kg, a.m, 2, a.KS, a.ntaps, a.sc};
-    int dig[6], inc[6];
-    {
-      int v = btid, w = bthreads;
-#pragma unroll
-      for (int i = 0; i < 6; ++i) {
-        dig[i] = v % rad[i], v /= rad[i];
-        inc[i] = w % rad[i], w /= rad[i];
-      }
-    }
-    for (int ci = btid; ci < nchunk; ci += bthreads) {
-      const int kk = dig[0], gi = dig[1], kc2 = dig[2], ks = dig[3], t = dig[4], j = dig[5];
-      {
-        int carry = 0;
-#pragma unroll
-        for (int i = 0; i < 6; ++i) {
-          dig[i] += inc[i] + carry;
-          carry = dig[i] >= rad[i];
-          if (carry) dig[i] -= rad[i];
-        }
-      }
-      const int k0 = ks * 16 + kc2 * 8;
-      const int ka = max(k0, gi * a.Cg), kb = min(k0 + 8, (gi + 1) * a.Cg);
-      if (ka >= kb) continue;  // off the diagonal: zero
-      const T* src = wg + ((int64_t)(g0 + j * a.m + gi) * a.Kg + kk) * a.taps_total * a.Cg + (int64_t)t * a.Cg +
-                     (ka - gi * a.Cg);
-      T* dst = B + (size_t)ci * 8 + (ka - k0);
-      const int bytes = (kb - ka) * (int)sizeof(T);
-      const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
-      const uint32_t da = smem_u32(dst);
-      if (bytes == 16 && ((sa | da) & 15) == 0) {
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(da), "l"(src) : "memory");
-      } else if (bytes == 8 && ((sa | da) & 7) == 0) {
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(da), "l"(src) : "memory");
-      } else if (bytes == 4 && ((sa | da) & 3) == 0) {
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(da), "l"(src) : "memory");
-      } else {
-        for (int e = 0; e < kb - ka; ++e) dst[e] = src[e];
-      }
-    }
-    }
-    (void)wa;
-    for (int i = btid; i < a.sc * a.Nn; i += bthreads)
-      bias_s[i] = bg != nullptr ? Elem<T>::to_f32(bg[(int64_t)g0 * a.Kg + i]) : 0.f;
     // Per-issuer MMA lists.  The tile's work is split into units u = grp * np
     // + p (accumulator grp = mt * sc + j, partial p summing the taps t with
     // t % np == p); issuer w owns units w, w + kIssuers, ...  Its list holds,
@@ -466,10 +405,87 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         base += len;
       }
     }
+    grid_dependency_wait();  // w, bias (and, for the epilogue warps, y) from here on
+    asm volatile("bar.sync 2, %0;" ::"r"(kThreads) : "memory");  // barriers initialised
+    T* B = reinterpret_cast<T*>(Bs);
+    if (a.w_tma) {
+      // Cg and Kg multiples of 8: the 8 input channels of a (tap, ks, kc2)
+      // slab lie in one group gi, and for that group the slab's Kg rows n =
+      // gi*Kg + kk are one TMA box {8 channels, 1 tap, Kg output channels}
+      // of the weight tensor viewed as [G*Kg][taps][Cg].
+      // One copy per builder thread (a single thread issuing them all would
+      // serialise about 0.1 us per copy); thread 0 arms the barrier with the
+      // total bytes (copies may complete before that: the transaction count
+      // may go negative until then).
+      const int ncopy = a.sc * a.ntaps * a.KS * 2;
+      if (btid == 0) mbar_arrive_expect_tx(w_full, (uint32_t)ncopy * (uint32_t)a.Kg * 16u);
+      for (int i = btid; i < ncopy; i += bthreads) {
+        const int kc2 = i & 1, r = i >> 1;
+        const int ks = r % a.KS, t = (r / a.KS) % a.ntaps, j = r / (a.KS * a.ntaps);
+        const int k0 = ks * 16 + kc2 * 8;
+        const int gi = k0 / a.Cg, c0 = k0 - gi * a.Cg;
+        tma_load_3d(B + ((size_t)i * a.Nn + (size_t)gi * a.Kg) * 8, &wmap, w_full, c0, t, (g0 + j * a.m + gi) * a.Kg);
+      }
+    } else {
+    // chunk index ci = (((j*ntaps + t)*KS + ks)*2 + kc2)*Nn + n, n = gi*Kg + kk,
+    // as mixed-radix digits advanced by bthreads with carries (no division
+    // per chunk)
+    const int rad[6] = {a.Kg, a.m, 2, a.KS, a.ntaps, a.sc};
+    int dig[6], inc[6];
+    {
+      int v = btid, w = bthreads;
+#pragma unroll
+      for (int i = 0; i < 6; ++i) {
+        dig[i] = v % rad[i], v /= rad[i];
+        inc[i] = w % rad[i], w /= rad[i];
+      }
+    }
+    for (int ci = btid; ci < nchunk; ci += bthreads) {
+      const int kk = dig[0], gi = dig[1], kc2 = dig[2], ks = dig[3], t = dig[4], j = dig[5];
+      {
+        int carry = 0;
+#pragma unroll
+        for (int i = 0; i < 6; ++i) {
+          dig[i] += inc[i] + carry;
+          carry = dig[i] >= rad[i];
+          if (carry) dig[i] -= rad[i];
+        }
+      }
+      const int k0 = ks * 16 + kc2 * 8;
+      const int ka = max(k0, gi * a.Cg), kb = min(k0 + 8, (gi + 1) * a.Cg);
+      if (ka >= kb) continue;  // off the diagonal: zero
+      const T* src = wg + ((int64_t)(g0 + j * a.m + gi) * a.Kg + kk) * a.taps_total * a.Cg + (int64_t)t * a.Cg +
+                     (ka - gi * a.Cg);
+      T* dst = B + (size_t)ci * 8 + (ka - k0);
+      const int bytes = (kb - ka) * (int)sizeof(T);
+      const uintptr_t sa = reinterpret_cast<uintptr_t>(src);
+      const uint32_t da = smem_u32(dst);
+      if (bytes == 16 && ((sa | da) & 15) == 0) {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(da), "l"(src) : "memory");
+      } else if (bytes == 8 && ((sa | da) & 7) == 0) {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(da), "l"(src) : "memory");
+      } else if (bytes == 4 && ((sa | da) & 3) == 0) {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(da), "l"(src) : "memory");
+      } else {
+        for (int e = 0; e < kb - ka; ++e) dst[e] = src[e];
+      }
+    }
+    }
+    (void)wa;
+    for (int i = btid; i < a.sc * a.Nn; i += bthreads)
+      bias_s[i] = bg != nullptr ? Elem<T>::to_f32(bg[(int64_t)g0 * a.Kg + i]) : 0.f;
+    if (warp == 1) {  // while the weight copies are in flight
+      __syncwarp();     // the allocation is a whole-warp instruction
+      tmem_alloc(tmem_slot, a.tmem_cols);
+      tmem_relinquish();
+    }
     asm volatile("cp.async.wait_all;" ::: "memory");
     if (a.w_tma && !mbar_wait(w_full, 0u, a.wait_limit_ns)) report(a.status, kDevTimeout, 6);
     fence_proxy_async_smem();  // generic-proxy writes of B -> visible to the tensor core
+    fence_before_sync();
     asm volatile("bar.sync 1, %0;" ::"r"(bthreads) : "memory");
+    fence_after_sync();
+    tmem_base = *tmem_slot;
   }
 
   if (warp == 0) {
@@ -612,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
   __syncwarp();
   fence_before_sync();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     fence_after_sync();
     tmem_dealloc(tmem_base, a.tmem_cols);
   }

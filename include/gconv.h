@@ -112,6 +112,14 @@ typedef struct gconv_options {
                             16-byte chunk planes, [7] extra shared memory (KB),
                             negative: stage the epilogue through shared memory
                             for coalesced stores (default: store from registers). */
+  int32_t serial_launch; /* 0: the kernel is launched as a programmatic dependent
+                            launch: its CTAs may start, and set up barriers,
+                            tensor memory and tables, while the previous kernel
+                            in the stream is still running; every access to
+                            global memory waits until that kernel has completed
+                            and its writes are visible, so stream order holds
+                            for x, w, bias and y.  1: plain launch (the kernel
+                            starts only after the previous one has finished). */
 } gconv_options;
 
 /*

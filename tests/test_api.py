@@ -42,7 +42,9 @@ def test_struct_layout():
     assert ctypes.sizeof(B.gconv_problem) == 88
     assert B.gconv_problem.N.offset == 8
     assert B.gconv_problem.dil.offset == 76
-    assert ctypes.sizeof(B.gconv_options) == 56
+    assert ctypes.sizeof(B.gconv_options) == 64
+    assert B.gconv_options.tile.offset == 24
+    assert B.gconv_options.serial_launch.offset == 56
 
 
 def good(**kw):
