@@ -193,9 +193,24 @@ def whole_job_rate(units_per_step: float, steps: int, world: int, max_ms: float)
 
 
 # ---------------------------------------------------------------------------
-def kernel_source_hash() -> str:
+# Sources each kernel's device code and launch plan are built from (the
+# tensor-core files do not enter the depthwise kernel, and so on).
+KERNEL_SOURCES = {
+    "direct_dw": ("api.cu", "common.cuh", "kernels.h", "plan_cache.h", "dw.cu", "dw_f16.cu", "dw_bf16.cu",
+                  "dw_f32.cu", "dw_impl.cuh", "dwc_impl.cuh", "dw_launch.cuh"),
+    "igemm_tc": ("api.cu", "common.cuh", "kernels.h", "plan_cache.h", "tc.cu", "tc_impl.cuh", "tc_ptx.cuh"),
+    "direct_generic": ("api.cu", "common.cuh", "kernels.h", "plan_cache.h", "generic.cu"),
+}
+
+
+def kernel_source_hash(kernel_name: str = None) -> str:
+    """Hash of the sources of one kernel (all of csrc/ when no name is given);
+    stored DRAM-traffic counters are valid only while it matches."""
+    csrc = os.path.join(ROOT, "depthwise_convolution_forward_gb300", "csrc")
+    names = KERNEL_SOURCES.get(kernel_name)
+    paths = [os.path.join(csrc, n) for n in names] if names else sorted(glob.glob(os.path.join(csrc, "*")))
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "depthwise_convolution_forward_gb300", "csrc", "*"))):
+    for p in paths:
         h.update(open(p, "rb").read())
     return h.hexdigest()[:16]
 
@@ -214,7 +229,7 @@ def load_traffic(kernel_name: str, workload: str):
         return None
     d = json.load(open(p))
     ent = d.get(f"{kernel_name}:{workload}")
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or ent.get("source_hash") != kernel_source_hash(kernel_name):
         return None
     return ent.get("dram_bytes_per_launch")
 

@@ -166,7 +166,7 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
       // The same lists the kernel would build, with shared-memory offsets
       // instead of descriptors (the kernel adds its shared-memory base).
       const int units = G2 * np, steps = ((taps + np - 1) / np) * c.KS;
-      const uint32_t lbo_b = (uint32_t)c.Nn * 16u;
+      const uint32_t slab = (uint32_t)c.Nn * 16u;  // one (chunk, K step, K half, tap) slab of B
       int base = 0;
       for (int w = 0; w < tc::kIssuers; ++w) {
         const int nu = units > w ? (units - w + tc::kIssuers - 1) / tc::kIssuers : 0;
@@ -185,7 +185,7 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
             else
               aoff = c.a_off + (uint32_t)(c.tap_phase[t] * c.nchunks + 2 * ks) * c.plane_stride +
                      (uint32_t)(mt * 128 + c.tap_off[t]) * 16u;
-            const uint32_t boff = c.b_off + (uint32_t)(((j * taps + t) * c.KS + ks) * 2) * lbo_b;
+            const uint32_t boff = c.b_off + (uint32_t)((j * c.KS + ks) * 2 * taps + t) * slab;
             e = make_uint2((aoff >> 4) | ((boff >> 4) << 16),
                            (uint32_t)((pp * G2 + grp) * c.Nn) | ((st == 0 ? 0u : 1u) << 16));
           }
@@ -302,20 +302,25 @@ cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   if (encode_tiled(&map, tt, 5, la.x, dims, strides, box, estr,
                    p.sw ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  // Weights as [G*Kg][taps][Cg] for TMA staging of the block-diagonal B
-  // (8-channel boxes of Kg output channels); otherwise the threads copy them.
+  // Weights viewed as (Cg, G*Kg, taps) -- channels innermost, then output
+  // channel rows, then taps -- for TMA staging of the block-diagonal B: a box
+  // of 8 channels x Kg rows x (all taps when one group fills a chunk, else 1
+  // tap) lands as [tap][row][8], the tap-major order of B's slabs.  Otherwise
+  // the threads copy them.
   CUtensorMap wmap = map;
   int w_tma = 0;
+  const uint64_t taps = (uint64_t)g.taps();
+  const int box_taps = (p.a.m == 1 && taps <= 256) ? (int)taps : 1;
   if (g.Cg % 8 == 0 && g.Kg % 8 == 0 && (reinterpret_cast<uintptr_t>(la.w) & 15) == 0) {
-    const uint64_t taps = (uint64_t)g.taps();
-    uint64_t wdims[3] = {(uint64_t)g.Cg, taps, (uint64_t)g.K()};
-    uint64_t wstrides[2] = {(uint64_t)g.Cg * es, taps * g.Cg * es};
-    uint32_t wbox[3] = {8u, 1u, (uint32_t)g.Kg};
+    uint64_t wdims[3] = {(uint64_t)g.Cg, (uint64_t)g.K(), taps};
+    uint64_t wstrides[2] = {taps * g.Cg * es, (uint64_t)g.Cg * es};
+    uint32_t wbox[3] = {8u, (uint32_t)g.Kg, (uint32_t)box_taps};
     uint32_t westr[3] = {1u, 1u, 1u};
     if (encode_tiled(&wmap, tt, 3, la.w, wdims, wstrides, wbox, westr) == CUDA_SUCCESS) w_tma = 1;
   }
   TcArgs a = p.a;
   a.w_tma = w_tma;
+  a.w_box_taps = box_taps;
   a.w = la.w;
   a.bias = la.bias;
   a.y = la.y;

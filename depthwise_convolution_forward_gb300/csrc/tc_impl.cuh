@@ -64,6 +64,7 @@ struct TcArgs {
   uint32_t a_off, b_off, bias_off, tab_off;  // smem offsets (tab: MMA descriptor table)
   uint32_t epi_off;  // epilogue staging (4 x 4 KB), or 0 to store straight from registers
   int w_tma;         // 1: weights staged by TMA through the weight tensor map (Cg, Kg % 8 == 0)
+  int w_box_taps;    // taps one weight box covers: all of them (one group per chunk) or 1
   int stages;
   uint32_t tmem_cols, idesc;
   int n_gc, cpg, tiles_w, tiles_h;
@@ -320,9 +321,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     // previous kernel in the stream.
     const int btid = tid - 32, bthreads = (int)blockDim.x - 32;
     // Weights of this group chunk as block-diagonal B_t[n][k], K-major core
-    // matrices: byte offset ((((t*KS + ks)*2 + kc2)*Nn + n)*8 + e)*2 holds
-    // k = ks*16 + kc2*8 + e, in sc sub-blocks (one per group chunk j), each
-    // [t][ks][kc2][n][8].  Walked in destination order (consecutive threads
+    // matrices: byte offset (((((j*KS + ks)*2 + kc2)*ntaps + t)*Nn + n)*8 + e)*2
+    // holds k = ks*16 + kc2*8 + e of tap t for group chunk j, i.e. slabs
+    // [j][ks][kc2][t] of Nn rows x 16 bytes.  The two K halves of one MMA are
+    // ntaps slabs apart (the descriptor's leading byte offset), and the taps
+    // of one (j, ks, kc2) are consecutive, so one TMA box can fill them all.
+    // The thread copy walks chunks in destination order (consecutive threads
     // fill consecutive 16-byte chunks: no bank conflicts); each chunk's
     // nonzero run (the input channels of output n's group) is one cp.async
     // when it is 16, 8 or 4 bytes and aligned, and every thread issues all its
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     if (a.ntab > 0) {
       uint4* tab = reinterpret_cast<uint4*>(smem + a.tab_off);
       const uint32_t base = smem_u32(smem);
-      const uint32_t lbo_b = (uint32_t)a.Nn * 16u;
+      const uint32_t lbo_b = (uint32_t)(a.ntaps * a.Nn) * 16u;
       for (int i = btid; i < a.ntab; i += bthreads) {
         const uint2 e = a.tab[i];
         uint4 e0 = make_uint4(0u, 0u, 0u, 0u);
@@ -371,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
       const int units = G2 * NP;
       const int steps = ((a.ntaps + NP - 1) / NP) * a.KS;
       const uint32_t a_base = smem_u32(As), b_base = smem_u32(Bs);
-      const uint32_t lbo_b = (uint32_t)a.Nn * 16u;
+      const uint32_t lbo_b = (uint32_t)(a.ntaps * a.Nn) * 16u;
       int base = 0;
       for (int w = 0; w < kIssuers; ++w) {
         const int nu = units > w ? (units - w + kIssuers - 1) / kIssuers : 0;
@@ -395,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
               adesc = smem_desc(plane0 + (uint32_t)(2 * ks) * a.plane_stride + row0, a.plane_stride, 128u);
             }
             const uint64_t bdesc =
-                smem_desc(b_base + (uint32_t)(((j * a.ntaps + t) * a.KS + ks) * 2) * lbo_b, lbo_b, 128u);
+                smem_desc(b_base + (uint32_t)(((j * a.KS + ks) * 2 * a.ntaps + t) * a.Nn) * 16u, lbo_b, 128u);
             e0 = make_uint4((uint32_t)adesc, (uint32_t)(adesc >> 32), (uint32_t)bdesc, (uint32_t)(bdesc >> 32));
             e1 = make_uint4((uint32_t)((p * G2 + grp) * a.Nn), 0u, 0u, st == 0 ? 0u : 1u);
           }
@@ -408,29 +412,39 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     grid_dependency_wait();  // w, bias (and, for the epilogue warps, y) from here on
     asm volatile("bar.sync 2, %0;" ::"r"(kThreads) : "memory");  // barriers initialised
     T* B = reinterpret_cast<T*>(Bs);
+    // Bias: the first value of each thread is loaded now and stored once the
+    // weight copies are issued, so its latency overlaps them.
+    const int nbias = a.sc * a.Nn;
+    T b_first = Elem<T>::from_f32(0.f);
+    if (btid < nbias && bg != nullptr) b_first = bg[(int64_t)g0 * a.Kg + btid];
     if (a.w_tma) {
-      // Cg and Kg multiples of 8: the 8 input channels of a (tap, ks, kc2)
-      // slab lie in one group gi, and for that group the slab's Kg rows n =
-      // gi*Kg + kk are one TMA box {8 channels, 1 tap, Kg output channels}
-      // of the weight tensor viewed as [G*Kg][taps][Cg].
-      // One copy per builder thread (a single thread issuing them all would
-      // serialise about 0.1 us per copy); thread 0 arms the barrier with the
-      // total bytes (copies may complete before that: the transaction count
-      // may go negative until then).
-      const int ncopy = a.sc * a.ntaps * a.KS * 2;
-      if (btid == 0) mbar_arrive_expect_tx(w_full, (uint32_t)ncopy * (uint32_t)a.Kg * 16u);
+      // Cg and Kg multiples of 8: the 8 input channels of a (ks, kc2) slab lie
+      // in one group gi, and for that group the slab's Kg rows n = gi*Kg + kk
+      // are one TMA box {8 channels, Kg output channels, taps} of the weight
+      // tensor viewed as (Cg, G*Kg, taps).  With one group per chunk (m = 1)
+      // a box covers every tap (its [tap][row][8] landing order is the slabs'
+      // order); otherwise one tap, at row offset gi*Kg of the slab.
+      // Copies are spread over the builder threads (a single thread issuing
+      // them all would serialise about 0.1 us per copy); thread 0 arms the
+      // barrier with the total bytes (copies may complete before that: the
+      // transaction count may go negative until then).
+      const int per = a.w_box_taps, nt = a.ntaps / per;
+      const int ncopy = a.sc * a.KS * 2 * nt;
+      if (btid == 0) mbar_arrive_expect_tx(w_full, (uint32_t)ncopy * (uint32_t)(a.Kg * per) * 16u);
       for (int i = btid; i < ncopy; i += bthreads) {
-        const int kc2 = i & 1, r = i >> 1;
-        const int ks = r % a.KS, t = (r / a.KS) % a.ntaps, j = r / (a.KS * a.ntaps);
+        const int tq = i % nt, r = i / nt;  // r = (j*KS + ks)*2 + kc2
+        const int kc2 = r & 1, ks = (r >> 1) % a.KS, j = (r >> 1) / a.KS;
         const int k0 = ks * 16 + kc2 * 8;
         const int gi = k0 / a.Cg, c0 = k0 - gi * a.Cg;
-        tma_load_3d(B + ((size_t)i * a.Nn + (size_t)gi * a.Kg) * 8, &wmap, w_full, c0, t, (g0 + j * a.m + gi) * a.Kg);
+        const int t = tq * per;
+        tma_load_3d(B + ((size_t)(r * a.ntaps + t) * a.Nn + (size_t)gi * a.Kg) * 8, &wmap, w_full, c0,
+                    (g0 + j * a.m + gi) * a.Kg, t);
       }
     } else {
-    // chunk index ci = (((j*ntaps + t)*KS + ks)*2 + kc2)*Nn + n, n = gi*Kg + kk,
-    // as mixed-radix digits advanced by bthreads with carries (no division
-    // per chunk)
-    const int rad[6] = {a.Kg, a.m, 2, a.KS, a.ntaps, a.sc};
+    // chunk index ci = ((((j*KS + ks)*2 + kc2)*ntaps + t)*Nn + n, n = gi*Kg +
+    // kk, as mixed-radix digits advanced by bthreads with carries (no
+    // division per chunk)
+    const int rad[6] = {a.Kg, a.m, a.ntaps, 2, a.KS, a.sc};
     int dig[6], inc[6];
     {
       int v = btid, w = bthreads;
@@ -441,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
       }
     }
     for (int ci = btid; ci < nchunk; ci += bthreads) {
-      const int kk = dig[0], gi = dig[1], kc2 = dig[2], ks = dig[3], t = dig[4], j = dig[5];
+      const int kk = dig[0], gi = dig[1], t = dig[2], kc2 = dig[3], ks = dig[4], j = dig[5];
       {
         int carry = 0;
 #pragma unroll
@@ -472,7 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     }
     }
     (void)wa;
-    for (int i = btid; i < a.sc * a.Nn; i += bthreads)
+    if (btid < nbias) bias_s[btid] = Elem<T>::to_f32(b_first);
+    for (int i = btid + bthreads; i < nbias; i += bthreads)
       bias_s[i] = bg != nullptr ? Elem<T>::to_f32(bg[(int64_t)g0 * a.Kg + i]) : 0.f;
     if (warp == 1) {  // while the weight copies are in flight
       __syncwarp();     // the allocation is a whole-warp instruction
@@ -500,6 +515,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
           break;
         }
         if (withhold && k == 0) continue;
+        // At launch every CTA requests its stages at once.  Holding the second
+        // tile's copy until the first tile and the weights have landed lets
+        // the first MMAs start sooner; later copies overlap the MMAs.
+        if (k == 1 && !withhold &&
+            (!mbar_wait(&a_full[0], 0u, a.wait_limit_ns) || (a.w_tma && !mbar_wait(w_full, 0u, a.wait_limit_ns)))) {
+          failed = true;
+          break;
+        }
         const SpatialTile st = decode_spatial(a, sp);
         const int id0 = st.od * a.sD - a.pD;
         mbar_arrive_expect_tx(&a_full[s], a.tx_bytes);
