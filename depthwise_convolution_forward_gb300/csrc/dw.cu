@@ -20,8 +20,8 @@ bool dw_supported(const Geometry& g, DType dt, const LaunchArgs* a) {
   if (g.C() % vec != 0) return false;
   if (g.Z > 7 || (g.Z - 1) * g.dD + 1 > 16) return false;
   if (g.W > (1 << 30) || g.H > (1 << 30)) return false;
-  // tile indices are decoded in 32 bits
-  if ((double)g.N * g.Do * g.Ho * g.Wo * (double)g.C() >= 2e9) return false;
+  // the image index is a 32-bit tensor-map coordinate (element offsets are 64-bit)
+  if (g.N >= (int64_t)1 << 31) return false;
   // all weights stay resident in shared memory (fp32 copy, at most 64 KB)
   if ((int64_t)g.taps() * g.C() * 4 > 64 * 1024) return false;
   if (a) {

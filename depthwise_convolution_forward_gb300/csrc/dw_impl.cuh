@@ -55,10 +55,25 @@ struct TileCoord {
 };
 
 // Tile index -> coordinates, channel tile fastest.  32-bit unsigned
-// arithmetic: the host only launches when the tile count fits.
+// arithmetic while the tile count fits in 32 bits, 64-bit beyond.
 __device__ __forceinline__ TileCoord decode_tile(const DwArgs& a, int64_t t64) {
-  uint32_t t = (uint32_t)t64;
   TileCoord c;
+  if (a.num_tiles > 0xffffffffll) {  // more tiles than 32 bits count: 64-bit division
+    int64_t q64 = t64 / a.tiles_c;
+    c.ct = (int)(t64 - q64 * a.tiles_c);
+    t64 = q64;
+    q64 = t64 / a.tiles_w;
+    c.tw = (int)(t64 - q64 * a.tiles_w);
+    t64 = q64;
+    q64 = t64 / a.tiles_h;
+    c.th = (int)(t64 - q64 * a.tiles_h);
+    t64 = q64;
+    q64 = t64 / a.Do;
+    c.od = (int)(t64 - q64 * a.Do);
+    c.n = (int)q64;
+    return c;
+  }
+  uint32_t t = (uint32_t)t64;
   uint32_t q = t / (uint32_t)a.tiles_c;
   c.ct = (int)(t - q * (uint32_t)a.tiles_c);
   t = q;

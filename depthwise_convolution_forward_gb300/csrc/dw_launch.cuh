@@ -343,7 +343,9 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
     if (!planned && kind != 3) planned = make_plan(g, es, la.tile, dev.num_sms, &p);
     if (!planned) return cudaErrorNotSupported;
     if (p.direct) {
-      if (pick_ldg_kernel<T>(g.sH, g.dH, p.WB, p.mode) == nullptr) return cudaErrorNotSupported;
+      // one CTA per tile: the grid's x extent bounds the tile count
+      if (p.num_tiles >= ((int64_t)1 << 31) || pick_ldg_kernel<T>(g.sH, g.dH, p.WB, p.mode) == nullptr)
+        return cudaErrorNotSupported;
     } else {
       DwKernel<T> k = p.col ? pick_col_kernel<T>(g.sH, g.dH, p.mode) : pick_kernel<T>(g.sH, g.dH, p.WB, p.mode);
       if (k == nullptr || p.smem_bytes > (uint32_t)dev.max_smem_optin) return cudaErrorNotSupported;

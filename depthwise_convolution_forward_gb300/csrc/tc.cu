@@ -133,20 +133,21 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     c.a_stage_bytes = round_up((uint32_t)(c.nphase * c.nchunks) * c.plane_stride, 1024);
     c.tx_bytes = (uint32_t)(c.nphase * c.nchunks) * (uint32_t)(c.Dh * c.Hh * c.P) * row_bytes;
     const uint32_t b_bytes = round_up((uint32_t)(c.sc * taps * c.Kt * c.Nn * 2), 1024);
-    // Partial accumulators so that the tile has at least kIssuers
-    // independent units of MMA work: np in {4, 2, 1} within 512 TMEM columns.
     // Partial accumulators (taps split np ways, summed by the epilogue): at
-    // least enough that the tile has kIssuers independent units of MMA work.
+    // least enough that the tile has kIssuers independent units of MMA work,
+    // within 512 TMEM columns.  An explicit count (override slot 4) replaces
+    // that minimum (issuers without a unit then only commit).
     const int G2 = c.sc * c.nmt;
     int np = 1;
     while (np * 2 <= tc::kIssuers && G2 * np < tc::kIssuers && np * 2 <= taps &&
            2 * (np * 2) * G2 * c.Nn <= 512)
       np *= 2;
-    if (np_cand < np || np_cand > taps) continue;
-    np = np_cand;
     if (ov && ov[4]) {
-      if (np_cand != 1) continue;
+      if (np_cand != 1 || ov[4] < 1 || ov[4] > taps) continue;
       np = ov[4];
+    } else {
+      if (np_cand < np || np_cand > taps) continue;
+      np = np_cand;
     }
     c.np = np;
     // per-issuer MMA lists: 32 bytes per entry
