@@ -1,4 +1,5 @@
-"""CPU oracle for grouped convolution forward -- TEST INFRASTRUCTURE ONLY.
+"""CPU oracle for grouped convolution forward and backward data -- TEST
+INFRASTRUCTURE ONLY.
 
 The oracle (``oracle.c``) is a plain fp64 direct-loop grouped convolution
 written from the definition (see the header of ``oracle.c`` for the formula,
@@ -63,6 +64,8 @@ class Oracle:
         lib.oracle_grouped_conv_fwd_points.argtypes = (
             [_dp, _dp, _dp] + [ctypes.c_long] * 4 + [_i32p] * 5
             + [ctypes.POINTER(ctypes.c_int64), ctypes.c_long, _dp])
+        lib.oracle_grouped_conv_bwd_data.restype = ctypes.c_int
+        lib.oracle_grouped_conv_bwd_data.argtypes = [_dp, _dp, _dp] + [ctypes.c_long] * 4 + [_i32p] * 5
         self.lib = lib
 
     # -- helpers ---------------------------------------------------------
@@ -118,6 +121,21 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle rejected the problem or an index")
         return out
+
+
+    def bwd_data(self, prob, dy, w) -> np.ndarray:
+        """Backward data: dx as float64 in x's layout [N, (D), H, W, G, Cg] (D
+        omitted for 2D), the adjoint of ``forward`` in x applied to ``dy``."""
+        dyd, wd = self._f64(dy), self._f64(w)
+        D, H, W = prob.inp
+        dx = np.empty((prob.N, D, H, W, prob.G, prob.Cg), dtype=np.float64)
+        rc = self.lib.oracle_grouped_conv_bwd_data(
+            dyd.ctypes.data_as(_dp), wd.ctypes.data_as(_dp), dx.ctypes.data_as(_dp), *self._args(prob))
+        if rc != 0:
+            raise ValueError("oracle rejected the problem")
+        if prob.ndim == 2:
+            dx = dx.reshape(prob.N, H, W, prob.G, prob.Cg)
+        return dx
 
 
 _default: Optional[Oracle] = None

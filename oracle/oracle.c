@@ -179,3 +179,71 @@ int oracle_grouped_conv_fwd_points(const double *x, const double *w, const doubl
     }
     return bad ? -1 : 0;
 }
+
+/*
+ * Backward data: the gradient with respect to x of a loss whose gradient
+ * with respect to y is dy, i.e. the adjoint (transpose) of the forward map in
+ * x.  Grouped Convolution Tile Engine and Grouped Convolution -- Python
+ * Examples (Examples, Runner argument contract): a backward-data variant
+ * takes dY and W.  Written as the forward definition read backwards -- every
+ * product dy * w that the forward sum would have formed from input position
+ * i is accumulated into dx at i:
+ *
+ *   dx[n, id, ih, iw, g, cg] += dy[n, od, oh, ow, g, k] * w[g, k, z, yy, xx, cg]
+ *     for every (od, oh, ow, k, z, yy, xx) with
+ *     id = od*sD - pD + z*dD,  ih = oh*sH - pH + yy*dH,  iw = ow*sW - pW + xx*dW
+ *     inside the input; dx starts at zero.
+ *
+ * Layouts: dy [N][Do][Ho][Wo][G][Kg] (the forward output layout), w as in the
+ * forward pass, dx [N][D][H][W][G][Cg] (the forward input layout).  Parallel
+ * over (n, g): those slices of dx are disjoint.  Returns 0, or -1 for a
+ * malformed or empty problem.
+ */
+int oracle_grouped_conv_bwd_data(const double *dy, const double *w, double *dx,
+                                 long N, long G, long Cg, long Kg,
+                                 const int32_t *in3, const int32_t *ker3, const int32_t *st3,
+                                 const int32_t *pd3, const int32_t *dl3)
+{
+    long in[3], ker[3], st[3], pd[3], dl[3], out[3];
+    if (N <= 0 || G <= 0 || Cg <= 0 || Kg <= 0)
+        return -1;
+    if (unpack(in3, ker3, st3, pd3, dl3, in, ker, st, pd, dl, out))
+        return -1;
+    const long D = in[0], H = in[1], W = in[2];
+    const long Z = ker[0], Y = ker[1], X = ker[2];
+    const long Do = out[0], Ho = out[1], Wo = out[2];
+    const long C = G * Cg, K = G * Kg;
+    const long nx = N * D * H * W * C;
+    for (long i = 0; i < nx; ++i)
+        dx[i] = 0.0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long ng = 0; ng < N * G; ++ng) {
+        const long n = ng / G, g = ng % G;
+        for (long od = 0; od < Do; ++od)
+            for (long oh = 0; oh < Ho; ++oh)
+                for (long ow = 0; ow < Wo; ++ow)
+                    for (long k = 0; k < Kg; ++k) {
+                        const double d = dy[(((n * Do + od) * Ho + oh) * Wo + ow) * K + g * Kg + k];
+                        for (long z = 0; z < Z; ++z) {
+                            const long id = od * st[0] - pd[0] + z * dl[0];
+                            if (id < 0 || id >= D)
+                                continue;
+                            for (long yy = 0; yy < Y; ++yy) {
+                                const long ih = oh * st[1] - pd[1] + yy * dl[1];
+                                if (ih < 0 || ih >= H)
+                                    continue;
+                                for (long xx = 0; xx < X; ++xx) {
+                                    const long iw = ow * st[2] - pd[2] + xx * dl[2];
+                                    if (iw < 0 || iw >= W)
+                                        continue;
+                                    double *xp = dx + ((((n * D + id) * H + ih) * W + iw) * C + g * Cg);
+                                    const double *wp = w + ((((g * Kg + k) * Z + z) * Y + yy) * X + xx) * Cg;
+                                    for (long cg = 0; cg < Cg; ++cg)
+                                        xp[cg] += d * wp[cg];
+                                }
+                            }
+                        }
+                    }
+    }
+    return 0;
+}

@@ -275,3 +275,62 @@ ALL_PINS = [
     pin_out_extent_vs_torch,
     pin_points_match_forward,
 ]
+
+
+# ---------------------------------------------------------------------------
+# Backward data: pins that do not use the oracle's own backward code
+# ---------------------------------------------------------------------------
+def torch_bwd_data(p: Workload, dy, w):
+    """torch.nn.grad.conv{2,3}d_input(groups=G) on CPU float64, layouts permuted."""
+    dyt = torch.as_tensor(np.asarray(dy, dtype=np.float64))
+    wt = torch.as_tensor(np.asarray(w, dtype=np.float64))
+    if p.ndim == 2:
+        Ho, Wo = dyt.shape[1], dyt.shape[2]
+        dyc = dyt.reshape(p.N, Ho, Wo, p.K).permute(0, 3, 1, 2)
+        wc = wt.reshape(p.K, p.ker[1], p.ker[2], p.Cg).permute(0, 3, 1, 2)
+        dx = torch.nn.grad.conv2d_input((p.N, p.C, p.inp[1], p.inp[2]), wc, dyc, stride=p.stride[1:],
+                                        padding=p.pad[1:], dilation=p.dil[1:], groups=p.G)
+        return dx.permute(0, 2, 3, 1).reshape(p.N, p.inp[1], p.inp[2], p.G, p.Cg).numpy()
+    dyc = dyt.reshape(p.N, *dyt.shape[1:4], p.K).permute(0, 4, 1, 2, 3)
+    wc = wt.reshape(p.K, *p.ker, p.Cg).permute(0, 4, 1, 2, 3)
+    dx = torch.nn.grad.conv3d_input((p.N, p.C, *p.inp), wc, dyc, stride=p.stride, padding=p.pad,
+                                    dilation=p.dil, groups=p.G)
+    return dx.permute(0, 2, 3, 4, 1).reshape(p.N, *p.inp, p.G, p.Cg).numpy()
+
+
+def bwd_problems():
+    return [
+        wl(2, 2, 4, 3, 2, (9, 7), (3, 3), (1, 1), (1, 1), (1, 1)),
+        wl(2, 1, 6, 1, 1, (8, 9), (3, 3), (2, 2), (1, 1), (1, 1)),  # depthwise, stride 2
+        wl(2, 1, 3, 2, 5, (10, 9), (3, 3), (2, 1), (2, 2), (2, 2)),
+        wl(3, 1, 2, 3, 2, (5, 6, 6), (3, 3, 3), (1, 2, 1), (1, 1, 1), (1, 1, 2)),
+        wl(2, 2, 1, 5, 4, (7, 6), (3, 2), (1, 1), (1, 0), (1, 1)),  # groups == 1
+        wl(2, 1, 2, 2, 3, (6, 6), (1, 1), (1, 1), (1, 1), (1, 1)),  # pad beyond the filter
+    ]
+
+
+def _rand_dy(p: Workload, orc, seed):
+    out = orc.out_shape(p)
+    shape = (p.N, out[1], out[2], p.G, p.Kg) if p.ndim == 2 else (p.N, *out, p.G, p.Kg)
+    return np.random.default_rng(seed).uniform(-1, 1, size=shape)
+
+
+def pin_bwd_adjoint(orc):
+    """Backward data is the adjoint of the (pinned) forward map in x:
+    <forward(x), dy> == <x, bwd_data(dy)> for any x, dy (no bias)."""
+    for i, p in enumerate(bwd_problems()):
+        x, w, _ = rand_inputs(p, 300 + i)
+        dy = _rand_dy(p, orc, 400 + i)
+        lhs = float(np.sum(orc.forward(p, x, w, None) * dy))
+        rhs = float(np.sum(x.reshape(orc.bwd_data(p, dy, w).shape) * orc.bwd_data(p, dy, w)))
+        assert abs(lhs - rhs) <= 1e-10 * (1.0 + abs(lhs)), (i, lhs, rhs)
+
+
+def pin_bwd_torch(orc):
+    for i, p in enumerate(bwd_problems()):
+        _, w, _ = rand_inputs(p, 500 + i)
+        dy = _rand_dy(p, orc, 600 + i)
+        _close(orc.bwd_data(p, dy, w), torch_bwd_data(p, dy, w))
+
+
+BWD_PINS = [pin_bwd_adjoint, pin_bwd_torch]
