@@ -61,6 +61,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tile", default="", help="tuning override TH,TW,WB,stages,ctas_per_sm,fma_form")
     ap.add_argument("--force-kernel", type=int, default=0)
+    ap.add_argument("--op", choices=["fwd", "bwd_data"], default="fwd",
+                    help="fwd: the forward pass (default); bwd_data: the gradient with respect to x, given dy "
+                         "(no end-to-end leg)")
     ap.add_argument("--serial-launch", action="store_true",
                     help="launch without programmatic dependent launch (each kernel starts after the previous ends)")
     return ap.parse_args()
@@ -283,13 +286,20 @@ def cpu_oracle_prepare(wls):
     return orc, prep, np
 
 
-def cpu_baseline(wls, min_seconds=10.0, max_seconds=30.0):
+def cpu_baseline(wls, min_seconds=10.0, max_seconds=30.0, op="fwd"):
     """Whole-workload oracle passes, repeated for about min_seconds."""
     orc, prep, np = cpu_oracle_prepare(wls)
+    if op == "bwd_data":
+        for p in prep:
+            p["dy"] = np.random.default_rng(1).uniform(-1, 1, size=(p["wl"].N,) + tuple(
+                o for o in orc.out_shape(p["wl"])[3 - p["wl"].ndim:]) + (p["wl"].G, p["wl"].Kg))
     reps, t0 = 0, time.perf_counter()
     while True:
         for p in prep:
-            orc.forward(p["wl"], p["x"], p["w"], p["b"])
+            if op == "bwd_data":
+                orc.bwd_data(p["wl"], p["dy"], p["w"])
+            else:
+                orc.forward(p["wl"], p["x"], p["w"], p["b"])
         reps += 1
         el = time.perf_counter() - t0
         if el >= min_seconds or el * (reps + 1) / reps > max_seconds:
@@ -299,7 +309,7 @@ def cpu_baseline(wls, min_seconds=10.0, max_seconds=30.0):
     tot_flops = sum(p["flops"] for p in prep)
     return {"value": tot_bytes / per / 1e9, "unit": "GB/s", "tflops": tot_flops / per / 1e12,
             "cores": oracle_threads(), "kind": "oracle",
-            "sample": f"{reps} full pass(es) of the whole workload ({len(prep)} convolutions), "
+            "sample": f"{reps} full pass(es) of the whole workload ({len(prep)} convolutions, {op}), "
                       f"{el:.1f} s of fp64 direct-loop OpenMP work", "ms_per_step": per * 1e3}
 
 
@@ -371,8 +381,12 @@ def run_ours(args, wls, set_name, rank, world):
     convs = []
     step_bytes = 0
     step_flops = 0
+    bwd = args.op == "bwd_data"
     for wl in wls:
         x, w, b = inputs.make_inputs(wl)
+        if bwd:
+            wl = wl.with_(bias=False)
+            b = None
         p = gc.problem_of(wl)
         out = gc.grouped_conv_out_shape(p)
         ysh = (wl.N, out[1], out[2], wl.G, wl.Kg) if wl.ndim == 2 else (wl.N, *out, wl.G, wl.Kg)
@@ -389,12 +403,22 @@ def run_ours(args, wls, set_name, rank, world):
     for r in range(R):
         s = []
         for c in convs:
-            xd = c["x"].to(dev)
             wd = c["w"].to(dev)
-            bd = c["b"].to(dev) if c["b"] is not None else None
-            yd = torch.empty(c["ysh"], dtype=c["x"].dtype, device=dev)
+            if bwd:  # input dy (forward output layout, U(-1, 1)), output dx (forward input layout)
+                g = torch.Generator().manual_seed(9500 + r)
+                xd = (torch.rand(c["ysh"], generator=g) * 2 - 1).to(c["x"].dtype).to(dev)
+                yd = torch.empty(c["x"].shape, dtype=c["x"].dtype, device=dev)
+                bd = None
+            else:
+                xd = c["x"].to(dev)
+                bd = c["b"].to(dev) if c["b"] is not None else None
+                yd = torch.empty(c["ysh"], dtype=c["x"].dtype, device=dev)
             s.append((xd, wd, bd, yd))
         sets.append(s)
+    if bwd:  # one workspace per convolution (stream order keeps consecutive calls apart)
+        for c in convs:
+            c["ws_bytes"] = gc.grouped_conv_bwd_data_workspace_size(c["p"], c["dt"])
+            c["ws"] = torch.empty(max(1, c["ws_bytes"]), dtype=torch.uint8, device=dev)
     torch.cuda.synchronize(dev)
 
     opt = B.gconv_options()
@@ -407,10 +431,17 @@ def run_ours(args, wls, set_name, rank, world):
     def launch(r, ci):
         c = convs[ci]
         xd, wd, bd, yd = sets[r][ci]
-        st = lib.grouped_conv_fwd_ex(xd.data_ptr(), wd.data_ptr(), bd.data_ptr() if bd is not None else None,
-                                     yd.data_ptr(), ctypes.byref(c["p"]), c["dt"], sh, optp)
+        if bwd:
+            st = lib.grouped_conv_bwd_data_ex(xd.data_ptr(), wd.data_ptr(), yd.data_ptr(), ctypes.byref(c["p"]),
+                                              c["dt"], c["ws"].data_ptr() if c["ws_bytes"] else None,
+                                              c["ws_bytes"], sh, optp)
+        else:
+            st = lib.grouped_conv_fwd_ex(xd.data_ptr(), wd.data_ptr(), bd.data_ptr() if bd is not None else None,
+                                         yd.data_ptr(), ctypes.byref(c["p"]), c["dt"], sh, optp)
         if st != 0:
-            raise RuntimeError(f"grouped_conv_fwd_ex failed: {gc.gconv_last_error()}")
+            raise RuntimeError(f"grouped_conv launch failed: {gc.gconv_last_error()}")
+        if bwd:
+            c["kernel"] = opt.selected
 
     # warm-up (eager): plans cached, device state initialised
     with torch.cuda.stream(stream):
@@ -524,7 +555,7 @@ def run_ours(args, wls, set_name, rank, world):
     else:
         achieved = d["flops"] / (d["ms"] / 1e3) / 1e12
         peak, unit = tc_peak, "TFLOP/s"
-    traffic = load_traffic(dom, set_name)
+    traffic = None if bwd else load_traffic(dom, set_name)
     roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
             "traffic": traffic, "kernel": dom, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)"
             if peak_kind == "measured" else "fallback",
@@ -547,7 +578,7 @@ def run_ours(args, wls, set_name, rank, world):
 
     # end-to-end: pinned host buffers, copies inside the timed region
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not bwd:
         e2e = run_e2e(args, convs, lib, dev, stream, world, dist, step_bytes, gc)
 
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -556,7 +587,8 @@ def run_ours(args, wls, set_name, rank, world):
             "config": {"workload": describe(wls), "layout": "NHWGC / GKYXC / NHWGK",
                        "l2": f"rotating {R} input/output sets ({R * per_set / 1e6:.0f} MB > 2x L2)",
                        "parallelism": "replicas" if world > 1 else "single GPU",
-                       "launch": "serial" if args.serial_launch else "programmatic dependent launch"},
+                       "launch": "serial" if args.serial_launch else "programmatic dependent launch",
+                       "op": args.op},
             "tflops": tflops, "median_ms_per_step": med,
             "value_from_median": step_bytes / (med / 1e3) / 1e9,
             "per_launch": per_launch, "roofline": roof,
@@ -566,7 +598,7 @@ def run_ours(args, wls, set_name, rank, world):
     if e2e:
         line["e2e"] = e2e
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wls)
+        line["cpu_baseline"] = cpu_baseline(wls, op=args.op)
     if rank == 0:
         print(json.dumps(line), flush=True)
 

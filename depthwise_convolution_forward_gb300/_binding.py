@@ -26,8 +26,9 @@ GCONV_F32, GCONV_F16, GCONV_BF16 = 0, 1, 2
 DTYPE_CODES = {"f32": GCONV_F32, "f16": GCONV_F16, "bf16": GCONV_BF16}
 
 KERNEL_AUTO, KERNEL_DIRECT_DW, KERNEL_DIRECT_GENERIC, KERNEL_IGEMM_TC = 0, 1, 2, 3
+KERNEL_BWD_DATA_DIRECT = 4
 KERNEL_NAMES = {KERNEL_DIRECT_DW: "direct_dw", KERNEL_DIRECT_GENERIC: "direct_generic",
-                KERNEL_IGEMM_TC: "igemm_tc"}
+                KERNEL_IGEMM_TC: "igemm_tc", KERNEL_BWD_DATA_DIRECT: "bwd_data_direct"}
 
 
 class gconv_problem(ctypes.Structure):
@@ -73,6 +74,13 @@ def load_library(path: Optional[str] = None):
         lib.grouped_conv_fwd_ex.restype = i32
         lib.grouped_conv_fwd_ex.argtypes = [vp, vp, vp, vp, prob_p, i32, vp,
                                             ctypes.POINTER(gconv_options)]
+        lib.grouped_conv_bwd_data.restype = i32
+        lib.grouped_conv_bwd_data.argtypes = [vp, vp, vp, prob_p, i32, vp, i64, vp]
+        lib.grouped_conv_bwd_data_ex.restype = i32
+        lib.grouped_conv_bwd_data_ex.argtypes = [vp, vp, vp, prob_p, i32, vp, i64, vp,
+                                                 ctypes.POINTER(gconv_options)]
+        lib.grouped_conv_bwd_data_workspace_size.restype = i32
+        lib.grouped_conv_bwd_data_workspace_size.argtypes = [prob_p, i32, ctypes.POINTER(i64)]
         lib.grouped_conv_out_shape.restype = i32
         lib.grouped_conv_out_shape.argtypes = [prob_p, ctypes.POINTER(i32)]
         lib.grouped_conv_select.restype = i32
@@ -174,3 +182,31 @@ def gconv_status_string(status: int) -> str:
 
 def gconv_last_error() -> str:
     return load_library().gconv_last_error().decode()
+
+
+def grouped_conv_bwd_data_workspace_size(p: gconv_problem, dtype: int) -> int:
+    """Device workspace bytes grouped_conv_bwd_data needs (0 when none)."""
+    lib = load_library()
+    n = ctypes.c_int64(0)
+    _check(lib.grouped_conv_bwd_data_workspace_size(ctypes.byref(p), dtype, ctypes.byref(n)))
+    return n.value
+
+
+def grouped_conv_bwd_data(dy, w, dx, p: gconv_problem, dtype: int, workspace=None, workspace_bytes: int = 0,
+                          stream=None) -> None:
+    lib = load_library()
+    if workspace is not None and not isinstance(workspace, int) and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.grouped_conv_bwd_data(_ptr(dy), _ptr(w), _ptr(dx), ctypes.byref(p), dtype, _ptr(workspace),
+                                     workspace_bytes, _stream(stream)))
+
+
+def grouped_conv_bwd_data_ex(dy, w, dx, p: gconv_problem, dtype: int, workspace=None, workspace_bytes: int = 0,
+                             stream=None, opt: Optional[gconv_options] = None) -> gconv_options:
+    lib = load_library()
+    o = opt if opt is not None else gconv_options()
+    if workspace is not None and not isinstance(workspace, int) and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.grouped_conv_bwd_data_ex(_ptr(dy), _ptr(w), _ptr(dx), ctypes.byref(p), dtype, _ptr(workspace),
+                                        workspace_bytes, _stream(stream), ctypes.byref(o)))
+    return o

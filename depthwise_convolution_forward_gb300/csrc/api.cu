@@ -1,7 +1,7 @@
-// C ABI of the grouped-convolution forward library: argument validation,
-// output-shape rule, shape-based kernel selection, tensor-map encoding and
-// launch.  Everything here runs on the host; the arithmetic runs in the
-// kernels (dw*.cu, generic.cu, tc*.cu).
+// C ABI of the grouped-convolution library (forward pass and backward data):
+// argument validation, output-shape rule, shape-based kernel selection,
+// tensor-map encoding and launch.  Everything here runs on the host; the
+// arithmetic runs in the kernels (dw*.cu, generic.cu, tc*.cu, bwd.cu).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -149,6 +149,85 @@ gconv_status read_and_clear_status(DevSlot* slot, cudaStream_t stream, int32_t* 
   return GCONV_OK;
 }
 
+LaunchArgs make_args(const void* x, const void* w, const void* bias, void* y, DType dt, struct CUstream_st* stream,
+                     DevSlot* slot, const gconv_options* opt) {
+  LaunchArgs a;
+  a.x = x, a.w = w, a.bias = bias, a.y = y;
+  a.dt = dt;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  a.status = slot->status;
+  a.wait_limit_ns = (opt && opt->wait_limit_ns > 0) ? (uint64_t)opt->wait_limit_ns : 2000000000ull;
+  a.test_flags = opt ? opt->test_flags : 0;
+  for (int i = 0; i < 8; ++i) a.tile[i] = opt ? opt->tile[i] : 0;
+  a.pdl = !(opt && opt->serial_launch);
+  return a;
+}
+
+// Forward convolution of geometry g on the buffers of a: the forced kernel
+// (1..3) or the selector's choice; nothing is launched on an error.
+gconv_status launch_forward(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev, int forced,
+                            int32_t* selected) {
+  const int kernel = forced ? forced : select_kernel(g, a.dt, &a);
+  if (kernel == GCONV_KERNEL_DIRECT_DW && !dw_supported(g, a.dt, &a))
+    return fail(GCONV_ERR_UNSUPPORTED, "depthwise kernel cannot run this problem");
+  if (kernel == GCONV_KERNEL_IGEMM_TC && !tc_supported(g, a.dt, &a))
+    return fail(GCONV_ERR_UNSUPPORTED, "tensor-core kernel cannot run this problem");
+  if (kernel < GCONV_KERNEL_DIRECT_DW || kernel > GCONV_KERNEL_IGEMM_TC)
+    return fail(GCONV_ERR_UNSUPPORTED, "unknown kernel id %d", kernel);
+  if (selected) *selected = kernel;
+  cudaError_t e;
+  switch (kernel) {
+    case GCONV_KERNEL_DIRECT_DW: e = dw_launch(g, a, dev); break;
+    case GCONV_KERNEL_IGEMM_TC: e = tc_launch(g, a, dev); break;
+    default: e = generic_launch(g, a, dev); break;
+  }
+  if (e == cudaErrorNotSupported) return fail(GCONV_ERR_UNSUPPORTED, "no launch plan for this problem");
+  if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+  return GCONV_OK;
+}
+
+// Debug mode: wait for the stream and turn a device-side timeout into the
+// return value.
+gconv_status finish(DevSlot* slot, const LaunchArgs& a, const gconv_options* opt) {
+  if (opt && opt->debug) {
+    int32_t code = 0, where = 0;
+    gconv_status st = read_and_clear_status(slot, a.stream, &code, &where);
+    if (st != GCONV_OK) return st;
+    if (code != 0) return fail(GCONV_ERR_TIMEOUT, "in-kernel wait timed out (site %d)", where);
+  }
+  return GCONV_OK;
+}
+
+// Backward data by the forward kernels: stride 1 and pad <= dil*(k-1) in
+// every dimension.  Fills *fg with the forward geometry that computes dx from
+// dy: Cg and Kg swapped, input extents = the forward output's, padding
+// dil*(k-1) - pad, output extents = the forward input's.
+bool bwd_as_forward(const Geometry& g, Geometry* fg) {
+  const int k[3] = {g.Z, g.Y, g.X}, s[3] = {g.sD, g.sH, g.sW}, p[3] = {g.pD, g.pH, g.pW},
+            d[3] = {g.dD, g.dH, g.dW};
+  int q[3];
+  for (int i = 0; i < 3; ++i) {
+    if (s[i] != 1) return false;
+    q[i] = d[i] * (k[i] - 1) - p[i];
+    if (q[i] < 0) return false;
+  }
+  Geometry f = g;
+  f.Cg = g.Kg, f.Kg = g.Cg;
+  f.D = g.Do, f.H = g.Ho, f.W = g.Wo;
+  f.Do = g.D, f.Ho = g.H, f.Wo = g.W;
+  f.pD = q[0], f.pH = q[1], f.pW = q[2];
+  if (out_extent(f.D, f.Z, 1, f.pD, f.dD) != g.D || out_extent(f.H, f.Y, 1, f.pH, f.dH) != g.H ||
+      out_extent(f.W, f.X, 1, f.pW, f.dW) != g.W)
+    return false;
+  *fg = f;
+  return true;
+}
+
+int64_t bwd_workspace_bytes(const Geometry& g, DType dt) {
+  Geometry f;
+  return bwd_as_forward(g, &f) ? g.w_elems() * dtype_bytes(dt) : 0;
+}
+
 }  // namespace
 
 CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, uint32_t rank, const void* base,
@@ -222,41 +301,71 @@ gconv_status grouped_conv_fwd_ex(const void* x, const void* w, const void* bias,
   DevSlot* slot = nullptr;
   cudaError_t e = device_slot(&slot);
   if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
+  LaunchArgs a = make_args(x, w, bias, y, (DType)dt, stream, slot, opt);
+  s = launch_forward(g, a, slot->info, opt ? opt->force_kernel : 0, opt ? &opt->selected : nullptr);
+  if (s != GCONV_OK) return s;
+  return finish(slot, a, opt);
+}
 
-  LaunchArgs a;
-  a.x = x, a.w = w, a.bias = bias, a.y = y;
-  a.dt = (DType)dt;
-  a.stream = reinterpret_cast<cudaStream_t>(stream);
-  a.status = slot->status;
-  a.wait_limit_ns = (opt && opt->wait_limit_ns > 0) ? (uint64_t)opt->wait_limit_ns : 2000000000ull;
-  a.test_flags = opt ? opt->test_flags : 0;
-  for (int i = 0; i < 8; ++i) a.tile[i] = opt ? opt->tile[i] : 0;
-  a.pdl = !(opt && opt->serial_launch);
-
-  int kernel = (opt && opt->force_kernel) ? opt->force_kernel : select_kernel(g, a.dt, &a);
-  if (kernel == GCONV_KERNEL_DIRECT_DW && !dw_supported(g, a.dt, &a))
-    return fail(GCONV_ERR_UNSUPPORTED, "depthwise kernel cannot run this problem");
-  if (kernel == GCONV_KERNEL_IGEMM_TC && !tc_supported(g, a.dt, &a))
-    return fail(GCONV_ERR_UNSUPPORTED, "tensor-core kernel cannot run this problem");
-  if (kernel < GCONV_KERNEL_DIRECT_DW || kernel > GCONV_KERNEL_IGEMM_TC)
-    return fail(GCONV_ERR_UNSUPPORTED, "unknown kernel id %d", kernel);
-  if (opt) opt->selected = kernel;
-
-  switch (kernel) {
-    case GCONV_KERNEL_DIRECT_DW: e = dw_launch(g, a, slot->info); break;
-    case GCONV_KERNEL_IGEMM_TC: e = tc_launch(g, a, slot->info); break;
-    default: e = generic_launch(g, a, slot->info); break;
-  }
-  if (e == cudaErrorNotSupported) return fail(GCONV_ERR_UNSUPPORTED, "no launch plan for this problem");
-  if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
-
-  if (opt && opt->debug) {
-    int32_t code = 0, where = 0;
-    gconv_status st = read_and_clear_status(slot, a.stream, &code, &where);
-    if (st != GCONV_OK) return st;
-    if (code != 0) return fail(GCONV_ERR_TIMEOUT, "in-kernel wait timed out (site %d)", where);
-  }
+gconv_status grouped_conv_bwd_data_workspace_size(const gconv_problem* p, gconv_dtype dt, int64_t* bytes) {
+  Geometry g;
+  gconv_status s = validate(p, &g);
+  if (s != GCONV_OK) return s;
+  if (dt != GCONV_F32 && dt != GCONV_F16 && dt != GCONV_BF16) return fail(GCONV_ERR_UNSUPPORTED, "unknown dtype %d", (int)dt);
+  if (bytes == nullptr) return fail(GCONV_ERR_INVALID_ARG, "bytes pointer is NULL");
+  *bytes = bwd_workspace_bytes(g, (DType)dt);
   return GCONV_OK;
+}
+
+gconv_status grouped_conv_bwd_data_ex(const void* dy, const void* w, void* dx, const gconv_problem* p,
+                                      gconv_dtype dt, void* workspace, int64_t workspace_bytes,
+                                      struct CUstream_st* stream, gconv_options* opt) {
+  Geometry g;
+  gconv_status s = validate(p, &g);
+  if (s != GCONV_OK) return s;
+  if (dt != GCONV_F32 && dt != GCONV_F16 && dt != GCONV_BF16) return fail(GCONV_ERR_UNSUPPORTED, "unknown dtype %d", (int)dt);
+  if (dy == nullptr || w == nullptr || dx == nullptr) return fail(GCONV_ERR_INVALID_ARG, "dy, w and dx must not be NULL");
+  const DType t = (DType)dt;
+  const int es = dtype_bytes(t);
+  const int64_t dxb = g.x_elems() * es;
+  const int forced = opt ? opt->force_kernel : 0;
+  Geometry fg;
+  const bool as_fwd = forced != GCONV_KERNEL_BWD_DATA_DIRECT && bwd_as_forward(g, &fg);
+  if (forced != 0 && forced != GCONV_KERNEL_BWD_DATA_DIRECT && !as_fwd)
+    return fail(GCONV_ERR_UNSUPPORTED, "kernel %d needs stride 1 and pad <= dil*(k-1)", forced);
+  const int64_t need = as_fwd ? g.w_elems() * es : 0;
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15)))
+    return fail(GCONV_ERR_INVALID_ARG, "workspace must be 16-byte aligned and hold %lld bytes",
+                (long long)need);
+  if (overlaps(dx, dxb, dy, g.y_elems() * es) || overlaps(dx, dxb, w, g.w_elems() * es) ||
+      (need > 0 && overlaps(dx, dxb, workspace, need)))
+    return fail(GCONV_ERR_INVALID_ARG, "dx overlaps an input buffer or the workspace");
+  if (need > 0 && (overlaps(workspace, need, dy, g.y_elems() * es) || overlaps(workspace, need, w, g.w_elems() * es)))
+    return fail(GCONV_ERR_INVALID_ARG, "the workspace overlaps dy or w");
+
+  DevSlot* slot = nullptr;
+  cudaError_t e = device_slot(&slot);
+  if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
+  if (as_fwd) {
+    // transposed, flipped weights into the workspace, then the forward pass
+    LaunchArgs flip = make_args(dy, w, nullptr, workspace, t, stream, slot, opt);
+    e = bwd_weight_flip_launch(g, flip, workspace, slot->info);
+    if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    LaunchArgs a = make_args(dy, workspace, nullptr, dx, t, stream, slot, opt);
+    s = launch_forward(fg, a, slot->info, forced, opt ? &opt->selected : nullptr);
+    if (s != GCONV_OK) return s;
+    return finish(slot, a, opt);
+  }
+  LaunchArgs a = make_args(dy, w, nullptr, dx, t, stream, slot, opt);
+  e = bwd_data_direct_launch(g, a, slot->info);
+  if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+  if (opt) opt->selected = GCONV_KERNEL_BWD_DATA_DIRECT;
+  return finish(slot, a, opt);
+}
+
+gconv_status grouped_conv_bwd_data(const void* dy, const void* w, void* dx, const gconv_problem* p, gconv_dtype dt,
+                                   void* workspace, int64_t workspace_bytes, struct CUstream_st* stream) {
+  return grouped_conv_bwd_data_ex(dy, w, dx, p, dt, workspace, workspace_bytes, stream, nullptr);
 }
 
 gconv_status grouped_conv_fwd(const void* x, const void* w, const void* bias, void* y, const gconv_problem* p,

@@ -1,0 +1,159 @@
+// Grouped convolution backward data (the gradient with respect to x).
+//
+// dx[n, i, g, c] = sum over (o, t, k) with i = o*s - p + t*d in every
+// dimension of dy[n, o, g, k] * w[g, k, t, c] -- the adjoint of the forward
+// map in x.  The backward-data variant and its runner contract (dY, W) are
+// listed by the pages' CK grouped-convolution tile engine and its Python
+// examples; the arithmetic is that adjoint.
+//
+// Two routes (chosen in api.cu):
+//  - stride 1 and pad <= d*(k-1) in every dimension: dx is the forward
+//    convolution of dy with per-group transposed, spatially flipped weights
+//    wt[g, c, t', k] = w[g, k, flip(t'), c] and padding d*(k-1) - p, so the
+//    forward kernels (depthwise, tensor-core, generic) run it after
+//    weight_flip_kernel has written wt into the caller's workspace;
+//  - otherwise bwd_data_direct_kernel gathers, for each dx element, the
+//    outputs whose windows cover it (fp32 accumulation, one rounding).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gconv {
+namespace {
+
+// wt[g][c][z][y][x][k] = w[g][k][Z-1-z][Y-1-y][X-1-x][c]: consecutive threads
+// write consecutive k (coalesced writes; the reads are a small gather from a
+// tensor that stays in L2).
+template <typename T>
+__global__ void __launch_bounds__(256) weight_flip_kernel(const T* __restrict__ w, T* __restrict__ wt,
+                                                          int64_t total, int Kg, int Cg, int Z, int Y, int X) {
+  grid_dependency_wait();  // w and the workspace are touched only from here on
+  for (int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; o < total;
+       o += (int64_t)gridDim.x * blockDim.x) {
+    int64_t f = o;
+    const int k = (int)(f % Kg);
+    f /= Kg;
+    const int xx = (int)(f % X);
+    f /= X;
+    const int yy = (int)(f % Y);
+    f /= Y;
+    const int z = (int)(f % Z);
+    f /= Z;
+    const int c = (int)(f % Cg);
+    const int64_t g = f / Cg;
+    wt[o] = w[((((g * Kg + k) * Z + (Z - 1 - z)) * Y + (Y - 1 - yy)) * (int64_t)X + (X - 1 - xx)) * Cg + c];
+  }
+}
+
+struct BwdArgs {
+  const void* dy;
+  const void* w;
+  void* dx;
+  int64_t total;  // dx elements
+  int G, Cg, Kg;
+  int D, H, W, Do, Ho, Wo, Z, Y, X;
+  int sD, sH, sW, pD, pH, pW, dD, dH, dW;
+};
+
+// One thread per dx element (channel fastest: coalesced dx writes and weight
+// reads, dy reads shared by the warp).  Output positions o along a dimension
+// satisfy o*s = i + p - t*d; taps whose offset is not a multiple of the stride
+// or lands outside the output contribute nothing.
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_data_direct_kernel(const BwdArgs a) {
+  const T* __restrict__ dy = static_cast<const T*>(a.dy);
+  const T* __restrict__ w = static_cast<const T*>(a.w);
+  T* __restrict__ dx = static_cast<T*>(a.dx);
+  const int64_t K = (int64_t)a.G * a.Kg;
+  const int64_t kstride = (int64_t)a.Z * a.Y * a.X * a.Cg;  // weight stride between output channels
+  grid_dependency_wait();  // dy, w and dx are touched only from here on
+  for (int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; o < a.total;
+       o += (int64_t)gridDim.x * blockDim.x) {
+    int64_t f = o;
+    const int c = (int)(f % a.Cg);
+    f /= a.Cg;
+    const int g = (int)(f % a.G);
+    f /= a.G;
+    const int iw = (int)(f % a.W);
+    f /= a.W;
+    const int ih = (int)(f % a.H);
+    f /= a.H;
+    const int id = (int)(f % a.D);
+    const int64_t n = f / a.D;
+    float acc = 0.f;
+    for (int z = 0; z < a.Z; ++z) {
+      const int nd = id + a.pD - z * a.dD;
+      if (nd < 0 || nd % a.sD != 0) continue;
+      const int od = nd / a.sD;
+      if (od >= a.Do) continue;
+      for (int yy = 0; yy < a.Y; ++yy) {
+        const int nh = ih + a.pH - yy * a.dH;
+        if (nh < 0 || nh % a.sH != 0) continue;
+        const int oh = nh / a.sH;
+        if (oh >= a.Ho) continue;
+        for (int xx = 0; xx < a.X; ++xx) {
+          const int nw = iw + a.pW - xx * a.dW;
+          if (nw < 0 || nw % a.sW != 0) continue;
+          const int ow = nw / a.sW;
+          if (ow >= a.Wo) continue;
+          const T* dyp = dy + (((n * a.Do + od) * a.Ho + oh) * (int64_t)a.Wo + ow) * K + (int64_t)g * a.Kg;
+          const T* wp = w + ((((int64_t)g * a.Kg * a.Z + z) * a.Y + yy) * a.X + xx) * a.Cg + c;
+#pragma unroll 4
+          for (int k = 0; k < a.Kg; ++k)
+            acc = fmaf(Elem<T>::to_f32(dyp[k]), Elem<T>::to_f32(wp[k * kstride]), acc);
+        }
+      }
+    }
+    dx[o] = epilogue_one<T>(acc, 0.f);
+  }
+}
+
+int grid_blocks(int64_t total, const DeviceInfo& dev) {
+  const int64_t blocks = (total + 255) / 256;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)dev.num_sms * 16));
+}
+
+}  // namespace
+
+cudaError_t bwd_weight_flip_launch(const Geometry& g, const LaunchArgs& a, void* wt, const DeviceInfo& dev) {
+  const int64_t total = g.w_elems();
+  const dim3 grid(grid_blocks(total, dev)), block(256);
+  switch (a.dt) {
+    case kF32:
+      return launch_kernel(weight_flip_kernel<float>, grid, block, 0, a, static_cast<const float*>(a.w),
+                           static_cast<float*>(wt), total, g.Kg, g.Cg, g.Z, g.Y, g.X);
+    case kF16:
+      return launch_kernel(weight_flip_kernel<__half>, grid, block, 0, a, static_cast<const __half*>(a.w),
+                           static_cast<__half*>(wt), total, g.Kg, g.Cg, g.Z, g.Y, g.X);
+    case kBF16:
+      return launch_kernel(weight_flip_kernel<__nv_bfloat16>, grid, block, 0, a,
+                           static_cast<const __nv_bfloat16*>(a.w), static_cast<__nv_bfloat16*>(wt), total, g.Kg,
+                           g.Cg, g.Z, g.Y, g.X);
+  }
+  return cudaErrorNotSupported;
+}
+
+cudaError_t bwd_data_direct_launch(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev) {
+  BwdArgs p;
+  p.dy = a.x;  // the forward kernels' x slot carries dy
+  p.w = a.w;
+  p.dx = a.y;
+  p.total = g.x_elems();
+  p.G = g.G, p.Cg = g.Cg, p.Kg = g.Kg;
+  p.D = g.D, p.H = g.H, p.W = g.W, p.Do = g.Do, p.Ho = g.Ho, p.Wo = g.Wo;
+  p.Z = g.Z, p.Y = g.Y, p.X = g.X;
+  p.sD = g.sD, p.sH = g.sH, p.sW = g.sW, p.pD = g.pD, p.pH = g.pH, p.pW = g.pW;
+  p.dD = g.dD, p.dH = g.dH, p.dW = g.dW;
+  const dim3 grid(grid_blocks(p.total, dev)), block(256);
+  switch (a.dt) {
+    case kF32: return launch_kernel(bwd_data_direct_kernel<float>, grid, block, 0, a, p);
+    case kF16: return launch_kernel(bwd_data_direct_kernel<__half>, grid, block, 0, a, p);
+    case kBF16: return launch_kernel(bwd_data_direct_kernel<__nv_bfloat16>, grid, block, 0, a, p);
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace gconv

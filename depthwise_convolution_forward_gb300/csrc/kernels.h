@@ -92,6 +92,12 @@ cudaError_t generic_launch(const Geometry& g, const LaunchArgs& a, const DeviceI
 bool tc_supported(const Geometry& g, DType dt, const LaunchArgs* a);
 cudaError_t tc_launch(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
 
+// ---- backward data ---------------------------------------------------------
+// wt[g][c][t'][k] = w[g][k][flip(t')][c] into wt (w_elems elements); a.w is w.
+cudaError_t bwd_weight_flip_launch(const Geometry& g, const LaunchArgs& a, void* wt, const DeviceInfo& dev);
+// Direct gather: a.x carries dy, a.w the forward weights, a.y receives dx.
+cudaError_t bwd_data_direct_launch(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
+
 // ---- Kc alone (epilogue test entry) --------------------------------------
 cudaError_t epilogue_launch(const float* acc, const void* bias, void* y, int64_t rows, int cols,
                             DType dt, cudaStream_t stream);

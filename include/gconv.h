@@ -80,7 +80,8 @@ typedef enum gconv_kernel {
   GCONV_KERNEL_AUTO = 0,
   GCONV_KERNEL_DIRECT_DW = 1,      /* Ka: TMA-staged depthwise direct kernel        */
   GCONV_KERNEL_DIRECT_GENERIC = 2, /* direct kernel for any shape/dtype/alignment   */
-  GCONV_KERNEL_IGEMM_TC = 3        /* Kb: tcgen05/TMEM grouped implicit GEMM        */
+  GCONV_KERNEL_IGEMM_TC = 3,       /* Kb: tcgen05/TMEM grouped implicit GEMM        */
+  GCONV_KERNEL_BWD_DATA_DIRECT = 4 /* backward data: direct gather kernel           */
 } gconv_kernel;
 
 /* Options of grouped_conv_fwd_ex.  Zero-initialise, then set what you need. */
@@ -156,6 +157,54 @@ gconv_status grouped_conv_fwd(const void *x, const void *w, const void *bias, vo
 gconv_status grouped_conv_fwd_ex(const void *x, const void *w, const void *bias, void *y,
                                  const gconv_problem *p, gconv_dtype dt, struct CUstream_st *stream,
                                  gconv_options *opt);
+
+/*
+ * grouped_conv_bwd_data -- dx, the gradient of y = grouped_conv(x, w) with
+ * respect to x, given dy = the gradient with respect to y (the adjoint of the
+ * forward map in x; the backward-data variant of the CK grouped-convolution
+ * tile engine, whose runner takes dY and W):
+ *   dx[n, i, g, c] = sum over (o, t, k) with i = o*s - p + t*d in every
+ *                    dimension of dy[n, o, g, k] * w[g, k, t, c]
+ *   dy   device, [N, (Do), Ho, Wo, G, Kg] packed, dtype dt  (the forward output
+ *        layout; read only)
+ *   w    device, [G, Kg, (Z), Y, X, Cg] packed, dtype dt     (read only)
+ *   dx   device, [N, (D), H, W, G, Cg] packed, dtype dt      (written; must not
+ *        overlap dy, w or the workspace)
+ *   p    the forward problem (in[] = dx's extents; Do, Ho, Wo follow from it)
+ *   workspace  device scratch of at least
+ *        grouped_conv_bwd_data_workspace_size() bytes, 16-byte aligned; NULL
+ *        when that size is 0.  Owned by the caller; the call uses it until the
+ *        stream passes the launch.
+ * Stride 1 with pad <= dil*(k-1) in every dimension runs as a forward
+ * convolution of dy with per-group transposed, flipped weights (written into
+ * the workspace) and padding dil*(k-1) - pad, on the forward kernels; other
+ * problems run a direct gather kernel and need no workspace.  fp32
+ * accumulation, one round-to-nearest-even cast.  Asynchronous on `stream`.
+ * Errors: as grouped_conv_fwd, plus GCONV_ERR_INVALID_ARG for a workspace that
+ * is missing, too small or misaligned.
+ */
+gconv_status grouped_conv_bwd_data(const void *dy, const void *w, void *dx, const gconv_problem *p,
+                                   gconv_dtype dt, void *workspace, int64_t workspace_bytes,
+                                   struct CUstream_st *stream);
+
+/*
+ * grouped_conv_bwd_data_ex -- grouped_conv_bwd_data with options.
+ * opt->force_kernel: GCONV_KERNEL_BWD_DATA_DIRECT forces the direct gather
+ * kernel; GCONV_KERNEL_DIRECT_DW / _DIRECT_GENERIC / _IGEMM_TC force the
+ * forward kernel of the transposed-weights route (stride-1 problems only,
+ * else GCONV_ERR_UNSUPPORTED).  opt->selected reports the kernel used.
+ * Other fields as for grouped_conv_fwd_ex.
+ */
+gconv_status grouped_conv_bwd_data_ex(const void *dy, const void *w, void *dx, const gconv_problem *p,
+                                      gconv_dtype dt, void *workspace, int64_t workspace_bytes,
+                                      struct CUstream_st *stream, gconv_options *opt);
+
+/*
+ * grouped_conv_bwd_data_workspace_size -- device workspace bytes that
+ * grouped_conv_bwd_data needs for problem p in dtype dt (0 when none).  Host
+ * only.  GCONV_ERR_INVALID_ARG for a malformed problem or a NULL `bytes`.
+ */
+gconv_status grouped_conv_bwd_data_workspace_size(const gconv_problem *p, gconv_dtype dt, int64_t *bytes);
 
 /*
  * grouped_conv_out_shape -- output extents {Do, Ho, Wo} of problem p

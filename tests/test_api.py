@@ -126,3 +126,39 @@ def test_epilogue_entry_validates():
     assert e.value.status == B.GCONV_ERR_INVALID_ARG
     with pytest.raises(gc.GconvError):
         gc.gconv_epilogue_apply(16, None, 32, 4, 0, B.GCONV_F16, None)
+
+
+# ---- backward data: host-side logic (nothing is launched on these errors) ----
+def test_bwd_data_workspace_size():
+    p = good()  # stride 1, pad 1 <= dil*(k-1) = 2: forward-kernel route, transposed weights
+    w_bytes = 12 * 9 * 2 * 2  # K * taps * Cg * fp16
+    assert gc.grouped_conv_bwd_data_workspace_size(p, B.GCONV_F16) == w_bytes
+    assert gc.grouped_conv_bwd_data_workspace_size(p, B.GCONV_F32) == 2 * w_bytes
+    assert gc.grouped_conv_bwd_data_workspace_size(good(stride=(1, 2, 2)), B.GCONV_F16) == 0  # direct kernel
+    assert gc.grouped_conv_bwd_data_workspace_size(good(ker=(1, 1, 1)), B.GCONV_F16) == 0  # pad > dil*(k-1)
+    assert gc.grouped_conv_bwd_data_workspace_size(good(ker=(1, 1, 1), pad=(0, 0, 0)), B.GCONV_F16) == 12 * 2 * 2
+
+
+def test_bwd_data_workspace_required():
+    p = good()
+    need = gc.grouped_conv_bwd_data_workspace_size(p, B.GCONV_F16)
+    base = 1 << 30
+    for ws, nbytes in ((None, 0), (base + (1 << 24), need - 2), (base + (1 << 24) + 8, need)):
+        with pytest.raises(gc.GconvError) as e:
+            gc.grouped_conv_bwd_data(base, base + (1 << 20), base + (1 << 22), p, B.GCONV_F16, ws, nbytes)
+        assert e.value.status == B.GCONV_ERR_INVALID_ARG
+        assert "workspace" in gc.gconv_last_error()
+
+
+def test_bwd_data_overlap_and_forced_route_rejected():
+    p = good()
+    base = 1 << 30
+    with pytest.raises(gc.GconvError) as e:  # dx overlaps dy
+        gc.grouped_conv_bwd_data(base, base + (1 << 20), base + 64, p, B.GCONV_F16, base + (1 << 24), 1 << 16)
+    assert e.value.status == B.GCONV_ERR_INVALID_ARG and "overlap" in gc.gconv_last_error()
+    opt = gc.gconv_options()
+    opt.force_kernel = B.KERNEL_IGEMM_TC  # a forward kernel needs the stride-1 route
+    with pytest.raises(gc.GconvError) as e:
+        gc.grouped_conv_bwd_data_ex(base, base + (1 << 20), base + (1 << 22), good(stride=(1, 2, 2)), B.GCONV_F16,
+                                    None, 0, None, opt)
+    assert e.value.status == B.GCONV_ERR_UNSUPPORTED
