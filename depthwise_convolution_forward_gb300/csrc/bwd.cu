@@ -12,8 +12,11 @@
 //    wt[g, c, t', k] = w[g, k, flip(t'), c] and padding d*(k-1) - p, so the
 //    forward kernels (depthwise, tensor-core, generic) run it after
 //    weight_flip_kernel has written wt into the caller's workspace;
-//  - otherwise bwd_data_direct_kernel gathers, for each dx element, the
-//    outputs whose windows cover it (fp32 accumulation, one rounding).
+//  - otherwise a direct kernel gathers, for each dx element, the outputs
+//    whose windows cover it (fp32 accumulation, one rounding):
+//    bwd_data_vec_kernel handles 16 bytes of channels per thread where they
+//    share a group (or are depthwise groups), bwd_data_direct_kernel one
+//    element per thread otherwise.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -59,10 +62,11 @@ struct BwdArgs {
 };
 
 // One thread per dx element (channel fastest: coalesced dx writes and weight
-// reads, dy reads shared by the warp).  Output positions o along a dimension
+// reads, dy reads shared by the warp).  I is the index type of the element
+// decode: 32-bit unsigned when the element count fits, else 64-bit.  Output positions o along a dimension
 // satisfy o*s = i + p - t*d; taps whose offset is not a multiple of the stride
 // or lands outside the output contribute nothing.
-template <typename T>
+template <typename T, typename I>
 __global__ void __launch_bounds__(256) bwd_data_direct_kernel(const BwdArgs a) {
   const T* __restrict__ dy = static_cast<const T*>(a.dy);
   const T* __restrict__ w = static_cast<const T*>(a.w);
@@ -70,19 +74,19 @@ __global__ void __launch_bounds__(256) bwd_data_direct_kernel(const BwdArgs a) {
   const int64_t K = (int64_t)a.G * a.Kg;
   const int64_t kstride = (int64_t)a.Z * a.Y * a.X * a.Cg;  // weight stride between output channels
   grid_dependency_wait();  // dy, w and dx are touched only from here on
-  for (int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; o < a.total;
-       o += (int64_t)gridDim.x * blockDim.x) {
-    int64_t f = o;
-    const int c = (int)(f % a.Cg);
-    f /= a.Cg;
-    const int g = (int)(f % a.G);
-    f /= a.G;
-    const int iw = (int)(f % a.W);
-    f /= a.W;
-    const int ih = (int)(f % a.H);
-    f /= a.H;
-    const int id = (int)(f % a.D);
-    const int64_t n = f / a.D;
+  const I total = (I)a.total;
+  for (I o = (I)blockIdx.x * (I)blockDim.x + (I)threadIdx.x; o < total; o += (I)gridDim.x * (I)blockDim.x) {
+    I f = o;
+    const int c = (int)(f % (I)a.Cg);
+    f /= (I)a.Cg;
+    const int g = (int)(f % (I)a.G);
+    f /= (I)a.G;
+    const int iw = (int)(f % (I)a.W);
+    f /= (I)a.W;
+    const int ih = (int)(f % (I)a.H);
+    f /= (I)a.H;
+    const int id = (int)(f % (I)a.D);
+    const int64_t n = (int64_t)(f / (I)a.D);
     float acc = 0.f;
     for (int z = 0; z < a.Z; ++z) {
       const int nd = id + a.pD - z * a.dD;
@@ -107,7 +111,92 @@ __global__ void __launch_bounds__(256) bwd_data_direct_kernel(const BwdArgs a) {
         }
       }
     }
-    dx[o] = epilogue_one<T>(acc, 0.f);
+    dx[(int64_t)o] = epilogue_one<T>(acc, 0.f);
+  }
+}
+
+// V = 16 / sizeof(T) consecutive dx channels per thread (one 16-byte store).
+// MODE 0: the V channels lie in one group (Cg % V == 0): a single dy value per
+//   (output, k) serves all V, and their weights are one 16-byte load.
+// MODE 1: depthwise (Cg == Kg == 1, G % V == 0): the V channels are V groups;
+//   their dy values are one 16-byte load, their weights V scalar loads.
+// I is the index type of the element decode: 32-bit unsigned when the vector
+// count fits, else 64-bit.  Same sums in the same order as the scalar kernel.
+template <typename T, int MODE, typename I>
+__global__ void __launch_bounds__(256) bwd_data_vec_kernel(const BwdArgs a) {
+  constexpr int V = 16 / (int)sizeof(T);
+  const T* __restrict__ dy = static_cast<const T*>(a.dy);
+  const T* __restrict__ w = static_cast<const T*>(a.w);
+  T* __restrict__ dx = static_cast<T*>(a.dx);
+  const int64_t C = (int64_t)a.G * a.Cg, K = (int64_t)a.G * a.Kg;
+  const int taps = a.Z * a.Y * a.X;
+  const int64_t kstride = (int64_t)taps * a.Cg;
+  const I per_pixel = (I)(MODE == 0 ? (a.Cg / V) * a.G : a.G / V);  // vectors per dx pixel
+  const I nvec = (I)(a.total / V);
+  grid_dependency_wait();  // dy, w and dx are touched only from here on
+  for (I o = (I)blockIdx.x * (I)blockDim.x + (I)threadIdx.x; o < nvec; o += (I)gridDim.x * (I)blockDim.x) {
+    I f = o;
+    const int v = (int)(f % per_pixel);
+    f /= per_pixel;
+    int g, c;
+    if constexpr (MODE == 0) {
+      const int cvs = a.Cg / V;
+      g = v / cvs;
+      c = (v - g * cvs) * V;
+    } else {
+      g = v * V;
+      c = 0;
+    }
+    const int iw = (int)(f % (I)a.W);
+    f /= (I)a.W;
+    const int ih = (int)(f % (I)a.H);
+    f /= (I)a.H;
+    const int id = (int)(f % (I)a.D);
+    const int64_t n = (int64_t)(f / (I)a.D);
+    float acc[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) acc[j] = 0.f;
+    for (int z = 0; z < a.Z; ++z) {
+      const int nd = id + a.pD - z * a.dD;
+      if (nd < 0 || nd % a.sD != 0) continue;
+      const int od = nd / a.sD;
+      if (od >= a.Do) continue;
+      for (int yy = 0; yy < a.Y; ++yy) {
+        const int nh = ih + a.pH - yy * a.dH;
+        if (nh < 0 || nh % a.sH != 0) continue;
+        const int oh = nh / a.sH;
+        if (oh >= a.Ho) continue;
+        for (int xx = 0; xx < a.X; ++xx) {
+          const int nw = iw + a.pW - xx * a.dW;
+          if (nw < 0 || nw % a.sW != 0) continue;
+          const int ow = nw / a.sW;
+          if (ow >= a.Wo) continue;
+          const int64_t opix = ((n * a.Do + od) * a.Ho + oh) * (int64_t)a.Wo + ow;
+          if constexpr (MODE == 0) {
+            const T* dyp = dy + opix * K + (int64_t)g * a.Kg;
+            const T* wp = w + ((((int64_t)g * a.Kg * a.Z + z) * a.Y + yy) * a.X + xx) * a.Cg + c;
+#pragma unroll 2
+            for (int k = 0; k < a.Kg; ++k) {
+              const float d = Elem<T>::to_f32(dyp[k]);
+              float wf[V];
+              unpack16<T>(*reinterpret_cast<const uint4*>(wp + k * kstride), wf);
+#pragma unroll
+              for (int j = 0; j < V; ++j) acc[j] = fmaf(d, wf[j], acc[j]);
+            }
+          } else {
+            float df[V];
+            unpack16<T>(*reinterpret_cast<const uint4*>(dy + opix * K + g), df);
+            const int t = (z * a.Y + yy) * a.X + xx;
+#pragma unroll
+            for (int j = 0; j < V; ++j)
+              acc[j] = fmaf(df[j], Elem<T>::to_f32(w[(int64_t)(g + j) * taps + t]), acc[j]);
+          }
+        }
+      }
+    }
+    const float zero[V] = {};
+    epilogue_store<T, V>(dx + (((n * a.D + id) * a.H + ih) * (int64_t)a.W + iw) * C + (int64_t)g * a.Cg + c, acc,
+                         zero);
   }
 }
 
@@ -147,12 +236,43 @@ cudaError_t bwd_data_direct_launch(const Geometry& g, const LaunchArgs& a, const
   p.Z = g.Z, p.Y = g.Y, p.X = g.X;
   p.sD = g.sD, p.sH = g.sH, p.sW = g.sW, p.pD = g.pD, p.pH = g.pH, p.pW = g.pW;
   p.dD = g.dD, p.dH = g.dH, p.dW = g.dW;
-  const dim3 grid(grid_blocks(p.total, dev)), block(256);
-  switch (a.dt) {
-    case kF32: return launch_kernel(bwd_data_direct_kernel<float>, grid, block, 0, a, p);
-    case kF16: return launch_kernel(bwd_data_direct_kernel<__half>, grid, block, 0, a, p);
-    case kBF16: return launch_kernel(bwd_data_direct_kernel<__nv_bfloat16>, grid, block, 0, a, p);
+  // Vector form when 16 bytes of dx channels share a group (or are 16 bytes of
+  // depthwise groups) and the vector accesses are aligned; else one element
+  // per thread.
+  const int V = 16 / dtype_bytes(a.dt);
+  const bool a16 = ((reinterpret_cast<uintptr_t>(a.x) | reinterpret_cast<uintptr_t>(a.w) |
+                     reinterpret_cast<uintptr_t>(a.y)) & 15) == 0;
+  int mode = -1;
+  if (a16 && g.Cg % V == 0) mode = 0;
+  else if (a16 && g.Cg == 1 && g.Kg == 1 && g.G % V == 0) mode = 1;
+  if (mode >= 0) {
+    const bool narrow = p.total / V < ((int64_t)1 << 31);
+    const dim3 grid(grid_blocks(p.total / V, dev)), block(256);
+#define GCONV_BWD_VEC(TT)                                                                                  \
+  if (mode == 0)                                                                                           \
+    return narrow ? launch_kernel(bwd_data_vec_kernel<TT, 0, uint32_t>, grid, block, 0, a, p)              \
+                  : launch_kernel(bwd_data_vec_kernel<TT, 0, int64_t>, grid, block, 0, a, p);              \
+  return narrow ? launch_kernel(bwd_data_vec_kernel<TT, 1, uint32_t>, grid, block, 0, a, p)                \
+                : launch_kernel(bwd_data_vec_kernel<TT, 1, int64_t>, grid, block, 0, a, p);
+    switch (a.dt) {
+      case kF32: GCONV_BWD_VEC(float)
+      case kF16: GCONV_BWD_VEC(__half)
+      case kBF16: GCONV_BWD_VEC(__nv_bfloat16)
+    }
+#undef GCONV_BWD_VEC
+    return cudaErrorNotSupported;
   }
+  const dim3 grid(grid_blocks(p.total, dev)), block(256);
+  const bool narrow = p.total < ((int64_t)1 << 31);
+#define GCONV_BWD_ONE(TT)                                                                   \
+  return narrow ? launch_kernel(bwd_data_direct_kernel<TT, uint32_t>, grid, block, 0, a, p) \
+                : launch_kernel(bwd_data_direct_kernel<TT, int64_t>, grid, block, 0, a, p);
+  switch (a.dt) {
+    case kF32: GCONV_BWD_ONE(float)
+    case kF16: GCONV_BWD_ONE(__half)
+    case kBF16: GCONV_BWD_ONE(__nv_bfloat16)
+  }
+#undef GCONV_BWD_ONE
   return cudaErrorNotSupported;
 }
 
