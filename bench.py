@@ -320,23 +320,40 @@ def run_reference(args, wls, rank, world):
     orc, prep, np = cpu_oracle_prepare(wls)
     total_steps = args.steps + args.warmup
     budget_s = 120.0
-    # outputs per step for each conv: a contiguous run of flat outputs sized
-    # from a quick rate probe so the whole run stays within the budget
-    probe_n = 20000
-    for p in prep:
-        idx = np.arange(min(probe_n, p["total"]), dtype=np.int64)
-        t0 = time.perf_counter()
-        orc.points(p["wl"], p["x"], p["w"], p["b"], idx)
-        p["rate"] = len(idx) / max(time.perf_counter() - t0, 1e-6)
     per_step_s = budget_s / total_steps / len(prep)
-    for p in prep:
-        p["n"] = int(max(64, min(p["total"], p["rate"] * per_step_s)))
     rng = np.random.default_rng(0)
+    bwd = getattr(args, "op", "fwd") == "bwd_data"
+    if bwd:
+        # whole images per step (backward data of an image needs all of its dy):
+        # a contiguous run of images sized from a one-image rate probe
+        for p in prep:
+            wl = p["wl"]
+            p["total"] = wl.N
+            p["bytes"] = p["bytes"] - (wl.K * (2 if wl.dtype != "f32" else 4) if wl.bias else 0)
+            p["dy"] = rng.uniform(-1, 1, size=(wl.N,) + tuple(p["out"][3 - wl.ndim:]) + (wl.G, wl.Kg))
+            t0 = time.perf_counter()
+            orc.bwd_data(wl.with_(N=1), p["dy"][:1], p["w"])
+            p["rate"] = 1.0 / max(time.perf_counter() - t0, 1e-6)
+            p["n"] = int(max(1, min(wl.N, p["rate"] * per_step_s)))
+    else:
+        # outputs per step for each conv: a contiguous run of flat outputs sized
+        # from a quick rate probe so the whole run stays within the budget
+        probe_n = 20000
+        for p in prep:
+            idx = np.arange(min(probe_n, p["total"]), dtype=np.int64)
+            t0 = time.perf_counter()
+            orc.points(p["wl"], p["x"], p["w"], p["b"], idx)
+            p["rate"] = len(idx) / max(time.perf_counter() - t0, 1e-6)
+        for p in prep:
+            p["n"] = int(max(64, min(p["total"], p["rate"] * per_step_s)))
 
     def step(i):
         for p in prep:
             start = int(rng.integers(0, max(1, p["total"] - p["n"])))
-            orc.points(p["wl"], p["x"], p["w"], p["b"], np.arange(start, start + p["n"], dtype=np.int64))
+            if bwd:
+                orc.bwd_data(p["wl"].with_(N=p["n"]), p["dy"][start:start + p["n"]], p["w"])
+            else:
+                orc.points(p["wl"], p["x"], p["w"], p["b"], np.arange(start, start + p["n"], dtype=np.int64))
 
     for i in range(args.warmup):
         step(i)
@@ -346,13 +363,15 @@ def run_reference(args, wls, rank, world):
     el = time.perf_counter() - t0
     frac_bytes = sum(p["bytes"] * p["n"] / p["total"] for p in prep)
     value = frac_bytes * args.steps / el / 1e9
-    sample = ("per step: " + ", ".join(f"{p['n']} of {p['total']} outputs of {p['wl'].name}" for p in prep)
-              + "; bytes credited in proportion to outputs computed")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+    unit = "images (backward data)" if bwd else "outputs"
+    sample = ("per step: " + ", ".join(f"{p['n']} of {p['total']} {unit} of {p['wl'].name}" for p in prep)
+              + "; bytes credited in proportion to the work computed")
+    line = {"impl": "reference", "metric": METRIC.replace("fwd", "bwd_data") if bwd else METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": wls[0].dtype, "data": "synthetic",
-            "config": {"workload": describe(wls), "layout": "NHWGC / GKYXC / NHWGK"},
+            "config": {"workload": describe(wls), "layout": "NHWGC / GKYXC / NHWGK",
+                       "op": "bwd_data" if bwd else "fwd"},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -581,7 +600,8 @@ def run_ours(args, wls, set_name, rank, world):
     if not args.no_e2e and not bwd:
         e2e = run_e2e(args, convs, lib, dev, stream, world, dist, step_bytes, gc)
 
-    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+    line = {"metric": METRIC.replace("fwd", "bwd_data") if bwd else METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wls[0].dtype, "data": "synthetic",
             "config": {"workload": describe(wls), "layout": "NHWGC / GKYXC / NHWGK",
