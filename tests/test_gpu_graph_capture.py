@@ -1,0 +1,73 @@
+"""The C-ABI calls inside a CUDA graph: capture a forward depthwise, a
+forward tensor-core and a backward-data call once, then replay the graph over
+new input values copied into the captured buffers, and compare every output
+with the oracle after each replay (the batch-1 launch-overhead path: one graph
+launch for a sequence of layers)."""
+import pytest
+import torch
+
+import depthwise_convolution_forward_gb300 as gc
+from depthwise_convolution_forward_gb300 import inputs
+from gpu_util import assert_close, out_shape_of, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def test_capture_and_replay(orc):
+    dw = inputs.by_name("mbv2_dw_s1_f16").with_(N=2)
+    tc = inputs.by_name("resnext_b_bf16").with_(N=2)
+    bw = inputs.by_name("resnext_a_bf16").with_(N=1, bias=False)
+    cases = []
+    for wl in (dw, tc):
+        x, w, b = inputs.make_inputs(wl)
+        cases.append(dict(wl=wl, x=x.to(DEV), w=w.to(DEV), b=b.to(DEV),
+                          y=torch.empty(out_shape_of(wl), dtype=x.dtype, device=DEV)))
+    _, wb, _ = inputs.make_inputs(bw)
+    dy = torch.empty(out_shape_of(bw), dtype=wb.dtype, device=DEV)
+    wbd = wb.to(DEV)
+    dx = torch.empty(bw.x_shape(), dtype=wb.dtype, device=DEV)
+    need = gc.grouped_conv_bwd_data_workspace_size(gc.problem_of(bw), gc.DTYPE_CODES[bw.dtype])
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=DEV)
+
+    s = torch.cuda.Stream(DEV)
+    graph = torch.cuda.CUDAGraph()
+    s.wait_stream(torch.cuda.current_stream(DEV))
+    with torch.cuda.stream(s):
+        for c in cases:  # warm-up outside capture: plans cached, attributes set
+            gc.grouped_conv_fwd(c["x"], c["w"], c["b"], c["y"], gc.problem_of(c["wl"]),
+                                gc.DTYPE_CODES[c["wl"].dtype], s)
+        gc.grouped_conv_bwd_data(dy, wbd, dx, gc.problem_of(bw), gc.DTYPE_CODES[bw.dtype], ws, need, s)
+    s.synchronize()
+    with torch.cuda.graph(graph, stream=s):
+        for c in cases:
+            gc.grouped_conv_fwd(c["x"], c["w"], c["b"], c["y"], gc.problem_of(c["wl"]),
+                                gc.DTYPE_CODES[c["wl"].dtype], s)
+        gc.grouped_conv_bwd_data(dy, wbd, dx, gc.problem_of(bw), gc.DTYPE_CODES[bw.dtype], ws, need, s)
+
+    for rep in range(3):
+        gen = torch.Generator().manual_seed(4242 + rep)
+        host = []
+        for c in cases:
+            xh = (torch.rand(c["x"].shape, generator=gen) * 2 - 1).to(c["x"].dtype)
+            c["x"].copy_(xh)
+            host.append(xh)
+        dyh = (torch.rand(dy.shape, generator=gen) * 2 - 1).to(dy.dtype)
+        dy.copy_(dyh)
+        c_y = [c["y"] for c in cases]
+        for y in c_y:
+            y.fill_(float("nan"))
+        dx.fill_(float("nan"))
+        torch.cuda.synchronize(DEV)
+        graph.replay()
+        torch.cuda.synchronize(DEV)
+        for c, xh in zip(cases, host):
+            ref = orc.forward(c["wl"], xh, c["w"].cpu(), c["b"].cpu())
+            assert_close(c["y"].cpu().double().numpy(), ref, c["wl"].dtype, f"replay {rep}: {c['wl'].name}")
+        assert_close(dx.cpu().double().numpy(), orc.bwd_data(bw, dyh, wb), bw.dtype, f"replay {rep}: bwd data")
