@@ -52,3 +52,26 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--warmup", "0"], capture_output=True, text=True, env=env, timeout=300)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+@pytest.mark.parametrize("op", ["fwd", "bwd_data"])
+def test_reference_arm_json_line(op):
+    """Rank 0 of the reference arm prints one JSON line with the contract's keys,
+    for the forward pass and for backward data (the oracle on the host cores)."""
+    import json
+
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--op", op,
+                        "--workload", "grouped2d_f32_smoke", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["config"]["op"] == op
+    assert ("bwd_data" in d["metric"]) == (op == "bwd_data")
+    for k in ("value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "cpu_baseline",
+              "e2e"):
+        assert k in d, k
+    assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
