@@ -1,0 +1,55 @@
+// Test harness (host only): the tensor-core kernel's tile planner on problems
+// read from stdin, one JSON line per problem on stdout.  Built and run by
+// tests/test_plans.py; nothing here launches a kernel.
+#include "../../depthwise_convolution_forward_gb300/csrc/tc.cu"
+
+#include <cstdio>
+
+namespace gconv {
+// The planner never encodes a tensor map; the launch path that would is not run.
+CUresult encode_tiled(CUtensorMap*, CUtensorMapDataType, uint32_t, const void*, const uint64_t*, const uint64_t*,
+                      const uint32_t*, const uint32_t*, CUtensorMapSwizzle) {
+  return CUDA_ERROR_NOT_SUPPORTED;
+}
+}  // namespace gconv
+
+using namespace gconv;
+
+int main() {
+  Geometry g{};
+  int bf16, ov[8];
+  long long N;
+  while (scanf("%lld %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d", &N, &g.G,
+               &g.Cg, &g.Kg, &g.D, &g.H, &g.W, &g.Do, &g.Ho, &g.Wo, &g.Z, &g.Y, &g.X, &g.sD, &g.sH, &g.sW, &g.pD,
+               &g.pH, &g.pW, &g.dD, &g.dH, &g.dW, &g.ndim, &bf16, &ov[0], &ov[2], &ov[3], &ov[4]) == 28) {
+    g.N = N;
+    ov[1] = ov[5] = ov[6] = ov[7] = 0;
+    const bool any_ov = ov[0] || ov[2] || ov[3] || ov[4];
+    TcPlan p;
+    std::memset(&p, 0, sizeof(p));
+    const int m = merge_factor(g);
+    const bool ok = m > 0 && make_tc_plan(g, bf16 != 0, 152, 232448, any_ov ? ov : nullptr, &p);
+    if (!ok) {
+      printf("{\"ok\": false, \"m\": %d}\n", m);
+      continue;
+    }
+    const tc::TcArgs& a = p.a;
+    uint32_t max_a = 0, max_b = 0;
+    for (int i = 0; i < a.ntab; ++i) {
+      const uint2 e = a.tab[i];
+      if ((e.y >> 16) & 2u) continue;  // skipped slot
+      max_a = std::max(max_a, (e.x & 0xffffu) << 4);
+      max_b = std::max(max_b, (e.x >> 16) << 4);
+    }
+    printf("{\"ok\": true, \"m\": %d, \"sw\": %d, \"smem\": %u, \"grid\": %d, \"tmem_cols\": %u, \"np\": %d, "
+           "\"nmt\": %d, \"sc\": %d, \"Nn\": %d, \"KS\": %d, \"TH\": %d, \"TWo\": %d, \"P\": %d, \"Hh\": %d, "
+           "\"Dh\": %d, \"stages\": %d, \"a_off\": %u, \"b_off\": %u, \"a_stage_bytes\": %u, \"plane_stride\": %u, "
+           "\"nphase\": %d, \"nchunks\": %d, \"tx_bytes\": %u, \"tiles_h\": %d, \"tiles_w\": %d, \"spatial\": %d, "
+           "\"cpg\": %d, \"n_gc\": %d, \"ntab\": %d, \"max_a\": %u, \"max_b\": %u, \"tab_off\": %u, "
+           "\"bias_off\": %u}\n",
+           m, (int)p.sw, p.smem_bytes, p.grid, a.tmem_cols, a.np, a.nmt, a.sc, a.Nn, a.KS, a.TH, a.TWo, a.P, a.Hh,
+           a.Dh, a.stages, a.a_off, a.b_off, a.a_stage_bytes, a.plane_stride, a.nphase, a.nchunks, a.tx_bytes,
+           a.tiles_h, a.tiles_w, a.spatial_tiles, a.cpg, a.n_gc, a.ntab, max_a, max_b, a.tab_off, a.bias_off);
+  }
+  return 0;
+}

@@ -1,0 +1,181 @@
+"""Host-side tile planners against the invariants their kernels rely on (no GPU).
+
+The planners of the depthwise and tensor-core kernels are compiled into two
+host-only harnesses (``tests/harness/plan_*.cu``, built with nvcc) and run on
+every workload family, random problems and maximum-size problems:
+
+* shared memory within the per-block and per-SM budgets, for the planned
+  CTAs per SM; thread counts within the kernels' launch bounds;
+* TMA boxes within 256 elements per dimension, with 16-byte inner extents,
+  and stage / operand bases 1024-byte aligned;
+* tiles that cover the whole output; halo extents that match the filter;
+* tensor-core plans: TMEM columns a power of two that holds the double-
+  buffered (partial) accumulators, the host MMA table within its bound and
+  its offsets inside the operand regions, the grid = group chunks x CTAs
+  per chunk.
+"""
+import json
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+from depthwise_convolution_forward_gb300 import inputs
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+SMEM_BLOCK = 232448  # opt-in shared memory per block on sm_103a
+SMEM_SM = 233472     # shared memory per SM
+RESERVED = 1024      # per-block reservation
+
+
+@pytest.fixture(scope="module")
+def harness(tmp_path_factory):
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    out = tmp_path_factory.mktemp("plans")
+    exes = {}
+    for name in ("plan_tc", "plan_dw"):
+        exe = str(out / name)
+        subprocess.run([nvcc, "-std=c++17", "-O1", "-gencode", "arch=compute_103a,code=sm_103a",
+                        "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include"),
+                        os.path.join(HERE, "harness", name + ".cu"), "-o", exe],
+                       check=True, capture_output=True, text=True)
+        exes[name] = exe
+    return exes
+
+
+def _extent(i, k, s, p, d):
+    room = i + 2 * p - (d * (k - 1) + 1)
+    return room // s + 1 if room >= 0 else 0
+
+
+def _geom(wl):
+    out = [_extent(wl.inp[i], wl.ker[i], wl.stride[i], wl.pad[i], wl.dil[i]) for i in range(3)]
+    return out, [wl.N, wl.G, wl.Cg, wl.Kg, *wl.inp, *out, *wl.ker, *wl.stride, *wl.pad, *wl.dil, wl.ndim]
+
+
+def _run(exe, lines):
+    r = subprocess.run([exe], input="\n".join(lines) + "\n", capture_output=True, text=True, check=True,
+                       timeout=300)
+    return [json.loads(ln) for ln in r.stdout.splitlines()]
+
+
+def _problems(seed, n, **kw):
+    rng = np.random.default_rng(seed)
+    return [inputs.random_problem(rng, **kw) for _ in range(n)]
+
+
+def _dw_candidates():
+    probs = [wl for wl in inputs.all_workloads() if wl.Cg == 1 and wl.Kg == 1]
+    probs += [inputs.by_name("mbv2_dw_s1_f16").with_(N=4800)]
+    rng = np.random.default_rng(77)
+    for _ in range(300):
+        dt = str(rng.choice(["f16", "bf16", "f32"]))
+        vec = 4 if dt == "f32" else 8
+        s, d = int(rng.integers(1, 3)), int(rng.integers(1, 3))
+        nd = int(rng.choice([2, 2, 3]))
+        hw = [int(rng.integers(1, 80)), int(rng.integers(1, 80))]
+        z = int(rng.choice([1, 3])) if nd == 3 else 1
+        dz = int(rng.integers(1, 3)) if nd == 3 else 1
+        inp = (int(rng.integers(max(1, dz * (z - 1) + 1), 9)) if nd == 3 else 1, *hw)
+        wl = inputs.Workload("r", 0, 0, nd, int(rng.integers(1, 9)), vec * int(rng.integers(1, 65)), 1, 1,
+                             inp, (z, 3, 3), (1 if nd == 2 else int(rng.integers(1, 3)), s, s),
+                             (0 if nd == 2 else int(rng.integers(0, 2)), d, d), (dz, d, d), dt, True)
+        if min(_geom(wl)[0]) >= 1:
+            probs.append(wl)
+    return probs
+
+
+def test_depthwise_plans(harness):
+    probs = _dw_candidates()
+    lines = []
+    for wl in probs:
+        es = 4 if wl.dtype == "f32" else 2
+        lines.append(" ".join(map(str, _geom(wl)[1] + [es, 96])))  # 96 registers: above any build's count
+    res = _run(harness["plan_dw"], lines)
+    assert len(res) == len(probs)
+    planned = 0
+    for wl, p in zip(probs, res):
+        if not p["ok"]:
+            continue
+        planned += 1
+        out = _geom(wl)[0]
+        es = 4 if wl.dtype == "f32" else 2
+        ctx = (wl, p)
+        assert p["smem"] <= SMEM_BLOCK, ctx
+        assert p["ctas"] * (p["smem"] + RESERVED) <= SMEM_SM, ctx
+        assert p["threads"] % 32 == 0 and p["threads"] <= 1024, ctx
+        if p["col"]:
+            assert p["threads"] <= p["max_threads"], ctx
+        assert p["TC"] <= 256 and (p["TC"] * es) % 16 == 0 and wl.C % p["TC"] == 0, ctx
+        assert max(p["Wh"], p["Hh"], p["Dh"]) <= 256, ctx
+        assert p["stage_off"] % 1024 == 0 and p["stage_stride"] % 1024 == 0, ctx
+        assert p["stage_bytes"] == p["Dh"] * p["Hh"] * p["Wh"] * p["TC"] * es, ctx
+        assert p["stage_bytes"] <= p["stage_stride"], ctx
+        assert p["smem"] >= p["stage_off"] + p["stages"] * p["stage_stride"], ctx
+        assert 2 <= p["stages"] <= 4, ctx
+        assert p["Hh"] == (p["TH"] - 1) * wl.stride[1] + 2 * wl.dil[1] + 1, ctx
+        assert p["tiles_h"] * p["TH"] >= out[1] and (p["tiles_h"] - 1) * p["TH"] < out[1], ctx
+        assert p["tiles_w"] * p["TW"] >= out[2] and (p["tiles_w"] - 1) * p["TW"] < out[2], ctx
+        assert p["num_tiles"] == p["tiles_c"] * p["tiles_w"] * p["tiles_h"] * out[0] * wl.N, ctx
+        if p["col"]:
+            assert p["h0"] == p["Hh"], ctx  # one copy per tile unless requested
+    assert planned >= 0.9 * len(probs)
+
+
+def _tc_candidates():
+    probs = [wl for wl in inputs.all_workloads() if wl.dtype != "f32" and not (wl.Cg == 1 and wl.Kg == 1)]
+    probs += [inputs.by_name("sweep_g32_d1_s1_bf16").with_(N=5400)]
+    # random shapes with a merge factor: per-group channels that 16-channel
+    # MMA operands can pack, and enough groups to merge
+    rng = np.random.default_rng(99)
+    for wl in _problems(99, 400, max_c=64, max_hw=40):
+        cg, kg = (int(rng.choice([2, 4, 8, 16, 32, 64])) for _ in range(2))
+        G = int(rng.choice([1, 2, 4, 8, 16, 32])) * max(1, 16 // min(cg, kg))
+        probs.append(wl.with_(Cg=cg, Kg=kg, G=G, N=int(rng.integers(1, 9)),
+                              dtype="bf16" if wl.dtype == "f32" else wl.dtype))
+    return [wl for wl in probs if wl.stride[1] == wl.stride[2] and wl.stride[1] <= 2 and min(_geom(wl)[0]) >= 1]
+
+
+def test_tensor_core_plans(harness):
+    probs = _tc_candidates()
+    lines = [" ".join(map(str, _geom(wl)[1] + [int(wl.dtype == "bf16"), 0, 0, 0, 0])) for wl in probs]
+    res = _run(harness["plan_tc"], lines)
+    assert len(res) == len(probs)
+    planned = mergeable = 0
+    for wl, p in zip(probs, res):
+        mergeable += p["m"] > 0
+        if not p["ok"]:
+            continue
+        planned += 1
+        out = _geom(wl)[0]
+        ctx = (wl, p)
+        G2 = p["sc"] * p["nmt"]
+        assert p["smem"] <= SMEM_BLOCK, ctx
+        assert p["tmem_cols"] in (32, 64, 128, 256, 512), ctx
+        assert p["tmem_cols"] >= 2 * p["np"] * G2 * p["Nn"], ctx  # double-buffered (partial) accumulators
+        if p["tmem_cols"] > 256:  # a second CTA could not allocate beside it: keep it off the SM
+            assert p["smem"] + RESERVED > SMEM_SM // 2, ctx
+        assert 1 <= p["np"] <= max(1, wl.taps), ctx
+        assert p["Nn"] % 16 == 0 and 16 <= p["Nn"] <= 256, ctx
+        assert p["a_off"] % 1024 == 0 and p["b_off"] % 1024 == 0 and p["a_stage_bytes"] % 1024 == 0, ctx
+        assert p["plane_stride"] % (128 if p["sw"] else 16) == 0, ctx
+        assert p["a_off"] + p["stages"] * p["a_stage_bytes"] <= p["smem"], ctx
+        assert p["tx_bytes"] <= p["a_stage_bytes"], ctx
+        assert 2 <= p["stages"] <= 4, ctx
+        # TMA boxes: (channels, P, Hh, Dh, 1) with at most 256 per dimension
+        assert p["P"] <= 256 and p["Hh"] * wl.stride[1] <= 256 + 2 and p["Dh"] <= 256, ctx
+        assert p["TH"] * p["tiles_h"] >= out[1] and p["TWo"] * p["tiles_w"] >= out[2], ctx
+        assert p["spatial"] == wl.N * out[0] * p["tiles_h"] * p["tiles_w"], ctx
+        assert p["grid"] == (p["n_gc"] // p["sc"]) * p["cpg"], ctx
+        assert 0 <= p["ntab"] <= 2048, ctx
+        if p["ntab"]:
+            assert p["a_off"] <= p["max_a"] < p["a_off"] + p["a_stage_bytes"], ctx
+            assert p["b_off"] <= p["max_b"] < p["a_off"], ctx
+        assert p["bias_off"] < p["tab_off"] <= p["b_off"], ctx
+    assert mergeable >= 0.8 * len(probs)
+    assert planned >= 0.9 * mergeable, (planned, mergeable)
