@@ -1,5 +1,5 @@
-"""CPU oracle for grouped convolution forward and backward data -- TEST
-INFRASTRUCTURE ONLY.
+"""CPU oracle for grouped convolution forward, backward data and backward
+weight -- TEST INFRASTRUCTURE ONLY.
 
 The oracle (``oracle.c``) is a plain fp64 direct-loop grouped convolution
 written from the definition (see the header of ``oracle.c`` for the formula,
@@ -64,6 +64,8 @@ class Oracle:
         lib.oracle_grouped_conv_fwd_points.argtypes = (
             [_dp, _dp, _dp] + [ctypes.c_long] * 4 + [_i32p] * 5
             + [ctypes.POINTER(ctypes.c_int64), ctypes.c_long, _dp])
+        lib.oracle_grouped_conv_bwd_weight.restype = ctypes.c_int
+        lib.oracle_grouped_conv_bwd_weight.argtypes = [_dp, _dp, _dp] + [ctypes.c_long] * 4 + [_i32p] * 5
         lib.oracle_grouped_conv_bwd_data.restype = ctypes.c_int
         lib.oracle_grouped_conv_bwd_data.argtypes = [_dp, _dp, _dp] + [ctypes.c_long] * 4 + [_i32p] * 5
         self.lib = lib
@@ -136,6 +138,21 @@ class Oracle:
         if prob.ndim == 2:
             dx = dx.reshape(prob.N, H, W, prob.G, prob.Cg)
         return dx
+
+
+    def bwd_weight(self, prob, x, dy) -> np.ndarray:
+        """Backward weight: dw as float64 in w's layout [G, Kg, (Z), Y, X, Cg]
+        (Z omitted for 2D), the gradient of <forward(x, w), dy> with respect to w."""
+        xd, dyd = self._f64(x), self._f64(dy)
+        Z, Y, X = prob.ker
+        dw = np.empty((prob.G, prob.Kg, Z, Y, X, prob.Cg), dtype=np.float64)
+        rc = self.lib.oracle_grouped_conv_bwd_weight(
+            xd.ctypes.data_as(_dp), dyd.ctypes.data_as(_dp), dw.ctypes.data_as(_dp), *self._args(prob))
+        if rc != 0:
+            raise ValueError("oracle rejected the problem")
+        if prob.ndim == 2:
+            dw = dw.reshape(prob.G, prob.Kg, Y, X, prob.Cg)
+        return dw
 
 
 _default: Optional[Oracle] = None

@@ -247,3 +247,66 @@ int oracle_grouped_conv_bwd_data(const double *dy, const double *w, double *dx,
     }
     return 0;
 }
+
+/*
+ * Backward weight: the gradient with respect to w of a loss whose gradient
+ * with respect to y is dy.  Grouped Convolution Tile Engine and Grouped
+ * Convolution -- Python Examples (Examples, Runner argument contract): a
+ * backward-weight variant takes X and dY.  Written from the forward
+ * definition: each weight multiplies the input values its taps read, so
+ *
+ *   dw[g, k, z, yy, xx, cg] = sum over (n, od, oh, ow) of
+ *       dy[n, od, oh, ow, g, k] * x[n, od*sD - pD + z*dD, oh*sH - pH + yy*dH, ow*sW - pW + xx*dW, g, cg]
+ *
+ * with out-of-range input positions contributing zero.  Layouts: x as in the
+ * forward pass, dy [N][Do][Ho][Wo][G][Kg], dw [G][Kg][Z][Y][X][Cg].  Parallel
+ * over (g, k): those slices of dw are disjoint.  Returns 0, or -1 for a
+ * malformed or empty problem.
+ */
+int oracle_grouped_conv_bwd_weight(const double *x, const double *dy, double *dw,
+                                   long N, long G, long Cg, long Kg,
+                                   const int32_t *in3, const int32_t *ker3, const int32_t *st3,
+                                   const int32_t *pd3, const int32_t *dl3)
+{
+    long in[3], ker[3], st[3], pd[3], dl[3], out[3];
+    if (N <= 0 || G <= 0 || Cg <= 0 || Kg <= 0)
+        return -1;
+    if (unpack(in3, ker3, st3, pd3, dl3, in, ker, st, pd, dl, out))
+        return -1;
+    const long D = in[0], H = in[1], W = in[2];
+    const long Z = ker[0], Y = ker[1], X = ker[2];
+    const long Do = out[0], Ho = out[1], Wo = out[2];
+    const long C = G * Cg, K = G * Kg;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long gk = 0; gk < G * Kg; ++gk) {
+        const long g = gk / Kg, k = gk % Kg;
+        for (long z = 0; z < Z; ++z)
+            for (long yy = 0; yy < Y; ++yy)
+                for (long xx = 0; xx < X; ++xx) {
+                    double *wp = dw + ((((g * Kg + k) * Z + z) * Y + yy) * X + xx) * Cg;
+                    for (long cg = 0; cg < Cg; ++cg)
+                        wp[cg] = 0.0;
+                    for (long n = 0; n < N; ++n)
+                        for (long od = 0; od < Do; ++od) {
+                            const long di = od * st[0] - pd[0] + z * dl[0];
+                            if (di < 0 || di >= D)
+                                continue;
+                            for (long oh = 0; oh < Ho; ++oh) {
+                                const long hi = oh * st[1] - pd[1] + yy * dl[1];
+                                if (hi < 0 || hi >= H)
+                                    continue;
+                                for (long ow = 0; ow < Wo; ++ow) {
+                                    const long wi = ow * st[2] - pd[2] + xx * dl[2];
+                                    if (wi < 0 || wi >= W)
+                                        continue;
+                                    const double dyv = dy[(((n * Do + od) * Ho + oh) * Wo + ow) * K + g * Kg + k];
+                                    const double *xp = x + ((((n * D + di) * H + hi) * W + wi) * C + g * Cg);
+                                    for (long cg = 0; cg < Cg; ++cg)
+                                        wp[cg] += dyv * xp[cg];
+                                }
+                            }
+                        }
+                }
+    }
+    return 0;
+}

@@ -334,3 +334,44 @@ def pin_bwd_torch(orc):
 
 
 BWD_PINS = [pin_bwd_adjoint, pin_bwd_torch]
+
+
+# ---------------------------------------------------------------------------
+# Backward weight: pins that do not use the oracle's own backward code
+# ---------------------------------------------------------------------------
+def torch_bwd_weight(p: Workload, x, dy):
+    """torch.nn.grad.conv{2,3}d_weight(groups=G) on CPU float64, layouts permuted."""
+    xt = torch.as_tensor(np.asarray(x, dtype=np.float64))
+    dyt = torch.as_tensor(np.asarray(dy, dtype=np.float64))
+    if p.ndim == 2:
+        xc = xt.reshape(p.N, p.inp[1], p.inp[2], p.C).permute(0, 3, 1, 2)
+        dyc = dyt.reshape(p.N, dyt.shape[1], dyt.shape[2], p.K).permute(0, 3, 1, 2)
+        dw = torch.nn.grad.conv2d_weight(xc, (p.K, p.Cg, p.ker[1], p.ker[2]), dyc, stride=p.stride[1:],
+                                         padding=p.pad[1:], dilation=p.dil[1:], groups=p.G)
+        return dw.permute(0, 2, 3, 1).reshape(p.G, p.Kg, p.ker[1], p.ker[2], p.Cg).numpy()
+    xc = xt.reshape(p.N, *p.inp, p.C).permute(0, 4, 1, 2, 3)
+    dyc = dyt.reshape(p.N, *dyt.shape[1:4], p.K).permute(0, 4, 1, 2, 3)
+    dw = torch.nn.grad.conv3d_weight(xc, (p.K, p.Cg, *p.ker), dyc, stride=p.stride, padding=p.pad,
+                                     dilation=p.dil, groups=p.G)
+    return dw.permute(0, 2, 3, 4, 1).reshape(p.G, p.Kg, *p.ker, p.Cg).numpy()
+
+
+def pin_bwd_weight_adjoint(orc):
+    """The forward pass is linear in w: <forward(x, w), dy> == <w, bwd_weight(x, dy)>."""
+    for i, p in enumerate(bwd_problems()):
+        x, w, _ = rand_inputs(p, 700 + i)
+        dy = _rand_dy(p, orc, 800 + i)
+        lhs = float(np.sum(orc.forward(p, x, w, None) * dy))
+        dw = orc.bwd_weight(p, x, dy)
+        rhs = float(np.sum(np.asarray(w).reshape(dw.shape) * dw))
+        assert abs(lhs - rhs) <= 1e-10 * (1.0 + abs(lhs)), (i, lhs, rhs)
+
+
+def pin_bwd_weight_torch(orc):
+    for i, p in enumerate(bwd_problems()):
+        x, _, _ = rand_inputs(p, 900 + i)
+        dy = _rand_dy(p, orc, 1000 + i)
+        _close(orc.bwd_weight(p, x, dy), torch_bwd_weight(p, x, dy))
+
+
+BWD_WEIGHT_PINS = [pin_bwd_weight_adjoint, pin_bwd_weight_torch]

@@ -17,7 +17,8 @@ BWD_MUTANTS = {
     "bwd_pad_sign": ("const long ih = oh * st[1] - pd[1]", "const long ih = oh * st[1] + pd[1]"),
     "bwd_drop_dilation_w": ("const long iw = ow * st[2] - pd[2] + xx * dl[2];",
                             "const long iw = ow * st[2] - pd[2] + xx;"),
-    "bwd_dy_channel_transposed": ("* K + g * Kg + k];", "* K + k * G + g];"),
+    "bwd_dy_channel_transposed": ("const double d = dy[(((n * Do + od) * Ho + oh) * Wo + ow) * K + g * Kg + k];",
+                                  "const double d = dy[(((n * Do + od) * Ho + oh) * Wo + ow) * K + k * G + g];"),
     "bwd_dx_group_uses_kg": ("* W + iw) * C + g * Cg);\n                                    const double *wp",
                              "* W + iw) * C + g * Kg);\n                                    const double *wp"),
     "bwd_kernel_flipped": ("const double *wp = w + ((((g * Kg + k) * Z + z) * Y + yy) * X + xx) * Cg;\n"
