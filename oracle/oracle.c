@@ -1,12 +1,14 @@
 /*
- * Grouped convolution forward -- CPU oracle (TEST INFRASTRUCTURE ONLY).
+ * Grouped convolution forward, backward data and backward weight -- CPU
+ * oracle (TEST INFRASTRUCTURE ONLY).
  *
  * This file is the slow, obviously-correct reference that the CUDA path is
  * checked against.  Only the test-suite, the smoke check and the benchmark's
  * CPU-baseline leg may build, load or call it; the product never does.  It
  * shares no code, header or table with the CUDA library.
  *
- * What it computes (the plain definition of grouped convolution):
+ * What it computes (the plain definition of grouped convolution; the two
+ * gradients are defined beside their functions at the end of the file):
  *
  *   y[n, od, oh, ow, g, k] =
  *       sum_{z, yy, xx} sum_{cg < Cg}
