@@ -1,7 +1,8 @@
 /*
- * gconv.h -- C ABI of the GB300 grouped-convolution forward library.
+ * gconv.h -- C ABI of the GB300 grouped-convolution library: the forward
+ * pass and backward data (grouped_conv_bwd_data, further below).
  *
- * The operation is the grouped convolution forward pass (groups > 1,
+ * The main operation is the grouped convolution forward pass (groups > 1,
  * including depthwise groups == C), 2D and 3D, with optional bias, stride,
  * padding and dilation:
  *

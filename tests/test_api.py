@@ -162,3 +162,50 @@ def test_bwd_data_overlap_and_forced_route_rejected():
         gc.grouped_conv_bwd_data_ex(base, base + (1 << 20), base + (1 << 22), good(stride=(1, 2, 2)), B.GCONV_F16,
                                     None, 0, None, opt)
     assert e.value.status == B.GCONV_ERR_UNSUPPORTED
+
+
+def test_plain_c_program_uses_the_abi(tmp_path):
+    """The header is plain C: a C99 program includes it, links libgconv.so and
+    calls the host-only entry points (no GPU needed for these)."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    lib = B.load_library()
+    libdir = os.path.dirname(lib._name)
+    src = tmp_path / "use_abi.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include "gconv.h"
+int main(void) {
+  gconv_problem p = {0};
+  p.ndim = 2; p.N = 32; p.G = 144; p.C = 144; p.K = 144;
+  p.in[0] = 1; p.in[1] = 56; p.in[2] = 56;
+  p.ker[0] = 1; p.ker[1] = 3; p.ker[2] = 3;
+  p.stride[0] = 1; p.stride[1] = 2; p.stride[2] = 2;
+  p.pad[0] = 0; p.pad[1] = 1; p.pad[2] = 1;
+  p.dil[0] = 1; p.dil[1] = 1; p.dil[2] = 1;
+  int32_t out[3], kernel = -1;
+  int64_t ws = -1;
+  if (grouped_conv_out_shape(&p, out) != GCONV_OK) return 1;
+  if (grouped_conv_select(&p, GCONV_F16, &kernel) != GCONV_OK) return 2;
+  if (grouped_conv_bwd_data_workspace_size(&p, GCONV_F16, &ws) != GCONV_OK) return 3;
+  p.C = 145;
+  gconv_status bad = grouped_conv_out_shape(&p, out);
+  printf("%d %d %d %d %lld %d %s\n", out[0], out[1], out[2], kernel, (long long)ws, (int)bad,
+         gconv_status_string(bad));
+  return 0;
+}
+""")
+    exe = tmp_path / "use_abi"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I" + os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                    "-L" + libdir, "-lgconv", "-Wl,-rpath," + libdir], check=True, capture_output=True, text=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    d, h, w, kernel, ws, bad, text = r.stdout.split(maxsplit=6)
+    assert (int(d), int(h), int(w)) == (1, 28, 28)
+    assert int(kernel) == B.KERNEL_DIRECT_DW
+    assert int(ws) == 0  # stride 2: the direct backward kernel needs no workspace
+    assert int(bad) == B.GCONV_ERR_INVALID_ARG and text.strip() == "invalid argument"
