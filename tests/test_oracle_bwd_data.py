@@ -47,3 +47,34 @@ def test_bwd_mutant_is_caught(tmp_path, name):
         except (AssertionError, ValueError):
             caught.append(pin.__name__)
     assert caught, f"mutant {name} passed every pin"
+
+
+def test_stride1_backward_data_is_a_forward_pass(orc):
+    """The identity the library's stride-1 backward-data route runs on, checked
+    with the pinned oracles alone: for stride 1 and pad <= d*(k-1), backward
+    data equals the forward convolution of dy with per-group transposed,
+    spatially flipped weights wt[g, c, t', k] = w[g, k, flip(t'), c], Cg and
+    Kg swapped and padding d*(k-1) - pad."""
+    import numpy as np
+
+    from depthwise_convolution_forward_gb300 import inputs
+
+    rng = np.random.default_rng(11)
+    checked = 0
+    for _ in range(400):
+        wl = inputs.random_problem(rng)
+        if any(s != 1 for s in wl.stride) or any(p > d * (k - 1) for p, d, k in zip(wl.pad, wl.dil, wl.ker)):
+            continue
+        w = rng.normal(size=wl.w_shape())
+        out = orc.out_shape(wl)
+        dy = rng.uniform(-1, 1, size=(wl.N, *out, wl.G, wl.Kg))
+        ref = orc.bwd_data(wl, dy, w).reshape(wl.N, *wl.inp, wl.G, wl.Cg)
+        w6 = w.reshape(wl.G, wl.Kg, *wl.ker, wl.Cg)
+        wt = np.ascontiguousarray(np.transpose(w6[:, :, ::-1, ::-1, ::-1, :], (0, 5, 2, 3, 4, 1)))
+        f = wl.with_(Cg=wl.Kg, Kg=wl.Cg, inp=tuple(out), bias=False,
+                     pad=tuple(d * (k - 1) - p for p, d, k in zip(wl.pad, wl.dil, wl.ker)))
+        assert orc.out_shape(f) == tuple(wl.inp)
+        got = orc.forward(f, dy, wt, None).reshape(ref.shape)
+        assert np.allclose(got, ref, rtol=1e-12, atol=1e-12), wl
+        checked += 1
+    assert checked >= 20
