@@ -141,6 +141,35 @@ def _tc_candidates():
     return [wl for wl in probs if wl.stride[1] == wl.stride[2] and wl.stride[1] <= 2 and min(_geom(wl)[0]) >= 1]
 
 
+def _check_tc_plan(wl, p):
+    """Invariants of one tensor-core plan (see the module docstring)."""
+    out = _geom(wl)[0]
+    ctx = (wl, p)
+    G2 = p["sc"] * p["nmt"]
+    assert p["smem"] <= SMEM_BLOCK, ctx
+    assert p["tmem_cols"] in (32, 64, 128, 256, 512), ctx
+    assert p["tmem_cols"] >= 2 * p["np"] * G2 * p["Nn"], ctx  # double-buffered (partial) accumulators
+    if p["tmem_cols"] > 256:  # a second CTA could not allocate beside it: keep it off the SM
+        assert p["smem"] + RESERVED > SMEM_SM // 2, ctx
+    assert 1 <= p["np"] <= max(1, wl.taps), ctx
+    assert p["Nn"] % 16 == 0 and 16 <= p["Nn"] <= 256, ctx
+    assert p["a_off"] % 1024 == 0 and p["b_off"] % 1024 == 0 and p["a_stage_bytes"] % 1024 == 0, ctx
+    assert p["plane_stride"] % (128 if p["sw"] else 16) == 0, ctx
+    assert p["a_off"] + p["stages"] * p["a_stage_bytes"] <= p["smem"], ctx
+    assert p["tx_bytes"] <= p["a_stage_bytes"], ctx
+    assert 2 <= p["stages"] <= 4, ctx
+    # TMA boxes: (channels, P, Hh, Dh, 1) with at most 256 per dimension
+    assert p["P"] <= 256 and p["Hh"] * wl.stride[1] <= 256 + 2 and p["Dh"] <= 256, ctx
+    assert p["TH"] * p["tiles_h"] >= out[1] and p["TWo"] * p["tiles_w"] >= out[2], ctx
+    assert p["spatial"] == wl.N * out[0] * p["tiles_h"] * p["tiles_w"], ctx
+    assert p["grid"] == (p["n_gc"] // p["sc"]) * p["cpg"], ctx
+    assert 0 <= p["ntab"] <= 2048, ctx
+    if p["ntab"]:
+        assert p["a_off"] <= p["max_a"] < p["a_off"] + p["a_stage_bytes"], ctx
+        assert p["b_off"] <= p["max_b"] < p["a_off"], ctx
+    assert p["bias_off"] < p["tab_off"] <= p["b_off"], ctx
+
+
 def test_tensor_core_plans(harness):
     probs = _tc_candidates()
     lines = [" ".join(map(str, _geom(wl)[1] + [int(wl.dtype == "bf16"), 0, 0, 0, 0])) for wl in probs]
@@ -149,33 +178,31 @@ def test_tensor_core_plans(harness):
     planned = mergeable = 0
     for wl, p in zip(probs, res):
         mergeable += p["m"] > 0
-        if not p["ok"]:
-            continue
-        planned += 1
-        out = _geom(wl)[0]
-        ctx = (wl, p)
-        G2 = p["sc"] * p["nmt"]
-        assert p["smem"] <= SMEM_BLOCK, ctx
-        assert p["tmem_cols"] in (32, 64, 128, 256, 512), ctx
-        assert p["tmem_cols"] >= 2 * p["np"] * G2 * p["Nn"], ctx  # double-buffered (partial) accumulators
-        if p["tmem_cols"] > 256:  # a second CTA could not allocate beside it: keep it off the SM
-            assert p["smem"] + RESERVED > SMEM_SM // 2, ctx
-        assert 1 <= p["np"] <= max(1, wl.taps), ctx
-        assert p["Nn"] % 16 == 0 and 16 <= p["Nn"] <= 256, ctx
-        assert p["a_off"] % 1024 == 0 and p["b_off"] % 1024 == 0 and p["a_stage_bytes"] % 1024 == 0, ctx
-        assert p["plane_stride"] % (128 if p["sw"] else 16) == 0, ctx
-        assert p["a_off"] + p["stages"] * p["a_stage_bytes"] <= p["smem"], ctx
-        assert p["tx_bytes"] <= p["a_stage_bytes"], ctx
-        assert 2 <= p["stages"] <= 4, ctx
-        # TMA boxes: (channels, P, Hh, Dh, 1) with at most 256 per dimension
-        assert p["P"] <= 256 and p["Hh"] * wl.stride[1] <= 256 + 2 and p["Dh"] <= 256, ctx
-        assert p["TH"] * p["tiles_h"] >= out[1] and p["TWo"] * p["tiles_w"] >= out[2], ctx
-        assert p["spatial"] == wl.N * out[0] * p["tiles_h"] * p["tiles_w"], ctx
-        assert p["grid"] == (p["n_gc"] // p["sc"]) * p["cpg"], ctx
-        assert 0 <= p["ntab"] <= 2048, ctx
-        if p["ntab"]:
-            assert p["a_off"] <= p["max_a"] < p["a_off"] + p["a_stage_bytes"], ctx
-            assert p["b_off"] <= p["max_b"] < p["a_off"], ctx
-        assert p["bias_off"] < p["tab_off"] <= p["b_off"], ctx
+        if p["ok"]:
+            planned += 1
+            _check_tc_plan(wl, p)
     assert mergeable >= 0.8 * len(probs)
     assert planned >= 0.9 * mergeable, (planned, mergeable)
+
+
+@pytest.mark.parametrize("name", ["sweep_g8_d1_s1_bf16", "resnext_a_bf16", "resnext_b_bf16", "resnext3d_n8_f16"])
+def test_tensor_core_overridden_plans(harness, name):
+    """Tile overrides (M tiles per CTA x partial accumulators x stages): every
+    combination whose accumulators fit tensor memory gets a plan, and every
+    plan keeps the invariants."""
+    wl = inputs.by_name(name)
+    combos = [(nmt, np_, st) for nmt in (1, 2, 3, 4) for np_ in (1, 2, 4) for st in (0, 2, 3)]
+    lines = [" ".join(map(str, _geom(wl)[1] + [int(wl.dtype == "bf16"), 0, nmt, st, np_])) for nmt, np_, st in combos]
+    res = _run(harness["plan_tc"], lines)
+    auto = _run(harness["plan_tc"], [" ".join(map(str, _geom(wl)[1] + [int(wl.dtype == "bf16"), 0, 0, 0, 0]))])[0]
+    assert auto["ok"]
+    G2_per_nmt = auto["sc"]  # accumulators per M tile
+    for (nmt, np_, st), p in zip(combos, res):
+        if p["ok"]:
+            assert p["nmt"] == nmt and p["np"] == np_, (nmt, np_, p)
+            if st:
+                assert p["stages"] <= st
+            _check_tc_plan(wl, p)
+        elif np_ <= wl.taps and 2 * np_ * G2_per_nmt * nmt * auto["Nn"] <= 512 and nmt <= 2 and st == 0:
+            # small tiles that fit tensor memory must be plannable
+            raise AssertionError(f"{name}: no plan for nmt {nmt} np {np_}")
