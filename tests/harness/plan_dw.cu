@@ -1,5 +1,6 @@
 // Test harness (host only): the depthwise kernel's tile planners (column and
-// row-blocked forms) on problems read from stdin, one JSON line per problem
+// row-blocked forms) on problems (with optional tile overrides) read from
+// stdin, one JSON line per problem
 // on stdout.  Built and run by tests/test_plans.py; nothing here launches a
 // kernel.  The register count the column planner needs is an input.
 #include "../../depthwise_convolution_forward_gb300/csrc/dw_launch.cuh"
@@ -17,20 +18,22 @@ using namespace gconv;
 
 int main() {
   Geometry g{};
-  int es, regs;
+  int es, regs, ov[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   long long N;
-  while (scanf("%lld %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d", &N, &g.G, &g.Cg,
-               &g.Kg, &g.D, &g.H, &g.W, &g.Do, &g.Ho, &g.Wo, &g.Z, &g.Y, &g.X, &g.sD, &g.sH, &g.sW, &g.pD, &g.pH,
-               &g.pW, &g.dD, &g.dH, &g.dW, &g.ndim, &es, &regs) == 25) {
+  // per problem: geometry, element size, registers, then overrides TH TW stages ctas (0 = automatic)
+  while (scanf("%lld %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d %d", &N, &g.G,
+               &g.Cg, &g.Kg, &g.D, &g.H, &g.W, &g.Do, &g.Ho, &g.Wo, &g.Z, &g.Y, &g.X, &g.sD, &g.sH, &g.sW, &g.pD,
+               &g.pH, &g.pW, &g.dD, &g.dH, &g.dW, &g.ndim, &es, &regs, &ov[0], &ov[1], &ov[3], &ov[4]) == 29) {
     g.N = N;
+    const bool any_ov = ov[0] || ov[1] || ov[3] || ov[4];
     dw::Plan p{};
     bool ok;
     int form = 0;
     if (g.Z == 1) {
       form = dw::col_form(es, nullptr);
-      ok = dw::make_col_plan(g, es, nullptr, 152, form, regs, &p);
+      ok = dw::make_col_plan(g, es, any_ov ? ov : nullptr, 152, form, regs, &p);
     } else {
-      ok = dw::make_plan(g, es, nullptr, 152, &p);
+      ok = dw::make_plan(g, es, any_ov ? ov : nullptr, 152, &p);
     }
     if (!ok) {
       printf("{\"ok\": false}\n");

@@ -95,36 +95,60 @@ def test_depthwise_plans(harness):
     lines = []
     for wl in probs:
         es = 4 if wl.dtype == "f32" else 2
-        lines.append(" ".join(map(str, _geom(wl)[1] + [es, 96])))  # 96 registers: above any build's count
+        lines.append(" ".join(map(str, _geom(wl)[1] + [es, 96, 0, 0, 0, 0])))  # 96 registers: above any build's
     res = _run(harness["plan_dw"], lines)
     assert len(res) == len(probs)
     planned = 0
     for wl, p in zip(probs, res):
+        if p["ok"]:
+            planned += 1
+            _check_dw_plan(wl, p)
+    assert planned >= 0.9 * len(probs)
+
+
+@pytest.mark.parametrize("name", ["mbv2_dw_s1_f16", "mbv2_dw_s2_f16", "sweep_g512_d2_s1_bf16"])
+def test_depthwise_overridden_plans(harness, name):
+    """Tile overrides of the column form (TH x TW x stages x CTAs per SM): every
+    plan they produce keeps the invariants, and the override is honoured."""
+    wl = inputs.by_name(name)
+    combos = [(th, tw, st, ct) for th in (0, 2, 4, 7, 14) for tw in (0, 7, 14, 28) for st in (0, 2, 3, 4)
+              for ct in (0, 1, 2, 3)]
+    lines = [" ".join(map(str, _geom(wl)[1] + [2, 96, th, tw, st, ct])) for th, tw, st, ct in combos]
+    res = _run(harness["plan_dw"], lines)
+    planned = 0
+    for (th, tw, st, ct), p in zip(combos, res):
         if not p["ok"]:
             continue
         planned += 1
-        out = _geom(wl)[0]
-        es = 4 if wl.dtype == "f32" else 2
-        ctx = (wl, p)
-        assert p["smem"] <= SMEM_BLOCK, ctx
-        assert p["ctas"] * (p["smem"] + RESERVED) <= SMEM_SM, ctx
-        assert p["threads"] % 32 == 0 and p["threads"] <= 1024, ctx
-        if p["col"]:
-            assert p["threads"] <= p["max_threads"], ctx
-        assert p["TC"] <= 256 and (p["TC"] * es) % 16 == 0 and wl.C % p["TC"] == 0, ctx
-        assert max(p["Wh"], p["Hh"], p["Dh"]) <= 256, ctx
-        assert p["stage_off"] % 1024 == 0 and p["stage_stride"] % 1024 == 0, ctx
-        assert p["stage_bytes"] == p["Dh"] * p["Hh"] * p["Wh"] * p["TC"] * es, ctx
-        assert p["stage_bytes"] <= p["stage_stride"], ctx
-        assert p["smem"] >= p["stage_off"] + p["stages"] * p["stage_stride"], ctx
-        assert 2 <= p["stages"] <= 4, ctx
-        assert p["Hh"] == (p["TH"] - 1) * wl.stride[1] + 2 * wl.dil[1] + 1, ctx
-        assert p["tiles_h"] * p["TH"] >= out[1] and (p["tiles_h"] - 1) * p["TH"] < out[1], ctx
-        assert p["tiles_w"] * p["TW"] >= out[2] and (p["tiles_w"] - 1) * p["TW"] < out[2], ctx
-        assert p["num_tiles"] == p["tiles_c"] * p["tiles_w"] * p["tiles_h"] * out[0] * wl.N, ctx
-        if p["col"]:
-            assert p["h0"] == p["Hh"], ctx  # one copy per tile unless requested
-    assert planned >= 0.9 * len(probs)
+        assert (not th or p["TH"] == th) and (not tw or p["TW"] == tw), (th, tw, p)
+        assert (not st or p["stages"] == st) and (not ct or p["ctas"] == ct), (st, ct, p)
+        _check_dw_plan(wl, p)
+    assert planned >= len(combos) // 4, planned
+
+
+def _check_dw_plan(wl, p):
+    """Invariants of one depthwise plan (see the module docstring)."""
+    out = _geom(wl)[0]
+    es = 4 if wl.dtype == "f32" else 2
+    ctx = (wl, p)
+    assert p["smem"] <= SMEM_BLOCK, ctx
+    assert p["ctas"] * (p["smem"] + RESERVED) <= SMEM_SM, ctx
+    assert p["threads"] % 32 == 0 and p["threads"] <= 1024, ctx
+    if p["col"]:
+        assert p["threads"] <= p["max_threads"], ctx
+    assert p["TC"] <= 256 and (p["TC"] * es) % 16 == 0 and wl.C % p["TC"] == 0, ctx
+    assert max(p["Wh"], p["Hh"], p["Dh"]) <= 256, ctx
+    assert p["stage_off"] % 1024 == 0 and p["stage_stride"] % 1024 == 0, ctx
+    assert p["stage_bytes"] == p["Dh"] * p["Hh"] * p["Wh"] * p["TC"] * es, ctx
+    assert p["stage_bytes"] <= p["stage_stride"], ctx
+    assert p["smem"] >= p["stage_off"] + p["stages"] * p["stage_stride"], ctx
+    assert 2 <= p["stages"] <= 4, ctx
+    assert p["Hh"] == (p["TH"] - 1) * wl.stride[1] + 2 * wl.dil[1] + 1, ctx
+    assert p["tiles_h"] * p["TH"] >= out[1] and (p["tiles_h"] - 1) * p["TH"] < out[1], ctx
+    assert p["tiles_w"] * p["TW"] >= out[2] and (p["tiles_w"] - 1) * p["TW"] < out[2], ctx
+    assert p["num_tiles"] == p["tiles_c"] * p["tiles_w"] * p["tiles_h"] * out[0] * wl.N, ctx
+    if p["col"]:
+        assert p["h0"] == p["Hh"], ctx  # one copy per tile unless requested
 
 
 def _tc_candidates():
