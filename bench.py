@@ -8,11 +8,17 @@ One "step" is one pass of the forward path over one batch of the workload
 Timing (per rank): inputs and outputs are rotated over R buffer sets whose
 total exceeds twice the L2, so no step reads the previous step's data from
 L2.  The K timed steps are captured into CUDA graphs of the library's own
-C-ABI calls with external event-record nodes between launches, then replayed
-between a barrier + synchronize on both sides.  The per-launch events give
-each kernel's device time inside the timed region (used for the roofline
-entry); the events around the whole region give ms_per_step.  Clocks are
-sampled with nvidia-smi during the timed region.
+C-ABI calls and replayed between a barrier + synchronize on both sides, with
+CUDA events on the launching stream at the start and the end only (an event
+between launches would add front-end work to every kernel); they give
+ms_per_step and `value`.  Clocks are sampled with nvidia-smi meanwhile.
+
+Per-launch times do not depend on K: every convolution of the step, and then
+every other workload of every config (``--per-launch``), is timed alone over
+a fixed number of back-to-back launches (``--launches``, graphs of 250
+launches bracketed by events).  The dominant kernel's mean gives the roofline
+entry; ``per_launch`` lists mean, median, GB/s, TFLOP/s and the fraction of
+the min(compute, HBM) roofline of each workload.
 
 ``--impl reference`` times the CPU oracle (the plain fp64 direct loop) on
 the host cores instead, each step a bounded sample of the same workload.
@@ -42,6 +48,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
 
 BENCH_SETS = {
+    "all": None,  # every workload of every config (filled in by resolve)
     "mbv2_dw": ["mbv2_dw_s1_f16", "mbv2_dw_s2_f16"],
     "resnext": ["resnext_a_bf16", "resnext_b_bf16"],
     "resnext3d_n8": ["resnext3d_n8_f16"],
@@ -66,55 +73,12 @@ def parse():
                          "(no end-to-end leg)")
     ap.add_argument("--serial-launch", action="store_true",
                     help="launch without programmatic dependent launch (each kernel starts after the previous ends)")
+    ap.add_argument("--launches", type=int, default=2000,
+                    help="back-to-back launches per convolution for its per-launch time (independent of --steps)")
+    ap.add_argument("--per-launch", default="all",
+                    help="workloads timed one at a time for per_launch besides the step's own: a bench set, "
+                         "comma-separated names, or none")
     return ap.parse_args()
-
-
-# ---------------------------------------------------------------------------
-# Driver-API events (external event-record nodes inside captured graphs)
-# ---------------------------------------------------------------------------
-class DriverEvents:
-    def __init__(self):
-        self.cu = ctypes.CDLL("libcuda.so.1")
-        self._create = self.cu.cuEventCreate
-        self._create.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_uint]
-        self._record = self.cu.cuEventRecordWithFlags
-        self._record.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
-        try:
-            self._elapsed = self.cu.cuEventElapsedTime_v2
-        except AttributeError:
-            self._elapsed = self.cu.cuEventElapsedTime
-        self._elapsed.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p]
-        try:
-            self._destroy = self.cu.cuEventDestroy_v2
-        except AttributeError:
-            self._destroy = self.cu.cuEventDestroy
-        self._destroy.argtypes = [ctypes.c_void_p]
-
-    def create(self, n):
-        out = []
-        for _ in range(n):
-            e = ctypes.c_void_p()
-            r = self._create(ctypes.byref(e), 0)
-            if r != 0:
-                raise RuntimeError(f"cuEventCreate failed: {r}")
-            out.append(e.value)
-        return out
-
-    def record_external(self, ev, stream_handle):
-        r = self._record(ctypes.c_void_p(ev), ctypes.c_void_p(stream_handle), 1)
-        if r != 0:
-            raise RuntimeError(f"cuEventRecordWithFlags failed: {r}")
-
-    def elapsed_ms(self, a, b):
-        ms = ctypes.c_float()
-        r = self._elapsed(ctypes.byref(ms), ctypes.c_void_p(a), ctypes.c_void_p(b))
-        if r != 0:
-            raise RuntimeError(f"cuEventElapsedTime failed: {r}")
-        return ms.value
-
-    def destroy(self, evs):
-        for e in evs:
-            self._destroy(ctypes.c_void_p(e))
 
 
 # ---------------------------------------------------------------------------
@@ -242,7 +206,10 @@ def resolve(names_arg):
     workload's shape in another storage type (f32, f16, bf16)."""
     from depthwise_convolution_forward_gb300 import inputs
 
-    names = BENCH_SETS.get(names_arg, None) or names_arg.split(",")
+    if names_arg == "all":
+        names = [wl.name for wl in inputs.all_workloads()]
+    else:
+        names = BENCH_SETS.get(names_arg, None) or names_arg.split(",")
     wls = []
     for n in names:
         base, _, dt = n.partition(":")
@@ -381,141 +348,181 @@ def run_reference(args, wls, rank, world):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+class GpuArm:
+    """Device buffers, launches and timing of one or more convolutions on one
+    GPU, through the library's C ABI (``grouped_conv_fwd_ex`` /
+    ``grouped_conv_bwd_data_ex``)."""
+
+    def __init__(self, args, dev, stream, bwd):
+        import depthwise_convolution_forward_gb300 as gc
+        from depthwise_convolution_forward_gb300 import _binding as B
+
+        self.gc, self.B = gc, B
+        self.lib = B.load_library()
+        self.dev, self.stream, self.sh = dev, stream, stream.cuda_stream
+        self.bwd = bwd
+        self.opt = B.gconv_options()
+        self.opt.force_kernel = args.force_kernel
+        self.opt.serial_launch = 1 if args.serial_launch else 0
+        tile = [int(t) for t in args.tile.split(",")] if args.tile else []
+        for i, t in enumerate(tile[:8]):
+            self.opt.tile[i] = t
+        self.optp = ctypes.byref(self.opt)
+
+    def prepare(self, wls):
+        """Host inputs, problem records and algorithmic work of each workload,
+        plus R device buffer sets whose total exceeds twice the L2."""
+        import torch
+
+        from depthwise_convolution_forward_gb300 import inputs, roofline
+
+        gc = self.gc
+        convs = []
+        for wl in wls:
+            x, w, b = inputs.make_inputs(wl)
+            if self.bwd:
+                wl = wl.with_(bias=False)
+                b = None
+            p = gc.problem_of(wl)
+            out = gc.grouped_conv_out_shape(p)
+            ysh = (wl.N, out[1], out[2], wl.G, wl.Kg) if wl.ndim == 2 else (wl.N, *out, wl.G, wl.Kg)
+            dt = gc.DTYPE_CODES[wl.dtype]
+            kernel = self.opt.force_kernel or gc.grouped_conv_select(p, dt)
+            convs.append(dict(wl=wl, x=x, w=w, b=b, p=p, ysh=ysh, out=out, dt=dt, kernel=kernel,
+                              bytes=roofline.algorithmic_bytes(wl, out), flops=roofline.flops(wl, out)))
+        per_set = sum(c["bytes"] for c in convs)
+        R = max(3, -(-2 * L2_BYTES // max(per_set, 1)) + 1)
+        sets = []
+        for r in range(R):
+            s = []
+            for c in convs:
+                wd = c["w"].to(self.dev)
+                if self.bwd:  # input dy (forward output layout, U(-1, 1)), output dx (forward input layout)
+                    g = torch.Generator().manual_seed(9500 + r)
+                    xd = (torch.rand(c["ysh"], generator=g) * 2 - 1).to(c["x"].dtype).to(self.dev)
+                    yd = torch.empty(c["x"].shape, dtype=c["x"].dtype, device=self.dev)
+                    bd = None
+                else:
+                    xd = c["x"].to(self.dev)
+                    bd = c["b"].to(self.dev) if c["b"] is not None else None
+                    yd = torch.empty(c["ysh"], dtype=c["x"].dtype, device=self.dev)
+                s.append((xd, wd, bd, yd))
+            sets.append(s)
+        if self.bwd:  # one workspace per convolution (stream order keeps consecutive calls apart)
+            for c in convs:
+                c["ws_bytes"] = gc.grouped_conv_bwd_data_workspace_size(c["p"], c["dt"])
+                c["ws"] = torch.empty(max(1, c["ws_bytes"]), dtype=torch.uint8, device=self.dev)
+        torch.cuda.synchronize(self.dev)
+        return convs, sets, R, per_set
+
+    def launch(self, convs, sets, r, ci):
+        c = convs[ci]
+        xd, wd, bd, yd = sets[r][ci]
+        if self.bwd:
+            st = self.lib.grouped_conv_bwd_data_ex(xd.data_ptr(), wd.data_ptr(), yd.data_ptr(), ctypes.byref(c["p"]),
+                                                   c["dt"], c["ws"].data_ptr() if c["ws_bytes"] else None,
+                                                   c["ws_bytes"], self.sh, self.optp)
+        else:
+            st = self.lib.grouped_conv_fwd_ex(xd.data_ptr(), wd.data_ptr(),
+                                              bd.data_ptr() if bd is not None else None, yd.data_ptr(),
+                                              ctypes.byref(c["p"]), c["dt"], self.sh, self.optp)
+        if st != 0:
+            raise RuntimeError(f"grouped_conv launch failed: {self.gc.gconv_last_error()}")
+        c["kernel"] = self.opt.selected
+        # launches of the library's kernels this call made (the transposed-
+        # weights route of backward data adds the weight-flip kernel)
+        c["kernels_per_call"] = 2 if self.bwd and c.get("ws_bytes") else 1
+
+    def capture(self, n_units, launch_unit, per_graph=1000):
+        """Graphs of back-to-back library calls (no event nodes inside: an
+        event between two launches adds several microseconds of front-end work
+        to each kernel's measured time)."""
+        import torch
+
+        graphs = []
+        u0 = 0
+        while u0 < n_units:
+            u1 = min(n_units, u0 + per_graph)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                for u in range(u0, u1):
+                    launch_unit(u)
+            graphs.append(g)
+            u0 = u1
+        return graphs
+
+    def replay_timed(self, graphs):
+        """Replays the graphs back to back; device time (ms) of each graph,
+        from CUDA events recorded on the launching stream between graphs."""
+        import torch
+
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
+        with torch.cuda.stream(self.stream):
+            evs[0].record(self.stream)
+            for i, g in enumerate(graphs):
+                g.replay()
+                evs[i + 1].record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return [evs[i].elapsed_time(evs[i + 1]) for i in range(len(graphs))]
+
+    def time_launches(self, convs, sets, R, ci, launches, per_graph):
+        """One convolution alone: `launches` back-to-back calls over the
+        rotating buffer sets, in graphs of `per_graph` calls, each graph
+        bracketed by events.  Returns (mean ms, median ms) per launch; the
+        median is over the graphs' per-launch means."""
+        import torch
+
+        n_graphs = max(1, -(-launches // per_graph))
+        graphs = self.capture(per_graph, lambda u: self.launch(convs, sets, u % R, ci), per_graph=per_graph)
+        self.replay_timed(graphs)  # settle
+        times = self.replay_timed(graphs * n_graphs)
+        del graphs
+        torch.cuda.synchronize(self.dev)
+        per = [t / per_graph for t in times]
+        return sum(times) / (per_graph * n_graphs), statistics.median(per)
+
+
+def roofline_of(c, mean_ms, hbm_peak, tc_peak):
+    """Roofline position of one convolution's launch: the bound (HBM or the
+    tensor pipe, whichever takes longer at the measured peaks), achieved
+    rates and the fraction of the min(compute, HBM) roofline."""
+    t_hbm = c["bytes"] / (hbm_peak * 1e9)
+    t_tc = c["flops"] / (tc_peak * 1e12)
+    s = mean_ms / 1e3
+    return {"bound": "tensor" if t_tc > t_hbm else "hbm", "GB_s": c["bytes"] / s / 1e9,
+            "TFLOP_s": c["flops"] / s / 1e12, "frac_hbm": c["bytes"] / s / 1e9 / hbm_peak,
+            "frac_roofline": max(t_hbm, t_tc) / s}
+
+
 def run_ours(args, wls, set_name, rank, world):
     import torch
 
-    import depthwise_convolution_forward_gb300 as gc
-    from depthwise_convolution_forward_gb300 import _binding as B
-    from depthwise_convolution_forward_gb300 import build, inputs, roofline
+    from depthwise_convolution_forward_gb300 import build
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     build.build()
-    lib = B.load_library()
     stream = torch.cuda.Stream(dev)
-    sh = stream.cuda_stream
-
-    tile = [int(t) for t in args.tile.split(",")] if args.tile else []
-    convs = []
-    step_bytes = 0
-    step_flops = 0
     bwd = args.op == "bwd_data"
-    for wl in wls:
-        x, w, b = inputs.make_inputs(wl)
-        if bwd:
-            wl = wl.with_(bias=False)
-            b = None
-        p = gc.problem_of(wl)
-        out = gc.grouped_conv_out_shape(p)
-        ysh = (wl.N, out[1], out[2], wl.G, wl.Kg) if wl.ndim == 2 else (wl.N, *out, wl.G, wl.Kg)
-        nbytes = roofline.algorithmic_bytes(wl, out)
-        step_bytes += nbytes
-        step_flops += roofline.flops(wl, out)
-        convs.append(dict(wl=wl, x=x, w=w, b=b, p=p, ysh=ysh, bytes=nbytes, flops=roofline.flops(wl, out),
-                          dt=gc.DTYPE_CODES[wl.dtype],
-                          kernel=gc.grouped_conv_select(p, gc.DTYPE_CODES[wl.dtype]) if not args.force_kernel
-                          else args.force_kernel))
-    per_set = sum(c["bytes"] for c in convs)  # x + y + w + bias of one step
-    R = max(3, -(-2 * L2_BYTES // max(per_set, 1)) + 1)
-    sets = []
-    for r in range(R):
-        s = []
-        for c in convs:
-            wd = c["w"].to(dev)
-            if bwd:  # input dy (forward output layout, U(-1, 1)), output dx (forward input layout)
-                g = torch.Generator().manual_seed(9500 + r)
-                xd = (torch.rand(c["ysh"], generator=g) * 2 - 1).to(c["x"].dtype).to(dev)
-                yd = torch.empty(c["x"].shape, dtype=c["x"].dtype, device=dev)
-                bd = None
-            else:
-                xd = c["x"].to(dev)
-                bd = c["b"].to(dev) if c["b"] is not None else None
-                yd = torch.empty(c["ysh"], dtype=c["x"].dtype, device=dev)
-            s.append((xd, wd, bd, yd))
-        sets.append(s)
-    if bwd:  # one workspace per convolution (stream order keeps consecutive calls apart)
-        for c in convs:
-            c["ws_bytes"] = gc.grouped_conv_bwd_data_workspace_size(c["p"], c["dt"])
-            c["ws"] = torch.empty(max(1, c["ws_bytes"]), dtype=torch.uint8, device=dev)
-    torch.cuda.synchronize(dev)
-
-    opt = B.gconv_options()
-    opt.force_kernel = args.force_kernel
-    opt.serial_launch = 1 if args.serial_launch else 0
-    for i, t in enumerate(tile[:8]):
-        opt.tile[i] = t
-    optp = ctypes.byref(opt)
-
-    def launch(r, ci):
-        c = convs[ci]
-        xd, wd, bd, yd = sets[r][ci]
-        if bwd:
-            st = lib.grouped_conv_bwd_data_ex(xd.data_ptr(), wd.data_ptr(), yd.data_ptr(), ctypes.byref(c["p"]),
-                                              c["dt"], c["ws"].data_ptr() if c["ws_bytes"] else None,
-                                              c["ws_bytes"], sh, optp)
-        else:
-            st = lib.grouped_conv_fwd_ex(xd.data_ptr(), wd.data_ptr(), bd.data_ptr() if bd is not None else None,
-                                         yd.data_ptr(), ctypes.byref(c["p"]), c["dt"], sh, optp)
-        if st != 0:
-            raise RuntimeError(f"grouped_conv launch failed: {gc.gconv_last_error()}")
-        if bwd:
-            c["kernel"] = opt.selected
+    arm = GpuArm(args, dev, stream, bwd)
+    convs, sets, R, per_set = arm.prepare(wls)
+    nl = len(convs)
+    step_bytes = sum(c["bytes"] for c in convs)
+    step_flops = sum(c["flops"] for c in convs)
 
     # warm-up (eager): plans cached, device state initialised
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
-            for ci in range(len(convs)):
-                launch(i % R, ci)
+            for ci in range(nl):
+                arm.launch(convs, sets, i % R, ci)
     stream.synchronize()
 
-    # Graphs of back-to-back launches with external event nodes only every
-    # CH units: an event node between every two launches would add several
-    # microseconds of front-end work to each kernel's measured time.
-    dv = DriverEvents()
-    nl = len(convs)
+    # The K timed steps: graphs of back-to-back steps, events only at the
+    # start and the end of the timed region.
     K = args.steps
-    CH = max(1, min(50, K // 8))
-
-    def capture(n_units, launch_unit, per_graph=1000):
-        bounds = list(range(0, n_units, CH)) + [n_units]
-        events = dv.create(len(bounds))
-        graphs = []
-        u0, ei = 0, 0
-        while u0 < n_units:
-            u1 = min(n_units, u0 + per_graph)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                if u0 == 0:
-                    dv.record_external(events[0], sh)
-                    ei = 1
-                for u in range(u0, u1):
-                    launch_unit(u)
-                    if ei < len(bounds) and u + 1 == bounds[ei]:
-                        dv.record_external(events[ei], sh)
-                        ei += 1
-            graphs.append(g)
-            u0 = u1
-        return graphs, events, bounds
-
-    def replay(graphs):
-        with torch.cuda.stream(stream):
-            for g in graphs:
-                g.replay()
-
-    def chunk_stats(events, bounds):
-        total = dv.elapsed_ms(events[0], events[-1])
-        per_unit = [dv.elapsed_ms(events[i], events[i + 1]) / (bounds[i + 1] - bounds[i])
-                    for i in range(len(bounds) - 1)]
-        return total, per_unit
-
-    def step_unit(k):
-        for ci in range(nl):
-            launch(k % R, ci)
-
-    step_graphs, step_events, step_bounds = capture(K, step_unit)
-    replay(step_graphs[:1])  # one untimed replay to settle
-    stream.synchronize()
+    step_graphs = arm.capture(K, lambda k: [arm.launch(convs, sets, k % R, ci) for ci in range(nl)])
+    arm.replay_timed(step_graphs[:1])  # one untimed replay to settle
 
     dist = None
     if world > 1:
@@ -528,36 +535,29 @@ def run_ours(args, wls, set_name, rank, world):
         dist.barrier()
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter()
-    replay(step_graphs)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for g in step_graphs:
+            g.replay()
+        ev1.record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - t_wall
     if dist:
         dist.barrier()
     clocks = sampler.stop()
-    total_ms, step_ms = chunk_stats(step_events, step_bounds)
+    total_ms = reduce_max(ev0.elapsed_time(ev1), dist, dev)
     del step_graphs
-    dv.destroy(step_events)
-    total_ms = reduce_max(total_ms, dist, dev)
 
-    # Per-kernel device time: each convolution of the step alone, back to
-    # back over the same rotating buffers, timed the same way.
-    M = min(K, 2000)
-    conv_ms = []
-    for ci in range(nl):
-        g_ci, ev_ci, b_ci = capture(M, lambda u, ci=ci: launch(u % R, ci))
-        replay(g_ci[:1])
-        torch.cuda.synchronize(dev)
-        replay(g_ci)
-        torch.cuda.synchronize(dev)
-        tot_ci, per_ci = chunk_stats(ev_ci, b_ci)
-        del g_ci
-        dv.destroy(ev_ci)
-        conv_ms.append((tot_ci / M, statistics.median(per_ci)))
+    # Per-launch device time of each convolution of the step, alone, over a
+    # fixed number of back-to-back launches whatever K is.
+    hbm_peak, tc_peak, peak_kind = load_peaks()
+    M, PG = args.launches, min(250, args.launches)
+    conv_ms = [arm.time_launches(convs, sets, R, ci, M, PG) for ci in range(nl)]
 
-    # per-kernel aggregation over one step (kernel name -> bytes, flops, ms)
     per_kernel = {}
     for ci, c in enumerate(convs):
-        name = gc.KERNEL_NAMES.get(c["kernel"], str(c["kernel"]))
+        name = arm.gc.KERNEL_NAMES.get(c["kernel"], str(c["kernel"]))
         e = per_kernel.setdefault(name, {"bytes": 0, "flops": 0, "ms": 0.0, "launches": 0})
         e["bytes"] += c["bytes"]
         e["flops"] += c["flops"]
@@ -565,9 +565,7 @@ def run_ours(args, wls, set_name, rank, world):
         e["launches"] += 1
     dom = max(per_kernel, key=lambda n: per_kernel[n]["ms"])
     d = per_kernel[dom]
-    hbm_peak, tc_peak, peak_kind = load_peaks()
-    bound = "tensor" if dom == "igemm_tc" and d["flops"] / d["bytes"] > (tc_peak * 1e12) / (hbm_peak * 1e9) \
-        else "hbm"
+    bound = "tensor" if d["flops"] / (tc_peak * 1e12) > d["bytes"] / (hbm_peak * 1e9) else "hbm"
     if bound == "hbm":
         achieved = d["bytes"] / (d["ms"] / 1e3) / 1e9
         peak, unit = hbm_peak, "GB/s"
@@ -580,25 +578,42 @@ def run_ours(args, wls, set_name, rank, world):
             if peak_kind == "measured" else "fallback",
             "algorithmic_bytes_per_launch": d["bytes"] / d["launches"],
             "avg_launch_us": d["ms"] / d["launches"] * 1e3,
-            "timing": f"mean over {M} back-to-back launches per convolution, CUDA events every {CH} launches"}
+            "timing": f"mean over {M} back-to-back launches per convolution (graphs of {PG} launches, CUDA "
+                      f"events on the launching stream between graphs), whatever --steps is"}
 
+    def launch_entry(c, mean, med):
+        e = {"kernel": arm.gc.KERNEL_NAMES.get(c["kernel"]), "median_us": med * 1e3, "mean_us": mean * 1e3,
+             "launches": M, "bytes": c["bytes"], "flops": c["flops"]}
+        e.update(roofline_of(c, mean, hbm_peak, tc_peak))
+        return e
+
+    per_launch = {c["wl"].name: launch_entry(c, *conv_ms[ci]) for ci, c in enumerate(convs)}
     ms_per_step = total_ms / K
     value = whole_job_rate(step_bytes, K, world, total_ms) / 1e9
     tflops = whole_job_rate(step_flops, K, world, total_ms) / 1e12
-    med = statistics.median(step_ms)
-    per_launch = {}
-    for ci, c in enumerate(convs):
-        mean, m = conv_ms[ci]
-        per_launch[c["wl"].name] = {
-            "kernel": gc.KERNEL_NAMES.get(c["kernel"]), "median_us": m * 1e3, "mean_us": mean * 1e3,
-            "GB_s": c["bytes"] / (m / 1e3) / 1e9, "TFLOP_s": c["flops"] / (m / 1e3) / 1e12,
-            "frac_hbm": c["bytes"] / (m / 1e3) / 1e9 / hbm_peak,
-            "frac_roofline": max(c["bytes"] / (hbm_peak * 1e9), c["flops"] / (tc_peak * 1e12)) / (m / 1e3)}
+    med_step = sum(m for _, m in conv_ms)
+
+    # The other workloads of every config, timed the same way one at a time
+    # (outside the timed region; each with its own rotating buffer sets).
+    if args.per_launch != "none":
+        _, more = resolve(args.per_launch)
+        for wl in more:
+            if wl.name in per_launch:
+                continue
+            cs, ss, r_sets, _ = arm.prepare([wl])
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    arm.launch(cs, ss, i % r_sets, 0)
+            stream.synchronize()
+            mean, med = arm.time_launches(cs, ss, r_sets, 0, M, PG)
+            per_launch[wl.name] = launch_entry(cs[0], mean, med)
+            del cs, ss
+            torch.cuda.empty_cache()
 
     # end-to-end: pinned host buffers, copies inside the timed region
     e2e = None
     if not args.no_e2e and not bwd:
-        e2e = run_e2e(args, convs, lib, dev, stream, world, dist, step_bytes, gc)
+        e2e = run_e2e(args, convs, arm.lib, dev, stream, world, dist, step_bytes, arm.gc)
 
     line = {"metric": METRIC.replace("fwd", "bwd_data") if bwd else METRIC, "value": value, "unit": "GB/s",
             "n_gpus": world, "steps": K,
@@ -609,10 +624,10 @@ def run_ours(args, wls, set_name, rank, world):
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "launch": "serial" if args.serial_launch else "programmatic dependent launch",
                        "op": args.op},
-            "tflops": tflops, "median_ms_per_step": med,
-            "value_from_median": step_bytes / (med / 1e3) / 1e9,
-            "per_launch": per_launch, "roofline": roof,
-            "gpu_launches": K * nl, "timed_region_wall_s": wall}
+            "tflops": tflops, "median_ms_per_step": med_step,
+            "value_from_median": step_bytes / (med_step / 1e3) / 1e9,
+            "roofline": roof, "per_launch": per_launch,
+            "gpu_launches": K * sum(c.get("kernels_per_call", 1) for c in convs), "timed_region_wall_s": wall}
     if clocks:
         line["clocks"] = clocks
     if e2e:

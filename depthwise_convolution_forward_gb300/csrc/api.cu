@@ -87,18 +87,28 @@ bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
   return a0 < b0 + (uintptr_t)bbytes && b0 < a0 + (uintptr_t)abytes;
 }
 
-int select_kernel(const Geometry& g, DType dt, const LaunchArgs* a) {
-  if (dw_supported(g, dt, a)) return GCONV_KERNEL_DIRECT_DW;
-  if (tc_supported(g, dt, a)) return GCONV_KERNEL_IGEMM_TC;
+// Shape-based choice: the depthwise kernel, else the tensor-core kernel, else
+// the generic kernel; each specialised kernel is taken only when its planner
+// finds a launch plan for this device (dev; NULL: a GB300's SM count and
+// shared memory, for the host-only query).
+int select_kernel(const Geometry& g, DType dt, const LaunchArgs* a, const DeviceInfo* dev) {
+  const int sms = dev ? dev->num_sms : kDefaultSms;
+  const int smem = dev ? dev->max_smem_optin : kDefaultSmemOptin;
+  if (dw_supported(g, dt, a, sms)) return GCONV_KERNEL_DIRECT_DW;
+  if (tc_supported(g, dt, a, sms, smem)) return GCONV_KERNEL_IGEMM_TC;
   return GCONV_KERNEL_DIRECT_GENERIC;
 }
 
 // ---------------------------------------------------------------------------
 // Per-device cache: SM count, shared-memory limit, status-word address.
 // ---------------------------------------------------------------------------
+// The set-up makes no stream operation and no synchronisation (the status
+// word starts at zero when the module is loaded), so a device's first call
+// may also come inside a stream capture.  A failed set-up is not kept: the
+// next call on that device tries again.
 struct DevSlot {
-  std::once_flag once;
-  cudaError_t err = cudaSuccess;
+  std::mutex mu;
+  std::atomic<bool> ready{false};
   DeviceInfo info{};
   int* status = nullptr;
 };
@@ -111,18 +121,21 @@ cudaError_t device_slot(DevSlot** out) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   DevSlot& s = g_dev[dev];
-  std::call_once(s.once, [&s, dev]() {
-    s.info.device = dev;
-    cudaError_t r = cudaDeviceGetAttribute(&s.info.num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (r == cudaSuccess)
-      r = cudaDeviceGetAttribute(&s.info.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (r == cudaSuccess) r = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.status), g_status_word);
-    if (r == cudaSuccess) r = cudaMemset(s.status, 0, 2 * sizeof(int));
-    if (r == cudaSuccess) r = cudaDeviceSynchronize();
-    s.err = r;
-  });
   *out = &s;
-  return s.err;
+  if (s.ready.load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (s.ready.load(std::memory_order_relaxed)) return cudaSuccess;
+  DeviceInfo info{};
+  info.device = dev;
+  int* status = nullptr;
+  cudaError_t r = cudaDeviceGetAttribute(&info.num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (r == cudaSuccess) r = cudaDeviceGetAttribute(&info.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (r == cudaSuccess) r = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_status_word);
+  if (r != cudaSuccess) return r;
+  s.info = info;
+  s.status = status;
+  s.ready.store(true, std::memory_order_release);
+  return cudaSuccess;
 }
 
 // ---------------------------------------------------------------------------
@@ -167,20 +180,27 @@ LaunchArgs make_args(const void* x, const void* w, const void* bias, void* y, DT
 // (1..3) or the selector's choice; nothing is launched on an error.
 gconv_status launch_forward(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev, int forced,
                             int32_t* selected) {
-  const int kernel = forced ? forced : select_kernel(g, a.dt, &a);
-  if (kernel == GCONV_KERNEL_DIRECT_DW && !dw_supported(g, a.dt, &a))
+  int kernel = forced ? forced : select_kernel(g, a.dt, &a, &dev);
+  if (kernel == GCONV_KERNEL_DIRECT_DW && !dw_supported(g, a.dt, &a, dev.num_sms))
     return fail(GCONV_ERR_UNSUPPORTED, "depthwise kernel cannot run this problem");
-  if (kernel == GCONV_KERNEL_IGEMM_TC && !tc_supported(g, a.dt, &a))
+  if (kernel == GCONV_KERNEL_IGEMM_TC && !tc_supported(g, a.dt, &a, dev.num_sms, dev.max_smem_optin))
     return fail(GCONV_ERR_UNSUPPORTED, "tensor-core kernel cannot run this problem");
   if (kernel < GCONV_KERNEL_DIRECT_DW || kernel > GCONV_KERNEL_IGEMM_TC)
     return fail(GCONV_ERR_UNSUPPORTED, "unknown kernel id %d", kernel);
-  if (selected) *selected = kernel;
   cudaError_t e;
   switch (kernel) {
     case GCONV_KERNEL_DIRECT_DW: e = dw_launch(g, a, dev); break;
     case GCONV_KERNEL_IGEMM_TC: e = tc_launch(g, a, dev); break;
     default: e = generic_launch(g, a, dev); break;
   }
+  // A selector's choice whose launch finds no plan on this device (the
+  // occupancy or shared-memory limits of the device itself) runs on the
+  // generic kernel instead; nothing was launched.
+  if (e == cudaErrorNotSupported && !forced && kernel != GCONV_KERNEL_DIRECT_GENERIC) {
+    kernel = GCONV_KERNEL_DIRECT_GENERIC;
+    e = generic_launch(g, a, dev);
+  }
+  if (selected) *selected = kernel;
   if (e == cudaErrorNotSupported) return fail(GCONV_ERR_UNSUPPORTED, "no launch plan for this problem");
   if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
   return GCONV_OK;
@@ -281,7 +301,7 @@ gconv_status grouped_conv_select(const gconv_problem* p, gconv_dtype dt, int32_t
   if (s != GCONV_OK) return s;
   if (dt != GCONV_F32 && dt != GCONV_F16 && dt != GCONV_BF16) return fail(GCONV_ERR_UNSUPPORTED, "unknown dtype %d", (int)dt);
   if (kernel == nullptr) return fail(GCONV_ERR_INVALID_ARG, "kernel pointer is NULL");
-  *kernel = select_kernel(g, (DType)dt, nullptr);
+  *kernel = select_kernel(g, (DType)dt, nullptr, nullptr);
   return GCONV_OK;
 }
 

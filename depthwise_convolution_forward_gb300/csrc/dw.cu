@@ -1,5 +1,9 @@
 // Ka dispatch: support check and per-dtype launch.
+#include <cstring>
+
+#include "dw_launch.cuh"
 #include "kernels.h"
+#include "plan_cache.h"
 
 namespace gconv {
 
@@ -9,8 +13,10 @@ cudaError_t dw_launch_bf16(const Geometry& g, const LaunchArgs& a, const DeviceI
 
 // Depthwise (Cg == Kg == 1), 3x3 spatial filter, equal H/W stride and
 // dilation in {1, 2}; channels a multiple of one 16-byte vector; x and y
-// 16-byte aligned (TMA and vector-store requirements).  Any depth filter.
-bool dw_supported(const Geometry& g, DType dt, const LaunchArgs* a) {
+// 16-byte aligned (TMA and vector-store requirements).  Any depth filter, as
+// long as the planner finds a tile that fits shared memory for this device's
+// SM count (num_sms).
+bool dw_supported(const Geometry& g, DType dt, const LaunchArgs* a, int num_sms) {
   const int es = dtype_bytes(dt);
   const int vec = 16 / es;
   if (g.Cg != 1 || g.Kg != 1) return false;
@@ -27,7 +33,22 @@ bool dw_supported(const Geometry& g, DType dt, const LaunchArgs* a) {
   if (a) {
     if ((reinterpret_cast<uintptr_t>(a->x) & 15) || (reinterpret_cast<uintptr_t>(a->y) & 15)) return false;
   }
-  return true;
+  struct Key {
+    Geometry g;
+    int tile[8];
+    int es, num_sms;
+  } key;
+  std::memset(&key, 0, sizeof(key));
+  key.g = g;
+  if (a) std::memcpy(key.tile, a->tile, sizeof(key.tile));
+  key.es = es;
+  key.num_sms = num_sms;
+  static PlanCache<int> cache;
+  int ok = 0;
+  if (cache.get(key, &ok)) return ok != 0;
+  ok = dw::plannable(g, es, a ? a->tile : nullptr, num_sms) ? 1 : 0;
+  cache.put(key, ok);
+  return ok != 0;
 }
 
 cudaError_t dw_launch(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev) {

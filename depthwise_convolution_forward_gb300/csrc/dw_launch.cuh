@@ -41,13 +41,13 @@ inline int pick_tc(int C, int vec) {
   return 256 / vec * vec;
 }
 
-inline bool make_plan(const Geometry& g, int es, const int* tile_override, int num_sms, Plan* out) {
+// Row-blocked form for channel tile TC (see make_plan).
+inline bool make_plan_tc(const Geometry& g, int es, const int* tile_override, int num_sms, int TC, Plan* out) {
   const int vec = 16 / es;
   const int direct = (tile_override && tile_override[6] == 2) ? 1 : 0;
   const int S = g.sH, DL = g.dH;
   Plan best{};
   double best_cost = 1e30;
-  const int TC = pick_tc(g.C(), vec);
   const int NV = TC / vec;
   const int Dh = (g.Z - 1) * g.dD + 1;
   for (int WB : {4, 8}) {
@@ -118,6 +118,20 @@ inline bool make_plan(const Geometry& g, int es, const int* tile_override, int n
   }
   *out = best;
   return true;
+}
+
+// Row-blocked (and direct-load) form: the channel tile is the whole pixel or
+// the largest divisor of C up to 256 channels; when even the smallest spatial
+// tile of that channel tile overflows the stage budget (deep filters, wide
+// fp32 channels), narrower channel tiles (divisors of C, multiples of one
+// 16-byte vector) are tried in turn.
+inline bool make_plan(const Geometry& g, int es, const int* tile_override, int num_sms, Plan* out) {
+  const int vec = 16 / es;
+  const int tc0 = pick_tc(g.C(), vec);
+  if (make_plan_tc(g, es, tile_override, num_sms, tc0, out)) return true;
+  for (int tc = tc0 - vec; tc >= vec; tc -= vec)
+    if (g.C() % tc == 0 && make_plan_tc(g, es, tile_override, num_sms, tc, out)) return true;
+  return false;
 }
 
 // Operand form of the column kernel (override slot 5): 1 split 16-bit /
@@ -229,6 +243,20 @@ inline bool make_col_plan(const Geometry& g, int es, const int* ov, int num_sms,
   best.smem_bytes = best.stage_off + best.stages * best.stage_stride;
   *out = best;
   return true;
+}
+
+// Whether some launch plan exists for the depthwise kernel (host only, no
+// GPU): the column form when the depth filter is 1 (planned with the largest
+// register count a thread can have, so the launch, which uses the kernel's
+// real count, finds a plan too), else the row-blocked form.  tile[6] picks the
+// form as in dw_launch_typed.
+inline bool plannable(const Geometry& g, int es, const int* ov, int num_sms) {
+  Plan p;
+  const int kind = ov ? ov[6] : 0;
+  if ((kind == 0 || kind == 3) && g.Z == 1 && make_col_plan(g, es, ov, num_sms, col_form(es, ov), 255, &p))
+    return true;
+  if (kind == 3) return false;
+  return make_plan(g, es, ov, num_sms, &p);
 }
 
 template <typename T>

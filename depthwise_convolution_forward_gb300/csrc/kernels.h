@@ -80,16 +80,25 @@ CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, uint32_t rank,
                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                       const uint32_t* elem_strides, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE);
 
+// SM count and opt-in shared memory per block assumed by the host-only
+// selector (grouped_conv_select, no device at hand): those of a GB300.
+constexpr int kDefaultSms = 152;
+constexpr int kDefaultSmemOptin = 232448;
+
 // ---- Ka: TMA-staged depthwise direct kernel (Cg == Kg == 1) -------------
-// Returns true when the kernel supports this problem (shape, dtype, alignment).
-bool dw_supported(const Geometry& g, DType dt, const LaunchArgs* a);
+// Returns true when the kernel supports this problem (shape, dtype, alignment)
+// and its planner finds a launch plan for a device with num_sms SMs.
+bool dw_supported(const Geometry& g, DType dt, const LaunchArgs* a, int num_sms);
 cudaError_t dw_launch(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
 
 // ---- generic direct kernel (any shape, dtype, alignment) ----------------
 cudaError_t generic_launch(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
 
 // ---- Kb: tcgen05 / TMEM grouped implicit GEMM ----------------------------
-bool tc_supported(const Geometry& g, DType dt, const LaunchArgs* a);
+// Returns true when the kernel supports this problem and its planner finds a
+// launch plan for a device with num_sms SMs and max_smem bytes of opt-in
+// shared memory per block.
+bool tc_supported(const Geometry& g, DType dt, const LaunchArgs* a, int num_sms, int max_smem);
 cudaError_t tc_launch(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
 
 // ---- backward data ---------------------------------------------------------

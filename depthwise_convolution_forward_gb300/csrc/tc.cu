@@ -334,7 +334,7 @@ cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
 
 }  // namespace
 
-bool tc_supported(const Geometry& g, DType dt, const LaunchArgs* a) {
+bool tc_supported(const Geometry& g, DType dt, const LaunchArgs* a, int num_sms, int max_smem) {
   if (dt == kF32) return false;  // fp32 stays on FFMA (no TF32 rounding)
   if (merge_factor(g) == 0) return false;
   if (g.sH != g.sW || g.sH < 1 || g.sH > 2) return false;
@@ -347,17 +347,20 @@ bool tc_supported(const Geometry& g, DType dt, const LaunchArgs* a) {
   struct Key {
     Geometry g;
     int tile[8];
-    int bf16;
+    int bf16, num_sms, max_smem;
   } key;
   std::memset(&key, 0, sizeof(key));
   key.g = g;
   if (a) std::memcpy(key.tile, a->tile, sizeof(key.tile));
   key.bf16 = dt == kBF16;
+  key.num_sms = num_sms;
+  key.max_smem = max_smem;
   static PlanCache<int> cache;
   int ok = 0;
   if (cache.get(key, &ok)) return ok != 0;
   TcPlan p;
-  ok = make_tc_plan(g, dt == kBF16, 148, 227 * 1024, a ? a->tile : nullptr, &p) ? 1 : 0;
+  // the same planner, SM count and shared-memory limit as tc_launch_typed
+  ok = make_tc_plan(g, dt == kBF16, num_sms, max_smem, a ? a->tile : nullptr, &p) ? 1 : 0;
   cache.put(key, ok);
   return ok != 0;
 }

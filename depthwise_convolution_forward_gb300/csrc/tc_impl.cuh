@@ -22,10 +22,14 @@
 //    pitch; the (pitch - TWo) wrap-around rows per output row are computed
 //    and discarded.  Stride 2 uses four polyphase planes loaded with TMA
 //    element strides, so every tap is again a plain shift.
-//  * Warp 1 (one lane) issues tcgen05.mma (M = 128, N = m*Kg, K = 16) into
-//    fp32 accumulators in tensor memory, double-buffered across tiles, and
-//    signals completion with tcgen05.commit on mbarriers.
-//  * Warps 2-5 read the accumulators (tcgen05.ld), apply the fused bias +
+//  * Warps 1-4 (kIssuers warps, one lane each) issue tcgen05.mma (M = 128,
+//    N = m*Kg, K = 16) into fp32 accumulators in tensor memory,
+//    double-buffered across tiles.  The tile's accumulators, and partial
+//    accumulators that each sum a share of the taps, are dealt to the
+//    issuers, so four MMA streams run at once; each issuer signals completion
+//    with tcgen05.commit on mbarriers.
+//  * Warps 5-8 (four epilogue warps, one per TMEM lane quarter) read the
+//    accumulators (tcgen05.ld), add the partials, apply the fused bias +
 //    round-to-nearest-even epilogue and store channels-last output.
 //  * All waits are bounded; on expiry every role reports a timeout, waits
 //    (bounded) for its in-flight copies / MMAs, and the CTA frees its tensor

@@ -26,7 +26,15 @@
  * tensors' dtype, added in fp32 before one round-to-nearest-even cast.
  *
  * Every function is thread-safe.  Device functions are asynchronous on the
- * caller's stream unless stated otherwise.
+ * caller's stream unless stated otherwise.  A device's first call only reads
+ * device attributes and a symbol address (no allocation, copy or
+ * synchronisation), so it may also be made inside a stream capture.
+ *
+ * Status word: each device has one status word that every call on that
+ * device shares, whatever its stream.  A kernel whose bounded wait expires
+ * writes it (the first writer wins); gconv_device_status and debug mode read
+ * and clear it.  With several streams in flight, a timeout it reports may
+ * therefore come from another call on the same device.
  */
 #ifndef GCONV_H_
 #define GCONV_H_
@@ -137,6 +145,9 @@ typedef struct gconv_options {
  * allocates no device memory, keeps no per-call state and copies nothing
  * between host and device.  The launch is asynchronous; buffers must stay
  * valid until the stream reaches it.
+ * Every well-formed problem runs: the selector takes a specialised kernel only
+ * when its planner finds a launch plan on this device, and otherwise (also
+ * when the device's own limits turn a plan down at launch) the generic kernel.
  * Errors: GCONV_ERR_INVALID_ARG for a malformed problem (C or K not divisible
  * by G, non-positive extents, empty output, 2D fields not neutral), NULL
  * x/w/y/p, or y overlapping an input; GCONV_ERR_UNSUPPORTED for an unknown
@@ -216,7 +227,8 @@ gconv_status grouped_conv_out_shape(const gconv_problem *p, int32_t out[3]);
 
 /*
  * grouped_conv_select -- which gconv_kernel grouped_conv_fwd would launch for
- * (p, dt) with 16-byte aligned buffers.  Host only, no GPU needed.
+ * (p, dt) with 16-byte aligned buffers on a GB300 (152 SMs, 227 KB of
+ * shared memory per block).  Host only, no GPU needed.
  */
 gconv_status grouped_conv_select(const gconv_problem *p, gconv_dtype dt, int32_t *kernel);
 

@@ -71,3 +71,57 @@ def test_capture_and_replay(orc):
             ref = orc.forward(c["wl"], xh, c["w"].cpu(), c["b"].cpu())
             assert_close(c["y"].cpu().double().numpy(), ref, c["wl"].dtype, f"replay {rep}: {c['wl'].name}")
         assert_close(dx.cpu().double().numpy(), orc.bwd_data(bw, dyh, wb), bw.dtype, f"replay {rep}: bwd data")
+
+
+FIRST_CALL_SCRIPT = r"""
+import sys
+sys.path.insert(0, {root!r})
+sys.path.insert(0, {tests!r})
+import numpy as np
+import torch
+import depthwise_convolution_forward_gb300 as gc
+from depthwise_convolution_forward_gb300 import inputs
+import oracle
+from gpu_util import out_shape_of, TOL
+dev = torch.device("cuda:0")
+torch.zeros(1, device=dev)
+cases = []
+for name in ("mbv2_dw_s2_f16", "resnext_b_bf16", "grouped2d_f32_smoke"):
+    wl = inputs.by_name(name).with_(N=1)
+    x, w, b = inputs.make_inputs(wl)
+    cases.append((wl, x, w, b, x.to(dev), w.to(dev), b.to(dev) if b is not None else None,
+                  torch.full(out_shape_of(wl), float("nan"), dtype=x.dtype, device=dev)))
+s = torch.cuda.Stream(dev)
+s.wait_stream(torch.cuda.current_stream(dev))
+torch.cuda.synchronize(dev)
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=s):  # the library's first calls in this process
+    for wl, _, _, _, xd, wd, bd, yd in cases:
+        gc.grouped_conv_fwd(xd, wd, bd, yd, gc.problem_of(wl), gc.DTYPE_CODES[wl.dtype], s)
+g.replay()
+torch.cuda.synchronize(dev)
+orc = oracle.get()
+for wl, x, w, b, _, _, _, yd in cases:
+    ref = orc.forward(wl, x, w, b)
+    got = yd.cpu().double().numpy()
+    atol, rtol = TOL[wl.dtype]
+    ok = np.all(np.isfinite(got)) and np.all(np.abs(got - ref) <= atol + rtol * np.abs(ref))
+    print(wl.name, "ok" if ok else "MISMATCH")
+"""
+
+
+def test_first_call_inside_capture():
+    """A fresh process whose first library calls are made inside a stream
+    capture (torch.cuda.graph, global capture mode): the per-device set-up
+    does nothing that a capture forbids, and the replayed graph computes the
+    right outputs on the depthwise, tensor-core and generic kernels."""
+    import os
+    import subprocess
+    import sys
+
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = FIRST_CALL_SCRIPT.format(root=os.path.dirname(here), tests=here)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.endswith(("ok", "MISMATCH"))]
+    assert len(lines) == 3 and all(ln.endswith(" ok") for ln in lines), r.stdout

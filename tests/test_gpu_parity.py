@@ -160,6 +160,22 @@ def test_depthwise_3d(orc):
     assert_close(y.double().numpy(), orc.forward(wl, x, w, b), "f16", "dw3d")
 
 
+@pytest.mark.parametrize("wl", [
+    # the smallest whole-pixel tile of these overflows a stage, so the planner
+    # narrows the channel tile (fp32 C=256 3x3x3; fp16 C=256, depth 5 dilated 2)
+    inputs.Workload("dw3d_f32_c256", 7, 2, 3, 2, 256, 1, 1, (8, 14, 14), (3, 3, 3), (1, 1, 1), (1, 1, 1),
+                    (1, 1, 1), "f32", True),
+    inputs.Workload("dw3d_f16_c256_z5", 7, 3, 3, 1, 256, 1, 1, (12, 10, 10), (5, 3, 3), (1, 1, 1), (4, 1, 1),
+                    (2, 1, 1), "f16", True),
+], ids=lambda w: w.name)
+def test_depthwise_3d_channel_tiles(orc, wl):
+    x, w, b = inputs.make_inputs(wl)
+    assert gc.grouped_conv_select(gc.problem_of(wl), gc.DTYPE_CODES[wl.dtype]) == B.KERNEL_DIRECT_DW
+    y, sel = run_gpu(wl, x, w, b)
+    assert sel == B.KERNEL_DIRECT_DW
+    assert_close(y.double().numpy(), orc.forward(wl, x, w, b), wl.dtype, wl.name)
+
+
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 def test_integer_inputs_bit_exact(orc, dt):
     """Small integers: every product and partial sum is exact in fp32 and the

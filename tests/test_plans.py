@@ -38,7 +38,7 @@ def harness(tmp_path_factory):
         pytest.skip("nvcc not available")
     out = tmp_path_factory.mktemp("plans")
     exes = {}
-    for name in ("plan_tc", "plan_dw"):
+    for name in ("plan_tc", "plan_dw", "plan_select"):
         exe = str(out / name)
         subprocess.run([nvcc, "-std=c++17", "-O1", "-gencode", "arch=compute_103a,code=sm_103a",
                         "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include"),
@@ -230,3 +230,38 @@ def test_tensor_core_overridden_plans(harness, name):
         elif np_ <= wl.taps and 2 * np_ * G2_per_nmt * nmt * auto["Nn"] <= 512 and nmt <= 2 and st == 0:
             # small tiles that fit tensor memory must be plannable
             raise AssertionError(f"{name}: no plan for nmt {nmt} np {np_}")
+
+
+def _select_candidates():
+    """Every workload family, random grouped problems in all dtypes, and the
+    deep depthwise 3D filters whose smallest whole-pixel tile overflows a
+    stage (fp32 C=256 3x3x3; fp16 C=256 depth 5 dilated 2)."""
+    probs = [wl for wl in inputs.all_workloads()]
+    probs += [inputs.Workload("dw3d_f32_c256", 0, 0, 3, 2, 256, 1, 1, (8, 28, 28), (3, 3, 3), (1, 1, 1),
+                              (1, 1, 1), (1, 1, 1), "f32", True),
+              inputs.Workload("dw3d_f16_c256_z5", 0, 0, 3, 2, 256, 1, 1, (12, 28, 28), (5, 3, 3), (1, 1, 1),
+                              (4, 1, 1), (2, 1, 1), "f16", True)]
+    probs += _dw_candidates()[:120]
+    probs += _tc_candidates()[:200]
+    return [wl for wl in probs if min(_geom(wl)[0]) >= 1]
+
+
+@pytest.mark.parametrize("sms", [132, 148, 152, 160])
+def test_selector_agrees_with_launch_planners(harness, sms):
+    """The selector takes a specialised kernel only when that kernel's
+    launcher finds a plan on a device with the same SM count and shared
+    memory, so an auto-selected problem never fails for want of a plan."""
+    probs = _select_candidates()
+    code = {"f32": 0, "f16": 1, "bf16": 2}
+    lines = [" ".join(map(str, _geom(wl)[1] + [code[wl.dtype], sms, SMEM_BLOCK, 96])) for wl in probs]
+    res = _run(harness["plan_select"], lines)
+    assert len(res) == len(probs)
+    for wl, r in zip(probs, res):
+        if r["dw_sel"]:
+            assert r["dw_plan"], (wl, r)
+        assert bool(r["tc_sel"]) == bool(r["tc_plan"]), (wl, r)
+    by_name = {wl.name: r for wl, r in zip(probs, res)}
+    # the deep 3D depthwise filters are planned with narrower channel tiles
+    for name in ("dw3d_f32_c256", "dw3d_f16_c256_z5"):
+        assert by_name[name]["dw_sel"] and by_name[name]["dw_plan"], by_name[name]
+        assert by_name[name]["dw_TC"] < 256, by_name[name]
