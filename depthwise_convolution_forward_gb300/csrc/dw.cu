@@ -10,6 +10,9 @@ namespace gconv {
 cudaError_t dw_launch_f32(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
 cudaError_t dw_launch_f16(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
 cudaError_t dw_launch_bf16(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
+int dw_col_regs_f32(int S, int DL, int form);
+int dw_col_regs_f16(int S, int DL, int form);
+int dw_col_regs_bf16(int S, int DL, int form);
 
 // Depthwise (Cg == Kg == 1), 3x3 spatial filter, equal H/W stride and
 // dilation in {1, 2}; channels a multiple of one 16-byte vector; x and y
@@ -36,17 +39,28 @@ bool dw_supported(const Geometry& g, DType dt, const LaunchArgs* a, int num_sms)
   struct Key {
     Geometry g;
     int tile[8];
-    int es, num_sms;
+    int es, num_sms, with_device;
   } key;
   std::memset(&key, 0, sizeof(key));
   key.g = g;
   if (a) std::memcpy(key.tile, a->tile, sizeof(key.tile));
   key.es = es;
+  key.with_device = a != nullptr;
   key.num_sms = num_sms;
   static PlanCache<int> cache;
   int ok = 0;
   if (cache.get(key, &ok)) return ok != 0;
-  ok = dw::plannable(g, es, a ? a->tile : nullptr, num_sms) ? 1 : 0;
+  // With launch arguments a device is at hand: plan with the column kernel's
+  // real register count, as the launch does (tile overrides may need it);
+  // the host-only query plans with the most it can have.
+  const int form = dw::col_form(es, a ? a->tile : nullptr);
+  int regs = dw::col_max_regs(form);
+  if (a && g.Z == 1) {
+    const int r = dt == kF32 ? dw_col_regs_f32(g.sH, g.dH, form)
+                             : (dt == kF16 ? dw_col_regs_f16(g.sH, g.dH, form) : dw_col_regs_bf16(g.sH, g.dH, form));
+    if (r > 0) regs = r;
+  }
+  ok = dw::plannable(g, es, a ? a->tile : nullptr, num_sms, regs) ? 1 : 0;
   cache.put(key, ok);
   return ok != 0;
 }

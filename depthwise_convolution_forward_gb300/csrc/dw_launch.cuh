@@ -245,16 +245,21 @@ inline bool make_col_plan(const Geometry& g, int es, const int* ov, int num_sms,
   return true;
 }
 
-// Whether some launch plan exists for the depthwise kernel (host only, no
-// GPU): the column form when the depth filter is 1 (planned with the largest
-// register count a thread can have, so the launch, which uses the kernel's
-// real count, finds a plan too), else the row-blocked form.  tile[6] picks the
-// form as in dw_launch_typed.
-inline bool plannable(const Geometry& g, int es, const int* ov, int num_sms) {
+// Most registers a thread of the column kernel can have: its launch bound
+// leaves at most 65536 / max threads, in steps of 8.
+inline int col_max_regs(int form) { return 65536 / col_max_threads(form) / 8 * 8; }
+
+// Whether some launch plan exists for the depthwise kernel (host only): the
+// column form when the depth filter is 1, else the row-blocked form.  The
+// column form is planned with `regs` registers per thread: the kernel's own
+// count when the caller knows it, else col_max_regs (a plan found with that
+// many is found with fewer too).  tile[6] picks the form as in
+// dw_launch_typed.
+inline bool plannable(const Geometry& g, int es, const int* ov, int num_sms, int regs) {
   Plan p;
   const int kind = ov ? ov[6] : 0;
-  if ((kind == 0 || kind == 3) && g.Z == 1 && make_col_plan(g, es, ov, num_sms, col_form(es, ov), 255, &p))
-    return true;
+  const int form = col_form(es, ov);
+  if ((kind == 0 || kind == 3) && g.Z == 1 && make_col_plan(g, es, ov, num_sms, form, regs, &p)) return true;
   if (kind == 3) return false;
   return make_plan(g, es, ov, num_sms, &p);
 }
@@ -334,6 +339,16 @@ DwLdgKernel<T> pick_ldg_kernel(int S, int DL, int WB, int mode) {
   GCONV_DW_CASE(2, 2, 8)
 #undef GCONV_DW_CASE
   return nullptr;
+}
+
+// Registers per thread of the column kernel for (stride, dilation, operand
+// form), or -1 when there is no such kernel or the query fails.
+template <typename T>
+int col_kernel_regs(int S, int DL, int form) {
+  DwKernel<T> k = pick_col_kernel<T>(S, DL, form);
+  cudaFuncAttributes fa{};
+  if (k == nullptr || cudaFuncGetAttributes(&fa, k) != cudaSuccess) return -1;
+  return fa.numRegs;
 }
 
 template <typename T>

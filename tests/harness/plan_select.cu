@@ -16,6 +16,9 @@ CUresult encode_tiled(CUtensorMap*, CUtensorMapDataType, uint32_t, const void*, 
 cudaError_t dw_launch_f32(const Geometry&, const LaunchArgs&, const DeviceInfo&) { return cudaErrorNotSupported; }
 cudaError_t dw_launch_f16(const Geometry&, const LaunchArgs&, const DeviceInfo&) { return cudaErrorNotSupported; }
 cudaError_t dw_launch_bf16(const Geometry&, const LaunchArgs&, const DeviceInfo&) { return cudaErrorNotSupported; }
+int dw_col_regs_f32(int, int, int) { return -1; }
+int dw_col_regs_f16(int, int, int) { return -1; }
+int dw_col_regs_bf16(int, int, int) { return -1; }
 }  // namespace gconv
 
 using namespace gconv;
