@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     gconv_status_string,
     grouped_conv_bwd_data,
     grouped_conv_bwd_data_ex,
+    grouped_conv_bwd_data_noalloc,
     grouped_conv_bwd_data_workspace_size,
     grouped_conv_fwd,
     grouped_conv_fwd_ex,

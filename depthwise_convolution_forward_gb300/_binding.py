@@ -79,6 +79,8 @@ def load_library(path: Optional[str] = None):
         lib.grouped_conv_bwd_data_ex.restype = i32
         lib.grouped_conv_bwd_data_ex.argtypes = [vp, vp, vp, prob_p, i32, vp, i64, vp,
                                                  ctypes.POINTER(gconv_options)]
+        lib.grouped_conv_bwd_data_noalloc.restype = i32
+        lib.grouped_conv_bwd_data_noalloc.argtypes = [vp, vp, vp, prob_p, i32, vp]
         lib.grouped_conv_bwd_data_workspace_size.restype = i32
         lib.grouped_conv_bwd_data_workspace_size.argtypes = [prob_p, i32, ctypes.POINTER(i64)]
         lib.grouped_conv_out_shape.restype = i32
@@ -210,3 +212,14 @@ def grouped_conv_bwd_data_ex(dy, w, dx, p: gconv_problem, dtype: int, workspace=
     _check(lib.grouped_conv_bwd_data_ex(_ptr(dy), _ptr(w), _ptr(dx), ctypes.byref(p), dtype, _ptr(workspace),
                                         workspace_bytes, _stream(stream), ctypes.byref(o)))
     return o
+
+
+GCONV_NOALLOC_SCRATCH_BYTES = 1 << 20  # include/gconv.h
+
+
+def grouped_conv_bwd_data_noalloc(dy, w, dx, p: gconv_problem, dtype: int, stream=None) -> None:
+    """Backward data without a caller workspace: the library's fixed scratch
+    array (GCONV_NOALLOC_SCRATCH_BYTES) stands in for it; see gconv.h."""
+    lib = load_library()
+    _check(lib.grouped_conv_bwd_data_noalloc(_ptr(dy), _ptr(w), _ptr(dx), ctypes.byref(p), dtype,
+                                             _stream(stream)))

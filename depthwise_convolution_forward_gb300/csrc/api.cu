@@ -250,6 +250,14 @@ int64_t bwd_workspace_bytes(const Geometry& g, DType dt) {
 
 }  // namespace
 
+gconv_status set_last_error(gconv_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
 CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType type, uint32_t rank, const void* base,
                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                       const uint32_t* elem_strides, CUtensorMapSwizzle swizzle) {

@@ -8,6 +8,8 @@
 
 #include <utility>
 
+#include "../../include/gconv.h"
+
 namespace gconv {
 
 enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
@@ -110,6 +112,10 @@ cudaError_t bwd_data_direct_launch(const Geometry& g, const LaunchArgs& a, const
 // ---- Kc alone (epilogue test entry) --------------------------------------
 cudaError_t epilogue_launch(const float* acc, const void* bias, void* y, int64_t rows, int cols,
                             DType dt, cudaStream_t stream);
+
+// Records a formatted reason as the calling thread's gconv_last_error() and
+// returns s (for entry points outside api.cu).
+gconv_status set_last_error(gconv_status s, const char* fmt, ...);
 
 // Status codes written into the device status word.
 enum DevStatus : int { kDevOk = 0, kDevTimeout = 1 };

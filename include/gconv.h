@@ -219,6 +219,35 @@ gconv_status grouped_conv_bwd_data_ex(const void *dy, const void *w, void *dx, c
 gconv_status grouped_conv_bwd_data_workspace_size(const gconv_problem *p, gconv_dtype dt, int64_t *bytes);
 
 /*
+ * grouped_conv_bwd_data_noalloc -- grouped_conv_bwd_data for callers that
+ * cannot allocate device memory, nor have it allocated for them, while they
+ * run: for example a plugin enqueued on a stream an inference engine owns, or
+ * a runtime that reserves all of its memory at start-up and forbids
+ * allocation (and the synchronisation an allocation can cause) later.  The
+ * pages have no counterpart: this is a library convenience, not a step of the
+ * method.
+ * Same operation, arguments (minus the workspace), layouts, ownership and
+ * errors as grouped_conv_bwd_data.  The scratch that call takes from the
+ * caller (the transposed, flipped weights of its stride-1 route) comes here
+ * from a fixed array of GCONV_NOALLOC_SCRATCH_BYTES bytes in the library's
+ * own static device memory, which every GPU that loads the library holds
+ * until the process exits.  Nothing is allocated and nothing is freed.
+ *   - A problem whose scratch would exceed GCONV_NOALLOC_SCRATCH_BYTES
+ *     returns GCONV_ERR_UNSUPPORTED without launching anything
+ *     (grouped_conv_bwd_data_workspace_size gives the size it needs).
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - Every call shares the one array and leaves its contents behind; each
+ *     call rewrites every byte it reads, so no clearing is needed.  Calls
+ *     whose work overlaps on the GPU (other streams, unordered host threads)
+ *     race on it: keep them ordered, e.g. on one stream.
+ */
+#define GCONV_NOALLOC_SCRATCH_BYTES (1 << 20)
+gconv_status grouped_conv_bwd_data_noalloc(const void *dy, const void *w, void *dx, const gconv_problem *p,
+                                           gconv_dtype dt, struct CUstream_st *stream);
+
+/*
  * grouped_conv_out_shape -- output extents {Do, Ho, Wo} of problem p
  * (Do = 1 for 2D), by O = floor((I + 2p - d*(k-1) - 1)/s) + 1.  Host only,
  * no GPU needed.  GCONV_ERR_INVALID_ARG for a malformed or empty problem.
