@@ -57,6 +57,21 @@ enum ColForm : int { kColSplit = 0, kColPacked = 1, kColWide = 2, kColPacked8 = 
 // 8-channel form, whose threads hold twice the weights and accumulators).
 __host__ __device__ constexpr int col_max_threads(int form) { return form == kColPacked8 ? 416 : 544; }
 
+// Registers per thread the compiler may use (a cap, not a launch bound: the
+// planner reads the kernel's real count).  Every form fits its
+// col_max_threads at its cap.  The default 16-bit form keeps 72 when three
+// output rows are live (stride 1 or 2 at dilation 1, stride 2 at dilation 2),
+// so three CTAs of nine warps fit an SM when shared memory allows; five live
+// rows (stride 1, dilation 2) take 88.  The other forms and fp32 hold more
+// per thread (wider weights or operands) and get 96 to 152.
+template <typename T, int S, int DL>
+__host__ __device__ constexpr int col_reg_cap(int form) {
+  return form == kColPacked8                                       ? 152
+         : (form != kColPacked || sizeof(T) == 4) ? ((2 * DL) / S + 1 > 3 ? 112 : 96)
+         : ((2 * DL) / S + 1 > 3)                                  ? 88
+                                                                   : 72;
+}
+
 __device__ __forceinline__ void lds64(uint32_t addr, uint32_t (&v)[2]) {
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(addr));
 }
@@ -257,6 +272,35 @@ __device__ __forceinline__ void col_store(T* dst, const float (&acc)[CPT]) {
   }
 }
 
+// The same, stored only where `pred` holds.
+template <typename T, int CPT>
+__device__ __forceinline__ void col_store_if(T* dst, const float (&acc)[CPT], bool pred) {
+  uint32_t wd[4];
+  if constexpr (std::is_same<T, float>::value) {
+    static_assert(CPT == 4, "fp32 stores 4 channels");
+#pragma unroll
+    for (int i = 0; i < 4; ++i) wd[i] = __float_as_uint(acc[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < CPT / 2; ++i) {
+      if constexpr (std::is_same<T, __half>::value) {
+        const __half2 h = __floats2half2_rn(acc[2 * i], acc[2 * i + 1]);
+        wd[i] = *reinterpret_cast<const uint32_t*>(&h);
+      } else {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        wd[i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+    }
+  }
+  // the conversion runs unconditionally and only the store is guarded, so
+  // the guard compiles to a predicated store rather than a branch
+  if constexpr (std::is_same<T, float>::value || CPT == 8) {
+    if (pred) *reinterpret_cast<uint4*>(dst) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+  } else {
+    if (pred) *reinterpret_cast<uint2*>(dst) = make_uint2(wd[0], wd[1]);
+  }
+}
+
 // Per-stage tile header, written by the producer before it arms the stage's
 // barrier: the output element index of the tile origin (n, od, oh0, ow0, c0)
 // and the tile's first output row, rows, first column and first channel.
@@ -307,7 +351,7 @@ __host__ __device__ constexpr bool col_row_used(int u) {
 // the row walk needs no bounds tests.
 template <typename T, int FORM, int S, int DL, int NA, int U_, int KY>
 __device__ __forceinline__ void col_tap_row(ColState<T, FORM, NA>& c, const typename ColOps<T, FORM>::Op (&xv)[3][ColOps<T, FORM>::kOps],
-                                            int oh_base, T* yb) {
+                                            int oh_base, T* const (&yp)[NA]) {
   using Ops = ColOps<T, FORM>;
   if constexpr (col_hits<S, DL>(U_, KY)) {
     constexpr int rel = (U_ - KY * DL) / S;  // output row - oh_base (exact)
@@ -320,9 +364,9 @@ __device__ __forceinline__ void col_tap_row(ColState<T, FORM, NA>& c, const type
     Ops::mac(c.acc[slot], xv[1], c.wr[KY][1], c.acc[slot]);
     Ops::mac(c.acc[slot], xv[2], c.wr[KY][2], c.acc[slot]);
     if constexpr (KY == 2) {
-      const int oh_l = oh_base + rel;
-      if (c.store_ok && (unsigned)oh_l < (unsigned)c.nrows)
-        col_store<T, Ops::kCpt>(yb + rel * c.y_row_step, c.acc[slot]);
+      static_assert(rel <= 0 && rel > -NA, "a finished output row lies in this block's window");
+      const bool ok = c.store_ok & ((unsigned)(oh_base + rel) < (unsigned)c.nrows);
+      col_store_if<T, Ops::kCpt>(yp[-rel], c.acc[slot], ok);
     }
   }
 }
@@ -331,7 +375,7 @@ __device__ __forceinline__ void col_tap_row(ColState<T, FORM, NA>& c, const type
 // the filter rows it sits under.  Returns false (and does nothing) past the
 // last halo row when CHECK is set.
 template <typename T, int FORM, int S, int DL, int NA, bool CHECK, int U_>
-__device__ __forceinline__ bool col_row(ColState<T, FORM, NA>& c, int r0, int Hh, int oh_base, T* yb) {
+__device__ __forceinline__ bool col_row(ColState<T, FORM, NA>& c, int r0, int Hh, int oh_base, T* const (&yp)[NA]) {
   using Ops = ColOps<T, FORM>;
   if constexpr (!col_row_used<S, DL>(U_)) {
     return true;
@@ -342,9 +386,9 @@ __device__ __forceinline__ bool col_row(ColState<T, FORM, NA>& c, int r0, int Hh
     Ops::load_x(rb, xv[0]);
     Ops::load_x(rb + c.col_step, xv[1]);
     Ops::load_x(rb + 2 * c.col_step, xv[2]);
-    col_tap_row<T, FORM, S, DL, NA, U_, 0>(c, xv, oh_base, yb);
-    col_tap_row<T, FORM, S, DL, NA, U_, 1>(c, xv, oh_base, yb);
-    col_tap_row<T, FORM, S, DL, NA, U_, 2>(c, xv, oh_base, yb);
+    col_tap_row<T, FORM, S, DL, NA, U_, 0>(c, xv, oh_base, yp);
+    col_tap_row<T, FORM, S, DL, NA, U_, 1>(c, xv, oh_base, yp);
+    col_tap_row<T, FORM, S, DL, NA, U_, 2>(c, xv, oh_base, yp);
     return true;
   }
 }
@@ -353,15 +397,22 @@ __device__ __forceinline__ bool col_row(ColState<T, FORM, NA>& c, int r0, int Hh
 // starts at an output row that is a multiple of NA and the accumulator slot
 // of each (row, filter row) pair is the same in every block).  Expanded at
 // compile time over the U rows.
+// yb points at output row oh_base of the thread's column; the rows a block
+// finishes are oh_base - NA + 1 .. oh_base, whose addresses are formed once
+// per block.
 template <typename T, int FORM, int S, int DL, int NA, bool CHECK, int... Us>
 __device__ __forceinline__ void col_block(ColState<T, FORM, NA>& c, int r0, int Hh, T* yb,
                                           std::integer_sequence<int, Us...>) {
   const int oh_base = r0 / S;
-  (void)(col_row<T, FORM, S, DL, NA, CHECK, Us>(c, r0, Hh, oh_base, yb) && ...);
+  T* yp[NA];
+  yp[0] = yb;
+#pragma unroll
+  for (int i = 1; i < NA; ++i) yp[i] = yp[i - 1] - c.y_row_step;
+  (void)(col_row<T, FORM, S, DL, NA, CHECK, Us>(c, r0, Hh, oh_base, yp) && ...);
 }
 
 template <typename T, int S, int DL, int FORM>
-__global__ void __launch_bounds__(col_max_threads(FORM)) dw_col_kernel(const __grid_constant__ CUtensorMap xmap,
+__global__ void __maxnreg__((col_reg_cap<T, S, DL>(FORM))) dw_col_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                   const __grid_constant__ CUtensorMap xmap0,
                                                                   const __grid_constant__ CUtensorMap xmap1,
                                                                   const DwArgs a) {
