@@ -196,18 +196,27 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
       }
       c.ntab = (int)entries;
     }
+    // Epilogue: stores straight from registers by default.  On request
+    // (override 7 < 0) the tile's output box is staged in shared memory and
+    // written with TMA tensor stores, one per channel slice of W bytes per
+    // pixel (the CTA's sc * Nn channels, at most 128 bytes per slice), when
+    // the staging fits beside two input stages.  The TMA-store epilogue
+    // measured no faster on GB300 (within -5..+2% on the tensor-core
+    // workloads): the scattered 32-byte stores are not what bounds a tile.
+    const uint32_t chan_bytes = (uint32_t)(c.sc * c.Nn) * 2u;
+    c.epi_w = (int)std::min<uint32_t>(128u, chan_bytes);
+    c.epi_slices = (int)(chan_bytes / (uint32_t)c.epi_w);
+    c.epi_slice_bytes = round_up((uint32_t)(c.TH * c.TWo) * (uint32_t)c.epi_w, 1024);
+    const uint32_t epi_bytes = (uint32_t)c.epi_slices * c.epi_slice_bytes;
+    const bool want_epi = ov && ov[7] < 0;
     int stages = (ov && ov[3]) ? ov[3] : tc::kMaxStages;
     stages = std::min(stages, tc::kMaxStages);
-    while (stages > 2 && c.a_off + stages * c.a_stage_bytes > budget) --stages;
-    if (c.a_off + stages * c.a_stage_bytes > budget) continue;
+    auto a_end_of = [&](int st) { return c.a_off + (uint32_t)st * c.a_stage_bytes; };
+    bool epi = want_epi && a_end_of(2) + epi_bytes <= budget;
+    while (stages > 2 && a_end_of(stages) + (epi ? epi_bytes : 0u) > budget) --stages;
+    if (a_end_of(stages) > budget) continue;
     c.stages = stages;
-    // Epilogue through shared-memory staging (coalesced 128-byte stores), on
-    // request (override 7 < 0) when 16 KB are left.  Measured slower than
-    // storing from registers on GB300 (the staged path spills at the
-    // 168-register cap of 9 warps per CTA), so it is off by default.
-    c.epi_off = 0;
-    const uint32_t a_end = c.a_off + stages * c.a_stage_bytes;
-    if (a_end + 16384u <= budget && ov && ov[7] < 0) c.epi_off = a_end;
+    c.epi_off = epi ? a_end_of(stages) : 0u;
     uint32_t cols = 32;
     while (cols < (uint32_t)(2 * np * G2 * c.Nn)) cols <<= 1;
     if (cols > 512) continue;
@@ -220,7 +229,7 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     TcPlan p;
     p.a = c;
     p.sw = sw;
-    p.smem_bytes = c.a_off + stages * c.a_stage_bytes + (c.epi_off ? 16384u : 0u);
+    p.smem_bytes = c.a_off + stages * c.a_stage_bytes + (c.epi_off ? epi_bytes : 0u);
     // Keep a second CTA off the SM when both could not hold their tensor
     // memory at once (its allocation would wait for the first CTA to exit).
     if (cols > 256) p.smem_bytes = std::max<uint32_t>(p.smem_bytes, 117 * 1024);
@@ -245,7 +254,7 @@ bool make_tc_plan(const Geometry& g, bool bf16, int num_sms, int max_smem, const
 }
 
 template <typename T>
-using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const TcArgs);
+using TcKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const TcArgs);
 
 template <typename T>
 TcKernel<T> pick_tc_kernel(const TcPlan& p) {
@@ -319,6 +328,21 @@ cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
     uint32_t westr[3] = {1u, 1u, 1u};
     if (encode_tiled(&wmap, tt, 3, la.w, wdims, wstrides, wbox, westr) == CUDA_SUCCESS) w_tma = 1;
   }
+  // Output viewed as (K, Wo, Ho, Do, N) for the staged epilogue's TMA
+  // stores: a box of one channel slice x TWo x TH of the tile.
+  CUtensorMap ymap = map;
+  if (p.a.epi_off != 0) {
+    uint64_t ydims[5] = {(uint64_t)g.K(), (uint64_t)g.Wo, (uint64_t)g.Ho, (uint64_t)g.Do, (uint64_t)g.N};
+    const uint64_t K = g.K();
+    uint64_t ystrides[4] = {K * es, K * es * g.Wo, K * es * g.Wo * g.Ho, K * es * g.Wo * g.Ho * g.Do};
+    uint32_t ybox[5] = {(uint32_t)(p.a.epi_w / es), (uint32_t)p.a.TWo, (uint32_t)p.a.TH, 1u, 1u};
+    uint32_t yestr[5] = {1u, 1u, 1u, 1u, 1u};
+    const CUtensorMapSwizzle ysw = p.a.epi_w == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : p.a.epi_w == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                      : CU_TENSOR_MAP_SWIZZLE_32B;
+    if (encode_tiled(&ymap, tt, 5, la.y, ydims, ystrides, ybox, yestr, ysw) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   TcArgs a = p.a;
   a.w_tma = w_tma;
   a.w_box_taps = box_taps;
@@ -329,7 +353,7 @@ cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   a.wait_limit_ns = la.wait_limit_ns;
   a.test_flags = la.test_flags;
   const TcKernel<T> kern = pick_tc_kernel<T>(p);
-  return launch_kernel(kern, dim3(p.grid), dim3(tc::kThreads), p.smem_bytes, la, map, wmap, a);
+  return launch_kernel(kern, dim3(p.grid), dim3(tc::kThreads), p.smem_bytes, la, map, wmap, ymap, a);
 }
 
 }  // namespace

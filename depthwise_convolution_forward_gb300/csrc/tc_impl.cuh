@@ -66,7 +66,9 @@ struct TcArgs {
   int np;                  // partial accumulators per accumulator (taps split np ways)
   uint32_t plane_stride, a_stage_bytes, tx_bytes;
   uint32_t a_off, b_off, bias_off, tab_off;  // smem offsets (tab: MMA descriptor table)
-  uint32_t epi_off;  // epilogue staging (4 x 4 KB), or 0 to store straight from registers
+  uint32_t epi_off;  // output-box staging for TMA tensor stores, or 0 to store straight from registers
+  uint32_t epi_slice_bytes;  // staging bytes of one channel slice (1024-aligned)
+  int epi_w, epi_slices;     // bytes per pixel of a slice (128, 64 or 32) and slices per CTA row
   int w_tma;         // 1: weights staged by TMA through the weight tensor map (Cg, Kg % 8 == 0)
   int w_box_taps;    // taps one weight box covers: all of them (one group per chunk) or 1
   int stages;
@@ -170,91 +172,64 @@ __device__ __forceinline__ void epilogue_row(uint32_t lane_base, int mt, int G2,
   }
 }
 
-// Epilogue for one 128-row slab of a tile through a per-warp shared-memory
-// staging buffer (32 rows x 128 bytes, 16-byte units XOR-swizzled by row).
-// Each group of 4 chunks (64 channels) is written row by row (lane = pixel
-// row), then read back transposed: in each of 4 rounds, 4 lanes cover the
-// 4 chunks of one pixel and a warp store instruction writes 8 whole 128-byte
-// pixel segments instead of 32 scattered 32-byte pieces.
+// Epilogue into the shared-memory image of the tile's output box, for a
+// TMA tensor store.  The box is [TH][TWo][slice of the CTA's channels] per
+// channel slice of W bytes per pixel (W = 128, 64 or 32), each slice with the
+// TMA swizzle of its width: the 16-byte chunk c of pixel p sits at chunk
+// c ^ (bits 7.. of p * W), so the 8 consecutive pixels one warp quarter
+// writes land in 8 different bank groups.  Lane = one pixel row of the
+// accumulator (f = mt * 128 + row); wrap-around rows (jj >= TWo) and rows
+// past the tile (i >= TH) are not part of the box and are skipped.
 template <typename T, int NP>
-__device__ __forceinline__ void epilogue_row_staged(uint32_t lane_base, int mt, int G2, int sc, int Nn, bool valid,
-                                                    T* dst, const float* bias_s, bool v8, uint32_t sbuf) {
+__device__ __forceinline__ void epilogue_row_tma(uint32_t lane_base, int mt, int G2, int sc, int Nn, bool valid,
+                                                 int p, const float* bias_s, uint32_t stage_base, uint32_t slice_bytes,
+                                                 int W) {
   constexpr int kPer = 4 / NP;
-  const int lane = threadIdx.x & 31;
   const int nchunk16 = sc * Nn / 16;
-  const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
-  const uint32_t row_addr = sbuf + (uint32_t)lane * 128u;
-  const uint64_t my_dst = reinterpret_cast<uint64_t>(dst);
-  for (int c0 = 0; c0 < nchunk16; c0 += 4) {
-    const int cend = min(c0 + 4, nchunk16);
-    for (int cb = c0; cb < cend; cb += kPer) {
-      uint32_t r[kPer][NP][16];
+  const uint32_t swz = ((uint32_t)p * (uint32_t)W >> 7) & (uint32_t)(W / 16 - 1);
+  const uint32_t row_addr = stage_base + (uint32_t)p * (uint32_t)W;
+  for (int c = 0; c < nchunk16; c += kPer) {
+    uint32_t r[kPer][NP][16];
 #pragma unroll
-      for (int b = 0; b < kPer; ++b) {
-        const int cc = cb + b;
-        if (cc < cend) {
-          const int col = cc * 16;  // channel offset within the row of sc chunks
-          const int j = col / Nn, cn = col - j * Nn;
+    for (int b = 0; b < kPer; ++b) {
+      const int cc = c + b;
+      if (cc < nchunk16) {
+        const int col = cc * 16;  // channel offset within the row of sc chunks
+        const int j = col / Nn, cn = col - j * Nn;
 #pragma unroll
-          for (int p = 0; p < NP; ++p) tmem_ld16(lane_base + (uint32_t)((p * G2 + mt * sc + j) * Nn + cn), r[b][p]);
-        }
+        for (int q = 0; q < NP; ++q) tmem_ld16(lane_base + (uint32_t)((q * G2 + mt * sc + j) * Nn + cn), r[b][q]);
       }
-      tmem_ld_wait();
+    }
+    tmem_ld_wait();
+    if (valid) {
 #pragma unroll
       for (int b = 0; b < kPer; ++b) {
-        const int cc = cb + b;
-        if (cc < cend) {
+        const int cc = c + b;
+        if (cc < nchunk16) {
           uint32_t wd[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             float s0 = __uint_as_float(r[b][0][2 * i]), s1 = __uint_as_float(r[b][0][2 * i + 1]);
 #pragma unroll
-            for (int p = 1; p < NP; ++p) {
-              s0 += __uint_as_float(r[b][p][2 * i]);
-              s1 += __uint_as_float(r[b][p][2 * i + 1]);
+            for (int q = 1; q < NP; ++q) {
+              s0 += __uint_as_float(r[b][q][2 * i]);
+              s1 += __uint_as_float(r[b][q][2 * i + 1]);
             }
             wd[i] = epilogue_pair<T>(s0, s1, bias_s[cc * 16 + 2 * i], bias_s[cc * 16 + 2 * i + 1]);
           }
-          const uint32_t u0 = (uint32_t)(cc - c0) * 2u;
-          const uint32_t sw = (uint32_t)(lane & 7);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row_addr + ((u0 ^ sw) << 4)), "r"(wd[0]),
+          // 32 bytes of this pixel: chunks c16, c16 + 1 of its slice row
+          const uint32_t byte = (uint32_t)cc * 32u;
+          const uint32_t slice = byte / (uint32_t)W, c16 = (byte % (uint32_t)W) >> 4;
+          const uint32_t base = row_addr + slice * slice_bytes;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + ((c16 ^ swz) << 4)), "r"(wd[0]),
                        "r"(wd[1]), "r"(wd[2]), "r"(wd[3])
                        : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row_addr + (((u0 + 1u) ^ sw) << 4)),
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(base + (((c16 + 1u) ^ swz) << 4)),
                        "r"(wd[4]), "r"(wd[5]), "r"(wd[6]), "r"(wd[7])
                        : "memory");
         }
       }
     }
-    __syncwarp();
-    const int c = lane & 3;
-    const bool c_ok = c0 + c < cend;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int p = 8 * i + (lane >> 2);  // pixel row whose chunk c this lane stores
-      const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)my_dst, p);
-      const uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)(my_dst >> 32), p);
-      if (((vmask >> p) & 1u) && c_ok) {
-        T* pd = reinterpret_cast<T*>(((uint64_t)hi << 32) | lo) + (c0 + c) * 16;
-        const uint32_t prow = sbuf + (uint32_t)p * 128u, psw = (uint32_t)(p & 7);
-        uint32_t a[4], b[4];
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
-                     : "r"(prow + (((2u * c) ^ psw) << 4)));
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3])
-                     : "r"(prow + (((2u * c + 1u) ^ psw) << 4)));
-        if (v8) {
-          asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(pd), "r"(a[0]), "r"(a[1]),
-                       "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3])
-                       : "memory");
-        } else {
-          *reinterpret_cast<uint4*>(pd) = make_uint4(a[0], a[1], a[2], a[3]);
-          *reinterpret_cast<uint4*>(pd + 8) = make_uint4(b[0], b[1], b[2], b[3]);
-        }
-      }
-    }
-    __syncwarp();  // the staging rows are rewritten by the next group
   }
 }
 
@@ -265,6 +240,7 @@ __device__ __forceinline__ void epilogue_row_staged(uint32_t lane_base, int mt, 
 template <typename T, bool SW, bool STAGED>
 __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__ CUtensorMap xmap,
                                                         const __grid_constant__ CUtensorMap wmap,
+                                                        const __grid_constant__ CUtensorMap ymap,
                                                         const __grid_constant__ TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* a_full = reinterpret_cast<uint64_t*>(smem);
@@ -302,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     fence_mbar_init();
     tma_prefetch_desc(&xmap);
     if (a.w_tma) tma_prefetch_desc(&wmap);
+    if (STAGED) tma_prefetch_desc(&ymap);
   }
   // Named barrier 2 (all threads): warp 0 arrives once the barriers are
   // initialised and goes straight on to copy input tiles; warps 1.. sync on
@@ -619,6 +596,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     // 32-byte stores when every 16-channel piece starts on a 32-byte boundary
     // (each chunk row's channel offset is a multiple of 16)
     const bool v8 = (reinterpret_cast<uintptr_t>(yg) & 31) == 0 && (a.Ktot & 15) == 0;
+    // STAGED (on request): the four epilogue warps write the tile's output
+    // box into shared memory and one thread stores it with TMA tensor stores
+    // (one per channel slice); the next tile waits until those stores have
+    // read the staging buffer.
+    const bool store_thread = warp == kIssuers + 1 && lane == 0;
+    const uint32_t stage_base = smem_u32(smem + a.epi_off);
     int k = 0;
     for (int sp = cta_in_gc; sp < a.spatial_tiles; sp += a.cpg, ++k) {
       const int ab = k & 1;
@@ -629,27 +612,54 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
       fence_after_sync();
       const SpatialTile st = decode_spatial(a, sp);
       const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * NP * G2 * a.Nn);
+      if constexpr (STAGED) {
+        if (store_thread) tma_store_wait_read();  // the previous tile's stores have read the buffer
+        asm volatile("bar.sync 3, 128;" ::: "memory");
+      }
       for (int mt = 0; mt < a.nmt; ++mt) {
         const int f = mt * 128 + row;
         const int i = f / a.P, jj = f - i * a.P;
         const int oh = st.oh0 + i, ow = st.ow0 + jj;
-        const bool valid = i < a.TH && jj < a.TWo && oh < a.Ho && ow < a.Wo;
-        T* dst = yg + ((((int64_t)st.n * a.Do + st.od) * a.Ho + oh) * (int64_t)a.Wo + ow) * a.Ktot +
-                 (int64_t)g0 * a.Kg;
         if constexpr (STAGED) {
-          const uint32_t sbuf = smem_u32(smem + a.epi_off) + (uint32_t)q * 4096u;
-          if (NP == 1) epilogue_row_staged<T, 1>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8, sbuf);
-          else if (NP == 2) epilogue_row_staged<T, 2>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8, sbuf);
-          else epilogue_row_staged<T, 4>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8, sbuf);
+          // pixels past the image edge are written too; the TMA store clips them
+          const bool valid = i < a.TH && jj < a.TWo;
+          const int p = i * a.TWo + jj;
+          if (NP == 1)
+            epilogue_row_tma<T, 1>(lane_base, mt, G2, a.sc, a.Nn, valid, p, bias_s, stage_base, a.epi_slice_bytes,
+                                   a.epi_w);
+          else if (NP == 2)
+            epilogue_row_tma<T, 2>(lane_base, mt, G2, a.sc, a.Nn, valid, p, bias_s, stage_base, a.epi_slice_bytes,
+                                   a.epi_w);
+          else
+            epilogue_row_tma<T, 4>(lane_base, mt, G2, a.sc, a.Nn, valid, p, bias_s, stage_base, a.epi_slice_bytes,
+                                   a.epi_w);
         } else {
+          const bool valid = i < a.TH && jj < a.TWo && oh < a.Ho && ow < a.Wo;
+          T* dst = yg + ((((int64_t)st.n * a.Do + st.od) * a.Ho + oh) * (int64_t)a.Wo + ow) * a.Ktot +
+                   (int64_t)g0 * a.Kg;
           if (NP == 1) epilogue_row<T, 1>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8);
           else if (NP == 2) epilogue_row<T, 2>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8);
           else epilogue_row<T, 4>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8);
         }
       }
+      // every tcgen05.ld of this tile has completed: the accumulators are free
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[ab]);
+      if constexpr (STAGED) {
+        fence_proxy_async_smem();  // the staging writes -> visible to the TMA engine
+        asm volatile("bar.sync 3, 128;" ::: "memory");
+        if (store_thread) {
+          const int c0 = g0 * a.Kg;
+          for (int sl = 0; sl < a.epi_slices; ++sl)
+            tma_store_5d(&ymap, smem + a.epi_off + (size_t)sl * a.epi_slice_bytes, c0 + sl * (a.epi_w / 2), st.ow0,
+                         st.oh0, st.od, st.n);
+          tma_store_commit();
+        }
+      }
+    }
+    if constexpr (STAGED) {
+      if (store_thread) tma_store_wait_all();  // the stores are complete before the CTA exits
     }
   }
   __syncwarp();

@@ -120,8 +120,9 @@ typedef struct gconv_options {
                             Tensor-core kernel: [0] TH, [2] M tiles per CTA,
                             [3] stages, [4] partial accumulators, [6] 1 = force
                             16-byte chunk planes, [7] extra shared memory (KB),
-                            negative: stage the epilogue through shared memory
-                            for coalesced stores (default: store from registers). */
+                            negative: stage the tile's output box in shared
+                            memory and write it with TMA tensor stores
+                            (default: store from registers). */
   int32_t serial_launch; /* 0: the kernel is launched as a programmatic dependent
                             launch: its CTAs may start, and set up barriers,
                             tensor memory and tables, while the previous kernel

@@ -138,11 +138,15 @@ def test_depthwise_column_tiles(orc, name, tiles, one_copy):
     assert_close(y.double().numpy(), ref, wl.dtype, f"{name} tiles {tiles}")
 
 
-@pytest.mark.parametrize("name", ["resnext_b_bf16", "sweep_g8_d1_s1_bf16", "resnext3d_n1_f16", "sweep_g256_d2_s2_bf16"])
-@pytest.mark.parametrize("staged", [True, False], ids=["staged", "direct"])
+@pytest.mark.parametrize("name", ["resnext_b_bf16", "sweep_g8_d1_s1_bf16", "resnext3d_n1_f16", "sweep_g256_d2_s2_bf16",
+                                  "resnext_a_bf16", "sweep_g64_d2_s1_bf16"])
+@pytest.mark.parametrize("staged", [True, False], ids=["tma-store", "registers"])
 def test_tensor_core_epilogue_paths(orc, name, staged):
-    """Both epilogues of the tensor-core kernel: straight from registers (the
-    default) and through shared-memory staging (override slot 7 < 0)."""
+    """Both epilogues of the tensor-core kernel: stores straight from
+    registers (the default), and the output box staged in shared memory and
+    written by TMA tensor stores (override slot 7 < 0).  The workloads cover
+    128-, 64-byte channel slices, ragged bottom and right tile edges that the
+    TMA store clips, and one to four partial accumulators."""
     wl = inputs.by_name(name).with_(N=min(inputs.by_name(name).N, 2))
     x, w, b = inputs.make_inputs(wl)
     ref = orc.forward(wl, x, w, b)

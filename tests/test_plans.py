@@ -12,7 +12,8 @@ every workload family, random problems and maximum-size problems:
 * tensor-core plans: TMEM columns a power of two that holds the double-
   buffered (partial) accumulators, the host MMA table within its bound and
   its offsets inside the operand regions, the grid = group chunks x CTAs
-  per chunk.
+  per chunk; the staged epilogue's output boxes (TMA store) inside shared
+  memory, 1024-byte aligned, covering the CTA's channels.
 """
 import json
 import os
@@ -192,6 +193,13 @@ def _check_tc_plan(wl, p):
         assert p["a_off"] <= p["max_a"] < p["a_off"] + p["a_stage_bytes"], ctx
         assert p["b_off"] <= p["max_b"] < p["a_off"], ctx
     assert p["bias_off"] < p["tab_off"] <= p["b_off"], ctx
+    if p["epi_off"]:  # output box staged for TMA stores, one box per channel slice
+        assert p["epi_off"] % 1024 == 0 and p["epi_slice_bytes"] % 1024 == 0, ctx
+        assert p["epi_off"] >= p["a_off"] + p["stages"] * p["a_stage_bytes"], ctx
+        assert p["epi_off"] + p["epi_slices"] * p["epi_slice_bytes"] <= p["smem"], ctx
+        assert p["epi_w"] in (32, 64, 128) and p["epi_w"] * p["epi_slices"] == p["sc"] * p["Nn"] * 2, ctx
+        assert p["TH"] * p["TWo"] * p["epi_w"] <= p["epi_slice_bytes"], ctx
+        assert p["TWo"] <= 256 and p["TH"] <= 256, ctx
 
 
 def test_tensor_core_plans(harness):
