@@ -68,8 +68,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tile", default="", help="tuning override TH,TW,WB,stages,ctas_per_sm,fma_form")
     ap.add_argument("--force-kernel", type=int, default=0)
-    ap.add_argument("--op", choices=["fwd", "bwd_data"], default="fwd",
-                    help="fwd: the forward pass (default); bwd_data: the gradient with respect to x, given dy "
+    ap.add_argument("--op", choices=["fwd", "bwd_data", "bwd_weight"], default="fwd",
+                    help="fwd: the forward pass (default); bwd_data: the gradient with respect to x, given dy; "
+                         "bwd_weight: the gradient with respect to w, given x and dy "
                          "(no end-to-end leg)")
     ap.add_argument("--serial-launch", action="store_true",
                     help="launch without programmatic dependent launch (each kernel starts after the previous ends)")
@@ -256,7 +257,7 @@ def cpu_oracle_prepare(wls):
 def cpu_baseline(wls, min_seconds=10.0, max_seconds=30.0, op="fwd"):
     """Whole-workload oracle passes, repeated for about min_seconds."""
     orc, prep, np = cpu_oracle_prepare(wls)
-    if op == "bwd_data":
+    if op != "fwd":
         for p in prep:
             p["dy"] = np.random.default_rng(1).uniform(-1, 1, size=(p["wl"].N,) + tuple(
                 o for o in orc.out_shape(p["wl"])[3 - p["wl"].ndim:]) + (p["wl"].G, p["wl"].Kg))
@@ -265,6 +266,8 @@ def cpu_baseline(wls, min_seconds=10.0, max_seconds=30.0, op="fwd"):
         for p in prep:
             if op == "bwd_data":
                 orc.bwd_data(p["wl"], p["dy"], p["w"])
+            elif op == "bwd_weight":
+                orc.bwd_weight(p["wl"], p["x"], p["dy"])
             else:
                 orc.forward(p["wl"], p["x"], p["w"], p["b"])
         reps += 1
@@ -289,9 +292,18 @@ def run_reference(args, wls, rank, world):
     budget_s = 120.0
     per_step_s = budget_s / total_steps / len(prep)
     rng = np.random.default_rng(0)
-    bwd = getattr(args, "op", "fwd") == "bwd_data"
+    op = getattr(args, "op", "fwd")
+    bwd = op != "fwd"
+
+    def bwd_call(p, n, start):
+        wl = p["wl"].with_(N=n)
+        if op == "bwd_data":
+            orc.bwd_data(wl, p["dy"][start:start + n], p["w"])
+        else:
+            orc.bwd_weight(wl, p["x"][start:start + n], p["dy"][start:start + n])
+
     if bwd:
-        # whole images per step (backward data of an image needs all of its dy):
+        # whole images per step (an image's backward pass needs all of its dy):
         # a contiguous run of images sized from a one-image rate probe
         for p in prep:
             wl = p["wl"]
@@ -299,7 +311,7 @@ def run_reference(args, wls, rank, world):
             p["bytes"] = p["bytes"] - (wl.K * (2 if wl.dtype != "f32" else 4) if wl.bias else 0)
             p["dy"] = rng.uniform(-1, 1, size=(wl.N,) + tuple(p["out"][3 - wl.ndim:]) + (wl.G, wl.Kg))
             t0 = time.perf_counter()
-            orc.bwd_data(wl.with_(N=1), p["dy"][:1], p["w"])
+            bwd_call(p, 1, 0)
             p["rate"] = 1.0 / max(time.perf_counter() - t0, 1e-6)
             p["n"] = int(max(1, min(wl.N, p["rate"] * per_step_s)))
     else:
@@ -318,7 +330,7 @@ def run_reference(args, wls, rank, world):
         for p in prep:
             start = int(rng.integers(0, max(1, p["total"] - p["n"])))
             if bwd:
-                orc.bwd_data(p["wl"].with_(N=p["n"]), p["dy"][start:start + p["n"]], p["w"])
+                bwd_call(p, p["n"], start)
             else:
                 orc.points(p["wl"], p["x"], p["w"], p["b"], np.arange(start, start + p["n"], dtype=np.int64))
 
@@ -330,15 +342,15 @@ def run_reference(args, wls, rank, world):
     el = time.perf_counter() - t0
     frac_bytes = sum(p["bytes"] * p["n"] / p["total"] for p in prep)
     value = frac_bytes * args.steps / el / 1e9
-    unit = "images (backward data)" if bwd else "outputs"
+    unit = f"images ({op.replace('_', ' ')})" if bwd else "outputs"
     sample = ("per step: " + ", ".join(f"{p['n']} of {p['total']} {unit} of {p['wl'].name}" for p in prep)
               + "; bytes credited in proportion to the work computed")
-    line = {"impl": "reference", "metric": METRIC.replace("fwd", "bwd_data") if bwd else METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+    line = {"impl": "reference", "metric": METRIC.replace("fwd", op), "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": wls[0].dtype, "data": "synthetic",
             "config": {"workload": describe(wls), "layout": "NHWGC / GKYXC / NHWGK",
-                       "op": "bwd_data" if bwd else "fwd"},
+                       "op": op},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -350,17 +362,19 @@ def run_reference(args, wls, rank, world):
 # ---------------------------------------------------------------------------
 class GpuArm:
     """Device buffers, launches and timing of one or more convolutions on one
-    GPU, through the library's C ABI (``grouped_conv_fwd_ex`` /
-    ``grouped_conv_bwd_data_ex``)."""
+    GPU, through the library's C ABI (``grouped_conv_fwd_ex``,
+    ``grouped_conv_bwd_data_ex`` or ``grouped_conv_bwd_weight_ex``, by
+    ``op``)."""
 
-    def __init__(self, args, dev, stream, bwd):
+    def __init__(self, args, dev, stream, op):
         import depthwise_convolution_forward_gb300 as gc
         from depthwise_convolution_forward_gb300 import _binding as B
 
         self.gc, self.B = gc, B
         self.lib = B.load_library()
         self.dev, self.stream, self.sh = dev, stream, stream.cuda_stream
-        self.bwd = bwd
+        self.op = op if op else "fwd"
+        self.bwd = self.op != "fwd"
         self.opt = B.gconv_options()
         self.opt.force_kernel = args.force_kernel
         self.opt.serial_launch = 1 if args.serial_launch else 0
@@ -397,10 +411,16 @@ class GpuArm:
             s = []
             for c in convs:
                 wd = c["w"].to(self.dev)
-                if self.bwd:  # input dy (forward output layout, U(-1, 1)), output dx (forward input layout)
+                if self.op == "bwd_data":  # input dy (forward output layout, U(-1, 1)), output dx (input layout)
                     g = torch.Generator().manual_seed(9500 + r)
                     xd = (torch.rand(c["ysh"], generator=g) * 2 - 1).to(c["x"].dtype).to(self.dev)
                     yd = torch.empty(c["x"].shape, dtype=c["x"].dtype, device=self.dev)
+                    bd = None
+                elif self.op == "bwd_weight":  # inputs x and dy (U(-1, 1)), output dw (weight layout)
+                    g = torch.Generator().manual_seed(9700 + r)
+                    xd = c["x"].to(self.dev)
+                    wd = (torch.rand(c["ysh"], generator=g) * 2 - 1).to(c["x"].dtype).to(self.dev)
+                    yd = torch.empty(c["w"].shape, dtype=c["x"].dtype, device=self.dev)
                     bd = None
                 else:
                     xd = c["x"].to(self.dev)
@@ -410,7 +430,9 @@ class GpuArm:
             sets.append(s)
         if self.bwd:  # one workspace per convolution (stream order keeps consecutive calls apart)
             for c in convs:
-                c["ws_bytes"] = gc.grouped_conv_bwd_data_workspace_size(c["p"], c["dt"])
+                size = gc.grouped_conv_bwd_data_workspace_size if self.op == "bwd_data" else \
+                    gc.grouped_conv_bwd_weight_workspace_size
+                c["ws_bytes"] = size(c["p"], c["dt"])
                 c["ws"] = torch.empty(max(1, c["ws_bytes"]), dtype=torch.uint8, device=self.dev)
         torch.cuda.synchronize(self.dev)
         return convs, sets, R, per_set
@@ -418,10 +440,14 @@ class GpuArm:
     def launch(self, convs, sets, r, ci):
         c = convs[ci]
         xd, wd, bd, yd = sets[r][ci]
-        if self.bwd:
+        if self.op == "bwd_data":
             st = self.lib.grouped_conv_bwd_data_ex(xd.data_ptr(), wd.data_ptr(), yd.data_ptr(), ctypes.byref(c["p"]),
                                                    c["dt"], c["ws"].data_ptr() if c["ws_bytes"] else None,
                                                    c["ws_bytes"], self.sh, self.optp)
+        elif self.op == "bwd_weight":  # x, dy -> dw
+            st = self.lib.grouped_conv_bwd_weight_ex(xd.data_ptr(), wd.data_ptr(), yd.data_ptr(),
+                                                     ctypes.byref(c["p"]), c["dt"], c["ws"].data_ptr(),
+                                                     c["ws_bytes"], self.sh, self.optp)
         else:
             st = self.lib.grouped_conv_fwd_ex(xd.data_ptr(), wd.data_ptr(),
                                               bd.data_ptr() if bd is not None else None, yd.data_ptr(),
@@ -430,8 +456,9 @@ class GpuArm:
             raise RuntimeError(f"grouped_conv launch failed: {self.gc.gconv_last_error()}")
         c["kernel"] = self.opt.selected
         # launches of the library's kernels this call made (the transposed-
-        # weights route of backward data adds the weight-flip kernel)
-        c["kernels_per_call"] = 2 if self.bwd and c.get("ws_bytes") else 1
+        # weights route of backward data adds the weight-flip kernel;
+        # backward weight is a partial kernel and a reduction)
+        c["kernels_per_call"] = 2 if (self.op == "bwd_weight" or (self.bwd and c.get("ws_bytes"))) else 1
 
     def capture(self, n_units, launch_unit, per_graph=1000):
         """Graphs of back-to-back library calls (no event nodes inside: an
@@ -504,8 +531,8 @@ def run_ours(args, wls, set_name, rank, world):
     dev = torch.device("cuda", local)
     build.build()
     stream = torch.cuda.Stream(dev)
-    bwd = args.op == "bwd_data"
-    arm = GpuArm(args, dev, stream, bwd)
+    bwd = args.op != "fwd"
+    arm = GpuArm(args, dev, stream, args.op)
     convs, sets, R, per_set = arm.prepare(wls)
     nl = len(convs)
     step_bytes = sum(c["bytes"] for c in convs)
@@ -615,7 +642,7 @@ def run_ours(args, wls, set_name, rank, world):
     if not args.no_e2e and not bwd:
         e2e = run_e2e(args, convs, arm.lib, dev, stream, world, dist, step_bytes, arm.gc)
 
-    line = {"metric": METRIC.replace("fwd", "bwd_data") if bwd else METRIC, "value": value, "unit": "GB/s",
+    line = {"metric": METRIC.replace("fwd", args.op), "value": value, "unit": "GB/s",
             "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wls[0].dtype, "data": "synthetic",

@@ -18,6 +18,9 @@ from ._binding import (  # noqa: F401
     grouped_conv_bwd_data,
     grouped_conv_bwd_data_ex,
     grouped_conv_bwd_data_noalloc,
+    grouped_conv_bwd_weight,
+    grouped_conv_bwd_weight_ex,
+    grouped_conv_bwd_weight_workspace_size,
     grouped_conv_bwd_data_workspace_size,
     grouped_conv_fwd,
     grouped_conv_fwd_ex,

@@ -27,8 +27,10 @@ DTYPE_CODES = {"f32": GCONV_F32, "f16": GCONV_F16, "bf16": GCONV_BF16}
 
 KERNEL_AUTO, KERNEL_DIRECT_DW, KERNEL_DIRECT_GENERIC, KERNEL_IGEMM_TC = 0, 1, 2, 3
 KERNEL_BWD_DATA_DIRECT = 4
+KERNEL_BWD_WEIGHT = 5
 KERNEL_NAMES = {KERNEL_DIRECT_DW: "direct_dw", KERNEL_DIRECT_GENERIC: "direct_generic",
-                KERNEL_IGEMM_TC: "igemm_tc", KERNEL_BWD_DATA_DIRECT: "bwd_data_direct"}
+                KERNEL_IGEMM_TC: "igemm_tc", KERNEL_BWD_DATA_DIRECT: "bwd_data_direct",
+                KERNEL_BWD_WEIGHT: "bwd_weight"}
 
 
 class gconv_problem(ctypes.Structure):
@@ -79,6 +81,13 @@ def load_library(path: Optional[str] = None):
         lib.grouped_conv_bwd_data_ex.restype = i32
         lib.grouped_conv_bwd_data_ex.argtypes = [vp, vp, vp, prob_p, i32, vp, i64, vp,
                                                  ctypes.POINTER(gconv_options)]
+        lib.grouped_conv_bwd_weight.restype = i32
+        lib.grouped_conv_bwd_weight.argtypes = [vp, vp, vp, prob_p, i32, vp, i64, vp]
+        lib.grouped_conv_bwd_weight_ex.restype = i32
+        lib.grouped_conv_bwd_weight_ex.argtypes = [vp, vp, vp, prob_p, i32, vp, i64, vp,
+                                                   ctypes.POINTER(gconv_options)]
+        lib.grouped_conv_bwd_weight_workspace_size.restype = i32
+        lib.grouped_conv_bwd_weight_workspace_size.argtypes = [prob_p, i32, ctypes.POINTER(i64)]
         lib.grouped_conv_bwd_data_noalloc.restype = i32
         lib.grouped_conv_bwd_data_noalloc.argtypes = [vp, vp, vp, prob_p, i32, vp]
         lib.grouped_conv_bwd_data_workspace_size.restype = i32
@@ -211,6 +220,34 @@ def grouped_conv_bwd_data_ex(dy, w, dx, p: gconv_problem, dtype: int, workspace=
         workspace_bytes = workspace.numel() * workspace.element_size()
     _check(lib.grouped_conv_bwd_data_ex(_ptr(dy), _ptr(w), _ptr(dx), ctypes.byref(p), dtype, _ptr(workspace),
                                         workspace_bytes, _stream(stream), ctypes.byref(o)))
+    return o
+
+
+def grouped_conv_bwd_weight_workspace_size(p: gconv_problem, dtype: int) -> int:
+    """Device workspace bytes grouped_conv_bwd_weight needs (never 0)."""
+    lib = load_library()
+    n = ctypes.c_int64(0)
+    _check(lib.grouped_conv_bwd_weight_workspace_size(ctypes.byref(p), dtype, ctypes.byref(n)))
+    return n.value
+
+
+def grouped_conv_bwd_weight(x, dy, dw, p: gconv_problem, dtype: int, workspace=None, workspace_bytes: int = 0,
+                            stream=None) -> None:
+    lib = load_library()
+    if workspace is not None and not isinstance(workspace, int) and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.grouped_conv_bwd_weight(_ptr(x), _ptr(dy), _ptr(dw), ctypes.byref(p), dtype, _ptr(workspace),
+                                       workspace_bytes, _stream(stream)))
+
+
+def grouped_conv_bwd_weight_ex(x, dy, dw, p: gconv_problem, dtype: int, workspace=None, workspace_bytes: int = 0,
+                               stream=None, opt: Optional[gconv_options] = None) -> gconv_options:
+    lib = load_library()
+    o = opt if opt is not None else gconv_options()
+    if workspace is not None and not isinstance(workspace, int) and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.grouped_conv_bwd_weight_ex(_ptr(x), _ptr(dy), _ptr(dw), ctypes.byref(p), dtype, _ptr(workspace),
+                                          workspace_bytes, _stream(stream), ctypes.byref(o)))
     return o
 
 

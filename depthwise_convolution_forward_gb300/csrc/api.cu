@@ -396,6 +396,52 @@ gconv_status grouped_conv_bwd_data(const void* dy, const void* w, void* dx, cons
   return grouped_conv_bwd_data_ex(dy, w, dx, p, dt, workspace, workspace_bytes, stream, nullptr);
 }
 
+gconv_status grouped_conv_bwd_weight_workspace_size(const gconv_problem* p, gconv_dtype dt, int64_t* bytes) {
+  Geometry g;
+  gconv_status s = validate(p, &g);
+  if (s != GCONV_OK) return s;
+  if (dt != GCONV_F32 && dt != GCONV_F16 && dt != GCONV_BF16) return fail(GCONV_ERR_UNSUPPORTED, "unknown dtype %d", (int)dt);
+  if (bytes == nullptr) return fail(GCONV_ERR_INVALID_ARG, "bytes pointer is NULL");
+  *bytes = bwd_weight_workspace_bytes(g, (DType)dt);
+  return GCONV_OK;
+}
+
+gconv_status grouped_conv_bwd_weight_ex(const void* x, const void* dy, void* dw, const gconv_problem* p,
+                                        gconv_dtype dt, void* workspace, int64_t workspace_bytes,
+                                        struct CUstream_st* stream, gconv_options* opt) {
+  Geometry g;
+  gconv_status s = validate(p, &g);
+  if (s != GCONV_OK) return s;
+  if (dt != GCONV_F32 && dt != GCONV_F16 && dt != GCONV_BF16) return fail(GCONV_ERR_UNSUPPORTED, "unknown dtype %d", (int)dt);
+  if (x == nullptr || dy == nullptr || dw == nullptr) return fail(GCONV_ERR_INVALID_ARG, "x, dy and dw must not be NULL");
+  if (opt && opt->force_kernel != 0 && opt->force_kernel != GCONV_KERNEL_BWD_WEIGHT)
+    return fail(GCONV_ERR_UNSUPPORTED, "kernel %d does not compute backward weight", opt->force_kernel);
+  const DType t = (DType)dt;
+  const int es = dtype_bytes(t);
+  const int64_t dwb = g.w_elems() * es, xb = g.x_elems() * es, dyb = g.y_elems() * es;
+  const int64_t need = bwd_weight_workspace_bytes(g, t);
+  if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15))
+    return fail(GCONV_ERR_INVALID_ARG, "workspace must be 16-byte aligned and hold %lld bytes", (long long)need);
+  if (overlaps(dw, dwb, x, xb) || overlaps(dw, dwb, dy, dyb) || overlaps(dw, dwb, workspace, need))
+    return fail(GCONV_ERR_INVALID_ARG, "dw overlaps an input buffer or the workspace");
+  if (overlaps(workspace, need, x, xb) || overlaps(workspace, need, dy, dyb))
+    return fail(GCONV_ERR_INVALID_ARG, "the workspace overlaps x or dy");
+
+  DevSlot* slot = nullptr;
+  cudaError_t e = device_slot(&slot);
+  if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
+  LaunchArgs a = make_args(x, dy, nullptr, dw, t, stream, slot, opt);
+  e = bwd_weight_launch(g, a, workspace, slot->info);
+  if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+  if (opt) opt->selected = GCONV_KERNEL_BWD_WEIGHT;
+  return finish(slot, a, opt);
+}
+
+gconv_status grouped_conv_bwd_weight(const void* x, const void* dy, void* dw, const gconv_problem* p, gconv_dtype dt,
+                                     void* workspace, int64_t workspace_bytes, struct CUstream_st* stream) {
+  return grouped_conv_bwd_weight_ex(x, dy, dw, p, dt, workspace, workspace_bytes, stream, nullptr);
+}
+
 gconv_status grouped_conv_fwd(const void* x, const void* w, const void* bias, void* y, const gconv_problem* p,
                               gconv_dtype dt, struct CUstream_st* stream) {
   return grouped_conv_fwd_ex(x, w, bias, y, p, dt, stream, nullptr);

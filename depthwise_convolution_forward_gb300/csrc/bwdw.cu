@@ -1,0 +1,403 @@
+// Grouped convolution backward weight (the gradient with respect to w).
+//
+//   dw[g, k, z, yy, xx, c] = sum over (n, od, oh, ow) of
+//       dy[n, od, oh, ow, g, k] * x[n, od*sD - pD + z*dD, oh*sH - pH + yy*dH, ow*sW - pW + xx*dW, g, c]
+//
+// with zero padding outside x.  The backward-weight variant, whose runner
+// takes X and dY and which can reduce through an fp32 workspace in two
+// stages, is listed by the pages' CK grouped-convolution tile engine and its
+// Python examples (Examples; Config-options harness, two_stage).
+//
+// Two stages, both deterministic (fixed split and summation order):
+//  1. bwd_weight_partial_kernel: the output pixels (the sum's range) are cut
+//     into S equal runs ("splits").  For each split, every work item -- a
+//     vector of V input channels x one output channel x a block of up to
+//     kTapBlock taps -- accumulates its products in fp32 registers; items
+//     that share a CTA may also share the split's pixels ("pixel lanes") and
+//     are then summed through shared memory.  Each split writes its fp32
+//     partial of every dw element into the caller's workspace [S][E].
+//  2. bwd_weight_reduce_kernel: dw[e] = round(sum over s of partial[s][e]),
+//     one round-to-nearest-even cast; 32 threads per element share its
+//     splits and their sums are added in a fixed order.
+// Work items: MODE 0 (grouped) takes V consecutive input channels of one
+// group (Cg % V == 0) and one output channel k, lanes ordered k fastest so
+// the dy reads of a warp are consecutive and its x reads are shared;
+// MODE 1 (depthwise, Cg == Kg == 1) takes V consecutive groups, whose dy and
+// x values are both V-element vectors.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "plan_cache.h"
+
+namespace gconv {
+namespace {
+
+constexpr int kTapBlock = 9;      // taps one work item accumulates (registers: kTapBlock x V)
+constexpr int kBwwThreads = 256;  // threads per CTA of the partial kernel
+
+struct BwwArgs {
+  const void* x;
+  const void* dy;
+  float* ws;
+  void* dw;
+  int G, Cg, Kg;
+  int D, H, W, Do, Ho, Wo, Z, Y, X;
+  int sD, sH, sW, pD, pH, pW, dD, dH, dW;
+  int taps, ntb;      // taps per filter, tap blocks
+  int64_t P;          // output pixels N * Do * Ho * Wo (the sum's range)
+  int S;              // splits of the pixel range
+  int64_t E;          // dw elements
+  int items;          // work items per split
+  int ipc, lanes;     // items per CTA, pixel lanes per item (ipc * lanes <= kBwwThreads)
+};
+
+template <typename T, int V>
+__device__ __forceinline__ void load_vec(const T* p, float (&v)[V]) {
+  constexpr int bytes = V * (int)sizeof(T);
+  if constexpr (bytes == 16) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    unpack16<T>(w, v);
+  } else if constexpr (bytes == 8) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    widen_word<T>(u.x, v);
+    widen_word<T>(u.y, v + 4 / (int)sizeof(T));
+  } else if constexpr (bytes == 4 && sizeof(T) == 2) {
+    widen_word<T>(*reinterpret_cast<const uint32_t*>(p), v);
+  } else {
+#pragma unroll
+    for (int i = 0; i < V; ++i) v[i] = Elem<T>::to_f32(p[i]);
+  }
+}
+
+// NW consecutive 32-bit words (NW = 4, 2 or 1: 16-, 8- or 4-byte aligned).
+template <int NW, typename T>
+__device__ __forceinline__ void load_words(const T* p, uint32_t (&w)[NW]) {
+  if constexpr (NW == 4) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    w[0] = u.x, w[1] = u.y, w[2] = u.z, w[3] = u.w;
+  } else if constexpr (NW == 2) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    w[0] = u.x, w[1] = u.y;
+  } else {
+    w[0] = *reinterpret_cast<const uint32_t*>(p);
+  }
+}
+
+// Stage 1.  Grid: (CTAs per split, S).  Thread = (item, pixel lane).
+template <typename T, int V, int MODE>
+__global__ void __launch_bounds__(kBwwThreads) bwd_weight_partial_kernel(const BwwArgs a) {
+  const T* __restrict__ x = static_cast<const T*>(a.x);
+  const T* __restrict__ dy = static_cast<const T*>(a.dy);
+  // pixel-lane partials for the in-CTA sum (lanes > 1 only): [tap * V + v][thread]
+  extern __shared__ float red[];
+  const int tid = threadIdx.x;
+  const int nthr = a.ipc * a.lanes;
+  const int li = tid % a.ipc, lane = tid / a.ipc;
+  const int item = blockIdx.x * a.ipc + li;
+  const bool active = lane < a.lanes && item < a.items;
+  const int64_t C = (int64_t)a.G * a.Cg, K = (int64_t)a.G * a.Kg;
+
+  // item -> (g, k, channel offset, tap block)
+  int g = 0, k = 0, c0 = 0, tb = 0;
+  if (active) {
+    int f = item;
+    if (MODE == 0) {
+      k = f % a.Kg;
+      f /= a.Kg;
+      const int ncv = a.Cg / V;
+      c0 = (f % ncv) * V;
+      f /= ncv;
+      tb = f % a.ntb;
+      g = f / a.ntb;
+    } else {
+      const int ngv = a.G / V;
+      g = (f % ngv) * V;  // first of V groups
+      tb = f / ngv;
+    }
+  }
+  const int t0 = tb * kTapBlock;
+  const int nt = min(kTapBlock, a.taps - t0);
+
+  float acc[kTapBlock][V];
+#pragma unroll
+  for (int t = 0; t < kTapBlock; ++t)
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[t][v] = 0.f;
+
+  grid_dependency_wait();  // x, dy and the workspace are touched only from here on
+
+  if (active) {
+    const int64_t p0 = a.P * blockIdx.y / a.S, p1 = a.P * (blockIdx.y + 1) / a.S;
+    int64_t p = p0 + lane;
+    if (p < p1) {
+      // pixel p -> (n, od, oh, ow), then walked incrementally by `lanes`
+      int64_t q = p;
+      int ow = (int)(q % a.Wo);
+      q /= a.Wo;
+      int oh = (int)(q % a.Ho);
+      q /= a.Ho;
+      int od = (int)(q % a.Do);
+      int64_t n = q / a.Do;
+      const int64_t cx = MODE == 0 ? (int64_t)g * a.Cg + c0 : (int64_t)g;  // x channel of element 0
+      const int64_t cy = MODE == 0 ? (int64_t)g * a.Kg + k : (int64_t)g;   // dy channel of element 0
+      // per tap of the block: its input-position offsets and its element
+      // offset in x (the same for every output pixel)
+      int tz[kTapBlock], ty[kTapBlock], tx[kTapBlock];
+      int64_t toff[kTapBlock];
+#pragma unroll
+      for (int t = 0; t < kTapBlock; ++t) {
+        const int tt = min(t0 + t, a.taps - 1);
+        const int xx = tt % a.X, r = tt / a.X;
+        const int yy = r % a.Y, z = r / a.Y;
+        tz[t] = z * a.dD, ty[t] = yy * a.dH, tx[t] = xx * a.dW;
+        toff[t] = (((int64_t)tz[t] * a.H + ty[t]) * a.W + tx[t]) * C;
+      }
+      // 16-bit data stays packed: the products are mixed-precision FMAs
+      // (fp32 product and sum) of the stored halves
+      constexpr bool kPacked = sizeof(T) == 2 && (V % 2) == 0;
+      for (; p < p1; p += a.lanes) {
+        const T* dyp = dy + p * K + cy;
+        float dv[MODE == 0 ? 1 : V];
+        uint32_t dw32[kPacked ? V / 2 : 1];
+        if constexpr (kPacked) {
+          if constexpr (MODE == 0) {
+            const uint32_t h = *reinterpret_cast<const unsigned short*>(dyp);
+            dw32[0] = h | (h << 16);
+          } else {
+            load_words<V / 2>(dyp, dw32);
+          }
+        } else if constexpr (MODE == 0) {
+          dv[0] = Elem<T>::to_f32(*dyp);
+        } else {
+          load_vec<T, V>(dyp, dv);
+        }
+        const int ih0 = oh * a.sH - a.pH, iw0 = ow * a.sW - a.pW, id0 = od * a.sD - a.pD;
+        const T* xp = x + (((n * a.D + id0) * a.H + ih0) * (int64_t)a.W + iw0) * C + cx;
+#pragma unroll
+        for (int t = 0; t < kTapBlock; ++t) {
+          if (t < nt && (unsigned)(id0 + tz[t]) < (unsigned)a.D && (unsigned)(ih0 + ty[t]) < (unsigned)a.H &&
+              (unsigned)(iw0 + tx[t]) < (unsigned)a.W) {
+            if constexpr (kPacked) {
+              uint32_t xw[V / 2];
+              load_words<V / 2>(xp + toff[t], xw);
+#pragma unroll
+              for (int i = 0; i < V / 2; ++i)
+                fma_mixed_pair<T>(xw[i], dw32[MODE == 0 ? 0 : i], acc[t][2 * i], acc[t][2 * i + 1]);
+            } else {
+              float xv[V];
+              load_vec<T, V>(xp + toff[t], xv);
+#pragma unroll
+              for (int v = 0; v < V; ++v) acc[t][v] = fmaf(MODE == 0 ? dv[0] : dv[v], xv[v], acc[t][v]);
+            }
+          }
+        }
+        // advance the pixel by `lanes` positions
+        ow += a.lanes;
+        while (ow >= a.Wo) {
+          ow -= a.Wo;
+          if (++oh == a.Ho) {
+            oh = 0;
+            if (++od == a.Do) {
+              od = 0;
+              ++n;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // Sum the pixel lanes of each item (in lane order) and write the split's
+  // partial: ws[s][e], e the dw element index.
+  float* ws = a.ws + (int64_t)blockIdx.y * a.E;
+  if (a.lanes > 1) {
+    if (active) {
+#pragma unroll
+      for (int t = 0; t < kTapBlock; ++t)
+#pragma unroll
+        for (int v = 0; v < V; ++v) red[(t * V + v) * nthr + tid] = acc[t][v];
+    }
+    __syncthreads();
+    if (active && lane == 0) {
+      for (int l = 1; l < a.lanes; ++l)
+#pragma unroll
+        for (int t = 0; t < kTapBlock; ++t)
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc[t][v] += red[(t * V + v) * nthr + l * a.ipc + li];
+    }
+  }
+  if (active && lane == 0) {
+#pragma unroll
+    for (int t = 0; t < kTapBlock; ++t) {
+      if (t < nt) {
+        const int tt = t0 + t;
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+          const int64_t e = MODE == 0 ? ((((int64_t)g * a.Kg + k) * a.taps + tt) * a.Cg + c0 + v)
+                                      : ((int64_t)(g + v) * a.taps + tt);
+          ws[e] = acc[t][v];
+        }
+      }
+    }
+  }
+}
+
+// Stage 2: dw[e] = round(sum over s of ws[s][e]).  A CTA of 32 x 32
+// threads takes 32 consecutive elements (coalesced reads of each split's
+// row); thread (e, j) sums the splits s = j, j + 32, ... and the 32 sums of
+// an element are then added in j order, so the order is fixed.
+template <typename T>
+__global__ void __launch_bounds__(1024) bwd_weight_reduce_kernel(const BwwArgs a) {
+  T* __restrict__ dw = static_cast<T*>(a.dw);
+  __shared__ float part[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  grid_dependency_wait();  // the partials are complete
+  for (int64_t e0 = (int64_t)blockIdx.x * 32; e0 < a.E; e0 += (int64_t)gridDim.x * 32) {
+    const int64_t e = e0 + tx;
+    float s = 0.f;
+    if (e < a.E) {
+      int i = ty;
+      for (; i + 96 < a.S; i += 128) {  // four loads in flight
+        const float v0 = a.ws[(int64_t)i * a.E + e], v1 = a.ws[(int64_t)(i + 32) * a.E + e],
+                    v2 = a.ws[(int64_t)(i + 64) * a.E + e], v3 = a.ws[(int64_t)(i + 96) * a.E + e];
+        s += v0;
+        s += v1;
+        s += v2;
+        s += v3;
+      }
+      for (; i < a.S; i += 32) s += a.ws[(int64_t)i * a.E + e];
+    }
+    part[ty][tx] = s;
+    __syncthreads();
+    if (ty == 0 && e < a.E) {
+      float t = 0.f;
+#pragma unroll 8
+      for (int j = 0; j < 32; ++j) t += part[j][tx];
+      dw[e] = epilogue_one<T>(t, 0.f);
+    }
+    __syncthreads();
+  }
+}
+
+// Launch plan: mode, vector width, items, CTA shape and splits.  Depends on
+// the problem and element size only (not on the device), so the workspace
+// size can be queried without a GPU.
+struct BwwPlan {
+  int mode, V, items, ipc, lanes, ctas_per_split, S;
+  int64_t E;
+};
+
+// Items and CTA shape for vector width V.
+void shape_bww(const Geometry& g, int V, BwwPlan* p) {
+  const int ntb = (g.taps() + kTapBlock - 1) / kTapBlock;
+  p->V = V;
+  p->items = p->mode == 1 ? (g.G / V) * ntb : g.G * g.Kg * (g.Cg / V) * ntb;
+  p->ipc = std::min(p->items, kBwwThreads);
+  p->lanes = kBwwThreads / p->ipc;
+  p->ctas_per_split = (p->items + p->ipc - 1) / p->ipc;
+}
+
+// vmax: the widest vector (elements) the buffers' alignment allows.  The
+// splits S are those of the widest vector the shape allows, whatever vmax,
+// so the workspace size does not depend on the pointers.
+BwwPlan plan_bww(const Geometry& g, int es, int vmax) {
+  BwwPlan p{};
+  p.mode = (g.Cg == 1 && g.Kg == 1) ? 1 : 0;
+  auto widest = [&](int cap) {
+    int V = cap;
+    while (V > 1 && (p.mode == 1 ? g.G % V : g.Cg % V) != 0) V /= 2;
+    return V;
+  };
+  shape_bww(g, widest(16 / es), &p);
+  p.E = (int64_t)g.K() * g.taps() * g.Cg;
+  const int64_t P = g.N * (int64_t)g.Do * g.Ho * g.Wo;
+  // about 1024 threads per SM of a 152-SM GPU, at least 16 pixels per
+  // thread, and at most 32 MB of partials
+  const int64_t want = std::max<int64_t>(1, (int64_t)152 * 1024 / ((int64_t)p.ctas_per_split * kBwwThreads));
+  const int64_t by_pixels = std::max<int64_t>(1, P / ((int64_t)p.lanes * 16));
+  const int64_t by_bytes = std::max<int64_t>(1, ((int64_t)32 << 20) / (p.E * 4));
+  p.S = (int)std::min<int64_t>(std::min(want, by_pixels), std::min<int64_t>(by_bytes, 65535));
+  shape_bww(g, widest(std::min(vmax, 16 / es)), &p);
+  return p;
+}
+
+template <typename T, int V, int MODE>
+cudaError_t launch_partial(const BwwArgs& a, const BwwPlan& p, const LaunchArgs& la, const DeviceInfo& dev) {
+  const size_t smem = p.lanes > 1 ? (size_t)kTapBlock * V * p.ipc * p.lanes * sizeof(float) : 0;
+  static SmemAttr attr;
+  if (smem > 48 * 1024) {
+    cudaError_t e = attr.ensure(bwd_weight_partial_kernel<T, V, MODE>, dev.device, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_kernel(bwd_weight_partial_kernel<T, V, MODE>, dim3(p.ctas_per_split, p.S), dim3(kBwwThreads), smem,
+                       la, a);
+}
+
+template <typename T>
+cudaError_t bwd_weight_typed(const Geometry& g, const LaunchArgs& la, float* ws, const DeviceInfo& dev) {
+  // the widest vector both x and dy are aligned to
+  int vmax = 16 / (int)sizeof(T);
+  while (vmax > 1 && ((reinterpret_cast<uintptr_t>(la.x) | reinterpret_cast<uintptr_t>(la.w)) &
+                      (uintptr_t)(vmax * sizeof(T) - 1)))
+    vmax /= 2;
+  const BwwPlan p = plan_bww(g, (int)sizeof(T), vmax);
+  BwwArgs a{};
+  a.x = la.x;
+  a.dy = la.w;  // a.w carries dy (see kernels.h)
+  a.ws = ws;
+  a.dw = la.y;
+  a.G = g.G, a.Cg = g.Cg, a.Kg = g.Kg;
+  a.D = g.D, a.H = g.H, a.W = g.W, a.Do = g.Do, a.Ho = g.Ho, a.Wo = g.Wo, a.Z = g.Z, a.Y = g.Y, a.X = g.X;
+  a.sD = g.sD, a.sH = g.sH, a.sW = g.sW, a.pD = g.pD, a.pH = g.pH, a.pW = g.pW, a.dD = g.dD, a.dH = g.dH,
+  a.dW = g.dW;
+  a.taps = g.taps();
+  a.ntb = (a.taps + kTapBlock - 1) / kTapBlock;
+  a.P = g.N * (int64_t)g.Do * g.Ho * g.Wo;
+  a.S = p.S;
+  a.E = p.E;
+  a.items = p.items;
+  a.ipc = p.ipc;
+  a.lanes = p.lanes;
+  cudaError_t e = cudaErrorNotSupported;
+  // vector widths: 16 / sizeof(T) and below, as the plan's divisibility allows
+#define GCONV_BWW(v_)                                                                   \
+  if (p.V == v_) {                                                                      \
+    e = p.mode == 1 ? launch_partial<T, v_, 1>(a, p, la, dev) : launch_partial<T, v_, 0>(a, p, la, dev); \
+  }
+  GCONV_BWW(1)
+  GCONV_BWW(2)
+  GCONV_BWW(4)
+  if constexpr (sizeof(T) == 2) {
+    GCONV_BWW(8)
+  }
+#undef GCONV_BWW
+  if (e != cudaSuccess) return e;
+  const int64_t blocks = std::min<int64_t>((p.E + 31) / 32, (int64_t)dev.num_sms * 2);
+  return launch_kernel(bwd_weight_reduce_kernel<T>, dim3((unsigned)std::max<int64_t>(1, blocks)), dim3(1024), 0, la,
+                       a);
+}
+
+}  // namespace
+
+int64_t bwd_weight_workspace_bytes(const Geometry& g, DType dt) {
+  const BwwPlan p = plan_bww(g, dtype_bytes(dt), 16 / dtype_bytes(dt));
+  return (int64_t)p.S * p.E * 4;
+}
+
+cudaError_t bwd_weight_launch(const Geometry& g, const LaunchArgs& a, void* workspace, const DeviceInfo& dev) {
+  float* ws = static_cast<float*>(workspace);
+  switch (a.dt) {
+    case kF32: return bwd_weight_typed<float>(g, a, ws, dev);
+    case kF16: return bwd_weight_typed<__half>(g, a, ws, dev);
+    case kBF16: return bwd_weight_typed<__nv_bfloat16>(g, a, ws, dev);
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace gconv

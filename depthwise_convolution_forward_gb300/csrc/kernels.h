@@ -109,6 +109,13 @@ cudaError_t bwd_weight_flip_launch(const Geometry& g, const LaunchArgs& a, void*
 // Direct gather: a.x carries dy, a.w the forward weights, a.y receives dx.
 cudaError_t bwd_data_direct_launch(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
 
+// ---- backward weight -------------------------------------------------------
+// fp32 partials of dw for a fixed number of pixel splits, then one reduction
+// and rounding.  a.x carries x, a.w carries dy, a.y receives dw; the
+// workspace holds bwd_weight_workspace_bytes (independent of the device).
+int64_t bwd_weight_workspace_bytes(const Geometry& g, DType dt);
+cudaError_t bwd_weight_launch(const Geometry& g, const LaunchArgs& a, void* workspace, const DeviceInfo& dev);
+
 // ---- Kc alone (epilogue test entry) --------------------------------------
 cudaError_t epilogue_launch(const float* acc, const void* bias, void* y, int64_t rows, int cols,
                             DType dt, cudaStream_t stream);

@@ -1,6 +1,7 @@
 /*
  * gconv.h -- C ABI of the GB300 grouped-convolution library: the forward
- * pass and backward data (grouped_conv_bwd_data, further below).
+ * pass, backward data and backward weight (grouped_conv_bwd_data and
+ * grouped_conv_bwd_weight, further below).
  *
  * The main operation is the grouped convolution forward pass (groups > 1,
  * including depthwise groups == C), 2D and 3D, with optional bias, stride,
@@ -90,7 +91,8 @@ typedef enum gconv_kernel {
   GCONV_KERNEL_DIRECT_DW = 1,      /* Ka: TMA-staged depthwise direct kernel        */
   GCONV_KERNEL_DIRECT_GENERIC = 2, /* direct kernel for any shape/dtype/alignment   */
   GCONV_KERNEL_IGEMM_TC = 3,       /* Kb: tcgen05/TMEM grouped implicit GEMM        */
-  GCONV_KERNEL_BWD_DATA_DIRECT = 4 /* backward data: direct gather kernel           */
+  GCONV_KERNEL_BWD_DATA_DIRECT = 4, /* backward data: direct gather kernel          */
+  GCONV_KERNEL_BWD_WEIGHT = 5       /* backward weight: split fp32 partials + reduce */
 } gconv_kernel;
 
 /* Options of grouped_conv_fwd_ex.  Zero-initialise, then set what you need. */
@@ -218,6 +220,53 @@ gconv_status grouped_conv_bwd_data_ex(const void *dy, const void *w, void *dx, c
  * only.  GCONV_ERR_INVALID_ARG for a malformed problem or a NULL `bytes`.
  */
 gconv_status grouped_conv_bwd_data_workspace_size(const gconv_problem *p, gconv_dtype dt, int64_t *bytes);
+
+/*
+ * grouped_conv_bwd_weight -- dw, the gradient of y = grouped_conv(x, w) with
+ * respect to w, given x and dy = the gradient with respect to y (the
+ * backward-weight variant of the CK grouped-convolution tile engine, whose
+ * runner takes X and dY and whose two_stage option reduces through an fp32
+ * workspace -- "Grouped Convolution -- Python Examples", Examples and
+ * Config-options harness):
+ *   dw[g, k, z, yy, xx, c] = sum over (n, od, oh, ow) of dy[n, od, oh, ow, g, k]
+ *        * x[n, od*sD - pD + z*dD, oh*sH - pH + yy*dH, ow*sW - pW + xx*dW, g, c]
+ *   x    device, [N, (D), H, W, G, Cg] packed, dtype dt      (read only)
+ *   dy   device, [N, (Do), Ho, Wo, G, Kg] packed, dtype dt  (read only)
+ *   dw   device, [G, Kg, (Z), Y, X, Cg] packed, dtype dt     (written; must not
+ *        overlap x, dy or the workspace)
+ *   p    the forward problem
+ *   workspace  device scratch of at least
+ *        grouped_conv_bwd_weight_workspace_size() bytes, 16-byte aligned,
+ *        owned by the caller, used until the stream passes the call.
+ * Two stages: the sum over output pixels is cut into a fixed number of
+ * equal runs whose fp32 partials land in the workspace, then one kernel adds
+ * the partials in run order and rounds once (round-to-nearest-even).  The
+ * result is deterministic: it depends on the problem only, not on the device
+ * or on timing.  Asynchronous on `stream`; two launches.
+ * Errors: as grouped_conv_fwd, plus GCONV_ERR_INVALID_ARG for a workspace
+ * that is missing, too small or misaligned.
+ */
+gconv_status grouped_conv_bwd_weight(const void *x, const void *dy, void *dw, const gconv_problem *p,
+                                     gconv_dtype dt, void *workspace, int64_t workspace_bytes,
+                                     struct CUstream_st *stream);
+
+/*
+ * grouped_conv_bwd_weight_ex -- grouped_conv_bwd_weight with options:
+ * opt->selected reports GCONV_KERNEL_BWD_WEIGHT; a force_kernel other than
+ * AUTO or GCONV_KERNEL_BWD_WEIGHT returns GCONV_ERR_UNSUPPORTED; debug and
+ * the other fields as for grouped_conv_fwd_ex.
+ */
+gconv_status grouped_conv_bwd_weight_ex(const void *x, const void *dy, void *dw, const gconv_problem *p,
+                                        gconv_dtype dt, void *workspace, int64_t workspace_bytes,
+                                        struct CUstream_st *stream, gconv_options *opt);
+
+/*
+ * grouped_conv_bwd_weight_workspace_size -- device workspace bytes that
+ * grouped_conv_bwd_weight needs for problem p in dtype dt (never 0).  Host
+ * only, no GPU needed.  GCONV_ERR_INVALID_ARG for a malformed problem or a
+ * NULL `bytes`.
+ */
+gconv_status grouped_conv_bwd_weight_workspace_size(const gconv_problem *p, gconv_dtype dt, int64_t *bytes);
 
 /*
  * grouped_conv_bwd_data_noalloc -- grouped_conv_bwd_data for callers that

@@ -164,6 +164,43 @@ def test_bwd_data_overlap_and_forced_route_rejected():
     assert e.value.status == B.GCONV_ERR_UNSUPPORTED
 
 
+# ---- backward weight: host-side logic (nothing is launched on these errors) ----
+def test_bwd_weight_workspace_size():
+    """fp32 partials of every dw element for a fixed number of pixel runs:
+    a positive multiple of the dw element count, the same for every dtype's
+    vector width choice of one shape, and at most 32 MB unless one run
+    already needs more."""
+    for p in (good(), good(stride=(1, 2, 2)), good(G=4, C=4, K=4),
+              B.make_problem(3, 1, 32, 64, 128, (8, 28, 28), (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1))):
+        E = p.K * p.ker[0] * p.ker[1] * p.ker[2] * (p.C // p.G)
+        for dt in (B.GCONV_F16, B.GCONV_BF16, B.GCONV_F32):
+            n = gc.grouped_conv_bwd_weight_workspace_size(p, dt)
+            assert n > 0 and n % (4 * E) == 0, (n, E)
+            assert n <= max(32 << 20, 4 * E)
+
+
+def test_bwd_weight_argument_errors():
+    p = good()
+    need = gc.grouped_conv_bwd_weight_workspace_size(p, B.GCONV_F16)
+    base = 1 << 30
+    for ws, nbytes in ((None, 0), (base + (1 << 26), need - 4), (base + (1 << 26) + 8, need)):
+        with pytest.raises(gc.GconvError) as e:
+            gc.grouped_conv_bwd_weight(base, base + (1 << 20), base + (1 << 22), p, B.GCONV_F16, ws, nbytes)
+        assert e.value.status == B.GCONV_ERR_INVALID_ARG and "workspace" in gc.gconv_last_error()
+    with pytest.raises(gc.GconvError) as e:  # dw overlaps x
+        gc.grouped_conv_bwd_weight(base, base + (1 << 20), base + 64, p, B.GCONV_F16, base + (1 << 26), need)
+    assert e.value.status == B.GCONV_ERR_INVALID_ARG and "overlap" in gc.gconv_last_error()
+    with pytest.raises(gc.GconvError) as e:  # NULL dy
+        gc.grouped_conv_bwd_weight(base, None, base + (1 << 22), p, B.GCONV_F16, base + (1 << 26), need)
+    assert e.value.status == B.GCONV_ERR_INVALID_ARG
+    opt = gc.gconv_options()
+    opt.force_kernel = B.KERNEL_DIRECT_DW
+    with pytest.raises(gc.GconvError) as e:
+        gc.grouped_conv_bwd_weight_ex(base, base + (1 << 20), base + (1 << 22), p, B.GCONV_F16,
+                                      base + (1 << 26), need, None, opt)
+    assert e.value.status == B.GCONV_ERR_UNSUPPORTED
+
+
 def test_plain_c_program_uses_the_abi(tmp_path):
     """The header is plain C: a C99 program includes it, links libgconv.so and
     calls the host-only entry points (no GPU needed for these)."""
