@@ -11,8 +11,9 @@
 // Two stages, both deterministic (fixed split and summation order):
 //  1. bwd_weight_partial_kernel: the output pixels (the sum's range) are cut
 //     into S equal runs ("splits").  For each split, every work item -- a
-//     vector of V input channels x one output channel x a block of up to
-//     kTapBlock taps -- accumulates its products in fp32 registers; items
+//     vector of V input channels x one output channel x a block of taps
+//     (one filter row of at most 3, else up to 9) -- accumulates its
+//     products in fp32 registers; items
 //     that share a CTA may also share the split's pixels ("pixel lanes") and
 //     are then summed through shared memory.  Each split writes its fp32
 //     partial of every dw element into the caller's workspace [S][E].
@@ -37,7 +38,7 @@
 namespace gconv {
 namespace {
 
-constexpr int kTapBlock = 9;      // taps one work item accumulates (registers: kTapBlock x V)
+constexpr int kTapBlockMax = 9;   // most taps one work item accumulates (registers: taps x V)
 constexpr int kBwwThreads = 256;  // threads per CTA of the partial kernel
 
 struct BwwArgs {
@@ -90,7 +91,7 @@ __device__ __forceinline__ void load_words(const T* p, uint32_t (&w)[NW]) {
 }
 
 // Stage 1.  Grid: (CTAs per split, S).  Thread = (item, pixel lane).
-template <typename T, int V, int MODE>
+template <typename T, int V, int MODE, int kTapBlock>
 __global__ void __launch_bounds__(kBwwThreads) bwd_weight_partial_kernel(const BwwArgs a) {
   const T* __restrict__ x = static_cast<const T*>(a.x);
   const T* __restrict__ dy = static_cast<const T*>(a.dy);
@@ -289,13 +290,13 @@ __global__ void __launch_bounds__(1024) bwd_weight_reduce_kernel(const BwwArgs a
 // the problem and element size only (not on the device), so the workspace
 // size can be queried without a GPU.
 struct BwwPlan {
-  int mode, V, items, ipc, lanes, ctas_per_split, S;
+  int mode, V, tb, items, ipc, lanes, ctas_per_split, S;
   int64_t E;
 };
 
 // Items and CTA shape for vector width V.
 void shape_bww(const Geometry& g, int V, BwwPlan* p) {
-  const int ntb = (g.taps() + kTapBlock - 1) / kTapBlock;
+  const int ntb = (g.taps() + p->tb - 1) / p->tb;
   p->V = V;
   p->items = p->mode == 1 ? (g.G / V) * ntb : g.G * g.Kg * (g.Cg / V) * ntb;
   p->ipc = std::min(p->items, kBwwThreads);
@@ -309,6 +310,10 @@ void shape_bww(const Geometry& g, int V, BwwPlan* p) {
 BwwPlan plan_bww(const Geometry& g, int es, int vmax) {
   BwwPlan p{};
   p.mode = (g.Cg == 1 && g.Kg == 1) ? 1 : 0;
+  // taps per work item: one filter row (X taps) when that is at most 3,
+  // else up to kTapBlockMax; fewer registers per thread keep more warps
+  // resident to hide the load latency
+  p.tb = g.X <= 3 ? g.X : kTapBlockMax;
   auto widest = [&](int cap) {
     int V = cap;
     while (V > 1 && (p.mode == 1 ? g.G % V : g.Cg % V) != 0) V /= 2;
@@ -327,16 +332,25 @@ BwwPlan plan_bww(const Geometry& g, int es, int vmax) {
   return p;
 }
 
-template <typename T, int V, int MODE>
-cudaError_t launch_partial(const BwwArgs& a, const BwwPlan& p, const LaunchArgs& la, const DeviceInfo& dev) {
-  const size_t smem = p.lanes > 1 ? (size_t)kTapBlock * V * p.ipc * p.lanes * sizeof(float) : 0;
+template <typename T, int V, int MODE, int TB>
+cudaError_t launch_partial_tb(const BwwArgs& a, const BwwPlan& p, const LaunchArgs& la, const DeviceInfo& dev) {
+  const size_t smem = p.lanes > 1 ? (size_t)TB * V * p.ipc * p.lanes * sizeof(float) : 0;
   static SmemAttr attr;
   if (smem > 48 * 1024) {
-    cudaError_t e = attr.ensure(bwd_weight_partial_kernel<T, V, MODE>, dev.device, (int)smem);
+    cudaError_t e = attr.ensure(bwd_weight_partial_kernel<T, V, MODE, TB>, dev.device, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch_kernel(bwd_weight_partial_kernel<T, V, MODE>, dim3(p.ctas_per_split, p.S), dim3(kBwwThreads), smem,
-                       la, a);
+  return launch_kernel(bwd_weight_partial_kernel<T, V, MODE, TB>, dim3(p.ctas_per_split, p.S), dim3(kBwwThreads),
+                       smem, la, a);
+}
+template <typename T, int V, int MODE>
+cudaError_t launch_partial(const BwwArgs& a, const BwwPlan& p, const LaunchArgs& la, const DeviceInfo& dev) {
+  switch (p.tb) {
+    case 1: return launch_partial_tb<T, V, MODE, 1>(a, p, la, dev);
+    case 2: return launch_partial_tb<T, V, MODE, 2>(a, p, la, dev);
+    case 3: return launch_partial_tb<T, V, MODE, 3>(a, p, la, dev);
+    default: return launch_partial_tb<T, V, MODE, kTapBlockMax>(a, p, la, dev);
+  }
 }
 
 template <typename T>
@@ -357,7 +371,7 @@ cudaError_t bwd_weight_typed(const Geometry& g, const LaunchArgs& la, float* ws,
   a.sD = g.sD, a.sH = g.sH, a.sW = g.sW, a.pD = g.pD, a.pH = g.pH, a.pW = g.pW, a.dD = g.dD, a.dH = g.dH,
   a.dW = g.dW;
   a.taps = g.taps();
-  a.ntb = (a.taps + kTapBlock - 1) / kTapBlock;
+  a.ntb = (a.taps + p.tb - 1) / p.tb;
   a.P = g.N * (int64_t)g.Do * g.Ho * g.Wo;
   a.S = p.S;
   a.E = p.E;
