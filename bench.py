@@ -455,10 +455,13 @@ class GpuArm:
         if st != 0:
             raise RuntimeError(f"grouped_conv launch failed: {self.gc.gconv_last_error()}")
         c["kernel"] = self.opt.selected
-        # launches of the library's kernels this call made (the transposed-
-        # weights route of backward data adds the weight-flip kernel;
-        # backward weight is a partial kernel and a reduction)
-        c["kernels_per_call"] = 2 if (self.op == "bwd_weight" or (self.bwd and c.get("ws_bytes"))) else 1
+        # launches of the library's kernels this call made (backward data:
+        # as its route reports; backward weight: a partial kernel and a
+        # reduction)
+        if self.op == "bwd_data":
+            c["kernels_per_call"] = self.gc.grouped_conv_bwd_data_route(c["p"], c["dt"])[1]
+        else:
+            c["kernels_per_call"] = 2 if self.op == "bwd_weight" else 1
 
     def capture(self, n_units, launch_unit, per_graph=1000):
         """Graphs of back-to-back library calls (no event nodes inside: an

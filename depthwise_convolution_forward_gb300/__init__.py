@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     grouped_conv_bwd_data,
     grouped_conv_bwd_data_ex,
     grouped_conv_bwd_data_noalloc,
+    grouped_conv_bwd_data_route,
     grouped_conv_bwd_weight,
     grouped_conv_bwd_weight_ex,
     grouped_conv_bwd_weight_workspace_size,

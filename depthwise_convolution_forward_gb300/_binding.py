@@ -88,6 +88,8 @@ def load_library(path: Optional[str] = None):
                                                    ctypes.POINTER(gconv_options)]
         lib.grouped_conv_bwd_weight_workspace_size.restype = i32
         lib.grouped_conv_bwd_weight_workspace_size.argtypes = [prob_p, i32, ctypes.POINTER(i64)]
+        lib.grouped_conv_bwd_data_route.restype = i32
+        lib.grouped_conv_bwd_data_route.argtypes = [prob_p, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
         lib.grouped_conv_bwd_data_noalloc.restype = i32
         lib.grouped_conv_bwd_data_noalloc.argtypes = [vp, vp, vp, prob_p, i32, vp]
         lib.grouped_conv_bwd_data_workspace_size.restype = i32
@@ -221,6 +223,15 @@ def grouped_conv_bwd_data_ex(dy, w, dx, p: gconv_problem, dtype: int, workspace=
     _check(lib.grouped_conv_bwd_data_ex(_ptr(dy), _ptr(w), _ptr(dx), ctypes.byref(p), dtype, _ptr(workspace),
                                         workspace_bytes, _stream(stream), ctypes.byref(o)))
     return o
+
+
+def grouped_conv_bwd_data_route(p: gconv_problem, dtype: int) -> tuple:
+    """(route, launches) of grouped_conv_bwd_data: route 0 direct gather,
+    1 stride 1 with transposed flipped weights, 2 stride phases."""
+    lib = load_library()
+    r, n = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib.grouped_conv_bwd_data_route(ctypes.byref(p), dtype, ctypes.byref(r), ctypes.byref(n)))
+    return r.value, n.value
 
 
 def grouped_conv_bwd_weight_workspace_size(p: gconv_problem, dtype: int) -> int:

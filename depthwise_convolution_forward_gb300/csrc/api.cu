@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -243,9 +244,112 @@ bool bwd_as_forward(const Geometry& g, Geometry* fg) {
   return true;
 }
 
+// Stride phases of backward data along one dimension (dx extent I, dy
+// extent O, filter k, stride s, pad p, dilation d).  dx position s*i + r
+// receives dy[i + q] * w[t] for the taps t with r + p - t*d = s*q; in the
+// order of ascending q (descending t) those taps form a stride-1
+// correlation of dy with dilation q[1] - q[0] and left padding -q[0].  The
+// phase's forward problem gets symmetric padding `pad` large enough on both
+// sides, so its output row `off + i` is dx's phase row i.
+struct Phase1D {
+  int n;      // dx positions of the phase
+  int L;      // taps of the sub-filter
+  int t[kMaxPhaseTaps];
+  int dil, pad, out, off;
+  bool empty;  // no tap reaches the phase (or it has no positions)
+};
+
+bool phase_1d(int I, int O, int k, int s, int p, int d, int r, Phase1D* ph) {
+  Phase1D f{};
+  f.n = r < I ? (I - r + s - 1) / s : 0;
+  int q[kMaxPhaseTaps];
+  for (int t = k - 1; t >= 0; --t) {
+    const int v = r + p - t * d;
+    if (((v % s) + s) % s != 0) continue;
+    if (f.L == kMaxPhaseTaps) return false;
+    q[f.L] = v / s;
+    f.t[f.L++] = t;
+  }
+  f.empty = f.L == 0 || f.n == 0;
+  if (f.empty) {
+    f.L = 1, f.t[0] = 0, f.dil = 1, f.pad = 0, f.out = 1, f.off = 0;
+    *ph = f;
+    return true;
+  }
+  f.dil = f.L >= 2 ? q[1] - q[0] : 1;
+  for (int j = 1; j < f.L; ++j)
+    if (q[j] - q[j - 1] != f.dil) return false;
+  const int qmin = q[0], qmax = q[f.L - 1];
+  f.pad = std::max(0, std::max(-qmin, f.n - O + qmax));
+  f.out = O + 2 * f.pad - (qmax - qmin);
+  f.off = f.pad + qmin;
+  if (f.off < 0 || f.off + f.n > f.out) return false;
+  *ph = f;
+  return true;
+}
+
+// The three dimensions of phase (rD, rH, rW); fg = its forward problem
+// (valid when not empty).
+struct Phase3D {
+  Phase1D d[3];
+  bool empty;
+  Geometry fg;
+};
+
+bool phase_3d(const Geometry& g, int rd, int rh, int rw, Phase3D* ph) {
+  const int I[3] = {g.D, g.H, g.W}, O[3] = {g.Do, g.Ho, g.Wo}, k[3] = {g.Z, g.Y, g.X},
+            st[3] = {g.sD, g.sH, g.sW}, pd[3] = {g.pD, g.pH, g.pW}, dl[3] = {g.dD, g.dH, g.dW};
+  const int r[3] = {rd, rh, rw};
+  ph->empty = false;
+  for (int i = 0; i < 3; ++i) {
+    if (!phase_1d(I[i], O[i], k[i], st[i], pd[i], dl[i], r[i], &ph->d[i])) return false;
+    ph->empty = ph->empty || ph->d[i].empty;
+  }
+  Geometry f = g;
+  f.Cg = g.Kg, f.Kg = g.Cg;
+  f.D = g.Do, f.H = g.Ho, f.W = g.Wo;
+  f.Z = ph->d[0].L, f.Y = ph->d[1].L, f.X = ph->d[2].L;
+  f.sD = f.sH = f.sW = 1;
+  f.pD = ph->d[0].pad, f.pH = ph->d[1].pad, f.pW = ph->d[2].pad;
+  f.dD = ph->d[0].dil, f.dH = ph->d[1].dil, f.dW = ph->d[2].dil;
+  f.Do = ph->d[0].out, f.Ho = ph->d[1].out, f.Wo = ph->d[2].out;
+  ph->fg = f;
+  return true;
+}
+
+// The stride-phase route: a stride above 1 somewhere, grouped channels (the
+// depthwise case stays on the direct kernel's group vectors), 16-bit data,
+// and every phase's forward problem planned on the tensor-core kernel (on a
+// GB300's SM count and shared memory, so the decision, and the workspace
+// size, depend on the problem only).  *pb_bytes: the largest phase buffer.
+bool phase_route(const Geometry& g, DType dt, int64_t* pb_bytes) {
+  if (g.sD == 1 && g.sH == 1 && g.sW == 1) return false;
+  if (dt == kF32 || (g.Cg == 1 && g.Kg == 1)) return false;
+  int64_t pb = 0;
+  for (int rd = 0; rd < g.sD; ++rd)
+    for (int rh = 0; rh < g.sH; ++rh)
+      for (int rw = 0; rw < g.sW; ++rw) {
+        Phase3D ph;
+        if (!phase_3d(g, rd, rh, rw, &ph)) return false;
+        if (ph.empty) continue;
+        if (!tc_supported(ph.fg, dt, nullptr, kDefaultSms, kDefaultSmemOptin)) return false;
+        pb = std::max(pb, ph.fg.y_elems() * dtype_bytes(dt));
+      }
+  if (pb_bytes) *pb_bytes = pb;
+  return true;
+}
+
+inline int64_t align256(int64_t v) { return (v + 255) / 256 * 256; }
+
+// Workspace of backward data: the transposed, flipped weights of the
+// stride-1 route; the phase route's sub-filter weights (at most w's size)
+// and its largest phase buffer; nothing for the direct kernel.
 int64_t bwd_workspace_bytes(const Geometry& g, DType dt) {
   Geometry f;
-  return bwd_as_forward(g, &f) ? g.w_elems() * dtype_bytes(dt) : 0;
+  if (bwd_as_forward(g, &f)) return g.w_elems() * dtype_bytes(dt);
+  int64_t pb = 0;
+  if (phase_route(g, dt, &pb)) return align256(g.w_elems() * dtype_bytes(dt)) + pb;
+  return 0;
 }
 
 }  // namespace
@@ -359,9 +463,12 @@ gconv_status grouped_conv_bwd_data_ex(const void* dy, const void* w, void* dx, c
   const int forced = opt ? opt->force_kernel : 0;
   Geometry fg;
   const bool as_fwd = forced != GCONV_KERNEL_BWD_DATA_DIRECT && bwd_as_forward(g, &fg);
-  if (forced != 0 && forced != GCONV_KERNEL_BWD_DATA_DIRECT && !as_fwd)
-    return fail(GCONV_ERR_UNSUPPORTED, "kernel %d needs stride 1 and pad <= dil*(k-1)", forced);
-  const int64_t need = as_fwd ? g.w_elems() * es : 0;
+  int64_t pb_bytes = 0;
+  const bool phases = !as_fwd && forced != GCONV_KERNEL_BWD_DATA_DIRECT && phase_route(g, t, &pb_bytes);
+  if (forced != 0 && forced != GCONV_KERNEL_BWD_DATA_DIRECT && !as_fwd && !phases)
+    return fail(GCONV_ERR_UNSUPPORTED, "kernel %d needs a forward-kernel route (stride 1 with pad <= dil*(k-1), "
+                "or stride phases of grouped 16-bit data)", forced);
+  const int64_t need = as_fwd ? g.w_elems() * es : (phases ? align256(g.w_elems() * es) + pb_bytes : 0);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15)))
     return fail(GCONV_ERR_INVALID_ARG, "workspace must be 16-byte aligned and hold %lld bytes",
                 (long long)need);
@@ -384,6 +491,46 @@ gconv_status grouped_conv_bwd_data_ex(const void* dy, const void* w, void* dx, c
     if (s != GCONV_OK) return s;
     return finish(slot, a, opt);
   }
+  if (phases) {
+    // per stride phase: its sub-filter (transposed channels) into the
+    // workspace, its stride-1 forward correlation of dy into the phase
+    // buffer, then the buffer's rows to the phase's dx positions
+    uint8_t* wt = static_cast<uint8_t*>(workspace);
+    uint8_t* pb = wt + align256(g.w_elems() * es);
+    LaunchArgs a = make_args(dy, w, nullptr, dx, t, stream, slot, opt);
+    for (int rd = 0; rd < g.sD; ++rd)
+      for (int rh = 0; rh < g.sH; ++rh)
+        for (int rw = 0; rw < g.sW; ++rw) {
+          Phase3D ph;
+          if (!phase_3d(g, rd, rh, rw, &ph)) return fail(GCONV_ERR_UNSUPPORTED, "stride phase not decomposable");
+          PhaseScatter ps{};
+          ps.N = g.N;
+          ps.C = g.C();
+          const int I3[3] = {g.D, g.H, g.W}, s3[3] = {g.sD, g.sH, g.sW}, r3[3] = {rd, rh, rw};
+          for (int i = 0; i < 3; ++i) {
+            ps.in[i] = I3[i], ps.s[i] = s3[i], ps.r[i] = r3[i];
+            ps.n[i] = ph.d[i].n, ps.o[i] = ph.d[i].out, ps.off[i] = ph.d[i].off;
+          }
+          ps.empty = ph.empty ? 1 : 0;
+          if (ps.n[0] == 0 || ps.n[1] == 0 || ps.n[2] == 0) continue;  // no dx positions in this phase
+          if (!ph.empty) {
+            PhaseTaps pt{};
+            for (int i = 0; i < 3; ++i) {
+              pt.L[i] = ph.d[i].L;
+              for (int j = 0; j < ph.d[i].L; ++j) pt.t[i][j] = ph.d[i].t[j];
+            }
+            LaunchArgs wa = make_args(dy, w, nullptr, wt, t, stream, slot, opt);
+            e = phase_weight_launch(g, wa, pt, wt, slot->info);
+            if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+            LaunchArgs fa = make_args(dy, wt, nullptr, pb, t, stream, slot, opt);
+            s = launch_forward(ph.fg, fa, slot->info, forced, opt ? &opt->selected : nullptr);
+            if (s != GCONV_OK) return s;
+          }
+          e = phase_scatter_launch(ps, pb, dx, a, slot->info);
+          if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+        }
+    return finish(slot, a, opt);
+  }
   LaunchArgs a = make_args(dy, w, nullptr, dx, t, stream, slot, opt);
   e = bwd_data_direct_launch(g, a, slot->info);
   if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
@@ -394,6 +541,32 @@ gconv_status grouped_conv_bwd_data_ex(const void* dy, const void* w, void* dx, c
 gconv_status grouped_conv_bwd_data(const void* dy, const void* w, void* dx, const gconv_problem* p, gconv_dtype dt,
                                    void* workspace, int64_t workspace_bytes, struct CUstream_st* stream) {
   return grouped_conv_bwd_data_ex(dy, w, dx, p, dt, workspace, workspace_bytes, stream, nullptr);
+}
+
+gconv_status grouped_conv_bwd_data_route(const gconv_problem* p, gconv_dtype dt, int32_t* route, int32_t* launches) {
+  Geometry g;
+  gconv_status s = validate(p, &g);
+  if (s != GCONV_OK) return s;
+  if (dt != GCONV_F32 && dt != GCONV_F16 && dt != GCONV_BF16) return fail(GCONV_ERR_UNSUPPORTED, "unknown dtype %d", (int)dt);
+  if (route == nullptr) return fail(GCONV_ERR_INVALID_ARG, "route pointer is NULL");
+  Geometry f;
+  int r = 0, n = 1;
+  if (bwd_as_forward(g, &f)) {
+    r = 1, n = 2;
+  } else if (phase_route(g, (DType)dt, nullptr)) {
+    r = 2, n = 0;
+    for (int rd = 0; rd < g.sD; ++rd)
+      for (int rh = 0; rh < g.sH; ++rh)
+        for (int rw = 0; rw < g.sW; ++rw) {
+          Phase3D ph;
+          phase_3d(g, rd, rh, rw, &ph);
+          if (ph.d[0].n == 0 || ph.d[1].n == 0 || ph.d[2].n == 0) continue;
+          n += ph.empty ? 1 : 3;
+        }
+  }
+  *route = r;
+  if (launches) *launches = n;
+  return GCONV_OK;
 }
 
 gconv_status grouped_conv_bwd_weight_workspace_size(const gconv_problem* p, gconv_dtype dt, int64_t* bytes) {

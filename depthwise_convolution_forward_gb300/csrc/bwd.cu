@@ -6,12 +6,19 @@
 // listed by the pages' CK grouped-convolution tile engine and its Python
 // examples; the arithmetic is that adjoint.
 //
-// Two routes (chosen in api.cu):
+// Three routes (chosen in api.cu):
 //  - stride 1 and pad <= d*(k-1) in every dimension: dx is the forward
 //    convolution of dy with per-group transposed, spatially flipped weights
 //    wt[g, c, t', k] = w[g, k, flip(t'), c] and padding d*(k-1) - p, so the
 //    forward kernels (depthwise, tensor-core, generic) run it after
 //    weight_flip_kernel has written wt into the caller's workspace;
+//  - stride > 1 with grouped channels: dx is cut into its stride phases
+//    (dx positions i = s*i' + r per dimension).  Phase r receives only the
+//    taps t with (r + p - t*d) divisible by s, at dy offset
+//    q = (r + p - t*d) / s, so it is a stride-1 forward correlation of dy
+//    with that sub-filter (taps in ascending q, transposed channels) into a
+//    phase buffer, which phase_scatter_kernel writes to dx's positions of
+//    the phase (phases without taps write zeros);
 //  - otherwise a direct kernel gathers, for each dx element, the outputs
 //    whose windows cover it (fp32 accumulation, one rounding):
 //    bwd_data_vec_kernel handles 16 bytes of channels per thread where they
@@ -200,6 +207,68 @@ __global__ void __launch_bounds__(256) bwd_data_vec_kernel(const BwdArgs a) {
   }
 }
 
+// Phase route, weights: wt[g][c][jd][jh][jw][k] = w[g][k][td[jd]][th[jh]][tw[jw]][c]
+// for the sub-filter of one stride phase (its taps in the order the phase's
+// forward correlation reads them).
+template <typename T>
+__global__ void __launch_bounds__(256) phase_weight_kernel(const T* __restrict__ w, T* __restrict__ wt,
+                                                           const PhaseTaps pt, int64_t total, int Kg, int Cg, int Z,
+                                                           int Y, int X) {
+  grid_dependency_wait();  // w and the workspace are touched only from here on
+  for (int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; o < total; o += (int64_t)gridDim.x * blockDim.x) {
+    int64_t f = o;
+    const int k = (int)(f % Kg);
+    f /= Kg;
+    const int jw = (int)(f % pt.L[2]);
+    f /= pt.L[2];
+    const int jh = (int)(f % pt.L[1]);
+    f /= pt.L[1];
+    const int jd = (int)(f % pt.L[0]);
+    f /= pt.L[0];
+    const int c = (int)(f % Cg);
+    const int64_t g = f / Cg;
+    wt[o] = w[((((g * Kg + k) * Z + pt.t[0][jd]) * Y + pt.t[1][jh]) * (int64_t)X + pt.t[2][jw]) * Cg + c];
+  }
+}
+
+// Phase route, output: dx[n][sD*i + rD][sH*j + rH][sW*l + rW][:] =
+// pb[n][i + oD][j + oH][l + oW][:] for the phase's (i, j, l) < (nD, nH, nW),
+// or 0 when the phase has no taps.  V elements (16 or fewer bytes) per
+// thread.
+template <typename T, int V>
+__global__ void __launch_bounds__(256) phase_scatter_kernel(const T* __restrict__ pb, T* __restrict__ dx,
+                                                            const PhaseScatter ps) {
+  grid_dependency_wait();  // the phase buffer is complete; dx is touched only from here on
+  const int64_t cv = ps.C / V;
+  const int64_t total = ps.N * ps.n[0] * ps.n[1] * ps.n[2] * cv;
+  for (int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; o < total; o += (int64_t)gridDim.x * blockDim.x) {
+    int64_t f = o;
+    const int64_t c = (f % cv) * V;
+    f /= cv;
+    const int l = (int)(f % ps.n[2]);
+    f /= ps.n[2];
+    const int j = (int)(f % ps.n[1]);
+    f /= ps.n[1];
+    const int i = (int)(f % ps.n[0]);
+    const int64_t n = f / ps.n[0];
+    T* d = dx + (((n * ps.in[0] + (int64_t)ps.s[0] * i + ps.r[0]) * ps.in[1] + (int64_t)ps.s[1] * j + ps.r[1]) *
+                     ps.in[2] + (int64_t)ps.s[2] * l + ps.r[2]) * ps.C + c;
+    if (ps.empty) {
+#pragma unroll
+      for (int v = 0; v < V; ++v) d[v] = Elem<T>::from_f32(0.f);
+      continue;
+    }
+    const T* src = pb + (((n * ps.o[0] + i + ps.off[0]) * ps.o[1] + j + ps.off[1]) * (int64_t)ps.o[2] + l + ps.off[2]) *
+                            ps.C + c;
+    if constexpr (V * sizeof(T) == 16) {
+      *reinterpret_cast<uint4*>(d) = *reinterpret_cast<const uint4*>(src);
+    } else {
+#pragma unroll
+      for (int v = 0; v < V; ++v) d[v] = src[v];
+    }
+  }
+}
+
 int grid_blocks(int64_t total, const DeviceInfo& dev) {
   const int64_t blocks = (total + 255) / 256;
   return (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)dev.num_sms * 16));
@@ -273,6 +342,43 @@ cudaError_t bwd_data_direct_launch(const Geometry& g, const LaunchArgs& a, const
     case kBF16: GCONV_BWD_ONE(__nv_bfloat16)
   }
 #undef GCONV_BWD_ONE
+  return cudaErrorNotSupported;
+}
+
+cudaError_t phase_weight_launch(const Geometry& g, const LaunchArgs& a, const PhaseTaps& pt, void* wt,
+                                const DeviceInfo& dev) {
+  const int64_t total = (int64_t)g.G * g.Cg * pt.L[0] * pt.L[1] * pt.L[2] * g.Kg;
+  const dim3 grid(grid_blocks(total, dev)), block(256);
+  switch (a.dt) {
+    case kF32:
+      return launch_kernel(phase_weight_kernel<float>, grid, block, 0, a, static_cast<const float*>(a.w),
+                           static_cast<float*>(wt), pt, total, g.Kg, g.Cg, g.Z, g.Y, g.X);
+    case kF16:
+      return launch_kernel(phase_weight_kernel<__half>, grid, block, 0, a, static_cast<const __half*>(a.w),
+                           static_cast<__half*>(wt), pt, total, g.Kg, g.Cg, g.Z, g.Y, g.X);
+    case kBF16:
+      return launch_kernel(phase_weight_kernel<__nv_bfloat16>, grid, block, 0, a,
+                           static_cast<const __nv_bfloat16*>(a.w), static_cast<__nv_bfloat16*>(wt), pt, total, g.Kg,
+                           g.Cg, g.Z, g.Y, g.X);
+  }
+  return cudaErrorNotSupported;
+}
+
+cudaError_t phase_scatter_launch(const PhaseScatter& ps, const void* pb, void* dx, const LaunchArgs& a,
+                                 const DeviceInfo& dev) {
+  const int es = dtype_bytes(a.dt);
+  const bool v16 = (ps.C * es) % 16 == 0 &&
+                   ((reinterpret_cast<uintptr_t>(pb) | reinterpret_cast<uintptr_t>(dx)) & 15) == 0;
+  const int V = v16 ? 16 / es : 1;
+  const int64_t total = ps.N * ps.n[0] * ps.n[1] * ps.n[2] * (ps.C / V);
+  const dim3 grid(grid_blocks(total, dev)), block(256);
+#define GCONV_SCATTER(TT)                                                                                          return v16 ? launch_kernel(phase_scatter_kernel<TT, 16 / sizeof(TT)>, grid, block, 0, a,                                                    static_cast<const TT*>(pb), static_cast<TT*>(dx), ps)                                           : launch_kernel(phase_scatter_kernel<TT, 1>, grid, block, 0, a, static_cast<const TT*>(pb),                                       static_cast<TT*>(dx), ps);
+  switch (a.dt) {
+    case kF32: GCONV_SCATTER(float)
+    case kF16: GCONV_SCATTER(__half)
+    case kBF16: GCONV_SCATTER(__nv_bfloat16)
+  }
+#undef GCONV_SCATTER
   return cudaErrorNotSupported;
 }
 

@@ -109,6 +109,31 @@ cudaError_t bwd_weight_flip_launch(const Geometry& g, const LaunchArgs& a, void*
 // Direct gather: a.x carries dy, a.w the forward weights, a.y receives dx.
 cudaError_t bwd_data_direct_launch(const Geometry& g, const LaunchArgs& a, const DeviceInfo& dev);
 
+// Stride-phase route of backward data.  One phase per (rD, rH, rW): its
+// sub-filter taps per dimension (original tap indices in the order the
+// phase's correlation reads them), and where its rows land in dx.
+constexpr int kMaxPhaseTaps = 16;
+struct PhaseTaps {
+  int L[3];                    // sub-filter extent per dimension
+  int t[3][kMaxPhaseTaps];     // original tap index of sub-filter position j
+};
+struct PhaseScatter {
+  int64_t N;
+  int64_t C;                   // channels per pixel of dx (and of the phase buffer)
+  int in[3];                   // dx extents D, H, W
+  int s[3], r[3];              // stride and phase per dimension
+  int n[3];                    // phase extents: dx positions with index % s == r
+  int o[3], off[3];            // phase buffer extents and the offset of the phase's first position
+  int empty;                   // 1: no tap reaches this phase (write zeros)
+};
+// wt = the phase's sub-filter of w with channels transposed, [G][Cg][L..][Kg];
+// a.w is w.
+cudaError_t phase_weight_launch(const Geometry& g, const LaunchArgs& a, const PhaseTaps& pt, void* wt,
+                                const DeviceInfo& dev);
+// dx positions of one phase from the phase buffer pb (or zeros).
+cudaError_t phase_scatter_launch(const PhaseScatter& ps, const void* pb, void* dx, const LaunchArgs& a,
+                                 const DeviceInfo& dev);
+
 // ---- backward weight -------------------------------------------------------
 // fp32 partials of dw for a fixed number of pixel splits, then one reduction
 // and rounding.  a.x carries x, a.w carries dy, a.y receives dw; the

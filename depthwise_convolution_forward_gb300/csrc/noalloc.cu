@@ -71,6 +71,14 @@ extern "C" gconv_status grouped_conv_bwd_data_noalloc(const void* dy, const void
   int64_t need = 0;
   gconv_status s = grouped_conv_bwd_data_workspace_size(p, dt, &need);
   if (s != GCONV_OK) return s;
+  if (need > (int64_t)GCONV_NOALLOC_SCRATCH_BYTES && p != nullptr &&
+      (p->stride[0] > 1 || p->stride[1] > 1 || p->stride[2] > 1)) {
+    // the stride-phase route would need more scratch than the array holds;
+    // the direct gather kernel computes the same result with none
+    gconv_options o{};
+    o.force_kernel = GCONV_KERNEL_BWD_DATA_DIRECT;
+    return grouped_conv_bwd_data_ex(dy, w, dx, p, dt, nullptr, 0, stream, &o);
+  }
   if (need > (int64_t)GCONV_NOALLOC_SCRATCH_BYTES)
     return set_last_error(GCONV_ERR_UNSUPPORTED,
                           "grouped_conv_bwd_data_noalloc: this problem needs %lld bytes of scratch, more than the "

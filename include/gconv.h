@@ -190,11 +190,20 @@ gconv_status grouped_conv_fwd_ex(const void *x, const void *w, const void *bias,
  *        grouped_conv_bwd_data_workspace_size() bytes, 16-byte aligned; NULL
  *        when that size is 0.  Owned by the caller; the call uses it until the
  *        stream passes the launch.
- * Stride 1 with pad <= dil*(k-1) in every dimension runs as a forward
- * convolution of dy with per-group transposed, flipped weights (written into
- * the workspace) and padding dil*(k-1) - pad, on the forward kernels; other
- * problems run a direct gather kernel and need no workspace.  fp32
- * accumulation, one round-to-nearest-even cast.  Asynchronous on `stream`.
+ * Three routes (grouped_conv_bwd_data_route tells which):
+ *   1. stride 1 with pad <= dil*(k-1) in every dimension: a forward
+ *      convolution of dy with per-group transposed, flipped weights (written
+ *      into the workspace) and padding dil*(k-1) - pad, on the forward
+ *      kernels;
+ *   2. a stride above 1 with grouped channels (not depthwise) in f16/bf16,
+ *      when every stride phase plans on the tensor-core kernel: dx is cut
+ *      into its stride phases (positions s*i + r per dimension); each phase
+ *      is a stride-1 forward correlation of dy with the sub-filter of taps t
+ *      that reach it (r + p - t*d divisible by s), computed into a phase
+ *      buffer in the workspace and copied to the phase's dx positions;
+ *   0. otherwise a direct gather kernel, which needs no workspace.
+ * fp32 accumulation, one round-to-nearest-even cast.  Asynchronous on
+ * `stream`.
  * Errors: as grouped_conv_fwd, plus GCONV_ERR_INVALID_ARG for a workspace that
  * is missing, too small or misaligned.
  */
@@ -206,13 +215,23 @@ gconv_status grouped_conv_bwd_data(const void *dy, const void *w, void *dx, cons
  * grouped_conv_bwd_data_ex -- grouped_conv_bwd_data with options.
  * opt->force_kernel: GCONV_KERNEL_BWD_DATA_DIRECT forces the direct gather
  * kernel; GCONV_KERNEL_DIRECT_DW / _DIRECT_GENERIC / _IGEMM_TC force the
- * forward kernel of the transposed-weights route (stride-1 problems only,
- * else GCONV_ERR_UNSUPPORTED).  opt->selected reports the kernel used.
+ * forward kernel of routes 1 and 2 (GCONV_ERR_UNSUPPORTED for a problem of
+ * route 0, or when the forced kernel cannot run a phase).  opt->selected
+ * reports the kernel used (for route 2, that of the last phase).
  * Other fields as for grouped_conv_fwd_ex.
  */
 gconv_status grouped_conv_bwd_data_ex(const void *dy, const void *w, void *dx, const gconv_problem *p,
                                       gconv_dtype dt, void *workspace, int64_t workspace_bytes,
                                       struct CUstream_st *stream, gconv_options *opt);
+
+/*
+ * grouped_conv_bwd_data_route -- which route grouped_conv_bwd_data takes for
+ * (p, dt) without a forced kernel: *route = 0 (direct gather), 1 (stride 1,
+ * transposed flipped weights) or 2 (stride phases), and, if `launches` is
+ * not NULL, how many kernels the call launches.  Host only, no GPU needed;
+ * depends on the problem only.
+ */
+gconv_status grouped_conv_bwd_data_route(const gconv_problem *p, gconv_dtype dt, int32_t *route, int32_t *launches);
 
 /*
  * grouped_conv_bwd_data_workspace_size -- device workspace bytes that
@@ -283,8 +302,10 @@ gconv_status grouped_conv_bwd_weight_workspace_size(const gconv_problem *p, gcon
  * own static device memory, which every GPU that loads the library holds
  * until the process exits.  Nothing is allocated and nothing is freed.
  *   - A problem whose scratch would exceed GCONV_NOALLOC_SCRATCH_BYTES
- *     returns GCONV_ERR_UNSUPPORTED without launching anything
- *     (grouped_conv_bwd_data_workspace_size gives the size it needs).
+ *     runs on the direct gather kernel (which needs none) when it has a
+ *     stride above 1, and otherwise returns GCONV_ERR_UNSUPPORTED without
+ *     launching anything (grouped_conv_bwd_data_workspace_size gives the
+ *     size a problem needs).
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before
  *     any stream capture.

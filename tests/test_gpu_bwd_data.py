@@ -65,13 +65,19 @@ def _reduced(wl):
 
 FAMILY = ["mbv2_dw_s1_f16", "mbv2_dw_s2_f16", "resnext_a_bf16", "resnext_b_bf16", "resnext3d_n1_f16",
           "grouped2d_f32_smoke", "sweep_g8_d2_s1_bf16", "sweep_g64_d1_s1_bf16", "sweep_g256_d2_s2_bf16",
-          "sweep_g512_d2_s1_bf16"]
+          "sweep_g512_d2_s1_bf16", "sweep_g8_d1_s2_bf16", "sweep_g32_d1_s2_bf16", "sweep_g64_d2_s2_bf16",
+          "sweep_g512_d1_s2_bf16"]
 
 
 def _expected_route(wl):
+    """The route the library reports (0 direct gather, 1 stride-1
+    transposed weights, 2 stride phases); stride-1 problems with
+    pad <= dil*(k-1) always take route 1."""
+    route, _ = gc.grouped_conv_bwd_data_route(gc.problem_of(wl), gc.DTYPE_CODES[wl.dtype])
     stride1 = all(s == 1 for s in wl.stride)
     fits = all(p <= d * (k - 1) for p, d, k in zip(wl.pad, wl.dil, wl.ker))
-    return stride1 and fits
+    assert (route == 1) == (stride1 and fits)
+    return route
 
 
 @pytest.mark.parametrize("name", FAMILY)
@@ -80,8 +86,9 @@ def test_reduced_batch_full_compare(orc, name):
     _, w, _ = inputs.make_inputs(wl)
     dy = make_dy(wl, 9000 + wl.cfg * 10 + wl.variant)
     dx, sel, need = run_bwd(wl, dy, w)
-    assert (sel != B.KERNEL_BWD_DATA_DIRECT) == _expected_route(wl), (name, sel)
-    assert (need > 0) == _expected_route(wl)
+    route = _expected_route(wl)
+    assert (sel != B.KERNEL_BWD_DATA_DIRECT) == (route != 0), (name, sel)
+    assert (need > 0) == (route != 0)
     assert_close(dx.double().numpy(), orc.bwd_data(wl, dy, w), wl.dtype, f"{name} (kernel {sel})")
 
 
@@ -115,3 +122,42 @@ def test_random_small_problems(orc, seed):
     dy = make_dy(wl, 9300 + seed)
     dx, sel, _ = run_bwd(wl, dy, w)
     assert_close(dx.double().numpy(), orc.bwd_data(wl, dy, w), wl.dtype, f"{wl} (kernel {sel})")
+
+
+PHASE_CASES = [
+    # (name, workload): grouped stride-2 problems on the stride-phase route
+    inputs.by_name("resnext_b_bf16").with_(N=2, bias=False),
+    inputs.by_name("sweep_g256_d2_s2_bf16").with_(N=2, bias=False),
+    # odd extents and no padding: phases of unequal size and empty edges
+    inputs.Workload("ph_odd", 9, 1, 2, 2, 4, 16, 16, (1, 13, 11), (1, 3, 3), (1, 2, 2), (0, 0, 0), (1, 1, 1),
+                    "bf16", False),
+    # 5x5 filter, pad 2, f16
+    inputs.Workload("ph_k5", 9, 2, 2, 1, 2, 16, 32, (1, 12, 10), (1, 5, 5), (1, 2, 2), (0, 2, 2), (1, 1, 1),
+                    "f16", False),
+    # dilation 2 with stride 2 (half the phases get no taps), pad 1
+    inputs.Workload("ph_d2", 9, 3, 2, 2, 4, 16, 16, (1, 12, 12), (1, 3, 3), (1, 2, 2), (0, 1, 1), (1, 2, 2),
+                    "bf16", False),
+    # stride 2 in H only, stride 3 in W
+    inputs.Workload("ph_s23", 9, 4, 2, 1, 2, 32, 16, (1, 11, 14), (1, 3, 3), (1, 2, 3), (0, 1, 1), (1, 1, 1),
+                    "bf16", False),
+    # 3D stride 2 in every dimension
+    inputs.Workload("ph_3d", 9, 5, 3, 1, 4, 16, 16, (7, 9, 8), (3, 3, 3), (2, 2, 2), (1, 1, 1), (1, 1, 1),
+                    "f16", False),
+]
+
+
+@pytest.mark.parametrize("wl", PHASE_CASES, ids=lambda w: w.name)
+def test_stride_phase_route(orc, wl):
+    """Stride-phase route (forward kernels on the phase sub-filters, then a
+    scatter into dx) against the oracle and against the direct kernel."""
+    route, launches = gc.grouped_conv_bwd_data_route(gc.problem_of(wl), gc.DTYPE_CODES[wl.dtype])
+    assert route == 2 and launches >= 2, (route, launches)
+    _, w, _ = inputs.make_inputs(wl)
+    dy = make_dy(wl, 9400 + wl.variant)
+    ref = orc.bwd_data(wl, dy, w)
+    dx, sel, need = run_bwd(wl, dy, w)
+    assert need > 0 and sel != B.KERNEL_BWD_DATA_DIRECT
+    assert_close(dx.double().numpy(), ref, wl.dtype, f"{wl.name} phases (kernel {sel})")
+    dx2, sel2, _ = run_bwd(wl, dy, w, B.KERNEL_BWD_DATA_DIRECT)
+    assert sel2 == B.KERNEL_BWD_DATA_DIRECT
+    assert_close(dx2.double().numpy(), ref, wl.dtype, f"{wl.name} direct")
