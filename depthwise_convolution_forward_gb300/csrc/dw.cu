@@ -14,15 +14,18 @@ int dw_col_regs_f32(int S, int DL, int form);
 int dw_col_regs_f16(int S, int DL, int form);
 int dw_col_regs_bf16(int S, int DL, int form);
 
-// Depthwise (Cg == Kg == 1), 3x3 spatial filter, equal H/W stride and
-// dilation in {1, 2}; channels a multiple of one 16-byte vector; x and y
-// 16-byte aligned (TMA and vector-store requirements).  Any depth filter, as
-// long as the planner finds a tile that fits shared memory for this device's
-// SM count (num_sms).
+// Depthwise (Cg == Kg == 1), or groups of two channels (Cg == Kg == 2,
+// 16-bit data, depth filter 1: the column form's two-channel dot products),
+// 3x3 spatial filter, equal H/W stride and dilation in {1, 2}; channels a
+// multiple of one 16-byte vector; x and y 16-byte aligned (TMA and
+// vector-store requirements).  Any depth filter for depthwise, as long as
+// the planner finds a tile that fits shared memory for this device's SM
+// count (num_sms).
 bool dw_supported(const Geometry& g, DType dt, const LaunchArgs* a, int num_sms) {
   const int es = dtype_bytes(dt);
   const int vec = 16 / es;
-  if (g.Cg != 1 || g.Kg != 1) return false;
+  const bool group2 = g.Cg == 2 && g.Kg == 2 && es == 2 && g.Z == 1;
+  if (!((g.Cg == 1 && g.Kg == 1) || group2)) return false;
   if (g.Y != 3 || g.X != 3) return false;
   if (g.sH != g.sW || g.dH != g.dW) return false;
   if (g.sH < 1 || g.sH > 2 || g.dH < 1 || g.dH > 2) return false;
@@ -32,7 +35,7 @@ bool dw_supported(const Geometry& g, DType dt, const LaunchArgs* a, int num_sms)
   // the image index is a 32-bit tensor-map coordinate (element offsets are 64-bit)
   if (g.N >= (int64_t)1 << 31) return false;
   // all weights stay resident in shared memory (fp32 copy, at most 64 KB)
-  if ((int64_t)g.taps() * g.C() * 4 > 64 * 1024) return false;
+  if ((int64_t)g.taps() * g.C() * g.Cg * 4 > 64 * 1024) return false;
   if (a) {
     if ((reinterpret_cast<uintptr_t>(a->x) & 15) || (reinterpret_cast<uintptr_t>(a->y) & 15)) return false;
   }
@@ -53,7 +56,7 @@ bool dw_supported(const Geometry& g, DType dt, const LaunchArgs* a, int num_sms)
   // With launch arguments a device is at hand: plan with the column kernel's
   // real register count, as the launch does (tile overrides may need it);
   // the host-only query plans with the most it can have.
-  const int form = dw::col_form(es, a ? a->tile : nullptr);
+  const int form = dw::col_form(es, a ? a->tile : nullptr, g.Cg);
   int regs = dw::col_max_regs(form);
   if (a && g.Z == 1) {
     const int r = dt == kF32 ? dw_col_regs_f32(g.sH, g.dH, form)

@@ -138,7 +138,8 @@ inline bool make_plan(const Geometry& g, int es, const int* tile_override, int n
 // scalar fp32, 2 packed 16-bit x4, 3 widened fp32x2, 4 packed 16-bit x8;
 // automatic: packed x4 for 16-bit storage (as fast as the others and the
 // fewest registers), scalar for fp32.
-inline int col_form(int es, const int* ov) {
+inline int col_form(int es, const int* ov, int cg = 1) {
+  if (cg == 2) return kColGroup2;  // groups of two channels have one form
   const int ov_form = ov ? ov[5] : 0;
   int form = es == 2 ? kColPacked : kColSplit;
   if (ov_form == 1) form = kColSplit;
@@ -258,9 +259,9 @@ inline int col_max_regs(int form) { return 65536 / col_max_threads(form) / 8 * 8
 inline bool plannable(const Geometry& g, int es, const int* ov, int num_sms, int regs) {
   Plan p;
   const int kind = ov ? ov[6] : 0;
-  const int form = col_form(es, ov);
+  const int form = col_form(es, ov, g.Cg);
   if ((kind == 0 || kind == 3) && g.Z == 1 && make_col_plan(g, es, ov, num_sms, form, regs, &p)) return true;
-  if (kind == 3) return false;
+  if (kind == 3 || g.Cg != 1) return false;  // groups of two channels: column form only
   return make_plan(g, es, ov, num_sms, &p);
 }
 
@@ -304,6 +305,9 @@ DwKernel<T> pick_col_kernel(int S, int DL, int form) {
     if constexpr (sizeof(T) == 2) {                                                 \
       if (form == kColPacked) return dw_col_kernel<T, s_, d_, kColPacked>;          \
       if (form == kColPacked8) return dw_col_kernel<T, s_, d_, kColPacked8>;        \
+      if (form == kColGroup2) return dw_col_kernel<T, s_, d_, kColGroup2>;          \
+    } else {                                                                        \
+      if (form == kColGroup2) return nullptr;                                       \
     }                                                                               \
     if (form == kColWide) return dw_col_kernel<T, s_, d_, kColWide>;                \
     return dw_col_kernel<T, s_, d_, kColSplit>;                                     \
@@ -375,7 +379,7 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
     const int kind = la.tile[6];
     bool planned = false;
     if ((kind == 0 || kind == 3) && g.Z == 1) {
-      const int form = col_form(es, la.tile);
+      const int form = col_form(es, la.tile, g.Cg);
       DwKernel<T> k = pick_col_kernel<T>(g.sH, g.dH, form);
       cudaFuncAttributes fa{};
       if (k == nullptr) return cudaErrorNotSupported;
@@ -383,7 +387,7 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
       if (e != cudaSuccess) return e;
       planned = make_col_plan(g, es, la.tile, dev.num_sms, form, fa.numRegs, &p);
     }
-    if (!planned && kind != 3) planned = make_plan(g, es, la.tile, dev.num_sms, &p);
+    if (!planned && kind != 3 && g.Cg == 1) planned = make_plan(g, es, la.tile, dev.num_sms, &p);
     if (!planned) return cudaErrorNotSupported;
     if (p.direct) {
       // one CTA per tile: the grid's x extent bounds the tile count

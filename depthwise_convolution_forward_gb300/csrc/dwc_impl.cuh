@@ -51,7 +51,11 @@ namespace dw {
 //               scalar fmaf (the default for fp32);
 //  kColWide     4 channels widened to fp32 once per load, multiplied in
 //               channel pairs with the packed fp32x2 FMA.
-enum ColForm : int { kColSplit = 0, kColPacked = 1, kColWide = 2, kColPacked8 = 3 };
+//  kColGroup2   16-bit storage, groups of two channels (Cg == Kg == 2): a
+//               thread's 4 channels are 2 groups; each output is the
+//               two-term dot product of its group's input pair with its
+//               weight pair, per tap.
+enum ColForm : int { kColSplit = 0, kColPacked = 1, kColWide = 2, kColPacked8 = 3, kColGroup2 = 4 };
 
 // Threads per CTA: a producer warp and up to 16 consumer warps (12 for the
 // 8-channel form, whose threads hold twice the weights and accumulators).
@@ -71,6 +75,8 @@ __host__ __device__ constexpr int col_reg_cap(int form) {
          : ((2 * DL) / S + 1 > 3)                                  ? 88
                                                                    : 72;
 }
+// Weight values per (tap, output channel): the group's input channels.
+__host__ __device__ constexpr int col_vpc(int form) { return form == kColGroup2 ? 2 : 1; }
 
 __device__ __forceinline__ void lds64(uint32_t addr, uint32_t (&v)[2]) {
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(addr));
@@ -105,15 +111,17 @@ struct ColOpsF32 {
   static constexpr int kOps = 4;  // registers per 4-channel piece
   using Op = float;
   static constexpr int kWeightBytes = 4;
+  static constexpr int kWOps = kOps;  // registers per tap of weights
+  static constexpr int kVpc = 1;
   __device__ __forceinline__ static void load_x(uint32_t addr, Op (&v)[kOps]) {
     uint32_t w[4];
     lds128a(addr, w);
 #pragma unroll
     for (int e = 0; e < 4; ++e) v[e] = __uint_as_float(w[e]);
   }
-  __device__ __forceinline__ static void load_w(uint32_t addr, Op (&v)[kOps]) { load_x(addr, v); }
+  __device__ __forceinline__ static void load_w(uint32_t addr, Op (&v)[kWOps]) { load_x(addr, v); }
   __device__ __forceinline__ static void stage_w(uint8_t* dst, float v) { *reinterpret_cast<float*>(dst) = v; }
-  __device__ __forceinline__ static void mac(float (&d)[kCpt], const Op (&x)[kOps], const Op (&w)[kOps],
+  __device__ __forceinline__ static void mac(float (&d)[kCpt], const Op (&x)[kOps], const Op (&w)[kWOps],
                                              const float (&c)[kCpt]) {
 #pragma unroll
     for (int e = 0; e < kCpt; ++e) d[e] = fmaf(x[e], w[e], c[e]);
@@ -126,6 +134,8 @@ struct ColOpsWide {
   static constexpr int kOps = 4;
   using Op = float;
   static constexpr int kWeightBytes = 4;
+  static constexpr int kWOps = kOps;  // registers per tap of weights
+  static constexpr int kVpc = 1;
   __device__ __forceinline__ static void load_x(uint32_t addr, Op (&v)[kOps]) {
     if constexpr (sizeof(T) == 4) {
       uint32_t w[4];
@@ -139,7 +149,7 @@ struct ColOpsWide {
       widen_word<T>(w[1], v + 2);
     }
   }
-  __device__ __forceinline__ static void load_w(uint32_t addr, Op (&v)[kOps]) {
+  __device__ __forceinline__ static void load_w(uint32_t addr, Op (&v)[kWOps]) {
     uint32_t w[4];
     lds128a(addr, w);
 #pragma unroll
@@ -148,7 +158,7 @@ struct ColOpsWide {
   __device__ __forceinline__ static void stage_w(uint8_t* dst, T v) {
     *reinterpret_cast<float*>(dst) = Elem<T>::to_f32(v);
   }
-  __device__ __forceinline__ static void mac(float (&d)[kCpt], const Op (&x)[kOps], const Op (&w)[kOps],
+  __device__ __forceinline__ static void mac(float (&d)[kCpt], const Op (&x)[kOps], const Op (&w)[kWOps],
                                              const float (&c)[kCpt]) {
 #pragma unroll
     for (int e = 0; e < kCpt; e += 2) {
@@ -165,12 +175,14 @@ struct ColOps16Split {
   static constexpr int kOps = 4;
   using Op = uint32_t;  // value in the low 16 bits
   static constexpr int kWeightBytes = 4;
+  static constexpr int kWOps = kOps;  // registers per tap of weights
+  static constexpr int kVpc = 1;
   __device__ __forceinline__ static void load_x(uint32_t addr, Op (&v)[kOps]) {
     uint32_t w[2];
     lds64(addr, w);
     v[0] = w[0], v[1] = w[0] >> 16, v[2] = w[1], v[3] = w[1] >> 16;
   }
-  __device__ __forceinline__ static void load_w(uint32_t addr, Op (&v)[kOps]) {
+  __device__ __forceinline__ static void load_w(uint32_t addr, Op (&v)[kWOps]) {
     uint32_t w[4];
     lds128a(addr, w);
 #pragma unroll
@@ -179,7 +191,7 @@ struct ColOps16Split {
   __device__ __forceinline__ static void stage_w(uint8_t* dst, T v) {
     *reinterpret_cast<uint32_t*>(dst) = (uint32_t)(*reinterpret_cast<const unsigned short*>(&v));
   }
-  __device__ __forceinline__ static void mac(float (&d)[kCpt], const Op (&x)[kOps], const Op (&w)[kOps],
+  __device__ __forceinline__ static void mac(float (&d)[kCpt], const Op (&x)[kOps], const Op (&w)[kWOps],
                                              const float (&c)[kCpt]) {
 #pragma unroll
     for (int e = 0; e < kCpt; ++e) d[e] = mixed_fma<T>((unsigned short)x[e], (unsigned short)w[e], c[e]);
@@ -217,6 +229,8 @@ struct ColOps16Packed {
   static constexpr int kOps = CPT / 2;  // packed pairs
   using Op = uint32_t;
   static constexpr int kWeightBytes = 2;
+  static constexpr int kWOps = kOps;
+  static constexpr int kVpc = 1;
   __device__ __forceinline__ static void load_x(uint32_t addr, Op (&v)[kOps]) {
     if constexpr (CPT == 8) {
       lds128a(addr, v);
@@ -224,24 +238,73 @@ struct ColOps16Packed {
       lds64(addr, v);
     }
   }
-  __device__ __forceinline__ static void load_w(uint32_t addr, Op (&v)[kOps]) { load_x(addr, v); }
+  __device__ __forceinline__ static void load_w(uint32_t addr, Op (&v)[kWOps]) { load_x(addr, v); }
   __device__ __forceinline__ static void stage_w(uint8_t* dst, T v) { *reinterpret_cast<T*>(dst) = v; }
-  __device__ __forceinline__ static void mac(float (&d)[kCpt], const Op (&x)[kOps], const Op (&w)[kOps],
+  __device__ __forceinline__ static void mac(float (&d)[kCpt], const Op (&x)[kOps], const Op (&w)[kWOps],
                                              const float (&c)[kCpt]) {
 #pragma unroll
     for (int i = 0; i < kOps; ++i) mixed_fma_pair<T>(x[i], w[i], c[2 * i], c[2 * i + 1], d[2 * i], d[2 * i + 1]);
   }
 };
 
+// acc + x.lo * w.lo + x.hi * w.hi with mixed-precision FMAs (fp32 products
+// and sums, one rounding each): the two-term dot product of a group's input
+// pair with one output channel's weight pair.
+template <typename T>
+__device__ __forceinline__ float mixed_dot2(uint32_t x, uint32_t w, float c);
+template <>
+__device__ __forceinline__ float mixed_dot2<__half>(uint32_t x, uint32_t w, float c) {
+  float d;
+  asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t.reg .f32 t;\n\t"
+      "mov.b32 {xl, xh}, %1;\n\tmov.b32 {wl, wh}, %2;\n\t"
+      "fma.rn.f32.f16 t, xl, wl, %3;\n\tfma.rn.f32.f16 %0, xh, wh, t;\n\t}"
+      : "=f"(d)
+      : "r"(x), "r"(w), "f"(c));
+  return d;
+}
+template <>
+__device__ __forceinline__ float mixed_dot2<__nv_bfloat16>(uint32_t x, uint32_t w, float c) {
+  float d;
+  asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t.reg .f32 t;\n\t"
+      "mov.b32 {xl, xh}, %1;\n\tmov.b32 {wl, wh}, %2;\n\t"
+      "fma.rn.f32.bf16 t, xl, wl, %3;\n\tfma.rn.f32.bf16 %0, xh, wh, t;\n\t}"
+      : "=f"(d)
+      : "r"(x), "r"(w), "f"(c));
+  return d;
+}
+
+// Groups of two channels: the thread's 4 channels are groups g, g + 1; x
+// word i holds group i's input pair, weight word j = 2 * i + k the pair of
+// output channel k of group i.  Staged weights are [tap][output channel][2].
+template <typename T>
+struct ColOps16Group2 {
+  static constexpr int kCpt = 4;
+  static constexpr int kOps = 2;
+  using Op = uint32_t;
+  static constexpr int kWeightBytes = 2;
+  static constexpr int kWOps = 4;
+  static constexpr int kVpc = 2;
+  __device__ __forceinline__ static void load_x(uint32_t addr, Op (&v)[kOps]) { lds64(addr, v); }
+  __device__ __forceinline__ static void load_w(uint32_t addr, Op (&v)[kWOps]) { lds128a(addr, v); }
+  __device__ __forceinline__ static void stage_w(uint8_t* dst, T v) { *reinterpret_cast<T*>(dst) = v; }
+  __device__ __forceinline__ static void mac(float (&d)[kCpt], const Op (&x)[kOps], const Op (&w)[kWOps],
+                                             const float (&c)[kCpt]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d[j] = mixed_dot2<T>(x[j >> 1], w[j], c[j]);
+  }
+};
+
 template <typename T, int FORM>
 using ColOps = typename std::conditional<
+    FORM == kColGroup2 && sizeof(T) == 2, ColOps16Group2<T>,
+    typename std::conditional<
     FORM == kColWide, ColOpsWide<T>,
     typename std::conditional<
         std::is_same<T, float>::value, ColOpsF32,
         typename std::conditional<
             FORM == kColPacked8, ColOps16Packed<T, 8>,
             typename std::conditional<FORM == kColPacked, ColOps16Packed<T, 4>,
-                                      ColOps16Split<T>>::type>::type>::type>::type;
+                                      ColOps16Split<T>>::type>::type>::type>::type>::type;
 
 // Channels per thread of a (storage type, form) pair, for the host planner.
 inline int col_cpt(int es, int form) { return (es == 2 && form == kColPacked8) ? 8 : 4; }
@@ -330,7 +393,7 @@ struct ColState {
   int nrows;
   bool store_ok;
   int64_t y_row_step;
-  const typename Ops::Op (&wr)[3][3][Ops::kOps];
+  const typename Ops::Op (&wr)[3][3][Ops::kWOps];
   const float (&br)[Ops::kCpt];
   float (&acc)[NA][Ops::kCpt];
 };
@@ -521,19 +584,24 @@ __global__ void __maxnreg__((col_reg_cap<T, S, DL>(FORM))) dw_col_kernel(const _
   // weights [c][tap] in global -> [tap][c] in shared; bias -> fp32 (consumer
   // warps only, while the first copies are in flight)
   // (global reads in source order: coalesced; four loads in flight per thread)
-  for (int i0 = ctid; i0 < 9 * a.C; i0 += 4 * ncons) {
+  // (w is [output channel][tap][input channel of the group]: kVpc values per
+  // tap and output channel; staged as [tap][output channel][kVpc])
+  constexpr int VPC = Ops::kVpc;
+  const int nw = 9 * VPC * a.C;
+  for (int i0 = ctid; i0 < nw; i0 += 4 * ncons) {
     T v[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * ncons;
-      if (i < 9 * a.C) v[u] = wg[i];
+      if (i < nw) v[u] = wg[i];
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = i0 + u * ncons;
-      if (i < 9 * a.C) {
-        const int ch = i / 9, t = i - ch * 9;
-        Ops::stage_w(w_s + ((size_t)t * a.C + ch) * Ops::kWeightBytes, v[u]);
+      if (i < nw) {
+        const int ch = i / (9 * VPC), r = i - ch * (9 * VPC);
+        const int t = r / VPC, e = r - t * VPC;
+        Ops::stage_w(w_s + (((size_t)t * a.C + ch) * VPC + e) * Ops::kWeightBytes, v[u]);
       }
     }
   }
@@ -551,7 +619,7 @@ __global__ void __maxnreg__((col_reg_cap<T, S, DL>(FORM))) dw_col_kernel(const _
   const int64_t thread_off = (int64_t)wl * a.C + q * CPT;
   const int Hh = a.Hh;
 
-  Op wr[3][3][Ops::kOps];
+  Op wr[3][3][Ops::kWOps];
   float br[CPT];
   int cur_c0 = -1;
   int s = 0;
@@ -585,7 +653,7 @@ __global__ void __maxnreg__((col_reg_cap<T, S, DL>(FORM))) dw_col_kernel(const _
       cur_c0 = h.c0;
 #pragma unroll
       for (int t = 0; t < 9; ++t)
-        Ops::load_w(smem_u32(w_s + ((size_t)t * a.C + chl) * Ops::kWeightBytes), wr[t / 3][t % 3]);
+        Ops::load_w(smem_u32(w_s + ((size_t)t * a.C + chl) * VPC * Ops::kWeightBytes), wr[t / 3][t % 3]);
 #pragma unroll
       for (int i = 0; i < CPT; i += 4) {
         const float4 b4 = *reinterpret_cast<const float4*>(b_s + chl + i);

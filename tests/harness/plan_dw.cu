@@ -30,7 +30,7 @@ int main() {
     bool ok;
     int form = 0;
     if (g.Z == 1) {
-      form = dw::col_form(es, nullptr);
+      form = dw::col_form(es, nullptr, g.Cg);
       ok = dw::make_col_plan(g, es, any_ov ? ov : nullptr, 152, form, regs, &p);
     } else {
       ok = dw::make_plan(g, es, any_ov ? ov : nullptr, 152, &p);

@@ -42,8 +42,8 @@ int main() {
     // planner with the device's SM count and shared memory
     dw::Plan dp{};
     bool dw_plan = false;
-    if (g.Z == 1) dw_plan = dw::make_col_plan(g, es, nullptr, sms, dw::col_form(es, nullptr), regs, &dp);
-    if (!dw_plan) dw_plan = dw::make_plan(g, es, nullptr, sms, &dp);
+    if (g.Z == 1) dw_plan = dw::make_col_plan(g, es, nullptr, sms, dw::col_form(es, nullptr, g.Cg), regs, &dp);
+    if (!dw_plan && g.Cg == 1) dw_plan = dw::make_plan(g, es, nullptr, sms, &dp);
     dw_plan = dw_plan && dp.smem_bytes <= (uint32_t)smem;
     TcPlan tp;
     std::memset(&tp, 0, sizeof(tp));

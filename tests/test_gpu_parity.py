@@ -180,6 +180,39 @@ def test_depthwise_3d_channel_tiles(orc, wl):
     assert_close(y.double().numpy(), orc.forward(wl, x, w, b), wl.dtype, wl.name)
 
 
+G2_EDGE = [
+    # (N, G, H, W, stride, pad, dil, dtype, tiles): groups of two channels on
+    # the column kernel (Cg == Kg == 2), forced, with ragged and explicit tiles
+    (2, 8, 13, 11, 1, 1, 1, "bf16", None),
+    (1, 12, 9, 17, 2, 0, 1, "f16", None),
+    (1, 8, 12, 12, 1, 2, 2, "bf16", None),
+    (2, 16, 15, 15, 2, 2, 2, "f16", None),
+    (1, 260, 6, 7, 1, 1, 1, "bf16", None),  # 520 channels: channel tiles
+    (2, 64, 28, 28, 1, 1, 1, "bf16", (5, 3, 0, 2, 1, 0, 3)),
+    (2, 64, 28, 28, 1, 1, 1, "f16", (3, 5, 0, 4, 2, 0, 3)),
+    (1, 4, 1, 1, 1, 1, 1, "bf16", None),  # 1x1 input, padding only
+]
+
+
+@pytest.mark.parametrize("case", G2_EDGE, ids=lambda c: "-".join(map(str, c[:8])))
+def test_group2_column_kernel(orc, case):
+    N, G, H, W, s, p, d, dt, tiles = case
+    wl = inputs.Workload("g2_edge", 7, G2_EDGE.index(case), 2, N, G, 2, 2, (1, H, W), (1, 3, 3), (1, s, s),
+                         (0, p, p), (1, d, d), dt, True)
+    x, w, b = inputs.make_inputs(wl)
+    y, sel = run_gpu(wl, x, w, b, force=B.KERNEL_DIRECT_DW, tile=list(tiles) if tiles else None)
+    assert sel == B.KERNEL_DIRECT_DW
+    assert_close(y.double().numpy(), orc.forward(wl, x, w, b), dt, str(case))
+
+
+def test_group2_selection():
+    """Stride 1 runs on the column kernel, stride 2 on the tensor-core kernel."""
+    s1 = gc.problem_of(inputs.by_name("sweep_g256_d1_s1_bf16"))
+    s2 = gc.problem_of(inputs.by_name("sweep_g256_d1_s2_bf16"))
+    assert gc.grouped_conv_select(s1, B.GCONV_BF16) == B.KERNEL_DIRECT_DW
+    assert gc.grouped_conv_select(s2, B.GCONV_BF16) == B.KERNEL_IGEMM_TC
+
+
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 def test_integer_inputs_bit_exact(orc, dt):
     """Small integers: every product and partial sum is exact in fp32 and the
@@ -187,7 +220,9 @@ def test_integer_inputs_bit_exact(orc, dt):
     for wl in (inputs.Workload("int_dw", 8, 0, 2, 2, 32, 1, 1, (1, 11, 10), (1, 3, 3), (1, 1, 1),
                                (0, 1, 1), (1, 1, 1), dt, True),
                inputs.Workload("int_grp", 8, 1, 2, 1, 4, 3, 5, (1, 7, 6), (1, 3, 3), (1, 2, 1),
-                               (0, 1, 1), (1, 1, 2), dt, True)):
+                               (0, 1, 1), (1, 1, 2), dt, True),
+               inputs.Workload("int_g2", 8, 2, 2, 2, 16, 2, 2, (1, 9, 10), (1, 3, 3), (1, 1, 1),
+                               (0, 1, 1), (1, 1, 1), dt, True)):
         g = torch.Generator().manual_seed(3)
         tdt = inputs.DTYPES[dt]
         x = torch.randint(-3, 4, wl.x_shape(), generator=g).to(tdt)

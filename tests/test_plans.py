@@ -71,7 +71,17 @@ def _problems(seed, n, **kw):
 
 
 def _dw_candidates():
-    probs = [wl for wl in inputs.all_workloads() if wl.Cg == 1 and wl.Kg == 1]
+    probs = [wl for wl in inputs.all_workloads() if (wl.Cg == 1 and wl.Kg == 1) or
+             (wl.Cg == 2 and wl.Kg == 2 and wl.ndim == 2)]
+    rng2 = np.random.default_rng(78)
+    for _ in range(40):  # groups of two channels (column form only)
+        s, d = int(rng2.integers(1, 3)), int(rng2.integers(1, 3))
+        hw = [int(rng2.integers(1, 60)), int(rng2.integers(1, 60))]
+        wl = inputs.Workload("g2", 0, 0, 2, int(rng2.integers(1, 5)), 4 * int(rng2.integers(1, 80)), 2, 2,
+                             (1, *hw), (1, 3, 3), (1, s, s), (0, d, d), (1, d, d),
+                             str(rng2.choice(["f16", "bf16"])), True)
+        if min(_geom(wl)[0]) >= 1:
+            probs.append(wl)
     probs += [inputs.by_name("mbv2_dw_s1_f16").with_(N=4800)]
     rng = np.random.default_rng(77)
     for _ in range(300):
