@@ -8,9 +8,10 @@ roofline discussion asks for per-group C_in_g rather than the full C, and its
 kernel multiplies because it merges groups into block-diagonal tiles are not
 credited.
 
-Bytes count each tensor moved once:  x + y + w (+ bias), in the storage dtype.
-For every benchmarked problem the filter windows cover the whole input, so
-all of x is read at least once.
+Bytes count each tensor moved once:  x + y + w (+ bias), in the storage dtype,
+where x counts only the input positions some filter tap reads.  With stride 2
+and dilation 2 (pad 2) only every other row and column of the input is ever
+read, so a quarter of x; every other benchmarked problem reads all of it.
 """
 from __future__ import annotations
 
@@ -26,10 +27,18 @@ def flops(wl, out_shape) -> int:
     return 2 * outputs(wl, out_shape) * wl.Cg * wl.taps
 
 
+def touched(i_ext: int, o_ext: int, k: int, s: int, p: int, d: int) -> int:
+    """Input positions along one dimension that some tap of some output
+    reads: o*s - p + t*d inside [0, i_ext) for o < o_ext, t < k."""
+    return len({o * s - p + t * d for o in range(o_ext) for t in range(k)} & set(range(i_ext)))
+
+
 def tensor_bytes(wl, out_shape) -> dict:
     es = ES[wl.dtype]
-    D, H, W = wl.inp
-    x = wl.N * D * H * W * wl.C * es
+    read = 1
+    for i in range(3):
+        read *= touched(wl.inp[i], out_shape[i], wl.ker[i], wl.stride[i], wl.pad[i], wl.dil[i])
+    x = wl.N * read * wl.C * es
     y = outputs(wl, out_shape) * es
     w = wl.K * wl.taps * wl.Cg * es
     b = wl.K * es if wl.bias else 0

@@ -30,3 +30,17 @@ def test_flops_scale_with_per_group_channels():
     f8 = roofline.flops(wl, out)
     f512 = roofline.flops(inputs.by_name("sweep_g512_d1_s1_bf16"), out)
     assert f8 == 64 * f512
+
+
+def test_input_bytes_count_touched_positions():
+    """Stride 2 with dilation 2 and pad 2 reads only the even rows and
+    columns: a quarter of x; stride 2 with pad 1 (3x3) and stride 1 read all."""
+    for name, frac in (("sweep_g64_d2_s2_bf16", 0.25), ("sweep_g64_d1_s2_bf16", 1.0), ("mbv2_dw_s2_f16", 1.0),
+                       ("sweep_g8_d2_s1_bf16", 1.0)):
+        wl = inputs.by_name(name)
+        out = gc.grouped_conv_out_shape(gc.problem_of(wl))
+        full = wl.N * wl.inp[0] * wl.inp[1] * wl.inp[2] * wl.C * roofline.ES[wl.dtype]
+        assert roofline.tensor_bytes(wl, out)["x"] == full * frac, name
+    # brute force on a small odd case: positions o*s - p + t*d inside the input
+    assert roofline.touched(7, 3, 3, 3, 0, 1) == 7 - 0  # windows [0,3), [3,6), [6,9) -> 0..6
+    assert roofline.touched(7, 2, 2, 3, 0, 2) == 4      # {0, 2} and {3, 5}
