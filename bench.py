@@ -615,6 +615,7 @@ def run_ours(args, wls, set_name, rank, world):
         e = {"kernel": arm.gc.KERNEL_NAMES.get(c["kernel"]), "median_us": med * 1e3, "mean_us": mean * 1e3,
              "launches": M, "bytes": c["bytes"], "flops": c["flops"]}
         e.update(roofline_of(c, mean, hbm_peak, tc_peak))
+        e["traffic"] = None if bwd else load_traffic(e["kernel"], c["wl"].name)
         return e
 
     per_launch = {c["wl"].name: launch_entry(c, *conv_ms[ci]) for ci, c in enumerate(convs)}
