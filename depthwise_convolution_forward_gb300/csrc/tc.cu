@@ -217,8 +217,17 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     if (a_end_of(stages) > budget) continue;
     c.stages = stages;
     c.epi_off = epi ? a_end_of(stages) : 0u;
+    // Accumulator buffers: as many as 512 tensor-memory columns hold (at
+    // most kMaxAccBufs, at least 2), or at most override slot 1.  With two
+    // buffers the MMAs of tile k wait for the epilogue of tile k - 2, which
+    // itself waited for the MMAs of tile k - 2 to complete.
+    const uint32_t per_buf = (uint32_t)(np * G2 * c.Nn);
+    int nbuf = (int)std::min<uint32_t>((uint32_t)tc::kMaxAccBufs, 512u / per_buf);
+    if (ov && ov[1]) nbuf = std::min(nbuf, ov[1]);
+    if (nbuf < 2) continue;
+    c.nbuf = nbuf;
     uint32_t cols = 32;
-    while (cols < (uint32_t)(2 * np * G2 * c.Nn)) cols <<= 1;
+    while (cols < (uint32_t)nbuf * per_buf) cols <<= 1;
     if (cols > 512) continue;
     c.tmem_cols = cols;
     c.idesc = tc::idesc_f16(bf16, 128, c.Nn);

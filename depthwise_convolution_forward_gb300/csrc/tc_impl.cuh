@@ -23,8 +23,10 @@
 //    and discarded.  Stride 2 uses four polyphase planes loaded with TMA
 //    element strides, so every tap is again a plain shift.
 //  * Warps 1-4 (kIssuers warps, one lane each) issue tcgen05.mma (M = 128,
-//    N = m*Kg, K = 16) into fp32 accumulators in tensor memory,
-//    double-buffered across tiles.  The tile's accumulators, and partial
+//    N = m*Kg, K = 16) into fp32 accumulators in tensor memory, in two to
+//    four buffers across tiles (as many as the 512 columns hold): the MMAs
+//    of tile k wait only for the epilogue of tile k - nbuf.  The tile's
+//    accumulators, and partial
 //    accumulators that each sum a share of the taps, are dealt to the
 //    issuers, so four MMA streams run at once; each issuer signals completion
 //    with tcgen05.commit on mbarriers.
@@ -44,6 +46,7 @@ namespace tc {
 constexpr int kMaxTaps = 32;
 constexpr int kMaxPhases = 4;
 constexpr int kMaxStages = 4;
+constexpr int kMaxAccBufs = 4;                    // accumulator buffers in tensor memory
 constexpr int kMaxTab = 2048;                     // host-built MMA list entries
 constexpr int kIssuers = 4;                       // MMA-issuing warps
 constexpr int kThreads = 32 * (1 + kIssuers + 4);  // producer, issuers, epilogue
@@ -64,6 +67,7 @@ struct TcArgs {
   int nchunks, Kt, Nn, KS, nmt;
   int sc;                  // group chunks per 128-byte row (swizzled layout), else 1
   int np;                  // partial accumulators per accumulator (taps split np ways)
+  int nbuf;                // accumulator buffers (2..kMaxAccBufs): tile k uses buffer k % nbuf
   uint32_t plane_stride, a_stage_bytes, tx_bytes;
   uint32_t a_off, b_off, bias_off, tab_off;  // smem offsets (tab: MMA descriptor table)
   uint32_t epi_off;  // output-box staging for TMA tensor stores, or 0 to store straight from registers
@@ -246,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
   uint64_t* a_full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* a_empty = a_full + kMaxStages;
   uint64_t* acc_full = a_full + 2 * kMaxStages;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* mma_done = acc_empty + 2;
+  uint64_t* acc_empty = acc_full + kMaxAccBufs;
+  uint64_t* mma_done = acc_empty + kMaxAccBufs;
   uint64_t* w_full = mma_done + 1;  // weight copies (TMA staging)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 256);
   float* bias_s = reinterpret_cast<float*>(smem + a.bias_off);
@@ -269,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
       mbar_init(&a_full[s], 1);
       mbar_init(&a_empty[s], kIssuers);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < a.nbuf; ++b) {
       mbar_init(&acc_full[b], kIssuers);
       mbar_init(&acc_empty[b], 4);
     }
@@ -552,12 +556,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
       const uint4* my_list = reinterpret_cast<const uint4*>(smem + a.tab_off) + 2 * my_base;
       for (int sp = cta_in_gc; sp < a.spatial_tiles; sp += a.cpg, ++k) {
         const int s = k % a.stages;
-        const int ab = k & 1;
+        const int ab = k % a.nbuf;
         if (!mbar_wait(&a_full[s], (uint32_t)((k / a.stages) & 1), a.wait_limit_ns)) {
           failed = true;
           break;
         }
-        if (k >= 2 && !mbar_wait(&acc_empty[ab], (uint32_t)(((k >> 1) - 1) & 1), a.wait_limit_ns)) {
+        if (k >= a.nbuf && !mbar_wait(&acc_empty[ab], (uint32_t)(((k / a.nbuf) - 1) & 1), a.wait_limit_ns)) {
           failed = true;
           break;
         }
@@ -604,8 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     const uint32_t stage_base = smem_u32(smem + a.epi_off);
     int k = 0;
     for (int sp = cta_in_gc; sp < a.spatial_tiles; sp += a.cpg, ++k) {
-      const int ab = k & 1;
-      if (!warp_wait(&acc_full[ab], (uint32_t)((k >> 1) & 1), a.wait_limit_ns)) {
+      const int ab = k % a.nbuf;
+      if (!warp_wait(&acc_full[ab], (uint32_t)((k / a.nbuf) & 1), a.wait_limit_ns)) {
         if (lane == 0) report(a.status, kDevTimeout, 5);
         break;
       }

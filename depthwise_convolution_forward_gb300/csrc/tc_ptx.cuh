@@ -41,31 +41,6 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
-// The same MMA issued by one lane of a converged warp (elect.sync picks the
-// lowest active lane): every lane of the warp executes this with the same
-// operands.  A warp that runs its issue loop converged and lets one elected
-// lane issue measured about twice the MMA issue rate of a loop run by lane 0
-// alone inside a divergent branch (about 70 against 140-150 cycles per MMA
-// on GB300 for N <= 64).
-__device__ __forceinline__ void mma_f16_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                              uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync r|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-}
-// commit() by the elected lane of a converged warp (the lane that issued the
-// warp's MMAs through mma_f16_elect).
-__device__ __forceinline__ void commit_elect(uint64_t* bar) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
-      "elect.sync r|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
-      : "memory");
-}
-
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void commit(uint64_t* bar) {

@@ -119,7 +119,9 @@ typedef struct gconv_options {
                             row-blocked, 2 = direct loads, 3 = column form; the
                             automatic choice is the column form when the depth
                             filter is 1, else the row-blocked form).
-                            Tensor-core kernel: [0] TH, [2] M tiles per CTA,
+                            Tensor-core kernel: [0] TH, [1] most accumulator
+                            buffers (2-4; default as many as tensor memory
+                            holds), [2] M tiles per CTA,
                             [3] stages, [4] partial accumulators, [6] 1 = force
                             16-byte chunk planes, [7] extra shared memory (KB),
                             negative: stage the tile's output box in shared

@@ -46,11 +46,12 @@ int main() {
            "\"Dh\": %d, \"stages\": %d, \"a_off\": %u, \"b_off\": %u, \"a_stage_bytes\": %u, \"plane_stride\": %u, "
            "\"nphase\": %d, \"nchunks\": %d, \"tx_bytes\": %u, \"tiles_h\": %d, \"tiles_w\": %d, \"spatial\": %d, "
            "\"cpg\": %d, \"n_gc\": %d, \"ntab\": %d, \"max_a\": %u, \"max_b\": %u, \"tab_off\": %u, "
-           "\"bias_off\": %u, \"epi_off\": %u, \"epi_w\": %d, \"epi_slices\": %d, \"epi_slice_bytes\": %u}\n",
+           "\"bias_off\": %u, \"epi_off\": %u, \"epi_w\": %d, \"epi_slices\": %d, \"epi_slice_bytes\": %u, "
+           "\"nbuf\": %d}\n",
            m, (int)p.sw, p.smem_bytes, p.grid, a.tmem_cols, a.np, a.nmt, a.sc, a.Nn, a.KS, a.TH, a.TWo, a.P, a.Hh,
            a.Dh, a.stages, a.a_off, a.b_off, a.a_stage_bytes, a.plane_stride, a.nphase, a.nchunks, a.tx_bytes,
            a.tiles_h, a.tiles_w, a.spatial_tiles, a.cpg, a.n_gc, a.ntab, max_a, max_b, a.tab_off, a.bias_off,
-           a.epi_off, a.epi_w, a.epi_slices, a.epi_slice_bytes);
+           a.epi_off, a.epi_w, a.epi_slices, a.epi_slice_bytes, a.nbuf);
   }
   return 0;
 }

@@ -183,7 +183,11 @@ def _check_tc_plan(wl, p):
     G2 = p["sc"] * p["nmt"]
     assert p["smem"] <= SMEM_BLOCK, ctx
     assert p["tmem_cols"] in (32, 64, 128, 256, 512), ctx
-    assert p["tmem_cols"] >= 2 * p["np"] * G2 * p["Nn"], ctx  # double-buffered (partial) accumulators
+    # 2..4 buffers of (partial) accumulators, all of them in the allocation
+    assert 2 <= p["nbuf"] <= 4, ctx
+    assert p["tmem_cols"] >= p["nbuf"] * p["np"] * G2 * p["Nn"], ctx
+    # as many buffers as 512 columns hold
+    assert p["nbuf"] == min(4, 512 // (p["np"] * G2 * p["Nn"])), ctx
     if p["tmem_cols"] > 256:  # a second CTA could not allocate beside it: keep it off the SM
         assert p["smem"] + RESERVED > SMEM_SM // 2, ctx
     assert 1 <= p["np"] <= max(1, wl.taps), ctx
