@@ -592,9 +592,12 @@ gconv_status grouped_conv_bwd_weight_ex(const void* x, const void* dy, void* dw,
   if (s != GCONV_OK) return s;
   if (dt != GCONV_F32 && dt != GCONV_F16 && dt != GCONV_BF16) return fail(GCONV_ERR_UNSUPPORTED, "unknown dtype %d", (int)dt);
   if (x == nullptr || dy == nullptr || dw == nullptr) return fail(GCONV_ERR_INVALID_ARG, "x, dy and dw must not be NULL");
-  if (opt && opt->force_kernel != 0 && opt->force_kernel != GCONV_KERNEL_BWD_WEIGHT)
-    return fail(GCONV_ERR_UNSUPPORTED, "kernel %d does not compute backward weight", opt->force_kernel);
+  const int forced = opt ? opt->force_kernel : 0;
+  if (forced != 0 && forced != GCONV_KERNEL_BWD_WEIGHT && forced != GCONV_KERNEL_IGEMM_TC)
+    return fail(GCONV_ERR_UNSUPPORTED, "kernel %d does not compute backward weight", forced);
   const DType t = (DType)dt;
+  if (forced == GCONV_KERNEL_IGEMM_TC && !bwd_weight_tc_supported(g, t))
+    return fail(GCONV_ERR_UNSUPPORTED, "tensor-core backward weight cannot run this problem");
   const int es = dtype_bytes(t);
   const int64_t dwb = g.w_elems() * es, xb = g.x_elems() * es, dyb = g.y_elems() * es;
   const int64_t need = bwd_weight_workspace_bytes(g, t);
@@ -609,9 +612,20 @@ gconv_status grouped_conv_bwd_weight_ex(const void* x, const void* dy, void* dw,
   cudaError_t e = device_slot(&slot);
   if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
   LaunchArgs a = make_args(x, dy, nullptr, dw, t, stream, slot, opt);
-  e = bwd_weight_launch(g, a, workspace, slot->info);
+  // Tensor-core route where the shape allows (it declines, before launching
+  // anything, when x or dy is not 16-byte aligned or its plan does not fit
+  // the device); the FFMA route otherwise or when forced.
+  int kernel = GCONV_KERNEL_BWD_WEIGHT;
+  e = cudaErrorNotSupported;
+  if (forced != GCONV_KERNEL_BWD_WEIGHT && bwd_weight_tc_supported(g, t)) {
+    e = bwd_weight_tc_launch(g, a, workspace, slot->info);
+    if (e == cudaSuccess) kernel = GCONV_KERNEL_IGEMM_TC;
+    else if (e == cudaErrorNotSupported && forced == GCONV_KERNEL_IGEMM_TC)
+      return fail(GCONV_ERR_UNSUPPORTED, "tensor-core backward weight needs 16-byte aligned x and dy");
+  }
+  if (e == cudaErrorNotSupported) e = bwd_weight_launch(g, a, workspace, slot->info);
   if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
-  if (opt) opt->selected = GCONV_KERNEL_BWD_WEIGHT;
+  if (opt) opt->selected = kernel;
   return finish(slot, a, opt);
 }
 

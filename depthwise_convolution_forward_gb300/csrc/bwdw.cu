@@ -397,11 +397,34 @@ cudaError_t bwd_weight_typed(const Geometry& g, const LaunchArgs& la, float* ws,
                        a);
 }
 
+template <typename T>
+cudaError_t reduce_typed(const Geometry& g, const LaunchArgs& la, float* ws, int S, const DeviceInfo& dev) {
+  BwwArgs a{};
+  a.ws = ws;
+  a.dw = la.y;
+  a.S = S;
+  a.E = g.w_elems();
+  const int64_t blocks = std::min<int64_t>((a.E + 31) / 32, (int64_t)dev.num_sms * 2);
+  return launch_kernel(bwd_weight_reduce_kernel<T>, dim3((unsigned)std::max<int64_t>(1, blocks)), dim3(1024), 0, la,
+                       a);
+}
+
 }  // namespace
+
+cudaError_t bwd_weight_reduce_launch(const Geometry& g, const LaunchArgs& a, float* ws, int S,
+                                     const DeviceInfo& dev) {
+  switch (a.dt) {
+    case kF32: return reduce_typed<float>(g, a, ws, S, dev);
+    case kF16: return reduce_typed<__half>(g, a, ws, S, dev);
+    case kBF16: return reduce_typed<__nv_bfloat16>(g, a, ws, S, dev);
+  }
+  return cudaErrorNotSupported;
+}
 
 int64_t bwd_weight_workspace_bytes(const Geometry& g, DType dt) {
   const BwwPlan p = plan_bww(g, dtype_bytes(dt), 16 / dtype_bytes(dt));
-  return (int64_t)p.S * p.E * 4;
+  // either route may run (the tensor-core one needs 16-byte aligned x and dy)
+  return std::max<int64_t>((int64_t)p.S * p.E * 4, bwd_weight_tc_workspace_bytes(g, dt));
 }
 
 cudaError_t bwd_weight_launch(const Geometry& g, const LaunchArgs& a, void* workspace, const DeviceInfo& dev) {

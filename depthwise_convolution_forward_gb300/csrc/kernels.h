@@ -140,6 +140,16 @@ cudaError_t phase_scatter_launch(const PhaseScatter& ps, const void* pb, void* d
 // workspace holds bwd_weight_workspace_bytes (independent of the device).
 int64_t bwd_weight_workspace_bytes(const Geometry& g, DType dt);
 cudaError_t bwd_weight_launch(const Geometry& g, const LaunchArgs& a, void* workspace, const DeviceInfo& dev);
+// dw = round(sum over the S splits of ws[s][e]) (stage 2 of either route).
+cudaError_t bwd_weight_reduce_launch(const Geometry& g, const LaunchArgs& a, float* ws, int S,
+                                     const DeviceInfo& dev);
+// Tensor-core route (16-bit, Cg == Kg dividing 64, C % 64 == 0, H / W
+// stride 1 or 2, at most 4 taps per filter row): shape check, workspace
+// bytes (0 when unsupported), and launch (cudaErrorNotSupported when x or
+// dy is not 16-byte aligned, or the plan does not fit the device).
+bool bwd_weight_tc_supported(const Geometry& g, DType dt);
+int64_t bwd_weight_tc_workspace_bytes(const Geometry& g, DType dt);
+cudaError_t bwd_weight_tc_launch(const Geometry& g, const LaunchArgs& a, void* workspace, const DeviceInfo& dev);
 
 // ---- Kc alone (epilogue test entry) --------------------------------------
 cudaError_t epilogue_launch(const float* acc, const void* bias, void* y, int64_t rows, int cols,

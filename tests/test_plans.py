@@ -39,7 +39,7 @@ def harness(tmp_path_factory):
         pytest.skip("nvcc not available")
     out = tmp_path_factory.mktemp("plans")
     exes = {}
-    for name in ("plan_tc", "plan_dw", "plan_select"):
+    for name in ("plan_tc", "plan_dw", "plan_select", "plan_bwt"):
         exe = str(out / name)
         subprocess.run([nvcc, "-std=c++17", "-O1", "-gencode", "arch=compute_103a,code=sm_103a",
                         "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include"),
@@ -287,3 +287,89 @@ def test_selector_agrees_with_launch_planners(harness, sms):
     for name in ("dw3d_f32_c256", "dw3d_f16_c256_z5"):
         assert by_name[name]["dw_sel"] and by_name[name]["dw_plan"], by_name[name]
         assert by_name[name]["dw_TC"] < 256, by_name[name]
+
+
+def _bwt_candidates():
+    """Every 16-bit workload family and random grouped problems in the
+    backward-weight tensor-core route's shape range (Cg == Kg dividing 64)."""
+    probs = [wl for wl in inputs.all_workloads() if wl.dtype != "f32"]
+    rng = np.random.default_rng(91)
+    for i in range(300):
+        Cg = int(rng.choice([1, 2, 4, 8, 16, 32, 64]))
+        G = 64 // Cg * int(rng.integers(1, 5))
+        nd = 3 if rng.random() < 0.2 else 2
+        s = int(rng.integers(1, 3))
+        k = int(rng.integers(1, 5))
+        d = int(rng.integers(1, 3))
+        hw = (int(rng.integers(2, 70)), int(rng.integers(2, 70)))
+        inp = (int(rng.integers(2, 9)) if nd == 3 else 1, *hw)
+        ker = (int(rng.integers(1, 4)) if nd == 3 else 1, k, k)
+        pad = (int(rng.integers(0, 2)) if nd == 3 else 0, int(rng.integers(0, k)), int(rng.integers(0, k)))
+        probs.append(inputs.Workload(f"bwt{i}", 0, i, nd, int(rng.integers(1, 4)), G, Cg, Cg, inp, ker,
+                                     (1, s, s), pad, (1, d, d), "bf16" if i % 2 else "f16", False))
+    return [wl for wl in probs if min(_geom(wl)[0]) >= 1]
+
+
+def test_backward_weight_tc_plans(harness):
+    """The tensor-core backward-weight plans keep every copy, MMA operand,
+    accumulator column and workspace write inside its buffer, and their
+    phase / offset tables reproduce the convolution's input coordinates."""
+    probs = _bwt_candidates()
+    lines = [" ".join(map(str, _geom(wl)[1] + [int(wl.dtype == "f16")])) for wl in probs]
+    res = _run(harness["plan_bwt"], lines)
+    assert len(res) == len(probs)
+    n_ok = 0
+    for wl, p in zip(probs, res):
+        shape_ok = wl.Cg == wl.Kg and 64 % wl.Cg == 0 and (wl.G * wl.Cg) % 64 == 0 and \
+            wl.stride[1] == wl.stride[2] and wl.stride[1] <= 2 and wl.ker[2] <= 4
+        if not p["ok"]:
+            continue
+        n_ok += 1
+        ctx = (wl, p)
+        assert shape_ok, ctx
+        s = wl.stride[1]
+        out, _ = _geom(wl)
+        Ho, Wo = out[1], out[2]
+        X, Y, Z = wl.ker[2], wl.ker[1], wl.ker[0]
+        # copies: boxes within TMA limits, landing inside their regions
+        assert s * p["P"] <= 256 and s * p["TH"] <= 256 and p["P"] <= 256, ctx
+        assert p["Kp"] % 16 == 0 and p["Kp"] >= 32 and p["TH"] * p["P"] <= p["Kp"], ctx
+        assert p["tx_bytes"] == (1 + p["nplane"]) * p["TH"] * p["P"] * 128, ctx
+        assert p["dy_bytes"] % 1024 == 0 and p["dy_bytes"] >= p["Kp"] * 128, ctx
+        assert p["plane_bytes"] % 1024 == 0 and p["stage_bytes"] == p["dy_bytes"] + p["nplane"] * p["plane_bytes"]
+        assert 2 <= p["stages"] <= 4, ctx
+        assert 1024 + p["stages"] * p["stage_bytes"] <= p["smem"] <= SMEM_BLOCK, ctx
+        # MMA operands: the last K step's B rows stay inside the x plane
+        for r in p["runs"]:
+            last = p["Kp"] - 16 + r["u0"] + (r["len"] - 1) * r["du"] + 15
+            assert last < p["plane_bytes"] // 128, ctx
+            assert r["idesc"] >> 24 == 4 and (r["idesc"] >> 17) & 63 == 64 * r["len"] // 8, ctx
+            assert (r["idesc"] >> 15) & 3 == 3, ctx  # both operands MN-major
+        # taps: every tap of the row exactly once, each at its input column
+        kxs = sorted(k for r in p["runs"] for k in r["kx"])
+        assert kxs == list(range(X)), ctx
+        for r in p["runs"]:
+            for b, kx in enumerate(r["kx"]):
+                v = kx * wl.dil[2] - wl.pad[2]
+                px = v % s
+                qx = (v - px) // s
+                assert px == p["plane_px"][r["plane"]], ctx
+                assert qx - p["qx_min"] == r["u0"] + b * r["du"], ctx
+                assert 0 <= r["u0"] + b * r["du"] <= p["P"] - Wo, ctx
+        for kz in range(Z):
+            for ky in range(Y):
+                rr = kz * Y + ky
+                assert s * p["row_qy"][rr] + p["row_py"][rr] == ky * wl.dil[1] - wl.pad[1], ctx
+        # tensor memory: two accumulator sets of 64 columns per tap
+        assert p["ncols"] == 64 * X and p["tmem_cols"] >= 2 * p["ncols"], ctx
+        assert p["tmem_cols"] in (32, 64, 128, 256, 512), ctx
+        if p["tmem_cols"] > 256:
+            assert p["smem"] > SMEM_SM // 2, ctx
+        # work split and workspace
+        assert p["tiles_h"] * p["TH"] >= Ho and p["tiles"] == wl.N * out[0] * p["tiles_h"], ctx
+        assert 1 <= p["S"] <= p["tiles"], ctx
+        assert p["rows"] == Z * Y and p["chunks"] * 64 == wl.G * wl.Cg, ctx
+        assert p["grid"] == p["rows"] * p["chunks"] * p["S"], ctx
+        assert p["E"] == wl.G * wl.Kg * X * Y * Z * wl.Cg, ctx
+    assert n_ok >= 150
+
