@@ -286,6 +286,31 @@ __global__ void __launch_bounds__(1024) bwd_weight_reduce_kernel(const BwwArgs a
   }
 }
 
+// Stage 2 for few splits (S <= kSmallS): each thread owns 4 consecutive
+// elements and adds their S partials in split order (coalesced 16-byte
+// loads; the 32 x 32 form above would leave most of its rows idle).
+constexpr int kSmallS = 64;
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_weight_reduce_few_kernel(const BwwArgs a) {
+  T* __restrict__ dw = static_cast<T*>(a.dw);
+  grid_dependency_wait();  // the partials are complete
+  const int64_t n4 = a.E / 4;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+    float4 acc = reinterpret_cast<const float4*>(a.ws)[i];
+    for (int s = 1; s < a.S; ++s) {
+      const float4 v = reinterpret_cast<const float4*>(a.ws + (int64_t)s * a.E)[i];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    dw[4 * i] = epilogue_one<T>(acc.x, 0.f);
+    dw[4 * i + 1] = epilogue_one<T>(acc.y, 0.f);
+    dw[4 * i + 2] = epilogue_one<T>(acc.z, 0.f);
+    dw[4 * i + 3] = epilogue_one<T>(acc.w, 0.f);
+  }
+}
+
 // Launch plan: mode, vector width, items, CTA shape and splits.  Depends on
 // the problem and element size only (not on the device), so the workspace
 // size can be queried without a GPU.
@@ -404,6 +429,11 @@ cudaError_t reduce_typed(const Geometry& g, const LaunchArgs& la, float* ws, int
   a.dw = la.y;
   a.S = S;
   a.E = g.w_elems();
+  if (S <= kSmallS && a.E % 4 == 0) {
+    const int64_t blocks = std::min<int64_t>((a.E / 4 + 255) / 256, (int64_t)dev.num_sms * 8);
+    return launch_kernel(bwd_weight_reduce_few_kernel<T>, dim3((unsigned)std::max<int64_t>(1, blocks)), dim3(256),
+                         0, la, a);
+  }
   const int64_t blocks = std::min<int64_t>((a.E + 31) / 32, (int64_t)dev.num_sms * 2);
   return launch_kernel(bwd_weight_reduce_kernel<T>, dim3((unsigned)std::max<int64_t>(1, blocks)), dim3(1024), 0, la,
                        a);

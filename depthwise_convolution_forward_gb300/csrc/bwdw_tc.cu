@@ -239,15 +239,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwt_kernel(const __grid_constant_
             tc::tmem_ld16(lane_addr + col + (uint32_t)c16, p0);
             tc::tmem_ld16(lane_addr + a.ncols + col + (uint32_t)c16, p1);
             tc::tmem_ld_wait();
-            if (lane < 16) {
+            if (lane < 16 && c16 + 16 > cl0 && c16 < cl0 + a.Cg) {
+              float v[16];
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const int cl = c16 + e;
-                if (cl >= cl0 && cl < cl0 + a.Cg) {
-                  // a split without tiles issued no MMA: its partial is zero
-                  const float v = has_split ? __uint_as_float(p0[e]) + __uint_as_float(p1[e]) : 0.f;
-                  wsp[(int64_t)tap * a.Cg + (cl - cl0)] = v;
-                }
+              for (int e = 0; e < 16; ++e)  // a split without tiles issued no MMA: its partial is zero
+                v[e] = has_split ? __uint_as_float(p0[e]) + __uint_as_float(p1[e]) : 0.f;
+              float* dst = wsp + (int64_t)tap * a.Cg + (c16 - cl0);
+              if (a.Cg >= 16) {  // the whole piece is the row's block: 16-byte aligned stores
+#pragma unroll
+                for (int e = 0; e < 16; e += 4)
+                  *reinterpret_cast<float4*>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  if (c16 + e >= cl0 && c16 + e < cl0 + a.Cg) dst[e] = v[e];
               }
             }
           }
