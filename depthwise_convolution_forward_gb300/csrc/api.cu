@@ -179,6 +179,7 @@ LaunchArgs make_args(const void* x, const void* w, const void* bias, void* y, DT
   a.test_flags = opt ? opt->test_flags : 0;
   for (int i = 0; i < 8; ++i) a.tile[i] = opt ? opt->tile[i] : 0;
   a.pdl = !(opt && opt->serial_launch);
+  a.omap = OutMap{};
   return a;
 }
 
@@ -498,8 +499,11 @@ gconv_status grouped_conv_bwd_data_ex(const void* dy, const void* w, void* dx, c
   }
   if (phases) {
     // per stride phase: its sub-filter (transposed channels) into the
-    // workspace, its stride-1 forward correlation of dy into the phase
-    // buffer, then the buffer's rows to the phase's dx positions
+    // workspace, then its stride-1 forward correlation of dy on the
+    // tensor-core kernel, whose epilogue writes the phase's outputs straight
+    // to their dx positions.  Where that kernel cannot take the call (a
+    // forced other kernel, pointers it cannot copy from), the correlation
+    // goes to the phase buffer and a scatter kernel places it.
     uint8_t* wt = static_cast<uint8_t*>(workspace);
     uint8_t* pb = wt + align256(g.w_elems() * es);
     LaunchArgs a = make_args(dy, w, nullptr, dx, t, stream, slot, opt);
@@ -527,6 +531,24 @@ gconv_status grouped_conv_bwd_data_ex(const void* dy, const void* w, void* dx, c
             LaunchArgs wa = make_args(dy, w, nullptr, wt, t, stream, slot, opt);
             e = phase_weight_launch(g, wa, pt, wt, slot->info);
             if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+            LaunchArgs da = make_args(dy, wt, nullptr, dx, t, stream, slot, opt);
+            da.omap.on = 1;
+            for (int i = 0; i < 3; ++i) {
+              da.omap.scale[i] = s3[i];
+              da.omap.add[i] = r3[i] - s3[i] * ph.d[i].off;
+              da.omap.lo[i] = ph.d[i].off;
+              da.omap.hi[i] = ph.d[i].off + ph.d[i].n;
+              da.omap.ext[i] = I3[i];
+            }
+            if ((forced == 0 || forced == GCONV_KERNEL_IGEMM_TC) &&
+                tc_supported(ph.fg, t, &da, slot->info.num_sms, slot->info.max_smem_optin)) {
+              e = tc_launch(ph.fg, da, slot->info);
+              if (e == cudaSuccess) {
+                if (opt) opt->selected = GCONV_KERNEL_IGEMM_TC;
+                continue;  // dx positions of this phase written
+              }
+              if (e != cudaErrorNotSupported) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+            }
             LaunchArgs fa = make_args(dy, wt, nullptr, pb, t, stream, slot, opt);
             s = launch_forward(ph.fg, fa, slot->info, forced, opt ? &opt->selected : nullptr);
             if (s != GCONV_OK) return s;
@@ -566,7 +588,7 @@ gconv_status grouped_conv_bwd_data_route(const gconv_problem* p, gconv_dtype dt,
           Phase3D ph;
           phase_3d(g, rd, rh, rw, &ph);
           if (ph.d[0].n == 0 || ph.d[1].n == 0 || ph.d[2].n == 0) continue;
-          n += ph.empty ? 1 : 3;
+          n += ph.empty ? 1 : 2;  // zeros; or sub-filter + forward written into dx
         }
   }
   *route = r;

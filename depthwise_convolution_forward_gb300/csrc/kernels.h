@@ -35,6 +35,15 @@ struct Geometry {
   int64_t w_elems() const { return (int64_t)K() * taps() * Cg; }
 };
 
+// Output placement for the tensor-core kernel (backward data by stride
+// phases): output coordinate v of dimension i (D, H, W) is kept when
+// lo[i] <= v < hi[i] and written at scale[i] * v + add[i] of a tensor with
+// extents ext[i] (same N and channel count); on = 0 keeps the plain layout.
+struct OutMap {
+  int on;
+  int scale[3], add[3], lo[3], hi[3], ext[3];
+};
+
 struct LaunchArgs {
   const void* x;
   const void* w;
@@ -47,6 +56,7 @@ struct LaunchArgs {
   int test_flags;
   int tile[8];  // tuning overrides, 0 = automatic
   bool pdl;     // programmatic dependent launch (the kernels wait on the grid dependency)
+  OutMap omap;  // tensor-core kernel only (others refuse a map that is on)
 };
 
 // Launches kernel k on a.stream.  With a.pdl the launch carries the

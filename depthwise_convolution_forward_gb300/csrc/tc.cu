@@ -352,7 +352,9 @@ cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
     if (encode_tiled(&ymap, tt, 5, la.y, ydims, ystrides, ybox, yestr, ysw) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  if (la.omap.on && p.a.epi_off != 0) return cudaErrorNotSupported;  // the TMA-store epilogue has no map
   TcArgs a = p.a;
+  a.om = la.omap;
   a.w_tma = w_tma;
   a.w_box_taps = box_taps;
   a.w = la.w;

@@ -82,6 +82,7 @@ struct TcArgs {
   int* status;
   uint64_t wait_limit_ns;
   int test_flags;
+  OutMap om;  // output placement (off: y in the plain NHWGK layout)
   // MMA lists computed on the host (ntab entries, issuer lists back to back),
   // or ntab = 0 to build them in the kernel.  Entry: x = A start offset >> 4
   // | B start offset >> 4 << 16 (bytes from the dynamic shared-memory base,
@@ -638,9 +639,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             epilogue_row_tma<T, 4>(lane_base, mt, G2, a.sc, a.Nn, valid, p, bias_s, stage_base, a.epi_slice_bytes,
                                    a.epi_w);
         } else {
-          const bool valid = i < a.TH && jj < a.TWo && oh < a.Ho && ow < a.Wo;
-          T* dst = yg + ((((int64_t)st.n * a.Do + st.od) * a.Ho + oh) * (int64_t)a.Wo + ow) * a.Ktot +
-                   (int64_t)g0 * a.Kg;
+          bool valid = i < a.TH && jj < a.TWo && oh < a.Ho && ow < a.Wo;
+          int64_t pix;
+          if (a.om.on) {  // kept outputs land at scale * v + add of the mapped tensor
+            valid = valid && st.od >= a.om.lo[0] && st.od < a.om.hi[0] && oh >= a.om.lo[1] && oh < a.om.hi[1] &&
+                    ow >= a.om.lo[2] && ow < a.om.hi[2];
+            pix = (((int64_t)st.n * a.om.ext[0] + (st.od * a.om.scale[0] + a.om.add[0])) * a.om.ext[1] +
+                   (oh * a.om.scale[1] + a.om.add[1])) * (int64_t)a.om.ext[2] + (ow * a.om.scale[2] + a.om.add[2]);
+          } else {
+            pix = (((int64_t)st.n * a.Do + st.od) * a.Ho + oh) * (int64_t)a.Wo + ow;
+          }
+          T* dst = yg + pix * a.Ktot + (int64_t)g0 * a.Kg;
           if (NP == 1) epilogue_row<T, 1>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8);
           else if (NP == 2) epilogue_row<T, 2>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8);
           else epilogue_row<T, 4>(lane_base, mt, G2, a.sc, a.Nn, valid, dst, bias_s, v8);

@@ -201,8 +201,12 @@ gconv_status grouped_conv_fwd_ex(const void *x, const void *w, const void *bias,
  *      when every stride phase plans on the tensor-core kernel: dx is cut
  *      into its stride phases (positions s*i + r per dimension); each phase
  *      is a stride-1 forward correlation of dy with the sub-filter of taps t
- *      that reach it (r + p - t*d divisible by s), computed into a phase
- *      buffer in the workspace and copied to the phase's dx positions;
+ *      that reach it (r + p - t*d divisible by s), run on the tensor-core
+ *      kernel, whose epilogue writes the phase's outputs straight to their
+ *      dx positions (phases with no taps are zero-filled).  When that kernel
+ *      cannot take a phase (a forced other kernel, dy or dx not 16-byte
+ *      aligned) the phase goes through a buffer in the workspace and a copy
+ *      to its dx positions instead;
  *   0. otherwise a direct gather kernel, which needs no workspace.
  * fp32 accumulation, one round-to-nearest-even cast.  Asynchronous on
  * `stream`.
@@ -230,8 +234,10 @@ gconv_status grouped_conv_bwd_data_ex(const void *dy, const void *w, void *dx, c
  * grouped_conv_bwd_data_route -- which route grouped_conv_bwd_data takes for
  * (p, dt) without a forced kernel: *route = 0 (direct gather), 1 (stride 1,
  * transposed flipped weights) or 2 (stride phases), and, if `launches` is
- * not NULL, how many kernels the call launches.  Host only, no GPU needed;
- * depends on the problem only.
+ * not NULL, how many kernels the call launches with 16-byte aligned
+ * buffers (route 2: two per phase with taps, one per phase without; a
+ * phase placed through the workspace buffer adds one).  Host only, no GPU
+ * needed; depends on the problem only.
  */
 gconv_status grouped_conv_bwd_data_route(const gconv_problem *p, gconv_dtype dt, int32_t *route, int32_t *launches);
 

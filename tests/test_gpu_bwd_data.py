@@ -148,16 +148,28 @@ PHASE_CASES = [
 
 @pytest.mark.parametrize("wl", PHASE_CASES, ids=lambda w: w.name)
 def test_stride_phase_route(orc, wl):
-    """Stride-phase route (forward kernels on the phase sub-filters, then a
-    scatter into dx) against the oracle and against the direct kernel."""
+    """Stride-phase route (the tensor-core kernel on the phase sub-filters,
+    writing dx directly) against the oracle and against the direct kernel."""
     route, launches = gc.grouped_conv_bwd_data_route(gc.problem_of(wl), gc.DTYPE_CODES[wl.dtype])
     assert route == 2 and launches >= 2, (route, launches)
     _, w, _ = inputs.make_inputs(wl)
     dy = make_dy(wl, 9400 + wl.variant)
     ref = orc.bwd_data(wl, dy, w)
     dx, sel, need = run_bwd(wl, dy, w)
-    assert need > 0 and sel != B.KERNEL_BWD_DATA_DIRECT
+    assert need > 0 and sel == B.KERNEL_IGEMM_TC
     assert_close(dx.double().numpy(), ref, wl.dtype, f"{wl.name} phases (kernel {sel})")
     dx2, sel2, _ = run_bwd(wl, dy, w, B.KERNEL_BWD_DATA_DIRECT)
     assert sel2 == B.KERNEL_BWD_DATA_DIRECT
     assert_close(dx2.double().numpy(), ref, wl.dtype, f"{wl.name} direct")
+
+
+@pytest.mark.parametrize("wl", PHASE_CASES[:3] + PHASE_CASES[-1:], ids=lambda w: w.name)
+def test_stride_phase_buffered_placement(orc, wl):
+    """A phase kernel that cannot write dx itself (the generic kernel,
+    forced) goes through the workspace's phase buffer and the scatter copy:
+    same dx."""
+    _, w, _ = inputs.make_inputs(wl)
+    dy = make_dy(wl, 9450 + wl.variant)
+    dx, sel, _ = run_bwd(wl, dy, w, force=B.KERNEL_DIRECT_GENERIC)
+    assert sel == B.KERNEL_DIRECT_GENERIC
+    assert_close(dx.double().numpy(), orc.bwd_data(wl, dy, w), wl.dtype, f"{wl.name} buffered phases")
