@@ -237,7 +237,7 @@ def oracle_threads() -> int:
     return int(env) if env else (os.cpu_count() or 1)
 
 
-def cpu_oracle_prepare(wls):
+def cpu_oracle_prepare(wls, op="fwd"):
     import numpy as np
 
     import oracle
@@ -249,14 +249,14 @@ def cpu_oracle_prepare(wls):
         x, w, b = inputs.make_inputs(wl)
         out = orc.out_shape(wl)
         prep.append(dict(wl=wl, x=orc._f64(x), w=orc._f64(w), b=orc._f64(b), out=out,
-                         total=roofline.outputs(wl, out), bytes=roofline.algorithmic_bytes(wl, out),
+                         total=roofline.outputs(wl, out), bytes=roofline.algorithmic_bytes(wl, out, op),
                          flops=roofline.flops(wl, out)))
     return orc, prep, np
 
 
 def cpu_baseline(wls, min_seconds=10.0, max_seconds=30.0, op="fwd"):
     """Whole-workload oracle passes, repeated for about min_seconds."""
-    orc, prep, np = cpu_oracle_prepare(wls)
+    orc, prep, np = cpu_oracle_prepare(wls, op)
     if op != "fwd":
         for p in prep:
             p["dy"] = np.random.default_rng(1).uniform(-1, 1, size=(p["wl"].N,) + tuple(
@@ -287,7 +287,7 @@ def run_reference(args, wls, rank, world):
     """--impl reference: the oracle on the host cores, bounded sample per step."""
     if rank != 0:
         return
-    orc, prep, np = cpu_oracle_prepare(wls)
+    orc, prep, np = cpu_oracle_prepare(wls, getattr(args, "op", "fwd"))
     total_steps = args.steps + args.warmup
     budget_s = 120.0
     per_step_s = budget_s / total_steps / len(prep)
@@ -403,7 +403,7 @@ class GpuArm:
             dt = gc.DTYPE_CODES[wl.dtype]
             kernel = self.opt.force_kernel or gc.grouped_conv_select(p, dt)
             convs.append(dict(wl=wl, x=x, w=w, b=b, p=p, ysh=ysh, out=out, dt=dt, kernel=kernel,
-                              bytes=roofline.algorithmic_bytes(wl, out), flops=roofline.flops(wl, out)))
+                              bytes=roofline.algorithmic_bytes(wl, out, self.op), flops=roofline.flops(wl, out)))
         per_set = sum(c["bytes"] for c in convs)
         R = max(3, -(-2 * L2_BYTES // max(per_set, 1)) + 1)
         sets = []

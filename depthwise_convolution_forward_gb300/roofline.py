@@ -12,6 +12,11 @@ Bytes count each tensor moved once:  x + y + w (+ bias), in the storage dtype,
 where x counts only the input positions some filter tap reads.  With stride 2
 and dilation 2 (pad 2) only every other row and column of the input is ever
 read, so a quarter of x; every other benchmarked problem reads all of it.
+
+The backward passes move the same three tensors: backward weight reads
+x (the touched positions) and dy (y's size) and writes dw (w's size);
+backward data reads dy and w and writes every position of dx, zeros
+included, so there x counts in full (``op="bwd_data"``).
 """
 from __future__ import annotations
 
@@ -33,11 +38,12 @@ def touched(i_ext: int, o_ext: int, k: int, s: int, p: int, d: int) -> int:
     return len({o * s - p + t * d for o in range(o_ext) for t in range(k)} & set(range(i_ext)))
 
 
-def tensor_bytes(wl, out_shape) -> dict:
+def tensor_bytes(wl, out_shape, op: str = "fwd") -> dict:
     es = ES[wl.dtype]
     read = 1
     for i in range(3):
-        read *= touched(wl.inp[i], out_shape[i], wl.ker[i], wl.stride[i], wl.pad[i], wl.dil[i])
+        read *= wl.inp[i] if op == "bwd_data" else \
+            touched(wl.inp[i], out_shape[i], wl.ker[i], wl.stride[i], wl.pad[i], wl.dil[i])
     x = wl.N * read * wl.C * es
     y = outputs(wl, out_shape) * es
     w = wl.K * wl.taps * wl.Cg * es
@@ -45,5 +51,5 @@ def tensor_bytes(wl, out_shape) -> dict:
     return {"x": x, "y": y, "w": w, "bias": b}
 
 
-def algorithmic_bytes(wl, out_shape) -> int:
-    return sum(tensor_bytes(wl, out_shape).values())
+def algorithmic_bytes(wl, out_shape, op: str = "fwd") -> int:
+    return sum(tensor_bytes(wl, out_shape, op).values())

@@ -44,3 +44,17 @@ def test_input_bytes_count_touched_positions():
     # brute force on a small odd case: positions o*s - p + t*d inside the input
     assert roofline.touched(7, 3, 3, 3, 0, 1) == 7 - 0  # windows [0,3), [3,6), [6,9) -> 0..6
     assert roofline.touched(7, 2, 2, 3, 0, 2) == 4      # {0, 2} and {3, 5}
+
+
+def test_backward_data_bytes_count_all_of_dx():
+    """Backward data writes every dx position (zeros where no output
+    reaches), so its x term is the whole input even when the forward pass
+    touches only a quarter of it."""
+    wl = inputs.by_name("sweep_g8_d2_s2_bf16")
+    out = [(wl.inp[i] + 2 * wl.pad[i] - wl.dil[i] * (wl.ker[i] - 1) - 1) // wl.stride[i] + 1 for i in range(3)]
+    fwd = roofline.tensor_bytes(wl, out)
+    bwd = roofline.tensor_bytes(wl, out, "bwd_data")
+    full = wl.N * wl.inp[0] * wl.inp[1] * wl.inp[2] * wl.C * 2
+    assert bwd["x"] == full and fwd["x"] == full // 4
+    assert roofline.algorithmic_bytes(wl, out, "bwd_weight") == roofline.algorithmic_bytes(wl, out)
+
