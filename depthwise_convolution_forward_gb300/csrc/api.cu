@@ -323,6 +323,86 @@ bool phase_3d(const Geometry& g, int rd, int rh, int rw, Phase3D* ph) {
   return true;
 }
 
+// All stride phases as one stride-1 forward problem.  For residue r of a
+// dimension, dx position s*m + r takes the taps t with r + p - t*d = s*q, from
+// dy row m + q.  Over every residue the offsets q span [qmin, qmax]; the
+// stacked problem convolves dy with a filter of Q = qmax - qmin + 1 offsets
+// per dimension whose output channels are (phase, dx channel) pairs, zero
+// where a phase has no tap at an offset.  Its output v maps to phase index
+// m = v - o_off (o_off = pad + qmin), written at s*m + r (OutMap mode 2).
+// Phases without taps come out as zeros.  Returns false when a dimension
+// has no tap reaching any residue.
+struct Stacked {
+  Geometry fg;
+  StackTaps st;
+  OutMap om;
+  int64_t w_elems;  // stacked weight elements
+};
+
+bool stacked_problem(const Geometry& g, Stacked* out) {
+  const int I[3] = {g.D, g.H, g.W}, O[3] = {g.Do, g.Ho, g.Wo}, k[3] = {g.Z, g.Y, g.X},
+            s[3] = {g.sD, g.sH, g.sW}, p[3] = {g.pD, g.pH, g.pW}, d[3] = {g.dD, g.dH, g.dW};
+  Stacked st{};
+  st.st.nph = s[0] * s[1] * s[2];
+  if (st.st.nph > kMaxStackPhases) return false;
+  Geometry f = g;
+  f.Cg = g.Kg, f.Kg = st.st.nph * g.Cg;
+  f.D = g.Do, f.H = g.Ho, f.W = g.Wo;
+  f.sD = f.sH = f.sW = 1;
+  f.dD = f.dH = f.dW = 1;
+  int fk[3], fp[3], fo[3];
+  st.om.on = 2;
+  for (int i = 0; i < 3; ++i) {
+    int qmin = 1 << 30, qmax = -(1 << 30);
+    for (int r = 0; r < s[i]; ++r)
+      for (int t = 0; t < k[i]; ++t) {
+        const int v = r + p[i] - t * d[i];
+        if (((v % s[i]) + s[i]) % s[i] != 0) continue;
+        const int q = (v - (((v % s[i]) + s[i]) % s[i])) / s[i];
+        qmin = std::min(qmin, q);
+        qmax = std::max(qmax, q);
+      }
+    if (qmin > qmax) return false;
+    const int Q = qmax - qmin + 1, M = (I[i] + s[i] - 1) / s[i];
+    const int pad = std::max(0, std::max(-qmin, M + qmax - O[i]));
+    fk[i] = Q, fp[i] = pad, fo[i] = O[i] + 2 * pad - Q + 1;
+    st.st.s[i] = s[i], st.st.p[i] = p[i], st.st.d[i] = d[i], st.st.k[i] = k[i];
+    st.st.Q[i] = Q, st.st.qmin[i] = qmin;
+    st.om.scale[i] = s[i];
+    st.om.add[i] = -s[i] * (pad + qmin);
+    st.om.lo[i] = pad + qmin;
+    st.om.hi[i] = fo[i];
+    st.om.ext[i] = I[i];
+  }
+  f.Z = fk[0], f.Y = fk[1], f.X = fk[2];
+  f.pD = fp[0], f.pH = fp[1], f.pW = fp[2];
+  f.Do = fo[0], f.Ho = fo[1], f.Wo = fo[2];
+  st.fg = f;
+  st.om.cpp = g.Cg, st.om.nph = st.st.nph, st.om.ctot = g.C();
+  for (int ph = 0; ph < st.st.nph; ++ph) {
+    st.om.res[ph][0] = ph / (s[1] * s[2]);
+    st.om.res[ph][1] = (ph / s[2]) % s[1];
+    st.om.res[ph][2] = ph % s[2];
+  }
+  st.w_elems = f.w_elems();
+  *out = st;
+  return true;
+}
+
+// The stacked phases on the tensor-core kernel (planned for a GB300), 16-bit
+// grouped data with a stride above 1.
+// Its epilogue stores 32-byte runs of one phase's channels (Cg a multiple of
+// 16) and reads one partial accumulator (tile override slot 4 = 1 for its
+// plans).
+bool stacked_route(const Geometry& g, DType dt, Stacked* st) {
+  if (g.sD == 1 && g.sH == 1 && g.sW == 1) return false;
+  if (dt == kF32 || g.Cg % 16 != 0) return false;
+  if (!stacked_problem(g, st)) return false;
+  LaunchArgs plan{};  // no buffers: alignment is checked at the call
+  plan.tile[4] = 1;
+  return tc_supported(st->fg, dt, &plan, kDefaultSms, kDefaultSmemOptin);
+}
+
 // The stride-phase route: a stride above 1 somewhere, grouped channels (the
 // depthwise case stays on the direct kernel's group vectors), 16-bit data,
 // and every phase's forward problem planned on the tensor-core kernel (on a
@@ -353,9 +433,11 @@ inline int64_t align256(int64_t v) { return (v + 255) / 256 * 256; }
 int64_t bwd_workspace_bytes(const Geometry& g, DType dt) {
   Geometry f;
   if (bwd_as_forward(g, &f)) return g.w_elems() * dtype_bytes(dt);
-  int64_t pb = 0;
-  if (phase_route(g, dt, &pb)) return align256(g.w_elems() * dtype_bytes(dt)) + pb;
-  return 0;
+  int64_t pb = 0, need = 0;
+  Stacked st;
+  if (stacked_route(g, dt, &st)) need = st.w_elems * dtype_bytes(dt);
+  if (phase_route(g, dt, &pb)) need = std::max(need, align256(g.w_elems() * dtype_bytes(dt)) + pb);
+  return need;
 }
 
 }  // namespace
@@ -470,11 +552,14 @@ gconv_status grouped_conv_bwd_data_ex(const void* dy, const void* w, void* dx, c
   Geometry fg;
   const bool as_fwd = forced != GCONV_KERNEL_BWD_DATA_DIRECT && bwd_as_forward(g, &fg);
   int64_t pb_bytes = 0;
-  const bool phases = !as_fwd && forced != GCONV_KERNEL_BWD_DATA_DIRECT && phase_route(g, t, &pb_bytes);
+  Stacked stk;
+  const bool stacked = !as_fwd && forced != GCONV_KERNEL_BWD_DATA_DIRECT && stacked_route(g, t, &stk);
+  const bool per_phase = !as_fwd && forced != GCONV_KERNEL_BWD_DATA_DIRECT && phase_route(g, t, &pb_bytes);
+  const bool phases = stacked || per_phase;
   if (forced != 0 && forced != GCONV_KERNEL_BWD_DATA_DIRECT && !as_fwd && !phases)
     return fail(GCONV_ERR_UNSUPPORTED, "kernel %d needs a forward-kernel route (stride 1 with pad <= dil*(k-1), "
                 "or stride phases of grouped 16-bit data)", forced);
-  const int64_t need = as_fwd ? g.w_elems() * es : (phases ? align256(g.w_elems() * es) + pb_bytes : 0);
+  const int64_t need = as_fwd ? g.w_elems() * es : (phases ? bwd_workspace_bytes(g, t) : 0);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15)))
     return fail(GCONV_ERR_INVALID_ARG, "workspace must be 16-byte aligned and hold %lld bytes",
                 (long long)need);
@@ -497,7 +582,25 @@ gconv_status grouped_conv_bwd_data_ex(const void* dy, const void* w, void* dx, c
     if (s != GCONV_OK) return s;
     return finish(slot, a, opt);
   }
-  if (phases) {
+  if (stacked && (forced == 0 || forced == GCONV_KERNEL_IGEMM_TC) && !((opt ? opt->test_flags : 0) & 2)) {
+    // every phase in one launch: the stacked sub-filters into the workspace,
+    // then the stacked forward problem on the tensor-core kernel, whose
+    // epilogue places each (phase, channel) output at its dx position
+    LaunchArgs da = make_args(dy, workspace, nullptr, dx, t, stream, slot, opt);
+    da.omap = stk.om;
+    da.tile[4] = 1;  // one partial accumulator
+    if (tc_supported(stk.fg, t, &da, slot->info.num_sms, slot->info.max_smem_optin)) {
+      LaunchArgs wa = make_args(dy, w, nullptr, workspace, t, stream, slot, opt);
+      e = phase_stack_launch(g, wa, stk.st, workspace, slot->info);
+      if (e == cudaSuccess) e = tc_launch(stk.fg, da, slot->info);
+      if (e == cudaSuccess) {
+        if (opt) opt->selected = GCONV_KERNEL_IGEMM_TC;
+        return finish(slot, da, opt);
+      }
+      if (e != cudaErrorNotSupported) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    }
+  }
+  if (per_phase) {
     // per stride phase: its sub-filter (transposed channels) into the
     // workspace, then its stride-1 forward correlation of dy on the
     // tensor-core kernel, whose epilogue writes the phase's outputs straight
@@ -558,6 +661,8 @@ gconv_status grouped_conv_bwd_data_ex(const void* dy, const void* w, void* dx, c
         }
     return finish(slot, a, opt);
   }
+  if (forced != 0 && forced != GCONV_KERNEL_BWD_DATA_DIRECT)
+    return fail(GCONV_ERR_UNSUPPORTED, "kernel %d cannot run this problem's stride phases", forced);
   LaunchArgs a = make_args(dy, w, nullptr, dx, t, stream, slot, opt);
   e = bwd_data_direct_launch(g, a, slot->info);
   if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
@@ -580,6 +685,8 @@ gconv_status grouped_conv_bwd_data_route(const gconv_problem* p, gconv_dtype dt,
   int r = 0, n = 1;
   if (bwd_as_forward(g, &f)) {
     r = 1, n = 2;
+  } else if (Stacked stk; stacked_route(g, (DType)dt, &stk)) {
+    r = 2, n = 2;  // stacked sub-filters, one tensor-core launch
   } else if (phase_route(g, (DType)dt, nullptr)) {
     r = 2, n = 0;
     for (int rd = 0; rd < g.sD; ++rd)

@@ -231,6 +231,42 @@ __global__ void __launch_bounds__(256) phase_weight_kernel(const T* __restrict__
   }
 }
 
+// Stacked phases: one sub-filter position q per dimension holds, for phase
+// ph (residue r per dimension), the tap t with r + p - t*d = s*(qmin + q),
+// if there is one; the stacked weights are zero elsewhere.
+template <typename T>
+__global__ void __launch_bounds__(256) phase_stack_kernel(const T* __restrict__ w, T* __restrict__ ws,
+                                                          const StackTaps st, int64_t total, int G, int Kg, int Cg,
+                                                          int Z, int Y, int X) {
+  grid_dependency_wait();  // w and the workspace are touched only from here on
+  for (int64_t o = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; o < total; o += (int64_t)gridDim.x * blockDim.x) {
+    int64_t f = o;
+    const int kc = (int)(f % Kg);  // dy channel = input channel of the stacked problem
+    f /= Kg;
+    int q[3];
+    q[2] = (int)(f % st.Q[2]);
+    f /= st.Q[2];
+    q[1] = (int)(f % st.Q[1]);
+    f /= st.Q[1];
+    q[0] = (int)(f % st.Q[0]);
+    f /= st.Q[0];
+    const int kp = (int)(f % (st.nph * Cg));
+    const int64_t g = f / (st.nph * Cg);
+    const int ph = kp / Cg, c = kp - ph * Cg;
+    const int r[3] = {ph / (st.s[1] * st.s[2]), (ph / st.s[2]) % st.s[1], ph % st.s[2]};
+    int t[3];
+    bool ok = true;
+    for (int i = 0; i < 3; ++i) {
+      const int num = r[i] + st.p[i] - st.s[i] * (st.qmin[i] + q[i]);
+      t[i] = num >= 0 && num % st.d[i] == 0 ? num / st.d[i] : -1;
+      ok = ok && t[i] >= 0 && t[i] < st.k[i];
+    }
+    T v = Elem<T>::from_f32(0.f);
+    if (ok) v = w[((((g * Kg + kc) * Z + t[0]) * Y + t[1]) * (int64_t)X + t[2]) * Cg + c];
+    ws[o] = v;
+  }
+}
+
 // Phase route, output: dx[n][sD*i + rD][sH*j + rH][sW*l + rW][:] =
 // pb[n][i + oD][j + oH][l + oW][:] for the phase's (i, j, l) < (nD, nH, nW),
 // or 0 when the phase has no taps.  V elements (16 or fewer bytes) per
@@ -362,6 +398,23 @@ cudaError_t phase_weight_launch(const Geometry& g, const LaunchArgs& a, const Ph
                            g.Cg, g.Z, g.Y, g.X);
   }
   return cudaErrorNotSupported;
+}
+
+cudaError_t phase_stack_launch(const Geometry& g, const LaunchArgs& a, const StackTaps& st, void* ws,
+                               const DeviceInfo& dev) {
+  const int64_t total = (int64_t)g.G * st.nph * g.Cg * st.Q[0] * st.Q[1] * st.Q[2] * g.Kg;
+  const dim3 grid(grid_blocks(total, dev)), block(256);
+  switch (a.dt) {
+    case kF16:
+      return launch_kernel(phase_stack_kernel<__half>, grid, block, 0, a, static_cast<const __half*>(a.w),
+                           static_cast<__half*>(ws), st, total, g.G, g.Kg, g.Cg, g.Z, g.Y, g.X);
+    case kBF16:
+      return launch_kernel(phase_stack_kernel<__nv_bfloat16>, grid, block, 0, a,
+                           static_cast<const __nv_bfloat16*>(a.w), static_cast<__nv_bfloat16*>(ws), st, total, g.G,
+                           g.Kg, g.Cg, g.Z, g.Y, g.X);
+    default:
+      return cudaErrorNotSupported;
+  }
 }
 
 cudaError_t phase_scatter_launch(const PhaseScatter& ps, const void* pb, void* dx, const LaunchArgs& a,

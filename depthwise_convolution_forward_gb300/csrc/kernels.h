@@ -36,12 +36,20 @@ struct Geometry {
 };
 
 // Output placement for the tensor-core kernel (backward data by stride
-// phases): output coordinate v of dimension i (D, H, W) is kept when
-// lo[i] <= v < hi[i] and written at scale[i] * v + add[i] of a tensor with
-// extents ext[i] (same N and channel count); on = 0 keeps the plain layout.
+// phases); on = 0 keeps the plain layout.
+//  on = 1: output coordinate v of dimension i (D, H, W) is kept when
+//          lo[i] <= v < hi[i] and written at scale[i] * v + add[i] of a
+//          tensor with extents ext[i] (same N and channel count).
+//  on = 2: phases stacked as output channels: output channel
+//          g * nph * cpp + ph * cpp + c goes to channel g * cpp + c (of ctot)
+//          at coordinate scale[i] * v + add[i] + res[ph][i], kept when
+//          v >= lo[i] and that coordinate is below ext[i].
+constexpr int kMaxStackPhases = 8;
 struct OutMap {
   int on;
   int scale[3], add[3], lo[3], hi[3], ext[3];
+  int cpp, nph, ctot;
+  int res[kMaxStackPhases][3];
 };
 
 struct LaunchArgs {
@@ -140,6 +148,15 @@ struct PhaseScatter {
 // a.w is w.
 cudaError_t phase_weight_launch(const Geometry& g, const LaunchArgs& a, const PhaseTaps& pt, void* wt,
                                 const DeviceInfo& dev);
+// Stacked phase weights: ws[g][ph * Cg + c][qz][qy][qx][k] = w[g][k][t][c]
+// for the tap t that reaches phase ph at sub-filter offset q (per dimension
+// t = (r + p - s * (qmin + q)) / d when that is a whole tap index), else 0.
+struct StackTaps {
+  int nph;
+  int s[3], p[3], d[3], k[3], Q[3], qmin[3];
+};
+cudaError_t phase_stack_launch(const Geometry& g, const LaunchArgs& a, const StackTaps& st, void* ws,
+                               const DeviceInfo& dev);
 // dx positions of one phase from the phase buffer pb (or zeros).
 cudaError_t phase_scatter_launch(const PhaseScatter& ps, const void* pb, void* dx, const LaunchArgs& a,
                                  const DeviceInfo& dev);

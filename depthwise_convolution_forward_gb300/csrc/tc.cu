@@ -353,6 +353,8 @@ cudaError_t tc_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
       return cudaErrorInvalidValue;
   }
   if (la.omap.on && p.a.epi_off != 0) return cudaErrorNotSupported;  // the TMA-store epilogue has no map
+  // the stacked epilogue reads one partial and stores 16-channel runs of one phase
+  if (la.omap.on == 2 && (p.a.np != 1 || la.omap.cpp % 16 != 0)) return cudaErrorNotSupported;
   TcArgs a = p.a;
   a.om = la.omap;
   a.w_tma = w_tma;

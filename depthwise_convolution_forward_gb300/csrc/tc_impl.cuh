@@ -177,6 +177,63 @@ __device__ __forceinline__ void epilogue_row(uint32_t lane_base, int mt, int G2,
   }
 }
 
+// Epilogue for one output row of a stacked-phase problem (OutMap mode 2,
+// one partial accumulator, channels per phase a multiple of 16): output
+// channel kk = k0 + column is (group, phase, channel), so each 16-column
+// piece lies in one phase and lands as one 32-byte run at its dx position,
+// when that position lies inside dx.  (group, phase, channel) advance by 16
+// channels per piece; the residues are recomputed only when the phase
+// changes.  No bias: backward data has none.
+template <typename T>
+__device__ __forceinline__ void epilogue_row_stacked(uint32_t lane_base, int mt, int sc, int Nn, bool valid, int n,
+                                                     int od, int oh, int ow, const OutMap& om, int k0, int Kgs,
+                                                     T* y) {
+  const int nchunk16 = sc * Nn / 16;
+  valid = valid && od >= om.lo[0] && oh >= om.lo[1] && ow >= om.lo[2];
+  const int base_d = od * om.scale[0] + om.add[0], base_h = oh * om.scale[1] + om.add[1],
+            base_w = ow * om.scale[2] + om.add[2];
+  int g = k0 / Kgs;
+  const int kp0 = k0 - g * Kgs;
+  int ph = kp0 / om.cpp, ch = kp0 - ph * om.cpp;
+  int rd = 0, rh = 0, rw = 0, cur = -1;
+  const int64_t row = (int64_t)om.ext[1] * om.ext[2];
+  for (int cc = 0; cc < nchunk16; ++cc) {
+    const int col = cc * 16;
+    const int j = col / Nn, cn = col - j * Nn;
+    uint32_t r[16];
+    tmem_ld16(lane_base + (uint32_t)((mt * sc + j) * Nn + cn), r);
+    tmem_ld_wait();
+    if (valid) {
+      if (ph != cur) {  // phase ph = (rd * sH + rh) * sW + rw
+        cur = ph;
+        rw = ph % om.scale[2];
+        const int rdh = ph / om.scale[2];
+        rh = rdh % om.scale[1], rd = rdh / om.scale[1];
+      }
+      const int md = base_d + rd, mh = base_h + rh, mw = base_w + rw;
+      if (md < om.ext[0] && mh < om.ext[1] && mw < om.ext[2]) {
+        T* dst = y + (((int64_t)n * om.ext[0] + md) * row + (int64_t)mh * om.ext[2] + mw) * om.ctot +
+                 (int64_t)g * om.cpp + ch;
+        uint32_t wd[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          wd[i] = epilogue_pair<T>(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), 0.f, 0.f);
+        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(wd[0]), "r"(wd[1]), "r"(wd[2]),
+                     "r"(wd[3])
+                     : "memory");
+        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 8), "r"(wd[4]), "r"(wd[5]), "r"(wd[6]),
+                     "r"(wd[7])
+                     : "memory");
+      }
+    }
+    ch += 16;  // next piece: 16 channels on, carrying into the phase and the group
+    if (ch == om.cpp) {
+      ch = 0;
+      if (++ph == om.nph) ph = 0, ++g;
+    }
+  }
+}
+
 // Epilogue into the shared-memory image of the tile's output box, for a
 // TMA tensor store.  The box is [TH][TWo][slice of the CTA's channels] per
 // channel slice of W bytes per pixel (W = 128, 64 or 32), each slice with the
@@ -640,6 +697,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                                    a.epi_w);
         } else {
           bool valid = i < a.TH && jj < a.TWo && oh < a.Ho && ow < a.Wo;
+          if (a.om.on == 2) {  // stacked phases (planned with one partial accumulator)
+            epilogue_row_stacked<T>(lane_base, mt, a.sc, a.Nn, valid, st.n, st.od, oh, ow, a.om, g0 * a.Kg, a.Kg,
+                                    yg);
+            continue;
+          }
           int64_t pix;
           if (a.om.on) {  // kept outputs land at scale * v + add of the mapped tensor
             valid = valid && st.od >= a.om.lo[0] && st.od < a.om.hi[0] && oh >= a.om.lo[1] && oh < a.om.hi[1] &&

@@ -102,7 +102,10 @@ typedef struct gconv_options {
                             device-side status (timeout) into the return value   */
   int64_t wait_limit_ns; /* bound on each in-kernel wait; 0 = 2 s                  */
   int32_t test_flags;    /* bit 0: withhold the first input copy of CTA 0 so its
-                            first wait cannot complete (timeout-path test)       */
+                            first wait cannot complete (timeout-path test);
+                            bit 1: backward data by stride phases launches one
+                            correlation per phase instead of one stacked
+                            launch (tests of that placement)                   */
   int32_t selected;      /* out: the gconv_kernel that was launched               */
   int32_t tile[8];       /* tuning overrides, 0 = automatic.
                             Depthwise kernel: [0] TH, [1] TW, [2] WB (row-blocked
@@ -198,15 +201,19 @@ gconv_status grouped_conv_fwd_ex(const void *x, const void *w, const void *bias,
  *      into the workspace) and padding dil*(k-1) - pad, on the forward
  *      kernels;
  *   2. a stride above 1 with grouped channels (not depthwise) in f16/bf16,
- *      when every stride phase plans on the tensor-core kernel: dx is cut
- *      into its stride phases (positions s*i + r per dimension); each phase
- *      is a stride-1 forward correlation of dy with the sub-filter of taps t
- *      that reach it (r + p - t*d divisible by s), run on the tensor-core
- *      kernel, whose epilogue writes the phase's outputs straight to their
- *      dx positions (phases with no taps are zero-filled).  When that kernel
- *      cannot take a phase (a forced other kernel, dy or dx not 16-byte
- *      aligned) the phase goes through a buffer in the workspace and a copy
- *      to its dx positions instead;
+ *      when the stride phases plan on the tensor-core kernel: dx is cut
+ *      into its stride phases (positions s*i + r per dimension); phase r is
+ *      a stride-1 forward correlation of dy with the sub-filter of taps t
+ *      that reach it (r + p - t*d divisible by s).  All phases run as one
+ *      tensor-core launch: the sub-filters are stacked as output channels
+ *      (phase, channel) of one filter over the union of their offsets, and
+ *      the epilogue writes each (phase, channel) output to its dx position
+ *      (phases with no taps come out as zeros).  Where that launch does not
+ *      plan (Cg not a multiple of 16, too many stacked channels) each
+ *      phase runs on its own,
+ *      written straight into dx; a phase the tensor-core kernel cannot take
+ *      (a forced other kernel, dy or dx not 16-byte aligned) goes through a
+ *      buffer in the workspace and a copy to its dx positions instead;
  *   0. otherwise a direct gather kernel, which needs no workspace.
  * fp32 accumulation, one round-to-nearest-even cast.  Asynchronous on
  * `stream`.
@@ -235,8 +242,9 @@ gconv_status grouped_conv_bwd_data_ex(const void *dy, const void *w, void *dx, c
  * (p, dt) without a forced kernel: *route = 0 (direct gather), 1 (stride 1,
  * transposed flipped weights) or 2 (stride phases), and, if `launches` is
  * not NULL, how many kernels the call launches with 16-byte aligned
- * buffers (route 2: two per phase with taps, one per phase without; a
- * phase placed through the workspace buffer adds one).  Host only, no GPU
+ * buffers (route 2: two for the stacked launch; else two per phase with
+ * taps and one per phase without, and a phase placed through the workspace
+ * buffer adds one).  Host only, no GPU
  * needed; depends on the problem only.
  */
 gconv_status grouped_conv_bwd_data_route(const gconv_problem *p, gconv_dtype dt, int32_t *route, int32_t *launches);

@@ -36,8 +36,9 @@ def make_dy(wl, seed):
     return (torch.rand(out_shape_of(wl), generator=g, dtype=torch.float32) * 2 - 1).to(inputs.DTYPES[wl.dtype])
 
 
-def run_bwd(wl, dy, w, force=0):
-    """dx on the host and the kernel that produced it."""
+def run_bwd(wl, dy, w, force=0, test_flags=0):
+    """dx on the host and the kernel that produced it (test_flags bit 1: one
+    launch per stride phase instead of the stacked launch)."""
     dt = inputs.DTYPES[wl.dtype]
     p = gc.problem_of(wl)
     code = gc.DTYPE_CODES[wl.dtype]
@@ -51,6 +52,7 @@ def run_bwd(wl, dy, w, force=0):
     ws = torch.empty(max(need, 1), dtype=torch.uint8, device=DEV) if need else None
     opt = B.gconv_options()
     opt.force_kernel = force
+    opt.test_flags = test_flags
     opt.debug = 1
     gc.grouped_conv_bwd_data_ex(dyd, wd, dx, p, code, ws, need, torch.cuda.current_stream(DEV), opt)
     torch.cuda.synchronize(DEV)
@@ -148,8 +150,9 @@ PHASE_CASES = [
 
 @pytest.mark.parametrize("wl", PHASE_CASES, ids=lambda w: w.name)
 def test_stride_phase_route(orc, wl):
-    """Stride-phase route (the tensor-core kernel on the phase sub-filters,
-    writing dx directly) against the oracle and against the direct kernel."""
+    """Stride-phase route: the stacked launch (every phase as output
+    channels of one tensor-core problem) and one launch per phase, both
+    writing dx directly, against the oracle and the direct kernel."""
     route, launches = gc.grouped_conv_bwd_data_route(gc.problem_of(wl), gc.DTYPE_CODES[wl.dtype])
     assert route == 2 and launches >= 2, (route, launches)
     _, w, _ = inputs.make_inputs(wl)
@@ -157,7 +160,10 @@ def test_stride_phase_route(orc, wl):
     ref = orc.bwd_data(wl, dy, w)
     dx, sel, need = run_bwd(wl, dy, w)
     assert need > 0 and sel == B.KERNEL_IGEMM_TC
-    assert_close(dx.double().numpy(), ref, wl.dtype, f"{wl.name} phases (kernel {sel})")
+    assert_close(dx.double().numpy(), ref, wl.dtype, f"{wl.name} stacked phases (kernel {sel})")
+    dx1, sel1, _ = run_bwd(wl, dy, w, test_flags=2)
+    assert sel1 == B.KERNEL_IGEMM_TC
+    assert_close(dx1.double().numpy(), ref, wl.dtype, f"{wl.name} one launch per phase (kernel {sel1})")
     dx2, sel2, _ = run_bwd(wl, dy, w, B.KERNEL_BWD_DATA_DIRECT)
     assert sel2 == B.KERNEL_BWD_DATA_DIRECT
     assert_close(dx2.double().numpy(), ref, wl.dtype, f"{wl.name} direct")
