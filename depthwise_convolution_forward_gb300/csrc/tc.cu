@@ -33,8 +33,14 @@ struct TcPlan {
   bool ok;
 };
 
+// aligned: (128-byte rows only) one copy of the tile per stride phase and
+// column shift cx of the taps, each copy shifted left by cx and laid out
+// with a pitch rounded up to 8 pixels, so every tap's A operand starts on
+// an 8-row boundary.  MMAs whose A start is not a multiple of 8 rows
+// measured about 57 cycles against 39-48 aligned (M = 128, N <= 64) on
+// GB300; the copies cost shared memory (up to 3x the input tile).
 bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, const int* ov, bool allow_sw,
-                       TcPlan* out) {
+                       bool aligned, TcPlan* out, double* cost_out) {
   TcArgs a;
   std::memset(&a, 0, sizeof(a));
   const int m = merge_factor(g);
@@ -53,6 +59,7 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
   const bool sw = allow_sw && g.C() % 64 == 0 && 64 % a.Kt == 0 && a.n_gc % (64 / a.Kt) == 0 && !(ov && ov[6] == 1);
   a.sc = sw ? 64 / a.Kt : 1;
   if (sw) a.nchunks = 1;
+  if (aligned && !sw) return false;
   a.ntaps = taps;
   a.Dh = (g.Z - 1) * g.dD + 1;
   // Phase decomposition: input row of tap ky for output row oh is
@@ -75,21 +82,24 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     qx_max = std::max(qx_max, qx[kx]);
   }
   a.qy_min = qy_min, a.qx_min = qx_min;
-  // used phases
-  int phase_of[4];
+  // used planes: one per stride phase (py, px), and in aligned mode one per
+  // (phase, column shift cx = qx - qx_min); plane_of[ky][kx]
+  int plane_of[16][16];
   a.nphase = 0;
-  for (int p = 0; p < 4; ++p) phase_of[p] = -1;
   for (int ky = 0; ky < g.Y; ++ky)
     for (int kx = 0; kx < g.X; ++kx) {
-      const int p = py[ky] * 2 + px[kx];
-      if (phase_of[p] < 0) {
-        phase_of[p] = a.nphase;
-        a.phase_py[a.nphase] = py[ky];
-        a.phase_px[a.nphase] = px[kx];
-        ++a.nphase;
+      const int cx = aligned ? qx[kx] - qx_min : 0;
+      int pl = -1;
+      for (int q = 0; q < a.nphase; ++q)
+        if (a.phase_py[q] == py[ky] && a.phase_px[q] == px[kx] && a.plane_cx[q] == cx) pl = q;
+      if (pl < 0) {
+        if (a.nphase == tc::kMaxPhases) return false;
+        pl = a.nphase++;
+        a.phase_py[pl] = py[ky], a.phase_px[pl] = px[kx], a.plane_cx[pl] = cx;
       }
+      plane_of[ky][kx] = pl;
     }
-  const int range_x = qx_max - qx_min, range_y = qy_max - qy_min;
+  const int range_x = aligned ? 0 : qx_max - qx_min, range_y = qy_max - qy_min;
   const uint32_t budget = (uint32_t)std::min(max_smem, 227 * 1024);
   // Tile shape: full output rows when they fit, TH rows so the flattened
   // M = TH * pitch fills nmt MMAs of 128 rows.  Every candidate nmt is
@@ -105,9 +115,10 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     const int nmt = combo / 3 + 1, np_cand = 1 << (combo % 3);
     if (ov && ov[2] && ov[2] != nmt) continue;
     TcArgs c = a;
-    const int TWo = std::min(g.Wo, std::min(tw_cap, 128 * nmt - range_x));
+    int TWo = std::min(g.Wo, std::min(tw_cap, 128 * nmt - range_x));
+    if (aligned) TWo = std::min(TWo, (std::min(256 / a.s, 128 * nmt) / 8) * 8);  // pitch round_up(TWo, 8) fits
     if (TWo < 1) continue;
-    const int P = TWo + range_x;
+    const int P = aligned ? (int)round_up((uint32_t)TWo, 8) : TWo + range_x;
     int TH = std::min(g.Ho, (128 * nmt) / P);
     if (ov && ov[0]) TH = std::min(ov[0], (128 * nmt) / P);
     if (TH < 1) continue;
@@ -123,8 +134,8 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
       for (int ky = 0; ky < g.Y; ++ky)
         for (int kx = 0; kx < g.X; ++kx) {
           const int t = (z * g.Y + ky) * g.X + kx;
-          c.tap_phase[t] = phase_of[py[ky] * 2 + px[kx]];
-          c.tap_off[t] = z * g.dD * c.Hh * c.P + (qy[ky] - qy_min) * c.P + (qx[kx] - qx_min);
+          c.tap_phase[t] = plane_of[ky][kx];
+          c.tap_off[t] = z * g.dD * c.Hh * c.P + (qy[ky] - qy_min) * c.P + (aligned ? 0 : qx[kx] - qx_min);
           max_off = std::max(max_off, c.tap_off[t]);
         }
     const uint32_t plane_px = round_up((uint32_t)std::max(c.Dh * c.Hh * c.P, c.nmt * 128 + max_off), 8);
@@ -254,12 +265,26 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
   }
   if (best >= 1e30) return false;
   *out = bestp;
+  if (cost_out) *cost_out = best;
   return true;
 }
 
+// Override slot 5: 2 = aligned copies (1 or 0 = shifted starts, the
+// default).  The copies measured slower on every configuration tried on
+// GB300 (ResNeXt (a) 26.7 against 23.9 us, sweep G=64 d1 s1 46.6 against
+// 45.0 us): they fit only one M tile and two stages per CTA, which costs
+// more than the faster MMAs save.
 bool make_tc_plan(const Geometry& g, bool bf16, int num_sms, int max_smem, const int* ov, TcPlan* out) {
-  return make_tc_plan_mode(g, bf16, num_sms, max_smem, ov, true, out) ||
-         make_tc_plan_mode(g, bf16, num_sms, max_smem, ov, false, out);
+  const int mode = ov && ov[5] == 2 ? 2 : 1;
+  TcPlan pa, pu;
+  double ca = 1e30, cu = 1e30;
+  const bool ok_a = mode == 2 && make_tc_plan_mode(g, bf16, num_sms, max_smem, ov, true, true, &pa, &ca);
+  const bool ok_u = mode != 2 && make_tc_plan_mode(g, bf16, num_sms, max_smem, ov, true, false, &pu, &cu);
+  if (ok_a || ok_u) {
+    *out = (ok_a && ca <= cu) ? pa : pu;
+    return true;
+  }
+  return mode != 2 && make_tc_plan_mode(g, bf16, num_sms, max_smem, ov, false, false, out, nullptr);
 }
 
 template <typename T>

@@ -44,7 +44,7 @@ namespace gconv {
 namespace tc {
 
 constexpr int kMaxTaps = 32;
-constexpr int kMaxPhases = 4;
+constexpr int kMaxPhases = 8;  // A planes per stage: stride phases (x column shift copies in aligned mode)
 constexpr int kMaxStages = 4;
 constexpr int kMaxAccBufs = 4;                    // accumulator buffers in tensor memory
 constexpr int kMaxTab = 2048;                     // host-built MMA list entries
@@ -60,8 +60,9 @@ struct TcArgs {
   int sD, pD, taps_total;  // depth stride / pad, taps per filter
   int TH, TWo, P, Hh, Dh;  // tile rows / cols, halo pitch, halo rows, halo planes
   int s, qy_min, qx_min;   // spatial stride, phase-row origin offsets
-  int nphase;
-  int phase_py[kMaxPhases], phase_px[kMaxPhases];
+  int nphase;              // A planes per stage
+  int phase_py[kMaxPhases], phase_px[kMaxPhases];  // the stride phase each plane holds
+  int plane_cx[kMaxPhases];  // column shift of the plane's copy (aligned mode), else 0
   int ntaps;
   int tap_phase[kMaxTaps], tap_off[kMaxTaps];
   int nchunks, Kt, Nn, KS, nmt;
@@ -572,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         uint8_t* stage = As + (size_t)s * a.a_stage_bytes;
         for (int ph = 0; ph < a.nphase; ++ph) {
           const int ih0 = a.s * (st.oh0 + a.qy_min) + a.phase_py[ph];
-          const int iw0 = a.s * (st.ow0 + a.qx_min) + a.phase_px[ph];
+          const int iw0 = a.s * (st.ow0 + a.qx_min + a.plane_cx[ph]) + a.phase_px[ph];
           if constexpr (SW) {
             tma_load_5d(stage + (size_t)ph * a.plane_stride, &xmap, &a_full[s], g0 * a.Cg, iw0, ih0, id0, st.n);
           } else {

@@ -125,7 +125,10 @@ typedef struct gconv_options {
                             Tensor-core kernel: [0] TH, [1] most accumulator
                             buffers (2-4; default as many as tensor memory
                             holds), [2] M tiles per CTA,
-                            [3] stages, [4] partial accumulators, [6] 1 = force
+                            [3] stages, [4] partial accumulators, [5] 2 = one
+                            copy of the tile per column shift, so every tap's
+                            A operand starts on an 8-row boundary (default:
+                            shifted starts), [6] 1 = force
                             16-byte chunk planes, [7] extra shared memory (KB),
                             negative: stage the tile's output box in shared
                             memory and write it with TMA tensor stores

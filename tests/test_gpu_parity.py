@@ -156,6 +156,33 @@ def test_tensor_core_epilogue_paths(orc, name, staged):
     assert_close(y.double().numpy(), ref, wl.dtype, f"{name} staged={staged}")
 
 
+ALIGNED_CASES = [
+    inputs.by_name("resnext_a_bf16").with_(N=2),
+    inputs.by_name("sweep_g64_d1_s1_bf16").with_(N=2),
+    inputs.by_name("sweep_g8_d1_s1_bf16").with_(N=2),
+    inputs.by_name("sweep_g32_d2_s1_bf16").with_(N=2),
+    inputs.by_name("sweep_g64_d2_s2_bf16").with_(N=2),
+    # ragged: odd width (pitch padded 23 -> 24), rows not a multiple of the tile
+    inputs.Workload("al_odd", 7, 2, 2, 2, 8, 16, 16, (1, 19, 23), (1, 3, 3), (1, 1, 1), (0, 1, 1), (1, 1, 1),
+                    "bf16", True),
+    inputs.Workload("al_f16", 7, 3, 2, 1, 16, 8, 8, (1, 17, 30), (1, 3, 3), (1, 1, 1), (0, 1, 1), (1, 2, 2),
+                    "f16", True),
+]
+
+
+@pytest.mark.parametrize("wl", ALIGNED_CASES, ids=lambda w: w.name)
+def test_tensor_core_aligned_copies(orc, wl):
+    """Tensor-core kernel with one copy of the tile per column shift
+    (override slot 5 = 2: every tap's A operand starts on an 8-row
+    boundary) against the oracle, and slot 5 = 1 (shifted starts)."""
+    x, w, b = inputs.make_inputs(wl)
+    ref = orc.forward(wl, x, w, b)
+    for mode in (2, 1):
+        y, sel = run_gpu(wl, x, w, b, force=B.KERNEL_IGEMM_TC, tile=[0, 0, 0, 0, 0, mode, 0, 0])
+        assert sel == B.KERNEL_IGEMM_TC
+        assert_close(y.double().numpy(), ref, wl.dtype, f"{wl.name} plane mode {mode}")
+
+
 def test_depthwise_3d(orc):
     wl = inputs.Workload("dw3d", 7, 1, 3, 2, 16, 1, 1, (5, 9, 10), (3, 3, 3), (2, 1, 1), (1, 1, 1),
                          (1, 1, 1), "f16", True)

@@ -218,7 +218,7 @@ def _check_tc_plan(wl, p):
 
 def test_tensor_core_plans(harness):
     probs = _tc_candidates()
-    lines = [" ".join(map(str, _geom(wl)[1] + [int(wl.dtype == "bf16"), 0, 0, 0, 0])) for wl in probs]
+    lines = [" ".join(map(str, _geom(wl)[1] + [int(wl.dtype == "bf16"), 0, 0, 0, 0, 0])) for wl in probs]
     res = _run(harness["plan_tc"], lines)
     assert len(res) == len(probs)
     planned = mergeable = 0
@@ -238,9 +238,9 @@ def test_tensor_core_overridden_plans(harness, name):
     plan keeps the invariants."""
     wl = inputs.by_name(name)
     combos = [(nmt, np_, st) for nmt in (1, 2, 3, 4) for np_ in (1, 2, 4) for st in (0, 2, 3)]
-    lines = [" ".join(map(str, _geom(wl)[1] + [int(wl.dtype == "bf16"), 0, nmt, st, np_])) for nmt, np_, st in combos]
+    lines = [" ".join(map(str, _geom(wl)[1] + [int(wl.dtype == "bf16"), 0, nmt, st, np_, 0])) for nmt, np_, st in combos]
     res = _run(harness["plan_tc"], lines)
-    auto = _run(harness["plan_tc"], [" ".join(map(str, _geom(wl)[1] + [int(wl.dtype == "bf16"), 0, 0, 0, 0]))])[0]
+    auto = _run(harness["plan_tc"], [" ".join(map(str, _geom(wl)[1] + [int(wl.dtype == "bf16"), 0, 0, 0, 0, 0]))])[0]
     assert auto["ok"]
     G2_per_nmt = auto["sc"]  # accumulators per M tile
     for (nmt, np_, st), p in zip(combos, res):
