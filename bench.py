@@ -162,12 +162,13 @@ def whole_job_rate(units_per_step: float, steps: int, world: int, max_ms: float)
 
 # ---------------------------------------------------------------------------
 # Sources each kernel's device code and launch plan are built from (the
-# tensor-core files do not enter the depthwise kernel, and so on).
+# tensor-core files do not enter the depthwise kernel, and so on; the API
+# layer's validation and dispatch do not change what a kernel moves).
 KERNEL_SOURCES = {
-    "direct_dw": ("api.cu", "common.cuh", "kernels.h", "plan_cache.h", "dw.cu", "dw_f16.cu", "dw_bf16.cu",
-                  "dw_f32.cu", "dw_impl.cuh", "dwc_impl.cuh", "dw_launch.cuh"),
-    "igemm_tc": ("api.cu", "common.cuh", "kernels.h", "plan_cache.h", "tc.cu", "tc_impl.cuh", "tc_ptx.cuh"),
-    "direct_generic": ("api.cu", "common.cuh", "kernels.h", "plan_cache.h", "generic.cu"),
+    "direct_dw": ("common.cuh", "kernels.h", "dw.cu", "dw_f16.cu", "dw_bf16.cu", "dw_f32.cu", "dw_impl.cuh",
+                  "dwc_impl.cuh", "dw_launch.cuh"),
+    "igemm_tc": ("common.cuh", "kernels.h", "tc.cu", "tc_impl.cuh", "tc_ptx.cuh"),
+    "direct_generic": ("common.cuh", "kernels.h", "generic.cu"),
 }
 
 
