@@ -155,6 +155,42 @@ class Oracle:
         return dw
 
 
+    def dw_pw_block(self, prob, x, w_dw, b_dw, act, w_pw, b_pw, dtype) -> np.ndarray:
+        """Depthwise convolution, activation, then a 1x1 projection: the tail
+        of a MobileNetV2-style block (the pages' depthwise benchmark layer and
+        its pointwise neighbour).  ``prob`` is the depthwise problem (G = C,
+        Cg = Kg = 1); ``w_pw`` is [K, C] (the 1x1 weight in GKYXC with G = 1),
+        ``b_pw`` [K] or None; ``act`` 0 none, 1 ReLU, 2 ReLU6 (min(max(v, 0),
+        6)).  The intermediate h = act(dw(x) + b_dw) is rounded once to the
+        storage ``dtype`` (a torch dtype), as a separate depthwise layer would
+        store it, then y = h @ w_pw^T + b_pw in float64 [N, Ho, Wo, K]."""
+        import torch  # the rounding step; the oracle's arithmetic stays float64
+
+        h = self.forward(prob, x, w_dw, b_dw)  # [N, Ho, Wo, C, 1]
+        if act == 1:
+            h = np.maximum(h, 0.0)
+        elif act == 2:
+            h = np.minimum(np.maximum(h, 0.0), 6.0)
+        elif act != 0:
+            raise ValueError("act must be 0, 1 or 2")
+        h = torch.from_numpy(np.ascontiguousarray(h)).to(dtype).double().numpy()
+        N, Ho, Wo = h.shape[0], h.shape[1], h.shape[2]
+        C = prob.G
+        wp = self._f64(w_pw).reshape(-1, C)
+        K = wp.shape[0]
+
+        class _Pw:  # the projection as a grouped convolution with G = 1, 1x1
+            ndim = 2
+            inp = (1, Ho, Wo)
+            ker = stride = dil = (1, 1, 1)
+            pad = (0, 0, 0)
+
+        pw = _Pw()
+        pw.N, pw.G, pw.Cg, pw.Kg = N, 1, C, K
+        y = self.forward(pw, h.reshape(N, Ho, Wo, C), wp, b_pw)
+        return y.reshape(N, Ho, Wo, K)
+
+
 _default: Optional[Oracle] = None
 
 
