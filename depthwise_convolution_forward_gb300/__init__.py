@@ -25,6 +25,9 @@ from ._binding import (  # noqa: F401
     grouped_conv_bwd_data_workspace_size,
     grouped_conv_fwd,
     grouped_conv_fwd_ex,
+    grouped_conv_fwd_dw_pw,
+    grouped_conv_fwd_dw_pw_ex,
+    grouped_conv_fwd_dw_pw_supported,
     grouped_conv_out_shape,
     grouped_conv_select,
     load_library,

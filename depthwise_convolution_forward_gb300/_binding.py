@@ -28,9 +28,10 @@ DTYPE_CODES = {"f32": GCONV_F32, "f16": GCONV_F16, "bf16": GCONV_BF16}
 KERNEL_AUTO, KERNEL_DIRECT_DW, KERNEL_DIRECT_GENERIC, KERNEL_IGEMM_TC = 0, 1, 2, 3
 KERNEL_BWD_DATA_DIRECT = 4
 KERNEL_BWD_WEIGHT = 5
+KERNEL_DW_PW = 6
 KERNEL_NAMES = {KERNEL_DIRECT_DW: "direct_dw", KERNEL_DIRECT_GENERIC: "direct_generic",
                 KERNEL_IGEMM_TC: "igemm_tc", KERNEL_BWD_DATA_DIRECT: "bwd_data_direct",
-                KERNEL_BWD_WEIGHT: "bwd_weight"}
+                KERNEL_BWD_WEIGHT: "bwd_weight", KERNEL_DW_PW: "dw_pw"}
 
 
 class gconv_problem(ctypes.Structure):
@@ -90,6 +91,13 @@ def load_library(path: Optional[str] = None):
         lib.grouped_conv_bwd_weight_workspace_size.argtypes = [prob_p, i32, ctypes.POINTER(i64)]
         lib.grouped_conv_bwd_data_route.restype = i32
         lib.grouped_conv_bwd_data_route.argtypes = [prob_p, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        lib.grouped_conv_fwd_dw_pw.restype = i32
+        lib.grouped_conv_fwd_dw_pw.argtypes = [vp, vp, vp, vp, vp, vp, prob_p, i32, i32, i32, vp]
+        lib.grouped_conv_fwd_dw_pw_ex.restype = i32
+        lib.grouped_conv_fwd_dw_pw_ex.argtypes = [vp, vp, vp, vp, vp, vp, prob_p, i32, i32, i32, vp,
+                                                  ctypes.POINTER(gconv_options)]
+        lib.grouped_conv_fwd_dw_pw_supported.restype = i32
+        lib.grouped_conv_fwd_dw_pw_supported.argtypes = [prob_p, i32, i32, i32, ctypes.POINTER(i32)]
         lib.grouped_conv_bwd_data_noalloc.restype = i32
         lib.grouped_conv_bwd_data_noalloc.argtypes = [vp, vp, vp, prob_p, i32, vp]
         lib.grouped_conv_bwd_data_workspace_size.restype = i32
@@ -271,3 +279,29 @@ def grouped_conv_bwd_data_noalloc(dy, w, dx, p: gconv_problem, dtype: int, strea
     lib = load_library()
     _check(lib.grouped_conv_bwd_data_noalloc(_ptr(dy), _ptr(w), _ptr(dx), ctypes.byref(p), dtype,
                                              _stream(stream)))
+
+
+def grouped_conv_fwd_dw_pw(x, w_dw, b_dw, w_pw, b_pw, y, p: gconv_problem, K: int, act: int, dtype: int,
+                           stream=None) -> None:
+    """Depthwise 3x3 + bias + activation, then the 1x1 projection + bias, in
+    one kernel (see gconv.h)."""
+    lib = load_library()
+    _check(lib.grouped_conv_fwd_dw_pw(_ptr(x), _ptr(w_dw), _ptr(b_dw), _ptr(w_pw), _ptr(b_pw), _ptr(y),
+                                      ctypes.byref(p), K, act, dtype, _stream(stream)))
+
+
+def grouped_conv_fwd_dw_pw_ex(x, w_dw, b_dw, w_pw, b_pw, y, p: gconv_problem, K: int, act: int, dtype: int,
+                              stream=None, opt: Optional[gconv_options] = None) -> gconv_options:
+    lib = load_library()
+    o = opt if opt is not None else gconv_options()
+    _check(lib.grouped_conv_fwd_dw_pw_ex(_ptr(x), _ptr(w_dw), _ptr(b_dw), _ptr(w_pw), _ptr(b_pw), _ptr(y),
+                                         ctypes.byref(p), K, act, dtype, _stream(stream), ctypes.byref(o)))
+    return o
+
+
+def grouped_conv_fwd_dw_pw_supported(p: gconv_problem, K: int, act: int, dtype: int) -> bool:
+    lib = load_library()
+    ok = ctypes.c_int32(0)
+    _check(lib.grouped_conv_fwd_dw_pw_supported(ctypes.byref(p), K, act, dtype, ctypes.byref(ok)))
+    return bool(ok.value)
+

@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "../../include/gconv.h"
+#include "fused.h"
 #include "kernels.h"
 
 namespace gconv {
@@ -761,6 +762,58 @@ gconv_status grouped_conv_bwd_weight_ex(const void* x, const void* dy, void* dw,
 gconv_status grouped_conv_bwd_weight(const void* x, const void* dy, void* dw, const gconv_problem* p, gconv_dtype dt,
                                      void* workspace, int64_t workspace_bytes, struct CUstream_st* stream) {
   return grouped_conv_bwd_weight_ex(x, dy, dw, p, dt, workspace, workspace_bytes, stream, nullptr);
+}
+
+gconv_status grouped_conv_fwd_dw_pw_ex(const void* x, const void* w_dw, const void* b_dw, const void* w_pw,
+                                       const void* b_pw, void* y, const gconv_problem* p, int32_t K, int32_t act,
+                                       gconv_dtype dt, struct CUstream_st* stream, gconv_options* opt) {
+  Geometry g;
+  gconv_status s = validate(p, &g);
+  if (s != GCONV_OK) return s;
+  if (dt != GCONV_F16 && dt != GCONV_BF16) return fail(GCONV_ERR_UNSUPPORTED, "the fused block takes f16 or bf16");
+  if (x == nullptr || w_dw == nullptr || w_pw == nullptr || y == nullptr)
+    return fail(GCONV_ERR_INVALID_ARG, "x, w_dw, w_pw and y must not be NULL");
+  if (K < 1) return fail(GCONV_ERR_INVALID_ARG, "K must be positive");
+  if (act < 0 || act > 2) return fail(GCONV_ERR_INVALID_ARG, "act must be 0, 1 or 2");
+  if (opt && opt->force_kernel != 0 && opt->force_kernel != GCONV_KERNEL_DW_PW)
+    return fail(GCONV_ERR_UNSUPPORTED, "kernel %d does not compute the fused block", opt->force_kernel);
+  const DType t = (DType)dt;
+  if (!dw_pw_supported(g, t, K, act))
+    return fail(GCONV_ERR_UNSUPPORTED, "the fused block takes 2D depthwise 3x3 (dilation 1, stride 1 or 2), "
+                "C %% 16 == 0 up to 256, K %% 8 == 0 up to 256, Wo up to 128");
+  const int es = dtype_bytes(t);
+  const int64_t yb = g.N * (int64_t)g.Ho * g.Wo * K * es, xb = g.x_elems() * es;
+  if (overlaps(y, yb, x, xb) || overlaps(y, yb, w_dw, g.w_elems() * es) ||
+      overlaps(y, yb, w_pw, (int64_t)K * g.C() * es) || (b_dw && overlaps(y, yb, b_dw, (int64_t)g.C() * es)) ||
+      (b_pw && overlaps(y, yb, b_pw, (int64_t)K * es)))
+    return fail(GCONV_ERR_INVALID_ARG, "y overlaps an input");
+  DevSlot* slot = nullptr;
+  cudaError_t e = device_slot(&slot);
+  if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "device query failed: %s", cudaGetErrorString(e));
+  LaunchArgs a = make_args(x, w_dw, b_dw, y, t, stream, slot, opt);
+  e = dw_pw_launch(g, a, w_pw, b_pw, K, act, slot->info);
+  if (e == cudaErrorNotSupported)
+    return fail(GCONV_ERR_UNSUPPORTED, "the fused block needs 16-byte aligned x, y and w_pw, and shared memory "
+                "for its tiles");
+  if (e != cudaSuccess) return fail(GCONV_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+  if (opt) opt->selected = GCONV_KERNEL_DW_PW;
+  return finish(slot, a, opt);
+}
+
+gconv_status grouped_conv_fwd_dw_pw(const void* x, const void* w_dw, const void* b_dw, const void* w_pw,
+                                    const void* b_pw, void* y, const gconv_problem* p, int32_t K, int32_t act,
+                                    gconv_dtype dt, struct CUstream_st* stream) {
+  return grouped_conv_fwd_dw_pw_ex(x, w_dw, b_dw, w_pw, b_pw, y, p, K, act, dt, stream, nullptr);
+}
+
+gconv_status grouped_conv_fwd_dw_pw_supported(const gconv_problem* p, int32_t K, int32_t act, gconv_dtype dt,
+                                              int32_t* ok) {
+  Geometry g;
+  gconv_status s = validate(p, &g);
+  if (s != GCONV_OK) return s;
+  if (ok == nullptr) return fail(GCONV_ERR_INVALID_ARG, "ok pointer is NULL");
+  *ok = (dt == GCONV_F16 || dt == GCONV_BF16) && act >= 0 && act <= 2 && dw_pw_supported(g, (DType)dt, K, act);
+  return GCONV_OK;
 }
 
 gconv_status grouped_conv_fwd(const void* x, const void* w, const void* bias, void* y, const gconv_problem* p,

@@ -92,7 +92,8 @@ typedef enum gconv_kernel {
   GCONV_KERNEL_DIRECT_GENERIC = 2, /* direct kernel for any shape/dtype/alignment   */
   GCONV_KERNEL_IGEMM_TC = 3,       /* Kb: tcgen05/TMEM grouped implicit GEMM        */
   GCONV_KERNEL_BWD_DATA_DIRECT = 4, /* backward data: direct gather kernel          */
-  GCONV_KERNEL_BWD_WEIGHT = 5       /* backward weight: split fp32 partials + reduce */
+  GCONV_KERNEL_BWD_WEIGHT = 5,      /* backward weight: split fp32 partials + reduce */
+  GCONV_KERNEL_DW_PW = 6            /* fused depthwise + activation + 1x1 projection */
 } gconv_kernel;
 
 /* Options of grouped_conv_fwd_ex.  Zero-initialise, then set what you need. */
@@ -377,6 +378,51 @@ const char *gconv_status_string(gconv_status s);
 
 /* Human-readable reason for the calling thread's last non-OK status. */
 const char *gconv_last_error(void);
+
+/*
+ * grouped_conv_fwd_dw_pw -- the tail of a MobileNetV2-style block in one
+ * kernel: a depthwise convolution with bias and activation, then a 1x1
+ * projection with bias.  The depthwise layer is the pages' MobileNetV2
+ * benchmark layer (TileOPs PR #1568, Code Review: the MobileNetV2 depthwise
+ * cases); the projection and the activation are its neighbours in that
+ * network, and fusing them keeps the intermediate h on chip instead of
+ * writing it to HBM and reading it back:
+ *   h[n, oh, ow, c] = round(act(sum_{yy,xx} x[n, oh*s - pH + yy, ow*s - pW + xx, c]
+ *                              * w_dw[c, 0, yy, xx, 0] + b_dw[c]))
+ *   y[n, oh, ow, k] = round(sum_c h[n, oh, ow, c] * w_pw[k, c] + b_pw[k])
+ * h is rounded to dt (round to nearest even) exactly as a separate depthwise
+ * layer would store it; both sums are fp32.
+ *   x     device, [N, H, W, C] packed, dtype dt            (read only)
+ *   w_dw  device, [C, 1, 3, 3, 1] (GKYXC with G = C)        (read only)
+ *   b_dw  device, [C], or NULL for no depthwise bias
+ *   w_pw  device, [K, C] (GKYXC with G = 1, 1x1), 16-byte aligned
+ *   b_pw  device, [K], or NULL for no projection bias
+ *   y     device, [N, Ho, Wo, K] packed (Ho, Wo from p), written; must not
+ *         overlap an input
+ *   p     the depthwise problem: 2D, G = C (Cg = Kg = 1), 3x3 filter,
+ *         dilation 1, equal H / W strides of 1 or 2, any padding
+ *   act   0 none, 1 ReLU (max(v, 0)), 2 ReLU6 (min(max(v, 0), 6)) on h
+ * Limits: dt f16 or bf16; C a multiple of 16 up to 256; K a multiple of 8 up
+ * to 256; Wo up to 128 and (Wo - 1) * s + 3 <= 256; x, y and w_pw 16-byte
+ * aligned.  Outside them the call returns GCONV_ERR_UNSUPPORTED and
+ * launches nothing (run grouped_conv_fwd and the projection separately).
+ * Asynchronous on `stream`; one launch.
+ */
+gconv_status grouped_conv_fwd_dw_pw(const void *x, const void *w_dw, const void *b_dw, const void *w_pw,
+                                    const void *b_pw, void *y, const gconv_problem *p, int32_t K, int32_t act,
+                                    gconv_dtype dt, struct CUstream_st *stream);
+
+/* grouped_conv_fwd_dw_pw with options (debug, wait limit, serial launch; opt->selected reports
+ * GCONV_KERNEL_DW_PW; force_kernel must be AUTO or GCONV_KERNEL_DW_PW). */
+gconv_status grouped_conv_fwd_dw_pw_ex(const void *x, const void *w_dw, const void *b_dw, const void *w_pw,
+                                       const void *b_pw, void *y, const gconv_problem *p, int32_t K,
+                                       int32_t act, gconv_dtype dt, struct CUstream_st *stream,
+                                       gconv_options *opt);
+
+/* Host only, no GPU needed: *ok = 1 when grouped_conv_fwd_dw_pw takes (p, K, act, dt) (its
+ * shape limits above; pointer alignment is checked at the call), else 0. */
+gconv_status grouped_conv_fwd_dw_pw_supported(const gconv_problem *p, int32_t K, int32_t act, gconv_dtype dt,
+                                              int32_t *ok);
 
 #ifdef __cplusplus
 }
