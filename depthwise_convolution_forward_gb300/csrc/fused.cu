@@ -10,25 +10,32 @@
 // round trip of h through HBM.  h is rounded to the storage type exactly as a
 // separate depthwise layer would store it.
 //
-// Design:
-//  * A CTA walks tiles of TH full output rows (TH * Wo <= 128 pixels).  Warp 0
-//    copies each tile's input rows with TMA, 16 channels per copy (the halo
-//    and the padding come from the box reaching past the tensor: zeros), 16
-//    to 64 channels per copy.
-//  * Warps 1-8 compute the depthwise outputs of a chunk: thread (pixel p,
-//    8-channel group) takes 8 channels of one pixel, mixed-precision FMAs
-//    (16-bit pairs in, fp32 products and sums) over the 9 taps,
-//    bias, activation, one round-to-nearest-even, and writes the 16 bytes
-//    straight into the K-major A operand of the projection (core matrices of
-//    8 pixels x 8 channels, no swizzle).
-//  * Once every chunk of the tile is written, one thread issues the
-//    projection: per 16 channels one tcgen05.mma (M = 128 pixels, N = K
-//    rounded up to 16, K = 16), accumulating in tensor memory.
-//  * Warps 1-4 (one per TMEM lane quarter) read the accumulators, add the
+// Design (one persistent CTA per SM, warp-specialised):
+//  * Output tiles of TH rows x TW columns (TW <= 16, TH * TW <= 128 pixels),
+//    walked round-robin by the CTAs.  Warp 0 copies each tile's haloed input
+//    box with TMA (all C channels in one copy, or in CH-channel chunks when
+//    that keeps two tiles in flight); reads past the tensor's edge fill with
+//    zeros, which is the convolution's zero padding.
+//  * Compute warps 6-13: a thread owns one tile column and one 8-channel
+//    group and walks down the column, loading each input row once (three
+//    16-byte loads, the horizontal taps) and adding it into every output row
+//    that uses it (three live rows at stride 1, two at stride 2).  Its 9 x 8
+//    weights stay in registers.  Lanes run over the channel groups first, so
+//    a warp's loads are consecutive 16-byte pieces of one shared-memory row.
+//    Mixed-precision FMAs (16-bit operands, fp32 products and sums), bias,
+//    activation, one round-to-nearest-even, and each output pixel's 8
+//    channels go as one 16-byte store into the projection's A operand:
+//    pixel-major rows of 128-byte-swizzled K atoms (64 channels), the layout
+//    a TMA copy with 128-byte swizzle would have written, so the stores of a
+//    warp spread over all banks.
+//  * Warp 1 issues the projection (one tcgen05.mma per 16 channels, M = 128
+//    pixel rows, N = K rounded up to 16) into one of two TMEM accumulators.
+//  * Warps 2-5 (one per TMEM lane quarter) read the accumulators, add the
 //    projection bias, round and store K channels per pixel.
-//  * All waits are bounded.  After a timeout a CTA records it in the status
-//    word and stops waiting, but still takes the same path through its
-//    barriers, so no warp is left behind.
+//  * A and the accumulators are double-buffered (A single when shared memory
+//    is short), so copies, depthwise math, MMAs and stores of neighbouring
+//    tiles overlap.  All waits are bounded; after a timeout a CTA records it
+//    in the status word, skips the remaining work and still reaches its exit.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -46,8 +53,14 @@ namespace gconv {
 namespace fz {
 
 constexpr int kMaxStages = 8;
-constexpr int kComputeWarps = 8;
-constexpr int kThreads = 32 * (1 + kComputeWarps);
+constexpr int kMaxA = 3;  // A buffers (barriers: 2 x 8 stages + 2 x 3 + 2 x 2 = 26 words of the first 256 bytes)
+constexpr int kMmaWarp = 1;
+constexpr int kEpiWarp0 = 2, kEpiWarps = 4;
+constexpr int kComputeWarp0 = 6, kComputeWarps = 8;
+constexpr int kComputeThreads = 32 * kComputeWarps;
+constexpr int kThreads = 32 * (kComputeWarp0 + kComputeWarps);
+constexpr uint32_t kAtomBytes = 128u * 128u;  // one 64-channel K atom of 128 pixel rows (128-byte swizzle)
+constexpr uint32_t kTailGroupBytes = 128u * 16u;  // one 8-channel group of 128 pixel rows (no swizzle)
 
 struct DwPwArgs {
   const void* w_dw;
@@ -55,76 +68,295 @@ struct DwPwArgs {
   const void* w_pw;
   const void* b_pw;
   void* y;
-  int C, K, Np;            // channels, projection outputs, N of the MMA (K rounded up to 16)
-  int Ho, Wo, s, act;      // output extents, stride, activation
-  int pH, pW;              // padding
-  int TH, tiles_h, tiles;  // output rows per tile, tiles per image, tiles in total
-  int Win, Hin;            // copied input columns / rows per tile
-  int CH, chunks, stages;  // channels per copied chunk (16..64), chunks, copy stages
-  uint32_t x_stage_bytes, x_stage_stride;  // bytes one copy lands (Win * Hin * CH * 2), stage spacing
+  int C, K, Np, G;                      // channels, projection outputs, N of the MMA (K rounded up to 16), C / 8
+  int Ho, Wo, act;                      // output extents, activation
+  int pH, pW;                           // padding
+  int TH, TW, tiles_h, tiles_w, tiles;  // tile = TH rows x TW columns; tiles down / across an image; in total
+  int Win, Hin;                         // input box columns / rows per tile
+  int CH, G8, chunks, stages, nA;       // channels per copy, its 8-channel groups, copies per tile, ring, A buffers
+  int NS, rps;                          // segments a column walk is split into, output rows per segment
+  uint32_t x_stage_bytes, x_stage_stride, a_bytes;
   uint32_t wdw_off, bdw_off, bpw_off, b_off, a_off, x_off;  // shared-memory offsets
   uint32_t tmem_cols, idesc;
   int* status;
   uint64_t wait_limit_ns;
 };
 
+// Two values rounded to nearest-even into one word (low half = first).
 template <typename T>
-__device__ __forceinline__ float act_f(float v, int act) {
-  if (act == 1) return fmaxf(v, 0.f);
-  if (act == 2) return fminf(fmaxf(v, 0.f), 6.f);
-  return v;
+__device__ __forceinline__ uint32_t pack_pair(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack_pair<__half>(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack_pair<__nv_bfloat16>(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// The same MMA issued by one lane of the converged issuing warp (elect.sync
+// picks it); every lane executes this with the same operands.
+__device__ __forceinline__ void mma_f16_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+// commit() by the elected lane (the one that issued the warp's MMAs).
+__device__ __forceinline__ void commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+// acc[0..7] (+)= one input row's three horizontal taps xr x the filter row's
+// weights wr[0..2] (8 channels each, 16-bit pairs).
 template <typename T>
+__device__ __forceinline__ void add_row(float (&acc)[8], const uint4 (&xr)[3], const uint4* wr) {
+#pragma unroll
+  for (int kx = 0; kx < 3; ++kx) {
+    fma_mixed_pair<T>(xr[kx].x, wr[kx].x, acc[0], acc[1]);
+    fma_mixed_pair<T>(xr[kx].y, wr[kx].y, acc[2], acc[3]);
+    fma_mixed_pair<T>(xr[kx].z, wr[kx].z, acc[4], acc[5]);
+    fma_mixed_pair<T>(xr[kx].w, wr[kx].w, acc[6], acc[7]);
+  }
+}
+
+// Activation and rounding of one output pixel's 8 channels (the bias is
+// already in acc), stored as 16 bytes at shared address addr.  act != 0
+// clamps to [0, hi] (hi = 6 for ReLU6, infinity for ReLU).
+template <typename T>
+__device__ __forceinline__ void put_h(uint32_t addr, float (&acc)[8], int act, float hi) {
+  if (act) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = fminf(fmaxf(acc[e], 0.f), hi);
+  }
+  uint32_t wd[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) wd[e] = pack_pair<T>(acc[2 * e], acc[2 * e + 1]);
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(wd[0]), "r"(wd[1]), "r"(wd[2]), "r"(wd[3])
+               : "memory");
+}
+
+// A holds the channels of whole 64-channel atoms in the 128-byte-swizzled
+// K-major layout and the remaining C % 64 channels (the tail) in the plain
+// K-major layout of 8-row x 16-byte core matrices, so it takes no more room
+// than C channels need.  Shared address of pixel row p in the thread's
+// 8-channel group g: gbase = the group's atom (or tail group) base, swz =
+// whether g lies in a swizzled atom.
+//   swizzled: 8-row block p / 8 (1024 B), row p % 8 (128 B), 16-byte chunk (g ^ p) % 8
+//   tail:     8-row block p / 8 (128 B), row p % 8 (16 B)
+__device__ __forceinline__ uint32_t a_addr(uint32_t gbase, bool swz, int p, int g) {
+  return swz ? gbase + (uint32_t)(p >> 3) * 1024u + (uint32_t)(p & 7) * 128u + ((uint32_t)((g ^ p) & 7) << 4)
+             : gbase + (uint32_t)(p >> 3) * 128u + (uint32_t)(p & 7) * 16u;
+}
+
+// Column walk over R output rows (j0 .. j0+R-1) of one tile column w and one
+// 8-channel group g, fully unrolled.  xs: the group's channels at box row 0,
+// box column w * S (tap 0); rowb / pixb: bytes per box row / column.  Each
+// input row is loaded once (three horizontal taps) and added into every
+// output row that uses it; output row j goes to A row p = j * TW + w.
+template <typename T, int S, int R>
+__device__ __forceinline__ void walk_fixed(const uint8_t* xs, uint32_t rowb, uint32_t pixb, const uint4 (&wv)[9],
+                                           const float (&bias)[8], int j0, int TW, int w, uint32_t gbase, bool swz,
+                                           int g, int act, float hi) {
+  float acc[R][8];
+  const uint8_t* x0 = xs + (size_t)(j0 * S) * rowb;
+#pragma unroll
+  for (int r = 0; r < (R - 1) * S + 3; ++r) {
+    uint4 xr[3];
+    const uint8_t* px = x0 + (size_t)r * rowb;
+    xr[0] = *reinterpret_cast<const uint4*>(px);
+    xr[1] = *reinterpret_cast<const uint4*>(px + pixb);
+    xr[2] = *reinterpret_cast<const uint4*>(px + 2 * pixb);
+#pragma unroll
+    for (int ky = 0; ky < 3; ++ky) {
+      // row r is filter row ky of output jj when jj * S + ky == r
+      if (r - ky < 0 || (r - ky) % S != 0 || (r - ky) / S >= R) continue;
+      const int jj = (r - ky) / S;
+      if (ky == 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[jj][e] = bias[e];
+      }
+      add_row<T>(acc[jj], xr, &wv[3 * ky]);
+      if (ky == 2) put_h<T>(a_addr(gbase, swz, (j0 + jj) * TW + w, g), acc[jj], act, hi);
+    }
+  }
+}
+
+// The same walk over R >= 2 output rows (runtime R) with a rolled loop: the
+// first and last input rows are peeled, and in between every input row
+// finishes one output row and starts the next (three live rows at stride
+// 1, two at stride 2), the accumulators moving down one role per row.  A
+// fraction of the unrolled walk's code, which measured faster for every
+// walk longer than one row (the unrolled body overflows the instruction
+// cache and the loop around it misses as well).
+template <typename T, int S>
+__device__ __forceinline__ void walk_roll(const uint8_t* xs, uint32_t rowb, uint32_t pixb, const uint4 (&wv)[9],
+                                          const float (&bias)[8], int j0, int R, int TW, int w, uint32_t gbase,
+                                          bool swz, int g, int act, float hi) {
+  const uint8_t* px = xs + (size_t)(j0 * S) * rowb;
+  auto ld = [&](uint4 (&xr)[3]) {
+    xr[0] = *reinterpret_cast<const uint4*>(px);
+    xr[1] = *reinterpret_cast<const uint4*>(px + pixb);
+    xr[2] = *reinterpret_cast<const uint4*>(px + 2 * pixb);
+    px += rowb;
+  };
+  auto start = [&](float (&acc)[8], const uint4 (&xr)[3]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = bias[e];
+    add_row<T>(acc, xr, &wv[0]);
+  };
+  auto put = [&](int j, float (&acc)[8]) { put_h<T>(a_addr(gbase, swz, (j0 + j) * TW + w, g), acc, act, hi); };
+  float A[8], B[8];
+  uint4 xr[3];
+  if constexpr (S == 1) {
+    // rows 0 and 1: outputs 0 (filter rows 0, 1) and 1 (filter row 0)
+    ld(xr);
+    start(A, xr);
+    ld(xr);
+    add_row<T>(A, xr, &wv[3]);
+    start(B, xr);
+#pragma unroll 1
+    for (int r = 2; r < R; ++r) {  // row r: finishes output r-2, continues r-1, starts r
+      ld(xr);
+      add_row<T>(A, xr, &wv[6]);
+      put(r - 2, A);
+      add_row<T>(B, xr, &wv[3]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) A[e] = B[e];
+      start(B, xr);
+    }
+    ld(xr);  // row R: finishes output R-2, continues R-1
+    add_row<T>(A, xr, &wv[6]);
+    put(R - 2, A);
+    add_row<T>(B, xr, &wv[3]);
+    ld(xr);  // row R+1: finishes output R-1
+    add_row<T>(B, xr, &wv[6]);
+    put(R - 1, B);
+  } else {
+    // rows 0 and 1: output 0 (filter rows 0, 1)
+    ld(xr);
+    start(A, xr);
+    ld(xr);
+    add_row<T>(A, xr, &wv[3]);
+#pragma unroll 1
+    for (int j = 1; j < R; ++j) {  // rows 2j (finishes output j-1, starts j) and 2j+1
+      ld(xr);
+      add_row<T>(A, xr, &wv[6]);
+      put(j - 1, A);
+      start(A, xr);
+      ld(xr);
+      add_row<T>(A, xr, &wv[3]);
+    }
+    ld(xr);  // row 2R: finishes output R-1
+    add_row<T>(A, xr, &wv[6]);
+    put(R - 1, A);
+    (void)B;
+  }
+}
+
+template <typename T, int S>
+__device__ __forceinline__ void walk_any(const uint8_t* xs, uint32_t rowb, uint32_t pixb, const uint4 (&wv)[9],
+                                         const float (&bias)[8], int j0, int j1, int TW, int w, uint32_t gbase,
+                                         bool swz, int g, int act, float hi) {
+  if (j1 - j0 == 1)
+    walk_fixed<T, S, 1>(xs, rowb, pixb, wv, bias, j0, TW, w, gbase, swz, g, act, hi);
+  else
+    walk_roll<T, S>(xs, rowb, pixb, wv, bias, j0, j1 - j0, TW, w, gbase, swz, g, act, hi);
+}
+
+template <typename T, int S>
 __global__ void __launch_bounds__(kThreads, 1) dw_pw_kernel(const __grid_constant__ CUtensorMap xmap,
                                                            const __grid_constant__ DwPwArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* x_full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* x_empty = x_full + kMaxStages;
-  uint64_t* mma_bar = x_empty + kMaxStages;
+  uint64_t* a_full = x_empty + kMaxStages;  // [nA] compute -> MMA: A written
+  uint64_t* a_empty = a_full + kMaxA;       // [nA] MMA -> compute: A read
+  uint64_t* acc_full = a_empty + kMaxA;     // [2] MMA -> epilogue: accumulators complete
+  uint64_t* acc_empty = acc_full + 2;       // [2] epilogue -> MMA: accumulators read
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 256);
   volatile int* failed = reinterpret_cast<volatile int*>(smem + 260);
-  T* wdw = reinterpret_cast<T*>(smem + a.wdw_off);          // [C/8][9 taps][8], the storage type
-  float* bdw = reinterpret_cast<float*>(smem + a.bdw_off);  // [C]
-  float* bpw = reinterpret_cast<float*>(smem + a.bpw_off);  // [Np]
-  uint8_t* Bs = smem + a.b_off;                              // [C/8][Np rows][16 B]
-  uint8_t* As = smem + a.a_off;                              // [C/8][128 rows][16 B]
-  uint8_t* Xs = smem + a.x_off;                              // stages x [Hin][Win][CH channels]
+  const T* wdw = reinterpret_cast<const T*>(smem + a.wdw_off);          // [G][9 taps][8], the storage type
+  const float* bdw = reinterpret_cast<const float*>(smem + a.bdw_off);  // [C]
+  const float* bpw = reinterpret_cast<const float*>(smem + a.bpw_off);  // [Np]
+  uint8_t* Xs = smem + a.x_off;                                          // stages x [Hin][Win][CH]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const T* __restrict__ wdg = static_cast<const T*>(a.w_dw);
-  const T* __restrict__ bdg = static_cast<const T*>(a.b_dw);
-  const T* __restrict__ wpg = static_cast<const T*>(a.w_pw);
-  const T* __restrict__ bpg = static_cast<const T*>(a.b_pw);
-  T* __restrict__ yg = static_cast<T*>(a.y);
 
   if (tid == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(&x_full[s], 1);
       mbar_init(&x_empty[s], kComputeWarps);
     }
-    mbar_init(mma_bar, 1);
+    for (int b = 0; b < kMaxA; ++b) {
+      mbar_init(&a_full[b], kComputeWarps);
+      mbar_init(&a_empty[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kEpiWarps);
+    }
     *failed = 0;
     fence_mbar_init();
     tma_prefetch_desc(&xmap);
   }
-  // Weights, biases and the projection's B operand, staged once per CTA
-  // after the wait on the previous grid (they are global memory).
+  const int per_img = a.tiles_h * a.tiles_w;
+  const int my_tiles = (int)blockIdx.x < a.tiles ? (a.tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int copies = my_tiles * a.chunks;
+  // copy k of this CTA: chunk k % chunks of its tile k / chunks, into stage
+  // k % stages (the input box of CH channels x Win columns x Hin rows from
+  // (oh0 * S - pH, ow0 * S - pW): the halo and the padding read as zeros)
+  auto issue_copy = [&](int k) {
+    const int s = k % a.stages, cc = k % a.chunks;
+    const int tile = blockIdx.x + (k / a.chunks) * gridDim.x;
+    const int n = tile / per_img, r = tile - n * per_img;
+    const int th = r / a.tiles_w, tw = r - th * a.tiles_w;
+    mbar_arrive_expect_tx(&x_full[s], a.x_stage_bytes);
+    tma_load_4d(Xs + (size_t)s * a.x_stage_stride, &xmap, &x_full[s], cc * a.CH, tw * a.TW * S - a.pW,
+                th * a.TH * S - a.pH, n);
+  };
+  // x is global memory: read only after the wait on the previous grid.  The
+  // producer fills the empty ring at once, while the other warps stage the
+  // weights.
   grid_dependency_wait();
-  for (int i = tid; i < a.C * 9; i += kThreads) {
-    const int c = i / 9, t = i - c * 9;
-    wdw[((c >> 3) * 9 + t) * 8 + (c & 7)] = wdg[i];
-  }
-  for (int i = tid; i < a.C; i += kThreads) bdw[i] = bdg ? Elem<T>::to_f32(bdg[i]) : 0.f;
-  for (int i = tid; i < a.Np; i += kThreads) bpw[i] = (bpg && i < a.K) ? Elem<T>::to_f32(bpg[i]) : 0.f;
-  for (int i = tid; i < (a.C / 8) * a.Np; i += kThreads) {
-    const int kc = i / a.Np, n = i - kc * a.Np;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (n < a.K) v = *reinterpret_cast<const uint4*>(wpg + (int64_t)n * a.C + kc * 8);
-    *reinterpret_cast<uint4*>(Bs + ((size_t)kc * a.Np + n) * 16) = v;
+  const int prologue = min(a.stages, copies);
+  if (tid == 0)
+    for (int k = 0; k < prologue; ++k) issue_copy(k);
+  // Weights, biases and the projection's B operand, staged once per CTA.
+  {
+    const T* __restrict__ wdg = static_cast<const T*>(a.w_dw);
+    const T* __restrict__ bdg = static_cast<const T*>(a.b_dw);
+    const T* __restrict__ wpg = static_cast<const T*>(a.w_pw);
+    const T* __restrict__ bpg = static_cast<const T*>(a.b_pw);
+    T* wdw_s = reinterpret_cast<T*>(smem + a.wdw_off);
+    float* bdw_s = reinterpret_cast<float*>(smem + a.bdw_off);
+    float* bpw_s = reinterpret_cast<float*>(smem + a.bpw_off);
+    uint8_t* Bs = smem + a.b_off;  // [C/8][Np rows][16 B], K-major, no swizzle
+    for (int i = tid - 32; i >= 0 && i < a.C * 9; i += kThreads - 32) {
+      const int c = i / 9, t = i - c * 9;
+      wdw_s[((c >> 3) * 9 + t) * 8 + (c & 7)] = wdg[i];
+    }
+    for (int i = tid - 32; i >= 0 && i < a.C; i += kThreads - 32) bdw_s[i] = bdg ? Elem<T>::to_f32(bdg[i]) : 0.f;
+    for (int i = tid - 32; i >= 0 && i < a.Np; i += kThreads - 32)
+      bpw_s[i] = (bpg && i < a.K) ? Elem<T>::to_f32(bpg[i]) : 0.f;
+    for (int i = tid - 32; i >= 0 && i < a.G * a.Np; i += kThreads - 32) {
+      const int kc = i / a.Np, n = i - kc * a.Np;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (n < a.K) v = *reinterpret_cast<const uint4*>(wpg + (int64_t)n * a.C + kc * 8);
+      *reinterpret_cast<uint4*>(Bs + ((size_t)kc * a.Np + n) * 16) = v;
+    }
   }
   fence_proxy_async_smem();  // B (generic-proxy writes) -> visible to the tensor core
-  if (warp == 1) {           // tensor memory only after the wait on the previous grid
+  if (warp == kMmaWarp) {    // tensor memory only after the wait on the previous grid
     tc::tmem_alloc(tmem_slot, a.tmem_cols);
     tc::tmem_relinquish();
   }
@@ -132,122 +364,98 @@ __global__ void __launch_bounds__(kThreads, 1) dw_pw_kernel(const __grid_constan
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  const uint32_t a_base0 = smem_u32(smem + a.a_off);
 
   if (warp == 0) {
     // ---------------- TMA producer: every (tile, chunk) in order ----------------
     if (lane == 0) {
-      int k = 0;
-      int last[kMaxStages];  // the last copy issued into each stage
-      for (int i = 0; i < kMaxStages; ++i) last[i] = -1;
-      for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x) {
-        const int n = tile / a.tiles_h, oh0 = (tile - n * a.tiles_h) * a.TH;
-        for (int cc = 0; cc < a.chunks; ++cc, ++k) {
-          const int s = k % a.stages;
-          if (k >= a.stages && !*failed &&
-              !mbar_wait(&x_empty[s], (uint32_t)(((k / a.stages) - 1) & 1), a.wait_limit_ns)) {
-            report(a.status, kDevTimeout, 41);
-            *failed = 1;
-          }
-          if (*failed) continue;
-          mbar_arrive_expect_tx(&x_full[s], a.x_stage_bytes);
-          // CH channels x Win columns x Hin rows from (oh0 * s - pH, -pW): the
-          // halo and the padding read past the tensor's edge as zeros
-          tma_load_4d(Xs + (size_t)s * a.x_stage_stride, &xmap, &x_full[s], cc * a.CH, -a.pW, oh0 * a.s - a.pH, n);
-          last[s] = k;
+      int issued = prologue;  // copies 0 .. issued-1 are in flight or landed
+      for (int k = prologue; k < copies; ++k) {
+        const int s = k % a.stages;
+        if (!*failed && !mbar_wait(&x_empty[s], (uint32_t)(((k / a.stages) - 1) & 1), a.wait_limit_ns)) {
+          report(a.status, kDevTimeout, 41);
+          *failed = 1;
         }
+        if (*failed) break;
+        issue_copy(k);
+        issued = k + 1;
       }
       // bounded drain (also after a timeout): no copy may still be landing
       // when the CTA exits
-      for (int s = 0; s < a.stages; ++s)
-        if (last[s] >= 0) mbar_wait(&x_full[s], (uint32_t)((last[s] / a.stages) & 1), a.wait_limit_ns);
+      for (int k = max(0, issued - a.stages); k < issued; ++k)
+        mbar_wait(&x_full[k % a.stages], (uint32_t)((k / a.stages) & 1), a.wait_limit_ns);
     }
-  } else {
-    // ---------------- compute warps 1..8 ----------------
-    const int tcid = tid - 32;
-    const int p = tcid & 127;  // pixel row of the A tile this thread computes
-    const uint32_t a_base = smem_u32(As), b_base = smem_u32(Bs);
-    const int g8n = a.CH / 8;  // 8-channel groups per chunk; thread takes groups tcid / 128, + 2, ...
-    int k = 0, tcount = 0;
-    for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, ++tcount) {
-      const int n = tile / a.tiles_h, oh0 = (tile - n * a.tiles_h) * a.TH;
-      const int rows = min(a.TH, a.Ho - oh0);
-      const int npx = rows * a.Wo;
-      const int ohl = p / a.Wo, ow = p - ohl * a.Wo;
-      for (int cc = 0; cc < a.chunks; ++cc, ++k) {
-        const int s = k % a.stages;
-        if (!*failed && !mbar_wait(&x_full[s], (uint32_t)((k / a.stages) & 1), a.wait_limit_ns)) {
-          report(a.status, kDevTimeout, 42);
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issuer: the whole warp, one elected lane issues ----------------
+    const uint32_t b_base = smem_u32(smem + a.b_off);
+    int i = 0, issued = -1;
+    for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, ++i) {
+      const int ab = i % a.nA, cb = i & 1;
+      if (lane == 0 && !*failed) {
+        if (!mbar_wait(&a_full[ab], (uint32_t)((i / a.nA) & 1), a.wait_limit_ns) ||
+            (i >= 2 && !mbar_wait(&acc_empty[cb], (uint32_t)(((i >> 1) - 1) & 1), a.wait_limit_ns))) {
+          report(a.status, kDevTimeout, 43);
           *failed = 1;
         }
-        if (p < npx && !*failed) {
-          const uint8_t* px0 = Xs + (size_t)s * a.x_stage_stride + ((size_t)(ohl * a.s) * a.Win + ow * a.s) * a.CH * 2;
-          for (int g8 = tcid >> 7; g8 < g8n; g8 += 2) {
-            const int kc = cc * g8n + g8;  // 8-channel group of the whole C
-            const uint4* wv = reinterpret_cast<const uint4*>(wdw + (size_t)kc * 72);
-            float acc[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = bdw[kc * 8 + e];
-#pragma unroll
-            for (int ky = 0; ky < 3; ++ky)
-#pragma unroll
-              for (int kx = 0; kx < 3; ++kx) {
-                // 8 channels of one input pixel and of one tap's weights, 16-bit
-                // pairs: fp32 products and sums with one rounding per FMA
-                const uint4 u = *reinterpret_cast<const uint4*>(px0 + ((size_t)ky * a.Win + kx) * a.CH * 2 + g8 * 16);
-                const uint4 wq = wv[ky * 3 + kx];
-                fma_mixed_pair<T>(u.x, wq.x, acc[0], acc[1]);
-                fma_mixed_pair<T>(u.y, wq.y, acc[2], acc[3]);
-                fma_mixed_pair<T>(u.z, wq.z, acc[4], acc[5]);
-                fma_mixed_pair<T>(u.w, wq.w, acc[6], acc[7]);
-              }
-            uint32_t wd[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              wd[e] = epilogue_pair<T>(act_f<T>(acc[2 * e], a.act), act_f<T>(acc[2 * e + 1], a.act), 0.f, 0.f);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a_base + (uint32_t)((kc * 128 + p) * 16)),
-                         "r"(wd[0]), "r"(wd[1]), "r"(wd[2]), "r"(wd[3])
-                         : "memory");
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&x_empty[s]);  // this warp's reads of the stage are done
       }
-      // the tile's h is complete: projection on the tensor cores
-      fence_proxy_async_smem();
-      tc::fence_before_sync();
-      asm volatile("bar.sync 1, %0;" ::"r"(32 * kComputeWarps) : "memory");
-      if (tcid == 0) {
-        tc::fence_after_sync();
-        for (int ks = 0; ks < a.C / 16; ++ks) {  // one K step per 16 channels
-          const uint64_t ad = tc::smem_desc(a_base + (uint32_t)ks * 4096u, 2048u, 128u);
-          const uint64_t bd = tc::smem_desc(b_base + (uint32_t)(2 * ks * a.Np) * 16u, (uint32_t)a.Np * 16u, 128u);
-          tc::mma_f16(tmem_base, ad, bd, a.idesc, ks > 0 ? 1u : 0u);
-        }
-        tc::commit(mma_bar);
+      __syncwarp();
+      tc::fence_after_sync();
+      if (*failed) continue;
+      const uint32_t d = tmem_base + (uint32_t)(cb * a.Np);
+      // descriptors built once; a K step advances their start-address field
+      // (bits 0-13, address / 16), which stays below 2^14 inside shared memory
+      const uint32_t a_buf = a_base0 + (uint32_t)ab * a.a_bytes;
+      const uint64_t ad0 = tc::smem_desc_sw128(a_buf);
+      const int ks_swz = (a.C / 64) * 4;  // K steps inside the swizzled atoms
+      const uint64_t at0 = tc::smem_desc(a_buf + (uint32_t)(a.C / 64) * kAtomBytes, kTailGroupBytes, 128u);
+      const uint64_t bd0 = tc::smem_desc(b_base, (uint32_t)a.Np * 16u, 128u);
+      for (int ks = 0; ks < a.C / 16; ++ks) {  // one K step per 16 channels
+        const uint64_t ad = ks < ks_swz ? ad0 + (((uint32_t)(ks >> 2) * kAtomBytes + (uint32_t)(ks & 3) * 32u) >> 4)
+                                        : at0 + ((uint32_t)(ks - ks_swz) * 2u * kTailGroupBytes >> 4);
+        const uint64_t bd = bd0 + ((uint32_t)(2 * ks * a.Np) * 16u >> 4);
+        mma_f16_elect(d, ad, bd, a.idesc, ks > 0 ? 1u : 0u);
       }
-      if (!*failed && !mbar_wait(mma_bar, (uint32_t)(tcount & 1), a.wait_limit_ns)) {
-        report(a.status, kDevTimeout, 43);
+      commit_elect(&a_empty[ab]);
+      commit_elect(&acc_full[cb]);
+      issued = i;
+    }
+    // the last accumulators must have landed before tensor memory is freed
+    if (issued >= 0 && lane == 0)
+      mbar_wait(&acc_full[issued & 1], (uint32_t)((issued >> 1) & 1), a.wait_limit_ns);
+    __syncwarp();
+  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
+    // ---------------- epilogue: TMEM lane quarter q = pixel rows 32q .. 32q+31 ----------------
+    T* __restrict__ yg = static_cast<T*>(a.y);
+    const int q = warp & 3;
+    const int p = q * 32 + lane;
+    const int j = p / a.TW, w = p - j * a.TW;
+    int i = 0;
+    for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, ++i) {
+      const int n = tile / per_img, r = tile - n * per_img;
+      const int th = r / a.tiles_w, tw = r - th * a.tiles_w;
+      const int oh0 = th * a.TH, ow0 = tw * a.TW;
+      const int cb = i & 1;
+      if (lane == 0 && !*failed && !mbar_wait(&acc_full[cb], (uint32_t)((i >> 1) & 1), a.wait_limit_ns)) {
+        report(a.status, kDevTimeout, 44);
         *failed = 1;
       }
+      __syncwarp();
       tc::fence_after_sync();
-      if (warp <= 4 && !*failed) {
-        // epilogue: warp w reads TMEM lanes 32 * (w & 3) .. + 31 = pixels of those A rows
-        const int q = warp & 3;
-        const int pe = q * 32 + lane;
-        const int eh = pe / a.Wo, ew = pe - eh * a.Wo;
-        T* dst = yg + (((int64_t)n * a.Ho + oh0 + eh) * a.Wo + ew) * a.K;
+      if (!*failed) {
+        const bool valid = j < min(a.TH, a.Ho - oh0) && w < min(a.TW, a.Wo - ow0);
+        T* dst = yg + (((int64_t)n * a.Ho + oh0 + j) * a.Wo + ow0 + w) * a.K;
         for (int c0 = 0; c0 < a.Np; c0 += 16) {
-          uint32_t r[16];
-          tc::tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
+          uint32_t rr[16];
+          tc::tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(cb * a.Np + c0), rr);
           tc::tmem_ld_wait();
-          if (pe < npx) {
+          if (valid) {
 #pragma unroll
             for (int h8 = 0; h8 < 16; h8 += 8) {
               if (c0 + h8 < a.K) {
                 uint32_t wd[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                  wd[e] = epilogue_pair<T>(__uint_as_float(r[h8 + 2 * e]), __uint_as_float(r[h8 + 2 * e + 1]),
+                  wd[e] = epilogue_pair<T>(__uint_as_float(rr[h8 + 2 * e]), __uint_as_float(rr[h8 + 2 * e + 1]),
                                            bpw[c0 + h8 + 2 * e], bpw[c0 + h8 + 2 * e + 1]);
                 *reinterpret_cast<uint4*>(dst + c0 + h8) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
               }
@@ -255,14 +463,106 @@ __global__ void __launch_bounds__(kThreads, 1) dw_pw_kernel(const __grid_constan
           }
         }
       }
-      // the accumulators and A are free for the next tile
+      // this warp's reads of the accumulators are done
       tc::fence_before_sync();
-      asm volatile("bar.sync 1, %0;" ::"r"(32 * kComputeWarps) : "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[cb]);
+    }
+  } else {
+    // ---------------- depthwise compute: (segment, column, group) items ----------------
+    // A thread's items are the same in every tile (f = tcid, tcid + 256, ...):
+    // the first one's decode, weights and bias are kept across tiles, and
+    // the ring position of the tile's copies advances by one tile per tile.
+    const int tcid = tid - 32 * kComputeWarp0;
+    const int cols_g = a.TW * a.G;
+    const int items = a.NS * cols_g;
+    const uint32_t pixb = (uint32_t)(a.CH * 2), rowb = (uint32_t)(a.Win * a.CH * 2);  // bytes per box column / row
+    const float hi = a.act == 2 ? 6.f : __int_as_float(0x7f800000);                      // ReLU6 / ReLU upper clamp
+    const int gfull = (a.C / 64) * 8;                                                     // groups in swizzled atoms
+    auto group_off = [&](int g) -> uint32_t {  // the group's atom (or tail group) inside an A buffer
+      return g < gfull ? (uint32_t)(g >> 3) * kAtomBytes
+                       : (uint32_t)(gfull >> 3) * kAtomBytes + (uint32_t)(g - gfull) * kTailGroupBytes;
+    };
+    // decode of the first item (the common case: one item per thread)
+    const int f0 = min(tcid, items - 1);
+    const int seg0 = f0 / cols_g, rem0 = f0 - seg0 * cols_g;
+    const int w0 = rem0 / a.G, g0 = rem0 - w0 * a.G;
+    const int cc0 = g0 / a.G8;
+    int kb_s = 0, kb_ph = 0;  // stage and phase parity of the tile's first copy
+    int i = 0;
+    for (int tile = blockIdx.x; tile < a.tiles; tile += gridDim.x, ++i) {
+      const int n = tile / per_img, r = tile - n * per_img;
+      const int th = r / a.tiles_w, tw = r - th * a.tiles_w;
+      const int rows = min(a.TH, a.Ho - th * a.TH), cols = min(a.TW, a.Wo - tw * a.TW);
+      const int ab = i % a.nA;
+      // A buffer ab free: the MMAs of tile i - nA have read it
+      if (i >= a.nA) {
+        if (lane == 0 && !*failed &&
+            !mbar_wait(&a_empty[ab], (uint32_t)(((i / a.nA) - 1) & 1), a.wait_limit_ns)) {
+          report(a.status, kDevTimeout, 45);
+          *failed = 1;
+        }
+        __syncwarp();
+      }
+      const uint32_t a_base = a_base0 + (uint32_t)ab * a.a_bytes;
+      auto stage_of = [&](int cc, int* ph) {  // ring stage and parity of this tile's copy cc
+        int st = kb_s + cc;
+        *ph = kb_ph;
+        if (st >= a.stages) st -= a.stages, *ph ^= 1;
+        return st;
+      };
+      for (int f = tcid; f < items; f += kComputeThreads) {
+        int seg = seg0, w = w0, g = g0, cc = cc0;
+        if (f != f0) {  // further items (more (column, group) pairs than threads)
+          seg = f / cols_g;
+          const int rem = f - seg * cols_g;
+          w = rem / a.G, g = rem - w * a.G;
+          cc = g / a.G8;
+        }
+        const int j0 = seg * a.rps, j1 = min(rows, j0 + a.rps);
+        if (w >= cols || j0 >= j1 || *failed) continue;
+        int ph;
+        const int s = stage_of(cc, &ph);
+        if (!mbar_wait(&x_full[s], (uint32_t)ph, a.wait_limit_ns)) {
+          report(a.status, kDevTimeout, 42);
+          *failed = 1;
+          continue;
+        }
+        uint4 wv[9];
+        const uint4* wsrc = reinterpret_cast<const uint4*>(wdw + (size_t)g * 72);
+#pragma unroll
+        for (int t = 0; t < 9; ++t) wv[t] = wsrc[t];
+        float bias[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) bias[e] = bdw[g * 8 + e];
+        const int gl = g - cc * a.G8;
+        const uint8_t* xs = Xs + (size_t)s * a.x_stage_stride + ((size_t)(w * S) * a.CH + gl * 8) * 2;
+        walk_any<T, S>(xs, rowb, pixb, wv, bias, j0, j1, a.TW, w, a_base + group_off(g), g < gfull, g, a.act, hi);
+      }
+      // A rows of this warp written (generic proxy) -> visible to the MMAs;
+      // each stage of the tile released once its copy is seen complete (so
+      // an arrival can never count toward an earlier use of the stage)
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        for (int cc = 0; cc < a.chunks; ++cc) {
+          int ph;
+          const int s = stage_of(cc, &ph);
+          if (!*failed && !mbar_wait(&x_full[s], (uint32_t)ph, a.wait_limit_ns)) {
+            report(a.status, kDevTimeout, 46);
+            *failed = 1;
+          }
+          mbar_arrive(&x_empty[s]);
+        }
+        mbar_arrive(&a_full[ab]);
+      }
+      kb_s += a.chunks;  // chunks <= stages: at most one wrap
+      if (kb_s >= a.stages) kb_s -= a.stages, kb_ph ^= 1;
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem_base, a.tmem_cols);
   }
@@ -273,52 +573,94 @@ __global__ void __launch_bounds__(kThreads, 1) dw_pw_kernel(const __grid_constan
 namespace {
 
 inline uint32_t round_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 struct DwPwPlan {
   fz::DwPwArgs a;
   uint32_t smem_bytes;
 };
 
+// Column walks: NS segments of rps output rows, as many segments as keep the
+// compute threads busy.
+inline void walk_split(int TH, int TW, int G, int* NS, int* rps) {
+  const int ns = std::max(1, std::min(TH, fz::kComputeThreads / (TW * G)));
+  *rps = ceil_div(TH, ns);
+  *NS = ceil_div(TH, *rps);
+}
+
+// Tile shape, copy chunking and buffering.  Candidates: TW the balanced
+// split of Wo into pieces of at most 16 (or 8) columns, TH the balanced split
+// of Ho with TH * TW <= 128; copies of all C channels or of 64/48/32/16; two
+// three, two or one A buffers.  Preferred, in order: two tiles of input in
+// flight, at least two A buffers, the lower estimated compute time per output
+// pixel (rounds of compute threads x a walk's FMAs and loads, plus a fixed
+// cost per tile; 15% more with two A buffers than with three), fewer copies
+// per tile.
 bool make_dw_pw_plan(const Geometry& g, bool bf16, int K, int act, int max_smem, DwPwPlan* out) {
-  (void)bf16;
   if (g.ndim != 2 || g.Cg != 1 || g.Kg != 1 || g.Z != 1 || g.Y != 3 || g.X != 3) return false;
   if (g.dH != 1 || g.dW != 1 || g.sH != g.sW || g.sH < 1 || g.sH > 2) return false;
-  const int C = g.C();
+  const int C = g.C(), S = g.sH;
   if (C % 16 != 0 || C > 256 || K % 8 != 0 || K < 8 || K > 256 || act < 0 || act > 2) return false;
-  if (g.Wo < 1 || g.Wo > 128 || g.Ho < 1) return false;
+  if (g.Wo < 1 || g.Ho < 1) return false;
   fz::DwPwArgs a;
   std::memset(&a, 0, sizeof(a));
-  a.C = C, a.K = K, a.Np = (K + 15) / 16 * 16;
-  a.Ho = g.Ho, a.Wo = g.Wo, a.s = g.sH, a.act = act, a.pH = g.pH, a.pW = g.pW;
-  a.TH = std::min(g.Ho, 128 / g.Wo);
-  a.tiles_h = (g.Ho + a.TH - 1) / a.TH;
-  const int64_t tiles = g.N * (int64_t)a.tiles_h;
-  if (tiles >= (1ll << 31)) return false;
-  a.tiles = (int)tiles;
-  a.Win = (g.Wo - 1) * a.s + 3;
-  a.Hin = (a.TH - 1) * a.s + 3;
-  if (a.Win > 256 || a.Hin > 256) return false;
-  // the largest copy chunk of 64, 48, 32 or 16 channels dividing C
-  a.CH = C % 64 == 0 ? 64 : C % 48 == 0 ? 48 : C % 32 == 0 ? 32 : 16;
-  a.chunks = C / a.CH;
-  a.x_stage_bytes = (uint32_t)(a.Win * a.Hin * a.CH) * 2u;
-  a.x_stage_stride = round_up(a.x_stage_bytes, 1024);
+  a.C = C, a.K = K, a.Np = (K + 15) / 16 * 16, a.G = C / 8;
+  a.Ho = g.Ho, a.Wo = g.Wo, a.act = act, a.pH = g.pH, a.pW = g.pW;
   a.wdw_off = 1024;
   a.bdw_off = a.wdw_off + (uint32_t)C * 9u * 2u;
   a.bpw_off = a.bdw_off + (uint32_t)C * 4u;
   a.b_off = round_up(a.bpw_off + (uint32_t)a.Np * 4u, 1024);
-  a.a_off = round_up(a.b_off + (uint32_t)(C / 8) * (uint32_t)a.Np * 16u, 1024);
-  a.x_off = round_up(a.a_off + (uint32_t)(C / 8) * 128u * 16u, 1024);
+  a.a_off = round_up(a.b_off + (uint32_t)a.G * (uint32_t)a.Np * 16u, 1024);
+  a.a_bytes = (uint32_t)(C / 64) * fz::kAtomBytes + (uint32_t)((C % 64) / 8) * fz::kTailGroupBytes;
   const uint32_t budget = (uint32_t)std::min(max_smem, 227 * 1024);
-  if (a.x_off + 2 * a.x_stage_stride > budget) return false;
-  // up to 4 stages; as many as keep two CTAs on an SM (113 KB each) when two
-  // fit at all, else as many as one CTA holds
-  const uint32_t two = 113u * 1024u;
-  a.stages = a.x_off + 2 * a.x_stage_stride <= two ? (int)((two - a.x_off) / a.x_stage_stride)
-                                                    : (int)((budget - a.x_off) / a.x_stage_stride);
-  a.stages = std::min(a.stages, 4);
+
+  bool found = false;
+  int best[5] = {0, 0, 0, 0, 0};  // score: (two tiles in flight, two+ A buffers, -cost', -copies, -TW)
+  for (int cap : {16, 8}) {
+    const int TW = ceil_div(g.Wo, ceil_div(g.Wo, cap));
+    for (int nA = fz::kMaxA; nA >= 1; --nA) {
+      if (a.a_off + (uint32_t)nA * a.a_bytes > budget) continue;
+      const uint32_t room = budget - a.a_off - (uint32_t)nA * a.a_bytes;
+      for (int thmax = std::min(g.Ho, 128 / TW); thmax >= 1; --thmax) {
+        const int TH = ceil_div(g.Ho, ceil_div(g.Ho, thmax));
+        if (TH != thmax) continue;  // each balanced TH once
+        const int Win = (TW - 1) * S + 3, Hin = (TH - 1) * S + 3;
+        if (Win > 256 || Hin > 256) continue;
+        int NS, rps;
+        walk_split(TH, TW, a.G, &NS, &rps);
+        const int rounds = ceil_div(NS * TW * a.G, fz::kComputeThreads);
+        // per walk: 72 FMAs per output row, 3 loads (~4 issue slots each) per input row
+        const int walk_cost = 72 * rps + 12 * ((rps - 1) * S + 3);
+        const int cost = (int)((1000ll * (rounds * walk_cost + 150)) / (TH * TW));
+        for (int CH : {C, 64, 48, 32, 16}) {
+          if (CH > C || C % CH != 0) continue;
+          const int chunks = C / CH;
+          const uint32_t bytes = (uint32_t)(Hin * Win * CH) * 2u, stride = round_up(bytes, 1024);
+          const int stages = (int)std::min<uint32_t>(fz::kMaxStages, room / stride);
+          if (stages < chunks) continue;
+          // cost' = cost, 15% more with two A buffers (the MMAs of tile i - 2
+          // then gate the compute of tile i)
+          const int costd = nA >= 3 ? cost : cost + cost * 15 / 100;
+          const int sc[5] = {stages >= 2 * chunks, nA >= 2, -costd, -chunks, -TW};
+          if (found && !std::lexicographical_compare(best, best + 5, sc, sc + 5)) continue;
+          found = true;
+          std::copy(sc, sc + 5, best);
+          a.TH = TH, a.TW = TW, a.Win = Win, a.Hin = Hin, a.CH = CH, a.G8 = CH / 8, a.chunks = chunks;
+          a.stages = stages, a.nA = nA, a.x_stage_bytes = bytes, a.x_stage_stride = stride;
+        }
+      }
+    }
+  }
+  if (!found) return false;
+  a.x_off = a.a_off + (uint32_t)a.nA * a.a_bytes;
+  a.tiles_h = ceil_div(g.Ho, a.TH);
+  a.tiles_w = ceil_div(g.Wo, a.TW);
+  const int64_t tiles = (int64_t)g.N * a.tiles_h * a.tiles_w;
+  if (tiles >= (1ll << 31)) return false;
+  a.tiles = (int)tiles;
+  walk_split(a.TH, a.TW, a.G, &a.NS, &a.rps);
   a.tmem_cols = 32;
-  while (a.tmem_cols < (uint32_t)a.Np) a.tmem_cols <<= 1;
+  while (a.tmem_cols < 2u * (uint32_t)a.Np) a.tmem_cols <<= 1;
   a.idesc = tc::idesc_f16(bf16, 128, a.Np);
   DwPwPlan p;
   p.a = a;
@@ -327,7 +669,7 @@ bool make_dw_pw_plan(const Geometry& g, bool bf16, int K, int act, int max_smem,
   return true;
 }
 
-template <typename T>
+template <typename T, int S>
 cudaError_t dw_pw_launch_typed(const Geometry& g, const LaunchArgs& la, const void* w_pw, const void* b_pw, int K,
                                int act, const DeviceInfo& dev) {
   DwPwPlan p;
@@ -337,12 +679,7 @@ cudaError_t dw_pw_launch_typed(const Geometry& g, const LaunchArgs& la, const vo
                        reinterpret_cast<uintptr_t>(w_pw);
   if (al & 15) return cudaErrorNotSupported;
   static SmemAttr attr;
-  cudaError_t e = attr.ensure(fz::dw_pw_kernel<T>, dev.device, (int)p.smem_bytes);
-  if (e != cudaSuccess) return e;
-  // all of the SM's unified memory as shared memory, so two CTAs fit (the
-  // occupancy query below follows this preference)
-  e = cudaFuncSetAttribute(fz::dw_pw_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared);
+  cudaError_t e = attr.ensure(fz::dw_pw_kernel<T, S>, dev.device, (int)p.smem_bytes);
   if (e != cudaSuccess) return e;
   // x as (C, W, H, N): CH channels x Win columns x Hin rows per copy
   const uint64_t es = sizeof(T), C = g.C();
@@ -363,11 +700,18 @@ cudaError_t dw_pw_launch_typed(const Geometry& g, const LaunchArgs& la, const vo
   a.status = la.status;
   a.wait_limit_ns = la.wait_limit_ns;
   int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fz::dw_pw_kernel<T>, fz::kThreads, p.smem_bytes);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fz::dw_pw_kernel<T, S>, fz::kThreads, p.smem_bytes);
   if (e != cudaSuccess) return e;
   occ = std::max(1, std::min(occ, 512 / (int)p.a.tmem_cols));
   const int grid = std::max(1, std::min(a.tiles, dev.num_sms * occ));
-  return launch_kernel(fz::dw_pw_kernel<T>, dim3(grid), dim3(fz::kThreads), p.smem_bytes, la, xmap, a);
+  return launch_kernel(fz::dw_pw_kernel<T, S>, dim3(grid), dim3(fz::kThreads), p.smem_bytes, la, xmap, a);
+}
+
+template <typename T>
+cudaError_t dw_pw_launch_stride(const Geometry& g, const LaunchArgs& la, const void* w_pw, const void* b_pw, int K,
+                                int act, const DeviceInfo& dev) {
+  return g.sH == 1 ? dw_pw_launch_typed<T, 1>(g, la, w_pw, b_pw, K, act, dev)
+                   : dw_pw_launch_typed<T, 2>(g, la, w_pw, b_pw, K, act, dev);
 }
 
 }  // namespace
@@ -380,8 +724,8 @@ bool dw_pw_supported(const Geometry& g, DType dt, int K, int act) {
 
 cudaError_t dw_pw_launch(const Geometry& g, const LaunchArgs& a, const void* w_pw, const void* b_pw, int K, int act,
                          const DeviceInfo& dev) {
-  if (a.dt == kF16) return dw_pw_launch_typed<__half>(g, a, w_pw, b_pw, K, act, dev);
-  if (a.dt == kBF16) return dw_pw_launch_typed<__nv_bfloat16>(g, a, w_pw, b_pw, K, act, dev);
+  if (a.dt == kF16) return dw_pw_launch_stride<__half>(g, a, w_pw, b_pw, K, act, dev);
+  if (a.dt == kBF16) return dw_pw_launch_stride<__nv_bfloat16>(g, a, w_pw, b_pw, K, act, dev);
   return cudaErrorNotSupported;
 }
 

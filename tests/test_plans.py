@@ -13,7 +13,10 @@ every workload family, random problems and maximum-size problems:
   buffered (partial) accumulators, the host MMA table within its bound and
   its offsets inside the operand regions, the grid = group chunks x CTAs
   per chunk; the staged epilogue's output boxes (TMA store) inside shared
-  memory, 1024-byte aligned, covering the CTA's channels.
+  memory, 1024-byte aligned, covering the CTA's channels;
+* the fused depthwise + projection planner: supported exactly on its shape
+  rules, tiles within the MMA's 128 rows, every input box read inside its
+  stage, the operand regions disjoint and inside shared memory.
 """
 import json
 import os
@@ -39,7 +42,7 @@ def harness(tmp_path_factory):
         pytest.skip("nvcc not available")
     out = tmp_path_factory.mktemp("plans")
     exes = {}
-    for name in ("plan_tc", "plan_dw", "plan_select", "plan_bwt"):
+    for name in ("plan_tc", "plan_dw", "plan_select", "plan_bwt", "plan_fused"):
         exe = str(out / name)
         subprocess.run([nvcc, "-std=c++17", "-O1", "-gencode", "arch=compute_103a,code=sm_103a",
                         "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include"),
@@ -373,3 +376,89 @@ def test_backward_weight_tc_plans(harness):
         assert p["E"] == wl.G * wl.Kg * X * Y * Z * wl.Cg, ctx
     assert n_ok >= 150
 
+
+
+def _fused_candidates():
+    """MobileNetV2 layers, the fused kernel's GPU test shapes, and random
+    shapes inside and just outside its rules."""
+    probs = []
+    for name in ("mbv2_dw_s1_f16", "mbv2_dw_s2_f16"):
+        probs.append((inputs.by_name(name), 24, 2))
+    for C, H, W, s, p in [(16, 13, 13, 1, 1), (32, 10, 9, 1, 0), (16, 7, 128, 1, 1), (48, 15, 21, 2, 1),
+                          (32, 5, 253, 2, 1), (256, 6, 14, 1, 1), (64, 17, 19, 1, 1)]:
+        for K in (8, 24, 32, 64, 256):
+            probs.append((inputs.Workload("fz", 0, 0, 2, 3, C, 1, 1, (1, H, W), (1, 3, 3), (1, s, s), (0, p, p),
+                                          (1, 1, 1), "bf16", True), K, 1))
+    rng = np.random.default_rng(77)
+    for i in range(400):
+        C = int(rng.choice([8, 16, 24, 32, 48, 64, 96, 144, 160, 192, 240, 256, 272]))
+        K = int(rng.choice([4, 8, 16, 24, 40, 64, 128, 200, 256, 264]))
+        s = int(rng.choice([1, 1, 2, 3]))
+        H, W = int(rng.integers(1, 300)), int(rng.integers(1, 300))
+        p = int(rng.integers(0, 3))
+        if H + 2 * p < 3 or W + 2 * p < 3:
+            continue
+        probs.append((inputs.Workload("fz", 0, i, 2, int(rng.integers(1, 5)), C, 1, 1, (1, H, W), (1, 3, 3),
+                                      (1, s, s), (0, p, p), (1, 1, 1), "f16", True), K, int(rng.integers(0, 4))))
+    return probs
+
+
+def test_fused_block_plans(harness):
+    probs = _fused_candidates()
+    lines = [" ".join(map(str, _geom(wl)[1] + [int(wl.dtype == "bf16"), K, act])) for wl, K, act in probs]
+    res = _run(harness["plan_fused"], lines)
+    assert len(res) == len(probs)
+    n_ok = 0
+    for (wl, K, act), p in zip(probs, res):
+        ctx = (wl, K, act, p)
+        C, s = wl.G, wl.stride[1]
+        rules = wl.ndim == 2 and C % 16 == 0 and C <= 256 and K % 8 == 0 and 8 <= K <= 256 and 0 <= act <= 2 \
+            and s in (1, 2)
+        assert p["ok"] == rules, ctx
+        if not p["ok"]:
+            continue
+        n_ok += 1
+        out, _ = _geom(wl)
+        Ho, Wo = out[1], out[2]
+        TH, TW = p["TH"], p["TW"]
+        # tiles: at most 128 pixel rows of the MMA, covering the output
+        assert 1 <= TW <= 16 and 1 <= TH <= Ho and TW <= Wo and TH * TW <= 128, ctx
+        assert p["tiles_h"] == -(-Ho // TH) and p["tiles_w"] == -(-Wo // TW), ctx
+        assert p["tiles"] == wl.N * p["tiles_h"] * p["tiles_w"], ctx
+        # input box: the tile's halo; TMA box limits and a 16-byte inner extent
+        assert p["Win"] == (TW - 1) * s + 3 and p["Hin"] == (TH - 1) * s + 3, ctx
+        assert max(p["Win"], p["Hin"], p["CH"]) <= 256 and (2 * p["CH"]) % 16 == 0, ctx
+        assert p["CH"] * p["chunks"] == C and p["G8"] * 8 == p["CH"], ctx
+        assert p["x_stage_bytes"] == p["Hin"] * p["Win"] * p["CH"] * 2, ctx
+        # the walk's last read (row (TH-1)s+2, column (TW-1)s+2, last group)
+        # ends exactly at the end of the stage
+        rowb, pixb = p["Win"] * p["CH"] * 2, p["CH"] * 2
+        last = ((TH - 1) * s + 2) * rowb + ((TW - 1) * s + 2) * pixb + (p["G8"] - 1) * 16 + 16
+        assert last == p["x_stage_bytes"] <= p["x_stage_stride"], ctx
+        assert p["x_stage_stride"] % 1024 == 0, ctx
+        # a whole tile's copies fit the ring
+        assert p["chunks"] <= p["stages"] <= p["max_stages"], ctx
+        # compute items: every (row, column, group) of a tile in exactly one
+        # segment of one column walk
+        assert p["NS"] * p["rps"] >= TH and (p["NS"] - 1) * p["rps"] < TH, ctx
+        assert p["G"] == C // 8, ctx
+        # shared-memory regions: disjoint, in order, aligned, inside the block
+        assert p["wdw_off"] >= 264 and p["bdw_off"] >= p["wdw_off"] + 18 * C, ctx
+        assert p["bdw_off"] % 16 == 0 and p["bpw_off"] >= p["bdw_off"] + 4 * C, ctx
+        assert p["b_off"] >= p["bpw_off"] + 4 * p["Np"] and p["b_off"] % 1024 == 0, ctx
+        assert p["a_off"] >= p["b_off"] + p["G"] * p["Np"] * 16 and p["a_off"] % 1024 == 0, ctx
+        # A: whole 64-channel swizzled atoms, then the C % 64 tail in 2 KB groups
+        assert p["a_bytes"] == (C // 64) * p["atom"] + (C % 64) // 8 * 2048 and p["atom"] == 128 * 128, ctx
+        assert p["a_bytes"] % 1024 == 0, ctx
+        assert p["nA"] in (1, 2, 3) and p["x_off"] == p["a_off"] + p["nA"] * p["a_bytes"], ctx
+        assert p["smem"] == p["x_off"] + p["stages"] * p["x_stage_stride"] <= SMEM_BLOCK, ctx
+        # projection: N = K rounded up to 16; two accumulators in TMEM
+        assert p["Np"] == -(-K // 16) * 16, ctx
+        assert p["tmem_cols"] in (32, 64, 128, 256, 512) and p["tmem_cols"] >= 2 * p["Np"], ctx
+        assert p["idesc"] >> 24 == 8 and (p["idesc"] >> 17) & 63 == p["Np"] // 8, ctx
+        assert p["threads"] == 448 and p["compute_threads"] == 256, ctx
+    assert n_ok > 100
+    mb = {wl.name: p for (wl, _, _), p in zip(probs, res) if wl.name.startswith("mbv2")}
+    # the MobileNetV2 layers keep two tiles of input in flight with two or more A buffers
+    for p in mb.values():
+        assert p["stages"] >= 2 * p["chunks"] and p["nA"] >= 2, p
