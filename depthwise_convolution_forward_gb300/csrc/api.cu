@@ -780,7 +780,7 @@ gconv_status grouped_conv_fwd_dw_pw_ex(const void* x, const void* w_dw, const vo
   const DType t = (DType)dt;
   if (!dw_pw_supported(g, t, K, act))
     return fail(GCONV_ERR_UNSUPPORTED, "the fused block takes 2D depthwise 3x3 (dilation 1, stride 1 or 2), "
-                "C %% 16 == 0 up to 256, K %% 8 == 0 up to 256, Wo up to 128");
+                "C %% 16 == 0 up to 256, K %% 8 == 0 up to 256");
   const int es = dtype_bytes(t);
   const int64_t yb = g.N * (int64_t)g.Ho * g.Wo * K * es, xb = g.x_elems() * es;
   if (overlaps(y, yb, x, xb) || overlaps(y, yb, w_dw, g.w_elems() * es) ||

@@ -403,17 +403,20 @@ const char *gconv_last_error(void);
  *         dilation 1, equal H / W strides of 1 or 2, any padding
  *   act   0 none, 1 ReLU (max(v, 0)), 2 ReLU6 (min(max(v, 0), 6)) on h
  * Limits: dt f16 or bf16; C a multiple of 16 up to 256; K a multiple of 8 up
- * to 256; Wo up to 128 and (Wo - 1) * s + 3 <= 256; x, y and w_pw 16-byte
- * aligned.  Outside them the call returns GCONV_ERR_UNSUPPORTED and
- * launches nothing (run grouped_conv_fwd and the projection separately).
- * Asynchronous on `stream`; one launch.
+ * to 256; any H and W; x, y and w_pw 16-byte aligned.  Outside them the call
+ * returns GCONV_ERR_UNSUPPORTED and launches nothing (run grouped_conv_fwd
+ * and the projection separately).  Asynchronous on `stream`; one launch.
  */
 gconv_status grouped_conv_fwd_dw_pw(const void *x, const void *w_dw, const void *b_dw, const void *w_pw,
                                     const void *b_pw, void *y, const gconv_problem *p, int32_t K, int32_t act,
                                     gconv_dtype dt, struct CUstream_st *stream);
 
 /* grouped_conv_fwd_dw_pw with options (debug, wait limit, serial launch; opt->selected reports
- * GCONV_KERNEL_DW_PW; force_kernel must be AUTO or GCONV_KERNEL_DW_PW). */
+ * GCONV_KERNEL_DW_PW; force_kernel must be AUTO or GCONV_KERNEL_DW_PW).  Tuning overrides,
+ * 0 = automatic: opt->tile[0] channels per depthwise thread (8, or 4 with twice the compute
+ * warps), opt->tile[1] / tile[2] the output tile's rows TH / columns TW (TW <= 16,
+ * TH * TW <= 128, TH a balanced split of Ho: ceil(Ho / ceil(Ho / TH)) == TH); a choice that
+ * does not fit returns GCONV_ERR_UNSUPPORTED. */
 gconv_status grouped_conv_fwd_dw_pw_ex(const void *x, const void *w_dw, const void *b_dw, const void *w_pw,
                                        const void *b_pw, void *y, const gconv_problem *p, int32_t K,
                                        int32_t act, gconv_dtype dt, struct CUstream_st *stream,

@@ -25,20 +25,20 @@ int main() {
                &g.pW, &g.dD, &g.dH, &g.dW, &g.ndim, &bf16, &K, &act) == 26) {
     g.N = N;
     DwPwPlan p;
-    if (!make_dw_pw_plan(g, bf16 != 0, K, act, kDefaultSmemOptin, &p)) {
+    if (!make_dw_pw_plan(g, bf16 != 0, K, act, kDefaultSmemOptin, nullptr, &p)) {
       printf("{\"ok\": false}\n");
       continue;
     }
     const fz::DwPwArgs& a = p.a;
     printf("{\"ok\": true, \"smem\": %u, \"threads\": %d, \"C\": %d, \"K\": %d, \"Np\": %d, \"G\": %d, "
            "\"TH\": %d, \"TW\": %d, \"tiles_h\": %d, \"tiles_w\": %d, \"tiles\": %d, \"Win\": %d, \"Hin\": %d, "
-           "\"CH\": %d, \"G8\": %d, \"chunks\": %d, \"stages\": %d, \"nA\": %d, \"NS\": %d, \"rps\": %d, "
+           "\"CH\": %d, \"GC\": %d, \"GT\": %d, \"cpt\": %d, \"chunks\": %d, \"stages\": %d, \"nA\": %d, \"NS\": %d, \"rps\": %d, "
            "\"x_stage_bytes\": %u, \"x_stage_stride\": %u, \"a_bytes\": %u, \"wdw_off\": %u, \"bdw_off\": %u, "
            "\"bpw_off\": %u, \"b_off\": %u, \"a_off\": %u, \"x_off\": %u, \"tmem_cols\": %u, \"idesc\": %u, "
            "\"compute_threads\": %d, \"atom\": %u, \"max_stages\": %d}\n",
-           p.smem_bytes, fz::kThreads, a.C, a.K, a.Np, a.G, a.TH, a.TW, a.tiles_h, a.tiles_w, a.tiles, a.Win, a.Hin,
-           a.CH, a.G8, a.chunks, a.stages, a.nA, a.NS, a.rps, a.x_stage_bytes, a.x_stage_stride, a.a_bytes,
-           a.wdw_off, a.bdw_off, a.bpw_off, a.b_off, a.a_off, a.x_off, a.tmem_cols, a.idesc, fz::kComputeThreads,
+           p.smem_bytes, a.cpt == 8 ? fz::Cfg<8>::kThreads : fz::Cfg<4>::kThreads, a.C, a.K, a.Np, a.G, a.TH, a.TW, a.tiles_h, a.tiles_w, a.tiles, a.Win, a.Hin,
+           a.CH, a.GC, a.GT, a.cpt, a.chunks, a.stages, a.nA, a.NS, a.rps, a.x_stage_bytes, a.x_stage_stride, a.a_bytes,
+           a.wdw_off, a.bdw_off, a.bpw_off, a.b_off, a.a_off, a.x_off, a.tmem_cols, a.idesc, compute_threads(a.cpt),
            fz::kAtomBytes, fz::kMaxStages);
   }
   return 0;

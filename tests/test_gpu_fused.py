@@ -2,7 +2,8 @@
 through the C ABI, against the oracle's block (Oracle.dw_pw_block) element
 by element: MobileNetV2 shapes at reduced batch and at full size, strides 1
 and 2, every activation, both 16-bit types, with and without biases, ragged
-row tiles, the width limit, and canary bands around y."""
+row and column tiles, wide rows, the 4-channel compute form and forced tile
+shapes, and canary bands around y."""
 import numpy as np
 import pytest
 import torch
@@ -32,7 +33,7 @@ def _pw(wl, K, seed):
     return w, b
 
 
-def run_fused(wl, x, w_dw, b_dw, w_pw, b_pw, act):
+def run_fused(wl, x, w_dw, b_dw, w_pw, b_pw, act, tile=(0, 0, 0)):
     dt = inputs.DTYPES[wl.dtype]
     K = w_pw.shape[0]
     shp = out_shape_of(wl)[:3] + (K,)
@@ -42,6 +43,7 @@ def run_fused(wl, x, w_dw, b_dw, w_pw, b_pw, act):
     y = buf[GUARD:GUARD + n].view(shp)
     opt = B.gconv_options()
     opt.debug = 1
+    opt.tile[0], opt.tile[1], opt.tile[2] = tile
     dev = [t.to(DEV) if t is not None else None for t in (x, w_dw, b_dw, w_pw, b_pw)]
     gc.grouped_conv_fwd_dw_pw_ex(*dev, y, gc.problem_of(wl), K, act, gc.DTYPE_CODES[wl.dtype],
                                  torch.cuda.current_stream(DEV), opt)
@@ -52,14 +54,14 @@ def run_fused(wl, x, w_dw, b_dw, w_pw, b_pw, act):
     return y.cpu()
 
 
-def _check(orc, wl, K, act, bias=True, seed=0):
+def _check(orc, wl, K, act, bias=True, seed=0, tile=(0, 0, 0)):
     x, w, b = inputs.make_inputs(wl)
     w_pw, b_pw = _pw(wl, K, 8800 + seed)
     if not bias:
         b, b_pw = None, None
-    y = run_fused(wl, x, w, b, w_pw, b_pw, act)
+    y = run_fused(wl, x, w, b, w_pw, b_pw, act, tile)
     ref = orc.dw_pw_block(wl, x, w, b, act, w_pw, b_pw, inputs.DTYPES[wl.dtype])
-    assert_close(y.double().numpy(), ref, wl.dtype, f"{wl.name} K={K} act={act} bias={bias}")
+    assert_close(y.double().numpy(), ref, wl.dtype, f"{wl.name} K={K} act={act} bias={bias} tile={tile}")
 
 
 @pytest.mark.parametrize("name", ["mbv2_dw_s1_f16", "mbv2_dw_s2_f16"])
@@ -82,14 +84,16 @@ def test_channel_counts(orc, dtype, K):
 
 
 CASES = [
-    # (C, H, W, stride, pad): ragged row tiles, no padding, the width limit,
-    # stride 2 with an odd input, one output row per tile, 256 channels
+    # (C, H, W, stride, pad): ragged row tiles, no padding, 128 output columns,
+    # stride 2 with an odd input, one output row per tile, 256 channels, a
+    # width split into ragged column tiles
     (16, 13, 13, 1, 1),
     (32, 10, 9, 1, 0),
     (16, 7, 128, 1, 1),
     (48, 15, 21, 2, 1),
     (32, 5, 253, 2, 1),
     (256, 6, 14, 1, 1),
+    (64, 9, 300, 1, 1),
 ]
 
 
@@ -114,3 +118,38 @@ def test_unsupported_shape_launches_nothing():
     w_pw, b_pw = _pw(wl, 24, 1)
     with pytest.raises(gc.GconvError):
         run_fused(wl, x, w, b, w_pw, b_pw, 2)
+
+
+FORCED = [
+    # (workload, K, (channels per thread, TH, TW)): the 4-channel form with
+    # twice the compute warps, walks of one row and of many, segments
+    ("mbv2_dw_s1_f16", 24, (4, 0, 0)),
+    ("mbv2_dw_s2_f16", 24, (4, 0, 0)),
+    ("mbv2_dw_s1_f16", 24, (8, 7, 14)),
+    ("mbv2_dw_s2_f16", 24, (4, 14, 7)),
+    ("mbv2_dw_s1_f16", 32, (4, 1, 14)),
+    ("mbv2_dw_s2_f16", 16, (8, 4, 14)),
+]
+
+
+@pytest.mark.parametrize("case", FORCED, ids=lambda c: "%s_K%d_cp%d_th%d_tw%d" % ((c[0], c[1]) + c[2]))
+def test_forced_forms(orc, case):
+    name, K, tile = case
+    _check(orc, inputs.by_name(name).with_(N=1), K, 2, seed=K + tile[0], tile=tile)
+
+
+@pytest.mark.parametrize("case", CASES[:3] + CASES[-2:], ids=lambda c: "C%d_%dx%d_s%d_p%d" % c)
+def test_shapes_four_channel_form(orc, case):
+    C, H, W, s, p = case
+    wl = inputs.Workload("fz_shape4", 0, C + H, 2, 3, C, 1, 1, (1, H, W), (1, 3, 3), (1, s, s), (0, p, p),
+                         (1, 1, 1), "bf16", True)
+    _check(orc, wl, 24, 1, seed=C + W + 1, tile=(4, 0, 0))
+
+
+def test_override_that_does_not_fit_raises():
+    """A tile shape outside the kernel (TW > 16) is refused, y untouched."""
+    wl = inputs.by_name("mbv2_dw_s1_f16").with_(N=1)
+    x, w, b = inputs.make_inputs(wl)
+    w_pw, b_pw = _pw(wl, 24, 2)
+    with pytest.raises(gc.GconvError):
+        run_fused(wl, x, w, b, w_pw, b_pw, 2, (8, 4, 17))

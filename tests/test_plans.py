@@ -428,12 +428,13 @@ def test_fused_block_plans(harness):
         # input box: the tile's halo; TMA box limits and a 16-byte inner extent
         assert p["Win"] == (TW - 1) * s + 3 and p["Hin"] == (TH - 1) * s + 3, ctx
         assert max(p["Win"], p["Hin"], p["CH"]) <= 256 and (2 * p["CH"]) % 16 == 0, ctx
-        assert p["CH"] * p["chunks"] == C and p["G8"] * 8 == p["CH"], ctx
+        assert p["CH"] * p["chunks"] == C and p["GC"] * p["cpt"] == p["CH"] and p["GT"] * p["cpt"] == C, ctx
+        assert p["cpt"] in (4, 8) and (2 * p["cpt"]) % 8 == 0, ctx
         assert p["x_stage_bytes"] == p["Hin"] * p["Win"] * p["CH"] * 2, ctx
         # the walk's last read (row (TH-1)s+2, column (TW-1)s+2, last group)
         # ends exactly at the end of the stage
         rowb, pixb = p["Win"] * p["CH"] * 2, p["CH"] * 2
-        last = ((TH - 1) * s + 2) * rowb + ((TW - 1) * s + 2) * pixb + (p["G8"] - 1) * 16 + 16
+        last = ((TH - 1) * s + 2) * rowb + ((TW - 1) * s + 2) * pixb + (p["GC"] - 1) * 2 * p["cpt"] + 2 * p["cpt"]
         assert last == p["x_stage_bytes"] <= p["x_stage_stride"], ctx
         assert p["x_stage_stride"] % 1024 == 0, ctx
         # a whole tile's copies fit the ring
@@ -456,7 +457,9 @@ def test_fused_block_plans(harness):
         assert p["Np"] == -(-K // 16) * 16, ctx
         assert p["tmem_cols"] in (32, 64, 128, 256, 512) and p["tmem_cols"] >= 2 * p["Np"], ctx
         assert p["idesc"] >> 24 == 8 and (p["idesc"] >> 17) & 63 == p["Np"] // 8, ctx
-        assert p["threads"] == 448 and p["compute_threads"] == 256, ctx
+        # 8 channels per thread with 8 compute warps, 4 with 16 (+ 6 warps of other roles)
+        assert p["compute_threads"] == {8: 256, 4: 512}[p["cpt"]], ctx
+        assert p["threads"] == p["compute_threads"] + 192, ctx
     assert n_ok > 100
     mb = {wl.name: p for (wl, _, _), p in zip(probs, res) if wl.name.startswith("mbv2")}
     # the MobileNetV2 layers keep two tiles of input in flight with two or more A buffers
