@@ -83,6 +83,7 @@ struct DwPwArgs {
   int Win, Hin;                         // input box columns / rows per tile
   int CH, GC, chunks, stages, nA;       // channels per copy, its cpt-channel groups, copies per tile, ring, A buffers
   int NS, rps;                          // segments a column walk is split into, output rows per segment
+  int inline_mma;                       // the compute warp that completes a tile's A issues its MMAs
   uint32_t x_stage_bytes, x_stage_stride, a_bytes;
   uint32_t wdw_off, bdw_off, bpw_off, b_off, a_off, x_off;  // shared-memory offsets
   uint32_t tmem_cols, idesc;
@@ -374,6 +375,7 @@ __global__ void __launch_bounds__(Cfg<CP>::kThreads, 1)
   uint64_t* acc_empty = acc_full + 2;       // [2] epilogue -> MMA: accumulators read
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 256);
   volatile int* failed = reinterpret_cast<volatile int*>(smem + 260);
+  uint32_t* a_done = reinterpret_cast<uint32_t*>(smem + 264);  // [kMaxA] compute warps done with A buffer b, ever
   const uint8_t* wdw = smem + a.wdw_off;                                // [GT][9 taps][CP], the storage type
   const float* bdw = reinterpret_cast<const float*>(smem + a.bdw_off);  // [C]
   const float* bpw = reinterpret_cast<const float*>(smem + a.bpw_off);  // [Np]
@@ -395,6 +397,7 @@ __global__ void __launch_bounds__(Cfg<CP>::kThreads, 1)
       mbar_init(&acc_empty[b], kEpiWarps);
     }
     *failed = 0;
+    for (int b = 0; b < kMaxA; ++b) a_done[b] = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&xmap);
   }
@@ -478,6 +481,9 @@ __global__ void __launch_bounds__(Cfg<CP>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t a_base0 = smem_u32(smem + a.a_off);
 
+  // Roles: warp 0 copies, warp 1 holds the tensor memory and issues the
+  // projection (or the compute warps issue it, a.inline_mma), warps 2-5 run
+  // the epilogue, warps 6.. the depthwise math.
   if (warp == 0) {
     // ---------------- TMA producer: every (tile, chunk) in order ----------------
     if (lane == 0) {
@@ -495,7 +501,7 @@ __global__ void __launch_bounds__(Cfg<CP>::kThreads, 1)
       for (int k = max(0, pk - a.stages); k < pk; ++k)
         mbar_wait(&x_full[k % a.stages], (uint32_t)((k / a.stages) & 1), a.wait_limit_ns);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp && !a.inline_mma) {
     // ---------------- MMA issuer: the whole warp, one elected lane issues ----------------
     const uint32_t b_base = smem_u32(smem + a.b_off);
     int i = 0, issued = -1;
@@ -579,12 +585,13 @@ __global__ void __launch_bounds__(Cfg<CP>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[cb]);
     }
-  } else {
+  } else if (warp >= kComputeWarp0) {
     // ---------------- depthwise compute: (segment, column, group) items ----------------
     // A thread's items are the same in every tile (f = tcid, tcid + 256, ...):
     // the first one's decode is kept across tiles, and the ring position of
     // the tile's copies advances by one tile per tile.
     const int tcid = tid - 32 * kComputeWarp0;
+    const uint32_t b_base = smem_u32(smem + a.b_off);
     const int cols_g = a.TW * a.GT;
     const int items = a.NS * cols_g;
     const uint32_t pixb = (uint32_t)(a.CH * 2), rowb = (uint32_t)(a.Win * a.CH * 2);  // bytes per box column / row
@@ -656,6 +663,7 @@ __global__ void __launch_bounds__(Cfg<CP>::kThreads, 1)
       // an arrival can never count toward an earlier use of the stage)
       fence_proxy_async_smem();
       __syncwarp();
+      uint32_t done = 0;
       if (lane == 0) {
         for (int cc = 0; cc < a.chunks; ++cc) {
           int ph;
@@ -666,12 +674,56 @@ __global__ void __launch_bounds__(Cfg<CP>::kThreads, 1)
           }
           mbar_arrive(&x_empty[s]);
         }
-        mbar_arrive(&a_full[ab]);
+        if (a.inline_mma) {
+          __threadfence_block();  // this warp's A rows before its count (release)
+          done = atomicAdd(&a_done[ab], 1u);
+        } else {
+          mbar_arrive(&a_full[ab]);
+        }
+      }
+      done = __shfl_sync(0xffffffffu, done, 0);
+      if (a.inline_mma && done % kComputeWarps == kComputeWarps - 1) {
+        // This warp completed tile i's A: it issues the projection itself.  A
+        // separate issuing warp shares its sub-partition with compute warps
+        // and measured up to ten times slower to issue; issuing here costs
+        // the compute warps that time instead, which pays when the MMAs, not
+        // the depthwise math, set the pace (see the planner).
+        __threadfence_block();  // the other warps' A rows (acquire)
+        const int cb = i & 1;
+        if (lane == 0 && i >= 2 && !*failed &&
+            !mbar_wait(&acc_empty[cb], (uint32_t)(((i >> 1) - 1) & 1), a.wait_limit_ns)) {
+          report(a.status, kDevTimeout, 43);
+          *failed = 1;
+        }
+        __syncwarp();
+        tc::fence_after_sync();
+        if (!*failed) {
+          const uint32_t d = tmem_base + (uint32_t)(cb * a.Np);
+          // descriptors built once; a K step advances their start-address
+          // field (bits 0-13, address / 16), below 2^14 inside shared memory
+          const uint64_t ad0 = tc::smem_desc_sw128(a_base);
+          const int ks_swz = (a.C / 64) * 4;  // K steps inside the swizzled atoms
+          const uint64_t at0 = tc::smem_desc(a_base + (uint32_t)(a.C / 64) * kAtomBytes, kTailGroupBytes, 128u);
+          const uint64_t bd0 = tc::smem_desc(b_base, (uint32_t)a.Np * 16u, 128u);
+          for (int ks = 0; ks < a.C / 16; ++ks) {  // one K step per 16 channels
+            const uint64_t ad = ks < ks_swz
+                                    ? ad0 + (((uint32_t)(ks >> 2) * kAtomBytes + (uint32_t)(ks & 3) * 32u) >> 4)
+                                    : at0 + ((uint32_t)(ks - ks_swz) * 2u * kTailGroupBytes >> 4);
+            const uint64_t bd = bd0 + ((uint32_t)(2 * ks * a.Np) * 16u >> 4);
+            mma_f16_elect(d, ad, bd, a.idesc, ks > 0 ? 1u : 0u);
+          }
+          commit_elect(&a_empty[ab]);
+          commit_elect(&acc_full[cb]);
+        }
       }
       kb_s += a.chunks;  // chunks <= stages: at most one wrap
       if (kb_s >= a.stages) kb_s -= a.stages, kb_ph ^= 1;
     }
   }
+  // the last tile's MMAs must have completed before tensor memory is freed
+  // (the epilogue waited for them too, unless a wait timed out)
+  if (warp == kMmaWarp && lane == 0 && my_tiles > 0)
+    mbar_wait(&acc_full[(my_tiles - 1) & 1], (uint32_t)(((my_tiles - 1) >> 1) & 1), a.wait_limit_ns);
   tc::fence_before_sync();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -702,25 +754,28 @@ inline void walk_split(int TH, int TW, int GT, int threads, int* NS, int* rps) {
 
 inline int compute_threads(int cp) { return cp == 8 ? fz::Cfg<8>::kComputeThreads : fz::Cfg<4>::kComputeThreads; }
 
-// Tile shape, channels per compute thread, copy chunking and buffering.
-// Candidates: 8 or 4 channels per compute thread; TW the balanced split of
-// Wo into pieces of at most 16 (or 8) columns, TH the balanced split of Ho
-// with TH * TW <= 128; copies of all C channels or of 64/48/32/16; three,
-// two or one A buffers.  Preferred, in order: two tiles of input in flight,
-// at least two A buffers, 8 channels per thread, more pixels per tile, fewer
-// output rows per compute thread, more A buffers, fewer copies per tile.  The order follows measurements on the
-// MobileNetV2 layers: a tile's fixed cost (its MMA batch, barriers and loop)
-// outweighs its depthwise work, so the largest tile wins, and at equal tiles
-// the 8-channel form beat the 4-channel one by 8-15%.  ov (may be null):
-// {channels per thread, TH, TW} to force, 0 = automatic.
+// Tile shape, channels per compute thread, copy chunking, buffering and the
+// MMA issuer.  Candidates: 8 or 4 channels per compute thread; TW the
+// balanced split of Wo into pieces of at most 16 (or 8) columns, TH the
+// balanced split of Ho with TH * TW <= 128; copies of all C channels or of
+// 64/48/32/16; three, two or one A buffers.  Preferred, in order: at least
+// two A buffers, 8 channels per thread, more pixels per tile, two tiles of
+// input in flight, fewer output rows per compute thread, more A buffers,
+// fewer copies per tile.  The order follows measurements on the MobileNetV2
+// layers: a tile's fixed cost (its MMA batch, barriers and loop) outweighs
+// its depthwise work, so the largest tile wins (even over double-buffered
+// input), and at equal tiles the 8-channel form beat the 4-channel one by
+// 8-15%.  ov (may be null): {channels per thread, TH, TW, MMA issuer (1 the
+// dedicated warp, 2 the compute warps)} to force, 0 = automatic.
 bool make_dw_pw_plan(const Geometry& g, bool bf16, int K, int act, int max_smem, const int* ov, DwPwPlan* out) {
   if (g.ndim != 2 || g.Cg != 1 || g.Kg != 1 || g.Z != 1 || g.Y != 3 || g.X != 3) return false;
   if (g.dH != 1 || g.dW != 1 || g.sH != g.sW || g.sH < 1 || g.sH > 2) return false;
   const int C = g.C(), S = g.sH;
   if (C % 16 != 0 || C > 256 || K % 8 != 0 || K < 8 || K > 256 || act < 0 || act > 2) return false;
   if (g.Wo < 1 || g.Ho < 1) return false;
-  const int ov_cp = ov ? ov[0] : 0, ov_th = ov ? ov[1] : 0, ov_tw = ov ? ov[2] : 0;
+  const int ov_cp = ov ? ov[0] : 0, ov_th = ov ? ov[1] : 0, ov_tw = ov ? ov[2] : 0, ov_mma = ov ? ov[3] : 0;
   if (ov_cp != 0 && ov_cp != 4 && ov_cp != 8) return false;
+  if (ov_mma < 0 || ov_mma > 2) return false;
   fz::DwPwArgs a;
   std::memset(&a, 0, sizeof(a));
   a.C = C, a.K = K, a.Np = (K + 15) / 16 * 16, a.G = C / 8;
@@ -759,7 +814,7 @@ bool make_dw_pw_plan(const Geometry& g, bool bf16, int K, int act, int max_smem,
             const uint32_t bytes = (uint32_t)(Hin * Win * CH) * 2u, stride = round_up(bytes, 1024);
             const int stages = (int)std::min<uint32_t>(fz::kMaxStages, room / stride);
             if (stages < chunks) continue;
-            const int sc[8] = {stages >= 2 * chunks, nA >= 2, cp == 8, TH * TW, -thread_rows, nA, -chunks, -TW};
+            const int sc[8] = {nA >= 2, cp == 8, TH * TW, stages >= 2 * chunks, -thread_rows, nA, -chunks, -TW};
             if (found && !std::lexicographical_compare(best, best + 8, sc, sc + 8)) continue;
             found = true;
             std::copy(sc, sc + 8, best);
@@ -779,6 +834,10 @@ bool make_dw_pw_plan(const Geometry& g, bool bf16, int K, int act, int max_smem,
   if (tiles >= (1ll << 31)) return false;
   a.tiles = (int)tiles;
   walk_split(a.TH, a.TW, a.GT, compute_threads(a.cpt), &a.NS, &a.rps);
+  // With three A buffers the MMAs of a tile have two tiles of compute to
+  // finish in, and the dedicated issuing warp keeps that time off the compute
+  // warps; with fewer the MMAs set the pace and the compute warps issue them.
+  a.inline_mma = ov_mma ? (ov_mma == 2) : (a.nA < 3);
   a.tmem_cols = 32;
   while (a.tmem_cols < 2u * (uint32_t)a.Np) a.tmem_cols <<= 1;
   a.idesc = tc::idesc_f16(bf16, 128, a.Np);

@@ -35,11 +35,11 @@ int main() {
            "\"CH\": %d, \"GC\": %d, \"GT\": %d, \"cpt\": %d, \"chunks\": %d, \"stages\": %d, \"nA\": %d, \"NS\": %d, \"rps\": %d, "
            "\"x_stage_bytes\": %u, \"x_stage_stride\": %u, \"a_bytes\": %u, \"wdw_off\": %u, \"bdw_off\": %u, "
            "\"bpw_off\": %u, \"b_off\": %u, \"a_off\": %u, \"x_off\": %u, \"tmem_cols\": %u, \"idesc\": %u, "
-           "\"compute_threads\": %d, \"atom\": %u, \"max_stages\": %d}\n",
+           "\"compute_threads\": %d, \"atom\": %u, \"max_stages\": %d, \"inline_mma\": %d}\n",
            p.smem_bytes, a.cpt == 8 ? fz::Cfg<8>::kThreads : fz::Cfg<4>::kThreads, a.C, a.K, a.Np, a.G, a.TH, a.TW, a.tiles_h, a.tiles_w, a.tiles, a.Win, a.Hin,
            a.CH, a.GC, a.GT, a.cpt, a.chunks, a.stages, a.nA, a.NS, a.rps, a.x_stage_bytes, a.x_stage_stride, a.a_bytes,
            a.wdw_off, a.bdw_off, a.bpw_off, a.b_off, a.a_off, a.x_off, a.tmem_cols, a.idesc, compute_threads(a.cpt),
-           fz::kAtomBytes, fz::kMaxStages);
+           fz::kAtomBytes, fz::kMaxStages, a.inline_mma);
   }
   return 0;
 }

@@ -33,7 +33,7 @@ def _pw(wl, K, seed):
     return w, b
 
 
-def run_fused(wl, x, w_dw, b_dw, w_pw, b_pw, act, tile=(0, 0, 0)):
+def run_fused(wl, x, w_dw, b_dw, w_pw, b_pw, act, tile=(0, 0, 0, 0)):
     dt = inputs.DTYPES[wl.dtype]
     K = w_pw.shape[0]
     shp = out_shape_of(wl)[:3] + (K,)
@@ -43,7 +43,8 @@ def run_fused(wl, x, w_dw, b_dw, w_pw, b_pw, act, tile=(0, 0, 0)):
     y = buf[GUARD:GUARD + n].view(shp)
     opt = B.gconv_options()
     opt.debug = 1
-    opt.tile[0], opt.tile[1], opt.tile[2] = tile
+    for i, v in enumerate(tile):
+        opt.tile[i] = v
     dev = [t.to(DEV) if t is not None else None for t in (x, w_dw, b_dw, w_pw, b_pw)]
     gc.grouped_conv_fwd_dw_pw_ex(*dev, y, gc.problem_of(wl), K, act, gc.DTYPE_CODES[wl.dtype],
                                  torch.cuda.current_stream(DEV), opt)
@@ -54,7 +55,7 @@ def run_fused(wl, x, w_dw, b_dw, w_pw, b_pw, act, tile=(0, 0, 0)):
     return y.cpu()
 
 
-def _check(orc, wl, K, act, bias=True, seed=0, tile=(0, 0, 0)):
+def _check(orc, wl, K, act, bias=True, seed=0, tile=(0, 0, 0, 0)):
     x, w, b = inputs.make_inputs(wl)
     w_pw, b_pw = _pw(wl, K, 8800 + seed)
     if not bias:
@@ -121,18 +122,24 @@ def test_unsupported_shape_launches_nothing():
 
 
 FORCED = [
-    # (workload, K, (channels per thread, TH, TW)): the 4-channel form with
-    # twice the compute warps, walks of one row and of many, segments
-    ("mbv2_dw_s1_f16", 24, (4, 0, 0)),
-    ("mbv2_dw_s2_f16", 24, (4, 0, 0)),
-    ("mbv2_dw_s1_f16", 24, (8, 7, 14)),
-    ("mbv2_dw_s2_f16", 24, (4, 14, 7)),
-    ("mbv2_dw_s1_f16", 32, (4, 1, 14)),
-    ("mbv2_dw_s2_f16", 16, (8, 4, 14)),
+    # (workload, K, (channels per thread, TH, TW, MMA issuer)): the
+    # 4-channel form with twice the compute warps, walks of one row and of
+    # many, segments, the dedicated issuing warp (1) and the compute warps
+    # issuing (2) on both strides
+    ("mbv2_dw_s1_f16", 24, (4, 0, 0, 0)),
+    ("mbv2_dw_s2_f16", 24, (4, 0, 0, 0)),
+    ("mbv2_dw_s1_f16", 24, (8, 7, 14, 0)),
+    ("mbv2_dw_s2_f16", 24, (4, 14, 7, 0)),
+    ("mbv2_dw_s1_f16", 32, (4, 1, 14, 0)),
+    ("mbv2_dw_s2_f16", 16, (8, 4, 14, 0)),
+    ("mbv2_dw_s1_f16", 24, (0, 0, 0, 2)),
+    ("mbv2_dw_s2_f16", 24, (0, 0, 0, 1)),
+    ("mbv2_dw_s1_f16", 40, (4, 0, 0, 2)),
+    ("mbv2_dw_s2_f16", 40, (4, 0, 0, 1)),
 ]
 
 
-@pytest.mark.parametrize("case", FORCED, ids=lambda c: "%s_K%d_cp%d_th%d_tw%d" % ((c[0], c[1]) + c[2]))
+@pytest.mark.parametrize("case", FORCED, ids=lambda c: "%s_K%d_cp%d_th%d_tw%d_mma%d" % ((c[0], c[1]) + c[2]))
 def test_forced_forms(orc, case):
     name, K, tile = case
     _check(orc, inputs.by_name(name).with_(N=1), K, 2, seed=K + tile[0], tile=tile)
@@ -143,7 +150,7 @@ def test_shapes_four_channel_form(orc, case):
     C, H, W, s, p = case
     wl = inputs.Workload("fz_shape4", 0, C + H, 2, 3, C, 1, 1, (1, H, W), (1, 3, 3), (1, s, s), (0, p, p),
                          (1, 1, 1), "bf16", True)
-    _check(orc, wl, 24, 1, seed=C + W + 1, tile=(4, 0, 0))
+    _check(orc, wl, 24, 1, seed=C + W + 1, tile=(4, 0, 0, 0))
 
 
 def test_override_that_does_not_fit_raises():
@@ -152,4 +159,14 @@ def test_override_that_does_not_fit_raises():
     x, w, b = inputs.make_inputs(wl)
     w_pw, b_pw = _pw(wl, 24, 2)
     with pytest.raises(gc.GconvError):
-        run_fused(wl, x, w, b, w_pw, b_pw, 2, (8, 4, 17))
+        run_fused(wl, x, w, b, w_pw, b_pw, 2, (8, 4, 17, 0))
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "C%d_%dx%d_s%d_p%d" % c)
+def test_shapes_other_mma_issuer(orc, case):
+    """The same shapes with the MMA issuer the planner did not choose."""
+    C, H, W, s, p = case
+    wl = inputs.Workload("fz_shape_m", 0, C + H, 2, 3, C, 1, 1, (1, H, W), (1, 3, 3), (1, s, s), (0, p, p),
+                         (1, 1, 1), "f16", True)
+    for mode in (1, 2):
+        _check(orc, wl, 32, 2, seed=C + W + 2 + mode, tile=(0, 0, 0, mode))
