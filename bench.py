@@ -20,6 +20,14 @@ launches bracketed by events).  The dominant kernel's mean gives the roofline
 entry; ``per_launch`` lists mean, median, GB/s, TFLOP/s and the fraction of
 the min(compute, HBM) roofline of each workload.
 
+``fused_block`` (forward only; ``--no-fused`` skips it) times each
+MobileNetV2 layer of the step as the fused depthwise + ReLU6 + 1x1 projection
+block (``grouped_conv_fwd_dw_pw``, projection to 24 channels at stride 1 and
+32 at stride 2, as in that network) the same way as ``per_launch``, with its
+algorithmic bytes, fraction of the HBM peak, the HBM bytes of h it avoids,
+and the floor of the separate path (the depthwise launch plus the
+projection's HBM time).
+
 ``--impl reference`` times the CPU oracle (the plain fp64 direct loop) on
 the host cores instead, each step a bounded sample of the same workload.
 
@@ -47,6 +55,12 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
 
+# The fused block (depthwise + ReLU6 + 1x1 projection) is timed on the
+# MobileNetV2 layers with the projection widths of that network: the
+# stride-1 layer (144 expanded channels at 56x56) projects back to 24, the
+# stride-2 layer (the first of the 28x28 stage) projects to 32.
+FUSED_K = {"mbv2_dw_s1_f16": 24, "mbv2_dw_s2_f16": 32}
+
 BENCH_SETS = {
     "all": None,  # every workload of every config (filled in by resolve)
     "mbv2_dw": ["mbv2_dw_s1_f16", "mbv2_dw_s2_f16"],
@@ -66,6 +80,8 @@ def parse():
                     help="a bench set (%s) or comma-separated workload names" % ", ".join(BENCH_SETS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fused", action="store_true",
+                    help="skip the fused depthwise + projection timing of the MobileNetV2 layers")
     ap.add_argument("--tile", default="", help="tuning override TH,TW,WB,stages,ctas_per_sm,fma_form")
     ap.add_argument("--force-kernel", type=int, default=0)
     ap.add_argument("--op", choices=["fwd", "bwd_data", "bwd_weight"], default="fwd",
@@ -513,6 +529,73 @@ class GpuArm:
         return sum(times) / (per_graph * n_graphs), statistics.median(per)
 
 
+def time_fused_blocks(arm, wls, per_launch, M, PG, hbm_peak):
+    """Each MobileNetV2 layer of the step as the fused block (depthwise +
+    ReLU6 + 1x1 projection, grouped_conv_fwd_dw_pw), alone, over M
+    back-to-back launches on rotating buffer sets larger than twice the L2.
+    Reports its time, algorithmic bytes and fraction of the HBM peak, and the
+    floor of the separate path: the depthwise launch measured above plus the
+    projection reading h and writing y at the HBM peak."""
+    import torch
+
+    from depthwise_convolution_forward_gb300 import inputs, roofline
+
+    gc, lib = arm.gc, arm.lib
+    out_entries = {}
+    for wl in wls:
+        K = FUSED_K.get(wl.name)
+        if K is None:
+            continue
+        x, w, b = inputs.make_inputs(wl)
+        g = torch.Generator().manual_seed(8800 + K)
+        w_pw = (torch.randn(K, wl.C, generator=g) / wl.C ** 0.5).to(x.dtype).to(arm.dev)
+        b_pw = ((torch.rand(K, generator=g) * 2 - 1) * 0.1).to(x.dtype).to(arm.dev)
+        p = gc.problem_of(wl)
+        out = gc.grouped_conv_out_shape(p)
+        nb = roofline.fused_block_bytes(wl, out, K)
+        moved = sum(v for k, v in nb.items() if k != "h_saved")
+        R = max(3, -(-2 * L2_BYTES // moved) + 1)
+        wd, bd = w.to(arm.dev), b.to(arm.dev)
+        xs = [x.to(arm.dev) for _ in range(R)]
+        ys = [torch.empty((wl.N, out[1], out[2], K), dtype=x.dtype, device=arm.dev) for _ in range(R)]
+        dt = gc.DTYPE_CODES[wl.dtype]
+        opt = arm.B.gconv_options()
+        optp = ctypes.byref(opt)
+
+        def launch(u):
+            st = lib.grouped_conv_fwd_dw_pw_ex(xs[u % R].data_ptr(), wd.data_ptr(), bd.data_ptr(), w_pw.data_ptr(),
+                                               b_pw.data_ptr(), ys[u % R].data_ptr(), ctypes.byref(p), K, 2, dt,
+                                               arm.sh, optp)
+            if st != 0:
+                raise RuntimeError(f"fused block launch failed: {gc.gconv_last_error()}")
+
+        with torch.cuda.stream(arm.stream):
+            for u in range(3):
+                launch(u)
+        arm.stream.synchronize()
+        n_graphs = max(1, -(-M // PG))
+        graphs = arm.capture(PG, launch, per_graph=PG)
+        arm.replay_timed(graphs)
+        times = arm.replay_timed(graphs * n_graphs)
+        del graphs
+        mean = sum(times) / (PG * n_graphs)
+        med = statistics.median([t / PG for t in times])
+        flops = roofline.fused_block_flops(wl, out, K)
+        dw_us = per_launch.get(wl.name, {}).get("mean_us")
+        proj_floor_us = (nb["h_saved"] // 2 + nb["w_pw"] + nb["b_pw"] + nb["y"]) / (hbm_peak * 1e9) * 1e6
+        out_entries[wl.name] = {
+            "kernel": gc.KERNEL_NAMES.get(opt.selected, str(opt.selected)), "K": K, "act": "relu6",
+            "median_us": med * 1e3, "mean_us": mean * 1e3, "launches": PG * n_graphs, "bytes": moved,
+            "GB_s": moved / (mean / 1e3) / 1e9, "frac_hbm": moved / (mean / 1e3) / 1e9 / hbm_peak,
+            "flops": flops, "TFLOP_s": flops / (mean / 1e3) / 1e12, "h_bytes_saved": nb["h_saved"],
+            "separate_path_floor_us": (dw_us + proj_floor_us) if dw_us is not None else None,
+            "separate_path_floor": "the depthwise launch's measured mean plus the projection's HBM floor "
+                                   "(read h, write y, at the measured peak)"}
+        del xs, ys
+        torch.cuda.empty_cache()
+    return out_entries
+
+
 def roofline_of(c, mean_ms, hbm_peak, tc_peak):
     """Roofline position of one convolution's launch: the bound (HBM or the
     tensor pipe, whichever takes longer at the measured peaks), achieved
@@ -642,6 +725,10 @@ def run_ours(args, wls, set_name, rank, world):
             del cs, ss
             torch.cuda.empty_cache()
 
+    fused = None
+    if not bwd and not args.no_fused:
+        fused = time_fused_blocks(arm, [c["wl"] for c in convs], per_launch, M, PG, hbm_peak) or None
+
     # end-to-end: pinned host buffers, copies inside the timed region
     e2e = None
     if not args.no_e2e and not bwd:
@@ -662,6 +749,8 @@ def run_ours(args, wls, set_name, rank, world):
             "gpu_launches": K * sum(c.get("kernels_per_call", 1) for c in convs), "timed_region_wall_s": wall}
     if clocks:
         line["clocks"] = clocks
+    if fused:
+        line["fused_block"] = fused
     if e2e:
         line["e2e"] = e2e
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -67,7 +67,11 @@ struct Cfg {
   static constexpr int kThreads = 32 * (kComputeWarp0 + kComputeWarps);
 };
 constexpr uint32_t kAtomBytes = 128u * 128u;  // one 64-channel K atom of 128 pixel rows (128-byte swizzle)
-constexpr uint32_t kTailGroupBytes = 128u * 16u;  // one 8-channel group of 128 pixel rows (no swizzle)
+// One 8-channel group of the A tail: 128 pixel rows x 16 bytes (no swizzle),
+// plus 16 bytes so consecutive groups start one bank chunk apart (the
+// groups' stores from one warp then fall in different banks; the MMA reads
+// the group stride as its K-direction core-matrix stride).
+constexpr uint32_t kTailGroupBytes = 128u * 16u + 16u;
 
 struct DwPwArgs {
   const void* w_dw;
@@ -377,7 +381,7 @@ __global__ void __launch_bounds__(Cfg<CP>::kThreads, 1)
   volatile int* failed = reinterpret_cast<volatile int*>(smem + 260);
   uint32_t* a_done = reinterpret_cast<uint32_t*>(smem + 264);  // [kMaxA] compute warps done with A buffer b, ever
   const uint8_t* wdw = smem + a.wdw_off;                                // [GT][9 taps][CP], the storage type
-  const float* bdw = reinterpret_cast<const float*>(smem + a.bdw_off);  // [C]
+  const uint8_t* bdw = smem + a.bdw_off;                                // [C], the storage type
   const float* bpw = reinterpret_cast<const float*>(smem + a.bpw_off);  // [Np]
   uint8_t* Xs = smem + a.x_off;                                          // stages x [Hin][Win][CH]
 
@@ -435,7 +439,7 @@ __global__ void __launch_bounds__(Cfg<CP>::kThreads, 1)
     const T* __restrict__ wpg = static_cast<const T*>(a.w_pw);
     const T* __restrict__ bpg = static_cast<const T*>(a.b_pw);
     T* wdw_s = reinterpret_cast<T*>(smem + a.wdw_off);
-    float* bdw_s = reinterpret_cast<float*>(smem + a.bdw_off);
+    T* bdw_s = reinterpret_cast<T*>(smem + a.bdw_off);
     float* bpw_s = reinterpret_cast<float*>(smem + a.bpw_off);
     uint8_t* Bs = smem + a.b_off;  // [C/8][Np rows][16 B], K-major, no swizzle
     constexpr int kB = 4, kN = kThreads - 32;
@@ -467,7 +471,7 @@ __global__ void __launch_bounds__(Cfg<CP>::kThreads, 1)
         if (i < a.C * 9) wdw_s[((c / kCPT) * 9 + t) * kCPT + (c % kCPT)] = v[q];
       }
     }
-    for (int i = t0; t0 >= 0 && i < a.C; i += kN) bdw_s[i] = bdg ? Elem<T>::to_f32(bdg[i]) : 0.f;
+    for (int i = t0; t0 >= 0 && i < a.C; i += kN) bdw_s[i] = bdg ? bdg[i] : Elem<T>::from_f32(0.f);
     for (int i = t0; t0 >= 0 && i < a.Np; i += kN) bpw_s[i] = (bpg && i < a.K) ? Elem<T>::to_f32(bpg[i]) : 0.f;
   }
   fence_proxy_async_smem();  // B (generic-proxy writes) -> visible to the tensor core
@@ -649,9 +653,12 @@ __global__ void __launch_bounds__(Cfg<CP>::kThreads, 1)
         Vec<kCPT> wv[9];
 #pragma unroll
         for (int t = 0; t < 9; ++t) wv[t] = ld_vec<kCPT>(wdw + ((size_t)g * 9 + t) * kCPT * 2);
-        float bias[kCPT];
+        float bias[kCPT];  // the group's bias, one load (consecutive groups: consecutive bytes), widened exactly
+        {
+          const Vec<kCPT> bq = ld_vec<kCPT>(bdw + (size_t)g * kCPT * 2);
 #pragma unroll
-        for (int e = 0; e < kCPT; ++e) bias[e] = bdw[g * kCPT + e];
+          for (int e = 0; e < kCPT / 2; ++e) widen_word<T>(bq.w[e], &bias[2 * e]);
+        }
         const int gl = g - cc * a.GC;
         const uint8_t* xs = Xs + (size_t)s * a.x_stage_stride + ((size_t)(w * S) * a.CH + gl * kCPT) * 2;
         const int g8 = (g * kCPT) >> 3;  // the 8-channel group of A the thread's channels fall in
@@ -782,10 +789,10 @@ bool make_dw_pw_plan(const Geometry& g, bool bf16, int K, int act, int max_smem,
   a.Ho = g.Ho, a.Wo = g.Wo, a.act = act, a.pH = g.pH, a.pW = g.pW;
   a.wdw_off = 1024;
   a.bdw_off = a.wdw_off + (uint32_t)C * 9u * 2u;
-  a.bpw_off = a.bdw_off + (uint32_t)C * 4u;
+  a.bpw_off = a.bdw_off + (uint32_t)C * 2u;
   a.b_off = round_up(a.bpw_off + (uint32_t)a.Np * 4u, 1024);
   a.a_off = round_up(a.b_off + (uint32_t)a.G * (uint32_t)a.Np * 16u, 1024);
-  a.a_bytes = (uint32_t)(C / 64) * fz::kAtomBytes + (uint32_t)((C % 64) / 8) * fz::kTailGroupBytes;
+  a.a_bytes = round_up((uint32_t)(C / 64) * fz::kAtomBytes + (uint32_t)((C % 64) / 8) * fz::kTailGroupBytes, 1024);
   const uint32_t budget = (uint32_t)std::min(max_smem, 227 * 1024);
 
   bool found = false;

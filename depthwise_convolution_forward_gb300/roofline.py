@@ -53,3 +53,23 @@ def tensor_bytes(wl, out_shape, op: str = "fwd") -> dict:
 
 def algorithmic_bytes(wl, out_shape, op: str = "fwd") -> int:
     return sum(tensor_bytes(wl, out_shape, op).values())
+
+
+def fused_block_bytes(wl, out_shape, K: int) -> dict:
+    """Tensors the fused depthwise + 1x1 projection block moves once: x (the
+    touched positions), the depthwise weights and bias, the projection's
+    weights [K, C] and bias [K], and y [N, Ho, Wo, K].  h, the depthwise
+    output, stays on chip; ``h_saved`` is the HBM traffic of writing it and
+    reading it back that a separate projection would add."""
+    es = ES[wl.dtype]
+    t = tensor_bytes(wl, out_shape)
+    pix = wl.N * out_shape[0] * out_shape[1] * out_shape[2]
+    return {"x": t["x"], "w_dw": t["w"], "b_dw": t["bias"], "w_pw": K * wl.C * es, "b_pw": K * es,
+            "y": pix * K * es, "h_saved": 2 * pix * wl.C * es}
+
+
+def fused_block_flops(wl, out_shape, K: int) -> int:
+    """Depthwise multiply-adds (9 per output channel) plus the projection's
+    (C per output of K)."""
+    pix = wl.N * out_shape[0] * out_shape[1] * out_shape[2]
+    return 2 * pix * wl.C * wl.taps + 2 * pix * wl.C * K

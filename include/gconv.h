@@ -415,8 +415,9 @@ gconv_status grouped_conv_fwd_dw_pw(const void *x, const void *w_dw, const void 
  * GCONV_KERNEL_DW_PW; force_kernel must be AUTO or GCONV_KERNEL_DW_PW).  Tuning overrides,
  * 0 = automatic: opt->tile[0] channels per depthwise thread (8, or 4 with twice the compute
  * warps), opt->tile[1] / tile[2] the output tile's rows TH / columns TW (TW <= 16,
- * TH * TW <= 128, TH a balanced split of Ho: ceil(Ho / ceil(Ho / TH)) == TH); a choice that
- * does not fit returns GCONV_ERR_UNSUPPORTED. */
+ * TH * TW <= 128, TH a balanced split of Ho: ceil(Ho / ceil(Ho / TH)) == TH), opt->tile[3]
+ * the projection's MMA issuer (1 a dedicated warp, 2 the depthwise warp that completes a
+ * tile); a choice that does not fit returns GCONV_ERR_UNSUPPORTED. */
 gconv_status grouped_conv_fwd_dw_pw_ex(const void *x, const void *w_dw, const void *b_dw, const void *w_pw,
                                        const void *b_pw, void *y, const gconv_problem *p, int32_t K,
                                        int32_t act, gconv_dtype dt, struct CUstream_st *stream,

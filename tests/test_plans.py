@@ -445,11 +445,13 @@ def test_fused_block_plans(harness):
         assert p["G"] == C // 8, ctx
         # shared-memory regions: disjoint, in order, aligned, inside the block
         assert p["wdw_off"] >= 264 and p["bdw_off"] >= p["wdw_off"] + 18 * C, ctx
-        assert p["bdw_off"] % 16 == 0 and p["bpw_off"] >= p["bdw_off"] + 4 * C, ctx
+        assert p["bdw_off"] % 16 == 0 and p["bpw_off"] >= p["bdw_off"] + 2 * C and p["bpw_off"] % 4 == 0, ctx
         assert p["b_off"] >= p["bpw_off"] + 4 * p["Np"] and p["b_off"] % 1024 == 0, ctx
         assert p["a_off"] >= p["b_off"] + p["G"] * p["Np"] * 16 and p["a_off"] % 1024 == 0, ctx
-        # A: whole 64-channel swizzled atoms, then the C % 64 tail in 2 KB groups
-        assert p["a_bytes"] == (C // 64) * p["atom"] + (C % 64) // 8 * 2048 and p["atom"] == 128 * 128, ctx
+        # A: whole 64-channel swizzled atoms, then the C % 64 tail in groups of
+        # 2 KB + 16 B, the buffer rounded up to 1 KB
+        tail = (C // 64) * p["atom"] + (C % 64) // 8 * 2064
+        assert p["a_bytes"] == -(-tail // 1024) * 1024 and p["atom"] == 128 * 128, ctx
         assert p["a_bytes"] % 1024 == 0, ctx
         assert p["nA"] in (1, 2, 3) and p["x_off"] == p["a_off"] + p["nA"] * p["a_bytes"], ctx
         assert p["smem"] == p["x_off"] + p["stages"] * p["x_stage_stride"] <= SMEM_BLOCK, ctx

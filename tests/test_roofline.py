@@ -58,3 +58,19 @@ def test_backward_data_bytes_count_all_of_dx():
     assert bwd["x"] == full and fwd["x"] == full // 4
     assert roofline.algorithmic_bytes(wl, out, "bwd_weight") == roofline.algorithmic_bytes(wl, out)
 
+
+
+def test_fused_block_accounting():
+    """Fused depthwise + 1x1 projection on the MobileNetV2 stride-1 layer
+    (N=32, C=144, 56x56, K=24, f16), every tensor once, worked by hand."""
+    wl = inputs.by_name("mbv2_dw_s1_f16")
+    out = (1, 56, 56)
+    pix = 32 * 56 * 56
+    b = roofline.fused_block_bytes(wl, out, 24)
+    assert b == {"x": pix * 144 * 2, "w_dw": 144 * 9 * 2, "b_dw": 144 * 2, "w_pw": 24 * 144 * 2, "b_pw": 24 * 2,
+                 "y": pix * 24 * 2, "h_saved": 2 * pix * 144 * 2}
+    assert roofline.fused_block_flops(wl, out, 24) == 2 * pix * 144 * 9 + 2 * pix * 144 * 24
+    # stride 2, pad 1: every input row and column is read; y at 28 x 28
+    w2 = inputs.by_name("mbv2_dw_s2_f16")
+    b2 = roofline.fused_block_bytes(w2, (1, 28, 28), 32)
+    assert b2["x"] == pix * 144 * 2 and b2["y"] == 32 * 28 * 28 * 32 * 2
