@@ -1,5 +1,6 @@
 // Kb host side: support check, tile planning, tensor-map encoding, launch.
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 
 #include "kernels.h"
@@ -257,10 +258,14 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     if (p.smem_bytes > budget) continue;
     p.grid = n_sc * c.cpg;
     p.ok = true;
-    // Cost: MMA rows per CTA plus a per-tile overhead.  Splitting the taps
-    // over 2 or more partial accumulators measured 5-7% faster on ResNeXt (a)
-    // and the G=32 / G=256 sweeps (shorter accumulation chains, finer tiles).
-    const double cost = (double)c.tiles_h * c.tiles_w * (nmt * 128 + 96) / c.cpg * (np >= 2 ? 0.8 : 1.0);
+    // Cost: MMA rows per CTA plus a per-tile overhead, over the tiles the
+    // busiest CTA of a group chunk walks (a CTA walks whole tiles: with fewer
+    // tiles than CTAs, as in a batch-1 3D layer, the time is one tile's).
+    // Splitting the taps over 2 or more partial accumulators measured 5-7%
+    // faster on ResNeXt (a) and the G=32 / G=256 sweeps (shorter accumulation
+    // chains, finer tiles).
+    const double per_cta = std::ceil((double)c.spatial_tiles / c.cpg);
+    const double cost = per_cta * (nmt * 128 + 96) * (np >= 2 ? 0.8 : 1.0);
     if (cost < best) best = cost, bestp = p;
   }
   if (best >= 1e30) return false;
