@@ -97,18 +97,50 @@ struct SpatialTile {
   int n, od, oh0, ow0;
 };
 
-__device__ __forceinline__ SpatialTile decode_spatial(const TcArgs& a, int sp) {
-  SpatialTile t;
-  const int tw = sp % a.tiles_w;
-  sp /= a.tiles_w;
-  const int th = sp % a.tiles_h;
-  sp /= a.tiles_h;
-  t.od = sp % a.Do;
-  t.n = sp / a.Do;
-  t.oh0 = th * a.TH;
-  t.ow0 = tw * a.TWo;
-  return t;
-}
+// A CTA's spatial tiles sp0, sp0 + step, ... with sp = ((n * Do + od) *
+// tiles_h + th) * tiles_w + tw: the digits (tw, th, od, n) of the tile index
+// are advanced by the digits of the step with carries, so a tile costs no
+// integer division (a runtime divide is a chain of about 150 cycles, and the
+// epilogue of every tile used to wait on three).  Each digit sum stays below
+// twice its radix, so one carry per digit is enough.
+struct SpatialWalk {
+  int tw, th, od, n;
+  int dtw, dth, dod, dn;
+  __device__ __forceinline__ void init(const TcArgs& a, int sp, int step) {
+    tw = sp % a.tiles_w, sp /= a.tiles_w;
+    th = sp % a.tiles_h, sp /= a.tiles_h;
+    od = sp % a.Do, n = sp / a.Do;
+    dtw = step % a.tiles_w, step /= a.tiles_w;
+    dth = step % a.tiles_h, step /= a.tiles_h;
+    dod = step % a.Do, dn = step / a.Do;
+  }
+  __device__ __forceinline__ void advance(const TcArgs& a) {
+    tw += dtw;
+    int c = tw >= a.tiles_w;
+    if (c) tw -= a.tiles_w;
+    th += dth + c;
+    c = th >= a.tiles_h;
+    if (c) th -= a.tiles_h;
+    od += dod + c;
+    c = od >= a.Do;
+    if (c) od -= a.Do;
+    n += dn + c;
+  }
+  __device__ __forceinline__ SpatialTile tile(const TcArgs& a) const {
+    SpatialTile t;
+    t.n = n, t.od = od, t.oh0 = th * a.TH, t.ow0 = tw * a.TWo;
+    return t;
+  }
+};
+
+// Position in a ring of `size` buffers and the parity of its current pass
+// (the k-th use is buffer k % size, pass k / size), advanced without division.
+struct Ring {
+  int pos = 0, ph = 0;
+  __device__ __forceinline__ void next(int size) {
+    if (++pos == size) pos = 0, ph ^= 1;
+  }
+};
 
 // All lanes of a warp wait on `bar`: lane 0 polls (bounded), then every lane
 // observes the completed phase itself.  Returns false on timeout.
@@ -132,13 +164,18 @@ __device__ __forceinline__ void epilogue_store32(T* dst, const float* v, const f
                : "memory");
 }
 
-// Epilogue for one output row of a tile: per batch, load 4 / NP chunks of 16
-// channels from each of the NP partial accumulators (at most 4 loads in
-// flight, one wait), sum the partials, add bias, round, store.
+// Epilogue for one output row of a tile: per batch, load kPer chunks of 16
+// channels from each of the NP partial accumulators (one wait per batch),
+// sum the partials, add bias, round, store.  A batch holds 64 loaded
+// registers with one partial and 32 with two or four partials.  The kernel's
+// nine warps cap a thread at 168 registers (three warps share one scheduler's
+// 16K registers), and 64 loaded registers of two partials made the kernel
+// spill; without spills (and without a division per tile) the tensor-core
+// workloads measured 6-17% faster.
 template <typename T, int NP>
 __device__ __forceinline__ void epilogue_row(uint32_t lane_base, int mt, int G2, int sc, int Nn, bool valid, T* dst,
                                              const float* bias_s, bool v8) {
-  constexpr int kPer = 4 / NP;
+  constexpr int kPer = NP == 1 ? 4 : 1;  // chunks per batch (see epilogue_row)
   const int nchunk16 = sc * Nn / 16;
   for (int c = 0; c < nchunk16; c += kPer) {
     uint32_t r[kPer][NP][16];
@@ -146,10 +183,10 @@ __device__ __forceinline__ void epilogue_row(uint32_t lane_base, int mt, int G2,
     for (int b = 0; b < kPer; ++b) {
       const int cc = c + b;
       if (cc < nchunk16) {
-        const int col = cc * 16;  // channel offset within the row of sc chunks
-        const int j = col / Nn, cn = col - j * Nn;
+        // chunk j = 16 cc / Nn of the row, column 16 cc % Nn in it: accumulator
+        // (p * G2 + mt * sc + j), i.e. column (p * G2 + mt * sc) * Nn + 16 cc
 #pragma unroll
-        for (int p = 0; p < NP; ++p) tmem_ld16(lane_base + (uint32_t)((p * G2 + mt * sc + j) * Nn + cn), r[b][p]);
+        for (int p = 0; p < NP; ++p) tmem_ld16(lane_base + (uint32_t)((p * G2 + mt * sc) * Nn + cc * 16), r[b][p]);
       }
     }
     tmem_ld_wait();
@@ -199,10 +236,8 @@ __device__ __forceinline__ void epilogue_row_stacked(uint32_t lane_base, int mt,
   int rd = 0, rh = 0, rw = 0, cur = -1;
   const int64_t row = (int64_t)om.ext[1] * om.ext[2];
   for (int cc = 0; cc < nchunk16; ++cc) {
-    const int col = cc * 16;
-    const int j = col / Nn, cn = col - j * Nn;
     uint32_t r[16];
-    tmem_ld16(lane_base + (uint32_t)((mt * sc + j) * Nn + cn), r);
+    tmem_ld16(lane_base + (uint32_t)(mt * sc * Nn + cc * 16), r);
     tmem_ld_wait();
     if (valid) {
       if (ph != cur) {  // phase ph = (rd * sH + rh) * sW + rw
@@ -247,7 +282,7 @@ template <typename T, int NP>
 __device__ __forceinline__ void epilogue_row_tma(uint32_t lane_base, int mt, int G2, int sc, int Nn, bool valid,
                                                  int p, const float* bias_s, uint32_t stage_base, uint32_t slice_bytes,
                                                  int W) {
-  constexpr int kPer = 4 / NP;
+  constexpr int kPer = NP == 1 ? 4 : 1;  // chunks per batch (see epilogue_row)
   const int nchunk16 = sc * Nn / 16;
   const uint32_t swz = ((uint32_t)p * (uint32_t)W >> 7) & (uint32_t)(W / 16 - 1);
   const uint32_t row_addr = stage_base + (uint32_t)p * (uint32_t)W;
@@ -257,10 +292,8 @@ __device__ __forceinline__ void epilogue_row_tma(uint32_t lane_base, int mt, int
     for (int b = 0; b < kPer; ++b) {
       const int cc = c + b;
       if (cc < nchunk16) {
-        const int col = cc * 16;  // channel offset within the row of sc chunks
-        const int j = col / Nn, cn = col - j * Nn;
 #pragma unroll
-        for (int q = 0; q < NP; ++q) tmem_ld16(lane_base + (uint32_t)((q * G2 + mt * sc + j) * Nn + cn), r[b][q]);
+        for (int q = 0; q < NP; ++q) tmem_ld16(lane_base + (uint32_t)((q * G2 + mt * sc) * Nn + cc * 16), r[b][q]);
       }
     }
     tmem_ld_wait();
@@ -552,9 +585,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     if (lane == 0) {
       int k = 0;
       bool failed = false;
-      for (int sp = cta_in_gc; sp < a.spatial_tiles; sp += a.cpg, ++k) {
-        const int s = k % a.stages;
-        if (k >= a.stages && !mbar_wait(&a_empty[s], (uint32_t)(((k / a.stages) - 1) & 1), a.wait_limit_ns)) {
+      SpatialWalk walk;
+      walk.init(a, cta_in_gc, a.cpg);
+      Ring sr;
+      for (int sp = cta_in_gc; sp < a.spatial_tiles; sp += a.cpg, ++k, walk.advance(a), sr.next(a.stages)) {
+        const int s = sr.pos;
+        if (k >= a.stages && !mbar_wait(&a_empty[s], (uint32_t)(sr.ph ^ 1), a.wait_limit_ns)) {
           failed = true;
           break;
         }
@@ -567,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
           failed = true;
           break;
         }
-        const SpatialTile st = decode_spatial(a, sp);
+        const SpatialTile st = walk.tile(a);
         const int id0 = st.od * a.sD - a.pD;
         mbar_arrive_expect_tx(&a_full[s], a.tx_bytes);
         uint8_t* stage = As + (size_t)s * a.a_stage_bytes;
@@ -598,7 +634,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     // t with t % np == p, and the epilogue adds the np partials.  Issuer w
     // takes the units u = grp * np + p with u % kIssuers == w; within an
     // issuer, consecutive MMAs cycle over its units (no back-to-back
-    // accumulation into one accumulator).
+    // accumulation into one accumulator).  Whole warps issuing through
+    // elect.sync (faster alone in a probe) measured 1.2-1.9x slower here, and
+    // three issuers (eight warps, no register cap) lost on tiles of four
+    // units, so four lone lanes issue.
     if (lane == 0) {
       const int w = warp - 1;
       int k = 0;
@@ -613,14 +652,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         if (v < w) my_base += steps * nu; else my_len = steps * nu;
       }
       const uint4* my_list = reinterpret_cast<const uint4*>(smem + a.tab_off) + 2 * my_base;
-      for (int sp = cta_in_gc; sp < a.spatial_tiles; sp += a.cpg, ++k) {
-        const int s = k % a.stages;
-        const int ab = k % a.nbuf;
-        if (!mbar_wait(&a_full[s], (uint32_t)((k / a.stages) & 1), a.wait_limit_ns)) {
+      Ring sr, ar;
+      for (int sp = cta_in_gc; sp < a.spatial_tiles; sp += a.cpg, ++k, sr.next(a.stages), ar.next(a.nbuf)) {
+        const int s = sr.pos;
+        const int ab = ar.pos;
+        if (!mbar_wait(&a_full[s], (uint32_t)sr.ph, a.wait_limit_ns)) {
           failed = true;
           break;
         }
-        if (k >= a.nbuf && !mbar_wait(&acc_empty[ab], (uint32_t)(((k / a.nbuf) - 1) & 1), a.wait_limit_ns)) {
+        if (k >= a.nbuf && !mbar_wait(&acc_empty[ab], (uint32_t)(ar.ph ^ 1), a.wait_limit_ns)) {
           failed = true;
           break;
         }
@@ -665,23 +705,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     // read the staging buffer.
     const bool store_thread = warp == kIssuers + 1 && lane == 0;
     const uint32_t stage_base = smem_u32(smem + a.epi_off);
-    int k = 0;
-    for (int sp = cta_in_gc; sp < a.spatial_tiles; sp += a.cpg, ++k) {
-      const int ab = k % a.nbuf;
-      if (!warp_wait(&acc_full[ab], (uint32_t)((k / a.nbuf) & 1), a.wait_limit_ns)) {
+    // This lane's accumulator row f = mt * 128 + row is output (i, jj) of the
+    // tile's flattened rows of pitch P; the same for every tile, so it is
+    // decoded once (f = row) and advanced by 128 rows per M tile.
+    const int i_row0 = row / a.P, jj_row0 = row - i_row0 * a.P;
+    const int di = 128 / a.P, dj = 128 - di * a.P;
+    SpatialWalk walk;
+    walk.init(a, cta_in_gc, a.cpg);
+    Ring ar;
+    for (int sp = cta_in_gc; sp < a.spatial_tiles; sp += a.cpg, walk.advance(a), ar.next(a.nbuf)) {
+      const int ab = ar.pos;
+      if (!warp_wait(&acc_full[ab], (uint32_t)ar.ph, a.wait_limit_ns)) {
         if (lane == 0) report(a.status, kDevTimeout, 5);
         break;
       }
       fence_after_sync();
-      const SpatialTile st = decode_spatial(a, sp);
+      const SpatialTile st = walk.tile(a);
       const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * NP * G2 * a.Nn);
       if constexpr (STAGED) {
         if (store_thread) tma_store_wait_read();  // the previous tile's stores have read the buffer
         asm volatile("bar.sync 3, 128;" ::: "memory");
       }
-      for (int mt = 0; mt < a.nmt; ++mt) {
-        const int f = mt * 128 + row;
-        const int i = f / a.P, jj = f - i * a.P;
+      int i = i_row0, jj = jj_row0;
+      for (int mt = 0; mt < a.nmt; ++mt, i += di, jj += dj) {
+        if (jj >= a.P) jj -= a.P, ++i;  // (i, jj) of row mt * 128 + row
         const int oh = st.oh0 + i, ow = st.ow0 + jj;
         if constexpr (STAGED) {
           // pixels past the image edge are written too; the TMA store clips them
