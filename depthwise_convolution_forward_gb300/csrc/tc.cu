@@ -145,10 +145,12 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     c.a_stage_bytes = round_up((uint32_t)(c.nphase * c.nchunks) * c.plane_stride, 1024);
     c.tx_bytes = (uint32_t)(c.nphase * c.nchunks) * (uint32_t)(c.Dh * c.Hh * c.P) * row_bytes;
     const uint32_t b_bytes = round_up((uint32_t)(c.sc * taps * c.Kt * c.Nn * 2), 1024);
-    // Partial accumulators (taps split np ways, summed by the epilogue): at
-    // least enough that the tile has kIssuers independent units of MMA work,
-    // within 512 TMEM columns.  An explicit count (override slot 4) replaces
-    // that minimum (issuers without a unit then only commit).
+    // Partial accumulators (taps split np ways, summed by the epilogue): the
+    // smallest count that gives the tile kIssuers independent units of MMA
+    // work, within 512 TMEM columns.  More partials only add tensor-memory
+    // reads to the epilogue: on GB300 they measured 2-5% slower on the
+    // stride-1 sweeps and ResNeXt (a).  An explicit count (override slot 4)
+    // replaces it (issuers without a unit then only commit).
     const int G2 = c.sc * c.nmt;
     int np = 1;
     while (np * 2 <= tc::kIssuers && G2 * np < tc::kIssuers && np * 2 <= taps &&
@@ -158,8 +160,7 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
       if (np_cand != 1 || ov[4] < 1 || ov[4] > taps) continue;
       np = ov[4];
     } else {
-      if (np_cand < np || np_cand > taps) continue;
-      np = np_cand;
+      if (np_cand != np) continue;
     }
     c.np = np;
     // per-issuer MMA lists: 32 bytes per entry
@@ -258,14 +259,19 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     if (p.smem_bytes > budget) continue;
     p.grid = n_sc * c.cpg;
     p.ok = true;
-    // Cost: MMA rows per CTA plus a per-tile overhead, over the tiles the
-    // busiest CTA of a group chunk walks (a CTA walks whole tiles: with fewer
-    // tiles than CTAs, as in a batch-1 3D layer, the time is one tile's).
-    // Splitting the taps over 2 or more partial accumulators measured 5-7%
-    // faster on ResNeXt (a) and the G=32 / G=256 sweeps (shorter accumulation
-    // chains, finer tiles).
+    // Cost, in MMA rows of the busiest CTA of a group chunk (a CTA walks
+    // whole tiles: with fewer tiles than CTAs, as in a batch-1 3D layer, the
+    // time is one tile's): the rows of its tiles, plus about 1.2 tiles of
+    // fill (the first copy and MMAs) and drain (the last epilogue) that no
+    // other tile overlaps, plus 96 rows of fixed work per tile, all scaled
+    // up when the tile has fewer units of MMA work than issuers.  Fitted to
+    // tile and tap-split sweeps of ten tensor-core workloads on GB300: it
+    // picks the fastest measured plan on seven and one within 3% on the
+    // other three.
+    const int units = G2 * np;
     const double per_cta = std::ceil((double)c.spatial_tiles / c.cpg);
-    const double cost = per_cta * (nmt * 128 + 96) * (np >= 2 ? 0.8 : 1.0);
+    const double idle = units < tc::kIssuers ? (double)tc::kIssuers / units : 1.0;
+    const double cost = ((per_cta + 1.2) * nmt * 128 + per_cta * 96) * idle;
     if (cost < best) best = cost, bestp = p;
   }
   if (best >= 1e30) return false;
