@@ -22,6 +22,7 @@ struct Plan {
   int64_t num_tiles;
   uint32_t stage_bytes, stage_stride, stage_off, smem_bytes;
   int threads;
+  int sub;  // > 1: planned for the input subsampled by this stride (phase_subsample)
 };
 
 constexpr int kDwK = 3;  // compiled filter extent (Y == X == 3)
@@ -268,6 +269,26 @@ inline bool plannable(const Geometry& g, int es, const int* ov, int num_sms, int
   return make_plan(g, es, ov, num_sms, &p);
 }
 
+// Every tap of a layer with stride s = dilation s >= 2 and padding a
+// multiple of s reads only input rows and columns that are multiples of s
+// (input row s*oh + s*ky - p = s*(oh + ky - p/s)).  Such a layer is the
+// stride-1, dilation-1 layer with padding p/s over the input subsampled by s
+// (extents ceil(H/s), ceil(W/s)), and the tensor map of that subsampled
+// input is the dense one with its W and H strides multiplied by s: the
+// copies then read only the positions the taps use (a quarter of x at
+// s = 2) instead of whole haloed boxes.
+inline bool phase_subsample(const Geometry& g, Geometry* gs) {
+  const int s = g.sH;
+  if (s < 2 || g.sW != s || g.dH != s || g.dW != s || g.pH % s != 0 || g.pW % s != 0) return false;
+  Geometry t = g;
+  t.H = (g.H + s - 1) / s, t.W = (g.W + s - 1) / s;
+  t.sH = t.sW = t.dH = t.dW = 1;
+  t.pH = g.pH / s, t.pW = g.pW / s;
+  if (t.H + 2 * t.pH - (t.Y - 1) != g.Ho || t.W + 2 * t.pW - (t.X - 1) != g.Wo) return false;
+  *gs = t;
+  return true;
+}
+
 template <typename T>
 inline CUtensorMapDataType tma_type() {
   if (std::is_same<T, float>::value) return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -376,30 +397,42 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
   Plan p;
   static SmemAttr attr[2][2][2][3];  // [S-1][DL-1][WB==8][mode]
   static SmemAttr attr_col[2][2][4];  // [S-1][DL-1][form]
+  // The TMA forms run a layer whose taps read one stride phase on the
+  // subsampled input (phase_subsample); the direct-load variant reads x
+  // itself and keeps the layer as it is.
+  Geometry gs;
+  const bool can_sub = la.tile[6] != 2 && phase_subsample(g, &gs);
   if (!cache.get(key, &p)) {
     // tile[6]: 0 automatic (column form when the depth filter is 1),
     // 1 row-blocked form, 2 direct-load variant, 3 column form only.
     const int kind = la.tile[6];
     bool planned = false;
-    if ((kind == 0 || kind == 3) && g.Z == 1) {
-      const int form = col_form(es, la.tile, g.Cg);
-      DwKernel<T> k = pick_col_kernel<T>(g.sH, g.dH, form);
-      cudaFuncAttributes fa{};
-      if (k == nullptr) return cudaErrorNotSupported;
-      cudaError_t e = cudaFuncGetAttributes(&fa, k);
-      if (e != cudaSuccess) return e;
-      planned = make_col_plan(g, es, la.tile, dev.num_sms, form, fa.numRegs, &p);
+    for (int attempt = can_sub ? 0 : 1; attempt < 2 && !planned; ++attempt) {
+      const Geometry& gq = attempt == 0 ? gs : g;
+      if ((kind == 0 || kind == 3) && gq.Z == 1) {
+        const int form = col_form(es, la.tile, gq.Cg);
+        DwKernel<T> k = pick_col_kernel<T>(gq.sH, gq.dH, form);
+        cudaFuncAttributes fa{};
+        if (k == nullptr) return cudaErrorNotSupported;
+        cudaError_t e = cudaFuncGetAttributes(&fa, k);
+        if (e != cudaSuccess) return e;
+        planned = make_col_plan(gq, es, la.tile, dev.num_sms, form, fa.numRegs, &p);
+      }
+      if (!planned && kind != 3 && gq.Cg == 1) planned = make_plan(gq, es, la.tile, dev.num_sms, &p);
+      p.sub = attempt == 0 ? g.sH : 1;
     }
-    if (!planned && kind != 3 && g.Cg == 1) planned = make_plan(g, es, la.tile, dev.num_sms, &p);
     if (!planned) return cudaErrorNotSupported;
+    const Geometry& gq = p.sub > 1 ? gs : g;
     if (p.direct) {
       // one CTA per tile: the grid's x extent bounds the tile count
-      if (p.num_tiles >= ((int64_t)1 << 31) || pick_ldg_kernel<T>(g.sH, g.dH, p.WB, p.mode) == nullptr)
+      if (p.sub > 1 || p.num_tiles >= ((int64_t)1 << 31) ||
+          pick_ldg_kernel<T>(gq.sH, gq.dH, p.WB, p.mode) == nullptr)
         return cudaErrorNotSupported;
     } else {
-      DwKernel<T> k = p.col ? pick_col_kernel<T>(g.sH, g.dH, p.mode) : pick_kernel<T>(g.sH, g.dH, p.WB, p.mode);
+      DwKernel<T> k = p.col ? pick_col_kernel<T>(gq.sH, gq.dH, p.mode) : pick_kernel<T>(gq.sH, gq.dH, p.WB, p.mode);
       if (k == nullptr || p.smem_bytes > (uint32_t)dev.max_smem_optin) return cudaErrorNotSupported;
-      SmemAttr& at = p.col ? attr_col[g.sH - 1][g.dH - 1][p.mode] : attr[g.sH - 1][g.dH - 1][p.WB == 8][p.mode];
+      SmemAttr& at =
+          p.col ? attr_col[gq.sH - 1][gq.dH - 1][p.mode] : attr[gq.sH - 1][gq.dH - 1][p.WB == 8][p.mode];
       cudaError_t e = at.ensure(k, dev.device, (int)p.smem_bytes);
       if (e != cudaSuccess) return e;
       int occ = 0;
@@ -410,30 +443,33 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
     }
     cache.put(key, p);
   }
+  const Geometry& gq = p.sub > 1 ? gs : g;
   if (p.direct) {
     DwArgs a{};
     a.x = la.x;
-    a.D = g.D, a.H = g.H, a.W = g.W;
+    a.D = gq.D, a.H = gq.H, a.W = gq.W;
     a.w = la.w;
     a.bias = la.bias;
     a.y = la.y;
-    a.C = g.C();
-    a.Do = g.Do, a.Ho = g.Ho, a.Wo = g.Wo;
-    a.Z = g.Z, a.dD = g.dD, a.sD = g.sD, a.pD = g.pD, a.pH = g.pH, a.pW = g.pW;
+    a.C = gq.C();
+    a.Do = gq.Do, a.Ho = gq.Ho, a.Wo = gq.Wo;
+    a.Z = gq.Z, a.dD = gq.dD, a.sD = gq.sD, a.pD = gq.pD, a.pH = gq.pH, a.pW = gq.pW;
     a.TH = p.TH, a.TW = p.TW, a.TC = p.TC;
     a.tiles_c = p.tiles_c, a.tiles_w = p.tiles_w, a.tiles_h = p.tiles_h;
     a.num_tiles = p.num_tiles;
     a.status = la.status;
     a.wait_limit_ns = la.wait_limit_ns;
-    DwLdgKernel<T> k = pick_ldg_kernel<T>(g.sH, g.dH, p.WB, p.mode);
+    DwLdgKernel<T> k = pick_ldg_kernel<T>(gq.sH, gq.dH, p.WB, p.mode);
     return launch_kernel(k, dim3((unsigned)p.num_tiles), dim3(p.threads), p.smem_bytes, la, a);
   }
 
   // x viewed as a 5-D tensor (C, W, H, D, N), innermost first.
   CUtensorMap map;
-  const uint64_t C = g.C();
-  uint64_t dims[5] = {C, (uint64_t)g.W, (uint64_t)g.H, (uint64_t)g.D, (uint64_t)g.N};
-  uint64_t strides[4] = {C * es, C * es * g.W, C * es * g.W * g.H, C * es * g.W * g.H * g.D};
+  const uint64_t C = gq.C();
+  uint64_t dims[5] = {C, (uint64_t)gq.W, (uint64_t)gq.H, (uint64_t)gq.D, (uint64_t)gq.N};
+  // (subsampled input: rows and columns s apart in the dense tensor g)
+  const uint64_t sub = (uint64_t)p.sub;
+  uint64_t strides[4] = {C * es * sub, C * es * g.W * sub, C * es * g.W * g.H, C * es * g.W * g.H * g.D};
   const int h0 = p.col ? p.h0 : p.Hh;
   uint32_t box[5] = {(uint32_t)p.TC, (uint32_t)p.Wh, (uint32_t)p.Hh, (uint32_t)p.Dh, 1u};
   uint32_t estr[5] = {1, 1, 1, 1, 1};
@@ -452,13 +488,13 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
 
   DwArgs a{};
   a.x = la.x;
-  a.D = g.D, a.H = g.H, a.W = g.W;
+  a.D = gq.D, a.H = gq.H, a.W = gq.W;
   a.w = la.w;
   a.bias = la.bias;
   a.y = la.y;
-  a.C = g.C();
-  a.Do = g.Do, a.Ho = g.Ho, a.Wo = g.Wo;
-  a.Z = g.Z, a.dD = g.dD, a.sD = g.sD, a.pD = g.pD, a.pH = g.pH, a.pW = g.pW;
+  a.C = gq.C();
+  a.Do = gq.Do, a.Ho = gq.Ho, a.Wo = gq.Wo;
+  a.Z = gq.Z, a.dD = gq.dD, a.sD = gq.sD, a.pD = gq.pD, a.pH = gq.pH, a.pW = gq.pW;
   a.TH = p.TH, a.TW = p.TW, a.TC = p.TC;
   a.Dh = p.Dh, a.Hh = p.Hh, a.Wh = p.Wh;
   a.tiles_c = p.tiles_c, a.tiles_w = p.tiles_w, a.tiles_h = p.tiles_h;
@@ -473,7 +509,7 @@ cudaError_t dw_launch_typed(const Geometry& g, const LaunchArgs& la, const Devic
 
   const int64_t grid64 = std::min<int64_t>(p.num_tiles, (int64_t)dev.num_sms * p.ctas_per_sm);
   const int grid = (int)std::max<int64_t>(1, grid64);
-  DwKernel<T> kern = p.col ? pick_col_kernel<T>(g.sH, g.dH, p.mode) : pick_kernel<T>(g.sH, g.dH, p.WB, p.mode);
+  DwKernel<T> kern = p.col ? pick_col_kernel<T>(gq.sH, gq.dH, p.mode) : pick_kernel<T>(gq.sH, gq.dH, p.WB, p.mode);
   a.h0 = h0;
   a.bytes0 = (uint32_t)h0 * p.Wh * p.TC * p.Dh * es;
   return launch_kernel(kern, dim3(grid), dim3(p.threads), p.smem_bytes, la, map, map0, map1, a);

@@ -90,6 +90,10 @@ DW_EDGE = [
     (1, 16, 3, 300, 1, 1, 1, "f16"),  # wide rows: several column tiles
     (3, 32, 1, 1, 1, 1, 1, "bf16"),   # 1x1 input, padding only
     (1, 16, 3, 3, 2, 1, 2, "f16"),    # output 1x1, dilated
+    # stride = dilation = 2 with padding a multiple of 2: every tap reads even
+    # rows and columns, so the TMA forms run on the input subsampled by 2
+    (1, 8, 14, 13, 2, 4, 2, "f16"),
+    (1, 8, 11, 12, 2, 0, 2, "bf16"),
 ]
 
 
