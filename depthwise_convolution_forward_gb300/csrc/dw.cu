@@ -56,14 +56,23 @@ bool dw_supported(const Geometry& g, DType dt, const LaunchArgs* a, int num_sms)
   // With launch arguments a device is at hand: plan with the column kernel's
   // real register count, as the launch does (tile overrides may need it);
   // the host-only query plans with the most it can have.
+  // The TMA forms run a layer whose taps read one stride phase as the
+  // stride-1 layer over the subsampled input (dw::phase_subsample), and fall
+  // back to the layer as it is; the launch plans in the same order.
   const int form = dw::col_form(es, a ? a->tile : nullptr, g.Cg);
-  int regs = dw::col_max_regs(form);
-  if (a && g.Z == 1) {
-    const int r = dt == kF32 ? dw_col_regs_f32(g.sH, g.dH, form)
-                             : (dt == kF16 ? dw_col_regs_f16(g.sH, g.dH, form) : dw_col_regs_bf16(g.sH, g.dH, form));
-    if (r > 0) regs = r;
+  Geometry gs;
+  const bool sub = !(a && a->tile[6] == 2) && dw::phase_subsample(g, &gs);
+  for (int attempt = sub ? 0 : 1; attempt < 2 && !ok; ++attempt) {
+    const Geometry& gq = attempt == 0 ? gs : g;
+    int regs = dw::col_max_regs(form);
+    if (a && gq.Z == 1) {
+      const int r = dt == kF32 ? dw_col_regs_f32(gq.sH, gq.dH, form)
+                               : (dt == kF16 ? dw_col_regs_f16(gq.sH, gq.dH, form)
+                                             : dw_col_regs_bf16(gq.sH, gq.dH, form));
+      if (r > 0) regs = r;
+    }
+    ok = dw::plannable(gq, es, a ? a->tile : nullptr, num_sms, regs) ? 1 : 0;
   }
-  ok = dw::plannable(g, es, a ? a->tile : nullptr, num_sms, regs) ? 1 : 0;
   cache.put(key, ok);
   return ok != 0;
 }
