@@ -93,13 +93,15 @@ bool overlaps(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
 // the generic kernel; each specialised kernel is taken only when its planner
 // finds a launch plan for this device (dev; NULL: a GB300's SM count and
 // shared memory, for the host-only query).  Groups of two channels run on
-// the direct kernel at stride 1 and on the tensor-core kernel at stride 2,
-// the faster of the two on GB300 (sweep G=256: 38.5 against 44.6-46.5 us
-// at stride 1, 18.2-16.2 against 21.8-23.6 us at stride 2).
+// the direct kernel at stride 1 and dilation 1 and on the tensor-core kernel
+// otherwise, the faster of the two on GB300 (sweep G=256: 33.4 against 35.6
+// us at stride 1 dilation 1; 38.3 against 35.4 us at dilation 2; 15.9-14.2
+// against 21.8-23.6 us at stride 2).
 int select_kernel(const Geometry& g, DType dt, const LaunchArgs* a, const DeviceInfo* dev) {
   const int sms = dev ? dev->num_sms : kDefaultSms;
   const int smem = dev ? dev->max_smem_optin : kDefaultSmemOptin;
-  if (g.Cg == 2 && g.Kg == 2 && (g.sH > 1 || g.sW > 1) && tc_supported(g, dt, a, sms, smem))
+  if (g.Cg == 2 && g.Kg == 2 && (g.sH > 1 || g.sW > 1 || g.dH > 1 || g.dW > 1) &&
+      tc_supported(g, dt, a, sms, smem))
     return GCONV_KERNEL_IGEMM_TC;
   if (dw_supported(g, dt, a, sms)) return GCONV_KERNEL_DIRECT_DW;
   if (tc_supported(g, dt, a, sms, smem)) return GCONV_KERNEL_IGEMM_TC;

@@ -114,6 +114,10 @@ def test_selector_is_shape_based():
     assert sel["mbv2_dw_s1_f16"] == B.KERNEL_DIRECT_DW
     assert sel["mbv2_dw_s2_f16"] == B.KERNEL_DIRECT_DW
     assert sel["sweep_g512_d2_s2_bf16"] == B.KERNEL_DIRECT_DW
+    # groups of two channels: the direct kernel at stride 1 and dilation 1 only
+    assert sel["sweep_g256_d1_s1_bf16"] == B.KERNEL_DIRECT_DW
+    assert sel["sweep_g256_d2_s1_bf16"] == B.KERNEL_IGEMM_TC
+    assert sel["sweep_g256_d1_s2_bf16"] == B.KERNEL_IGEMM_TC
     assert sel["grouped2d_f32_smoke"] == B.KERNEL_DIRECT_GENERIC  # fp32 never on tensor cores
     # depthwise with 3 channels breaks 16-byte vectors: generic path
     wl = inputs.by_name("mbv2_dw_s1_f16").with_(G=3)
