@@ -311,6 +311,201 @@ __global__ void __launch_bounds__(256) bwd_weight_reduce_few_kernel(const BwwArg
   }
 }
 
+template <typename T>
+cudaError_t reduce_typed(const Geometry& g, const LaunchArgs& la, float* ws, int S, const DeviceInfo& dev);
+
+// Tiled form for two input channels per group (Cg = 2) when every dw
+// element fits one CTA's threads: a CTA stages one output row (n, od, oh)
+// at a time in shared memory -- dy[n, od, oh, :, :] (Wo pixels x K channels)
+// and the Z * Y input rows its taps read, each WR = (Wo-1)*sW + (X-1)*dW + 1
+// pixels wide from column -pW, zeros outside x -- and thread (pair, part)
+// accumulates output channel k of group g (pair = g*Kg + k) against a
+// contiguous block of taps, all Cg input channels, over the row's pixels.
+// The per-pixel form above issues four small global loads for six MACs on
+// the 3D layers (Cg = 2, Kg = 4); here every operand comes from shared
+// memory.  A CTA takes rows cta, cta + S, ... and writes one fp32 partial of
+// every dw element; the reduction adds the S partials in order.
+constexpr int kTileThreads = 256;
+constexpr int kTileMaxTaps = 16;  // taps per thread
+constexpr int kTileSplits = 304;  // CTAs (two per SM of a 152-SM GPU), fixed so the workspace is device-free
+
+struct BwTileArgs {
+  const void* x;
+  const void* dy;
+  float* ws;
+  int G, Cg, Kg, C, K;
+  int D, H, W, Do, Ho, Wo, Z, Y, X;
+  int sD, sH, sW, pD, pH, pW, dD, dH, dW;
+  int taps, WR;     // taps per filter, staged row width in pixels
+  int tsplit, tpt;  // threads per (g, k) pair, taps per thread
+  int64_t rows;     // output rows N * Do * Ho
+  int S;            // CTAs = partials
+  int64_t E;        // dw elements
+  uint32_t x_bytes;  // staged input rows (the dy row follows)
+};
+
+// 16-byte copy global -> shared, asynchronous; src_bytes 0 writes zeros
+// (the source is then not read, but is still a valid address).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+template <typename T, int CG>
+__global__ void __launch_bounds__(kTileThreads) bwd_weight_tile_kernel(const BwTileArgs a) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  const uint4* __restrict__ x4 = static_cast<const uint4*>(a.x);
+  const uint4* __restrict__ dy4 = static_cast<const uint4*>(a.dy);
+  constexpr int kPiece = 16 / (int)sizeof(T);  // elements per 16-byte piece
+  const uint32_t buf_bytes = a.x_bytes + (uint32_t)(a.Wo * a.K) * (uint32_t)sizeof(T);  // one row's staging
+  const int tid = threadIdx.x;
+  const int pair = tid / a.tsplit, part = tid - pair * a.tsplit;
+  const bool active = pair < a.G * a.Kg;
+  const int g = active ? pair / a.Kg : 0;
+  const int t0 = part * a.tpt;
+  const int nt = active ? max(0, min(a.tpt, a.taps - t0)) : 0;
+  // per tap of this thread: its element offset in the staged rows at output column 0
+  int toff[kTileMaxTaps];
+#pragma unroll
+  for (int t = 0; t < kTileMaxTaps; ++t) {
+    const int tt = min(t0 + t, a.taps - 1);
+    const int xx = tt % a.X, r = tt / a.X;  // r = z * Y + yy
+    toff[t] = (r * a.WR + xx * a.dW) * a.C + g * CG;
+  }
+  float acc[kTileMaxTaps][CG];
+#pragma unroll
+  for (int t = 0; t < kTileMaxTaps; ++t)
+#pragma unroll
+    for (int c = 0; c < CG; ++c) acc[t][c] = 0.f;
+  const int colstep = a.sW * a.C;
+  const int ppx = a.C / kPiece;  // pieces per input pixel
+  const int row_pieces = a.WR * ppx;
+  const int dy_pieces = a.Wo * a.K / kPiece;
+  // the in-range pixels of an input row are contiguous in x, so staged
+  // piece k of a row maps to x piece base + k; pieces outside
+  // [pW * ppx, (pW + W) * ppx) are the zero padding
+  const int lo = a.pW * ppx, hi = (a.pW + a.W) * ppx;
+
+  // Copies of output row `row` into buffer b: the Z * Y input rows, then dy.
+  auto stage = [&](int64_t row, int b) {
+    uint8_t* base_s = sm + (size_t)b * buf_bytes;
+    uint4* xs4 = reinterpret_cast<uint4*>(base_s);
+    uint4* dys4 = reinterpret_cast<uint4*>(base_s + a.x_bytes);
+    const int oh = (int)(row % a.Ho);
+    const int64_t q = row / a.Ho;
+    const int od = (int)(q % a.Do);
+    const int64_t n = q / a.Do;
+    for (int r = 0; r < a.Z * a.Y; ++r) {
+      const int z = r / a.Y, yy = r - z * a.Y;
+      const int id = od * a.sD - a.pD + z * a.dD, ih = oh * a.sH - a.pH + yy * a.dH;
+      const bool rv = (unsigned)id < (unsigned)a.D && (unsigned)ih < (unsigned)a.H;
+      const int64_t base = rv ? ((n * a.D + id) * a.H + ih) * (int64_t)a.W * ppx - lo : 0;
+      for (int k = tid; k < row_pieces; k += kTileThreads) {
+        const bool in = rv && k >= lo && k < hi;
+        cp_async16(xs4 + (size_t)r * row_pieces + k, in ? x4 + base + k : x4, in ? 16u : 0u);
+      }
+    }
+    const uint4* dsrc = dy4 + (((n * a.Do + od) * a.Ho + oh) * (int64_t)a.Wo * a.K) / kPiece;
+    for (int k = tid; k < dy_pieces; k += kTileThreads) cp_async16(dys4 + k, dsrc + k, 16u);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+
+  grid_dependency_wait();  // x, dy and the workspace are touched only from here on
+
+  // Two buffers: the copies of the CTA's next row are in flight while its
+  // current row is summed.
+  int b = 0;
+  if ((int64_t)blockIdx.x < a.rows) stage(blockIdx.x, 0);
+  for (int64_t row = blockIdx.x; row < a.rows; row += a.S, b ^= 1) {
+    if (row + a.S < a.rows) {
+      stage(row + a.S, b ^ 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();
+    const T* xs = reinterpret_cast<const T*>(sm + (size_t)b * buf_bytes);
+    const T* dys = reinterpret_cast<const T*>(sm + (size_t)b * buf_bytes + a.x_bytes);
+    if (active) {
+      for (int ow = 0; ow < a.Wo; ++ow) {
+        const T dvt = dys[ow * a.K + pair];
+        const int cb = ow * colstep;
+        if constexpr (CG == 2 && sizeof(T) == 2) {
+          const uint32_t h = *reinterpret_cast<const unsigned short*>(&dvt);
+          const uint32_t dpair = h | (h << 16);
+#pragma unroll
+          for (int t = 0; t < kTileMaxTaps; ++t)
+            if (t < nt)
+              fma_mixed_pair<T>(*reinterpret_cast<const uint32_t*>(xs + cb + toff[t]), dpair, acc[t][0], acc[t][1]);
+        } else {
+          const float d = Elem<T>::to_f32(dvt);
+#pragma unroll
+          for (int t = 0; t < kTileMaxTaps; ++t)
+            if (t < nt)
+#pragma unroll
+              for (int c = 0; c < CG; ++c) acc[t][c] = fmaf(d, Elem<T>::to_f32(xs[cb + toff[t] + c]), acc[t][c]);
+        }
+      }
+    }
+    __syncthreads();  // buffer b is free for the copies of the row after next
+  }
+  float* ws = a.ws + (int64_t)blockIdx.x * a.E;
+#pragma unroll
+  for (int t = 0; t < kTileMaxTaps; ++t)
+    if (t < nt)
+#pragma unroll
+      for (int c = 0; c < CG; ++c) ws[((int64_t)pair * a.taps + t0 + t) * a.Cg + c] = acc[t][c];
+}
+
+// The tiled form's shape: threads per (g, k) pair, taps per thread, staged
+// bytes; false when the problem is outside its range.
+struct BwTilePlan {
+  int tsplit, tpt, WR, S;
+  uint32_t x_bytes, smem;
+};
+bool plan_bw_tile(const Geometry& g, int es, BwTilePlan* p) {
+  // two input channels per group: the per-pixel form's vectors serve one
+  // (depthwise: 62 against 114 us on the MobileNetV2 layer) and wider groups
+  if (g.Cg != 2) return false;
+  const int pairs = g.G * g.Kg;
+  if (pairs > kTileThreads) return false;
+  if ((g.C() * es) % 16 != 0 || (g.K() * es) % 16 != 0) return false;
+  const int tsplit = kTileThreads / pairs;
+  const int tpt = (g.taps() + tsplit - 1) / tsplit;
+  if (tpt > kTileMaxTaps) return false;
+  const int64_t WR = (int64_t)(g.Wo - 1) * g.sW + (int64_t)(g.X - 1) * g.dW + 1;
+  const int64_t xb = (int64_t)g.Z * g.Y * WR * g.C() * es, yb = (int64_t)g.Wo * g.K() * es;
+  if (2 * (xb + yb) > 110 * 1024) return false;  // two buffers, two CTAs per SM
+  const int64_t rows = g.N * (int64_t)g.Do * g.Ho;
+  p->tsplit = tsplit, p->tpt = tpt, p->WR = (int)WR;
+  p->S = (int)std::min<int64_t>(rows, kTileSplits);
+  p->x_bytes = (uint32_t)xb, p->smem = (uint32_t)(2 * (xb + yb));
+  return true;
+}
+
+template <typename T>
+cudaError_t bwd_weight_tile_typed(const Geometry& g, const LaunchArgs& la, float* ws, const BwTilePlan& p,
+                                  const DeviceInfo& dev) {
+  BwTileArgs a{};
+  a.x = la.x;
+  a.dy = la.w;  // a.w carries dy (see kernels.h)
+  a.ws = ws;
+  a.G = g.G, a.Cg = g.Cg, a.Kg = g.Kg, a.C = g.C(), a.K = g.K();
+  a.D = g.D, a.H = g.H, a.W = g.W, a.Do = g.Do, a.Ho = g.Ho, a.Wo = g.Wo, a.Z = g.Z, a.Y = g.Y, a.X = g.X;
+  a.sD = g.sD, a.sH = g.sH, a.sW = g.sW, a.pD = g.pD, a.pH = g.pH, a.pW = g.pW, a.dD = g.dD, a.dH = g.dH,
+  a.dW = g.dW;
+  a.taps = g.taps(), a.WR = p.WR, a.tsplit = p.tsplit, a.tpt = p.tpt;
+  a.rows = g.N * (int64_t)g.Do * g.Ho;
+  a.S = p.S;
+  a.E = g.w_elems();
+  a.x_bytes = p.x_bytes;
+  static SmemAttr attr;  // (plan_bw_tile takes Cg = 2 only)
+  cudaError_t e = attr.ensure(bwd_weight_tile_kernel<T, 2>, dev.device, (int)p.smem);
+  if (e == cudaSuccess) e = launch_kernel(bwd_weight_tile_kernel<T, 2>, dim3(p.S), dim3(kTileThreads), p.smem, la, a);
+  if (e != cudaSuccess) return e;
+  return reduce_typed<T>(g, la, ws, p.S, dev);
+}
+
 // Launch plan: mode, vector width, items, CTA shape and splits.  Depends on
 // the problem and element size only (not on the device), so the workspace
 // size can be queried without a GPU.
@@ -380,6 +575,13 @@ cudaError_t launch_partial(const BwwArgs& a, const BwwPlan& p, const LaunchArgs&
 
 template <typename T>
 cudaError_t bwd_weight_typed(const Geometry& g, const LaunchArgs& la, float* ws, const DeviceInfo& dev) {
+  // the tiled form where its range and the 16-byte alignment of x and dy allow
+  {
+    BwTilePlan tp;
+    if (plan_bw_tile(g, (int)sizeof(T), &tp) &&
+        ((reinterpret_cast<uintptr_t>(la.x) | reinterpret_cast<uintptr_t>(la.w)) & 15) == 0)
+      return bwd_weight_tile_typed<T>(g, la, ws, tp, dev);
+  }
   // the widest vector both x and dy are aligned to
   int vmax = 16 / (int)sizeof(T);
   while (vmax > 1 && ((reinterpret_cast<uintptr_t>(la.x) | reinterpret_cast<uintptr_t>(la.w)) &
@@ -453,8 +655,11 @@ cudaError_t bwd_weight_reduce_launch(const Geometry& g, const LaunchArgs& a, flo
 
 int64_t bwd_weight_workspace_bytes(const Geometry& g, DType dt) {
   const BwwPlan p = plan_bww(g, dtype_bytes(dt), 16 / dtype_bytes(dt));
-  // either route may run (the tensor-core one needs 16-byte aligned x and dy)
-  return std::max<int64_t>((int64_t)p.S * p.E * 4, bwd_weight_tc_workspace_bytes(g, dt));
+  // any route may run (the tensor-core and tiled ones need 16-byte aligned x and dy)
+  int64_t bytes = std::max<int64_t>((int64_t)p.S * p.E * 4, bwd_weight_tc_workspace_bytes(g, dt));
+  BwTilePlan tp;
+  if (plan_bw_tile(g, dtype_bytes(dt), &tp)) bytes = std::max<int64_t>(bytes, (int64_t)tp.S * g.w_elems() * 4);
+  return bytes;
 }
 
 cudaError_t bwd_weight_launch(const Geometry& g, const LaunchArgs& a, void* workspace, const DeviceInfo& dev) {
