@@ -222,7 +222,10 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
     c.epi_slice_bytes = round_up((uint32_t)(c.TH * c.TWo) * (uint32_t)c.epi_w, 1024);
     const uint32_t epi_bytes = (uint32_t)c.epi_slices * c.epi_slice_bytes;
     const bool want_epi = ov && ov[7] < 0;
-    int stages = (ov && ov[3]) ? ov[3] : tc::kMaxStages;
+    // At stride 1, three stages of 128-byte-row planes by default: a fourth,
+    // requested at launch with every CTA's first copies, measured 1.5% slower
+    // on ResNeXt (a).  At stride 2 the fourth measured 2-5% faster.
+    int stages = (ov && ov[3]) ? ov[3] : ((sw && a.s == 1) ? 3 : tc::kMaxStages);
     stages = std::min(stages, tc::kMaxStages);
     auto a_end_of = [&](int st) { return c.a_off + (uint32_t)st * c.a_stage_bytes; };
     bool epi = want_epi && a_end_of(2) + epi_bytes <= budget;
