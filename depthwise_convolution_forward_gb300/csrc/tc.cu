@@ -139,6 +139,24 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
           c.tap_off[t] = z * g.dD * c.Hh * c.P + (qy[ky] - qy_min) * c.P + (aligned ? 0 : qx[kx] - qx_min);
           max_off = std::max(max_off, c.tap_off[t]);
         }
+    // Row shift (shift <= 0): accumulator row f of a tile holds flattened
+    // output f + shift, so tap t's A operand starts at plane row mt * 128 +
+    // shift + tap_off[t].  An MMA whose A starts on an 8-row boundary costs
+    // about 39 cycles on GB300 against 57 off it (M = 128, N <= 64), so the
+    // shift that puts the most taps on that boundary is taken, while the
+    // tile's TH * P outputs still fit its nmt * 128 rows.  The rows before
+    // the first output read whatever precedes the plane in shared memory and
+    // are never stored.
+    {
+      int best = -1;
+      c.shift = 0;
+      for (int sh = 0; sh > -8; --sh) {
+        if (c.TH * c.P - sh > nmt * 128) break;
+        int cnt = 0;
+        for (int t = 0; t < taps; ++t) cnt += ((c.tap_off[t] + sh) & 7) == 0;
+        if (cnt > best) best = cnt, c.shift = sh;
+      }
+    }
     const uint32_t plane_px = round_up((uint32_t)std::max(c.Dh * c.Hh * c.P, c.nmt * 128 + max_off), 8);
     const uint32_t row_bytes = sw ? 128u : 16u;
     c.plane_stride = plane_px * row_bytes;
@@ -194,11 +212,11 @@ bool make_tc_plan_mode(const Geometry& g, bool bf16, int num_sms, int max_smem, 
           if (t < taps) {
             uint32_t aoff;
             if (sw)
-              aoff = c.a_off + (uint32_t)c.tap_phase[t] * c.plane_stride + (uint32_t)(mt * 128 + c.tap_off[t]) * 128u +
+              aoff = c.a_off + (uint32_t)c.tap_phase[t] * c.plane_stride + (uint32_t)(mt * 128 + c.shift + c.tap_off[t]) * 128u +
                      (uint32_t)(j * c.Kt * 2 + ks * 32);
             else
               aoff = c.a_off + (uint32_t)(c.tap_phase[t] * c.nchunks + 2 * ks) * c.plane_stride +
-                     (uint32_t)(mt * 128 + c.tap_off[t]) * 16u;
+                     (uint32_t)(mt * 128 + c.shift + c.tap_off[t]) * 16u;
             const uint32_t boff = c.b_off + (uint32_t)((j * c.KS + ks) * 2 * taps + t) * slab;
             e = make_uint2((aoff >> 4) | ((boff >> 4) << 16),
                            (uint32_t)((pp * G2 + grp) * c.Nn) | ((st == 0 ? 0u : 1u) << 16));

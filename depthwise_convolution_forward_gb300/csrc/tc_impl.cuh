@@ -68,6 +68,7 @@ struct TcArgs {
   int nchunks, Kt, Nn, KS, nmt;
   int sc;                  // group chunks per 128-byte row (swizzled layout), else 1
   int np;                  // partial accumulators per accumulator (taps split np ways)
+  int shift;               // <= 0: accumulator row f holds flattened output f + shift (8-row A alignment)
   int nbuf;                // accumulator buffers (2..kMaxAccBufs): tile k uses buffer k % nbuf
   uint32_t plane_stride, a_stage_bytes, tx_bytes;
   uint32_t a_off, b_off, bias_off, tab_off;  // smem offsets (tab: MMA descriptor table)
@@ -544,11 +545,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             uint64_t adesc;
             if constexpr (SW) {
               const uint32_t row = a_base + (uint32_t)a.tap_phase[t] * a.plane_stride +
-                                   (uint32_t)(mt * 128 + a.tap_off[t]) * 128u;
+                                   (uint32_t)(mt * 128 + a.shift + a.tap_off[t]) * 128u;
               adesc = smem_desc_sw128(row + (uint32_t)(j * a.Kt * 2 + ks * 32));
             } else {
               const uint32_t plane0 = a_base + (uint32_t)(a.tap_phase[t] * a.nchunks) * a.plane_stride;
-              const uint32_t row0 = (uint32_t)(mt * 128 + a.tap_off[t]) * 16u;
+              const uint32_t row0 = (uint32_t)(mt * 128 + a.shift + a.tap_off[t]) * 16u;
               adesc = smem_desc(plane0 + (uint32_t)(2 * ks) * a.plane_stride + row0, a.plane_stride, 128u);
             }
             const uint64_t bdesc =
@@ -783,10 +784,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     // read the staging buffer.
     const bool store_thread = warp == kIssuers + 1 && lane == 0;
     const uint32_t stage_base = smem_u32(smem + a.epi_off);
-    // This lane's accumulator row f = mt * 128 + row is output (i, jj) of the
-    // tile's flattened rows of pitch P; the same for every tile, so it is
-    // decoded once (f = row) and advanced by 128 rows per M tile.
-    const int i_row0 = row / a.P, jj_row0 = row - i_row0 * a.P;
+    // This lane's accumulator row f = mt * 128 + row is flattened output
+    // f + shift, i.e. (i, jj) of the tile's rows of pitch P; the same for
+    // every tile, so it is decoded once and advanced by 128 rows per M tile.
+    // Rows before the first output (i < 0) are never stored.
+    int i_row0 = 0, jj_row0 = row + a.shift;
+    while (jj_row0 < 0) jj_row0 += a.P, --i_row0;
+    i_row0 += jj_row0 / a.P;
+    jj_row0 -= (jj_row0 / a.P) * a.P;
     const int di = 128 / a.P, dj = 128 - di * a.P;
     SpatialWalk walk;
     walk.init(a, cta_in_gc, a.cpg);
@@ -810,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         const int oh = st.oh0 + i, ow = st.ow0 + jj;
         if constexpr (STAGED) {
           // pixels past the image edge are written too; the TMA store clips them
-          const bool valid = i < a.TH && jj < a.TWo;
+          const bool valid = i >= 0 && i < a.TH && jj < a.TWo;
           const int p = i * a.TWo + jj;
           if (NP == 1)
             epilogue_row_tma<T, 1>(lane_base, mt, G2, a.sc, a.Nn, valid, p, bias_s, stage_base, a.epi_slice_bytes,
@@ -822,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             epilogue_row_tma<T, 4>(lane_base, mt, G2, a.sc, a.Nn, valid, p, bias_s, stage_base, a.epi_slice_bytes,
                                    a.epi_w);
         } else {
-          bool valid = i < a.TH && jj < a.TWo && oh < a.Ho && ow < a.Wo;
+          bool valid = i >= 0 && i < a.TH && jj < a.TWo && oh < a.Ho && ow < a.Wo;
           if (a.om.on == 2) {  // stacked phases (planned with one partial accumulator)
             epilogue_row_stacked<T>(lane_base, mt, a.sc, a.Nn, valid, st.n, st.od, oh, ow, a.om, g0 * a.Kg, a.Kg,
                                     yg);

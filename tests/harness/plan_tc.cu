@@ -34,24 +34,25 @@ int main() {
       continue;
     }
     const tc::TcArgs& a = p.a;
-    uint32_t max_a = 0, max_b = 0;
+    uint32_t max_a = 0, max_b = 0, min_a = 0xffffffffu;
     for (int i = 0; i < a.ntab; ++i) {
       const uint2 e = a.tab[i];
       if ((e.y >> 16) & 2u) continue;  // skipped slot
       max_a = std::max(max_a, (e.x & 0xffffu) << 4);
+      min_a = std::min(min_a, (e.x & 0xffffu) << 4);
       max_b = std::max(max_b, (e.x >> 16) << 4);
     }
     printf("{\"ok\": true, \"m\": %d, \"sw\": %d, \"smem\": %u, \"grid\": %d, \"tmem_cols\": %u, \"np\": %d, "
            "\"nmt\": %d, \"sc\": %d, \"Nn\": %d, \"KS\": %d, \"TH\": %d, \"TWo\": %d, \"P\": %d, \"Hh\": %d, "
            "\"Dh\": %d, \"stages\": %d, \"a_off\": %u, \"b_off\": %u, \"a_stage_bytes\": %u, \"plane_stride\": %u, "
            "\"nphase\": %d, \"nchunks\": %d, \"tx_bytes\": %u, \"tiles_h\": %d, \"tiles_w\": %d, \"spatial\": %d, "
-           "\"cpg\": %d, \"n_gc\": %d, \"ntab\": %d, \"max_a\": %u, \"max_b\": %u, \"tab_off\": %u, "
+           "\"cpg\": %d, \"n_gc\": %d, \"ntab\": %d, \"max_a\": %u, \"min_a\": %u, \"shift\": %d, \"max_b\": %u, \"tab_off\": %u, "
            "\"bias_off\": %u, \"epi_off\": %u, \"epi_w\": %d, \"epi_slices\": %d, \"epi_slice_bytes\": %u, "
            "\"nbuf\": %d, \"plane_cx\": [%d, %d, %d, %d, %d, %d, %d, %d], \"tap_phase\": [%d, %d, %d, %d, %d, %d, %d, %d, %d], "
            "\"tap_off\": [%d, %d, %d, %d, %d, %d, %d, %d, %d]}\n",
            m, (int)p.sw, p.smem_bytes, p.grid, a.tmem_cols, a.np, a.nmt, a.sc, a.Nn, a.KS, a.TH, a.TWo, a.P, a.Hh,
            a.Dh, a.stages, a.a_off, a.b_off, a.a_stage_bytes, a.plane_stride, a.nphase, a.nchunks, a.tx_bytes,
-           a.tiles_h, a.tiles_w, a.spatial_tiles, a.cpg, a.n_gc, a.ntab, max_a, max_b, a.tab_off, a.bias_off,
+           a.tiles_h, a.tiles_w, a.spatial_tiles, a.cpg, a.n_gc, a.ntab, max_a, min_a, a.shift, max_b, a.tab_off, a.bias_off,
            a.epi_off, a.epi_w, a.epi_slices, a.epi_slice_bytes, a.nbuf, a.plane_cx[0], a.plane_cx[1], a.plane_cx[2],
            a.plane_cx[3], a.plane_cx[4], a.plane_cx[5], a.plane_cx[6], a.plane_cx[7], a.tap_phase[0], a.tap_phase[1],
            a.tap_phase[2], a.tap_phase[3], a.tap_phase[4], a.tap_phase[5], a.tap_phase[6], a.tap_phase[7],

@@ -206,8 +206,15 @@ def _check_tc_plan(wl, p):
     assert p["spatial"] == wl.N * out[0] * p["tiles_h"] * p["tiles_w"], ctx
     assert p["grid"] == (p["n_gc"] // p["sc"]) * p["cpg"], ctx
     assert 0 <= p["ntab"] <= 2048, ctx
+    # row shift: accumulator row f holds flattened output f + shift; the
+    # tile's outputs still fit its M tiles, and the earliest A start (rows
+    # before the plane, which feed only unstored rows) stays in shared memory
+    assert -8 < p["shift"] <= 0, ctx
+    assert p["TH"] * p["P"] - p["shift"] <= p["nmt"] * 128, ctx
     if p["ntab"]:
         assert p["a_off"] <= p["max_a"] < p["a_off"] + p["a_stage_bytes"], ctx
+        assert p["a_off"] + 8 * p["shift"] * (128 if p["sw"] else 16) <= p["min_a"], ctx
+        assert p["min_a"] >= 1024, ctx
         assert p["b_off"] <= p["max_b"] < p["a_off"], ctx
     assert p["bias_off"] < p["tab_off"] <= p["b_off"], ctx
     if p["epi_off"]:  # output box staged for TMA stores, one box per channel slice
