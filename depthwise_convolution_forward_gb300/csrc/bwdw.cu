@@ -351,7 +351,9 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t 
                : "memory");
 }
 
-template <typename T, int CG>
+// KG output channels of one group per thread (each x pair it loads feeds
+// 2 * KG FMAs), at most NT taps.
+template <typename T, int CG, int KG, int NT>
 __global__ void __launch_bounds__(kTileThreads) bwd_weight_tile_kernel(const BwTileArgs a) {
   extern __shared__ __align__(16) uint8_t sm[];
   const uint4* __restrict__ x4 = static_cast<const uint4*>(a.x);
@@ -359,24 +361,27 @@ __global__ void __launch_bounds__(kTileThreads) bwd_weight_tile_kernel(const BwT
   constexpr int kPiece = 16 / (int)sizeof(T);  // elements per 16-byte piece
   const uint32_t buf_bytes = a.x_bytes + (uint32_t)(a.Wo * a.K) * (uint32_t)sizeof(T);  // one row's staging
   const int tid = threadIdx.x;
-  const int pair = tid / a.tsplit, part = tid - pair * a.tsplit;
-  const bool active = pair < a.G * a.Kg;
+  const int unit = tid / a.tsplit, part = tid - unit * a.tsplit;  // unit = (group, block of KG channels)
+  const bool active = unit < a.G * (a.Kg / KG);
+  const int pair = unit * KG;  // first (g, k) pair of the unit: g * Kg + k0
   const int g = active ? pair / a.Kg : 0;
   const int t0 = part * a.tpt;
   const int nt = active ? max(0, min(a.tpt, a.taps - t0)) : 0;
   // per tap of this thread: its element offset in the staged rows at output column 0
-  int toff[kTileMaxTaps];
+  int toff[NT];
 #pragma unroll
-  for (int t = 0; t < kTileMaxTaps; ++t) {
+  for (int t = 0; t < NT; ++t) {
     const int tt = min(t0 + t, a.taps - 1);
     const int xx = tt % a.X, r = tt / a.X;  // r = z * Y + yy
     toff[t] = (r * a.WR + xx * a.dW) * a.C + g * CG;
   }
-  float acc[kTileMaxTaps][CG];
+  float acc[NT][KG][CG];
 #pragma unroll
-  for (int t = 0; t < kTileMaxTaps; ++t)
+  for (int t = 0; t < NT; ++t)
 #pragma unroll
-    for (int c = 0; c < CG; ++c) acc[t][c] = 0.f;
+    for (int k = 0; k < KG; ++k)
+#pragma unroll
+      for (int c = 0; c < CG; ++c) acc[t][k][c] = 0.f;
   const int colstep = a.sW * a.C;
   const int ppx = a.C / kPiece;  // pieces per input pixel
   const int row_pieces = a.WR * ppx;
@@ -428,22 +433,35 @@ __global__ void __launch_bounds__(kTileThreads) bwd_weight_tile_kernel(const BwT
     const T* dys = reinterpret_cast<const T*>(sm + (size_t)b * buf_bytes + a.x_bytes);
     if (active) {
       for (int ow = 0; ow < a.Wo; ++ow) {
-        const T dvt = dys[ow * a.K + pair];
+        const T* dyp = dys + ow * a.K + pair;  // KG consecutive output channels
         const int cb = ow * colstep;
         if constexpr (CG == 2 && sizeof(T) == 2) {
-          const uint32_t h = *reinterpret_cast<const unsigned short*>(&dvt);
-          const uint32_t dpair = h | (h << 16);
+          uint32_t dpair[KG];  // each channel's dy in both halves
 #pragma unroll
-          for (int t = 0; t < kTileMaxTaps; ++t)
-            if (t < nt)
-              fma_mixed_pair<T>(*reinterpret_cast<const uint32_t*>(xs + cb + toff[t]), dpair, acc[t][0], acc[t][1]);
+          for (int k = 0; k < KG; ++k) {
+            const uint32_t h = *reinterpret_cast<const unsigned short*>(dyp + k);
+            dpair[k] = h | (h << 16);
+          }
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            if (t < nt) {
+              const uint32_t xw = *reinterpret_cast<const uint32_t*>(xs + cb + toff[t]);
+#pragma unroll
+              for (int k = 0; k < KG; ++k) fma_mixed_pair<T>(xw, dpair[k], acc[t][k][0], acc[t][k][1]);
+            }
         } else {
-          const float d = Elem<T>::to_f32(dvt);
+          float d[KG];
 #pragma unroll
-          for (int t = 0; t < kTileMaxTaps; ++t)
+          for (int k = 0; k < KG; ++k) d[k] = Elem<T>::to_f32(dyp[k]);
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
             if (t < nt)
 #pragma unroll
-              for (int c = 0; c < CG; ++c) acc[t][c] = fmaf(d, Elem<T>::to_f32(xs[cb + toff[t] + c]), acc[t][c]);
+              for (int c = 0; c < CG; ++c) {
+                const float xv = Elem<T>::to_f32(xs[cb + toff[t] + c]);
+#pragma unroll
+                for (int k = 0; k < KG; ++k) acc[t][k][c] = fmaf(d[k], xv, acc[t][k][c]);
+              }
         }
       }
     }
@@ -451,33 +469,44 @@ __global__ void __launch_bounds__(kTileThreads) bwd_weight_tile_kernel(const BwT
   }
   float* ws = a.ws + (int64_t)blockIdx.x * a.E;
 #pragma unroll
-  for (int t = 0; t < kTileMaxTaps; ++t)
+  for (int t = 0; t < NT; ++t)
     if (t < nt)
 #pragma unroll
-      for (int c = 0; c < CG; ++c) ws[((int64_t)pair * a.taps + t0 + t) * a.Cg + c] = acc[t][c];
+      for (int k = 0; k < KG; ++k)
+#pragma unroll
+        for (int c = 0; c < CG; ++c) ws[((int64_t)(pair + k) * a.taps + t0 + t) * a.Cg + c] = acc[t][k][c];
 }
 
 // The tiled form's shape: threads per (g, k) pair, taps per thread, staged
 // bytes; false when the problem is outside its range.
 struct BwTilePlan {
-  int tsplit, tpt, WR, S;
+  int kg, tsplit, tpt, WR, S;  // output channels per thread, threads per unit, taps per thread
   uint32_t x_bytes, smem;
 };
 bool plan_bw_tile(const Geometry& g, int es, BwTilePlan* p) {
   // two input channels per group: the per-pixel form's vectors serve one
   // (depthwise: 62 against 114 us on the MobileNetV2 layer) and wider groups
   if (g.Cg != 2) return false;
-  const int pairs = g.G * g.Kg;
-  if (pairs > kTileThreads) return false;
   if ((g.C() * es) % 16 != 0 || (g.K() * es) % 16 != 0) return false;
-  const int tsplit = kTileThreads / pairs;
-  const int tpt = (g.taps() + tsplit - 1) / tsplit;
-  if (tpt > kTileMaxTaps) return false;
+  // two output channels per thread where their taps per thread fit
+  // (kTileMaxTaps / 2), else one: each x pair a thread loads then feeds four
+  // FMAs.  (3D N=8: 67 against 69 us; four channels per thread, 77 us, had
+  // eight threads of a group read eight taps' pixels on the same banks.)
+  int kg = 0, tsplit = 0, tpt = 0;
+  for (int k = 2; k >= 1 && kg == 0; k /= 2) {
+    if (g.Kg % k != 0) continue;
+    const int units = g.G * (g.Kg / k);
+    if (units > kTileThreads) continue;
+    const int ts = kTileThreads / units;
+    const int tp = (g.taps() + ts - 1) / ts;
+    if (tp <= kTileMaxTaps / k) kg = k, tsplit = ts, tpt = tp;
+  }
+  if (kg == 0) return false;
   const int64_t WR = (int64_t)(g.Wo - 1) * g.sW + (int64_t)(g.X - 1) * g.dW + 1;
   const int64_t xb = (int64_t)g.Z * g.Y * WR * g.C() * es, yb = (int64_t)g.Wo * g.K() * es;
   if (2 * (xb + yb) > 110 * 1024) return false;  // two buffers, two CTAs per SM
   const int64_t rows = g.N * (int64_t)g.Do * g.Ho;
-  p->tsplit = tsplit, p->tpt = tpt, p->WR = (int)WR;
+  p->kg = kg, p->tsplit = tsplit, p->tpt = tpt, p->WR = (int)WR;
   p->S = (int)std::min<int64_t>(rows, kTileSplits);
   p->x_bytes = (uint32_t)xb, p->smem = (uint32_t)(2 * (xb + yb));
   return true;
@@ -499,9 +528,20 @@ cudaError_t bwd_weight_tile_typed(const Geometry& g, const LaunchArgs& la, float
   a.S = p.S;
   a.E = g.w_elems();
   a.x_bytes = p.x_bytes;
-  static SmemAttr attr;  // (plan_bw_tile takes Cg = 2 only)
-  cudaError_t e = attr.ensure(bwd_weight_tile_kernel<T, 2>, dev.device, (int)p.smem);
-  if (e == cudaSuccess) e = launch_kernel(bwd_weight_tile_kernel<T, 2>, dim3(p.S), dim3(kTileThreads), p.smem, la, a);
+  // (plan_bw_tile takes Cg = 2 only)
+  cudaError_t e;
+  if (p.kg == 2) {
+    static SmemAttr attr;
+    e = attr.ensure(bwd_weight_tile_kernel<T, 2, 2, kTileMaxTaps / 2>, dev.device, (int)p.smem);
+    if (e == cudaSuccess)
+      e = launch_kernel(bwd_weight_tile_kernel<T, 2, 2, kTileMaxTaps / 2>, dim3(p.S), dim3(kTileThreads), p.smem, la,
+                        a);
+  } else {
+    static SmemAttr attr;
+    e = attr.ensure(bwd_weight_tile_kernel<T, 2, 1, kTileMaxTaps>, dev.device, (int)p.smem);
+    if (e == cudaSuccess)
+      e = launch_kernel(bwd_weight_tile_kernel<T, 2, 1, kTileMaxTaps>, dim3(p.S), dim3(kTileThreads), p.smem, la, a);
+  }
   if (e != cudaSuccess) return e;
   return reduce_typed<T>(g, la, ws, p.S, dev);
 }
